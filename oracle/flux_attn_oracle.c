@@ -1,0 +1,362 @@
+/*
+ * flux_attn_oracle.c -- plain fp64 CPU oracle for joint text/image attention
+ * with per-head Q/K RMSNorm and multi-axis RoPE.
+ *
+ * TEST INFRASTRUCTURE.  Only the tests, the smoke check of the package entry
+ * file and the CPU-baseline / reference legs of bench.py load this library.
+ * The CUDA path never calls, links or includes it, and it includes nothing
+ * from the CUDA path.
+ *
+ * What it computes (sources are web pages; none prints a formula, so the
+ * plainest reading is written out here):
+ *   - "Speed up image generation with FLUX 3 Image Klein on NVIDIA Blackwell
+ *     GPUs" (NVIDIA developer blog), section "FLUX 3 inference with TensorRT
+ *     LLM VisualGen": text, noisy-target-image and optional reference-image
+ *     token streams are processed separately and then merged by JOINT
+ *     attention -- one bidirectional softmax attention over the concatenated
+ *     sequence [txt | img | ref], no mask between streams.
+ *   - same page, section "GEMM kernel optimisation": the QKV projection
+ *     carries query/key normalisation and rotary position embedding (RoPE),
+ *     so attention consumes RMSNorm'ed, rotated Q and K; V is untouched.
+ *   - same page, section "Quantized and sparse attention": the FP8 variant
+ *     runs Q.K and P.V with FP8 Q, K and V (qk_dtype fp8, v_dtype fp8).
+ *
+ * Readings taken where the pages are silent:
+ *   R1 RMSNorm over the head dimension d: y_i = x_i / sqrt(mean_j x_j^2 + eps) * w_i,
+ *      one weight vector for Q and one for K, shared by all heads.
+ *   R2 RoPE rotates ADJACENT pairs (x_{2j}, x_{2j+1}); the head dimension is cut
+ *      into consecutive axis blocks of sizes axes[0..2]; in block a the pair j
+ *      turns by angle pos_a * theta^(-2j/axes[a]).
+ *   R3 Norm first, then RoPE.
+ *   R4 Softmax scale 1/sqrt(d).
+ *   R5 FP8: per (batch, head) and per tensor, scale = amax / 448 (1 when
+ *      amax = 0); codes are E4M3 (finite, max 448) rounded to nearest, ties
+ *      to even, saturating; attention then runs exactly on the dequantised
+ *      values code * scale.
+ *
+ * Every loop below follows the definition directly: no tiling, no online
+ * softmax, no reordering beyond summation order inside a dot product.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ---------------------------------------------------------------- inputs */
+
+/* An input tensor is either bf16 bit patterns or plain doubles. */
+typedef struct {
+  const void* p;
+  int is_bf16;
+} src_t;
+
+static double bf16_to_f64(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+static double ld(const src_t* s, int64_t i) {
+  if (s->is_bf16) return bf16_to_f64(((const uint16_t*)s->p)[i]);
+  return ((const double*)s->p)[i];
+}
+
+/* ------------------------------------------------------------ E4M3 codec */
+
+/* Decode one OCP E4M3 ("fn") code: 1 sign, 4 exponent bits (bias 7),
+ * 3 mantissa bits, no infinities, 0x7F / 0xFF are NaN. */
+double oracle_e4m3_decode(uint8_t c) {
+  int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0) v = ldexp((double)m, -9);            /* subnormal: m/8 * 2^-6 */
+  else v = ldexp(1.0 + m / 8.0, e - 7);
+  return s ? -v : v;
+}
+
+/* Encode a double to E4M3: round to nearest, ties to even, saturate finite
+ * values to +-448 (reading R5).  NaN maps to 0x7F. */
+uint8_t oracle_e4m3_encode(double x) {
+  uint8_t sign = signbit(x) ? 0x80 : 0;
+  double a = fabs(x);
+  if (isnan(x)) return 0x7F;
+  if (a >= 448.0) return (uint8_t)(sign | 0x7E);    /* 1.75 * 2^8 */
+  if (a < ldexp(1.0, -6)) {
+    /* subnormal range: a = q * 2^-9, q in [0, 8); q == 8 carries into the
+     * smallest normal, whose code (e=1, m=0) is exactly 8. */
+    double q = nearbyint(ldexp(a, 9));
+    return (uint8_t)(sign | (uint8_t)q);
+  }
+  int e2;
+  double fr = frexp(a, &e2);                        /* a = fr * 2^e2, fr in [0.5, 1) */
+  int e = e2 - 1;                                   /* a = (2 fr) * 2^e, 2fr in [1, 2) */
+  double m = nearbyint((2.0 * fr - 1.0) * 8.0);     /* exact products, RNE */
+  if (m == 8.0) { m = 0.0; e += 1; }
+  int be = e + 7;
+  if (be > 15 || (be == 15 && m == 7.0)) return (uint8_t)(sign | 0x7E);
+  return (uint8_t)(sign | (be << 3) | (int)m);
+}
+
+/* ------------------------------------------------------ per-row prologue */
+
+/* Reading R1: RMSNorm of one head row of length d. */
+static void rmsnorm_row(double* y, const double* x, int d, const double* w, double eps) {
+  double ss = 0.0;
+  for (int i = 0; i < d; ++i) ss += x[i] * x[i];
+  double inv = 1.0 / sqrt(ss / d + eps);
+  for (int i = 0; i < d; ++i) y[i] = x[i] * inv * w[i];
+}
+
+/* Reading R2: multi-axis RoPE on one head row, in place. */
+static void rope_row(double* y, int d, const int32_t* pos3, double theta, const int* axes) {
+  int off = 0;
+  for (int a = 0; a < 3; ++a) {
+    int da = axes[a];
+    for (int j = 0; j < da / 2; ++j) {
+      double ang = (double)pos3[a] * pow(theta, -2.0 * j / da);
+      double c = cos(ang), s = sin(ang);
+      double x0 = y[off + 2 * j], x1 = y[off + 2 * j + 1];
+      y[off + 2 * j] = x0 * c - x1 * s;
+      y[off + 2 * j + 1] = x0 * s + x1 * c;
+    }
+    off += da;
+  }
+  (void)d;
+}
+
+static int check_axes(int d, const int* axes) {
+  if (d <= 0) return -1;
+  if (axes[0] < 0 || axes[1] < 0 || axes[2] < 0) return -1;
+  if (axes[0] % 2 || axes[1] % 2 || axes[2] % 2) return -1;
+  if (axes[0] + axes[1] + axes[2] != d) return -1;
+  return 0;
+}
+
+/* Normalised + rotated rows for every token of head (b, h): out[N*d]. */
+static void prologue_head(double* out, const src_t* x, int b, int h, int N, int H, int d,
+                          const int32_t* pos, const double* w, double eps, double theta,
+                          const int* axes, int nt) {
+  int64_t n;
+#pragma omp parallel for num_threads(nt) schedule(static)
+  for (n = 0; n < N; ++n) {
+    double row[1024];
+    int64_t base = (((int64_t)b * N + n) * H + h) * d;
+    for (int i = 0; i < d; ++i) row[i] = ld(x, base + i);
+    rmsnorm_row(out + n * d, row, d, w, eps);
+    rope_row(out + n * d, d, pos + 3 * n, theta, axes);
+  }
+}
+
+static void plain_head(double* out, const src_t* x, int b, int h, int N, int H, int d, int nt) {
+  int64_t n;
+#pragma omp parallel for num_threads(nt) schedule(static)
+  for (n = 0; n < N; ++n) {
+    int64_t base = (((int64_t)b * N + n) * H + h) * d;
+    for (int i = 0; i < d; ++i) out[n * d + i] = ld(x, base + i);
+  }
+}
+
+/* Reading R5: per-tensor-per-head amax scale, quantise, dequantise in place.
+ * codes (optional) receives the E4M3 codes. Returns the scale. */
+static double fp8_roundtrip(double* a, int64_t count, uint8_t* codes) {
+  double amax = 0.0;
+  for (int64_t i = 0; i < count; ++i) if (fabs(a[i]) > amax) amax = fabs(a[i]);
+  double scale = amax > 0.0 ? amax / 448.0 : 1.0;
+  for (int64_t i = 0; i < count; ++i) {
+    uint8_t c = oracle_e4m3_encode(a[i] / scale);
+    if (codes) codes[i] = c;
+    a[i] = oracle_e4m3_decode(c) * scale;
+  }
+  return scale;
+}
+
+/* One output row: o = sum_m softmax_m(q.k_m / sqrt(d)) v_m (reading R4). */
+static void attention_row(double* o, const double* qh, const double* kh, const double* vh,
+                          int N, int d, double* srow) {
+  double inv_sqrt_d = 1.0 / sqrt((double)d);
+  double mx = -INFINITY;
+  for (int m = 0; m < N; ++m) {
+    double s = 0.0;
+    for (int i = 0; i < d; ++i) s += qh[i] * kh[(int64_t)m * d + i];
+    s *= inv_sqrt_d;
+    srow[m] = s;
+    if (s > mx) mx = s;
+  }
+  double l = 0.0;
+  for (int m = 0; m < N; ++m) {
+    srow[m] = exp(srow[m] - mx);
+    l += srow[m];
+  }
+  for (int i = 0; i < d; ++i) o[i] = 0.0;
+  for (int m = 0; m < N; ++m) {
+    double p = srow[m] / l;
+    for (int i = 0; i < d; ++i) o[i] += p * vh[(int64_t)m * d + i];
+  }
+}
+
+/* ------------------------------------------------------------ public API */
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+static int nthreads_or_max(int nt) { return nt > 0 ? nt : oracle_max_threads(); }
+
+/* Q or K prologue for every row: x [B,N,H,d] (bf16 bits or doubles) ->
+ * out [B,N,H,d] doubles. */
+static int prologue_all(const src_t* x, int B, int N, int H, int d, const int32_t* pos,
+                        const double* w, double eps, double theta, const int* axes,
+                        double* out, int nt) {
+  if (check_axes(d, axes) || d > 1024 || B < 0 || N < 0 || H < 0) return -1;
+  nt = nthreads_or_max(nt);
+  int64_t r, rows = (int64_t)B * N * H;
+#pragma omp parallel for num_threads(nt) schedule(static)
+  for (r = 0; r < rows; ++r) {
+    double row[1024];
+    int64_t n = (r / H) % N;
+    for (int i = 0; i < d; ++i) row[i] = ld(x, r * d + i);
+    rmsnorm_row(out + r * d, row, d, w, eps);
+    rope_row(out + r * d, d, pos + 3 * n, theta, axes);
+  }
+  return 0;
+}
+
+int oracle_prologue_bf16(const uint16_t* x, int B, int N, int H, int d, const int32_t* pos,
+                         const float* wf, double eps, double theta, const int* axes,
+                         double* out, int nt) {
+  double w[1024];
+  if (d > 1024 || d <= 0) return -1;
+  for (int i = 0; i < d; ++i) w[i] = (double)wf[i];
+  src_t s = {x, 1};
+  return prologue_all(&s, B, N, H, d, pos, w, eps, theta, axes, out, nt);
+}
+
+int oracle_prologue_f64(const double* x, int B, int N, int H, int d, const int32_t* pos,
+                        const double* w, double eps, double theta, const int* axes,
+                        double* out, int nt) {
+  src_t s = {x, 0};
+  return prologue_all(&s, B, N, H, d, pos, w, eps, theta, axes, out, nt);
+}
+
+/* Attention output for the requested query rows.
+ *   rows: nrows triples (b, h, n); out: nrows x d doubles.
+ * All rows of one (b, h) share the normalised K (and V) of that head, built
+ * once per distinct head in order of first appearance. */
+static int attention_rows(const src_t* q, const src_t* k, const src_t* v, int B, int N, int H,
+                          int d, const int32_t* pos, const double* wq, const double* wk,
+                          double eps, double theta, const int* axes, int fp8,
+                          const int64_t* rows, int64_t nrows, double* out, int nt) {
+  if (check_axes(d, axes) || d > 1024 || B <= 0 || N <= 0 || H <= 0) return -1;
+  for (int64_t r = 0; r < nrows; ++r) {
+    int64_t b = rows[3 * r], h = rows[3 * r + 1], n = rows[3 * r + 2];
+    if (b < 0 || b >= B || h < 0 || h >= H || n < 0 || n >= N) return -2;
+  }
+  nt = nthreads_or_max(nt);
+  int64_t nd = (int64_t)N * d;
+  double* kh = (double*)malloc(sizeof(double) * nd);
+  double* vh = (double*)malloc(sizeof(double) * nd);
+  double* qh = (double*)malloc(sizeof(double) * nd);
+  unsigned char* done = (unsigned char*)calloc((size_t)B * H, 1);
+  int64_t* idx = (int64_t*)malloc(sizeof(int64_t) * (nrows > 0 ? nrows : 1));
+  if (!kh || !vh || !qh || !done || !idx) {
+    free(kh); free(vh); free(qh); free(done); free(idx);
+    return -3;
+  }
+  for (int64_t r0 = 0; r0 < nrows; ++r0) {
+    int b = (int)rows[3 * r0], h = (int)rows[3 * r0 + 1];
+    if (done[(size_t)b * H + h]) continue;
+    done[(size_t)b * H + h] = 1;
+    /* the rows of this head */
+    int64_t cnt = 0;
+    for (int64_t r = r0; r < nrows; ++r)
+      if (rows[3 * r] == b && rows[3 * r + 1] == h) idx[cnt++] = r;
+    prologue_head(kh, k, b, h, N, H, d, pos, wk, eps, theta, axes, nt);
+    plain_head(vh, v, b, h, N, H, d, nt);
+    if (fp8) {
+      prologue_head(qh, q, b, h, N, H, d, pos, wq, eps, theta, axes, nt);
+      fp8_roundtrip(qh, nd, NULL);
+      fp8_roundtrip(kh, nd, NULL);
+      fp8_roundtrip(vh, nd, NULL);
+    }
+    int64_t t;
+#pragma omp parallel for num_threads(nt) schedule(dynamic, 4)
+    for (t = 0; t < cnt; ++t) {
+      int64_t r = idx[t];
+      int64_t n = rows[3 * r + 2];
+      double qrow[1024], tmp[1024];
+      double* srow = (double*)malloc(sizeof(double) * N);
+      const double* qp;
+      if (fp8) {
+        qp = qh + n * d;
+      } else {
+        int64_t base = (((int64_t)b * N + n) * H + h) * d;
+        for (int i = 0; i < d; ++i) tmp[i] = ld(q, base + i);
+        rmsnorm_row(qrow, tmp, d, wq, eps);
+        rope_row(qrow, d, pos + 3 * n, theta, axes);
+        qp = qrow;
+      }
+      if (srow) attention_row(out + r * d, qp, kh, vh, N, d, srow);
+      else for (int i = 0; i < d; ++i) out[r * d + i] = NAN;
+      free(srow);
+    }
+  }
+  free(kh); free(vh); free(qh); free(done); free(idx);
+  return 0;
+}
+
+int oracle_attention_rows_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                               int B, int N, int H, int d, const int32_t* pos,
+                               const float* wqf, const float* wkf, double eps, double theta,
+                               const int* axes, int fp8, const int64_t* rows, int64_t nrows,
+                               double* out, int nt) {
+  double wq[1024], wk[1024];
+  if (d > 1024 || d <= 0) return -1;
+  for (int i = 0; i < d; ++i) { wq[i] = wqf[i]; wk[i] = wkf[i]; }
+  src_t sq = {q, 1}, sk = {k, 1}, sv = {v, 1};
+  return attention_rows(&sq, &sk, &sv, B, N, H, d, pos, wq, wk, eps, theta, axes, fp8,
+                        rows, nrows, out, nt);
+}
+
+int oracle_attention_rows_f64(const double* q, const double* k, const double* v,
+                              int B, int N, int H, int d, const int32_t* pos,
+                              const double* wq, const double* wk, double eps, double theta,
+                              const int* axes, int fp8, const int64_t* rows, int64_t nrows,
+                              double* out, int nt) {
+  src_t sq = {q, 0}, sk = {k, 0}, sv = {v, 0};
+  return attention_rows(&sq, &sk, &sv, B, N, H, d, pos, wq, wk, eps, theta, axes, fp8,
+                        rows, nrows, out, nt);
+}
+
+/* FP8 intermediates of one head (reading R5): E4M3 codes of the normalised,
+ * rotated Q and K and of V, each [N*d] in token-major order, and the three
+ * scales (q, k, v). */
+int oracle_fp8_quantize_head_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                  int B, int N, int H, int d, const int32_t* pos,
+                                  const float* wqf, const float* wkf, double eps, double theta,
+                                  const int* axes, int b, int h, uint8_t* q8, uint8_t* k8,
+                                  uint8_t* v8, double* scales, int nt) {
+  double wq[1024], wk[1024];
+  if (check_axes(d, axes) || d > 1024 || b < 0 || b >= B || h < 0 || h >= H || N <= 0) return -1;
+  for (int i = 0; i < d; ++i) { wq[i] = wqf[i]; wk[i] = wkf[i]; }
+  nt = nthreads_or_max(nt);
+  int64_t nd = (int64_t)N * d;
+  double* t = (double*)malloc(sizeof(double) * nd);
+  if (!t) return -3;
+  src_t sq = {q, 1}, sk = {k, 1}, sv = {v, 1};
+  prologue_head(t, &sq, b, h, N, H, d, pos, wq, eps, theta, axes, nt);
+  scales[0] = fp8_roundtrip(t, nd, q8);
+  prologue_head(t, &sk, b, h, N, H, d, pos, wk, eps, theta, axes, nt);
+  scales[1] = fp8_roundtrip(t, nd, k8);
+  plain_head(t, &sv, b, h, N, H, d, nt);
+  scales[2] = fp8_roundtrip(t, nd, v8);
+  free(t);
+  return 0;
+}

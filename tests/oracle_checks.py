@@ -1,0 +1,413 @@
+"""Pins of the fp64 oracle against things other than itself.
+
+Each ``check_*`` function raises AssertionError on failure.  They are run by
+``test_oracle_pins.py`` against the in-tree oracle, and by
+``test_oracle_mutants.py`` against deliberately broken copies of the oracle
+source, each of which must fail at least one check.
+
+What the checks compare the oracle with:
+  * library routines in fp64: torch.nn.functional.rms_norm,
+    torch.nn.functional.scaled_dot_product_attention, torch's float8_e4m3fn
+    cast, numpy complex exponentials (RoPE written as a complex rotation);
+  * closed forms and special cases: constant inputs to RMSNorm, RoPE at
+    position zero, a hand-worked single-pair rotation per axis, constant V,
+    zero Q (uniform attention), a single token, a ones column in V (softmax
+    rows sum to one), a hand-worked two-token head;
+  * invariants: per-pair norms under RoPE, the output under a common shift
+    of every position on one axis, permutation equivariance over tokens;
+  * the E4M3 code table: every one of the 254 finite codes round-trips,
+    midpoints round to the even code, out-of-range values saturate.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+import torch.nn.functional as F
+
+import oracle
+from synthetic import bf16_bits_from_f32, bf16_bits_to_f32, position_ids
+
+AX = (16, 56, 56)
+THETA = 10000.0
+EPS = 1e-6
+D = 128
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+# ------------------------------------------------------- library references
+
+def lib_rms(x: np.ndarray, w: np.ndarray, eps: float = EPS) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(x, np.float64))
+    return F.rms_norm(t, (x.shape[-1],), weight=torch.from_numpy(np.asarray(w, np.float64)),
+                      eps=eps).numpy()
+
+
+def lib_rope(y: np.ndarray, pos: np.ndarray, theta: float = THETA, axes=AX) -> np.ndarray:
+    """RoPE as complex rotation: pair (y_2j, y_2j+1) of axis block a is the complex
+    number y_2j + i y_2j+1 multiplied by exp(i pos_a theta^(-2j/d_a))."""
+    B, N, H, d = y.shape
+    ang = []
+    for a, da in enumerate(axes):
+        j = np.arange(da // 2, dtype=np.float64)
+        freq = np.exp(-np.log(theta) * 2.0 * j / da)
+        ang.append(pos[:, a:a + 1].astype(np.float64) * freq[None, :])
+    ang = np.concatenate(ang, 1)                              # [N, d/2]
+    z = y[..., 0::2] + 1j * y[..., 1::2]
+    z = z * np.exp(1j * ang)[None, :, None, :]
+    out = np.empty_like(y)
+    out[..., 0::2] = z.real
+    out[..., 1::2] = z.imag
+    return out
+
+
+def lib_attention(qn: np.ndarray, kn: np.ndarray, v: np.ndarray) -> np.ndarray:
+    """torch SDPA (fp64, CPU) on [B, N, H, d] arrays, returns [B, N, H, d]."""
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float64)).permute(0, 2, 1, 3)
+    o = F.scaled_dot_product_attention(t(qn), t(kn), t(v))
+    return o.permute(0, 2, 1, 3).contiguous().numpy()
+
+
+def _close(a, b, tol, what):
+    err = float(np.max(np.abs(np.asarray(a) - np.asarray(b)))) if np.size(a) else 0.0
+    assert err <= tol, "%s: max abs err %.3e > %.1e" % (what, err, tol)
+
+
+# ------------------------------------------------------------------ E4M3
+
+def check_e4m3_exhaustive_roundtrip():
+    codes = np.arange(256, dtype=np.uint8)
+    finite = codes[(codes & 0x7F) != 0x7F]
+    assert finite.size == 254
+    dec = oracle.e4m3_decode(finite)
+    assert np.all(np.isfinite(dec))
+    enc = oracle.e4m3_encode(dec)
+    assert np.array_equal(enc, finite), "E4M3 code does not round-trip"
+    assert np.isnan(oracle.e4m3_decode(np.array([0x7F, 0xFF], np.uint8))).all()
+    # the decoded table is the torch float8_e4m3fn table
+    tv = torch.from_numpy(finite.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(dec, tv), "E4M3 decode differs from torch's table"
+
+
+def check_e4m3_matches_torch_cast():
+    rng = _rng(3)
+    mag = np.exp2(rng.uniform(-12.0, math.log2(463.0), 20000))
+    x = mag * rng.choice([-1.0, 1.0], mag.size)
+    ours = oracle.e4m3_decode(oracle.e4m3_encode(x))
+    theirs = torch.from_numpy(x).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(ours, theirs), "E4M3 rounding differs from torch's cast"
+
+
+def check_e4m3_ties_and_saturation():
+    cases = {
+        1.0625: 1.0,            # midpoint of 1.0 (m=0) and 1.125 (m=1) -> even m=0
+        1.1875: 1.25,           # midpoint of m=1 and m=2 -> m=2
+        2.0 ** -10: 0.0,        # half the smallest subnormal -> 0
+        3 * 2.0 ** -10: 2 * 2.0 ** -9,   # midpoint of 1 and 2 subnormal units -> 2
+        15 * 2.0 ** -10: 2.0 ** -6,      # midpoint of 7 units and the smallest normal -> normal
+        440.0: 448.0,           # midpoint of 416 and 448 -> m=6 (even)
+        447.9: 448.0,
+        463.99: 448.0,          # saturate
+        1e6: 448.0,
+        -1e6: -448.0,
+        0.0: 0.0,
+    }
+    for x, want in cases.items():
+        got = float(oracle.e4m3_decode(oracle.e4m3_encode(np.array([x])))[0])
+        assert got == want, "E4M3(%r) = %r, want %r" % (x, got, want)
+
+
+# --------------------------------------------------------------- RMSNorm
+
+def check_rmsnorm_matches_torch():
+    rng = _rng(4)
+    x = rng.standard_normal((2, 9, 3, D)) * rng.uniform(0.01, 30.0, (2, 9, 3, 1))
+    w = 1.0 + 0.1 * rng.standard_normal(D)
+    pos = np.zeros((9, 3), np.int32)          # RoPE is the identity at position 0
+    got = oracle.prologue(x, pos, w)
+    _close(got, lib_rms(x, w), 1e-12, "RMSNorm vs torch rms_norm")
+
+
+def check_rmsnorm_closed_form():
+    for c in (1.0, -3.0, 1e-4, 0.0):
+        x = np.full((1, 1, 1, D), c)
+        w = np.linspace(0.5, 1.5, D)
+        got = oracle.prologue(x, np.zeros((1, 3), np.int32), w)[0, 0, 0]
+        want = c / math.sqrt(c * c + EPS) * w
+        _close(got, want, 1e-13, "RMSNorm of a constant row (c=%g)" % c)
+
+
+# ------------------------------------------------------------------ RoPE
+
+def check_rope_complex_form():
+    rng = _rng(5)
+    N = 11
+    x = rng.standard_normal((1, N, 2, D))
+    w = 1.0 + 0.1 * rng.standard_normal(D)
+    pos = rng.integers(-50, 200, (N, 3)).astype(np.int32)
+    got = oracle.prologue(x, pos, w)
+    want = lib_rope(lib_rms(x, w), pos)
+    _close(got, want, 1e-11, "RoPE vs complex rotation")
+
+
+def check_rope_hand_cases():
+    """Single nonzero element e_i, w = 1: after RMSNorm it is u = 1/sqrt(1/d + eps);
+    the pair containing it turns by the hand-computed angle."""
+    u = 1.0 / math.sqrt(1.0 / D + EPS)
+    cases = [
+        # (dim, pos, angle)
+        (0, (1, 0, 0), 1.0),                                   # axis 0, pair 0, freq 1
+        (2, (5, 0, 0), 5.0 * THETA ** (-2.0 / 16)),            # axis 0, pair 1
+        (16, (0, 1, 0), 1.0),                                  # axis 1 starts at dim 16
+        (18, (0, 1, 0), THETA ** (-2.0 / 56)),                 # axis 1, pair 1
+        (72, (0, 0, 7), 7.0),                                  # axis 2 starts at dim 72
+        (126, (0, 0, 3), 3.0 * THETA ** (-54.0 / 56)),         # last pair of axis 2
+        (16, (9, 0, 4), 0.0),                                  # axis 1 untouched by axes 0 and 2
+    ]
+    for dim, p, ang in cases:
+        x = np.zeros((1, 1, 1, D))
+        x[..., dim] = 1.0
+        got = oracle.prologue(x, np.array([p], np.int32), np.ones(D))[0, 0, 0]
+        want = np.zeros(D)
+        want[dim] = u * math.cos(ang)
+        want[dim + 1] = u * math.sin(ang)
+        _close(got, want, 1e-12, "RoPE hand case dim=%d pos=%s" % (dim, p))
+
+
+def check_rope_pair_norms():
+    rng = _rng(6)
+    x = rng.standard_normal((1, 7, 2, D))
+    w = 1.0 + 0.1 * rng.standard_normal(D)
+    pos = rng.integers(0, 300, (7, 3)).astype(np.int32)
+    a = oracle.prologue(x, pos, w)
+    b = oracle.prologue(x, np.zeros_like(pos), w)
+    na = a[..., 0::2] ** 2 + a[..., 1::2] ** 2
+    nb = b[..., 0::2] ** 2 + b[..., 1::2] ** 2
+    _close(na, nb, 1e-11, "RoPE pair norms")
+    assert np.max(np.abs(a - b)) > 1e-3, "RoPE did nothing at nonzero positions"
+
+
+# ------------------------------------------------------------- attention
+
+def _geometry(txt=5, ih=4, iw=8, rh=0, rw=0):
+    return position_ids(txt, ih, iw, rh, rw)
+
+
+def check_attention_matches_torch_sdpa():
+    rng = _rng(7)
+    pos = _geometry(5, 4, 8, 2, 3)
+    N = pos.shape[0]
+    q = rng.standard_normal((2, N, 3, D))
+    k = rng.standard_normal((2, N, 3, D))
+    v = rng.standard_normal((2, N, 3, D))
+    wq = 1.0 + 0.1 * rng.standard_normal(D)
+    wk = 1.0 + 0.1 * rng.standard_normal(D)
+    got = oracle.attention_rows(q, k, v, pos, wq, wk)
+    want = lib_attention(lib_rope(lib_rms(q, wq), pos), lib_rope(lib_rms(k, wk), pos), v)
+    _close(got, want, 1e-12, "attention vs torch SDPA")
+
+
+def check_bf16_entry_matches_f64_entry():
+    rng = _rng(8)
+    pos = _geometry(3, 3, 5)
+    N = pos.shape[0]
+    bits = [bf16_bits_from_f32(rng.standard_normal((1, N, 2, D)).astype(np.float32)) for _ in range(3)]
+    as64 = [torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy() for b in bits]
+    assert np.array_equal(as64[0], bf16_bits_to_f32(bits[0]).astype(np.float64))
+    wq = (1.0 + 0.1 * rng.standard_normal(D)).astype(np.float32)
+    wk = (1.0 + 0.1 * rng.standard_normal(D)).astype(np.float32)
+    a = oracle.attention_rows(*bits, pos, wq, wk)
+    b = oracle.attention_rows(*as64, pos, wq.astype(np.float64), wk.astype(np.float64))
+    assert np.array_equal(a, b), "bf16 and fp64 entry points disagree"
+
+
+def _rand_head(seed, N=23, H=2, B=1):
+    rng = _rng(seed)
+    pos = rng.integers(0, 40, (N, 3)).astype(np.int32)
+    q, k, v = (rng.standard_normal((B, N, H, D)) for _ in range(3))
+    wq = 1.0 + 0.1 * rng.standard_normal(D)
+    wk = 1.0 + 0.1 * rng.standard_normal(D)
+    return q, k, v, pos, wq, wk
+
+
+def check_softmax_rows_sum_to_one():
+    q, k, v, pos, wq, wk = _rand_head(9)
+    v[..., 5] = 1.0
+    o = oracle.attention_rows(q, k, v, pos, wq, wk)
+    _close(o[..., 5], 1.0, 1e-13, "softmax row sum")
+
+
+def check_constant_v():
+    q, k, v, pos, wq, wk = _rand_head(10)
+    v[:] = np.linspace(-2, 2, D)
+    o = oracle.attention_rows(q, k, v, pos, wq, wk)
+    _close(o, v, 1e-13, "constant V")
+
+
+def check_zero_q_is_mean_v():
+    q, k, v, pos, wq, wk = _rand_head(11)
+    q[:] = 0.0
+    o = oracle.attention_rows(q, k, v, pos, wq, wk)
+    want = np.broadcast_to(v.mean(axis=1, keepdims=True), v.shape)
+    _close(o, want, 1e-13, "zero Q gives mean of V")
+
+
+def check_single_token():
+    q, k, v, pos, wq, wk = _rand_head(12, N=1, H=3)
+    o = oracle.attention_rows(q, k, v, pos, wq, wk)
+    _close(o, v, 1e-14, "single token returns v")
+
+
+def check_permutation_equivariance():
+    q, k, v, pos, wq, wk = _rand_head(13, N=29)
+    perm = _rng(14).permutation(29)
+    o = oracle.attention_rows(q, k, v, pos, wq, wk)
+    op = oracle.attention_rows(q[:, perm], k[:, perm], v[:, perm], pos[perm], wq, wk)
+    _close(op, o[:, perm], 1e-12, "permutation equivariance")
+
+
+def check_common_shift_invariance():
+    q, k, v, pos, wq, wk = _rand_head(15, N=31)
+    o = oracle.attention_rows(q, k, v, pos, wq, wk)
+    for axis, delta in ((0, 3), (1, -17), (2, 101)):
+        p2 = pos.copy()
+        p2[:, axis] += delta
+        o2 = oracle.attention_rows(q, k, v, p2, wq, wk)
+        _close(o2, o, 1e-11, "shift of axis %d" % axis)
+    p3 = pos.copy()
+    p3[0, 1] += 5                                   # moving one token does change the output
+    assert np.max(np.abs(oracle.attention_rows(q, k, v, p3, wq, wk) - o)) > 1e-6
+
+
+def check_hand_two_token_head():
+    """Two tokens, one head, w = 1, positions zero.
+    q_0 = 2 e_0, q_1 = e_1; k_0 = e_0, k_1 = 3 e_1 + 3 e_0 (norm spread over two dims);
+    v_0 = e_2, v_1 = e_3."""
+    u1 = 1.0 / math.sqrt(1.0 / D + EPS)                 # RMSNorm of a one-hot row (any scale c:
+    uc = lambda c: c / math.sqrt(c * c / D + EPS)       #   c / sqrt(c^2/d + eps))
+    u2 = 3.0 / math.sqrt(18.0 / D + EPS)                # RMSNorm of 3 e_0 + 3 e_1
+    q = np.zeros((1, 2, 1, D)); k = np.zeros((1, 2, 1, D)); v = np.zeros((1, 2, 1, D))
+    q[0, 0, 0, 0] = 2.0
+    q[0, 1, 0, 1] = 1.0
+    k[0, 0, 0, 0] = 1.0
+    k[0, 1, 0, 0] = 3.0; k[0, 1, 0, 1] = 3.0
+    v[0, 0, 0, 2] = 1.0
+    v[0, 1, 0, 3] = 1.0
+    # scores / sqrt(d)
+    s00 = uc(2.0) * u1 / math.sqrt(D)
+    s01 = uc(2.0) * u2 / math.sqrt(D)
+    s10 = 0.0
+    s11 = u1 * u2 / math.sqrt(D)
+    p0 = [math.exp(s00) / (math.exp(s00) + math.exp(s01)), math.exp(s01) / (math.exp(s00) + math.exp(s01))]
+    p1 = [math.exp(s10) / (math.exp(s10) + math.exp(s11)), math.exp(s11) / (math.exp(s10) + math.exp(s11))]
+    o = oracle.attention_rows(q, k, v, np.zeros((2, 3), np.int32), np.ones(D), np.ones(D))
+    want = np.zeros((1, 2, 1, D))
+    want[0, 0, 0, 2], want[0, 0, 0, 3] = p0
+    want[0, 1, 0, 2], want[0, 1, 0, 3] = p1
+    _close(o, want, 1e-14, "hand two-token head")
+
+
+def check_row_subset_matches_full():
+    q, k, v, pos, wq, wk = _rand_head(16, N=19, H=3, B=2)
+    full = oracle.attention_rows(q, k, v, pos, wq, wk)
+    rows = np.array([[1, 2, 18], [0, 0, 0], [1, 0, 7], [0, 2, 3]], np.int64)
+    sub = oracle.attention_rows(q, k, v, pos, wq, wk, rows=rows)
+    want = np.stack([full[b, n, h] for b, h, n in rows])
+    assert np.array_equal(sub, want)
+
+
+# ------------------------------------------------------------------- FP8
+
+def _fp8_inputs(seed, N=40, H=2, B=2):
+    rng = _rng(seed)
+    pos = _geometry(8, 4, 8)
+    assert pos.shape[0] == N
+    def draw():
+        x = rng.standard_normal((B, N, H, D)).astype(np.float32)
+        m = rng.random((B, N, H, D)) < 0.01
+        x[m] *= 8.0
+        return bf16_bits_from_f32(x)
+    q, k, v = draw(), draw(), draw()
+    wq = (1.0 + 0.1 * rng.standard_normal(D)).astype(np.float32)
+    wk = (1.0 + 0.1 * rng.standard_normal(D)).astype(np.float32)
+    return q, k, v, pos, wq, wk
+
+
+def _torch_e4m3(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).to(torch.float8_e4m3fn)
+
+
+def check_fp8_codes_and_scales():
+    q, k, v, pos, wq, wk = _fp8_inputs(17)
+    qn = oracle.prologue(q, pos, wq)
+    kn = oracle.prologue(k, pos, wk)
+    vf = bf16_bits_to_f32(v).astype(np.float64)
+    for b in range(2):
+        for h in range(2):
+            q8, k8, v8, sc = oracle.fp8_quantize_head(q, k, v, pos, wq, wk, b, h)
+            for name, x, codes, s in (("q", qn, q8, sc[0]), ("k", kn, k8, sc[1]), ("v", vf, v8, sc[2])):
+                xs = x[b, :, h, :]
+                want_s = np.max(np.abs(xs)) / 448.0
+                assert abs(s - want_s) <= 1e-15 * want_s, "%s scale" % name
+                want = _torch_e4m3(xs / want_s).view(torch.uint8).numpy()
+                assert np.array_equal(codes, want), "%s codes differ from torch's cast" % name
+
+
+def check_fp8_attention_on_dequantised_inputs():
+    q, k, v, pos, wq, wk = _fp8_inputs(18)
+    got = oracle.attention_rows(q, k, v, pos, wq, wk, fp8=True)
+    qn = oracle.prologue(q, pos, wq)
+    kn = oracle.prologue(k, pos, wk)
+    vf = bf16_bits_to_f32(v).astype(np.float64)
+    deq = []
+    for x in (qn, kn, vf):
+        y = np.empty_like(x)
+        for b in range(x.shape[0]):
+            for h in range(x.shape[2]):
+                xs = x[b, :, h, :]
+                s = np.max(np.abs(xs)) / 448.0
+                y[b, :, h, :] = _torch_e4m3(xs / s).to(torch.float64).numpy() * s
+        deq.append(y)
+    want = lib_attention(*deq)
+    _close(got, want, 1e-12, "FP8 attention vs SDPA on dequantised inputs")
+    # and it is not the unquantised result
+    plain = oracle.attention_rows(q, k, v, pos, wq, wk)
+    assert np.max(np.abs(plain - got)) > 1e-4
+
+
+def check_fp8_zero_head():
+    q, k, v, pos, wq, wk = _fp8_inputs(19)
+    q[:, :, 1] = 0; k[:, :, 1] = 0; v[:, :, 1] = 0
+    o = oracle.attention_rows(q, k, v, pos, wq, wk, fp8=True)
+    assert np.all(o[:, :, 1] == 0.0)
+    _, _, _, sc = oracle.fp8_quantize_head(q, k, v, pos, wq, wk, 0, 1)
+    assert np.all(sc == 1.0)
+
+
+ALL_CHECKS = [
+    check_e4m3_exhaustive_roundtrip,
+    check_e4m3_matches_torch_cast,
+    check_e4m3_ties_and_saturation,
+    check_rmsnorm_matches_torch,
+    check_rmsnorm_closed_form,
+    check_rope_complex_form,
+    check_rope_hand_cases,
+    check_rope_pair_norms,
+    check_attention_matches_torch_sdpa,
+    check_bf16_entry_matches_f64_entry,
+    check_softmax_rows_sum_to_one,
+    check_constant_v,
+    check_zero_q_is_mean_v,
+    check_single_token,
+    check_permutation_equivariance,
+    check_common_shift_invariance,
+    check_hand_two_token_head,
+    check_row_subset_matches_full,
+    check_fp8_codes_and_scales,
+    check_fp8_attention_on_dequantised_inputs,
+    check_fp8_zero_head,
+]

@@ -1,0 +1,60 @@
+"""Planted mistakes in a copy of the oracle source must each fail a pin (CPU).
+
+Every mutant below is a plausible slip (a dropped term, a wrong sign, index
+or operand).  The source copy is compiled into a temporary directory, the
+oracle module is pointed at it, and at least one check of oracle_checks must
+raise.  The in-tree oracle is never modified.
+"""
+import os
+
+import pytest
+
+import oracle
+import oracle_checks
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "flux_attn_oracle.c")
+
+MUTANTS = {
+    "rms_drop_eps": ("sqrt(ss / d + eps)", "sqrt(ss / d)"),
+    "rms_sum_not_mean": ("sqrt(ss / d + eps)", "sqrt(ss + eps)"),
+    "rms_drop_weight": ("y[i] = x[i] * inv * w[i]", "y[i] = x[i] * inv"),
+    "rope_sign": ("y[off + 2 * j] = x0 * c - x1 * s", "y[off + 2 * j] = x0 * c + x1 * s"),
+    "rope_freq_exponent": ("pow(theta, -2.0 * j / da)", "pow(theta, -1.0 * j / da)"),
+    "rope_axis_offset": ("    off += da;", "    off += 0;"),
+    "rope_axis_order": ("(double)pos3[a]", "(double)pos3[2 - a]"),
+    "softmax_no_scale": ("double inv_sqrt_d = 1.0 / sqrt((double)d);", "double inv_sqrt_d = 1.0;"),
+    "softmax_no_normalise": ("double p = srow[m] / l;", "double p = srow[m];"),
+    "pv_wrong_operand": ("o[i] += p * vh[(int64_t)m * d + i]", "o[i] += p * kh[(int64_t)m * d + i]"),
+    "qk_transposed_index": ("s += qh[i] * kh[(int64_t)m * d + i]", "s += qh[i] * kh[(int64_t)i * d + m % d]"),
+    "e4m3_truncate": ("double m = nearbyint((2.0 * fr - 1.0) * 8.0);", "double m = floor((2.0 * fr - 1.0) * 8.0);"),
+    "e4m3_saturate_nan": ("if (a >= 448.0) return (uint8_t)(sign | 0x7E);", "if (a >= 448.0) return (uint8_t)(sign | 0x7F);"),
+    "e4m3_subnormal_shift": ("double q = nearbyint(ldexp(a, 9));", "double q = nearbyint(ldexp(a, 8));"),
+    "fp8_scale_240": ("amax > 0.0 ? amax / 448.0 : 1.0", "amax > 0.0 ? amax / 240.0 : 1.0"),
+    "fp8_signed_amax": ("if (fabs(a[i]) > amax) amax = fabs(a[i]);", "if (a[i] > amax) amax = a[i];"),
+}
+
+
+@pytest.fixture(scope="module")
+def source():
+    with open(SRC) as f:
+        return f.read()
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, source, tmp_path):
+    old, new = MUTANTS[name]
+    assert source.count(old) == 1, "mutation anchor not unique: %r" % old
+    path = tmp_path / ("mut_%s.c" % name)
+    path.write_text(source.replace(old, new))
+    lib = oracle.compile_source(str(path), str(tmp_path / ("mut_%s.so" % name)))
+    oracle.use_library(lib)
+    failed = []
+    try:
+        for check in oracle_checks.ALL_CHECKS:
+            try:
+                check()
+            except (AssertionError, ValueError):
+                failed.append(check.__name__)
+    finally:
+        oracle.use_library(None)
+    assert failed, "mutant %s passed every pin" % name
