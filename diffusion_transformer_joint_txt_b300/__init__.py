@@ -1,0 +1,292 @@
+"""B300-native joint text/image attention for FLUX-style diffusion transformers.
+
+Python binding of the C ABI declared in ``include/flux_attn.h``.  It does
+argument marshalling only -- torch tensors become device pointers, the current
+torch CUDA stream becomes the ``cudaStream_t`` -- and every step of the path
+runs in the kernels of ``libflux_attn.so``.  There is no fallback: the first
+call into the package without the built library raises ImportError (the
+library is loaded on first use so that the build module itself can be
+imported before it exists).
+
+Entry points keep the C names (``flux_attn_create``, ``flux_attn_forward``,
+``flux_attn_prologue``, ``flux_attn_attend``, ``flux_attn_sync_status``,
+``flux_attn_destroy`` ...); ``FluxAttention`` wraps a handle for convenience.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence, Tuple
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libflux_attn.so")
+
+FLUX_ATTN_OK = 0
+FLUX_ATTN_ERR_INVALID_ARG = 1
+FLUX_ATTN_ERR_UNSUPPORTED = 2
+FLUX_ATTN_ERR_OOM = 3
+FLUX_ATTN_ERR_CUDA = 4
+FLUX_ATTN_ERR_DEVICE_TIMEOUT = 5
+FLUX_ATTN_BF16 = 0
+FLUX_ATTN_FP8_E4M3 = 1
+FLUX_ATTN_DEBUG_FORCE_TIMEOUT = 1
+
+HEAD_DIM = 128
+
+
+class flux_attn_config(ctypes.Structure):
+    _fields_ = [
+        ("batch", ctypes.c_int),
+        ("num_heads", ctypes.c_int),
+        ("head_dim", ctypes.c_int),
+        ("max_tokens", ctypes.c_int),
+        ("axes_dim", ctypes.c_int * 3),
+        ("rope_theta", ctypes.c_float),
+        ("rms_eps", ctypes.c_float),
+        ("precision", ctypes.c_int),
+        ("debug_flags", ctypes.c_int),
+    ]
+
+
+class FluxAttnError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__("flux_attn status %d (%s): %s" % (status, _status_string(status), message))
+        self.status = status
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError("libflux_attn.so is not built; run `python -m diffusion_transformer_joint_txt_b300.build` "
+                          "(expected at %s)" % LIB_PATH)
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    sig = {
+        "flux_attn_create": (I, [ctypes.POINTER(flux_attn_config), ctypes.POINTER(P)]),
+        "flux_attn_destroy": (I, [P]),
+        "flux_attn_forward": (I, [P, P, P, P, I, I, I, I, I, P, P, P, P, P]),
+        "flux_attn_prologue": (I, [P, P, P, I, I, I, I, I, P, P, P, P, P, P]),
+        "flux_attn_attend": (I, [P, P, P, P, I, P, P]),
+        "flux_attn_prologue_fp8": (I, [P, P, P, P, I, I, I, I, I, P, P, P, P, P, P, P, P]),
+        "flux_attn_attend_fp8": (I, [P, P, P, P, P, I, P, P]),
+        "flux_attn_sync_status": (I, [P, P]),
+        "flux_attn_workspace_bytes": (Z, [P]),
+        "flux_attn_launches_per_forward": (I, [P, I]),
+        "flux_attn_status_string": (ctypes.c_char_p, [I]),
+        "flux_attn_last_error": (ctypes.c_char_p, []),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    return lib
+
+
+_lib_handle = [None]
+
+
+def _L() -> ctypes.CDLL:
+    """The loaded library; raises ImportError when it has not been built."""
+    if _lib_handle[0] is None:
+        _lib_handle[0] = _load()
+    return _lib_handle[0]
+
+
+def _status_string(status: int) -> str:
+    return _L().flux_attn_status_string(status).decode()
+
+
+def _check(status: int) -> int:
+    if status != FLUX_ATTN_OK:
+        raise FluxAttnError(status, _L().flux_attn_last_error().decode())
+    return status
+
+
+def _ptr(t) -> Optional[int]:
+    """Device pointer of a tensor (or a raw integer address, or None)."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+# ------------------------------------------------------------ C-named calls
+
+def flux_attn_create(batch: int, num_heads: int, max_tokens: int, head_dim: int = HEAD_DIM,
+                     axes_dim: Sequence[int] = (16, 56, 56), rope_theta: float = 10000.0,
+                     rms_eps: float = 1e-6, precision: int = FLUX_ATTN_BF16, debug_flags: int = 0) -> int:
+    cfg = flux_attn_config(batch, num_heads, head_dim, max_tokens, (ctypes.c_int * 3)(*axes_dim),
+                           rope_theta, rms_eps, precision, debug_flags)
+    h = ctypes.c_void_p()
+    _check(_L().flux_attn_create(ctypes.byref(cfg), ctypes.byref(h)))
+    return h.value
+
+
+def flux_attn_destroy(h: int) -> None:
+    _check(_L().flux_attn_destroy(h))
+
+
+def flux_attn_forward(h, q, k, v, txt_len, img_h, img_w, ref_h, ref_w, pos_ids, q_norm_w, k_norm_w,
+                      out, stream=None) -> None:
+    _check(_L().flux_attn_forward(h, _ptr(q), _ptr(k), _ptr(v), txt_len, img_h, img_w, ref_h, ref_w,
+                                  _ptr(pos_ids), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(out), _stream(stream)))
+
+
+def flux_attn_prologue(h, q, k, txt_len, img_h, img_w, ref_h, ref_w, pos_ids, q_norm_w, k_norm_w,
+                       qn, kn, stream=None) -> None:
+    _check(_L().flux_attn_prologue(h, _ptr(q), _ptr(k), txt_len, img_h, img_w, ref_h, ref_w, _ptr(pos_ids),
+                                   _ptr(q_norm_w), _ptr(k_norm_w), _ptr(qn), _ptr(kn), _stream(stream)))
+
+
+def flux_attn_attend(h, qn, kn, v, n_tokens, out, stream=None) -> None:
+    _check(_L().flux_attn_attend(h, _ptr(qn), _ptr(kn), _ptr(v), n_tokens, _ptr(out), _stream(stream)))
+
+
+def flux_attn_prologue_fp8(h, q, k, v, txt_len, img_h, img_w, ref_h, ref_w, pos_ids, q_norm_w, k_norm_w,
+                           q8, k8, v8t, scales, stream=None) -> None:
+    _check(_L().flux_attn_prologue_fp8(h, _ptr(q), _ptr(k), _ptr(v), txt_len, img_h, img_w, ref_h, ref_w,
+                                       _ptr(pos_ids), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(q8), _ptr(k8),
+                                       _ptr(v8t), _ptr(scales), _stream(stream)))
+
+
+def flux_attn_attend_fp8(h, q8, k8, v8t, scales, n_tokens, out, stream=None) -> None:
+    _check(_L().flux_attn_attend_fp8(h, _ptr(q8), _ptr(k8), _ptr(v8t), _ptr(scales), n_tokens, _ptr(out),
+                                     _stream(stream)))
+
+
+def flux_attn_sync_status(h, stream=None) -> int:
+    """Synchronise the stream and return the device status (no exception)."""
+    return int(_L().flux_attn_sync_status(h, _stream(stream)))
+
+
+def flux_attn_workspace_bytes(h) -> int:
+    return int(_L().flux_attn_workspace_bytes(h))
+
+
+def flux_attn_launches_per_forward(h, n_tokens: int) -> int:
+    return int(_L().flux_attn_launches_per_forward(h, n_tokens))
+
+
+def flux_attn_status_string(status: int) -> str:
+    return _status_string(status)
+
+
+def flux_attn_last_error() -> str:
+    return _L().flux_attn_last_error().decode()
+
+
+# ---------------------------------------------------------------- wrapper
+
+def _require(t, dtype, shape, name):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.dtype != dtype or not t.is_cuda or not t.is_contiguous() or tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must be a contiguous CUDA %s tensor of shape %s (got %s %s %s)"
+                         % (name, dtype, tuple(shape), t.dtype, t.device, tuple(t.shape)))
+
+
+class FluxAttention:
+    """One library handle: joint attention with the QK-RMSNorm + RoPE prologue.
+
+    Tensors are torch CUDA tensors on the handle's device: q, k, v, out bf16
+    [B, N, H, 128]; q_norm_w, k_norm_w fp32 [128]; pos_ids int32 [N, 3] or
+    None (positions derived from the text/image/reference geometry).
+    """
+
+    def __init__(self, batch: int, num_heads: int, max_tokens: int, precision: str = "bf16",
+                 axes_dim: Sequence[int] = (16, 56, 56), rope_theta: float = 10000.0,
+                 rms_eps: float = 1e-6, debug_flags: int = 0):
+        self.batch, self.num_heads, self.max_tokens = batch, num_heads, max_tokens
+        self.precision = precision
+        prec = {"bf16": FLUX_ATTN_BF16, "fp8": FLUX_ATTN_FP8_E4M3}[precision]
+        self.handle = flux_attn_create(batch, num_heads, max_tokens, HEAD_DIM, axes_dim, rope_theta, rms_eps,
+                                       prec, debug_flags)
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            flux_attn_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def _shape(self, n: int) -> Tuple[int, int, int, int]:
+        return (self.batch, n, self.num_heads, HEAD_DIM)
+
+    def forward(self, q, k, v, txt_len: int, img_h: int, img_w: int, ref_h: int = 0, ref_w: int = 0,
+                q_norm_w=None, k_norm_w=None, pos_ids=None, out=None, stream=None):
+        import torch
+        n = txt_len + img_h * img_w + ref_h * ref_w
+        for t, name in ((q, "q"), (k, "k"), (v, "v")):
+            _require(t, torch.bfloat16, self._shape(n), name)
+        _require(q_norm_w, torch.float32, (HEAD_DIM,), "q_norm_w")
+        _require(k_norm_w, torch.float32, (HEAD_DIM,), "k_norm_w")
+        if pos_ids is not None:
+            _require(pos_ids, torch.int32, (n, 3), "pos_ids")
+        if out is None:
+            out = torch.empty_like(q)
+        _require(out, torch.bfloat16, self._shape(n), "out")
+        flux_attn_forward(self.handle, q, k, v, txt_len, img_h, img_w, ref_h, ref_w, pos_ids, q_norm_w,
+                          k_norm_w, out, stream)
+        return out
+
+    def prologue(self, q, k, txt_len: int, img_h: int, img_w: int, ref_h: int = 0, ref_w: int = 0,
+                 q_norm_w=None, k_norm_w=None, pos_ids=None, qn=None, kn=None, stream=None):
+        import torch
+        n = txt_len + img_h * img_w + ref_h * ref_w
+        _require(q, torch.bfloat16, self._shape(n), "q")
+        _require(k, torch.bfloat16, self._shape(n), "k")
+        _require(q_norm_w, torch.float32, (HEAD_DIM,), "q_norm_w")
+        _require(k_norm_w, torch.float32, (HEAD_DIM,), "k_norm_w")
+        hm = (self.batch, self.num_heads, n, HEAD_DIM)
+        qn = torch.empty(hm, dtype=torch.bfloat16, device=q.device) if qn is None else qn
+        kn = torch.empty(hm, dtype=torch.bfloat16, device=q.device) if kn is None else kn
+        _require(qn, torch.bfloat16, hm, "qn")
+        _require(kn, torch.bfloat16, hm, "kn")
+        flux_attn_prologue(self.handle, q, k, txt_len, img_h, img_w, ref_h, ref_w, pos_ids, q_norm_w, k_norm_w,
+                           qn, kn, stream)
+        return qn, kn
+
+    def attend(self, qn, kn, v, out=None, stream=None):
+        import torch
+        n = qn.shape[2]
+        hm = (self.batch, self.num_heads, n, HEAD_DIM)
+        _require(qn, torch.bfloat16, hm, "qn")
+        _require(kn, torch.bfloat16, hm, "kn")
+        _require(v, torch.bfloat16, self._shape(n), "v")
+        out = torch.empty_like(v) if out is None else out
+        _require(out, torch.bfloat16, self._shape(n), "out")
+        flux_attn_attend(self.handle, qn, kn, v, n, out, stream)
+        return out
+
+    def sync_status(self, stream=None) -> int:
+        return flux_attn_sync_status(self.handle, stream)
+
+    def workspace_bytes(self) -> int:
+        return flux_attn_workspace_bytes(self.handle)
+
+    def launches_per_forward(self, n_tokens: int) -> int:
+        return flux_attn_launches_per_forward(self.handle, n_tokens)

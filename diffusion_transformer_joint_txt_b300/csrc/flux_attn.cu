@@ -1,0 +1,413 @@
+// flux_attn.cu -- C ABI of the joint text/image attention library (see
+// include/flux_attn.h for the contract of every entry point).
+//
+// Host side only: argument checks, workspace, TMA tensor maps and launches.
+// The arithmetic of the path runs in the kernels of prologue.cuh,
+// attention_bf16.cuh and attention_fp8.cuh.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "flux_attn.h"
+#include "attention_bf16.cuh"
+#include "prologue.cuh"
+
+struct flux_attn {
+  flux_attn_config cfg;
+  int device;
+  int num_sms;
+  size_t ws_bytes;
+  void* ws;               // one allocation, carved below
+  __nv_bfloat16* qn;      // [B, H, max_tokens, 128]
+  __nv_bfloat16* kn;      // [B, H, max_tokens, 128]
+  uint32_t* err;          // device error word
+  flux::RopeTable rope;
+};
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int status, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return status;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(FLUX_ATTN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Driver entry points, fetched through the runtime so the library does not
+// link libcuda directly.
+struct Driver {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  PFN_cuPointerGetAttribute_v4000 ptr_attr = nullptr;
+};
+
+const Driver& driver() {
+  static Driver d;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      d.encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuPointerGetAttribute", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      d.ptr_attr = reinterpret_cast<PFN_cuPointerGetAttribute_v4000>(p);
+  });
+  return d;
+}
+
+// A device buffer argument: non-null, 16-byte aligned, device memory, and the
+// allocation it belongs to covers [p, p + bytes).
+int check_buffer(const void* p, size_t bytes, const char* name) {
+  if (p == nullptr) return fail(FLUX_ATTN_ERR_INVALID_ARG, "%s is NULL", name);
+  if (reinterpret_cast<uintptr_t>(p) & 15u)
+    return fail(FLUX_ATTN_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);
+  const Driver& d = driver();
+  if (d.ptr_attr == nullptr) return fail(FLUX_ATTN_ERR_CUDA, "cuPointerGetAttribute unavailable");
+  CUdeviceptr start = 0;
+  size_t size = 0;
+  unsigned int mem_type = 0;
+  const CUdeviceptr dp = reinterpret_cast<CUdeviceptr>(p);
+  if (d.ptr_attr(&mem_type, CU_POINTER_ATTRIBUTE_MEMORY_TYPE, dp) != CUDA_SUCCESS ||
+      mem_type != CU_MEMORYTYPE_DEVICE)
+    return fail(FLUX_ATTN_ERR_INVALID_ARG, "%s is not a device pointer", name);
+  if (d.ptr_attr(&start, CU_POINTER_ATTRIBUTE_RANGE_START_ADDR, dp) != CUDA_SUCCESS ||
+      d.ptr_attr(&size, CU_POINTER_ATTRIBUTE_RANGE_SIZE, dp) != CUDA_SUCCESS)
+    return fail(FLUX_ATTN_ERR_INVALID_ARG, "%s: cannot query its allocation", name);
+  if (dp + bytes > start + size)
+    return fail(FLUX_ATTN_ERR_INVALID_ARG, "%s: %zu bytes needed, its allocation ends %zu bytes after it", name,
+                bytes, static_cast<size_t>(start + size - dp));
+  return FLUX_ATTN_OK;
+}
+
+int check_handle(const flux_attn* h) {
+  if (h == nullptr) return fail(FLUX_ATTN_ERR_INVALID_ARG, "handle is NULL");
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev != h->device)
+    return fail(FLUX_ATTN_ERR_INVALID_ARG, "handle was created on device %d, current device is %d", h->device,
+                dev);
+  return FLUX_ATTN_OK;
+}
+
+int token_count(const flux_attn* h, int txt, int ih, int iw, int rh, int rw, int* n_out) {
+  if (txt < 0 || ih < 0 || iw < 0 || rh < 0 || rw < 0)
+    return fail(FLUX_ATTN_ERR_INVALID_ARG, "negative geometry (txt=%d img=%dx%d ref=%dx%d)", txt, ih, iw, rh, rw);
+  const long long n = static_cast<long long>(txt) + static_cast<long long>(ih) * iw +
+                      static_cast<long long>(rh) * rw;
+  if (n > h->cfg.max_tokens)
+    return fail(FLUX_ATTN_ERR_INVALID_ARG, "N = %lld tokens exceeds max_tokens = %d", n, h->cfg.max_tokens);
+  *n_out = static_cast<int>(n);
+  return FLUX_ATTN_OK;
+}
+
+size_t row_bytes(const flux_attn* h, int n) {
+  return static_cast<size_t>(h->cfg.batch) * n * h->cfg.num_heads * flux::kHeadDim * 2;
+}
+
+int encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, cuuint32_t rank, const void* base,
+                 const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box, const char* what) {
+  const Driver& d = driver();
+  if (d.encode == nullptr) return fail(FLUX_ATTN_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = d.encode(map, dt, rank, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FLUX_ATTN_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed: %d", what, (int)r);
+  return FLUX_ATTN_OK;
+}
+
+int launch_prologue(flux_attn* h, const void* q, const void* k, int txt, int ih, int iw, int rh, int rw,
+                    const int32_t* pos, const float* wq, const float* wk, __nv_bfloat16* qn, __nv_bfloat16* kn,
+                    int n, cudaStream_t stream) {
+  (void)rh;
+  flux::TokenGeometry geo{pos, txt, ih * iw, iw, rw};
+  const int B = h->cfg.batch, H = h->cfg.num_heads;
+  const long long warps = static_cast<long long>(B) * n;
+  const int per_block = flux::kPrologueThreads / 32;
+  const unsigned blocks = static_cast<unsigned>((warps + per_block - 1) / per_block);
+  flux::qk_norm_rope_kernel<<<blocks, flux::kPrologueThreads, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), wq, wk, geo, B, n, H,
+      h->cfg.rms_eps, h->rope, qn, kn);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "prologue launch");
+  return FLUX_ATTN_OK;
+}
+
+int launch_attention_bf16(flux_attn* h, const void* qn, const void* kn, const void* v, int n, void* out,
+                          cudaStream_t stream) {
+  using namespace flux::attn;
+  const int B = h->cfg.batch, H = h->cfg.num_heads;
+  CUtensorMap tq, tk, tv;
+  {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(HD), static_cast<cuuint64_t>(n),
+                                static_cast<cuuint64_t>(B) * H};
+    const cuuint64_t strides[2] = {HD * 2ull, static_cast<cuuint64_t>(n) * HD * 2ull};
+    const cuuint32_t box[3] = {64, BM, 1};
+    int rc = encode_tiled(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, qn, dims, strides, box, "Q'");
+    if (rc) return rc;
+    rc = encode_tiled(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, kn, dims, strides, box, "K'");
+    if (rc) return rc;
+  }
+  {
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(HD), static_cast<cuuint64_t>(H),
+                                static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(B)};
+    const cuuint64_t strides[3] = {HD * 2ull, static_cast<cuuint64_t>(H) * HD * 2ull,
+                                   static_cast<cuuint64_t>(n) * H * HD * 2ull};
+    const cuuint32_t box[4] = {64, 1, BN, 1};
+    int rc = encode_tiled(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, v, dims, strides, box, "V");
+    if (rc) return rc;
+  }
+  Params prm;
+  prm.out = static_cast<__nv_bfloat16*>(out);
+  prm.err = h->err;
+  prm.N = n;
+  prm.H = H;
+  prm.nkv = (n + BN - 1) / BN;
+  prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(HD)));
+  prm.debug = h->cfg.debug_flags;
+  const dim3 grid((n + BM - 1) / BM, B * H);
+  attn_bf16_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(tq, tk, tv, prm);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+  return FLUX_ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* flux_attn_status_string(int status) {
+  switch (status) {
+    case FLUX_ATTN_OK: return "ok";
+    case FLUX_ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case FLUX_ATTN_ERR_UNSUPPORTED: return "unsupported device or configuration";
+    case FLUX_ATTN_ERR_OOM: return "out of device memory";
+    case FLUX_ATTN_ERR_CUDA: return "CUDA error";
+    case FLUX_ATTN_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+const char* flux_attn_last_error(void) { return g_last_error.c_str(); }
+
+int flux_attn_create(const flux_attn_config* cfg, flux_attn_t* out) {
+  g_last_error.clear();
+  if (out == nullptr) return fail(FLUX_ATTN_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (cfg == nullptr) return fail(FLUX_ATTN_ERR_INVALID_ARG, "cfg is NULL");
+  if (cfg->head_dim != flux::kHeadDim)
+    return fail(FLUX_ATTN_ERR_UNSUPPORTED, "head_dim = %d, only 128 is built", cfg->head_dim);
+  if (cfg->batch < 1 || cfg->num_heads < 1 || cfg->max_tokens < 1)
+    return fail(FLUX_ATTN_ERR_INVALID_ARG, "batch, num_heads and max_tokens must be >= 1");
+  if (static_cast<long long>(cfg->batch) * cfg->num_heads > 65535)
+    return fail(FLUX_ATTN_ERR_INVALID_ARG, "batch * num_heads must be <= 65535");
+  if (cfg->max_tokens > (1 << 24)) return fail(FLUX_ATTN_ERR_INVALID_ARG, "max_tokens must be <= 2^24");
+  const int* ax = cfg->axes_dim;
+  if (ax[0] < 0 || ax[1] < 0 || ax[2] < 0 || (ax[0] | ax[1] | ax[2]) & 1 ||
+      ax[0] + ax[1] + ax[2] != cfg->head_dim)
+    return fail(FLUX_ATTN_ERR_INVALID_ARG, "axes_dim (%d, %d, %d) must be even and sum to head_dim", ax[0], ax[1],
+                ax[2]);
+  // The prologue gives each lane 8 consecutive dims; they must stay in one axis block.
+  if (ax[0] % 8 || ax[1] % 8)
+    return fail(FLUX_ATTN_ERR_UNSUPPORTED, "axes_dim[0] and axes_dim[1] must be multiples of 8");
+  if (!(cfg->rope_theta > 0.f) || !(cfg->rms_eps >= 0.f))
+    return fail(FLUX_ATTN_ERR_INVALID_ARG, "rope_theta must be > 0 and rms_eps >= 0");
+  if (cfg->precision != FLUX_ATTN_BF16 && cfg->precision != FLUX_ATTN_FP8_E4M3)
+    return fail(FLUX_ATTN_ERR_INVALID_ARG, "unknown precision %d", cfg->precision);
+  if (cfg->precision == FLUX_ATTN_FP8_E4M3)
+    return fail(FLUX_ATTN_ERR_UNSUPPORTED, "the FP8 E4M3 path is not built in this version");
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  cudaDeviceProp prop;
+  e = cudaGetDeviceProperties(&prop, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
+  if (prop.major != 10 || prop.minor != 3)
+    return fail(FLUX_ATTN_ERR_UNSUPPORTED, "device %d is sm_%d%d, this library is built for sm_103a", dev,
+                prop.major, prop.minor);
+  if (driver().encode == nullptr || driver().ptr_attr == nullptr)
+    return fail(FLUX_ATTN_ERR_CUDA, "driver entry points unavailable");
+  e = cudaFuncSetAttribute(flux::attn::attn_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(flux::attn::SMEM_BYTES));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+
+  flux_attn* h = new flux_attn();
+  h->cfg = *cfg;
+  h->device = dev;
+  h->num_sms = prop.multiProcessorCount;
+  // RoPE table: pair j of axis block a (local index jj) turns by pos_a * theta^(-2 jj / d_a).
+  {
+    int j = 0;
+    for (int a = 0; a < 3; ++a)
+      for (int jj = 0; jj < ax[a] / 2; ++jj, ++j) {
+        h->rope.freq[j] = static_cast<float>(std::pow(static_cast<double>(cfg->rope_theta), -2.0 * jj / ax[a]));
+        h->rope.axis[j] = a;
+      }
+  }
+  const size_t qk_bytes = static_cast<size_t>(cfg->batch) * cfg->num_heads * cfg->max_tokens * flux::kHeadDim * 2;
+  const size_t err_off = 2 * qk_bytes;
+  h->ws_bytes = err_off + 256;
+  e = cudaMalloc(&h->ws, h->ws_bytes);
+  if (e != cudaSuccess) {
+    const size_t want = h->ws_bytes;
+    delete h;
+    cudaGetLastError();
+    return fail(FLUX_ATTN_ERR_OOM, "cudaMalloc(%zu) failed: %s", want, cudaGetErrorString(e));
+  }
+  h->qn = reinterpret_cast<__nv_bfloat16*>(h->ws);
+  h->kn = reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(h->ws) + qk_bytes);
+  h->err = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(h->ws) + err_off);
+  e = cudaMemset(h->err, 0, 256);
+  if (e != cudaSuccess) {
+    cudaFree(h->ws);
+    delete h;
+    return cuda_fail(e, "cudaMemset");
+  }
+  *out = h;
+  return FLUX_ATTN_OK;
+}
+
+int flux_attn_destroy(flux_attn_t h) {
+  if (h == nullptr) return FLUX_ATTN_OK;
+  int prev = -1;
+  cudaGetDevice(&prev);
+  if (prev != h->device) cudaSetDevice(h->device);
+  cudaError_t e = cudaFree(h->ws);
+  if (prev >= 0 && prev != h->device) cudaSetDevice(prev);
+  delete h;
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFree");
+  return FLUX_ATTN_OK;
+}
+
+size_t flux_attn_workspace_bytes(flux_attn_t h) { return h ? h->ws_bytes : 0; }
+
+int flux_attn_launches_per_forward(flux_attn_t h, int n_tokens) {
+  if (h == nullptr || n_tokens <= 0) return 0;
+  return 2;
+}
+
+static int check_common(flux_attn* h, const void* q, const void* k, int txt, int ih, int iw, int rh, int rw,
+                        const int32_t* pos, const float* wq, const float* wk, int* n) {
+  int rc = check_handle(h);
+  if (rc) return rc;
+  rc = token_count(h, txt, ih, iw, rh, rw, n);
+  if (rc) return rc;
+  if (*n == 0) return FLUX_ATTN_OK;
+  const size_t bytes = row_bytes(h, *n);
+  if ((rc = check_buffer(q, bytes, "q"))) return rc;
+  if ((rc = check_buffer(k, bytes, "k"))) return rc;
+  if ((rc = check_buffer(wq, flux::kHeadDim * sizeof(float), "q_norm_w"))) return rc;
+  if ((rc = check_buffer(wk, flux::kHeadDim * sizeof(float), "k_norm_w"))) return rc;
+  if (pos != nullptr && (rc = check_buffer(pos, static_cast<size_t>(*n) * 3 * sizeof(int32_t), "pos_ids")))
+    return rc;
+  return FLUX_ATTN_OK;
+}
+
+int flux_attn_prologue(flux_attn_t h, const void* q, const void* k, int txt_len, int img_h, int img_w, int ref_h,
+                       int ref_w, const int32_t* pos_ids, const float* q_norm_w, const float* k_norm_w, void* qn,
+                       void* kn, cudaStream_t stream) {
+  g_last_error.clear();
+  int n = 0;
+  int rc = check_common(h, q, k, txt_len, img_h, img_w, ref_h, ref_w, pos_ids, q_norm_w, k_norm_w, &n);
+  if (rc || n == 0) return rc;
+  if (h->cfg.precision != FLUX_ATTN_BF16)
+    return fail(FLUX_ATTN_ERR_INVALID_ARG, "flux_attn_prologue needs a BF16 handle");
+  const size_t bytes = row_bytes(h, n);
+  if ((rc = check_buffer(qn, bytes, "qn"))) return rc;
+  if ((rc = check_buffer(kn, bytes, "kn"))) return rc;
+  return launch_prologue(h, q, k, txt_len, img_h, img_w, ref_h, ref_w, pos_ids, q_norm_w, k_norm_w,
+                         static_cast<__nv_bfloat16*>(qn), static_cast<__nv_bfloat16*>(kn), n, stream);
+}
+
+int flux_attn_attend(flux_attn_t h, const void* qn, const void* kn, const void* v, int n_tokens, void* out,
+                     cudaStream_t stream) {
+  g_last_error.clear();
+  int rc = check_handle(h);
+  if (rc) return rc;
+  if (h->cfg.precision != FLUX_ATTN_BF16)
+    return fail(FLUX_ATTN_ERR_INVALID_ARG, "flux_attn_attend needs a BF16 handle");
+  if (n_tokens < 0 || n_tokens > h->cfg.max_tokens)
+    return fail(FLUX_ATTN_ERR_INVALID_ARG, "n_tokens = %d outside [0, max_tokens = %d]", n_tokens,
+                h->cfg.max_tokens);
+  if (n_tokens == 0) return FLUX_ATTN_OK;
+  const size_t bytes = row_bytes(h, n_tokens);
+  if ((rc = check_buffer(qn, bytes, "qn"))) return rc;
+  if ((rc = check_buffer(kn, bytes, "kn"))) return rc;
+  if ((rc = check_buffer(v, bytes, "v"))) return rc;
+  if ((rc = check_buffer(out, bytes, "out"))) return rc;
+  return launch_attention_bf16(h, qn, kn, v, n_tokens, out, stream);
+}
+
+int flux_attn_forward(flux_attn_t h, const void* q, const void* k, const void* v, int txt_len, int img_h,
+                      int img_w, int ref_h, int ref_w, const int32_t* pos_ids, const float* q_norm_w,
+                      const float* k_norm_w, void* out, cudaStream_t stream) {
+  g_last_error.clear();
+  int n = 0;
+  int rc = check_common(h, q, k, txt_len, img_h, img_w, ref_h, ref_w, pos_ids, q_norm_w, k_norm_w, &n);
+  if (rc || n == 0) return rc;
+  const size_t bytes = row_bytes(h, n);
+  if ((rc = check_buffer(v, bytes, "v"))) return rc;
+  if ((rc = check_buffer(out, bytes, "out"))) return rc;
+  if (out == q || out == k || out == v) return fail(FLUX_ATTN_ERR_INVALID_ARG, "out aliases an input");
+  if (h->cfg.precision == FLUX_ATTN_BF16) {
+    rc = launch_prologue(h, q, k, txt_len, img_h, img_w, ref_h, ref_w, pos_ids, q_norm_w, k_norm_w, h->qn, h->kn,
+                         n, stream);
+    if (rc) return rc;
+    return launch_attention_bf16(h, h->qn, h->kn, v, n, out, stream);
+  }
+  return fail(FLUX_ATTN_ERR_UNSUPPORTED, "the FP8 E4M3 path is not built in this version");
+}
+
+int flux_attn_prologue_fp8(flux_attn_t h, const void* q, const void* k, const void* v, int txt_len, int img_h,
+                           int img_w, int ref_h, int ref_w, const int32_t* pos_ids, const float* q_norm_w,
+                           const float* k_norm_w, void* q8, void* k8, void* v8t, float* scales,
+                           cudaStream_t stream) {
+  (void)h; (void)q; (void)k; (void)v; (void)txt_len; (void)img_h; (void)img_w; (void)ref_h; (void)ref_w;
+  (void)pos_ids; (void)q_norm_w; (void)k_norm_w; (void)q8; (void)k8; (void)v8t; (void)scales; (void)stream;
+  return fail(FLUX_ATTN_ERR_UNSUPPORTED, "the FP8 E4M3 path is not built in this version");
+}
+
+int flux_attn_attend_fp8(flux_attn_t h, const void* q8, const void* k8, const void* v8t, const float* scales,
+                         int n_tokens, void* out, cudaStream_t stream) {
+  (void)h; (void)q8; (void)k8; (void)v8t; (void)scales; (void)n_tokens; (void)out; (void)stream;
+  return fail(FLUX_ATTN_ERR_UNSUPPORTED, "the FP8 E4M3 path is not built in this version");
+}
+
+int flux_attn_sync_status(flux_attn_t h, cudaStream_t stream) {
+  g_last_error.clear();
+  int rc = check_handle(h);
+  if (rc) return rc;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  uint32_t word = 0;
+  e = cudaMemcpy(&word, h->err, sizeof word, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+  if (word != 0) {
+    e = cudaMemset(h->err, 0, sizeof word);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
+    return fail(FLUX_ATTN_ERR_DEVICE_TIMEOUT, "a bounded device wait ran out (error word 0x%x)", word);
+  }
+  return FLUX_ATTN_OK;
+}
+
+}  // extern "C"

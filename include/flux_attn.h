@@ -1,0 +1,164 @@
+/*
+ * flux_attn.h -- C ABI of the B300 (sm_103a) joint text/image attention library.
+ *
+ * One operation: the attention forward pass of a FLUX-style diffusion
+ * transformer block, where the text tokens, the noisy target-image tokens and
+ * (for image-to-image) the reference-image tokens are concatenated into one
+ * sequence and attend jointly ("Speed up image generation with FLUX 3 Image
+ * Klein on NVIDIA Blackwell GPUs", section "FLUX 3 inference with TensorRT LLM
+ * VisualGen").  Q and K first get per-head RMSNorm and multi-axis rotary
+ * position embedding, the normalisation and RoPE that the same page's section
+ * "GEMM kernel optimisation" fuses into the QKV projection.  An FP8 (E4M3)
+ * variant with per-(batch, head) scales follows the same page's section
+ * "Quantized and sparse attention" (qk_dtype fp8, v_dtype fp8).
+ *
+ * Math, per batch b and head h, with d = head_dim = 128:
+ *   q'_n = RoPE(RMSNorm(q_n) * w_q, pos_n),  k'_n = RoPE(RMSNorm(k_n) * w_k, pos_n)
+ *   RMSNorm(x)_i = x_i / sqrt(mean_j x_j^2 + eps)
+ *   RoPE: the head dimension is cut into consecutive blocks of axes_dim[0..2]
+ *         dims; in block a the adjacent pair (2j, 2j+1) is rotated by
+ *         pos_n[a] * theta^(-2j / axes_dim[a]).
+ *   out_n = sum_m softmax_m(q'_n . k'_m / sqrt(d)) v_m   (no mask, non-causal)
+ *
+ * Conventions shared by every call:
+ *   - Tensors q, k, v, out are bf16, layout [B, N, H, 128], contiguous
+ *     (token-major, heads interleaved, the layout a QKV projection writes).
+ *   - N = txt_len + img_h * img_w + ref_h * ref_w, token order
+ *     [text | image row-major | reference row-major].
+ *   - Every pointer is a DEVICE pointer unless stated otherwise, 16-byte
+ *     aligned, owned by the caller, and must stay valid until the work
+ *     enqueued on `stream` has completed.  The library owns its workspace.
+ *   - Calls enqueue work on `stream` and return without synchronising.  One
+ *     handle serves one stream at a time (its workspace is shared).
+ *   - Every call returns a flux_attn_status.  On a nonzero status nothing was
+ *     enqueued, except FLUX_ATTN_ERR_CUDA from a failed launch.  Errors found
+ *     on the device (a bounded wait that ran out) are reported later by
+ *     flux_attn_sync_status.  flux_attn_last_error() describes the last
+ *     failure of the calling thread.
+ */
+#ifndef FLUX_ATTN_H
+#define FLUX_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define FLUX_ATTN_API __attribute__((visibility("default")))
+#else
+#define FLUX_ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FLUX_ATTN_OK = 0,
+  FLUX_ATTN_ERR_INVALID_ARG = 1,    /* bad pointer, size, alignment or geometry */
+  FLUX_ATTN_ERR_UNSUPPORTED = 2,    /* device is not compute capability 10.3, or head_dim != 128 */
+  FLUX_ATTN_ERR_OOM = 3,            /* workspace allocation failed in create */
+  FLUX_ATTN_ERR_CUDA = 4,           /* a CUDA runtime or driver call failed */
+  FLUX_ATTN_ERR_DEVICE_TIMEOUT = 5  /* a kernel's bounded wait ran out; its output is invalid */
+} flux_attn_status;
+
+typedef enum {
+  FLUX_ATTN_BF16 = 0,      /* bf16 Q'/K'/V/P operands, fp32 accumulation */
+  FLUX_ATTN_FP8_E4M3 = 1   /* E4M3 Q'/K'/V operands with per-(b, h) scales, E4M3 P */
+} flux_attn_precision;
+
+/* debug_flags bits */
+#define FLUX_ATTN_DEBUG_FORCE_TIMEOUT 1  /* the attention kernel waits on a barrier nothing
+                                            signals; every CTA gives up after its bounded
+                                            wait and sync_status reports DEVICE_TIMEOUT */
+
+typedef struct {
+  int batch;          /* B >= 1 */
+  int num_heads;      /* H >= 1 */
+  int head_dim;       /* must be 128 */
+  int max_tokens;     /* upper bound on N for every later call (sizes the workspace) */
+  int axes_dim[3];    /* RoPE axis block sizes, even, summing to head_dim; FLUX uses 16, 56, 56 */
+  float rope_theta;   /* RoPE base, FLUX uses 10000 */
+  float rms_eps;      /* RMSNorm epsilon, FLUX uses 1e-6 */
+  int precision;      /* flux_attn_precision */
+  int debug_flags;    /* FLUX_ATTN_DEBUG_* bits, 0 in production */
+} flux_attn_config;
+
+typedef struct flux_attn* flux_attn_t;
+
+/* Create a handle on the current CUDA device: checks the device, allocates
+ * the workspace for cfg->max_tokens (normalised Q/K, FP8 codes and scales,
+ * the device error word).  *out receives the handle (NULL on failure). */
+FLUX_ATTN_API int flux_attn_create(const flux_attn_config* cfg, flux_attn_t* out);
+
+/* Destroy a handle and free its workspace.  The caller must have completed
+ * (synchronised) every stream that used it.  NULL is accepted. */
+FLUX_ATTN_API int flux_attn_destroy(flux_attn_t h);
+
+/* The whole hot path: QK-RMSNorm + RoPE prologue (and, in FP8 mode, the amax
+ * and quantisation passes) followed by the joint attention kernel.
+ *   q, k, v       bf16 [B, N, H, 128]
+ *   geometry      txt_len, img_h, img_w, ref_h, ref_w >= 0; N = txt + img_h*img_w + ref_h*ref_w,
+ *                 1 <= N <= max_tokens (N == 0 is accepted and does nothing)
+ *   pos_ids       int32 [N, 3] position ids, or NULL: then text tokens get (0,0,0), image token
+ *                 (r, c) gets (0, r, c) and reference token (r, c) gets (1, r, c)
+ *   q_norm_w, k_norm_w  fp32 [128] RMSNorm weights (shared by all heads)
+ *   out           bf16 [B, N, H, 128]; must not alias q, k or v */
+FLUX_ATTN_API int flux_attn_forward(flux_attn_t h, const void* q, const void* k, const void* v,
+                      int txt_len, int img_h, int img_w, int ref_h, int ref_w,
+                      const int32_t* pos_ids, const float* q_norm_w, const float* k_norm_w,
+                      void* out, cudaStream_t stream);
+
+/* Prologue step alone (BF16 handles): writes the normalised, rotated Q' and K'
+ * in head-major layout, bf16 [B, H, N, 128], into the caller's qn and kn.
+ * Same argument rules as flux_attn_forward. */
+FLUX_ATTN_API int flux_attn_prologue(flux_attn_t h, const void* q, const void* k,
+                       int txt_len, int img_h, int img_w, int ref_h, int ref_w,
+                       const int32_t* pos_ids, const float* q_norm_w, const float* k_norm_w,
+                       void* qn, void* kn, cudaStream_t stream);
+
+/* Attention step alone (BF16 handles): out = softmax(qn kn^T / sqrt(128)) v for
+ *   qn, kn  bf16 [B, H, N, 128] (as written by flux_attn_prologue)
+ *   v       bf16 [B, N, H, 128]
+ *   out     bf16 [B, N, H, 128]
+ * with 1 <= n_tokens <= max_tokens (0 does nothing). */
+FLUX_ATTN_API int flux_attn_attend(flux_attn_t h, const void* qn, const void* kn, const void* v, int n_tokens,
+                     void* out, cudaStream_t stream);
+
+/* Prologue step alone (FP8 handles): per (b, h), amax of Q', K' and V, then
+ * E4M3 codes (round to nearest even, saturating at 448) of x / scale with
+ * scale = amax / 448 (1 when amax == 0).
+ *   q8, k8  uint8 [B, H, N, 128];  v8t  uint8 [B, H, 128, Npad] (V transposed,
+ *   Npad = N rounded up to a multiple of 16, padding columns zero)
+ *   scales  fp32 [B, H, 3] = (scale_q, scale_k, scale_v) */
+FLUX_ATTN_API int flux_attn_prologue_fp8(flux_attn_t h, const void* q, const void* k, const void* v,
+                           int txt_len, int img_h, int img_w, int ref_h, int ref_w,
+                           const int32_t* pos_ids, const float* q_norm_w, const float* k_norm_w,
+                           void* q8, void* k8, void* v8t, float* scales, cudaStream_t stream);
+
+/* Attention step alone (FP8 handles) on the outputs of flux_attn_prologue_fp8;
+ * out bf16 [B, N, H, 128]. */
+FLUX_ATTN_API int flux_attn_attend_fp8(flux_attn_t h, const void* q8, const void* k8, const void* v8t,
+                         const float* scales, int n_tokens, void* out, cudaStream_t stream);
+
+/* Synchronise `stream`, then read and clear the handle's device error word.
+ * Returns FLUX_ATTN_OK, FLUX_ATTN_ERR_DEVICE_TIMEOUT or FLUX_ATTN_ERR_CUDA. */
+FLUX_ATTN_API int flux_attn_sync_status(flux_attn_t h, cudaStream_t stream);
+
+/* Bytes of device workspace the handle holds. */
+FLUX_ATTN_API size_t flux_attn_workspace_bytes(flux_attn_t h);
+
+/* Kernel launches one flux_attn_forward call makes for n_tokens tokens. */
+FLUX_ATTN_API int flux_attn_launches_per_forward(flux_attn_t h, int n_tokens);
+
+/* Static description of a status code. */
+FLUX_ATTN_API const char* flux_attn_status_string(int status);
+
+/* Description of the last failure in the calling thread ("" if none). */
+FLUX_ATTN_API const char* flux_attn_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLUX_ATTN_H */

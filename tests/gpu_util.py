@@ -1,0 +1,49 @@
+"""Shared helpers of the GPU tests: move seeded inputs to the device, compare
+against the oracle with the stated tolerances."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+# Tolerances: BF16 max-abs 1e-2 and mean-abs 1e-3, FP8 max-abs 6e-2 (against
+# the oracle on its own dequantised inputs); plus an internal gate on the
+# relative RMS error so that a small systematic error cannot hide under a
+# loose absolute bound.
+BF16_MAX_ABS = 1e-2
+BF16_MEAN_ABS = 1e-3
+BF16_REL_RMS = 1e-2
+FP8_MAX_ABS = 6e-2
+
+
+def dev_bf16(bits: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def host_f64(t: torch.Tensor) -> np.ndarray:
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def device_inputs(inp):
+    return dict(q=dev_bf16(inp.q), k=dev_bf16(inp.k), v=dev_bf16(inp.v),
+                q_norm_w=torch.from_numpy(inp.w_q).cuda(), k_norm_w=torch.from_numpy(inp.w_k).cuda(),
+                pos_ids=torch.from_numpy(inp.pos).cuda())
+
+
+def gather_rows(out_bnhd: np.ndarray, rows: np.ndarray) -> np.ndarray:
+    return out_bnhd[rows[:, 0], rows[:, 2], rows[:, 1], :]
+
+
+def compare(got: np.ndarray, want: np.ndarray, max_abs: float, mean_abs: float = None,
+            rel_rms: float = None, what: str = ""):
+    assert got.shape == want.shape, (got.shape, want.shape)
+    assert np.all(np.isfinite(got)), "%s: non-finite output" % what
+    err = np.abs(got - want)
+    stats = dict(max_abs=float(err.max()), mean_abs=float(err.mean()),
+                 rel_rms=float(np.sqrt((err ** 2).mean() / max((want ** 2).mean(), 1e-300))))
+    msg = "%s: %s" % (what, stats)
+    assert stats["max_abs"] <= max_abs, msg
+    if mean_abs is not None:
+        assert stats["mean_abs"] <= mean_abs, msg
+    if rel_rms is not None:
+        assert stats["rel_rms"] <= rel_rms, msg
+    return stats
