@@ -68,6 +68,8 @@ def _load() -> ctypes.CDLL:
         "flux_attn_attend": (I, [P, P, P, P, I, P, P]),
         "flux_attn_prologue_fp8": (I, [P, P, P, P, I, I, I, I, I, P, P, P, P, P, P, P, P]),
         "flux_attn_attend_fp8": (I, [P, P, P, P, P, I, P, P]),
+        "flux_attn_forward_noalloc": (I, [ctypes.POINTER(flux_attn_config), P, P, P, I, I, I, I, I, P, P, P, P,
+                                          P, P]),
         "flux_attn_sync_status": (I, [P, P]),
         "flux_attn_workspace_bytes": (Z, [P]),
         "flux_attn_launches_per_forward": (I, [P, I]),
@@ -165,6 +167,25 @@ def flux_attn_prologue_fp8(h, q, k, v, txt_len, img_h, img_w, ref_h, ref_w, pos_
 def flux_attn_attend_fp8(h, q8, k8, v8t, scales, n_tokens, out, stream=None) -> None:
     _check(_L().flux_attn_attend_fp8(h, _ptr(q8), _ptr(k8), _ptr(v8t), _ptr(scales), n_tokens, _ptr(out),
                                      _stream(stream)))
+
+
+def make_config(batch: int, num_heads: int, max_tokens: int, head_dim: int = HEAD_DIM,
+                axes_dim: Sequence[int] = (16, 56, 56), rope_theta: float = 10000.0, rms_eps: float = 1e-6,
+                precision: int = FLUX_ATTN_BF16, debug_flags: int = 0) -> flux_attn_config:
+    return flux_attn_config(batch, num_heads, head_dim, max_tokens, (ctypes.c_int * 3)(*axes_dim),
+                            rope_theta, rms_eps, precision, debug_flags)
+
+
+def flux_attn_forward_noalloc(cfg: flux_attn_config, q, k, v, txt_len, img_h, img_w, ref_h, ref_w, pos_ids,
+                              q_norm_w, k_norm_w, out, device_error=None, stream=None) -> None:
+    """The allocation-free forward: same result as flux_attn_forward without a
+    handle and without any device allocation (for callers that reserve all
+    device memory up front).  Its scratch is one array shared by every call on
+    a device, so calls must not overlap on the GPU; the limit is
+    batch * num_heads * N <= 32768."""
+    _check(_L().flux_attn_forward_noalloc(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), txt_len, img_h, img_w,
+                                          ref_h, ref_w, _ptr(pos_ids), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(out),
+                                          _ptr(device_error), _stream(stream)))
 
 
 def flux_attn_sync_status(h, stream=None) -> int:

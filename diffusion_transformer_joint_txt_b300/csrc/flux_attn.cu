@@ -411,3 +411,149 @@ int flux_attn_sync_status(flux_attn_t h, cudaStream_t stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free forward.
+//
+// Some callers must not allocate device memory on the call path: inference
+// engines that reserve and plan all device memory once at start-up and forbid
+// any later cudaMalloc, plugin hosts that give a plugin only the buffers it
+// declared, and latency-critical callers that cannot take the implicit
+// device-wide synchronisation that cudaMalloc / cudaFree may cause.  For them
+// flux_attn_forward_noalloc runs the same two kernels as flux_attn_forward
+// without a handle: the normalised Q'/K' scratch and the device error word
+// live in the file-scope array below, which the CUDA module holds on every
+// device that loads this library until the process exits.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocWordBytes = 256;                       // device error word (+ padding)
+constexpr size_t kNoAllocQKBytes = size_t(16) << 20;            // Q' and K', bf16
+constexpr size_t kNoAllocRowBytes = flux::kHeadDim * 2;         // one bf16 head row
+constexpr long long kNoAllocMaxTokenHeads = kNoAllocQKBytes / (2 * kNoAllocRowBytes);  // 32768
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocWordBytes + kNoAllocQKBytes];
+
+struct NoAllocDevice {
+  std::once_flag once;
+  int status = FLUX_ATTN_ERR_CUDA;
+  uint8_t* base = nullptr;  // device address of g_noalloc_scratch on this device
+  std::string msg;
+};
+constexpr int kNoAllocMaxDevices = 64;
+NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
+
+// Once per device, with that device current: look up the device address of
+// the scratch array (the host-side symbol is only a stand-in) and raise the
+// attention kernel's dynamic shared-memory limit.
+int noalloc_setup(int dev, uint8_t** base) {
+  if (dev < 0 || dev >= kNoAllocMaxDevices)
+    return fail(FLUX_ATTN_ERR_UNSUPPORTED, "device ordinal %d beyond %d", dev, kNoAllocMaxDevices);
+  NoAllocDevice& d = g_noalloc_dev[dev];
+  std::call_once(d.once, [&d] {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) {
+      d.msg = std::string("cudaGetSymbolAddress(scratch): ") + cudaGetErrorString(e);
+      return;
+    }
+    e = cudaFuncSetAttribute(flux::attn::attn_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(flux::attn::SMEM_BYTES));
+    if (e != cudaSuccess) {
+      d.msg = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
+      return;
+    }
+    d.base = static_cast<uint8_t*>(p);
+    d.status = FLUX_ATTN_OK;
+  });
+  if (d.status != FLUX_ATTN_OK) return fail(d.status, "%s", d.msg.c_str());
+  *base = d.base;
+  return FLUX_ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" int flux_attn_forward_noalloc(const flux_attn_config* cfg, const void* q, const void* k, const void* v,
+                                         int txt_len, int img_h, int img_w, int ref_h, int ref_w,
+                                         const int32_t* pos_ids, const float* q_norm_w, const float* k_norm_w,
+                                         void* out, uint32_t* device_error, cudaStream_t stream) {
+  g_last_error.clear();
+  if (cfg == nullptr) return fail(FLUX_ATTN_ERR_INVALID_ARG, "cfg is NULL");
+  if (cfg->head_dim != flux::kHeadDim)
+    return fail(FLUX_ATTN_ERR_UNSUPPORTED, "head_dim = %d, only 128 is built", cfg->head_dim);
+  if (cfg->precision != FLUX_ATTN_BF16)
+    return fail(FLUX_ATTN_ERR_UNSUPPORTED, "the allocation-free forward is BF16 only");
+  if (cfg->batch < 1 || cfg->num_heads < 1 || cfg->max_tokens < 1)
+    return fail(FLUX_ATTN_ERR_INVALID_ARG, "batch, num_heads and max_tokens must be >= 1");
+  const int* ax = cfg->axes_dim;
+  if (ax[0] < 0 || ax[1] < 0 || ax[2] < 0 || (ax[0] | ax[1] | ax[2]) & 1 ||
+      ax[0] + ax[1] + ax[2] != cfg->head_dim)
+    return fail(FLUX_ATTN_ERR_INVALID_ARG, "axes_dim (%d, %d, %d) must be even and sum to head_dim", ax[0], ax[1],
+                ax[2]);
+  if (ax[0] % 8 || ax[1] % 8)
+    return fail(FLUX_ATTN_ERR_UNSUPPORTED, "axes_dim[0] and axes_dim[1] must be multiples of 8");
+  if (!(cfg->rope_theta > 0.f) || !(cfg->rms_eps >= 0.f))
+    return fail(FLUX_ATTN_ERR_INVALID_ARG, "rope_theta must be > 0 and rms_eps >= 0");
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  int major = 0, minor = 0;
+  if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+    return cuda_fail(e, "cudaDeviceGetAttribute");
+  if (major != 10 || minor != 3)
+    return fail(FLUX_ATTN_ERR_UNSUPPORTED, "device %d is sm_%d%d, this library is built for sm_103a", dev, major,
+                minor);
+
+  // A handle-shaped view of this call; nothing in it is allocated.
+  flux_attn view;
+  view.cfg = *cfg;
+  view.device = dev;
+  view.num_sms = 0;
+  view.ws = nullptr;
+  view.ws_bytes = 0;
+  {
+    int j = 0;
+    for (int a = 0; a < 3; ++a)
+      for (int jj = 0; jj < ax[a] / 2; ++jj, ++j) {
+        view.rope.freq[j] = static_cast<float>(std::pow(static_cast<double>(cfg->rope_theta), -2.0 * jj / ax[a]));
+        view.rope.axis[j] = a;
+      }
+  }
+  int n = 0;
+  int rc = token_count(&view, txt_len, img_h, img_w, ref_h, ref_w, &n);
+  if (rc || n == 0) return rc;
+  const long long token_heads = static_cast<long long>(cfg->batch) * cfg->num_heads * n;
+  if (token_heads > kNoAllocMaxTokenHeads)
+    return fail(FLUX_ATTN_ERR_INVALID_ARG,
+                "batch * num_heads * N = %lld exceeds the allocation-free limit of %lld (16 MiB of Q'/K' scratch)",
+                token_heads, kNoAllocMaxTokenHeads);
+  uint8_t* base = nullptr;
+  if ((rc = noalloc_setup(dev, &base))) return rc;
+  view.err = reinterpret_cast<uint32_t*>(base);
+  view.qn = reinterpret_cast<__nv_bfloat16*>(base + kNoAllocWordBytes);
+  view.kn = reinterpret_cast<__nv_bfloat16*>(base + kNoAllocWordBytes + token_heads * kNoAllocRowBytes);
+
+  if ((rc = check_common(&view, q, k, txt_len, img_h, img_w, ref_h, ref_w, pos_ids, q_norm_w, k_norm_w, &n)))
+    return rc;
+  const size_t bytes = row_bytes(&view, n);
+  if ((rc = check_buffer(v, bytes, "v"))) return rc;
+  if ((rc = check_buffer(out, bytes, "out"))) return rc;
+  if (out == q || out == k || out == v) return fail(FLUX_ATTN_ERR_INVALID_ARG, "out aliases an input");
+  if (device_error != nullptr && (rc = check_buffer(device_error, sizeof(uint32_t), "device_error"))) return rc;
+
+  // The scratch keeps the previous call's contents: the error word must start at zero.
+  e = cudaMemsetAsync(view.err, 0, sizeof(uint32_t), stream);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the scratch error word");
+  rc = launch_prologue(&view, q, k, txt_len, img_h, img_w, ref_h, ref_w, pos_ids, q_norm_w, k_norm_w, view.qn,
+                       view.kn, n, stream);
+  if (rc) return rc;
+  rc = launch_attention_bf16(&view, view.qn, view.kn, v, n, out, stream);
+  if (rc) return rc;
+  if (device_error != nullptr) {
+    e = cudaMemcpyAsync(device_error, view.err, sizeof(uint32_t), cudaMemcpyDeviceToDevice, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "copying the scratch error word");
+  }
+  return FLUX_ATTN_OK;
+}

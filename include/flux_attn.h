@@ -141,6 +141,37 @@ FLUX_ATTN_API int flux_attn_prologue_fp8(flux_attn_t h, const void* q, const voi
 FLUX_ATTN_API int flux_attn_attend_fp8(flux_attn_t h, const void* q8, const void* k8, const void* v8t,
                          const float* scales, int n_tokens, void* out, cudaStream_t stream);
 
+/* Allocation-free forward (BF16).  The pages this library follows have no
+ * counterpart to this call; it exists for callers that must not allocate
+ * device memory while they run: engines that reserve and plan all device
+ * memory once at start-up and forbid any later cudaMalloc, plugin hosts that
+ * hand a plugin only the buffers it declared, and latency-critical callers
+ * that cannot take the implicit device-wide synchronisation cudaMalloc and
+ * cudaFree may cause.
+ *
+ * It computes exactly what flux_attn_forward computes, with the same kernels,
+ * but needs no handle and allocates nothing: its Q'/K' scratch and its
+ * device error word live in one file-scope device array of 16 MiB + 256 B
+ * that the library's CUDA module holds on every device that loads it, until
+ * the process exits.
+ *   cfg           as for flux_attn_create; precision must be FLUX_ATTN_BF16
+ *   q, k, v, out, geometry, pos_ids, norm weights, stream: as for flux_attn_forward
+ *   device_error  optional device uint32: after the kernels it receives the
+ *                 call's device error word (0 when every bounded wait was
+ *                 satisfied, nonzero when one ran out); NULL to skip.
+ * Limits: batch * num_heads * N <= 32768 (FLUX_ATTN_ERR_INVALID_ARG beyond).
+ * Every call shares the one scratch array and the error word is cleared at
+ * the start of each call; calls that overlap on the GPU (other streams,
+ * other host threads) race on it, so serialise them per device.  The first
+ * call on a device does a one-time set-up (it looks up the array's device
+ * address and sets the attention kernel's shared-memory limit); make that
+ * first call before any stream capture. */
+FLUX_ATTN_API int flux_attn_forward_noalloc(const flux_attn_config* cfg, const void* q, const void* k,
+                                            const void* v, int txt_len, int img_h, int img_w, int ref_h,
+                                            int ref_w, const int32_t* pos_ids, const float* q_norm_w,
+                                            const float* k_norm_w, void* out, uint32_t* device_error,
+                                            cudaStream_t stream);
+
 /* Synchronise `stream`, then read and clear the handle's device error word.
  * Returns FLUX_ATTN_OK, FLUX_ATTN_ERR_DEVICE_TIMEOUT or FLUX_ATTN_ERR_CUDA. */
 FLUX_ATTN_API int flux_attn_sync_status(flux_attn_t h, cudaStream_t stream);
