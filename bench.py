@@ -9,8 +9,9 @@ Metric: joint-attention TFLOP/s = 4 B H N^2 d / step time, on the FLUX-dev
 seeded synthetic bf16 inputs already resident in HBM.  A step is one
 flux_attn_prologue + one flux_attn_attend call (= flux_attn_forward); L2 is
 flushed (a 256 MB write) before every timed step, outside the step's events.
-The FLUX 2048x2048 step (N=16896) is measured the same way and reported under
-"secondary".
+The FLUX 2048x2048 step (N=16896, BF16) and the FP8 classifier-free-guidance
+pair at 2048x2048 (B=2, N=16896: amax + E4M3 quantise + FP8 attention) are
+measured the same way and reported under "secondary".
 
 One JSON line on rank 0.  Under torchrun every rank runs its own replica of
 the workload (the (batch, head) units are independent; no collective is on
@@ -42,11 +43,11 @@ if ROOT not in sys.path:
 import synthetic  # noqa: E402
 
 PRIMARY = "flux_1024_4608"
-SECONDARY = "flux_2048_16896"
+SECONDARY = ["flux_2048_16896", "fp8_cfg_2048_16896"]
 METRIC = "joint-attn TFLOP/s & % of B300 BF16/FP8 TC peak at 4608/16896 tokens"
 FALLBACK_PEAKS = {"bf16_tflops": 1800.0, "hbm_gbs": 6400.0}
 L2_FLUSH_BYTES = 256 << 20
-ATTN_SOURCES = ["diffusion_transformer_joint_txt_b300/csrc/attention_bf16.cuh",
+ATTN_SOURCES = ["diffusion_transformer_joint_txt_b300/csrc/attention.cuh",
                 "diffusion_transformer_joint_txt_b300/csrc/ptx.cuh"]
 
 
@@ -154,30 +155,82 @@ def device_inputs(w, torch):
         torch.from_numpy(inp.w_k).cuda()
 
 
-def time_device(w, steps, warmup, torch, fa, flush):
-    """Device-timed steps: returns (mean step ms, mean attention-kernel ms, launches, out)."""
-    inp, q, k, v, wq, wk = device_inputs(w, torch)
-    n = w.tokens
-    attn = fa.FluxAttention(w.batch, w.heads, n)
-    hm = (w.batch, w.heads, n, 128)
-    qn = torch.empty(hm, dtype=torch.bfloat16, device="cuda")
-    kn = torch.empty(hm, dtype=torch.bfloat16, device="cuda")
-    out = torch.empty_like(q)
-    stream = torch.cuda.current_stream()
-    geo = (w.txt_len, w.img_h, w.img_w, w.ref_h, w.ref_w)
+class Step:
+    """One pass of the hot path over one workload, inputs resident in HBM:
+    the prologue call, then the attention call, each bracketed by CUDA events
+    on the launching stream."""
 
-    def step():
-        attn.prologue(q, k, *geo, wq, wk, qn=qn, kn=kn)
-        attn.attend(qn, kn, v, out=out)
+    def __init__(self, w, torch, fa):
+        self.w = w
+        self.fp8 = w.precision == "fp8"
+        self.inp, self.q, self.k, self.v, self.wq, self.wk = device_inputs(w, torch)
+        n = w.tokens
+        self.attn = fa.FluxAttention(w.batch, w.heads, n, precision=w.precision)
+        self.geo = (w.txt_len, w.img_h, w.img_w, w.ref_h, w.ref_w)
+        B, H = w.batch, w.heads
+        if self.fp8:
+            self.q8 = torch.empty((B, H, n, 128), dtype=torch.uint8, device="cuda")
+            self.k8 = torch.empty_like(self.q8)
+            self.v8t = torch.empty((B, H, 128, fa.pad16(n)), dtype=torch.uint8, device="cuda")
+            self.scales = torch.empty((B, H, 3), dtype=torch.float32, device="cuda")
+        else:
+            self.qn = torch.empty((B, H, n, 128), dtype=torch.bfloat16, device="cuda")
+            self.kn = torch.empty_like(self.qn)
+        self.out = torch.empty_like(self.q)
+        self.stream = torch.cuda.current_stream()
 
+    def prologue(self):
+        if self.fp8:
+            self.attn.prologue_fp8(self.q, self.k, self.v, *self.geo, self.wq, self.wk, q8=self.q8, k8=self.k8,
+                                   v8t=self.v8t, scales=self.scales)
+        else:
+            self.attn.prologue(self.q, self.k, *self.geo, self.wq, self.wk, qn=self.qn, kn=self.kn)
+
+    def attend(self):
+        if self.fp8:
+            self.attn.attend_fp8(self.q8, self.k8, self.v8t, self.scales, out=self.out)
+        else:
+            self.attn.attend(self.qn, self.kn, self.v, out=self.out)
+
+    def __call__(self, ev=None):
+        if ev is not None:
+            ev[0].record(self.stream)
+        self.prologue()
+        if ev is not None:
+            ev[1].record(self.stream)
+        self.attend()
+        if ev is not None:
+            ev[2].record(self.stream)
+
+    @property
+    def prologue_bytes(self):
+        """Algorithmic HBM bytes of the prologue per step.  BF16: read q, k and
+        write Q', K' (2 + 2 bytes per element each).  FP8: the amax pass reads
+        q, k, v; the quantise pass reads them again and writes one E4M3 byte
+        per element of Q', K', V (the scales need the whole head first)."""
+        elems = self.w.batch * self.w.tokens * self.w.heads * 128
+        return elems * (15 if self.fp8 else 8)
+
+
+def measure(step, steps, warmup, torch, flush, barrier):
+    """Mean step, attention-kernel and prologue times (ms) over `steps` timed
+    steps; L2 is flushed before every step, outside its events."""
     for _ in range(warmup):
         flush.zero_()
         step()
-    if attn.sync_status() != 0:
-        raise RuntimeError("device status error in warm-up")
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-    return attn, step, ev, (q, k, v, wq, wk, out, qn, kn), geo, inp, stream
+    if step.attn.sync_status() != 0:
+        raise RuntimeError("device status error in warm-up (%s)" % step.w.name)
+    ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(steps)]
+    barrier()
+    for e in ev:
+        flush.zero_()
+        step(e)
+    barrier()
+    if step.attn.sync_status() != 0:
+        raise RuntimeError("device status error during the timed region (%s)" % step.w.name)
+    return (sum(a.elapsed_time(c) for a, _, c in ev) / steps,
+            sum(b.elapsed_time(c) for _, b, c in ev) / steps,
+            sum(a.elapsed_time(b) for a, b, _ in ev) / steps)
 
 
 def run_ours(args):
@@ -190,11 +243,9 @@ def run_ours(args):
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     peaks, peak_kind = load_peaks()
-    w = synthetic.WORKLOADS[args.workload]
+    peak_bf16 = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
-
-    attn, step, ev, bufs, geo, inp, stream = time_device(w, args.steps, args.warmup, torch, fa, flush)
-    q, k, v, wq, wk, out, qn, kn = bufs
 
     def barrier():
         torch.cuda.synchronize()
@@ -202,100 +253,70 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize()
 
+    def slowest(vals):
+        t = torch.tensor(vals, dtype=torch.float64, device="cuda")
+        if world > 1:
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return t.tolist()
+
+    def summary(step, times, n_steps):
+        w = step.w
+        s_ms, a_ms, p_ms = times
+        peak = peak_bf16 * (2.0 if step.fp8 else 1.0)
+        nominal = 4500.0 if step.fp8 else 2250.0
+        achieved = w.flops / (a_ms * 1e-3) / 1e12
+        return {"workload": w.name, "precision": w.precision, "batch": w.batch, "heads": w.heads,
+                "tokens": w.tokens, "steps": n_steps, "value": w.flops * world / (s_ms * 1e-3) / 1e12,
+                "ms_per_step": s_ms, "attn_kernel_ms": a_ms, "attn_tflops": achieved,
+                "roofline_frac": achieved / peak, "peak_tflops": peak,
+                "frac_of_nominal": achieved / nominal, "nominal_tflops": nominal,
+                "prologue_ms": p_ms, "prologue_gbs": step.prologue_bytes / (p_ms * 1e-3) / 1e9,
+                "gpu_launches": n_steps * step.attn.launches_per_forward(w.tokens)}
+
+    w = synthetic.WORKLOADS[args.workload]
+    main_step = Step(w, torch, fa)
+    others = [] if args.no_secondary else [Step(synthetic.WORKLOADS[n], torch, fa) for n in args.secondary]
     with ClockSampler(local) as clocks:
-        barrier()
         t0 = time.perf_counter()
-        for i in range(args.steps):
-            flush.zero_()
-            e0, e1, e2 = ev[i]
-            e0.record(stream)
-            attn.prologue(q, k, *geo, wq, wk, qn=qn, kn=kn)
-            e1.record(stream)
-            attn.attend(qn, kn, v, out=out)
-            e2.record(stream)
-        barrier()
+        times = slowest(list(measure(main_step, args.steps, args.warmup, torch, flush, barrier)))
         wall = time.perf_counter() - t0
-    status = attn.sync_status()
-    if status != 0:
-        raise RuntimeError("device status %d during the timed region" % status)
-    step_ms = sum(a.elapsed_time(c) for a, _, c in ev) / args.steps
-    attn_ms = sum(b.elapsed_time(c) for _, b, c in ev) / args.steps
-    pro_ms = sum(a.elapsed_time(b) for a, b, _ in ev) / args.steps
-    launches = args.steps * attn.launches_per_forward(w.tokens)
-
-    # slowest rank decides
-    t = torch.tensor([step_ms, attn_ms, pro_ms], dtype=torch.float64, device="cuda")
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    step_ms, attn_ms, pro_ms = t.tolist()
-
-    flops = w.flops
-    value = flops * world / (step_ms * 1e-3) / 1e12
-    achieved = flops / (attn_ms * 1e-3) / 1e12
-    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    pro_bytes = 4 * w.batch * w.tokens * w.heads * 128 * 2      # read q, k; write q', k'
-    traffic = ncu_traffic(w.name)
+        other_times = [slowest(list(measure(st, args.steps2, args.warmup, torch, flush, barrier)))
+                       for st in others]
+    main = summary(main_step, times, args.steps)
+    secondary = [summary(st, t, args.steps2) for st, t in zip(others, other_times)]
 
     # end to end through the public API: pinned host inputs in, result back out, every step
-    e2e = run_e2e(w, inp, attn, torch, args.e2e_steps, world, dist)
-
-    secondary = None
-    if not args.no_secondary:
-        attn2, step2, ev2, bufs2, geo2, _, _ = time_device(synthetic.WORKLOADS[SECONDARY], args.steps2,
-                                                           args.warmup, torch, fa, flush)
-        q2, k2, v2, wq2, wk2, out2, qn2, kn2 = bufs2
-        barrier()
-        for i in range(args.steps2):
-            flush.zero_()
-            e0, e1, e2 = ev2[i]
-            e0.record(stream)
-            attn2.prologue(q2, k2, *geo2, wq2, wk2, qn=qn2, kn=kn2)
-            e1.record(stream)
-            attn2.attend(qn2, kn2, v2, out=out2)
-            e2.record(stream)
-        barrier()
-        if attn2.sync_status() != 0:
-            raise RuntimeError("device status error (secondary)")
-        s_ms = sum(a.elapsed_time(c) for a, _, c in ev2) / args.steps2
-        a_ms = sum(b.elapsed_time(c) for _, b, c in ev2) / args.steps2
-        w2 = synthetic.WORKLOADS[SECONDARY]
-        secondary = {"workload": SECONDARY, "tokens": w2.tokens, "steps": args.steps2,
-                     "value": w2.flops / (s_ms * 1e-3) / 1e12, "ms_per_step": s_ms,
-                     "attn_kernel_ms": a_ms, "attn_tflops": w2.flops / (a_ms * 1e-3) / 1e12,
-                     "roofline_frac": w2.flops / (a_ms * 1e-3) / 1e12 / peak,
-                     "frac_of_2250_nominal": w2.flops / (a_ms * 1e-3) / 1e12 / 2250.0}
-        attn2.close()
-        secondary["gpu_launches"] = args.steps2 * 2
+    e2e = run_e2e(w, main_step.inp, main_step.attn, torch, args.e2e_steps, world, dist)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, inp, args.cpu_seconds)
+        cpu = cpu_baseline(w, main_step.inp, args.cpu_seconds)
 
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "metric": METRIC, "value": main["value"], "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": main["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, norm weights 1+0.1N(0,1))",
         "config": {"workload": w.name, "batch": w.batch, "heads": w.heads, "head_dim": 128,
                    "tokens": w.tokens, "txt_len": w.txt_len, "img": [w.img_h, w.img_w],
                    "global_batch": w.batch * world, "seq_len": w.tokens,
                    "parallelism": "replicas" if world > 1 else "single",
                    "l2": "flushed before every timed step (256 MB write, outside the step events)"},
-        "roofline": {"bound": "tensor", "kernel": "attn_bf16_kernel", "achieved": achieved, "peak": peak,
-                     "unit": "TFLOP/s", "frac": achieved / peak, "peak_kind": peak_kind + " bf16 burst",
-                     "frac_of_2250_nominal": achieved / 2250.0, "traffic": traffic,
-                     "algorithmic_flops_per_launch": flops},
-        "prologue": {"ms": pro_ms, "gbs": pro_bytes / (pro_ms * 1e-3) / 1e9, "hbm_peak_gbs": hbm,
-                     "frac": pro_bytes / (pro_ms * 1e-3) / 1e9 / hbm, "algorithmic_bytes": pro_bytes},
-        "attn_kernel_ms": attn_ms,
+        "roofline": {"bound": "tensor", "kernel": "attn_kernel<bf16>", "achieved": main["attn_tflops"],
+                     "peak": peak_bf16, "unit": "TFLOP/s", "frac": main["roofline_frac"],
+                     "peak_kind": peak_kind + " bf16 burst", "frac_of_2250_nominal": main["frac_of_nominal"],
+                     "traffic": ncu_traffic(w.name), "algorithmic_flops_per_launch": w.flops},
+        "prologue": {"ms": main["prologue_ms"], "gbs": main["prologue_gbs"], "hbm_peak_gbs": hbm,
+                     "frac": main["prologue_gbs"] / hbm, "algorithmic_bytes": main_step.prologue_bytes},
+        "attn_kernel_ms": main["attn_kernel_ms"],
         "e2e": e2e,
-        "gpu_launches": launches,
+        "gpu_launches": main["gpu_launches"],
         "clocks": clocks.summary(),
         "wall_s_timed_region": wall,
         "cpu_baseline": cpu,
         "secondary": secondary,
     }
-    attn.close()
+    for st in [main_step] + others:
+        st.attn.close()
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
@@ -427,11 +448,13 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=PRIMARY, choices=sorted(synthetic.WORKLOADS))
-    ap.add_argument("--steps2", type=int, default=60, help="timed steps of the secondary workload")
+    ap.add_argument("--steps2", type=int, default=60, help="timed steps of each secondary workload")
+    ap.add_argument("--secondary", nargs="*", default=SECONDARY, choices=sorted(synthetic.WORKLOADS),
+                    help="workloads measured after the primary one and reported under \"secondary\"")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--reference-rows", type=int, default=2048)

@@ -211,6 +211,11 @@ def flux_attn_last_error() -> str:
 
 # ---------------------------------------------------------------- wrapper
 
+def pad16(n: int) -> int:
+    """Row length of the transposed FP8 V: N rounded up to a multiple of 16."""
+    return (n + 15) // 16 * 16
+
+
 def _require(t, dtype, shape, name):
     import torch
     if not isinstance(t, torch.Tensor):
@@ -301,6 +306,46 @@ class FluxAttention:
         out = torch.empty_like(v) if out is None else out
         _require(out, torch.bfloat16, self._shape(n), "out")
         flux_attn_attend(self.handle, qn, kn, v, n, out, stream)
+        return out
+
+    def prologue_fp8(self, q, k, v, txt_len: int, img_h: int, img_w: int, ref_h: int = 0, ref_w: int = 0,
+                     q_norm_w=None, k_norm_w=None, pos_ids=None, q8=None, k8=None, v8t=None, scales=None,
+                     stream=None):
+        """FP8 handles: E4M3 codes q8, k8 [B, H, N, 128], v8t [B, H, 128, pad16(N)]
+        (uint8 tensors) and scales [B, H, 3] (fp32), into the given tensors or
+        new ones."""
+        import torch
+        n = txt_len + img_h * img_w + ref_h * ref_w
+        for t, name in ((q, "q"), (k, "k"), (v, "v")):
+            _require(t, torch.bfloat16, self._shape(n), name)
+        _require(q_norm_w, torch.float32, (HEAD_DIM,), "q_norm_w")
+        _require(k_norm_w, torch.float32, (HEAD_DIM,), "k_norm_w")
+        if pos_ids is not None:
+            _require(pos_ids, torch.int32, (n, 3), "pos_ids")
+        B, H = self.batch, self.num_heads
+        new = lambda shape, dt: torch.empty(shape, dtype=dt, device=q.device)
+        q8 = new((B, H, n, HEAD_DIM), torch.uint8) if q8 is None else q8
+        k8 = new((B, H, n, HEAD_DIM), torch.uint8) if k8 is None else k8
+        v8t = new((B, H, HEAD_DIM, pad16(n)), torch.uint8) if v8t is None else v8t
+        scales = new((B, H, 3), torch.float32) if scales is None else scales
+        _require(q8, torch.uint8, (B, H, n, HEAD_DIM), "q8")
+        _require(k8, torch.uint8, (B, H, n, HEAD_DIM), "k8")
+        _require(v8t, torch.uint8, (B, H, HEAD_DIM, pad16(n)), "v8t")
+        _require(scales, torch.float32, (B, H, 3), "scales")
+        flux_attn_prologue_fp8(self.handle, q, k, v, txt_len, img_h, img_w, ref_h, ref_w, pos_ids, q_norm_w,
+                               k_norm_w, q8, k8, v8t, scales, stream)
+        return q8, k8, v8t, scales
+
+    def attend_fp8(self, q8, k8, v8t, scales, out=None, stream=None):
+        import torch
+        B, H, n = self.batch, self.num_heads, q8.shape[2]
+        _require(q8, torch.uint8, (B, H, n, HEAD_DIM), "q8")
+        _require(k8, torch.uint8, (B, H, n, HEAD_DIM), "k8")
+        _require(v8t, torch.uint8, (B, H, HEAD_DIM, pad16(n)), "v8t")
+        _require(scales, torch.float32, (B, H, 3), "scales")
+        out = torch.empty((B, n, H, HEAD_DIM), dtype=torch.bfloat16, device=q8.device) if out is None else out
+        _require(out, torch.bfloat16, self._shape(n), "out")
+        flux_attn_attend_fp8(self.handle, q8, k8, v8t, scales, n, out, stream)
         return out
 
     def sync_status(self, stream=None) -> int:

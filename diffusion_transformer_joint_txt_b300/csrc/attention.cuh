@@ -1,30 +1,44 @@
-// attention_bf16.cuh -- joint (non-causal) flash attention on sm_103a tensor cores.
+// attention.cuh -- joint (non-causal) flash attention on sm_103a tensor cores,
+// BF16 and FP8 (E4M3) operands.
 //
 // Joint attention of "Speed up image generation with FLUX 3 Image Klein on
 // NVIDIA Blackwell GPUs" (section "FLUX 3 inference with TensorRT LLM
 // VisualGen"): every query token of [text | image | reference] attends to
 // every key token of the same (batch, head); no mask.  The page measures the
-// BF16 "VANILLA" attention at about 60 % of DiT kernel time (section
-// "Quantized and sparse attention"); this kernel is that BF16 step.
+// BF16 "VANILLA" attention at about 60 % of DiT kernel time and replaces it
+// with FP8 attention (Q.K and P.V in FP8) in section "Quantized and sparse
+// attention"; this kernel is that step in both precisions.
 //
 // One CTA = one 128-row query tile of one (b, h).  Warp roles:
 //   warps 0-3  softmax + epilogue, thread t owns query row t (TMEM lane t)
-//   warp 4     TMA producer: Q once, then K_j / V_j into 2-stage rings
+//   warp 4     TMA producer: Q once, then K_j / V_j into rings
 //   warp 5     TMEM allocator and single-thread tcgen05.mma issuer
 // TMEM (512 columns): S_0 at 0, S_1 at 128 (S_j double-buffered so that
 // S_{j+1} = Q K_{j+1}^T runs while the softmax works on S_j), O at 256.
-// The softmax overwrites S_j with P_j (bf16, two per 32-bit column) and the
-// P.V MMA reads its A operand straight from TMEM.
+// The softmax overwrites S_j with P_j and the P.V MMA reads its A operand
+// straight from TMEM.
 //
-// Shared-memory layout of a 128 x 128 bf16 tile: two 16 KB halves (head-dim
-// columns 0-63, 64-127), each 128 rows x 128 bytes with the 128-byte TMA
-// swizzle, which is the canonical SW128 layout the MMA descriptors describe
-// (K-major for Q and K; MN-major for V, whose head dim is the N of P.V).
+// BF16: operands are bf16 (kind::f16, K = 16 per MMA).  A 128 x 128 tile is
+// two 16 KB halves (head-dim columns 0-63, 64-127), each 128 rows x 128 bytes
+// with the 128-byte TMA swizzle -- the canonical SW128 layout the MMA
+// descriptors describe (K-major for Q and K; MN-major for V, read in place
+// from [B, N, H, 128]).  P is bf16, two per TMEM column.
+//
+// FP8: Q', K' are E4M3 codes [B, H, N, 128] and V is E4M3 transposed
+// [B, H, 128, Npad] (kind::f8f6f4, K = 32 per MMA).  A 128 x 128 tile is one
+// 16 KB SW128 block, K-major for all three (for V^T the keys are the K
+// dimension of P.V).  P is E4M3 of 256 p, four per TMEM column; the row sum
+// l adds the values the codes stand for, so that O = sum p~ v / sum p~ is a
+// convex combination of the V rows whatever the rounding of P.  Scores are
+// scaled by s_q s_k and the output by s_v (per-(b, h) scales).
 //
 // Every wait is bounded (ptx.cuh); a wait that runs out sets the CTA abort
 // flag and the error word, all roles stop issuing, drain what they issued,
 // free TMEM and return.
 #pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "ptx.cuh"
 
@@ -34,17 +48,25 @@ namespace attn {
 constexpr int BM = 128;  // query rows per tile
 constexpr int BN = 128;  // keys per tile
 constexpr int HD = 128;  // head dim
-constexpr int KST = 2;   // K ring stages
-constexpr int VST = 2;   // V ring stages
-constexpr uint32_t TILE = BM * HD * 2;  // 32 KB
-constexpr uint32_t HALF = TILE / 2;     // one 64-column swizzle block: 128 rows x 128 B
 constexpr int THREADS = 192;
 constexpr int WARP_TMA = 4;
 constexpr int WARP_MMA = 5;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O = 256;
+constexpr uint32_t HALF = BM * 128;  // one SW128 block: 128 rows x 128 bytes = 16 KB
 
+template <bool FP8>
+struct Traits {
+  static constexpr uint32_t TILE = FP8 ? HALF : 2 * HALF;  // bytes of one 128 x 128 operand tile
+  static constexpr int KST = FP8 ? 3 : 2;                  // K ring stages
+  static constexpr int VST = FP8 ? 3 : 2;                  // V ring stages
+};
+
+template <bool FP8>
 struct __align__(1024) Smem {
+  static constexpr uint32_t TILE = Traits<FP8>::TILE;
+  static constexpr int KST = Traits<FP8>::KST;
+  static constexpr int VST = Traits<FP8>::VST;
   uint8_t q[TILE];
   uint8_t k[KST][TILE];
   uint8_t v[VST][TILE];
@@ -58,13 +80,17 @@ struct __align__(1024) Smem {
   uint32_t tmem_base;
   int abort;
 };
-constexpr size_t SMEM_BYTES = sizeof(Smem) + 1024;  // + slack to align the base to 1024
+template <bool FP8>
+constexpr size_t smem_bytes() {
+  return sizeof(Smem<FP8>) + 1024;  // + slack to align the base to 1024
+}
 
 struct Params {
-  __nv_bfloat16* out;  // [B, N, H, 128]
+  __nv_bfloat16* out;    // [B, N, H, 128]
   uint32_t* err;
+  const float* scales;   // FP8: [B*H, 3] (s_q, s_k, s_v); BF16: unused
   int N, H, nkv;
-  float scale_log2;    // log2(e) / sqrt(128)
+  float scale_log2;      // log2(e) / sqrt(128)
   int debug;
 };
 
@@ -80,27 +106,43 @@ __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity, uint3
   }
 }
 
-__device__ __forceinline__ void producer(Smem& sm, const CUtensorMap* tq, const CUtensorMap* tk,
+// Load one 128-row operand tile (rows `row0..+127` of slice `bh`) of a
+// [.., rows, 128 elements] tensor map: two 64-column boxes for bf16, one
+// 128-byte box for E4M3.
+template <bool FP8>
+__device__ __forceinline__ void load_rows(uint32_t dst, const CUtensorMap* map, uint64_t* bar, int row0, int bh) {
+  tma_load_3d(dst, map, bar, 0, row0, bh);
+  if (!FP8) tma_load_3d(dst + HALF, map, bar, 64, row0, bh);
+}
+
+template <bool FP8>
+__device__ __forceinline__ void producer(Smem<FP8>& sm, const CUtensorMap* tq, const CUtensorMap* tk,
                                          const CUtensorMap* tv, int q0, int bh, int b, int h, int nkv,
                                          volatile int* ab, uint32_t* err) {
+  constexpr uint32_t TILE = Traits<FP8>::TILE;
+  constexpr int KST = Traits<FP8>::KST, VST = Traits<FP8>::VST;
   mbar_arrive_expect_tx(&sm.q_full, TILE);
-  tma_load_3d(smem_u32(sm.q), tq, &sm.q_full, 0, q0, bh);
-  tma_load_3d(smem_u32(sm.q) + HALF, tq, &sm.q_full, 64, q0, bh);
+  load_rows<FP8>(smem_u32(sm.q), tq, &sm.q_full, q0, bh);
   int k_issued = 0, v_issued = 0;
   for (int j = 0; j < nkv; ++j) {
     const int ks = j % KST;
     const uint32_t ku = j / KST;
     if (ku > 0 && !mbar_wait(&sm.k_empty[ks], (ku - 1) & 1, ab, err)) break;
     mbar_arrive_expect_tx(&sm.k_full[ks], TILE);
-    tma_load_3d(smem_u32(sm.k[ks]), tk, &sm.k_full[ks], 0, j * BN, bh);
-    tma_load_3d(smem_u32(sm.k[ks]) + HALF, tk, &sm.k_full[ks], 64, j * BN, bh);
+    load_rows<FP8>(smem_u32(sm.k[ks]), tk, &sm.k_full[ks], j * BN, bh);
     ++k_issued;
     const int vs = j % VST;
     const uint32_t vu = j / VST;
     if (vu > 0 && !mbar_wait(&sm.v_empty[vs], (vu - 1) & 1, ab, err)) break;
     mbar_arrive_expect_tx(&sm.v_full[vs], TILE);
-    tma_load_4d(smem_u32(sm.v[vs]), tv, &sm.v_full[vs], 0, h, j * BN, b);
-    tma_load_4d(smem_u32(sm.v[vs]) + HALF, tv, &sm.v_full[vs], 64, h, j * BN, b);
+    if (FP8) {
+      // V^T [B*H, 128, Npad]: keys j*128.. are the inner (x) coordinate.
+      tma_load_3d(smem_u32(sm.v[vs]), tv, &sm.v_full[vs], j * BN, 0, bh);
+    } else {
+      // V [B, N, H, 128] in place: box (64 dims, 1 head, 128 keys, 1 batch).
+      tma_load_4d(smem_u32(sm.v[vs]), tv, &sm.v_full[vs], 0, h, j * BN, b);
+      tma_load_4d(smem_u32(sm.v[vs]) + HALF, tv, &sm.v_full[vs], 64, h, j * BN, b);
+    }
     ++v_issued;
   }
   // Drain: the latest phase of every barrier a copy was issued on has completed.
@@ -115,36 +157,61 @@ __device__ __forceinline__ void producer(Smem& sm, const CUtensorMap* tq, const 
   }
 }
 
-// S = Q K^T: 8 MMAs of 128 x 128 x 16.  Step kk covers head dims 16kk..16kk+15:
-// half kk/4 of the tile, 32-byte offset (kk%4) inside the 128-byte swizzle row.
+// S = Q K^T over the 128 head dims.
+//   BF16: 8 MMAs of 128 x 128 x 16; step kk covers head dims 16kk..16kk+15:
+//         half kk/4 of the tile, 32-byte offset (kk%4) inside the swizzle row.
+//   FP8:  4 MMAs of 128 x 128 x 32; step kk is the 32-byte offset 32kk.
+template <bool FP8>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t qa, uint32_t ka) {
-  constexpr uint32_t ID = idesc_f16(BM, BN, false);
+  if (FP8) {
+    constexpr uint32_t ID = idesc_e4m3(BM, BN, false);
 #pragma unroll
-  for (int kk = 0; kk < HD / 16; ++kk) {
-    const uint32_t off = (kk >> 2) * HALF + (kk & 3) * 32;
-    mma_f16_ss(d_tmem, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), ID, kk > 0);
+    for (int kk = 0; kk < HD / 32; ++kk)
+      mma_e4m3_ss(d_tmem, sdesc_sw128(qa + kk * 32, 16, 1024), sdesc_sw128(ka + kk * 32, 16, 1024), ID, kk > 0);
+  } else {
+    constexpr uint32_t ID = idesc_f16(BM, BN, false);
+#pragma unroll
+    for (int kk = 0; kk < HD / 16; ++kk) {
+      const uint32_t off = (kk >> 2) * HALF + (kk & 3) * 32;
+      mma_f16_ss(d_tmem, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), ID, kk > 0);
+    }
   }
 }
 
-// O (+)= P V: 8 MMAs of 128 x 128 x 16.  Step kk covers keys 16kk..16kk+15:
-// P columns 8kk.. (two bf16 per column), V rows 16kk.. (16 rows x 128 B = 2 KB);
-// V is MN-major: LBO = next 64 head-dim columns (the other half), SBO = next 8 keys.
+// O (+)= P V over the 128 keys of a tile.
+//   BF16: 8 MMAs of 128 x 128 x 16; step kk covers keys 16kk..16kk+15: P
+//         columns 8kk.. (two bf16 per column), V rows 16kk.. (16 rows x 128 B
+//         = 2 KB); V is MN-major: LBO = the other 64 head dims (the other
+//         half), SBO = next 8 keys.
+//   FP8:  4 MMAs of 128 x 128 x 32; step kk covers keys 32kk..: P columns
+//         8kk.. (four E4M3 per column), V^T K-major at byte offset 32kk.
+template <bool FP8>
 __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t va, bool accumulate) {
-  constexpr uint32_t ID = idesc_f16(BM, HD, true);
+  if (FP8) {
+    constexpr uint32_t ID = idesc_e4m3(BM, HD, false);
 #pragma unroll
-  for (int kk = 0; kk < BN / 16; ++kk) {
-    mma_f16_ts(o_tmem, p_tmem + kk * 8, sdesc_sw128(va + kk * 2048, HALF, 1024), ID,
-               (accumulate || kk > 0) ? 1u : 0u);
+    for (int kk = 0; kk < BN / 32; ++kk)
+      mma_e4m3_ts(o_tmem, p_tmem + kk * 8, sdesc_sw128(va + kk * 32, 16, 1024), ID,
+                  (accumulate || kk > 0) ? 1u : 0u);
+  } else {
+    constexpr uint32_t ID = idesc_f16(BM, HD, true);
+#pragma unroll
+    for (int kk = 0; kk < BN / 16; ++kk)
+      mma_f16_ts(o_tmem, p_tmem + kk * 8, sdesc_sw128(va + kk * 2048, HALF, 1024), ID,
+                 (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
-__device__ __forceinline__ void mma_issuer(Smem& sm, uint32_t tmem, int nkv, volatile int* ab, uint32_t* err) {
+template <bool FP8>
+__device__ __forceinline__ void mma_issuer(Smem<FP8>& sm, uint32_t tmem, int nkv, volatile int* ab,
+                                           uint32_t* err) {
+  constexpr int KST = Traits<FP8>::KST, VST = Traits<FP8>::VST;
   const uint32_t qa = smem_u32(sm.q);
   do {
     if (!mbar_wait(&sm.q_full, 0, ab, err)) break;
     if (!mbar_wait(&sm.k_full[0], 0, ab, err)) break;
     tc_fence_after_sync();
-    issue_qk(tmem + COL_S0, qa, smem_u32(sm.k[0]));
+    issue_qk<FP8>(tmem + COL_S0, qa, smem_u32(sm.k[0]));
     mma_commit(&sm.s_full[0]);
     mma_commit(&sm.k_empty[0]);
     for (int j = 0; j < nkv; ++j) {
@@ -154,7 +221,7 @@ __device__ __forceinline__ void mma_issuer(Smem& sm, uint32_t tmem, int nkv, vol
         if (!mbar_wait(&sm.k_full[ks], (jn / KST) & 1, ab, err)) break;
         tc_fence_after_sync();
         // S buffer jn&1 last held P_{j-1}, whose P.V MMA was issued before this one.
-        issue_qk(tmem + ((jn & 1) ? COL_S1 : COL_S0), qa, smem_u32(sm.k[ks]));
+        issue_qk<FP8>(tmem + ((jn & 1) ? COL_S1 : COL_S0), qa, smem_u32(sm.k[ks]));
         mma_commit(&sm.s_full[jn & 1]);
         mma_commit(&sm.k_empty[ks]);
       }
@@ -162,7 +229,7 @@ __device__ __forceinline__ void mma_issuer(Smem& sm, uint32_t tmem, int nkv, vol
       const int vs = j % VST;
       if (!mbar_wait(&sm.v_full[vs], (j / VST) & 1, ab, err)) break;
       tc_fence_after_sync();
-      issue_pv(tmem + COL_O, tmem + ((j & 1) ? COL_S1 : COL_S0), smem_u32(sm.v[vs]), j > 0);
+      issue_pv<FP8>(tmem + COL_O, tmem + ((j & 1) ? COL_S1 : COL_S0), smem_u32(sm.v[vs]), j > 0);
       mma_commit(&sm.o_done);
       mma_commit(&sm.v_empty[vs]);
     }
@@ -172,14 +239,41 @@ __device__ __forceinline__ void mma_issuer(Smem& sm, uint32_t tmem, int nkv, vol
   mbar_drain(&sm.mma_drain, 0, err);
 }
 
-__device__ __forceinline__ void softmax_epilogue(Smem& sm, uint32_t tmem, const Params& prm, int b, int h,
+// Four E4M3 codes (round to nearest even, saturating) in one word, a in the
+// lowest byte: the K order of an 8-bit A operand in a TMEM column.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+  return lo | (hi << 16);
+}
+
+// Sum of the values the four E4M3 codes of a word stand for (exact in fp16).
+__device__ __forceinline__ float sum_e4m3x4(uint32_t w) {
+  const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w & 0xFFFFu), __NV_E4M3);
+  const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w >> 16), __NV_E4M3);
+  const float2 a = __half22float2(__half2(lo));
+  const float2 c = __half22float2(__half2(hi));
+  return (a.x + a.y) + (c.x + c.y);
+}
+
+template <bool FP8>
+__device__ __forceinline__ void softmax_epilogue(Smem<FP8>& sm, uint32_t tmem, const Params& prm, int b, int h,
                                                  int q0, volatile int* ab) {
   const int t = threadIdx.x;  // 0..127
   const int warp = t >> 5;
   const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
   const int N = prm.N;
   const int nkv = prm.nkv;
-  const float sl2 = prm.scale_log2;
+  float sl2 = prm.scale_log2;
+  float out_scale = 1.f;
+  if (FP8) {
+    const float* sc = prm.scales + 3 * (static_cast<size_t>(b) * prm.H + h);
+    sl2 *= __ldg(sc) * __ldg(sc + 1);
+    out_scale = __ldg(sc + 2);
+  }
+  // FP8 stores P as E4M3 of 256 p: the 2^8 factor is folded into the exponent
+  // and cancels against l, which sums the same scaled values.
+  constexpr float kPBias = FP8 ? 8.f : 0.f;
   float m = -INFINITY;  // running max, in log2 units
   float l = 0.f;        // running row sum
   bool ok = true;
@@ -208,17 +302,27 @@ __device__ __forceinline__ void softmax_epilogue(Smem& sm, uint32_t tmem, const 
     for (int i = 1; i < BN; ++i) mx = fmaxf(mx, s[i]);
     const float m_new = fmaxf(m, mx * sl2);
     const float alpha = ex2_approx(m - m_new);  // 0 on the first tile
+    const float nm = kPBias - m_new;
     float rs = 0.f;
-    uint32_t pk[BN / 2];
+    if (FP8) {
+      uint32_t pk[32];
 #pragma unroll
-    for (int i = 0; i < BN / 2; ++i) {
-      const float p0 = ex2_approx(fmaf(s[2 * i], sl2, -m_new));
-      const float p1 = ex2_approx(fmaf(s[2 * i + 1], sl2, -m_new));
-      rs += p0 + p1;
-      pk[i] = pack_bf16x2(p0, p1);
-    }
-    l = l * alpha + rs;
-    {
+      for (int i = 0; i < 32; ++i) {
+        pk[i] = pack_e4m3x4(ex2_approx(fmaf(s[4 * i], sl2, nm)), ex2_approx(fmaf(s[4 * i + 1], sl2, nm)),
+                            ex2_approx(fmaf(s[4 * i + 2], sl2, nm)), ex2_approx(fmaf(s[4 * i + 3], sl2, nm)));
+        rs += sum_e4m3x4(pk[i]);
+      }
+      tmem_st32(tmem + lane_base + scol, pk);
+      tmem_st_wait();
+    } else {
+      uint32_t pk[BN / 2];
+#pragma unroll
+      for (int i = 0; i < BN / 2; ++i) {
+        const float p0 = ex2_approx(fmaf(s[2 * i], sl2, nm));
+        const float p1 = ex2_approx(fmaf(s[2 * i + 1], sl2, nm));
+        rs += p0 + p1;
+        pk[i] = pack_bf16x2(p0, p1);
+      }
       uint32_t r0[32], r1[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) { r0[i] = pk[i]; r1[i] = pk[32 + i]; }
@@ -226,6 +330,7 @@ __device__ __forceinline__ void softmax_epilogue(Smem& sm, uint32_t tmem, const 
       tmem_st32(tmem + lane_base + scol + 32, r1);
       tmem_st_wait();
     }
+    l = l * alpha + rs;
     // Every phase of o_done is confirmed in order (a parity wait is only exact
     // when the barrier is at most one phase away), then O is rescaled where
     // the running max moved.  P.V of tile j-1 has landed at this point.
@@ -256,7 +361,7 @@ __device__ __forceinline__ void softmax_epilogue(Smem& sm, uint32_t tmem, const 
   }
   if (!ok) return;
   tc_fence_after_sync();
-  const float inv_l = 1.f / l;
+  const float inv_l = out_scale / l;
   const int row = q0 + t;
   __nv_bfloat16* dst = prm.out + ((static_cast<size_t>(b) * N + row) * prm.H + h) * HD;
 #pragma unroll
@@ -276,11 +381,14 @@ __device__ __forceinline__ void softmax_epilogue(Smem& sm, uint32_t tmem, const 
   }
 }
 
+template <bool FP8>
 __global__ void __launch_bounds__(THREADS, 1)
-    attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_v, const Params prm) {
+    attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const Params prm) {
+  constexpr int KST = Traits<FP8>::KST, VST = Traits<FP8>::VST;
   extern __shared__ uint8_t smem_raw[];
-  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Smem<FP8>& sm =
+      *reinterpret_cast<Smem<FP8>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int bh = blockIdx.y;
@@ -320,13 +428,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 
   if (warp == WARP_TMA) {
-    if (lane == 0 && !*ab) producer(sm, &tm_q, &tm_k, &tm_v, q0, bh, b, h, prm.nkv, ab, prm.err);
+    if (lane == 0 && !*ab) producer<FP8>(sm, &tm_q, &tm_k, &tm_v, q0, bh, b, h, prm.nkv, ab, prm.err);
     __syncwarp();
   } else if (warp == WARP_MMA) {
-    if (lane == 0 && !*ab) mma_issuer(sm, tmem, prm.nkv, ab, prm.err);
+    if (lane == 0 && !*ab) mma_issuer<FP8>(sm, tmem, prm.nkv, ab, prm.err);
     __syncwarp();
   } else {
-    if (!*ab) softmax_epilogue(sm, tmem, prm, b, h, q0, ab);
+    if (!*ab) softmax_epilogue<FP8>(sm, tmem, prm, b, h, q0, ab);
   }
   tc_fence_before_sync();
   __syncthreads();

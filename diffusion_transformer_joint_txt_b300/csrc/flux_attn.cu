@@ -3,7 +3,7 @@
 //
 // Host side only: argument checks, workspace, TMA tensor maps and launches.
 // The arithmetic of the path runs in the kernels of prologue.cuh,
-// attention_bf16.cuh and attention_fp8.cuh.
+// quantize_fp8.cuh and attention.cuh.
 #include <cudaTypedefs.h>
 
 #include <cmath>
@@ -14,8 +14,9 @@
 #include <string>
 
 #include "flux_attn.h"
-#include "attention_bf16.cuh"
+#include "attention.cuh"
 #include "prologue.cuh"
+#include "quantize_fp8.cuh"
 
 struct flux_attn {
   flux_attn_config cfg;
@@ -23,8 +24,13 @@ struct flux_attn {
   int num_sms;
   size_t ws_bytes;
   void* ws;               // one allocation, carved below
-  __nv_bfloat16* qn;      // [B, H, max_tokens, 128]
-  __nv_bfloat16* kn;      // [B, H, max_tokens, 128]
+  __nv_bfloat16* qn;      // BF16: [B, H, max_tokens, 128]
+  __nv_bfloat16* kn;      // BF16: [B, H, max_tokens, 128]
+  uint8_t* q8;            // FP8: E4M3 [B, H, max_tokens, 128]
+  uint8_t* k8;            // FP8: E4M3 [B, H, max_tokens, 128]
+  uint8_t* v8t;           // FP8: E4M3 [B, H, 128, pad16(max_tokens)]
+  uint32_t* amax;         // FP8: [B, H, 3] fp32 bits
+  float* scales;          // FP8: [B, H, 3]
   uint32_t* err;          // device error word
   flux::RopeTable rope;
 };
@@ -152,43 +158,95 @@ int launch_prologue(flux_attn* h, const void* q, const void* k, int txt, int ih,
   return FLUX_ATTN_OK;
 }
 
-int launch_attention_bf16(flux_attn* h, const void* qn, const void* kn, const void* v, int n, void* out,
-                          cudaStream_t stream) {
+size_t pad16(int n) { return (static_cast<size_t>(n) + 15) & ~size_t(15); }
+
+// The two FP8 prologue passes: amax (after zeroing it), then the E4M3 codes
+// of Q', K' and of V transposed, and the scales.
+int launch_prologue_fp8(flux_attn* h, const void* q, const void* k, const void* v, int txt, int ih, int iw,
+                        int rw, const int32_t* pos, const float* wq, const float* wk, int n, uint8_t* q8,
+                        uint8_t* k8, uint8_t* v8t, float* scales, cudaStream_t stream) {
+  flux::TokenGeometry geo{pos, txt, ih * iw, iw, rw};
+  const int B = h->cfg.batch, H = h->cfg.num_heads;
+  const size_t amax_bytes = static_cast<size_t>(B) * H * 3 * sizeof(uint32_t);
+  cudaError_t e = cudaMemsetAsync(h->amax, 0, amax_bytes, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing amax");
+  const dim3 grid((n + flux::kQuantTokens - 1) / flux::kQuantTokens, B);
+  const auto* qb = static_cast<const __nv_bfloat16*>(q);
+  const auto* kb = static_cast<const __nv_bfloat16*>(k);
+  const auto* vb = static_cast<const __nv_bfloat16*>(v);
+  flux::fp8_amax_kernel<<<grid, flux::kQuantThreads, 3 * H * sizeof(uint32_t), stream>>>(
+      qb, kb, vb, wq, wk, geo, n, H, h->cfg.rms_eps, h->rope, h->amax);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "amax launch");
+  flux::fp8_quant_kernel<<<grid, flux::kQuantThreads, 0, stream>>>(qb, kb, vb, wq, wk, geo, n,
+                                                                    static_cast<int>(pad16(n)), H, h->cfg.rms_eps,
+                                                                    h->rope, h->amax, q8, k8, v8t, scales);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "quantise launch");
+  return FLUX_ATTN_OK;
+}
+
+// The attention kernel.  BF16: qn, kn bf16 [B*H, n, 128], v bf16 [B, n, H, 128].
+// FP8: qn, kn E4M3 [B*H, n, 128], v E4M3 V^T [B*H, 128, pad16(n)], scales [B*H, 3].
+int launch_attention(flux_attn* h, bool fp8, const void* qn, const void* kn, const void* v, const float* scales,
+                     int n, void* out, cudaStream_t stream) {
   using namespace flux::attn;
   const int B = h->cfg.batch, H = h->cfg.num_heads;
+  const size_t esz = fp8 ? 1 : 2;
+  const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUtensorMap tq, tk, tv;
   {
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(HD), static_cast<cuuint64_t>(n),
                                 static_cast<cuuint64_t>(B) * H};
-    const cuuint64_t strides[2] = {HD * 2ull, static_cast<cuuint64_t>(n) * HD * 2ull};
-    const cuuint32_t box[3] = {64, BM, 1};
-    int rc = encode_tiled(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, qn, dims, strides, box, "Q'");
+    const cuuint64_t strides[2] = {HD * esz, static_cast<cuuint64_t>(n) * HD * esz};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / esz), BM, 1};  // one 128-byte swizzle row
+    int rc = encode_tiled(&tq, dt, 3, qn, dims, strides, box, "Q'");
     if (rc) return rc;
-    rc = encode_tiled(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, kn, dims, strides, box, "K'");
+    rc = encode_tiled(&tk, dt, 3, kn, dims, strides, box, "K'");
     if (rc) return rc;
   }
-  {
+  if (fp8) {
+    const cuuint64_t np = pad16(n);
+    const cuuint64_t dims[3] = {np, static_cast<cuuint64_t>(HD), static_cast<cuuint64_t>(B) * H};
+    const cuuint64_t strides[2] = {np, np * HD};
+    const cuuint32_t box[3] = {BN, HD, 1};
+    int rc = encode_tiled(&tv, dt, 3, v, dims, strides, box, "V^T");
+    if (rc) return rc;
+  } else {
     const cuuint64_t dims[4] = {static_cast<cuuint64_t>(HD), static_cast<cuuint64_t>(H),
                                 static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(B)};
     const cuuint64_t strides[3] = {HD * 2ull, static_cast<cuuint64_t>(H) * HD * 2ull,
                                    static_cast<cuuint64_t>(n) * H * HD * 2ull};
     const cuuint32_t box[4] = {64, 1, BN, 1};
-    int rc = encode_tiled(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, v, dims, strides, box, "V");
+    int rc = encode_tiled(&tv, dt, 4, v, dims, strides, box, "V");
     if (rc) return rc;
   }
   Params prm;
   prm.out = static_cast<__nv_bfloat16*>(out);
   prm.err = h->err;
+  prm.scales = scales;
   prm.N = n;
   prm.H = H;
   prm.nkv = (n + BN - 1) / BN;
   prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(HD)));
   prm.debug = h->cfg.debug_flags;
   const dim3 grid((n + BM - 1) / BM, B * H);
-  attn_bf16_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(tq, tk, tv, prm);
+  if (fp8)
+    attn_kernel<true><<<grid, THREADS, smem_bytes<true>(), stream>>>(tq, tk, tv, prm);
+  else
+    attn_kernel<false><<<grid, THREADS, smem_bytes<false>(), stream>>>(tq, tk, tv, prm);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   return FLUX_ATTN_OK;
+}
+
+// Raise the dynamic shared-memory limit of both attention kernels (per device).
+cudaError_t set_attention_smem_limits() {
+  cudaError_t e = cudaFuncSetAttribute(flux::attn::attn_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(flux::attn::smem_bytes<false>()));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(flux::attn::attn_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(flux::attn::smem_bytes<true>()));
 }
 
 }  // namespace
@@ -233,8 +291,6 @@ int flux_attn_create(const flux_attn_config* cfg, flux_attn_t* out) {
     return fail(FLUX_ATTN_ERR_INVALID_ARG, "rope_theta must be > 0 and rms_eps >= 0");
   if (cfg->precision != FLUX_ATTN_BF16 && cfg->precision != FLUX_ATTN_FP8_E4M3)
     return fail(FLUX_ATTN_ERR_INVALID_ARG, "unknown precision %d", cfg->precision);
-  if (cfg->precision == FLUX_ATTN_FP8_E4M3)
-    return fail(FLUX_ATTN_ERR_UNSUPPORTED, "the FP8 E4M3 path is not built in this version");
 
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -247,8 +303,7 @@ int flux_attn_create(const flux_attn_config* cfg, flux_attn_t* out) {
                 prop.major, prop.minor);
   if (driver().encode == nullptr || driver().ptr_attr == nullptr)
     return fail(FLUX_ATTN_ERR_CUDA, "driver entry points unavailable");
-  e = cudaFuncSetAttribute(flux::attn::attn_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(flux::attn::SMEM_BYTES));
+  e = set_attention_smem_limits();
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
 
   flux_attn* h = new flux_attn();
@@ -264,8 +319,18 @@ int flux_attn_create(const flux_attn_config* cfg, flux_attn_t* out) {
         h->rope.axis[j] = a;
       }
   }
-  const size_t qk_bytes = static_cast<size_t>(cfg->batch) * cfg->num_heads * cfg->max_tokens * flux::kHeadDim * 2;
-  const size_t err_off = 2 * qk_bytes;
+  // Workspace, each piece 256-byte aligned:
+  //   BF16  Q', K' bf16 [B, H, max_tokens, 128]
+  //   FP8   Q', K' E4M3 [B, H, max_tokens, 128], V^T E4M3 [B, H, 128, pad16(max_tokens)],
+  //         amax and scales [B, H, 3]
+  //   both  the device error word
+  const size_t bh = static_cast<size_t>(cfg->batch) * cfg->num_heads;
+  const bool fp8 = cfg->precision == FLUX_ATTN_FP8_E4M3;
+  const auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+  const size_t qk_bytes = al(bh * cfg->max_tokens * flux::kHeadDim * (fp8 ? 1 : 2));
+  const size_t vt_bytes = fp8 ? al(bh * flux::kHeadDim * pad16(cfg->max_tokens)) : 0;
+  const size_t sc_bytes = fp8 ? al(bh * 3 * sizeof(float)) : 0;
+  const size_t err_off = 2 * qk_bytes + vt_bytes + 2 * sc_bytes;
   h->ws_bytes = err_off + 256;
   e = cudaMalloc(&h->ws, h->ws_bytes);
   if (e != cudaSuccess) {
@@ -274,9 +339,18 @@ int flux_attn_create(const flux_attn_config* cfg, flux_attn_t* out) {
     cudaGetLastError();
     return fail(FLUX_ATTN_ERR_OOM, "cudaMalloc(%zu) failed: %s", want, cudaGetErrorString(e));
   }
-  h->qn = reinterpret_cast<__nv_bfloat16*>(h->ws);
-  h->kn = reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(h->ws) + qk_bytes);
-  h->err = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(h->ws) + err_off);
+  uint8_t* base = static_cast<uint8_t*>(h->ws);
+  if (fp8) {
+    h->q8 = base;
+    h->k8 = base + qk_bytes;
+    h->v8t = base + 2 * qk_bytes;
+    h->amax = reinterpret_cast<uint32_t*>(base + 2 * qk_bytes + vt_bytes);
+    h->scales = reinterpret_cast<float*>(base + 2 * qk_bytes + vt_bytes + sc_bytes);
+  } else {
+    h->qn = reinterpret_cast<__nv_bfloat16*>(base);
+    h->kn = reinterpret_cast<__nv_bfloat16*>(base + qk_bytes);
+  }
+  h->err = reinterpret_cast<uint32_t*>(base + err_off);
   e = cudaMemset(h->err, 0, 256);
   if (e != cudaSuccess) {
     cudaFree(h->ws);
@@ -303,7 +377,9 @@ size_t flux_attn_workspace_bytes(flux_attn_t h) { return h ? h->ws_bytes : 0; }
 
 int flux_attn_launches_per_forward(flux_attn_t h, int n_tokens) {
   if (h == nullptr || n_tokens <= 0) return 0;
-  return 2;
+  // BF16: prologue + attention; FP8: amax + quantise + attention (the amax
+  // zeroing is a cudaMemsetAsync, not a kernel of this library).
+  return h->cfg.precision == FLUX_ATTN_FP8_E4M3 ? 3 : 2;
 }
 
 static int check_common(flux_attn* h, const void* q, const void* k, int txt, int ih, int iw, int rh, int rw,
@@ -355,7 +431,7 @@ int flux_attn_attend(flux_attn_t h, const void* qn, const void* kn, const void* 
   if ((rc = check_buffer(kn, bytes, "kn"))) return rc;
   if ((rc = check_buffer(v, bytes, "v"))) return rc;
   if ((rc = check_buffer(out, bytes, "out"))) return rc;
-  return launch_attention_bf16(h, qn, kn, v, n_tokens, out, stream);
+  return launch_attention(h, false, qn, kn, v, nullptr, n_tokens, out, stream);
 }
 
 int flux_attn_forward(flux_attn_t h, const void* q, const void* k, const void* v, int txt_len, int img_h,
@@ -373,24 +449,53 @@ int flux_attn_forward(flux_attn_t h, const void* q, const void* k, const void* v
     rc = launch_prologue(h, q, k, txt_len, img_h, img_w, ref_h, ref_w, pos_ids, q_norm_w, k_norm_w, h->qn, h->kn,
                          n, stream);
     if (rc) return rc;
-    return launch_attention_bf16(h, h->qn, h->kn, v, n, out, stream);
+    return launch_attention(h, false, h->qn, h->kn, v, nullptr, n, out, stream);
   }
-  return fail(FLUX_ATTN_ERR_UNSUPPORTED, "the FP8 E4M3 path is not built in this version");
+  rc = launch_prologue_fp8(h, q, k, v, txt_len, img_h, img_w, ref_w, pos_ids, q_norm_w, k_norm_w, n, h->q8, h->k8,
+                           h->v8t, h->scales, stream);
+  if (rc) return rc;
+  return launch_attention(h, true, h->q8, h->k8, h->v8t, h->scales, n, out, stream);
 }
 
 int flux_attn_prologue_fp8(flux_attn_t h, const void* q, const void* k, const void* v, int txt_len, int img_h,
                            int img_w, int ref_h, int ref_w, const int32_t* pos_ids, const float* q_norm_w,
                            const float* k_norm_w, void* q8, void* k8, void* v8t, float* scales,
                            cudaStream_t stream) {
-  (void)h; (void)q; (void)k; (void)v; (void)txt_len; (void)img_h; (void)img_w; (void)ref_h; (void)ref_w;
-  (void)pos_ids; (void)q_norm_w; (void)k_norm_w; (void)q8; (void)k8; (void)v8t; (void)scales; (void)stream;
-  return fail(FLUX_ATTN_ERR_UNSUPPORTED, "the FP8 E4M3 path is not built in this version");
+  g_last_error.clear();
+  int n = 0;
+  int rc = check_common(h, q, k, txt_len, img_h, img_w, ref_h, ref_w, pos_ids, q_norm_w, k_norm_w, &n);
+  if (rc || n == 0) return rc;
+  if (h->cfg.precision != FLUX_ATTN_FP8_E4M3)
+    return fail(FLUX_ATTN_ERR_INVALID_ARG, "flux_attn_prologue_fp8 needs an FP8 handle");
+  const size_t bh = static_cast<size_t>(h->cfg.batch) * h->cfg.num_heads;
+  if ((rc = check_buffer(v, row_bytes(h, n), "v"))) return rc;
+  if ((rc = check_buffer(q8, bh * n * flux::kHeadDim, "q8"))) return rc;
+  if ((rc = check_buffer(k8, bh * n * flux::kHeadDim, "k8"))) return rc;
+  if ((rc = check_buffer(v8t, bh * flux::kHeadDim * pad16(n), "v8t"))) return rc;
+  if ((rc = check_buffer(scales, bh * 3 * sizeof(float), "scales"))) return rc;
+  return launch_prologue_fp8(h, q, k, v, txt_len, img_h, img_w, ref_w, pos_ids, q_norm_w, k_norm_w, n,
+                             static_cast<uint8_t*>(q8), static_cast<uint8_t*>(k8), static_cast<uint8_t*>(v8t),
+                             scales, stream);
 }
 
 int flux_attn_attend_fp8(flux_attn_t h, const void* q8, const void* k8, const void* v8t, const float* scales,
                          int n_tokens, void* out, cudaStream_t stream) {
-  (void)h; (void)q8; (void)k8; (void)v8t; (void)scales; (void)n_tokens; (void)out; (void)stream;
-  return fail(FLUX_ATTN_ERR_UNSUPPORTED, "the FP8 E4M3 path is not built in this version");
+  g_last_error.clear();
+  int rc = check_handle(h);
+  if (rc) return rc;
+  if (h->cfg.precision != FLUX_ATTN_FP8_E4M3)
+    return fail(FLUX_ATTN_ERR_INVALID_ARG, "flux_attn_attend_fp8 needs an FP8 handle");
+  if (n_tokens < 0 || n_tokens > h->cfg.max_tokens)
+    return fail(FLUX_ATTN_ERR_INVALID_ARG, "n_tokens = %d outside [0, max_tokens = %d]", n_tokens,
+                h->cfg.max_tokens);
+  if (n_tokens == 0) return FLUX_ATTN_OK;
+  const size_t bh = static_cast<size_t>(h->cfg.batch) * h->cfg.num_heads;
+  if ((rc = check_buffer(q8, bh * n_tokens * flux::kHeadDim, "q8"))) return rc;
+  if ((rc = check_buffer(k8, bh * n_tokens * flux::kHeadDim, "k8"))) return rc;
+  if ((rc = check_buffer(v8t, bh * flux::kHeadDim * pad16(n_tokens), "v8t"))) return rc;
+  if ((rc = check_buffer(scales, bh * 3 * sizeof(float), "scales"))) return rc;
+  if ((rc = check_buffer(out, row_bytes(h, n_tokens), "out"))) return rc;
+  return launch_attention(h, true, q8, k8, v8t, scales, n_tokens, out, stream);
 }
 
 int flux_attn_sync_status(flux_attn_t h, cudaStream_t stream) {
@@ -457,8 +562,7 @@ int noalloc_setup(int dev, uint8_t** base) {
       d.msg = std::string("cudaGetSymbolAddress(scratch): ") + cudaGetErrorString(e);
       return;
     }
-    e = cudaFuncSetAttribute(flux::attn::attn_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(flux::attn::SMEM_BYTES));
+    e = set_attention_smem_limits();
     if (e != cudaSuccess) {
       d.msg = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
       return;
@@ -507,7 +611,7 @@ extern "C" int flux_attn_forward_noalloc(const flux_attn_config* cfg, const void
                 minor);
 
   // A handle-shaped view of this call; nothing in it is allocated.
-  flux_attn view;
+  flux_attn view{};
   view.cfg = *cfg;
   view.device = dev;
   view.num_sms = 0;
@@ -549,7 +653,7 @@ extern "C" int flux_attn_forward_noalloc(const flux_attn_config* cfg, const void
   rc = launch_prologue(&view, q, k, txt_len, img_h, img_w, ref_h, ref_w, pos_ids, q_norm_w, k_norm_w, view.qn,
                        view.kn, n, stream);
   if (rc) return rc;
-  rc = launch_attention_bf16(&view, view.qn, view.kn, v, n, out, stream);
+  rc = launch_attention(&view, false, view.qn, view.kn, v, nullptr, n, out, stream);
   if (rc) return rc;
   if (device_error != nullptr) {
     e = cudaMemcpyAsync(device_error, view.err, sizeof(uint32_t), cudaMemcpyDeviceToDevice, stream);

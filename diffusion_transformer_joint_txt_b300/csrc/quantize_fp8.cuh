@@ -1,0 +1,227 @@
+// quantize_fp8.cuh -- FP8 (E4M3) prologue: per-(batch, head) amax of the
+// normalised, rotated Q', K' and of V, then E4M3 codes of x / scale with
+// scale = amax / 448 (1 when amax == 0).
+//
+// "Speed up image generation with FLUX 3 Image Klein on NVIDIA Blackwell
+// GPUs", section "Quantized and sparse attention": the FP8 attention runs Q.K
+// and P.V with FP8 Q, K and V (qk_dtype fp8, v_dtype fp8); the quantisation
+// comes after the query/key normalisation and RoPE of section "GEMM kernel
+// optimisation".  Scales are per (batch, head) and per tensor.
+//
+// Two passes over q, k, v (bf16 [B, N, H, 128]):
+//   fp8_amax_kernel   recomputes Q', K' in fp32 (the same norm + rotation as
+//                     qk_norm_rope_kernel) and reduces |Q'|, |K'|, |V| per
+//                     (b, h) into amax[B*H][3] (fp32 bit patterns; positive
+//                     floats order like their bits, so atomicMax on the
+//                     bits is a float max).  amax must be zero on entry.
+//   fp8_quant_kernel  recomputes Q', K', scales and writes
+//                       q8, k8   E4M3 [B, H, N, 128]
+//                       v8t      E4M3 [B, H, 128, Npad]  (V transposed, keys
+//                                contiguous; columns N..Npad-1 zero)
+//                       scales   fp32 [B, H, 3] = (s_q, s_k, s_v)
+// Both take one block of 256 threads per 64 consecutive tokens of one batch
+// row; inside it a warp handles one token at a time (a half-warp per head
+// row, 8 elements per lane, as in the BF16 prologue).
+#pragma once
+
+#include <cuda_fp8.h>
+
+#include "prologue.cuh"
+
+namespace flux {
+
+constexpr int kQuantTokens = 64;     // tokens per block
+constexpr int kQuantThreads = 256;   // 8 warps
+constexpr float kE4M3Max = 448.f;
+
+// Rotation angles of the four pairs a lane owns (pairs 4 sub .. 4 sub + 3).
+__device__ __forceinline__ void lane_rotation(const TokenGeometry& geo, const RopeTable& tab, int n, int sub,
+                                              float (&c)[4], float (&s)[4]) {
+  int p[3];
+  token_position(geo, n, p);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int j = sub * 4 + i;
+    sincosf(static_cast<float>(p[tab.axis[j]]) * tab.freq[j], &s[i], &c[i]);
+  }
+}
+
+__device__ __forceinline__ void load_weights8(const float* w, int sub, float (&o)[8]) {
+  const float4* a = reinterpret_cast<const float4*>(w + sub * 8);
+  const float4 a0 = __ldg(a), a1 = __ldg(a + 1);
+  o[0] = a0.x; o[1] = a0.y; o[2] = a0.z; o[3] = a0.w;
+  o[4] = a1.x; o[5] = a1.y; o[6] = a1.z; o[7] = a1.w;
+}
+
+__device__ __forceinline__ float absmax8(const float (&x)[8]) {
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(x[i]));
+  return m;
+}
+
+// Max over the 16 lanes of a half-warp.
+__device__ __forceinline__ float half_warp_max(float v) {
+#pragma unroll
+  for (int off = 8; off >= 1; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, off));
+  return v;
+}
+
+// 1 / scale with scale = amax / 448, or 1 when amax == 0.
+__device__ __forceinline__ float inv_scale_of(uint32_t amax_bits) {
+  const float a = __uint_as_float(amax_bits);
+  return a > 0.f ? kE4M3Max / a : 1.f;
+}
+
+// Eight E4M3 codes of x * inv (round to nearest even, saturating), element 0 in the lowest byte.
+__device__ __forceinline__ uint2 quant8(const float (&x)[8], float inv) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    w[i] = __nv_cvt_float2_to_fp8x2(make_float2(x[2 * i] * inv, x[2 * i + 1] * inv), __NV_SATFINITE, __NV_E4M3);
+  return make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
+}
+
+__global__ void __launch_bounds__(kQuantThreads)
+    fp8_amax_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+                    const __nv_bfloat16* __restrict__ v, const float* __restrict__ wq,
+                    const float* __restrict__ wk, TokenGeometry geo, int N, int H, float eps, RopeTable tab,
+                    uint32_t* __restrict__ amax) {
+  extern __shared__ uint32_t s_amax[];  // [H][3]
+  const int b = blockIdx.y;
+  const int n0 = blockIdx.x * kQuantTokens;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sub = lane & 15, half = lane >> 4;
+  for (int i = threadIdx.x; i < 3 * H; i += blockDim.x) s_amax[i] = 0u;
+  __syncthreads();
+  float w_q[8], w_k[8];
+  load_weights8(wq, sub, w_q);
+  load_weights8(wk, sub, w_k);
+  for (int t = warp; t < kQuantTokens; t += kQuantThreads / 32) {
+    const int n = n0 + t;
+    if (n >= N) break;  // warp-uniform
+    float c[4], s[4];
+    lane_rotation(geo, tab, n, sub, c, s);
+    const size_t row0 = (static_cast<size_t>(b) * N + n) * H;
+    for (int hp = 0; hp < H; hp += 2) {
+      const int h = hp + half;
+      const bool valid = h < H;
+      uint4 uq = make_uint4(0, 0, 0, 0), uk = uq, uv = uq;
+      const size_t src = (row0 + h) * kHeadDim + sub * 8;
+      if (valid) {
+        uq = __ldg(reinterpret_cast<const uint4*>(q + src));
+        uk = __ldg(reinterpret_cast<const uint4*>(k + src));
+        uv = __ldg(reinterpret_cast<const uint4*>(v + src));
+      }
+      float xq[8], xk[8], xv[8];
+      unpack8(uq, xq);
+      unpack8(uk, xk);
+      unpack8(uv, xv);
+      norm_rope8(xq, w_q, c, s, eps);
+      norm_rope8(xk, w_k, c, s, eps);
+      const float mq = half_warp_max(absmax8(xq));
+      const float mk = half_warp_max(absmax8(xk));
+      const float mv = half_warp_max(absmax8(xv));
+      if (valid && sub == 0) {
+        atomicMax(&s_amax[3 * h + 0], __float_as_uint(mq));
+        atomicMax(&s_amax[3 * h + 1], __float_as_uint(mk));
+        atomicMax(&s_amax[3 * h + 2], __float_as_uint(mv));
+      }
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < 3 * H; i += blockDim.x)
+    if (s_amax[i] != 0u) atomicMax(&amax[static_cast<size_t>(b) * H * 3 + i], s_amax[i]);
+}
+
+// Row pitch (bytes) of the transposed V staging tile: 64 tokens + 16 bytes of
+// padding (keeps 16-byte alignment of every row for the vector read-out).
+constexpr int kVtPitch = kQuantTokens + 16;
+
+__global__ void __launch_bounds__(kQuantThreads)
+    fp8_quant_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+                     const __nv_bfloat16* __restrict__ v, const float* __restrict__ wq,
+                     const float* __restrict__ wk, TokenGeometry geo, int N, int npad, int H, float eps,
+                     RopeTable tab, const uint32_t* __restrict__ amax, uint8_t* __restrict__ q8,
+                     uint8_t* __restrict__ k8, uint8_t* __restrict__ v8t, float* __restrict__ scales) {
+  __shared__ __align__(16) uint8_t s_vt[kHeadDim * kVtPitch];
+  const int b = blockIdx.y;
+  const int n0 = blockIdx.x * kQuantTokens;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sub = lane & 15, half = lane >> 4;
+  const uint32_t* am = amax + static_cast<size_t>(b) * H * 3;
+
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < 3 * H; i += blockDim.x) {
+      const float a = __uint_as_float(am[i]);
+      scales[static_cast<size_t>(b) * H * 3 + i] = a > 0.f ? a / kE4M3Max : 1.f;
+    }
+
+  // Q', K' codes, head-major rows.
+  float w_q[8], w_k[8];
+  load_weights8(wq, sub, w_q);
+  load_weights8(wk, sub, w_k);
+  for (int t = warp; t < kQuantTokens; t += kQuantThreads / 32) {
+    const int n = n0 + t;
+    if (n >= N) break;  // warp-uniform
+    float c[4], s[4];
+    lane_rotation(geo, tab, n, sub, c, s);
+    const size_t row0 = (static_cast<size_t>(b) * N + n) * H;
+    for (int hp = 0; hp < H; hp += 2) {
+      const int h = hp + half;
+      const bool valid = h < H;
+      uint4 uq = make_uint4(0, 0, 0, 0), uk = uq;
+      const size_t src = (row0 + h) * kHeadDim + sub * 8;
+      if (valid) {
+        uq = __ldg(reinterpret_cast<const uint4*>(q + src));
+        uk = __ldg(reinterpret_cast<const uint4*>(k + src));
+      }
+      float xq[8], xk[8];
+      unpack8(uq, xq);
+      unpack8(uk, xk);
+      norm_rope8(xq, w_q, c, s, eps);
+      norm_rope8(xk, w_k, c, s, eps);
+      if (valid) {
+        const size_t dst = ((static_cast<size_t>(b) * H + h) * N + n) * kHeadDim + sub * 8;
+        *reinterpret_cast<uint2*>(q8 + dst) = quant8(xq, inv_scale_of(am[3 * h + 0]));
+        *reinterpret_cast<uint2*>(k8 + dst) = quant8(xk, inv_scale_of(am[3 * h + 1]));
+      }
+    }
+  }
+
+  // V^T codes: per head, stage the [64 tokens x 128 dims] block transposed in
+  // shared memory, then write 128 rows of 64 keys.  Keys N .. npad-1 get zero.
+  const int n_here = min(kQuantTokens, npad - n0);  // columns of v8t this block owns (multiple of 16)
+  for (int h = 0; h < H; ++h) {
+    const float inv = inv_scale_of(am[3 * h + 2]);
+    // Consecutive threads take consecutive tokens, so that the byte-wide
+    // transposed stores of a warp fill consecutive bytes of one row.
+    for (int i = threadIdx.x; i < kQuantTokens * (kHeadDim / 8); i += blockDim.x) {
+      const int t = i & (kQuantTokens - 1);  // token in the block
+      const int d0 = (i / kQuantTokens) * 8; // first of 8 dims
+      const int n = n0 + t;
+      uint2 code = make_uint2(0, 0);
+      if (n < N) {
+        float x[8];
+        unpack8(__ldg(reinterpret_cast<const uint4*>(v + ((static_cast<size_t>(b) * N + n) * H + h) * kHeadDim +
+                                                       d0)),
+                x);
+        code = quant8(x, inv);
+      }
+      const uint32_t w[2] = {code.x, code.y};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) s_vt[(d0 + e) * kVtPitch + t] = static_cast<uint8_t>(w[e >> 2] >> ((e & 3) * 8));
+    }
+    __syncthreads();
+    uint8_t* dst = v8t + (static_cast<size_t>(b) * H + h) * kHeadDim * static_cast<size_t>(npad) + n0;
+    const int chunks = n_here / 16;  // 16-byte pieces per row
+    for (int i = threadIdx.x; i < kHeadDim * chunks; i += blockDim.x) {
+      const int d = i / chunks, c = i - d * chunks;
+      *reinterpret_cast<uint4*>(dst + static_cast<size_t>(d) * npad + c * 16) =
+          *reinterpret_cast<const uint4*>(s_vt + d * kVtPitch + c * 16);
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace flux
