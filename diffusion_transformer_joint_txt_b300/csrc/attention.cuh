@@ -9,14 +9,31 @@
 // with FP8 attention (Q.K and P.V in FP8) in section "Quantized and sparse
 // attention"; this kernel is that step in both precisions.
 //
-// One CTA = one 128-row query tile of one (b, h).  Warp roles:
-//   warps 0-3  softmax + epilogue, thread t owns query row t (TMEM lane t)
-//   warp 4     TMA producer: Q once, then K_j / V_j into rings
-//   warp 5     TMEM allocator and single-thread tcgen05.mma issuer
-// TMEM (512 columns): S_0 at 0, S_1 at 128 (S_j double-buffered so that
-// S_{j+1} = Q K_{j+1}^T runs while the softmax works on S_j), O at 256.
-// The softmax overwrites S_j with P_j and the P.V MMA reads its A operand
-// straight from TMEM.
+// One CTA = two 128-row query tiles (0 and 1) of one (b, h) that share every
+// K/V tile.  Warp roles:
+//   warps 0-3  softmax + epilogue of query tile 0 (thread r owns row r, TMEM lane r)
+//   warps 4-7  softmax + epilogue of query tile 1
+//   warp 8     TMA producer: both Q tiles once, then K_j / V_j into rings
+//   warp 9     TMEM allocator and single-thread tcgen05.mma issuer
+// TMEM (512 columns): S_0 at 0, S_1 at 128, O_0 at 256, O_1 at 384.  The
+// softmax of a tile overwrites its S with P, and the P.V MMA reads P straight
+// from TMEM as its A operand.
+//
+// The MMA issue order is  QK_0(0) QK_1(0) | PV_0(j) QK_0(j+1) PV_1(j) QK_1(j+1) | ...
+// so while the softmax of tile 0 works on S_0(j+1) the tensor core runs
+// PV_1(j) and QK_1(j+1), and the other way round: each tile's softmax hides
+// behind the other tile's two MMAs.  The MMAs of one thread complete in issue
+// order, which is what makes two things safe: QK_t(j+1) overwrites the S_t
+// columns that PV_t(j) reads P from, and the commit that signals S_t(j+1)
+// also means that PV_t(j) has landed in O_t, so the softmax may rescale O_t
+// as soon as it sees S_t(j+1).
+//
+// Online softmax in log2 units with a deferred rescale (BF16): the running
+// max m only moves when a tile's max exceeds it by more than 2^8; until then
+// p = 2^(s - m) may reach 2^8, which bf16 and the fp32 sums carry exactly as
+// well.  O and l always use the same m, so the result is unchanged; most
+// tiles then skip the O rescale (a TMEM round trip of 128 columns).  FP8
+// rescales whenever m moves, because P is stored as E4M3 of 256 p <= 448.
 //
 // BF16: operands are bf16 (kind::f16, K = 16 per MMA).  A 128 x 128 tile is
 // two 16 KB halves (head-dim columns 0-63, 64-127), each 128 rows x 128 bytes
@@ -45,21 +62,28 @@
 namespace flux {
 namespace attn {
 
-constexpr int BM = 128;  // query rows per tile
-constexpr int BN = 128;  // keys per tile
-constexpr int HD = 128;  // head dim
-constexpr int THREADS = 192;
-constexpr int WARP_TMA = 4;
-constexpr int WARP_MMA = 5;
+constexpr int BM = 128;             // query rows per tile
+constexpr int BN = 128;             // keys per tile
+constexpr int HD = 128;             // head dim
+constexpr int TILES = 2;            // query tiles per CTA
+constexpr int CTA_ROWS = TILES * BM;
+constexpr int WARP_TMA = 4 * TILES;
+constexpr int WARP_MMA = WARP_TMA + 1;
+constexpr int THREADS = 32 * (WARP_MMA + 1);  // 320
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O = 256;
 constexpr uint32_t HALF = BM * 128;  // one SW128 block: 128 rows x 128 bytes = 16 KB
+
+__host__ __device__ constexpr uint32_t col_s(int t) { return 128u * t; }        // S_t / P_t
+__host__ __device__ constexpr uint32_t col_o(int t) { return 256u + 128u * t; } // O_t
 
 template <bool FP8>
 struct Traits {
   static constexpr uint32_t TILE = FP8 ? HALF : 2 * HALF;  // bytes of one 128 x 128 operand tile
   static constexpr int KST = FP8 ? 3 : 2;                  // K ring stages
   static constexpr int VST = FP8 ? 3 : 2;                  // V ring stages
+  // How far (log2 units) a tile's max may exceed the running max before O
+  // and l are rescaled: p = 2^(s - m) stays <= 2^RESCALE.
+  static constexpr float RESCALE = FP8 ? 0.f : 8.f;
 };
 
 template <bool FP8>
@@ -67,14 +91,13 @@ struct __align__(1024) Smem {
   static constexpr uint32_t TILE = Traits<FP8>::TILE;
   static constexpr int KST = Traits<FP8>::KST;
   static constexpr int VST = Traits<FP8>::VST;
-  uint8_t q[TILE];
+  uint8_t q[TILES][TILE];
   uint8_t k[KST][TILE];
   uint8_t v[VST][TILE];
-  uint64_t q_full;
+  uint64_t q_full[TILES];
   uint64_t k_full[KST], k_empty[KST];
   uint64_t v_full[VST], v_empty[VST];
-  uint64_t s_full[2], p_full[2];
-  uint64_t o_done;
+  uint64_t s_full[TILES], p_full[TILES], o_full[TILES];
   uint64_t mma_drain;
   uint64_t never;  // nothing arrives here (forced-timeout debug path)
   uint32_t tmem_base;
@@ -108,7 +131,7 @@ __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity, uint3
 
 // Load one 128-row operand tile (rows `row0..+127` of slice `bh`) of a
 // [.., rows, 128 elements] tensor map: two 64-column boxes for bf16, one
-// 128-byte box for E4M3.
+// 128-byte box for E4M3.  Rows past the end are zero-filled.
 template <bool FP8>
 __device__ __forceinline__ void load_rows(uint32_t dst, const CUtensorMap* map, uint64_t* bar, int row0, int bh) {
   tma_load_3d(dst, map, bar, 0, row0, bh);
@@ -121,8 +144,11 @@ __device__ __forceinline__ void producer(Smem<FP8>& sm, const CUtensorMap* tq, c
                                          volatile int* ab, uint32_t* err) {
   constexpr uint32_t TILE = Traits<FP8>::TILE;
   constexpr int KST = Traits<FP8>::KST, VST = Traits<FP8>::VST;
-  mbar_arrive_expect_tx(&sm.q_full, TILE);
-  load_rows<FP8>(smem_u32(sm.q), tq, &sm.q_full, q0, bh);
+#pragma unroll
+  for (int t = 0; t < TILES; ++t) {
+    mbar_arrive_expect_tx(&sm.q_full[t], TILE);
+    load_rows<FP8>(smem_u32(sm.q[t]), tq, &sm.q_full[t], q0 + t * BM, bh);
+  }
   int k_issued = 0, v_issued = 0;
   for (int j = 0; j < nkv; ++j) {
     const int ks = j % KST;
@@ -146,7 +172,8 @@ __device__ __forceinline__ void producer(Smem<FP8>& sm, const CUtensorMap* tq, c
     ++v_issued;
   }
   // Drain: the latest phase of every barrier a copy was issued on has completed.
-  mbar_drain(&sm.q_full, 0, err);
+#pragma unroll
+  for (int t = 0; t < TILES; ++t) mbar_drain(&sm.q_full[t], 0, err);
   for (int s = 0; s < KST; ++s) {
     const int cnt = k_issued > s ? (k_issued - s + KST - 1) / KST : 0;
     if (cnt > 0) mbar_drain(&sm.k_full[s], (cnt - 1) & 1, err);
@@ -206,32 +233,45 @@ template <bool FP8>
 __device__ __forceinline__ void mma_issuer(Smem<FP8>& sm, uint32_t tmem, int nkv, volatile int* ab,
                                            uint32_t* err) {
   constexpr int KST = Traits<FP8>::KST, VST = Traits<FP8>::VST;
-  const uint32_t qa = smem_u32(sm.q);
   do {
-    if (!mbar_wait(&sm.q_full, 0, ab, err)) break;
     if (!mbar_wait(&sm.k_full[0], 0, ab, err)) break;
-    tc_fence_after_sync();
-    issue_qk<FP8>(tmem + COL_S0, qa, smem_u32(sm.k[0]));
-    mma_commit(&sm.s_full[0]);
+    bool ok = true;
+#pragma unroll
+    for (int t = 0; t < TILES && ok; ++t) {
+      ok = mbar_wait(&sm.q_full[t], 0, ab, err);
+      if (!ok) break;
+      tc_fence_after_sync();
+      issue_qk<FP8>(tmem + col_s(t), smem_u32(sm.q[t]), smem_u32(sm.k[0]));
+      mma_commit(&sm.s_full[t]);
+    }
+    if (!ok) break;
     mma_commit(&sm.k_empty[0]);
-    for (int j = 0; j < nkv; ++j) {
-      if (j + 1 < nkv) {
-        const int jn = j + 1;
-        const int ks = jn % KST;
-        if (!mbar_wait(&sm.k_full[ks], (jn / KST) & 1, ab, err)) break;
-        tc_fence_after_sync();
-        // S buffer jn&1 last held P_{j-1}, whose P.V MMA was issued before this one.
-        issue_qk<FP8>(tmem + ((jn & 1) ? COL_S1 : COL_S0), qa, smem_u32(sm.k[ks]));
-        mma_commit(&sm.s_full[jn & 1]);
-        mma_commit(&sm.k_empty[ks]);
-      }
-      if (!mbar_wait(&sm.p_full[j & 1], (j >> 1) & 1, ab, err)) break;
+    for (int j = 0; j < nkv && ok; ++j) {
       const int vs = j % VST;
       if (!mbar_wait(&sm.v_full[vs], (j / VST) & 1, ab, err)) break;
-      tc_fence_after_sync();
-      issue_pv<FP8>(tmem + COL_O, tmem + ((j & 1) ? COL_S1 : COL_S0), smem_u32(sm.v[vs]), j > 0);
-      mma_commit(&sm.o_done);
-      mma_commit(&sm.v_empty[vs]);
+      const int jn = j + 1;
+      const int ks = jn % KST;
+#pragma unroll
+      for (int t = 0; t < TILES; ++t) {
+        ok = mbar_wait(&sm.p_full[t], j & 1, ab, err);
+        if (!ok) break;
+        tc_fence_after_sync();
+        issue_pv<FP8>(tmem + col_o(t), tmem + col_s(t), smem_u32(sm.v[vs]), j > 0);
+        if (t == TILES - 1) mma_commit(&sm.v_empty[vs]);
+        if (jn < nkv) {
+          if (t == 0) {
+            ok = mbar_wait(&sm.k_full[ks], (jn / KST) & 1, ab, err);
+            if (!ok) break;
+            tc_fence_after_sync();
+          }
+          // In issue order after PV_t(j), which read P_t from these columns.
+          issue_qk<FP8>(tmem + col_s(t), smem_u32(sm.q[t]), smem_u32(sm.k[ks]));
+          mma_commit(&sm.s_full[t]);
+          if (t == TILES - 1) mma_commit(&sm.k_empty[ks]);
+        } else {
+          mma_commit(&sm.o_full[t]);
+        }
+      }
     }
   } while (0);
   // Drain every MMA this thread issued before TMEM is released.
@@ -256,12 +296,14 @@ __device__ __forceinline__ float sum_e4m3x4(uint32_t w) {
   return (a.x + a.y) + (c.x + c.y);
 }
 
+// Softmax and epilogue of query tile `t` (128 threads, thread r = row r).
 template <bool FP8>
 __device__ __forceinline__ void softmax_epilogue(Smem<FP8>& sm, uint32_t tmem, const Params& prm, int b, int h,
-                                                 int q0, volatile int* ab) {
-  const int t = threadIdx.x;  // 0..127
-  const int warp = t >> 5;
-  const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+                                                 int row0, int t, volatile int* ab) {
+  const int r = threadIdx.x & (BM - 1);
+  const uint32_t lane_base = static_cast<uint32_t>(r & ~31) << 16;  // TMEM lanes of this warp
+  const uint32_t s_addr = tmem + lane_base + col_s(t);
+  const uint32_t o_addr = tmem + lane_base + col_o(t);
   const int N = prm.N;
   const int nkv = prm.nkv;
   float sl2 = prm.scale_log2;
@@ -274,109 +316,99 @@ __device__ __forceinline__ void softmax_epilogue(Smem<FP8>& sm, uint32_t tmem, c
   // FP8 stores P as E4M3 of 256 p: the 2^8 factor is folded into the exponent
   // and cancels against l, which sums the same scaled values.
   constexpr float kPBias = FP8 ? 8.f : 0.f;
+  constexpr float kRescale = Traits<FP8>::RESCALE;
   float m = -INFINITY;  // running max, in log2 units
   float l = 0.f;        // running row sum
   bool ok = true;
-  for (int j = 0; j < nkv && ok; ++j) {
-    const uint32_t scol = (j & 1) ? COL_S1 : COL_S0;
-    ok = mbar_wait(&sm.s_full[j & 1], (j >> 1) & 1, ab, prm.err);
+  for (int j = 0; j < nkv; ++j) {
+    ok = mbar_wait(&sm.s_full[t], j & 1, ab, prm.err);
     if (__any_sync(0xFFFFFFFFu, !ok)) { ok = false; break; }
     tc_fence_after_sync();
-    float s[BN];
-#pragma unroll
-    for (int c = 0; c < BN / 32; ++c) {
-      uint32_t r[32];
-      tmem_ld32(tmem + lane_base + scol + c * 32, r);
-      tmem_ld_wait(r);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[i]);
-    }
+    uint32_t s[BN];
+    tmem_ld128(s_addr, s);
+    tmem_ld_wait(s);
     const int valid = N - j * BN;  // keys of this tile that exist (> 0)
     if (valid < BN) {
 #pragma unroll
       for (int i = 0; i < BN; ++i)
-        if (i >= valid) s[i] = -INFINITY;
+        if (i >= valid) s[i] = __float_as_uint(-INFINITY);
     }
-    float mx = s[0];
+    float mx = __uint_as_float(s[0]);
 #pragma unroll
-    for (int i = 1; i < BN; ++i) mx = fmaxf(mx, s[i]);
-    const float m_new = fmaxf(m, mx * sl2);
-    const float alpha = ex2_approx(m - m_new);  // 0 on the first tile
+    for (int i = 1; i < BN; ++i) mx = fmaxf(mx, __uint_as_float(s[i]));
+    const float m_tile = fmaxf(m, mx * sl2);
+    // One decision per warp (TMEM moves are warp-wide); each row keeps its own alpha.
+    const bool rescale = __any_sync(0xFFFFFFFFu, m_tile > m + kRescale);
+    const float m_new = rescale ? m_tile : m;
+    const float alpha = rescale ? ex2_approx(m - m_new) : 1.f;  // 0 on the first tile
     const float nm = kPBias - m_new;
     float rs = 0.f;
     if (FP8) {
       uint32_t pk[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        pk[i] = pack_e4m3x4(ex2_approx(fmaf(s[4 * i], sl2, nm)), ex2_approx(fmaf(s[4 * i + 1], sl2, nm)),
-                            ex2_approx(fmaf(s[4 * i + 2], sl2, nm)), ex2_approx(fmaf(s[4 * i + 3], sl2, nm)));
+        pk[i] = pack_e4m3x4(ex2_approx(fmaf(__uint_as_float(s[4 * i]), sl2, nm)),
+                            ex2_approx(fmaf(__uint_as_float(s[4 * i + 1]), sl2, nm)),
+                            ex2_approx(fmaf(__uint_as_float(s[4 * i + 2]), sl2, nm)),
+                            ex2_approx(fmaf(__uint_as_float(s[4 * i + 3]), sl2, nm)));
         rs += sum_e4m3x4(pk[i]);
       }
-      tmem_st32(tmem + lane_base + scol, pk);
-      tmem_st_wait();
+      tmem_st32(s_addr, pk);
     } else {
       uint32_t pk[BN / 2];
+      float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
       for (int i = 0; i < BN / 2; ++i) {
-        const float p0 = ex2_approx(fmaf(s[2 * i], sl2, nm));
-        const float p1 = ex2_approx(fmaf(s[2 * i + 1], sl2, nm));
-        rs += p0 + p1;
+        const float p0 = ex2_approx(fmaf(__uint_as_float(s[2 * i]), sl2, nm));
+        const float p1 = ex2_approx(fmaf(__uint_as_float(s[2 * i + 1]), sl2, nm));
+        rs0 += p0;
+        rs1 += p1;
         pk[i] = pack_bf16x2(p0, p1);
       }
-      uint32_t r0[32], r1[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) { r0[i] = pk[i]; r1[i] = pk[32 + i]; }
-      tmem_st32(tmem + lane_base + scol, r0);
-      tmem_st32(tmem + lane_base + scol + 32, r1);
-      tmem_st_wait();
+      rs = rs0 + rs1;
+      tmem_st64(s_addr, pk);
     }
     l = l * alpha + rs;
-    // Every phase of o_done is confirmed in order (a parity wait is only exact
-    // when the barrier is at most one phase away), then O is rescaled where
-    // the running max moved.  P.V of tile j-1 has landed at this point.
-    if (j > 0) {
-      ok = mbar_wait(&sm.o_done, (j - 1) & 1, ab, prm.err);
-      if (__any_sync(0xFFFFFFFFu, !ok)) { ok = false; break; }
-      tc_fence_after_sync();
-      if (__any_sync(0xFFFFFFFFu, m_new > m)) {
+    // O_t holds P_t(j-1) V(j-1) already (see the issue order), and nothing
+    // else writes it until this thread arrives on p_full below.
+    if (rescale && j > 0) {
 #pragma unroll
-        for (int c = 0; c < HD / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(tmem + lane_base + COL_O + c * 32, r);
-          tmem_ld_wait(r);
+      for (int c = 0; c < HD / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(o_addr + c * 32, o);
+        tmem_ld_wait(o);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-          tmem_st32(tmem + lane_base + COL_O + c * 32, r);
-        }
-        tmem_st_wait();
+        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+        tmem_st32(o_addr + c * 32, o);
       }
     }
+    tmem_st_wait();
     m = m_new;
     tc_fence_before_sync();
-    mbar_arrive(&sm.p_full[j & 1]);
+    mbar_arrive(&sm.p_full[t]);
   }
   if (ok) {
-    ok = mbar_wait(&sm.o_done, (nkv - 1) & 1, ab, prm.err);
+    ok = mbar_wait(&sm.o_full[t], 0, ab, prm.err);
     if (__any_sync(0xFFFFFFFFu, !ok)) ok = false;
   }
   if (!ok) return;
   tc_fence_after_sync();
   const float inv_l = out_scale / l;
-  const int row = q0 + t;
+  const int row = row0 + r;
   __nv_bfloat16* dst = prm.out + ((static_cast<size_t>(b) * N + row) * prm.H + h) * HD;
 #pragma unroll
   for (int c = 0; c < HD / 32; ++c) {
-    uint32_t r[32];
-    tmem_ld32(tmem + lane_base + COL_O + c * 32, r);
-    tmem_ld_wait(r);
-    uint32_t o[16];
+    uint32_t o[32];
+    tmem_ld32(o_addr + c * 32, o);
+    tmem_ld_wait(o);
+    uint32_t w[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i)
-      o[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv_l, __uint_as_float(r[2 * i + 1]) * inv_l);
+      w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
     if (row < N) {
       uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) d4[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+      for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
     }
   }
 }
@@ -394,15 +426,18 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int bh = blockIdx.y;
   const int b = bh / prm.H;
   const int h = bh - b * prm.H;
-  const int q0 = blockIdx.x * BM;
+  const int q0 = blockIdx.x * CTA_ROWS;
   volatile int* ab = &sm.abort;
 
   if (threadIdx.x == 0) {
-    mbar_init(&sm.q_full, 1);
+    for (int t = 0; t < TILES; ++t) {
+      mbar_init(&sm.q_full[t], 1);
+      mbar_init(&sm.s_full[t], 1);
+      mbar_init(&sm.p_full[t], BM);
+      mbar_init(&sm.o_full[t], 1);
+    }
     for (int s = 0; s < KST; ++s) { mbar_init(&sm.k_full[s], 1); mbar_init(&sm.k_empty[s], 1); }
     for (int s = 0; s < VST; ++s) { mbar_init(&sm.v_full[s], 1); mbar_init(&sm.v_empty[s], 1); }
-    for (int s = 0; s < 2; ++s) { mbar_init(&sm.s_full[s], 1); mbar_init(&sm.p_full[s], BM); }
-    mbar_init(&sm.o_done, 1);
     mbar_init(&sm.mma_drain, 1);
     mbar_init(&sm.never, 1);
     sm.abort = 0;
@@ -434,7 +469,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0 && !*ab) mma_issuer<FP8>(sm, tmem, prm.nkv, ab, prm.err);
     __syncwarp();
   } else {
-    if (!*ab) softmax_epilogue<FP8>(sm, tmem, prm, b, h, q0, ab);
+    const int t = warp >> 2;  // query tile of this warpgroup
+    if (!*ab) softmax_epilogue<FP8>(sm, tmem, prm, b, h, q0 + t * BM, t, ab);
   }
   tc_fence_before_sync();
   __syncthreads();

@@ -230,7 +230,7 @@ int launch_attention(flux_attn* h, bool fp8, const void* qn, const void* kn, con
   prm.nkv = (n + BN - 1) / BN;
   prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(HD)));
   prm.debug = h->cfg.debug_flags;
-  const dim3 grid((n + BM - 1) / BM, B * H);
+  const dim3 grid((n + CTA_ROWS - 1) / CTA_ROWS, B * H);
   if (fp8)
     attn_kernel<true><<<grid, THREADS, smem_bytes<true>(), stream>>>(tq, tk, tv, prm);
   else
