@@ -13,8 +13,9 @@
 // K/V tile.  Warp roles:
 //   warps 0-3  softmax + epilogue of query tile 0 (thread r owns row r, TMEM lane r)
 //   warps 4-7  softmax + epilogue of query tile 1
-//   warp 8     TMA producer: both Q tiles once, then K_j / V_j into rings
-//   warp 9     TMEM allocator and single-thread tcgen05.mma issuer
+//   warp 8     TMA producer of the K ring
+//   warp 9     TMEM allocator and tcgen05.mma issuer (one elected lane)
+//   warp 10    TMA producer of both Q tiles and of the V ring
 // TMEM (512 columns): S_0 at 0, S_1 at 128, O_0 at 256, O_1 at 384.  The
 // softmax of a tile overwrites its S with P, and the P.V MMA reads P straight
 // from TMEM as its A operand.
@@ -22,11 +23,11 @@
 // The MMA issue order is  QK_0(0) QK_1(0) | PV_0(j) QK_0(j+1) PV_1(j) QK_1(j+1) | ...
 // so while the softmax of tile 0 works on S_0(j+1) the tensor core runs
 // PV_1(j) and QK_1(j+1), and the other way round: each tile's softmax hides
-// behind the other tile's two MMAs.  The MMAs of one thread complete in issue
-// order, which is what makes two things safe: QK_t(j+1) overwrites the S_t
-// columns that PV_t(j) reads P from, and the commit that signals S_t(j+1)
-// also means that PV_t(j) has landed in O_t, so the softmax may rescale O_t
-// as soon as it sees S_t(j+1).
+// behind the other tile's two MMAs.  The MMAs of one
+// thread complete in issue order, which is what makes two things safe:
+// QK_t(j+1) overwrites the S_t columns that PV_t(j) reads P from, and the
+// commit that signals S_t(j+1) also means that PV_t(j) has landed in O_t, so
+// the softmax may rescale O_t as soon as it sees S_t(j+1).
 //
 // Online softmax in log2 units with a deferred rescale (BF16): the running
 // max m only moves when a tile's max exceeds it by more than 2^8; until then
@@ -67,9 +68,10 @@ constexpr int BN = 128;             // keys per tile
 constexpr int HD = 128;             // head dim
 constexpr int TILES = 2;            // query tiles per CTA
 constexpr int CTA_ROWS = TILES * BM;
-constexpr int WARP_TMA = 4 * TILES;
-constexpr int WARP_MMA = WARP_TMA + 1;
-constexpr int THREADS = 32 * (WARP_MMA + 1);  // 320
+constexpr int WARP_LOAD_K = 4 * TILES;          // 8: TMA producer of the K ring
+constexpr int WARP_MMA = WARP_LOAD_K + 1;       // 9: MMA issuer, TMEM owner
+constexpr int WARP_LOAD_V = WARP_MMA + 1;       // 10: TMA producer of Q and the V ring
+constexpr int THREADS = 32 * (WARP_LOAD_V + 1); // 352
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t HALF = BM * 128;  // one SW128 block: 128 rows x 128 bytes = 16 KB
 
@@ -79,8 +81,8 @@ __host__ __device__ constexpr uint32_t col_o(int t) { return 256u + 128u * t; } 
 template <bool FP8>
 struct Traits {
   static constexpr uint32_t TILE = FP8 ? HALF : 2 * HALF;  // bytes of one 128 x 128 operand tile
-  static constexpr int KST = FP8 ? 3 : 2;                  // K ring stages
-  static constexpr int VST = FP8 ? 3 : 2;                  // V ring stages
+  static constexpr int KST = FP8 ? 4 : 3;                  // K ring stages
+  static constexpr int VST = FP8 ? 4 : 2;                  // V ring stages
   // How far (log2 units) a tile's max may exceed the running max before O
   // and l are rescaled: p = 2^(s - m) stays <= 2^RESCALE.
   static constexpr float RESCALE = FP8 ? 0.f : 8.f;
@@ -138,25 +140,49 @@ __device__ __forceinline__ void load_rows(uint32_t dst, const CUtensorMap* map, 
   if (!FP8) tma_load_3d(dst + HALF, map, bar, 64, row0, bh);
 }
 
-template <bool FP8>
-__device__ __forceinline__ void producer(Smem<FP8>& sm, const CUtensorMap* tq, const CUtensorMap* tk,
-                                         const CUtensorMap* tv, int q0, int bh, int b, int h, int nkv,
-                                         volatile int* ab, uint32_t* err) {
-  constexpr uint32_t TILE = Traits<FP8>::TILE;
-  constexpr int KST = Traits<FP8>::KST, VST = Traits<FP8>::VST;
-#pragma unroll
-  for (int t = 0; t < TILES; ++t) {
-    mbar_arrive_expect_tx(&sm.q_full[t], TILE);
-    load_rows<FP8>(smem_u32(sm.q[t]), tq, &sm.q_full[t], q0 + t * BM, bh);
+// Drain a ring: the latest phase of every full-barrier a copy was issued on
+// has completed (nothing may still be writing shared memory at exit).
+template <int ST>
+__device__ __forceinline__ void drain_ring(uint64_t (&full)[ST], int issued, uint32_t* err) {
+  for (int s = 0; s < ST; ++s) {
+    const int cnt = issued > s ? (issued - s + ST - 1) / ST : 0;
+    if (cnt > 0) mbar_drain(&full[s], (cnt - 1) & 1, err);
   }
-  int k_issued = 0, v_issued = 0;
+}
+
+// K ring producer: K_j into stage j % KST once both tiles' QK of its
+// previous occupant have completed.
+template <bool FP8>
+__device__ __forceinline__ void load_k(Smem<FP8>& sm, const CUtensorMap* tk, int bh, int nkv, volatile int* ab,
+                                       uint32_t* err) {
+  constexpr uint32_t TILE = Traits<FP8>::TILE;
+  constexpr int KST = Traits<FP8>::KST;
+  int issued = 0;
   for (int j = 0; j < nkv; ++j) {
     const int ks = j % KST;
     const uint32_t ku = j / KST;
     if (ku > 0 && !mbar_wait(&sm.k_empty[ks], (ku - 1) & 1, ab, err)) break;
     mbar_arrive_expect_tx(&sm.k_full[ks], TILE);
     load_rows<FP8>(smem_u32(sm.k[ks]), tk, &sm.k_full[ks], j * BN, bh);
-    ++k_issued;
+    ++issued;
+  }
+  drain_ring(sm.k_full, issued, err);
+}
+
+// Q and V ring producer: both Q tiles once, then V_j into stage j % VST once
+// both tiles' PV of its previous occupant have completed.
+template <bool FP8>
+__device__ __forceinline__ void load_qv(Smem<FP8>& sm, const CUtensorMap* tq, const CUtensorMap* tv, int q0, int bh,
+                                        int b, int h, int nkv, volatile int* ab, uint32_t* err) {
+  constexpr uint32_t TILE = Traits<FP8>::TILE;
+  constexpr int VST = Traits<FP8>::VST;
+#pragma unroll
+  for (int t = 0; t < TILES; ++t) {
+    mbar_arrive_expect_tx(&sm.q_full[t], TILE);
+    load_rows<FP8>(smem_u32(sm.q[t]), tq, &sm.q_full[t], q0 + t * BM, bh);
+  }
+  int issued = 0;
+  for (int j = 0; j < nkv; ++j) {
     const int vs = j % VST;
     const uint32_t vu = j / VST;
     if (vu > 0 && !mbar_wait(&sm.v_empty[vs], (vu - 1) & 1, ab, err)) break;
@@ -169,43 +195,42 @@ __device__ __forceinline__ void producer(Smem<FP8>& sm, const CUtensorMap* tq, c
       tma_load_4d(smem_u32(sm.v[vs]), tv, &sm.v_full[vs], 0, h, j * BN, b);
       tma_load_4d(smem_u32(sm.v[vs]) + HALF, tv, &sm.v_full[vs], 64, h, j * BN, b);
     }
-    ++v_issued;
+    ++issued;
   }
-  // Drain: the latest phase of every barrier a copy was issued on has completed.
 #pragma unroll
   for (int t = 0; t < TILES; ++t) mbar_drain(&sm.q_full[t], 0, err);
-  for (int s = 0; s < KST; ++s) {
-    const int cnt = k_issued > s ? (k_issued - s + KST - 1) / KST : 0;
-    if (cnt > 0) mbar_drain(&sm.k_full[s], (cnt - 1) & 1, err);
-  }
-  for (int s = 0; s < VST; ++s) {
-    const int cnt = v_issued > s ? (v_issued - s + VST - 1) / VST : 0;
-    if (cnt > 0) mbar_drain(&sm.v_full[s], (cnt - 1) & 1, err);
-  }
+  drain_ring(sm.v_full, issued, err);
 }
 
-// S = Q K^T over the 128 head dims.
+// Matrix descriptors are built once per CTA: the start-address field
+// (address >> 4, 14 bits) of a shared-memory tile never carries into the
+// other fields, so the descriptor of an operand at byte offset `off` inside a
+// tile is the tile's descriptor plus off >> 4.  That keeps the single issuing
+// thread at one add per MMA, which matters: it shares its scheduler with two
+// softmax warps and must issue an MMA every 64 cycles to keep up.
+__device__ __forceinline__ uint64_t desc_at(uint64_t d, uint32_t off) { return d + (off >> 4); }
+
+// S = Q K^T over the 128 head dims (qd, kd: SW128 K-major tile descriptors).
 //   BF16: 8 MMAs of 128 x 128 x 16; step kk covers head dims 16kk..16kk+15:
 //         half kk/4 of the tile, 32-byte offset (kk%4) inside the swizzle row.
 //   FP8:  4 MMAs of 128 x 128 x 32; step kk is the 32-byte offset 32kk.
 template <bool FP8>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t qa, uint32_t ka) {
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t qd, uint64_t kd) {
   if (FP8) {
     constexpr uint32_t ID = idesc_e4m3(BM, BN, false);
 #pragma unroll
-    for (int kk = 0; kk < HD / 32; ++kk)
-      mma_e4m3_ss(d_tmem, sdesc_sw128(qa + kk * 32, 16, 1024), sdesc_sw128(ka + kk * 32, 16, 1024), ID, kk > 0);
+    for (int kk = 0; kk < HD / 32; ++kk) mma_e4m3_ss(d_tmem, desc_at(qd, kk * 32), desc_at(kd, kk * 32), ID, kk > 0);
   } else {
     constexpr uint32_t ID = idesc_f16(BM, BN, false);
 #pragma unroll
     for (int kk = 0; kk < HD / 16; ++kk) {
       const uint32_t off = (kk >> 2) * HALF + (kk & 3) * 32;
-      mma_f16_ss(d_tmem, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), ID, kk > 0);
+      mma_f16_ss(d_tmem, desc_at(qd, off), desc_at(kd, off), ID, kk > 0);
     }
   }
 }
 
-// O (+)= P V over the 128 keys of a tile.
+// O (+)= P V over the 128 keys of a tile (vd: V tile descriptor).
 //   BF16: 8 MMAs of 128 x 128 x 16; step kk covers keys 16kk..16kk+15: P
 //         columns 8kk.. (two bf16 per column), V rows 16kk.. (16 rows x 128 B
 //         = 2 KB); V is MN-major: LBO = the other 64 head dims (the other
@@ -213,26 +238,37 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t qa, uint32_t 
 //   FP8:  4 MMAs of 128 x 128 x 32; step kk covers keys 32kk..: P columns
 //         8kk.. (four E4M3 per column), V^T K-major at byte offset 32kk.
 template <bool FP8>
-__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t va, bool accumulate) {
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t vd, bool accumulate) {
   if (FP8) {
     constexpr uint32_t ID = idesc_e4m3(BM, HD, false);
 #pragma unroll
     for (int kk = 0; kk < BN / 32; ++kk)
-      mma_e4m3_ts(o_tmem, p_tmem + kk * 8, sdesc_sw128(va + kk * 32, 16, 1024), ID,
-                  (accumulate || kk > 0) ? 1u : 0u);
+      mma_e4m3_ts(o_tmem, p_tmem + kk * 8, desc_at(vd, kk * 32), ID, (accumulate || kk > 0) ? 1u : 0u);
   } else {
     constexpr uint32_t ID = idesc_f16(BM, HD, true);
 #pragma unroll
     for (int kk = 0; kk < BN / 16; ++kk)
-      mma_f16_ts(o_tmem, p_tmem + kk * 8, sdesc_sw128(va + kk * 2048, HALF, 1024), ID,
-                 (accumulate || kk > 0) ? 1u : 0u);
+      mma_f16_ts(o_tmem, p_tmem + kk * 8, desc_at(vd, kk * 2048), ID, (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
+// The MMA issuer: QK_0(0) QK_1(0), then PV_0(j) QK_0(j+1) PV_1(j) QK_1(j+1)
+// for every j.  The whole warp runs this loop and one elected lane issues
+// (ptx.cuh).  One thread issues for both tiles: the fixed order is what
+// keeps the two tiles in turns (two independent issuers drift into step, and
+// then both softmaxes run at once and compete for the same schedulers).
 template <bool FP8>
 __device__ __forceinline__ void mma_issuer(Smem<FP8>& sm, uint32_t tmem, int nkv, volatile int* ab,
                                            uint32_t* err) {
+  constexpr uint32_t TILE = Traits<FP8>::TILE;
   constexpr int KST = Traits<FP8>::KST, VST = Traits<FP8>::VST;
+  // Tile descriptors: K-major SW128 (SBO = 8 rows x 128 B) for Q, K and the
+  // FP8 V^T; MN-major SW128 for the BF16 V (LBO = the other 64 head dims).
+  uint64_t qd[TILES];
+#pragma unroll
+  for (int t = 0; t < TILES; ++t) qd[t] = sdesc_sw128(smem_u32(sm.q[t]), 16, 1024);
+  const uint64_t kd0 = sdesc_sw128(smem_u32(sm.k[0]), 16, 1024);
+  const uint64_t vd0 = sdesc_sw128(smem_u32(sm.v[0]), FP8 ? 16 : HALF, 1024);
   do {
     if (!mbar_wait(&sm.k_full[0], 0, ab, err)) break;
     bool ok = true;
@@ -241,7 +277,7 @@ __device__ __forceinline__ void mma_issuer(Smem<FP8>& sm, uint32_t tmem, int nkv
       ok = mbar_wait(&sm.q_full[t], 0, ab, err);
       if (!ok) break;
       tc_fence_after_sync();
-      issue_qk<FP8>(tmem + col_s(t), smem_u32(sm.q[t]), smem_u32(sm.k[0]));
+      issue_qk<FP8>(tmem + col_s(t), qd[t], kd0);
       mma_commit(&sm.s_full[t]);
     }
     if (!ok) break;
@@ -249,14 +285,16 @@ __device__ __forceinline__ void mma_issuer(Smem<FP8>& sm, uint32_t tmem, int nkv
     for (int j = 0; j < nkv && ok; ++j) {
       const int vs = j % VST;
       if (!mbar_wait(&sm.v_full[vs], (j / VST) & 1, ab, err)) break;
+      const uint64_t vd = desc_at(vd0, vs * TILE);
       const int jn = j + 1;
       const int ks = jn % KST;
+      const uint64_t kd = desc_at(kd0, ks * TILE);
 #pragma unroll
       for (int t = 0; t < TILES; ++t) {
         ok = mbar_wait(&sm.p_full[t], j & 1, ab, err);
         if (!ok) break;
         tc_fence_after_sync();
-        issue_pv<FP8>(tmem + col_o(t), tmem + col_s(t), smem_u32(sm.v[vs]), j > 0);
+        issue_pv<FP8>(tmem + col_o(t), tmem + col_s(t), vd, j > 0);
         if (t == TILES - 1) mma_commit(&sm.v_empty[vs]);
         if (jn < nkv) {
           if (t == 0) {
@@ -265,7 +303,7 @@ __device__ __forceinline__ void mma_issuer(Smem<FP8>& sm, uint32_t tmem, int nkv
             tc_fence_after_sync();
           }
           // In issue order after PV_t(j), which read P_t from these columns.
-          issue_qk<FP8>(tmem + col_s(t), smem_u32(sm.q[t]), smem_u32(sm.k[ks]));
+          issue_qk<FP8>(tmem + col_s(t), qd[t], kd);
           mma_commit(&sm.s_full[t]);
           if (t == TILES - 1) mma_commit(&sm.k_empty[ks]);
         } else {
@@ -333,41 +371,55 @@ __device__ __forceinline__ void softmax_epilogue(Smem<FP8>& sm, uint32_t tmem, c
       for (int i = 0; i < BN; ++i)
         if (i >= valid) s[i] = __float_as_uint(-INFINITY);
     }
-    float mx = __uint_as_float(s[0]);
+    // Row max: four independent chains of three-input max (depth 16, not 127).
+    float acc[4];
 #pragma unroll
-    for (int i = 1; i < BN; ++i) mx = fmaxf(mx, __uint_as_float(s[i]));
+    for (int c = 0; c < 4; ++c) acc[c] = fmaxf(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1]));
+#pragma unroll
+    for (int i = 8; i < BN; i += 8) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        acc[c] = fmax3(acc[c], __uint_as_float(s[i + 2 * c]), __uint_as_float(s[i + 2 * c + 1]));
+    }
+    const float mx = fmax3(acc[0], acc[1], fmaxf(acc[2], acc[3]));
     const float m_tile = fmaxf(m, mx * sl2);
     // One decision per warp (TMEM moves are warp-wide); each row keeps its own alpha.
     const bool rescale = __any_sync(0xFFFFFFFFu, m_tile > m + kRescale);
     const float m_new = rescale ? m_tile : m;
     const float alpha = rescale ? ex2_approx(m - m_new) : 1.f;  // 0 on the first tile
     const float nm = kPBias - m_new;
-    float rs = 0.f;
+    // p = 2^(s sl2 - m): the argument of two scores per packed FMA; the row
+    // sum in four packed accumulators.
+    float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float rs;
     if (FP8) {
       uint32_t pk[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        pk[i] = pack_e4m3x4(ex2_approx(fmaf(__uint_as_float(s[4 * i]), sl2, nm)),
-                            ex2_approx(fmaf(__uint_as_float(s[4 * i + 1]), sl2, nm)),
-                            ex2_approx(fmaf(__uint_as_float(s[4 * i + 2]), sl2, nm)),
-                            ex2_approx(fmaf(__uint_as_float(s[4 * i + 3]), sl2, nm)));
-        rs += sum_e4m3x4(pk[i]);
+        float x0, x1, x2, x3;
+        fma2(x0, x1, __uint_as_float(s[4 * i]), __uint_as_float(s[4 * i + 1]), sl2, sl2, nm, nm);
+        fma2(x2, x3, __uint_as_float(s[4 * i + 2]), __uint_as_float(s[4 * i + 3]), sl2, sl2, nm, nm);
+        pk[i] = pack_e4m3x4(ex2_approx(x0), ex2_approx(x1), ex2_approx(x2), ex2_approx(x3));
+        sum[i & 7] += sum_e4m3x4(pk[i]);
       }
       tmem_st32(s_addr, pk);
     } else {
       uint32_t pk[BN / 2];
-      float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
       for (int i = 0; i < BN / 2; ++i) {
-        const float p0 = ex2_approx(fmaf(__uint_as_float(s[2 * i]), sl2, nm));
-        const float p1 = ex2_approx(fmaf(__uint_as_float(s[2 * i + 1]), sl2, nm));
-        rs0 += p0;
-        rs1 += p1;
+        float x0, x1;
+        fma2(x0, x1, __uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]), sl2, sl2, nm, nm);
+        const float p0 = ex2_approx(x0);
+        const float p1 = ex2_approx(x1);
+        add2(sum[2 * (i & 3)], sum[2 * (i & 3) + 1], p0, p1);
         pk[i] = pack_bf16x2(p0, p1);
       }
-      rs = rs0 + rs1;
       tmem_st64(s_addr, pk);
     }
+    add2(sum[0], sum[1], sum[2], sum[3]);
+    add2(sum[4], sum[5], sum[6], sum[7]);
+    add2(sum[0], sum[1], sum[4], sum[5]);
+    rs = sum[0] + sum[1];
     l = l * alpha + rs;
     // O_t holds P_t(j-1) V(j-1) already (see the issue order), and nothing
     // else writes it until this thread arrives on p_full below.
@@ -443,11 +495,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     sm.abort = 0;
     fence_mbarrier_init();
   }
-  if (warp == WARP_TMA && lane == 0) {
+  if (warp == WARP_LOAD_V && lane == 0) {
     tma_prefetch_desc(&tm_q);
-    tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
   }
+  if (warp == WARP_LOAD_K && lane == 0) tma_prefetch_desc(&tm_k);
   if (warp == WARP_MMA) {
     tmem_alloc(&sm.tmem_base, TMEM_COLS);
     tmem_relinquish();
@@ -462,11 +514,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncthreads();
   }
 
-  if (warp == WARP_TMA) {
-    if (lane == 0 && !*ab) producer<FP8>(sm, &tm_q, &tm_k, &tm_v, q0, bh, b, h, prm.nkv, ab, prm.err);
+  if (warp == WARP_LOAD_K) {
+    if (lane == 0 && !*ab) load_k<FP8>(sm, &tm_k, bh, prm.nkv, ab, prm.err);
+    __syncwarp();
+  } else if (warp == WARP_LOAD_V) {
+    if (lane == 0 && !*ab) load_qv<FP8>(sm, &tm_q, &tm_v, q0, bh, b, h, prm.nkv, ab, prm.err);
     __syncwarp();
   } else if (warp == WARP_MMA) {
-    if (lane == 0 && !*ab) mma_issuer<FP8>(sm, tmem, prm.nkv, ab, prm.err);
+    if (!*ab) mma_issuer<FP8>(sm, tmem, prm.nkv, ab, prm.err);  // the whole warp: see mma_commit
     __syncwarp();
   } else {
     const int t = warp >> 2;  // query tile of this warpgroup
