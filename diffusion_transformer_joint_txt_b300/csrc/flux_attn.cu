@@ -6,6 +6,7 @@
 // quantize_fp8.cuh and attention.cuh.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -147,12 +148,13 @@ int launch_prologue(flux_attn* h, const void* q, const void* k, int txt, int ih,
   (void)rh;
   flux::TokenGeometry geo{pos, txt, ih * iw, iw, rw};
   const int B = h->cfg.batch, H = h->cfg.num_heads;
-  const long long warps = static_cast<long long>(B) * n;
-  const int per_block = flux::kPrologueThreads / 32;
-  const unsigned blocks = static_cast<unsigned>((warps + per_block - 1) / per_block);
-  flux::qk_norm_rope_kernel<<<blocks, flux::kPrologueThreads, 0, stream>>>(
+  const int T = flux::prologue_chunk_tokens(H);
+  const long long chunks = (static_cast<long long>(B) * n + T - 1) / T;
+  const unsigned grid = static_cast<unsigned>(std::min<long long>(chunks, h->num_sms));
+  const size_t smem = static_cast<size_t>(flux::kProStages) * 2 * T * H * flux::kHeadDim * 2;
+  flux::qk_norm_rope_kernel<<<grid, flux::kPrologueThreads, smem, stream>>>(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), wq, wk, geo, B, n, H,
-      h->cfg.rms_eps, h->rope, qn, kn);
+      h->cfg.rms_eps, h->rope, qn, kn, h->err);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "prologue launch");
   return FLUX_ATTN_OK;
@@ -240,10 +242,14 @@ int launch_attention(flux_attn* h, bool fp8, const void* qn, const void* kn, con
   return FLUX_ATTN_OK;
 }
 
-// Raise the dynamic shared-memory limit of both attention kernels (per device).
+// Raise the dynamic shared-memory limit of the prologue and of both
+// attention kernels (per device).
 cudaError_t set_attention_smem_limits() {
-  cudaError_t e = cudaFuncSetAttribute(flux::attn::attn_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(flux::attn::smem_bytes<false>()));
+  cudaError_t e = cudaFuncSetAttribute(flux::qk_norm_rope_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       flux::kProStages * flux::kProStageBytes);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(flux::attn::attn_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(flux::attn::smem_bytes<false>()));
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(flux::attn::attn_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(flux::attn::smem_bytes<true>()));
@@ -278,6 +284,8 @@ int flux_attn_create(const flux_attn_config* cfg, flux_attn_t* out) {
     return fail(FLUX_ATTN_ERR_INVALID_ARG, "batch, num_heads and max_tokens must be >= 1");
   if (static_cast<long long>(cfg->batch) * cfg->num_heads > 65535)
     return fail(FLUX_ATTN_ERR_INVALID_ARG, "batch * num_heads must be <= 65535");
+  if (cfg->num_heads > flux::kProMaxHeads)
+    return fail(FLUX_ATTN_ERR_UNSUPPORTED, "num_heads = %d, at most %d are built", cfg->num_heads, flux::kProMaxHeads);
   if (cfg->max_tokens > (1 << 24)) return fail(FLUX_ATTN_ERR_INVALID_ARG, "max_tokens must be <= 2^24");
   const int* ax = cfg->axes_dim;
   if (ax[0] < 0 || ax[1] < 0 || ax[2] < 0 || (ax[0] | ax[1] | ax[2]) & 1 ||
@@ -589,6 +597,8 @@ extern "C" int flux_attn_forward_noalloc(const flux_attn_config* cfg, const void
     return fail(FLUX_ATTN_ERR_UNSUPPORTED, "the allocation-free forward is BF16 only");
   if (cfg->batch < 1 || cfg->num_heads < 1 || cfg->max_tokens < 1)
     return fail(FLUX_ATTN_ERR_INVALID_ARG, "batch, num_heads and max_tokens must be >= 1");
+  if (cfg->num_heads > flux::kProMaxHeads)
+    return fail(FLUX_ATTN_ERR_UNSUPPORTED, "num_heads = %d, at most %d are built", cfg->num_heads, flux::kProMaxHeads);
   const int* ax = cfg->axes_dim;
   if (ax[0] < 0 || ax[1] < 0 || ax[2] < 0 || (ax[0] | ax[1] | ax[2]) & 1 ||
       ax[0] + ax[1] + ax[2] != cfg->head_dim)
@@ -614,7 +624,8 @@ extern "C" int flux_attn_forward_noalloc(const flux_attn_config* cfg, const void
   flux_attn view{};
   view.cfg = *cfg;
   view.device = dev;
-  view.num_sms = 0;
+  if ((e = cudaDeviceGetAttribute(&view.num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return cuda_fail(e, "cudaDeviceGetAttribute");
   view.ws = nullptr;
   view.ws_bytes = 0;
   {

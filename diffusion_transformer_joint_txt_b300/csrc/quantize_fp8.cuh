@@ -21,7 +21,8 @@
 //                       scales   fp32 [B, H, 3] = (s_q, s_k, s_v)
 // Both take one block of 256 threads per 64 consecutive tokens of one batch
 // row; inside it a warp handles one token at a time (a half-warp per head
-// row, 8 elements per lane, as in the BF16 prologue).
+// row, 8 elements per lane, as in the BF16 prologue), eight heads per step
+// with all of their loads issued before the arithmetic.
 #pragma once
 
 #include <cuda_fp8.h>
@@ -32,19 +33,8 @@ namespace flux {
 
 constexpr int kQuantTokens = 64;     // tokens per block
 constexpr int kQuantThreads = 256;   // 8 warps
+constexpr int kQuantHeads = 8;       // heads per step of a warp (all loads of a step issued first)
 constexpr float kE4M3Max = 448.f;
-
-// Rotation angles of the four pairs a lane owns (pairs 4 sub .. 4 sub + 3).
-__device__ __forceinline__ void lane_rotation(const TokenGeometry& geo, const RopeTable& tab, int n, int sub,
-                                              float (&c)[4], float (&s)[4]) {
-  int p[3];
-  token_position(geo, n, p);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int j = sub * 4 + i;
-    sincosf(static_cast<float>(p[tab.axis[j]]) * tab.freq[j], &s[i], &c[i]);
-  }
-}
 
 __device__ __forceinline__ void load_weights8(const float* w, int sub, float (&o)[8]) {
   const float4* a = reinterpret_cast<const float4*>(w + sub * 8);
@@ -103,29 +93,37 @@ __global__ void __launch_bounds__(kQuantThreads)
     float c[4], s[4];
     lane_rotation(geo, tab, n, sub, c, s);
     const size_t row0 = (static_cast<size_t>(b) * N + n) * H;
-    for (int hp = 0; hp < H; hp += 2) {
-      const int h = hp + half;
-      const bool valid = h < H;
-      uint4 uq = make_uint4(0, 0, 0, 0), uk = uq, uv = uq;
-      const size_t src = (row0 + h) * kHeadDim + sub * 8;
-      if (valid) {
-        uq = __ldg(reinterpret_cast<const uint4*>(q + src));
-        uk = __ldg(reinterpret_cast<const uint4*>(k + src));
-        uv = __ldg(reinterpret_cast<const uint4*>(v + src));
+    for (int h0 = 0; h0 < H; h0 += kQuantHeads) {
+      // all loads of the group first (bytes in flight), then the arithmetic
+      uint4 uq[kQuantHeads / 2], uk[kQuantHeads / 2], uv[kQuantHeads / 2];
+#pragma unroll
+      for (int i = 0; i < kQuantHeads / 2; ++i) {
+        const int h = h0 + 2 * i + half;
+        uq[i] = uk[i] = uv[i] = make_uint4(0, 0, 0, 0);
+        if (h < H) {
+          const size_t src = (row0 + h) * kHeadDim + sub * 8;
+          uq[i] = __ldg(reinterpret_cast<const uint4*>(q + src));
+          uk[i] = __ldg(reinterpret_cast<const uint4*>(k + src));
+          uv[i] = __ldg(reinterpret_cast<const uint4*>(v + src));
+        }
       }
-      float xq[8], xk[8], xv[8];
-      unpack8(uq, xq);
-      unpack8(uk, xk);
-      unpack8(uv, xv);
-      norm_rope8(xq, w_q, c, s, eps);
-      norm_rope8(xk, w_k, c, s, eps);
-      const float mq = half_warp_max(absmax8(xq));
-      const float mk = half_warp_max(absmax8(xk));
-      const float mv = half_warp_max(absmax8(xv));
-      if (valid && sub == 0) {
-        atomicMax(&s_amax[3 * h + 0], __float_as_uint(mq));
-        atomicMax(&s_amax[3 * h + 1], __float_as_uint(mk));
-        atomicMax(&s_amax[3 * h + 2], __float_as_uint(mv));
+#pragma unroll
+      for (int i = 0; i < kQuantHeads / 2; ++i) {
+        const int h = h0 + 2 * i + half;
+        float xq[8], xk[8], xv[8];
+        unpack8(uq[i], xq);
+        unpack8(uk[i], xk);
+        unpack8(uv[i], xv);
+        norm_rope8(xq, w_q, c, s, eps);
+        norm_rope8(xk, w_k, c, s, eps);
+        const float mq = half_warp_max(absmax8(xq));
+        const float mk = half_warp_max(absmax8(xk));
+        const float mv = half_warp_max(absmax8(xv));
+        if (h < H && sub == 0) {
+          atomicMax(&s_amax[3 * h + 0], __float_as_uint(mq));
+          atomicMax(&s_amax[3 * h + 1], __float_as_uint(mk));
+          atomicMax(&s_amax[3 * h + 2], __float_as_uint(mv));
+        }
       }
     }
   }
@@ -167,24 +165,31 @@ __global__ void __launch_bounds__(kQuantThreads)
     float c[4], s[4];
     lane_rotation(geo, tab, n, sub, c, s);
     const size_t row0 = (static_cast<size_t>(b) * N + n) * H;
-    for (int hp = 0; hp < H; hp += 2) {
-      const int h = hp + half;
-      const bool valid = h < H;
-      uint4 uq = make_uint4(0, 0, 0, 0), uk = uq;
-      const size_t src = (row0 + h) * kHeadDim + sub * 8;
-      if (valid) {
-        uq = __ldg(reinterpret_cast<const uint4*>(q + src));
-        uk = __ldg(reinterpret_cast<const uint4*>(k + src));
+    for (int h0 = 0; h0 < H; h0 += kQuantHeads) {
+      uint4 uq[kQuantHeads / 2], uk[kQuantHeads / 2];
+#pragma unroll
+      for (int i = 0; i < kQuantHeads / 2; ++i) {
+        const int h = h0 + 2 * i + half;
+        uq[i] = uk[i] = make_uint4(0, 0, 0, 0);
+        if (h < H) {
+          const size_t src = (row0 + h) * kHeadDim + sub * 8;
+          uq[i] = __ldg(reinterpret_cast<const uint4*>(q + src));
+          uk[i] = __ldg(reinterpret_cast<const uint4*>(k + src));
+        }
       }
-      float xq[8], xk[8];
-      unpack8(uq, xq);
-      unpack8(uk, xk);
-      norm_rope8(xq, w_q, c, s, eps);
-      norm_rope8(xk, w_k, c, s, eps);
-      if (valid) {
-        const size_t dst = ((static_cast<size_t>(b) * H + h) * N + n) * kHeadDim + sub * 8;
-        *reinterpret_cast<uint2*>(q8 + dst) = quant8(xq, inv_scale_of(am[3 * h + 0]));
-        *reinterpret_cast<uint2*>(k8 + dst) = quant8(xk, inv_scale_of(am[3 * h + 1]));
+#pragma unroll
+      for (int i = 0; i < kQuantHeads / 2; ++i) {
+        const int h = h0 + 2 * i + half;
+        float xq[8], xk[8];
+        unpack8(uq[i], xq);
+        unpack8(uk[i], xk);
+        norm_rope8(xq, w_q, c, s, eps);
+        norm_rope8(xk, w_k, c, s, eps);
+        if (h < H) {
+          const size_t dst = ((static_cast<size_t>(b) * H + h) * N + n) * kHeadDim + sub * 8;
+          *reinterpret_cast<uint2*>(q8 + dst) = quant8(xq, inv_scale_of(am[3 * h + 0]));
+          *reinterpret_cast<uint2*>(k8 + dst) = quant8(xk, inv_scale_of(am[3 * h + 1]));
+        }
       }
     }
   }
@@ -196,16 +201,27 @@ __global__ void __launch_bounds__(kQuantThreads)
     const float inv = inv_scale_of(am[3 * h + 2]);
     // Consecutive threads take consecutive tokens, so that the byte-wide
     // transposed stores of a warp fill consecutive bytes of one row.
-    for (int i = threadIdx.x; i < kQuantTokens * (kHeadDim / 8); i += blockDim.x) {
+    constexpr int kChunks = kQuantTokens * (kHeadDim / 8) / kQuantThreads;  // 16-byte pieces per thread
+    uint4 raw[kChunks];
+#pragma unroll
+    for (int r = 0; r < kChunks; ++r) {
+      const int i = threadIdx.x + r * kQuantThreads;
       const int t = i & (kQuantTokens - 1);  // token in the block
       const int d0 = (i / kQuantTokens) * 8; // first of 8 dims
       const int n = n0 + t;
+      raw[r] = make_uint4(0, 0, 0, 0);
+      if (n < N)
+        raw[r] = __ldg(reinterpret_cast<const uint4*>(v + ((static_cast<size_t>(b) * N + n) * H + h) * kHeadDim + d0));
+    }
+#pragma unroll
+    for (int r = 0; r < kChunks; ++r) {
+      const int i = threadIdx.x + r * kQuantThreads;
+      const int t = i & (kQuantTokens - 1);
+      const int d0 = (i / kQuantTokens) * 8;
       uint2 code = make_uint2(0, 0);
-      if (n < N) {
+      if (n0 + t < N) {
         float x[8];
-        unpack8(__ldg(reinterpret_cast<const uint4*>(v + ((static_cast<size_t>(b) * N + n) * H + h) * kHeadDim +
-                                                       d0)),
-                x);
+        unpack8(raw[r], x);
         code = quant8(x, inv);
       }
       const uint32_t w[2] = {code.x, code.y};

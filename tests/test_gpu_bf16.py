@@ -41,8 +41,13 @@ def test_tiny_every_row():
     compare(host_f64(out), want, BF16_MAX_ABS, BF16_MEAN_ABS, BF16_REL_RMS, "tiny_320")
 
 
-def test_prologue_matches_oracle():
-    w = synthetic.Workload("prologue_ragged", 2, 3, 5, 7, 9, 2, 3)
+@pytest.mark.parametrize("B,H,txt,ih,iw,rh,rw", [
+    (2, 3, 5, 7, 9, 2, 3),        # 148 tokens: fewer chunks than SMs
+    (2, 5, 17, 30, 40, 9, 11),    # 2632 tokens, odd H: every block walks several chunks of the ring
+    (1, 24, 512, 16, 16, 0, 0),   # the FLUX head count, 768 tokens
+])
+def test_prologue_matches_oracle(B, H, txt, ih, iw, rh, rw):
+    w = synthetic.Workload("prologue", B, H, txt, ih, iw, rh, rw)
     inp = synthetic.make_inputs(w)
     d = device_inputs(inp)
     n = inp.pos.shape[0]
