@@ -80,6 +80,8 @@ def _load():
             f = getattr(lib, name)
             f.restype = I
             f.argtypes = [P, P, P, I, I, I, I, P, P, P, D, D, P, I, P, L, P, I]
+        lib.oracle_qkv_rows.restype = I
+        lib.oracle_qkv_rows.argtypes = [P, P, P, I, I, I, I, I, P, P, P, D, D, P, P, L, P, P, P, I]
         lib.oracle_fp8_quantize_head_bf16.restype = I
         lib.oracle_fp8_quantize_head_bf16.argtypes = [P, P, P, I, I, I, I, P, P, P, D, D, P, I, I,
                                                       P, P, P, P, I]
@@ -201,3 +203,36 @@ def fp8_quantize_head(q, k, v, pos, w_q, w_k, b: int, h: int, eps: float = 1e-6,
     if rc != 0:
         raise ValueError("oracle_fp8_quantize_head failed: %d" % rc)
     return q8, k8, v8, sc
+
+
+def qkv_rows(x: np.ndarray, w: np.ndarray, bias: Optional[np.ndarray], n_tokens: int, pos: np.ndarray,
+             w_q: np.ndarray, w_k: np.ndarray, heads: int, rows: Optional[np.ndarray] = None,
+             eps: float = 1e-6, theta: float = 10000.0, axes: Sequence[int] = AXES_DEFAULT, nthreads: int = 0):
+    """QKV projection y = x W^T (+ bias) of the requested token rows, split into
+    heads, with RMSNorm + RoPE on Q and K (reading R6 of the C source).
+
+    x: uint16 bf16 bits [M, D] (M = B * N); w: uint16 bf16 bits [3 H d, D];
+    bias: float32 [3 H d] or None.  Returns (q, k, v), each float64
+    [R, H, d] for rows (int64 token indices; None = all M rows).
+    """
+    lib = _load()
+    M, D = x.shape
+    F = w.shape[0]
+    d = F // (3 * heads)
+    assert w.shape == (3 * heads * d, D) and M % n_tokens == 0
+    rows = np.arange(M, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    R = rows.shape[0]
+    out = [np.empty((R, heads, d), np.float64) for _ in range(3)]
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    w = np.ascontiguousarray(w, dtype=np.uint16)
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    pos = np.ascontiguousarray(pos, dtype=np.int32)
+    assert pos.shape == (n_tokens, 3)
+    wq = np.ascontiguousarray(w_q, dtype=np.float32)
+    wk = np.ascontiguousarray(w_k, dtype=np.float32)
+    rc = lib.oracle_qkv_rows(_ptr(x), _ptr(w), None if b is None else _ptr(b), M, D, heads, d, n_tokens,
+                             _ptr(pos), _ptr(wq), _ptr(wk), eps, theta, _ptr(_axes(axes)), _ptr(rows), R,
+                             _ptr(out[0]), _ptr(out[1]), _ptr(out[2]), nthreads)
+    if rc != 0:
+        raise ValueError("oracle_qkv_rows failed: %d" % rc)
+    return tuple(out)

@@ -20,6 +20,9 @@
  *     so attention consumes RMSNorm'ed, rotated Q and K; V is untouched.
  *   - same page, section "Quantized and sparse attention": the FP8 variant
  *     runs Q.K and P.V with FP8 Q, K and V (qk_dtype fp8, v_dtype fp8).
+ *   - same page, section "GEMM kernel optimisation": the QKV projection is
+ *     one GEMM of the hidden states with the stacked Q, K, V weights, and its
+ *     epilogue applies the query/key normalisation and RoPE (oracle_qkv_rows).
  *
  * Readings taken where the pages are silent:
  *   R1 RMSNorm over the head dimension d: y_i = x_i / sqrt(mean_j x_j^2 + eps) * w_i,
@@ -33,6 +36,11 @@
  *      amax = 0); codes are E4M3 (finite, max 448) rounded to nearest, ties
  *      to even, saturating; attention then runs exactly on the dequantised
  *      values code * scale.
+ *   R6 QKV projection: y = x W^T (+ b) with W [3 H d, D] (output features
+ *      first, as a linear layer stores it); y splits into Q (features
+ *      0 .. H d - 1), K (the next H d) and V (the last H d), head h owning
+ *      features h d .. h d + d - 1 of its part; Q and K then get R1-R3, V
+ *      nothing.
  *
  * Every loop below follows the definition directly: no tiling, no online
  * softmax, no reordering beyond summation order inside a dot product.
@@ -358,5 +366,56 @@ int oracle_fp8_quantize_head_bf16(const uint16_t* q, const uint16_t* k, const ui
   plain_head(t, &sv, b, h, N, H, d, nt);
   scales[2] = fp8_roundtrip(t, nd, v8);
   free(t);
+  return 0;
+}
+
+/* Reading R6: the QKV projection of the requested token rows, then the
+ * query/key normalisation and RoPE of each head.
+ *   x      bf16 bits [M, D] (M = B * N token rows, row m = b * N + n)
+ *   w      bf16 bits [3 H d, D];  bias  float [3 H d] or NULL
+ *   rows   nrows token rows m;  out_q, out_k, out_v  [nrows, H, d] doubles
+ * Token row m takes the position ids of n = m % N. */
+int oracle_qkv_rows(const uint16_t* x, const uint16_t* w, const float* bias, int M, int D, int H, int d,
+                    int N, const int32_t* pos, const float* wqf, const float* wkf, double eps,
+                    double theta, const int* axes, const int64_t* rows, int64_t nrows, double* out_q,
+                    double* out_k, double* out_v, int nt) {
+  double wq[1024], wk[1024];
+  if (check_axes(d, axes) || d > 1024 || M <= 0 || D <= 0 || H <= 0 || N <= 0 || M % N) return -1;
+  for (int64_t r = 0; r < nrows; ++r)
+    if (rows[r] < 0 || rows[r] >= M) return -2;
+  for (int i = 0; i < d; ++i) { wq[i] = wqf[i]; wk[i] = wkf[i]; }
+  nt = nthreads_or_max(nt);
+  const int F = 3 * H * d;
+  int64_t r;
+#pragma omp parallel for num_threads(nt) schedule(dynamic, 1)
+  for (r = 0; r < nrows; ++r) {
+    const int64_t m = rows[r];
+    const int64_t n = m % N;
+    double* y = (double*)malloc(sizeof(double) * F);
+    double* xr = (double*)malloc(sizeof(double) * D);
+    if (!y || !xr) {
+      free(y); free(xr);
+      for (int i = 0; i < H * d; ++i) out_q[r * H * d + i] = out_k[r * H * d + i] = out_v[r * H * d + i] = NAN;
+      continue;
+    }
+    for (int c = 0; c < D; ++c) xr[c] = bf16_to_f64(x[m * D + c]);
+    for (int o = 0; o < F; ++o) {
+      double acc = 0.0;
+      for (int c = 0; c < D; ++c) acc += xr[c] * bf16_to_f64(w[(int64_t)o * D + c]);
+      y[o] = acc + (bias ? (double)bias[o] : 0.0);
+    }
+    for (int h = 0; h < H; ++h) {
+      double* q = out_q + (r * H + h) * d;
+      double* k = out_k + (r * H + h) * d;
+      double* v = out_v + (r * H + h) * d;
+      rmsnorm_row(q, y + (int64_t)h * d, d, wq, eps);
+      rope_row(q, d, pos + 3 * n, theta, axes);
+      rmsnorm_row(k, y + (int64_t)(H + h) * d, d, wk, eps);
+      rope_row(k, d, pos + 3 * n, theta, axes);
+      for (int i = 0; i < d; ++i) v[i] = y[(int64_t)(2 * H + h) * d + i];
+    }
+    free(y);
+    free(xr);
+  }
   return 0;
 }

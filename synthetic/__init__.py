@@ -23,6 +23,11 @@ Recipe (the same for every workload):
     uint16 bit pattern); the weights stay float32;
   * position ids per token: text (0, 0, 0), target image (0, row, col),
     reference image (1, row, col), row-major over each grid.
+
+QKV-projection inputs (make_qkv_inputs): hidden states x [B, N, D] standard
+normal, then the stacked weight W [3 H d, D] and bias [3 H d] drawn like a
+freshly initialised linear layer (uniform on +-1/sqrt(D)), then w_q, w_k as
+above; x and W are rounded to bf16, the bias stays float32.
 """
 from __future__ import annotations
 
@@ -167,3 +172,32 @@ def sample_rows(w: Workload, n_tokens: int, per_head: int, seed: int = 1) -> np.
             picks = set(edges) | set(rng.integers(0, n_tokens, per_head).tolist())
             rows.extend((b, h, n) for n in sorted(picks))
     return np.asarray(rows, dtype=np.int64)
+
+
+@dataclasses.dataclass
+class QKVInputs:
+    workload: Workload
+    d_model: int
+    x: np.ndarray      # uint16 bf16 bits [B * N, D]
+    w: np.ndarray      # uint16 bf16 bits [3 H d, D]
+    bias: np.ndarray   # float32 [3 H d]
+    w_q: np.ndarray    # float32 [d]
+    w_k: np.ndarray
+    pos: np.ndarray    # int32 [N, 3]
+
+
+def make_qkv_inputs(w: Workload, d_model: Optional[int] = None, seed: int = 0) -> QKVInputs:
+    """Seeded inputs of the QKV projection for workload ``w``; the hidden size
+    defaults to H * d (3072 for the FLUX workloads)."""
+    D = d_model or w.heads * w.head_dim
+    n = w.tokens
+    F = 3 * w.heads * w.head_dim
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((w.batch * n, D), dtype=np.float32)
+    lim = np.float32(1.0 / np.sqrt(D))
+    wt = rng.uniform(-lim, lim, (F, D)).astype(np.float32)
+    bias = rng.uniform(-lim, lim, F).astype(np.float32)
+    w_q = (1.0 + 0.1 * rng.standard_normal(w.head_dim)).astype(np.float32)
+    w_k = (1.0 + 0.1 * rng.standard_normal(w.head_dim)).astype(np.float32)
+    return QKVInputs(w, D, bf16_bits_from_f32(x), bf16_bits_from_f32(wt), bias, w_q, w_k,
+                     position_ids(w.txt_len, w.img_h, w.img_w, w.ref_h, w.ref_w))

@@ -16,7 +16,10 @@ What the checks compare the oracle with:
   * invariants: per-pair norms under RoPE, the output under a common shift
     of every position on one axis, permutation equivariance over tokens;
   * the E4M3 code table: every one of the 254 finite codes round-trips,
-    midpoints round to the even code, out-of-range values saturate.
+    midpoints round to the even code, out-of-range values saturate;
+  * the QKV projection: numpy's fp64 matmul (with torch rms_norm and the
+    complex-rotation RoPE on its Q and K parts), identity weights (the
+    prologue of x itself), a zero weight matrix (the bias alone).
 """
 from __future__ import annotations
 
@@ -388,6 +391,71 @@ def check_fp8_zero_head():
     assert np.all(sc == 1.0)
 
 
+# --------------------------------------------------------- QKV projection
+
+def _bf16(a):
+    bits = bf16_bits_from_f32(np.asarray(a, np.float32))
+    return bits, bf16_bits_to_f32(bits).astype(np.float64)
+
+
+def check_qkv_matches_numpy_matmul():
+    """x W^T + b by numpy in fp64, split into Q, K, V heads; Q and K through
+    torch rms_norm and the complex-rotation RoPE."""
+    rng = _rng(21)
+    B, N, H, Dm = 2, 5, 2, 96
+    pos = rng.integers(0, 30, (N, 3)).astype(np.int32)
+    xb, x = _bf16(rng.standard_normal((B * N, Dm)))
+    wb, w = _bf16(rng.standard_normal((3 * H * D, Dm)) / 8)
+    bias = rng.standard_normal(3 * H * D).astype(np.float32)
+    wq = (1.0 + 0.1 * rng.standard_normal(D)).astype(np.float32)
+    wk = (1.0 + 0.1 * rng.standard_normal(D)).astype(np.float32)
+    q, k, v = oracle.qkv_rows(xb, wb, bias, N, pos, wq, wk, H)
+    y = x @ w.T + bias.astype(np.float64)
+    parts = [y[:, i * H * D:(i + 1) * H * D].reshape(B, N, H, D) for i in range(3)]
+    want_q = lib_rope(lib_rms(parts[0], wq.astype(np.float64)), pos).reshape(B * N, H, D)
+    want_k = lib_rope(lib_rms(parts[1], wk.astype(np.float64)), pos).reshape(B * N, H, D)
+    _close(q, want_q, 1e-11, "QKV: Q vs numpy matmul + torch rms_norm + rotation")
+    _close(k, want_k, 1e-11, "QKV: K vs numpy matmul + torch rms_norm + rotation")
+    _close(v, parts[2].reshape(B * N, H, D), 1e-12, "QKV: V vs numpy matmul")
+
+
+def check_qkv_identity_weights():
+    """W_q = I, W_k = 2 I, W_v = I (D = H d), no bias: Q' is the prologue of x,
+    V is x."""
+    rng = _rng(22)
+    N, H = 7, 2
+    Dm = H * D
+    pos = _geometry(1, 2, 3)
+    xb, x = _bf16(rng.standard_normal((N, Dm)))
+    eye = np.eye(Dm)
+    wb, _ = _bf16(np.concatenate([eye, 2 * eye, eye], 0))
+    ones = np.ones(D, np.float32)
+    q, k, v = oracle.qkv_rows(xb, wb, None, N, pos, ones, ones, H)
+    xh = x.reshape(1, N, H, D)
+    _close(q, oracle.prologue(xh, pos, np.ones(D))[0], 1e-12, "QKV identity: Q")
+    _close(k, oracle.prologue(2 * xh, pos, np.ones(D))[0], 1e-12, "QKV identity: K")
+    _close(v, xh[0], 0.0, "QKV identity: V")
+
+
+def check_qkv_bias_only():
+    """W = 0: every token's V is the V part of the bias, Q' and K' the
+    normalised, rotated bias parts."""
+    rng = _rng(23)
+    N, H, Dm = 4, 3, 32
+    pos = _geometry(2, 1, 2)
+    xb, _ = _bf16(rng.standard_normal((N, Dm)))
+    wb, _ = _bf16(np.zeros((3 * H * D, Dm)))
+    bias = rng.standard_normal(3 * H * D).astype(np.float32)
+    ones = np.ones(D, np.float32)
+    q, k, v = oracle.qkv_rows(xb, wb, bias, N, pos, ones, ones, H)
+    bq, bk, bv = (bias.astype(np.float64)[i * H * D:(i + 1) * H * D].reshape(H, D) for i in range(3))
+    _close(v, np.broadcast_to(bv, (N, H, D)), 0.0, "QKV bias only: V")
+    bqn = np.broadcast_to(bq, (1, N, H, D)).copy()
+    _close(q, lib_rope(lib_rms(bqn, np.ones(D)), pos)[0], 1e-12, "QKV bias only: Q")
+    _close(k, lib_rope(lib_rms(np.broadcast_to(bk, (1, N, H, D)).copy(), np.ones(D)), pos)[0], 1e-12,
+           "QKV bias only: K")
+
+
 ALL_CHECKS = [
     check_e4m3_exhaustive_roundtrip,
     check_e4m3_matches_torch_cast,
@@ -410,4 +478,7 @@ ALL_CHECKS = [
     check_fp8_codes_and_scales,
     check_fp8_attention_on_dequantised_inputs,
     check_fp8_zero_head,
+    check_qkv_matches_numpy_matmul,
+    check_qkv_identity_weights,
+    check_qkv_bias_only,
 ]

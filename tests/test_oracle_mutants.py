@@ -31,6 +31,11 @@ MUTANTS = {
     "e4m3_subnormal_shift": ("double q = nearbyint(ldexp(a, 9));", "double q = nearbyint(ldexp(a, 8));"),
     "fp8_scale_240": ("amax > 0.0 ? amax / 448.0 : 1.0", "amax > 0.0 ? amax / 240.0 : 1.0"),
     "fp8_signed_amax": ("if (fabs(a[i]) > amax) amax = fabs(a[i]);", "if (a[i] > amax) amax = a[i];"),
+    "qkv_drop_bias": ("y[o] = acc + (bias ? (double)bias[o] : 0.0);", "y[o] = acc;"),
+    "qkv_swap_q_k": ("rmsnorm_row(q, y + (int64_t)h * d, d, wq, eps);", "rmsnorm_row(q, y + (int64_t)(H + h) * d, d, wq, eps);"),
+    "qkv_x_row_of_token": ("xr[c] = bf16_to_f64(x[m * D + c]);", "xr[c] = bf16_to_f64(x[n * D + c]);"),
+    "qkv_q_weights_everywhere": ("bf16_to_f64(w[(int64_t)o * D + c])", "bf16_to_f64(w[(int64_t)(o % (H * d)) * D + c])"),
+    "qkv_v_normalised": ("for (int i = 0; i < d; ++i) v[i] = y[(int64_t)(2 * H + h) * d + i];", "rmsnorm_row(v, y + (int64_t)(2 * H + h) * d, d, wk, eps);"),
 }
 
 
