@@ -68,6 +68,7 @@ def _load() -> ctypes.CDLL:
         "flux_attn_attend": (I, [P, P, P, P, I, P, P]),
         "flux_attn_prologue_fp8": (I, [P, P, P, P, I, I, I, I, I, P, P, P, P, P, P, P, P]),
         "flux_attn_attend_fp8": (I, [P, P, P, P, P, I, P, P]),
+        "flux_attn_qkv": (I, [P, P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, P]),
         "flux_attn_forward_noalloc": (I, [ctypes.POINTER(flux_attn_config), P, P, P, I, I, I, I, I, P, P, P, P,
                                           P, P]),
         "flux_attn_sync_status": (I, [P, P]),
@@ -167,6 +168,13 @@ def flux_attn_prologue_fp8(h, q, k, v, txt_len, img_h, img_w, ref_h, ref_w, pos_
 def flux_attn_attend_fp8(h, q8, k8, v8t, scales, n_tokens, out, stream=None) -> None:
     _check(_L().flux_attn_attend_fp8(h, _ptr(q8), _ptr(k8), _ptr(v8t), _ptr(scales), n_tokens, _ptr(out),
                                      _stream(stream)))
+
+
+def flux_attn_qkv(h, x, w_qkv, b_qkv, d_model, txt_len, img_h, img_w, ref_h, ref_w, pos_ids, q_norm_w, k_norm_w,
+                  qn, kn, v, stream=None) -> None:
+    _check(_L().flux_attn_qkv(h, _ptr(x), _ptr(w_qkv), _ptr(b_qkv), d_model, txt_len, img_h, img_w, ref_h, ref_w,
+                              _ptr(pos_ids), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(qn), _ptr(kn), _ptr(v),
+                              _stream(stream)))
 
 
 def make_config(batch: int, num_heads: int, max_tokens: int, head_dim: int = HEAD_DIM,
@@ -307,6 +315,36 @@ class FluxAttention:
         _require(out, torch.bfloat16, self._shape(n), "out")
         flux_attn_attend(self.handle, qn, kn, v, n, out, stream)
         return out
+
+    def qkv(self, x, w_qkv, b_qkv, txt_len: int, img_h: int, img_w: int, ref_h: int = 0, ref_w: int = 0,
+            q_norm_w=None, k_norm_w=None, pos_ids=None, qn=None, kn=None, v=None, stream=None):
+        """QKV projection with the fused QK-norm + RoPE epilogue: x bf16
+        [B, N, d_model] (or [B*N, d_model]), w_qkv bf16 [3 H 128, d_model],
+        b_qkv fp32 [3 H 128] or None.  Returns (qn, kn, v): bf16
+        [B, H, N, 128], [B, H, N, 128], [B, N, H, 128]."""
+        import torch
+        n = txt_len + img_h * img_w + ref_h * ref_w
+        B, H = self.batch, self.num_heads
+        d_model = x.shape[-1]
+        if x.dtype != torch.bfloat16 or not x.is_cuda or not x.is_contiguous() or x.numel() != B * n * d_model:
+            raise ValueError("x must be a contiguous CUDA bf16 tensor of B * N * d_model elements")
+        _require(w_qkv, torch.bfloat16, (3 * H * HEAD_DIM, d_model), "w_qkv")
+        if b_qkv is not None:
+            _require(b_qkv, torch.float32, (3 * H * HEAD_DIM,), "b_qkv")
+        _require(q_norm_w, torch.float32, (HEAD_DIM,), "q_norm_w")
+        _require(k_norm_w, torch.float32, (HEAD_DIM,), "k_norm_w")
+        if pos_ids is not None:
+            _require(pos_ids, torch.int32, (n, 3), "pos_ids")
+        hm = (B, H, n, HEAD_DIM)
+        qn = torch.empty(hm, dtype=torch.bfloat16, device=x.device) if qn is None else qn
+        kn = torch.empty(hm, dtype=torch.bfloat16, device=x.device) if kn is None else kn
+        v = torch.empty(self._shape(n), dtype=torch.bfloat16, device=x.device) if v is None else v
+        _require(qn, torch.bfloat16, hm, "qn")
+        _require(kn, torch.bfloat16, hm, "kn")
+        _require(v, torch.bfloat16, self._shape(n), "v")
+        flux_attn_qkv(self.handle, x, w_qkv, b_qkv, d_model, txt_len, img_h, img_w, ref_h, ref_w, pos_ids,
+                      q_norm_w, k_norm_w, qn, kn, v, stream)
+        return qn, kn, v
 
     def prologue_fp8(self, q, k, v, txt_len: int, img_h: int, img_w: int, ref_h: int = 0, ref_w: int = 0,
                      q_norm_w=None, k_norm_w=None, pos_ids=None, q8=None, k8=None, v8t=None, scales=None,

@@ -17,6 +17,7 @@
 #include "flux_attn.h"
 #include "attention.cuh"
 #include "prologue.cuh"
+#include "qkv_gemm.cuh"
 #include "quantize_fp8.cuh"
 
 struct flux_attn {
@@ -32,8 +33,9 @@ struct flux_attn {
   uint8_t* v8t;           // FP8: E4M3 [B, H, 128, pad16(max_tokens)]
   uint32_t* amax;         // FP8: [B, H, 3] fp32 bits
   float* scales;          // FP8: [B, H, 3]
+  float2* rope;           // BF16: (cos, sin) table [max_tokens][64] of the QKV projection
   uint32_t* err;          // device error word
-  flux::RopeTable rope;
+  flux::RopeTable rope_tab;
 };
 
 namespace {
@@ -154,7 +156,7 @@ int launch_prologue(flux_attn* h, const void* q, const void* k, int txt, int ih,
   const size_t smem = static_cast<size_t>(flux::kProStages) * 2 * T * H * flux::kHeadDim * 2;
   flux::qk_norm_rope_kernel<<<grid, flux::kPrologueThreads, smem, stream>>>(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), wq, wk, geo, B, n, H,
-      h->cfg.rms_eps, h->rope, qn, kn, h->err);
+      h->cfg.rms_eps, h->rope_tab, qn, kn, h->err);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "prologue launch");
   return FLUX_ATTN_OK;
@@ -177,12 +179,12 @@ int launch_prologue_fp8(flux_attn* h, const void* q, const void* k, const void* 
   const auto* kb = static_cast<const __nv_bfloat16*>(k);
   const auto* vb = static_cast<const __nv_bfloat16*>(v);
   flux::fp8_amax_kernel<<<grid, flux::kQuantThreads, 3 * H * sizeof(uint32_t), stream>>>(
-      qb, kb, vb, wq, wk, geo, n, H, h->cfg.rms_eps, h->rope, h->amax);
+      qb, kb, vb, wq, wk, geo, n, H, h->cfg.rms_eps, h->rope_tab, h->amax);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "amax launch");
   flux::fp8_quant_kernel<<<grid, flux::kQuantThreads, 0, stream>>>(qb, kb, vb, wq, wk, geo, n,
                                                                     static_cast<int>(pad16(n)), H, h->cfg.rms_eps,
-                                                                    h->rope, h->amax, q8, k8, v8t, scales);
+                                                                    h->rope_tab, h->amax, q8, k8, v8t, scales);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "quantise launch");
   return FLUX_ATTN_OK;
@@ -242,11 +244,66 @@ int launch_attention(flux_attn* h, bool fp8, const void* qn, const void* kn, con
   return FLUX_ATTN_OK;
 }
 
+// The QKV projection with its fused epilogue: the (cos, sin) table of the
+// call's tokens, then the persistent GEMM.
+int launch_qkv(flux_attn* h, const void* x, const void* w, const float* bias, int d_model, int txt, int ih, int iw,
+               int rw, const int32_t* pos, const float* wq, const float* wk, void* qn, void* kn, void* v, int n,
+               cudaStream_t stream) {
+  using namespace flux::qkv;
+  const int B = h->cfg.batch, H = h->cfg.num_heads;
+  const int M = B * n;
+  const int F = 3 * H * flux::kHeadDim;
+  flux::TokenGeometry geo{pos, txt, ih * iw, iw, rw};
+  const int pairs = n * (flux::kHeadDim / 2);
+  flux::qkv::rope_table_kernel<<<(pairs + 255) / 256, 256, 0, stream>>>(geo, n, h->rope_tab, h->rope);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "rope table launch");
+  CUtensorMap ta, tb;
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d_model), static_cast<cuuint64_t>(M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d_model) * 2};
+    const cuuint32_t box[2] = {BK, BM};
+    int rc = encode_tiled(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, dims, strides, box, "x");
+    if (rc) return rc;
+  }
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d_model), static_cast<cuuint64_t>(F)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d_model) * 2};
+    const cuuint32_t box[2] = {BK, BN};
+    int rc = encode_tiled(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w, dims, strides, box, "w_qkv");
+    if (rc) return rc;
+  }
+  Params p;
+  p.bias = bias;
+  p.wq = wq;
+  p.wk = wk;
+  p.rope = h->rope;
+  p.qn = static_cast<__nv_bfloat16*>(qn);
+  p.kn = static_cast<__nv_bfloat16*>(kn);
+  p.v = static_cast<__nv_bfloat16*>(v);
+  p.err = h->err;
+  p.M = M;
+  p.N = n;
+  p.H = H;
+  p.D = d_model;
+  p.m_tiles = (M + BM - 1) / BM;
+  p.n_tiles = (F + BN - 1) / BN;
+  p.eps = h->cfg.rms_eps;
+  const int tiles = p.m_tiles * p.n_tiles;
+  qkv_gemm_kernel<<<std::min(tiles, h->num_sms), THREADS, SMEM_BYTES, stream>>>(ta, tb, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "QKV GEMM launch");
+  return FLUX_ATTN_OK;
+}
+
 // Raise the dynamic shared-memory limit of the prologue and of both
 // attention kernels (per device).
 cudaError_t set_attention_smem_limits() {
   cudaError_t e = cudaFuncSetAttribute(flux::qk_norm_rope_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        flux::kProStages * flux::kProStageBytes);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(flux::qkv::qkv_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(flux::qkv::SMEM_BYTES));
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(flux::attn::attn_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(flux::attn::smem_bytes<false>()));
@@ -323,8 +380,8 @@ int flux_attn_create(const flux_attn_config* cfg, flux_attn_t* out) {
     int j = 0;
     for (int a = 0; a < 3; ++a)
       for (int jj = 0; jj < ax[a] / 2; ++jj, ++j) {
-        h->rope.freq[j] = static_cast<float>(std::pow(static_cast<double>(cfg->rope_theta), -2.0 * jj / ax[a]));
-        h->rope.axis[j] = a;
+        h->rope_tab.freq[j] = static_cast<float>(std::pow(static_cast<double>(cfg->rope_theta), -2.0 * jj / ax[a]));
+        h->rope_tab.axis[j] = a;
       }
   }
   // Workspace, each piece 256-byte aligned:
@@ -338,7 +395,8 @@ int flux_attn_create(const flux_attn_config* cfg, flux_attn_t* out) {
   const size_t qk_bytes = al(bh * cfg->max_tokens * flux::kHeadDim * (fp8 ? 1 : 2));
   const size_t vt_bytes = fp8 ? al(bh * flux::kHeadDim * pad16(cfg->max_tokens)) : 0;
   const size_t sc_bytes = fp8 ? al(bh * 3 * sizeof(float)) : 0;
-  const size_t err_off = 2 * qk_bytes + vt_bytes + 2 * sc_bytes;
+  const size_t rope_bytes = fp8 ? 0 : al(static_cast<size_t>(cfg->max_tokens) * (flux::kHeadDim / 2) * sizeof(float2));
+  const size_t err_off = 2 * qk_bytes + vt_bytes + 2 * sc_bytes + rope_bytes;
   h->ws_bytes = err_off + 256;
   e = cudaMalloc(&h->ws, h->ws_bytes);
   if (e != cudaSuccess) {
@@ -357,6 +415,7 @@ int flux_attn_create(const flux_attn_config* cfg, flux_attn_t* out) {
   } else {
     h->qn = reinterpret_cast<__nv_bfloat16*>(base);
     h->kn = reinterpret_cast<__nv_bfloat16*>(base + qk_bytes);
+    h->rope = reinterpret_cast<float2*>(base + 2 * qk_bytes);
   }
   h->err = reinterpret_cast<uint32_t*>(base + err_off);
   e = cudaMemset(h->err, 0, 256);
@@ -506,6 +565,38 @@ int flux_attn_attend_fp8(flux_attn_t h, const void* q8, const void* k8, const vo
   return launch_attention(h, true, q8, k8, v8t, scales, n_tokens, out, stream);
 }
 
+int flux_attn_qkv(flux_attn_t h, const void* x, const void* w_qkv, const float* b_qkv, int d_model, int txt_len,
+                  int img_h, int img_w, int ref_h, int ref_w, const int32_t* pos_ids, const float* q_norm_w,
+                  const float* k_norm_w, void* qn, void* kn, void* v, cudaStream_t stream) {
+  g_last_error.clear();
+  int rc = check_handle(h);
+  if (rc) return rc;
+  if (h->cfg.precision != FLUX_ATTN_BF16) return fail(FLUX_ATTN_ERR_UNSUPPORTED, "flux_attn_qkv needs a BF16 handle");
+  if (d_model < flux::qkv::BK || d_model % flux::qkv::BK || d_model > (1 << 16))
+    return fail(FLUX_ATTN_ERR_UNSUPPORTED, "d_model = %d must be a multiple of %d in [%d, 65536]", d_model,
+                flux::qkv::BK, flux::qkv::BK);
+  int n = 0;
+  if ((rc = token_count(h, txt_len, img_h, img_w, ref_h, ref_w, &n))) return rc;
+  if (n == 0) return FLUX_ATTN_OK;
+  const size_t M = static_cast<size_t>(h->cfg.batch) * n;
+  const size_t F = 3ull * h->cfg.num_heads * flux::kHeadDim;
+  if ((rc = check_buffer(x, M * d_model * 2, "x"))) return rc;
+  if ((rc = check_buffer(w_qkv, F * d_model * 2, "w_qkv"))) return rc;
+  if (b_qkv != nullptr && (rc = check_buffer(b_qkv, F * sizeof(float), "b_qkv"))) return rc;
+  if ((rc = check_buffer(q_norm_w, flux::kHeadDim * sizeof(float), "q_norm_w"))) return rc;
+  if ((rc = check_buffer(k_norm_w, flux::kHeadDim * sizeof(float), "k_norm_w"))) return rc;
+  if (pos_ids != nullptr && (rc = check_buffer(pos_ids, static_cast<size_t>(n) * 3 * sizeof(int32_t), "pos_ids")))
+    return rc;
+  const size_t bytes = row_bytes(h, n);
+  if ((rc = check_buffer(qn, bytes, "qn"))) return rc;
+  if ((rc = check_buffer(kn, bytes, "kn"))) return rc;
+  if ((rc = check_buffer(v, bytes, "v"))) return rc;
+  if (qn == kn || qn == v || kn == v || qn == x || kn == x || v == x)
+    return fail(FLUX_ATTN_ERR_INVALID_ARG, "qn, kn, v and x must be distinct buffers");
+  return launch_qkv(h, x, w_qkv, b_qkv, d_model, txt_len, img_h, img_w, ref_w, pos_ids, q_norm_w, k_norm_w, qn, kn,
+                    v, n, stream);
+}
+
 int flux_attn_sync_status(flux_attn_t h, cudaStream_t stream) {
   g_last_error.clear();
   int rc = check_handle(h);
@@ -632,8 +723,8 @@ extern "C" int flux_attn_forward_noalloc(const flux_attn_config* cfg, const void
     int j = 0;
     for (int a = 0; a < 3; ++a)
       for (int jj = 0; jj < ax[a] / 2; ++jj, ++j) {
-        view.rope.freq[j] = static_cast<float>(std::pow(static_cast<double>(cfg->rope_theta), -2.0 * jj / ax[a]));
-        view.rope.axis[j] = a;
+        view.rope_tab.freq[j] = static_cast<float>(std::pow(static_cast<double>(cfg->rope_theta), -2.0 * jj / ax[a]));
+        view.rope_tab.axis[j] = a;
       }
   }
   int n = 0;

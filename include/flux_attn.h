@@ -74,7 +74,7 @@ typedef enum {
 
 typedef struct {
   int batch;          /* B >= 1 */
-  int num_heads;      /* H >= 1 */
+  int num_heads;      /* 1 <= H <= 192 */
   int head_dim;       /* must be 128 */
   int max_tokens;     /* upper bound on N for every later call (sizes the workspace) */
   int axes_dim[3];    /* RoPE axis block sizes, even, summing to head_dim; FLUX uses 16, 56, 56 */
@@ -140,6 +140,24 @@ FLUX_ATTN_API int flux_attn_prologue_fp8(flux_attn_t h, const void* q, const voi
  * out bf16 [B, N, H, 128]. */
 FLUX_ATTN_API int flux_attn_attend_fp8(flux_attn_t h, const void* q8, const void* k8, const void* v8t,
                          const float* scales, int n_tokens, void* out, cudaStream_t stream);
+
+/* QKV projection with the query/key normalisation and RoPE fused into the
+ * GEMM epilogue ("Speed up image generation with FLUX 3 Image Klein on
+ * NVIDIA Blackwell GPUs", section "GEMM kernel optimisation"), BF16 handles:
+ *   y = x W^T (+ b),  y = [Q | K | V] with head h of each part owning features
+ *   h*128 .. h*128+127;  qn = RoPE(RMSNorm(Q) w_q), kn = RoPE(RMSNorm(K) w_k)
+ *   x       bf16 [B, N, d_model], token-major (row b*N + n)
+ *   w_qkv   bf16 [3 H 128, d_model] (a linear layer's [out, in] layout)
+ *   b_qkv   fp32 [3 H 128], or NULL for no bias
+ *   d_model a multiple of 64 in [64, 65536]
+ *   geometry, pos_ids, q_norm_w, k_norm_w: as for flux_attn_forward
+ *   qn, kn  bf16 [B, H, N, 128] (the layout flux_attn_attend reads)
+ *   v       bf16 [B, N, H, 128]
+ * Outputs must not overlap each other or x.  FLUX_ATTN_ERR_UNSUPPORTED on FP8
+ * handles and for other d_model. */
+FLUX_ATTN_API int flux_attn_qkv(flux_attn_t h, const void* x, const void* w_qkv, const float* b_qkv, int d_model,
+                  int txt_len, int img_h, int img_w, int ref_h, int ref_w, const int32_t* pos_ids,
+                  const float* q_norm_w, const float* k_norm_w, void* qn, void* kn, void* v, cudaStream_t stream);
 
 /* Allocation-free forward (BF16).  The pages this library follows have no
  * counterpart to this call; it exists for callers that must not allocate

@@ -1,0 +1,112 @@
+"""QKV projection with the fused QK-norm + RoPE epilogue against the fp64
+oracle (GPU).
+
+The GPU accumulates x W^T in fp32 over d_model products, applies bias, the
+RMSNorm and the rotation in fp32 and rounds once to bf16; the oracle does the
+same arithmetic in fp64.  So every output element must be within half a bf16
+ulp (2^-9 relative) plus the fp32 error, bounded here by 2^-8 |ref| + 1e-5.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic
+from gpu_util import dev_bf16, host_f64
+
+pytestmark = pytest.mark.gpu
+
+import diffusion_transformer_joint_txt_b300 as fa  # noqa: E402
+
+
+def _run(w, inp, bias=True, handle=None):
+    attn = handle or fa.FluxAttention(w.batch, w.heads, w.tokens)
+    x = dev_bf16(inp.x)
+    wt = dev_bf16(inp.w)
+    b = torch.from_numpy(inp.bias).cuda() if bias else None
+    qn, kn, v = attn.qkv(x, wt, b, w.txt_len, w.img_h, w.img_w, w.ref_h, w.ref_w,
+                         torch.from_numpy(inp.w_q).cuda(), torch.from_numpy(inp.w_k).cuda())
+    assert attn.sync_status() == 0
+    return attn, qn, kn, v
+
+
+def _check(got, want, what):
+    err = np.abs(got - want)
+    bound = 2.0 ** -8 * np.abs(want) + 1e-5
+    bad = err > bound
+    assert not bad.any(), "%s: %d of %d outside 2^-8 |ref| + 1e-5 (worst excess %.3e)" % (
+        what, int(bad.sum()), bad.size, float((err - bound).max()))
+
+
+def _compare(w, inp, qn, kn, v, rows=None, bias=True):
+    B, N, H = w.batch, w.tokens, w.heads
+    oq, ok, ov = oracle.qkv_rows(inp.x, inp.w, inp.bias if bias else None, N, inp.pos, inp.w_q, inp.w_k, H,
+                                 rows=rows)
+    m = np.arange(B * N) if rows is None else rows
+    b, n = m // N, m % N
+    gq = host_f64(qn)[b, :, n, :]          # [R, H, 128]
+    gk = host_f64(kn)[b, :, n, :]
+    gv = host_f64(v)[b, n, :, :]
+    _check(gq, oq, "Q'")
+    _check(gk, ok, "K'")
+    _check(gv, ov, "V")
+
+
+@pytest.mark.parametrize("B,H,txt,ih,iw,rh,rw,D,bias", [
+    (2, 2, 7, 5, 9, 0, 0, 256, True),       # N = 52: one partial token tile
+    (1, 3, 64, 16, 16, 2, 3, 192, False),   # odd H: a 256-wide tile straddles the Q/K and K/V boundaries
+    (2, 4, 100, 10, 12, 0, 0, 512, True),   # 440 tokens: several token tiles per weight tile
+])
+def test_qkv_every_element(B, H, txt, ih, iw, rh, rw, D, bias):
+    w = synthetic.Workload("qkv", B, H, txt, ih, iw, rh, rw)
+    inp = synthetic.make_qkv_inputs(w, D, seed=B * 10 + H)
+    _, qn, kn, v = _run(w, inp, bias)
+    _compare(w, inp, qn, kn, v, bias=bias)
+
+
+def test_qkv_flux_1024_sampled_rows():
+    w = synthetic.WORKLOADS["flux_1024_4608"]
+    inp = synthetic.make_qkv_inputs(w)
+    _, qn, kn, v = _run(w, inp)
+    rng = np.random.default_rng(3)
+    rows = np.unique(np.concatenate([[0, 127, 128, 511, 512, 4607], rng.integers(0, w.tokens, 40)]))
+    _compare(w, inp, qn, kn, v, rows=rows)
+
+
+def test_qkv_then_attend_matches_forward_on_the_projection():
+    """flux_attn_qkv + flux_attn_attend equals flux_attn_forward applied to the
+    (unnormalised) projection computed by torch on the GPU: the fused epilogue
+    and the prologue kernel agree."""
+    w = synthetic.Workload("qkv_chain", 1, 2, 30, 8, 8)
+    inp = synthetic.make_qkv_inputs(w, 256, seed=7)
+    attn, qn, kn, v = _run(w, inp)
+    out = attn.attend(qn, kn, v)
+    x = dev_bf16(inp.x).float()
+    y = x @ dev_bf16(inp.w).float().T + torch.from_numpy(inp.bias).cuda()
+    H, N = w.heads, w.tokens
+    q, k, vv = (y[:, i * H * 128:(i + 1) * H * 128].reshape(1, N, H, 128).to(torch.bfloat16) for i in range(3))
+    ref = attn.forward(q.contiguous(), k.contiguous(), vv.contiguous(), w.txt_len, w.img_h, w.img_w, 0, 0,
+                       torch.from_numpy(inp.w_q).cuda(), torch.from_numpy(inp.w_k).cuda())
+    assert attn.sync_status() == 0
+    diff = (out.float() - ref.float()).abs().max().item()
+    assert diff <= 2e-2, diff       # only the bf16 rounding of the projection before the prologue differs
+
+
+def test_qkv_rejects_bad_arguments():
+    w = synthetic.Workload("qkv_bad", 1, 2, 8, 2, 4)
+    inp = synthetic.make_qkv_inputs(w, 128)
+    attn = fa.FluxAttention(1, 2, w.tokens)
+    x, wt = dev_bf16(inp.x), dev_bf16(inp.w)
+    ones = torch.ones(128, device="cuda")
+    hm = torch.empty((1, 2, w.tokens, 128), dtype=torch.bfloat16, device="cuda")
+    vv = torch.empty((1, w.tokens, 2, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(fa.FluxAttnError) as e:      # d_model not a multiple of 64
+        fa.flux_attn_qkv(attn.handle, x, wt, None, 96, 8, 2, 4, 0, 0, None, ones, ones, hm, hm.clone(), vv)
+    assert e.value.status == fa.FLUX_ATTN_ERR_UNSUPPORTED
+    with pytest.raises(fa.FluxAttnError) as e:      # outputs alias
+        fa.flux_attn_qkv(attn.handle, x, wt, None, 128, 8, 2, 4, 0, 0, None, ones, ones, hm, hm, vv)
+    assert e.value.status == fa.FLUX_ATTN_ERR_INVALID_ARG
+    f8 = fa.FluxAttention(1, 2, w.tokens, precision="fp8")
+    with pytest.raises(fa.FluxAttnError) as e:
+        fa.flux_attn_qkv(f8.handle, x, wt, None, 128, 8, 2, 4, 0, 0, None, ones, ones, hm, hm.clone(), vv)
+    assert e.value.status == fa.FLUX_ATTN_ERR_UNSUPPORTED
