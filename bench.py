@@ -11,7 +11,9 @@ flux_attn_prologue + one flux_attn_attend call (= flux_attn_forward); L2 is
 flushed (a 256 MB write) before every timed step, outside the step's events.
 The FLUX 2048x2048 step (N=16896, BF16) and the FP8 classifier-free-guidance
 pair at 2048x2048 (B=2, N=16896: amax + E4M3 quantise + FP8 attention) are
-measured the same way and reported under "secondary".
+measured the same way and reported under "secondary"; the QKV projection
+with its fused QK-norm + RoPE epilogue (2 M F D flops: M = B N tokens,
+F = 3 H 128 features, D = H 128 hidden) is reported under "qkv_projection".
 
 One JSON line on rank 0.  Under torchrun every rank runs its own replica of
 the workload (the (batch, head) units are independent; no collective is on
@@ -212,6 +214,35 @@ class Step:
         return elems * (15 if self.fp8 else 8)
 
 
+class QKVStep:
+    """The QKV projection with its fused QK-norm + RoPE epilogue over one
+    workload (hidden size H * 128), inputs resident in HBM."""
+
+    def __init__(self, w, torch, fa):
+        self.w = w
+        inp = synthetic.make_qkv_inputs(w)
+        dev = lambda b: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).cuda()
+        self.x, self.wt = dev(inp.x), dev(inp.w)
+        self.bias = torch.from_numpy(inp.bias).cuda()
+        self.wq, self.wk = torch.from_numpy(inp.w_q).cuda(), torch.from_numpy(inp.w_k).cuda()
+        self.attn = fa.FluxAttention(w.batch, w.heads, w.tokens)
+        n, B, H = w.tokens, w.batch, w.heads
+        self.qn = torch.empty((B, H, n, 128), dtype=torch.bfloat16, device="cuda")
+        self.kn = torch.empty_like(self.qn)
+        self.v = torch.empty((B, n, H, 128), dtype=torch.bfloat16, device="cuda")
+        self.stream = torch.cuda.current_stream()
+        self.flops = 2 * B * n * (3 * H * 128) * inp.d_model
+
+    def __call__(self, ev=None):
+        if ev is not None:
+            ev[0].record(self.stream)
+        self.attn.qkv(self.x, self.wt, self.bias, self.w.txt_len, self.w.img_h, self.w.img_w, self.w.ref_h,
+                      self.w.ref_w, self.wq, self.wk, qn=self.qn, kn=self.kn, v=self.v)
+        if ev is not None:
+            ev[1].record(self.stream)
+            ev[2].record(self.stream)
+
+
 def measure(step, steps, warmup, torch, flush, barrier):
     """Mean step, attention-kernel and prologue times (ms) over `steps` timed
     steps; L2 is flushed before every step, outside its events."""
@@ -282,8 +313,20 @@ def run_ours(args):
         wall = time.perf_counter() - t0
         other_times = [slowest(list(measure(st, args.steps2, args.warmup, torch, flush, barrier)))
                        for st in others]
+        qkv_steps = [] if args.no_secondary else [QKVStep(synthetic.WORKLOADS[n], torch, fa) for n in args.qkv]
+        qkv_times = [slowest(list(measure(st, args.steps2, args.warmup, torch, flush, barrier)))
+                     for st in qkv_steps]
     main = summary(main_step, times, args.steps)
     secondary = [summary(st, t, args.steps2) for st, t in zip(others, other_times)]
+    qkv = []
+    for st, (s_ms, _, _) in zip(qkv_steps, qkv_times):
+        # one call = the (cos, sin) table kernel + the GEMM; both are in the time
+        tf = st.flops / (s_ms * 1e-3) / 1e12
+        qkv.append({"workload": st.w.name, "kernel": "qkv_gemm_kernel (+ rope_table_kernel)",
+                    "gemm": [st.w.batch * st.w.tokens, 3 * st.w.heads * 128, st.w.heads * 128],
+                    "ms": s_ms, "tflops": tf, "roofline_frac": tf / peak_bf16, "frac_of_2250_nominal": tf / 2250.0,
+                    "algorithmic_flops": st.flops, "gpu_launches": 2 * args.steps2})
+        st.attn.close()
 
     # end to end through the public API: pinned host inputs in, result back out, every step
     e2e = run_e2e(w, main_step.inp, main_step.attn, torch, args.e2e_steps, world, dist)
@@ -314,6 +357,7 @@ def run_ours(args):
         "wall_s_timed_region": wall,
         "cpu_baseline": cpu,
         "secondary": secondary,
+        "qkv_projection": qkv,
     }
     for st in [main_step] + others:
         st.attn.close()
@@ -458,7 +502,9 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--reference-rows", type=int, default=2048)
-    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--qkv", nargs="*", default=["flux_1024_4608", "flux_2048_16896"], choices=sorted(synthetic.WORKLOADS),
+                    help="workloads whose QKV projection (fused QK-norm + RoPE epilogue) is measured")
+    ap.add_argument("--no-secondary", action="store_true", help="measure the primary workload only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

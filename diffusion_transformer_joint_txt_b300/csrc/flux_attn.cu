@@ -288,6 +288,7 @@ int launch_qkv(flux_attn* h, const void* x, const void* w, const float* bias, in
   p.D = d_model;
   p.m_tiles = (M + BM - 1) / BM;
   p.n_tiles = (F + BN - 1) / BN;
+  p.group_m = group_rows(p.m_tiles, d_model);
   p.eps = h->cfg.rms_eps;
   const int tiles = p.m_tiles * p.n_tiles;
   qkv_gemm_kernel<<<std::min(tiles, h->num_sms), THREADS, SMEM_BYTES, stream>>>(ta, tb, p);

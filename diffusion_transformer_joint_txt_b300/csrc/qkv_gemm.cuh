@@ -66,6 +66,7 @@ struct Params {
   uint32_t* err;
   int M, N, H, D;           // tokens B*N, tokens per batch row, heads, hidden size
   int m_tiles, n_tiles;
+  int group_m;              // token tiles per group of the tile order
   float eps;
 };
 
@@ -102,11 +103,27 @@ __device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity, uint3
     }
 }
 
+// Tile order: groups of group_m token tiles; inside a group the token tile
+// varies fastest, then the weight block.  When all of x fits in L2 next to
+// the weights (4608 tokens: 28 MB) there is one group: every weight block is
+// then shared by all token tiles in flight.  When it does not (16896 tokens:
+// 104 MB), groups of 16 token tiles keep 12 MB of x resident while the group
+// walks all weight blocks; one group over all of x would stream x through L2
+// once per weight block.
+constexpr int GROUP_M = 16;
+constexpr size_t GROUP_X_BYTES = size_t(48) << 20;  // x rows that may form one group
+
+__host__ __device__ inline int group_rows(int m_tiles, int d_model) {
+  return static_cast<size_t>(m_tiles) * BM * d_model * 2 <= GROUP_X_BYTES ? m_tiles : GROUP_M;
+}
+
 __device__ __forceinline__ void tile_coords(const Params& p, int t, int& m0, int& n0) {
-  // consecutive tiles share their weight block (n) and walk the tokens (m)
-  const int nb = t / p.m_tiles;
-  m0 = (t - nb * p.m_tiles) * BM;
-  n0 = nb * BN;
+  const int per_group = p.group_m * p.n_tiles;
+  const int g = t / per_group;
+  const int rows = min(p.group_m, p.m_tiles - g * p.group_m);  // token tiles in this group
+  const int local = t - g * per_group;
+  m0 = (g * p.group_m + local % rows) * BM;
+  n0 = (local / rows) * BN;
 }
 
 __device__ __forceinline__ void producer(Smem& sm, const CUtensorMap* ta, const CUtensorMap* tb, const Params& p,
