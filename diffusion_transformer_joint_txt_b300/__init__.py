@@ -69,6 +69,7 @@ def _load() -> ctypes.CDLL:
         "flux_attn_prologue_fp8": (I, [P, P, P, P, I, I, I, I, I, P, P, P, P, P, P, P, P]),
         "flux_attn_attend_fp8": (I, [P, P, P, P, P, I, P, P]),
         "flux_attn_qkv": (I, [P, P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, P]),
+        "flux_attn_forward_hidden": (I, [P, P, P, P, I, I, I, I, I, I, P, P, P, P, P]),
         "flux_attn_forward_noalloc": (I, [ctypes.POINTER(flux_attn_config), P, P, P, I, I, I, I, I, P, P, P, P,
                                           P, P]),
         "flux_attn_sync_status": (I, [P, P]),
@@ -175,6 +176,13 @@ def flux_attn_qkv(h, x, w_qkv, b_qkv, d_model, txt_len, img_h, img_w, ref_h, ref
     _check(_L().flux_attn_qkv(h, _ptr(x), _ptr(w_qkv), _ptr(b_qkv), d_model, txt_len, img_h, img_w, ref_h, ref_w,
                               _ptr(pos_ids), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(qn), _ptr(kn), _ptr(v),
                               _stream(stream)))
+
+
+def flux_attn_forward_hidden(h, x, w_qkv, b_qkv, d_model, txt_len, img_h, img_w, ref_h, ref_w, pos_ids,
+                             q_norm_w, k_norm_w, out, stream=None) -> None:
+    _check(_L().flux_attn_forward_hidden(h, _ptr(x), _ptr(w_qkv), _ptr(b_qkv), d_model, txt_len, img_h, img_w,
+                                         ref_h, ref_w, _ptr(pos_ids), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(out),
+                                         _stream(stream)))
 
 
 def make_config(batch: int, num_heads: int, max_tokens: int, head_dim: int = HEAD_DIM,
@@ -345,6 +353,29 @@ class FluxAttention:
         flux_attn_qkv(self.handle, x, w_qkv, b_qkv, d_model, txt_len, img_h, img_w, ref_h, ref_w, pos_ids,
                       q_norm_w, k_norm_w, qn, kn, v, stream)
         return qn, kn, v
+
+    def forward_hidden(self, x, w_qkv, b_qkv, txt_len: int, img_h: int, img_w: int, ref_h: int = 0, ref_w: int = 0,
+                       q_norm_w=None, k_norm_w=None, pos_ids=None, out=None, stream=None):
+        """QKV projection (fused QK-norm + RoPE) and joint attention in one call;
+        returns out bf16 [B, N, H, 128]."""
+        import torch
+        n = txt_len + img_h * img_w + ref_h * ref_w
+        d_model = x.shape[-1]
+        if x.dtype != torch.bfloat16 or not x.is_cuda or not x.is_contiguous() or \
+                x.numel() != self.batch * n * d_model:
+            raise ValueError("x must be a contiguous CUDA bf16 tensor of B * N * d_model elements")
+        _require(w_qkv, torch.bfloat16, (3 * self.num_heads * HEAD_DIM, d_model), "w_qkv")
+        if b_qkv is not None:
+            _require(b_qkv, torch.float32, (3 * self.num_heads * HEAD_DIM,), "b_qkv")
+        _require(q_norm_w, torch.float32, (HEAD_DIM,), "q_norm_w")
+        _require(k_norm_w, torch.float32, (HEAD_DIM,), "k_norm_w")
+        if pos_ids is not None:
+            _require(pos_ids, torch.int32, (n, 3), "pos_ids")
+        out = torch.empty(self._shape(n), dtype=torch.bfloat16, device=x.device) if out is None else out
+        _require(out, torch.bfloat16, self._shape(n), "out")
+        flux_attn_forward_hidden(self.handle, x, w_qkv, b_qkv, d_model, txt_len, img_h, img_w, ref_h, ref_w,
+                                 pos_ids, q_norm_w, k_norm_w, out, stream)
+        return out
 
     def prologue_fp8(self, q, k, v, txt_len: int, img_h: int, img_w: int, ref_h: int = 0, ref_w: int = 0,
                      q_norm_w=None, k_norm_w=None, pos_ids=None, q8=None, k8=None, v8t=None, scales=None,

@@ -28,6 +28,7 @@ struct flux_attn {
   void* ws;               // one allocation, carved below
   __nv_bfloat16* qn;      // BF16: [B, H, max_tokens, 128]
   __nv_bfloat16* kn;      // BF16: [B, H, max_tokens, 128]
+  __nv_bfloat16* vw;      // BF16: [B, max_tokens, H, 128], V of flux_attn_forward_hidden
   uint8_t* q8;            // FP8: E4M3 [B, H, max_tokens, 128]
   uint8_t* k8;            // FP8: E4M3 [B, H, max_tokens, 128]
   uint8_t* v8t;           // FP8: E4M3 [B, H, 128, pad16(max_tokens)]
@@ -397,7 +398,8 @@ int flux_attn_create(const flux_attn_config* cfg, flux_attn_t* out) {
   const size_t vt_bytes = fp8 ? al(bh * flux::kHeadDim * pad16(cfg->max_tokens)) : 0;
   const size_t sc_bytes = fp8 ? al(bh * 3 * sizeof(float)) : 0;
   const size_t rope_bytes = fp8 ? 0 : al(static_cast<size_t>(cfg->max_tokens) * (flux::kHeadDim / 2) * sizeof(float2));
-  const size_t err_off = 2 * qk_bytes + vt_bytes + 2 * sc_bytes + rope_bytes;
+  const size_t v_bytes = fp8 ? 0 : qk_bytes;
+  const size_t err_off = 2 * qk_bytes + vt_bytes + 2 * sc_bytes + rope_bytes + v_bytes;
   h->ws_bytes = err_off + 256;
   e = cudaMalloc(&h->ws, h->ws_bytes);
   if (e != cudaSuccess) {
@@ -417,6 +419,7 @@ int flux_attn_create(const flux_attn_config* cfg, flux_attn_t* out) {
     h->qn = reinterpret_cast<__nv_bfloat16*>(base);
     h->kn = reinterpret_cast<__nv_bfloat16*>(base + qk_bytes);
     h->rope = reinterpret_cast<float2*>(base + 2 * qk_bytes);
+    h->vw = reinterpret_cast<__nv_bfloat16*>(base + 2 * qk_bytes + rope_bytes);
   }
   h->err = reinterpret_cast<uint32_t*>(base + err_off);
   e = cudaMemset(h->err, 0, 256);
@@ -596,6 +599,26 @@ int flux_attn_qkv(flux_attn_t h, const void* x, const void* w_qkv, const float* 
     return fail(FLUX_ATTN_ERR_INVALID_ARG, "qn, kn, v and x must be distinct buffers");
   return launch_qkv(h, x, w_qkv, b_qkv, d_model, txt_len, img_h, img_w, ref_w, pos_ids, q_norm_w, k_norm_w, qn, kn,
                     v, n, stream);
+}
+
+int flux_attn_forward_hidden(flux_attn_t h, const void* x, const void* w_qkv, const float* b_qkv, int d_model,
+                             int txt_len, int img_h, int img_w, int ref_h, int ref_w, const int32_t* pos_ids,
+                             const float* q_norm_w, const float* k_norm_w, void* out, cudaStream_t stream) {
+  g_last_error.clear();
+  int rc = check_handle(h);
+  if (rc) return rc;
+  if (h->cfg.precision != FLUX_ATTN_BF16)
+    return fail(FLUX_ATTN_ERR_UNSUPPORTED, "flux_attn_forward_hidden needs a BF16 handle");
+  int n = 0;
+  if ((rc = token_count(h, txt_len, img_h, img_w, ref_h, ref_w, &n))) return rc;
+  if (n == 0) return FLUX_ATTN_OK;
+  if ((rc = check_buffer(out, row_bytes(h, n), "out"))) return rc;
+  if (out == x) return fail(FLUX_ATTN_ERR_INVALID_ARG, "out aliases x");
+  // the projection's own checks, with the handle's workspace as its outputs
+  rc = flux_attn_qkv(h, x, w_qkv, b_qkv, d_model, txt_len, img_h, img_w, ref_h, ref_w, pos_ids, q_norm_w, k_norm_w,
+                     h->qn, h->kn, h->vw, stream);
+  if (rc) return rc;
+  return launch_attention(h, false, h->qn, h->kn, h->vw, nullptr, n, out, stream);
 }
 
 int flux_attn_sync_status(flux_attn_t h, cudaStream_t stream) {

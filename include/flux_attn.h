@@ -87,8 +87,9 @@ typedef struct {
 typedef struct flux_attn* flux_attn_t;
 
 /* Create a handle on the current CUDA device: checks the device, allocates
- * the workspace for cfg->max_tokens (normalised Q/K, FP8 codes and scales,
- * the device error word).  *out receives the handle (NULL on failure). */
+ * the workspace for cfg->max_tokens (BF16: normalised Q'/K', a V buffer and
+ * the RoPE table of the QKV projection; FP8: codes and scales; both: the
+ * device error word).  *out receives the handle (NULL on failure). */
 FLUX_ATTN_API int flux_attn_create(const flux_attn_config* cfg, flux_attn_t* out);
 
 /* Destroy a handle and free its workspace.  The caller must have completed
@@ -158,6 +159,16 @@ FLUX_ATTN_API int flux_attn_attend_fp8(flux_attn_t h, const void* q8, const void
 FLUX_ATTN_API int flux_attn_qkv(flux_attn_t h, const void* x, const void* w_qkv, const float* b_qkv, int d_model,
                   int txt_len, int img_h, int img_w, int ref_h, int ref_w, const int32_t* pos_ids,
                   const float* q_norm_w, const float* k_norm_w, void* qn, void* kn, void* v, cudaStream_t stream);
+
+/* The front half of a FLUX-style block in one call (BF16 handles): the QKV
+ * projection with its fused QK-norm + RoPE epilogue (flux_attn_qkv), written
+ * to the handle's workspace, then the joint attention over it.
+ *   x, w_qkv, b_qkv, d_model, geometry, pos_ids, norm weights: as for flux_attn_qkv
+ *   out     bf16 [B, N, H, 128]; must not alias x */
+FLUX_ATTN_API int flux_attn_forward_hidden(flux_attn_t h, const void* x, const void* w_qkv, const float* b_qkv,
+                             int d_model, int txt_len, int img_h, int img_w, int ref_h, int ref_w,
+                             const int32_t* pos_ids, const float* q_norm_w, const float* k_norm_w, void* out,
+                             cudaStream_t stream);
 
 /* Allocation-free forward (BF16).  The pages this library follows have no
  * counterpart to this call; it exists for callers that must not allocate

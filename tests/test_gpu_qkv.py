@@ -110,3 +110,15 @@ def test_qkv_rejects_bad_arguments():
     with pytest.raises(fa.FluxAttnError) as e:
         fa.flux_attn_qkv(f8.handle, x, wt, None, 128, 8, 2, 4, 0, 0, None, ones, ones, hm, hm.clone(), vv)
     assert e.value.status == fa.FLUX_ATTN_ERR_UNSUPPORTED
+
+
+def test_forward_hidden_equals_qkv_then_attend():
+    w = synthetic.Workload("hidden", 2, 3, 20, 9, 13, 2, 2)
+    inp = synthetic.make_qkv_inputs(w, 384, seed=9)
+    attn, qn, kn, v = _run(w, inp)
+    want = attn.attend(qn, kn, v)
+    got = attn.forward_hidden(dev_bf16(inp.x), dev_bf16(inp.w), torch.from_numpy(inp.bias).cuda(), w.txt_len,
+                              w.img_h, w.img_w, w.ref_h, w.ref_w, torch.from_numpy(inp.w_q).cuda(),
+                              torch.from_numpy(inp.w_k).cuda())
+    assert attn.sync_status() == 0
+    assert torch.equal(got, want)
