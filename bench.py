@@ -60,6 +60,20 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(values, world, dist, torch, device):
+    """Element-wise max of per-rank timings (the slowest rank decides); the
+    identity on one rank.  `device` is "cuda" under NCCL, "cpu" under gloo."""
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_throughput(flops_per_rank, world, ms):
+    """Whole-job TFLOP/s: every rank runs its own replica of the workload."""
+    return flops_per_rank * world / (ms * 1e-3) / 1e12
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -285,10 +299,7 @@ def run_ours(args):
         torch.cuda.synchronize()
 
     def slowest(vals):
-        t = torch.tensor(vals, dtype=torch.float64, device="cuda")
-        if world > 1:
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return t.tolist()
+        return max_over_ranks(vals, world, dist, torch, "cuda")
 
     def summary(step, times, n_steps):
         w = step.w
@@ -297,7 +308,7 @@ def run_ours(args):
         nominal = 4500.0 if step.fp8 else 2250.0
         achieved = w.flops / (a_ms * 1e-3) / 1e12
         return {"workload": w.name, "precision": w.precision, "batch": w.batch, "heads": w.heads,
-                "tokens": w.tokens, "steps": n_steps, "value": w.flops * world / (s_ms * 1e-3) / 1e12,
+                "tokens": w.tokens, "steps": n_steps, "value": job_throughput(w.flops, world, s_ms),
                 "ms_per_step": s_ms, "attn_kernel_ms": a_ms, "attn_tflops": achieved,
                 "roofline_frac": achieved / peak, "peak_tflops": peak,
                 "frac_of_nominal": achieved / nominal, "nominal_tflops": nominal,
@@ -401,13 +412,10 @@ def run_e2e(w, inp, attn, torch, steps, world, dist):
     e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
-    t = torch.tensor([ms], dtype=torch.float64, device="cuda")
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms = float(t.item())
+    ms = max_over_ranks([ms], world, dist, torch, "cuda")[0]
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hwq, hwk))
     d2h = hout.numel() * hout.element_size()
-    return {"value": w.flops * world / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
+    return {"value": job_throughput(w.flops, world, ms), "unit": "TFLOP/s", "ms_per_step": ms,
             "steps": steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "gpu_launches": steps * attn.launches_per_forward(w.tokens)}
 
