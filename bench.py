@@ -120,7 +120,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -142,16 +142,17 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self):
-        sm, mx, reasons = [], [], set()
+    def summary(self, first=0, last=None):
+        sm, mx, pw, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        for line in self.lines[first:last]:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 8:
                 continue
             try:
                 sm.append(float(parts[0]))
                 mx.append(float(parts[1]))
+                pw.append(float(parts[2]))
             except ValueError:
                 continue
             for name, val in zip(names, parts[4:8]):
@@ -159,9 +160,8 @@ class ClockSampler:
                     reasons.add(name)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        # samples under load: the upper part of the distribution
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "power_w": statistics.median(pw),
+                "reasons": sorted(reasons), "samples": len(sm)}
 
 
 def device_inputs(w, torch):
@@ -257,6 +257,30 @@ class QKVStep:
             ev[2].record(self.stream)
 
 
+def sustained(step, seconds, torch, clocks):
+    """The attention kernel back to back for about `seconds` (no L2 flush):
+    the power-limited steady state, with the clocks and power of that window."""
+    for _ in range(5):
+        step.attend()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    step.attend()
+    torch.cuda.synchronize()
+    reps = max(10, int(seconds / max(time.perf_counter() - t0, 1e-5)))
+    first = len(clocks.lines)
+    e0.record(step.stream)
+    for _ in range(reps):
+        step.attend()
+    e1.record(step.stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    if step.attn.sync_status() != 0:
+        raise RuntimeError("device status error in the sustained run (%s)" % step.w.name)
+    return ms, reps, clocks.summary(first, len(clocks.lines))
+
+
 def measure(step, steps, warmup, torch, flush, barrier):
     """Mean step, attention-kernel and prologue times (ms) over `steps` timed
     steps; L2 is flushed before every step, outside its events."""
@@ -320,15 +344,30 @@ def run_ours(args):
     others = [] if args.no_secondary else [Step(synthetic.WORKLOADS[n], torch, fa) for n in args.secondary]
     with ClockSampler(local) as clocks:
         t0 = time.perf_counter()
+        c0 = len(clocks.lines)
         times = slowest(list(measure(main_step, args.steps, args.warmup, torch, flush, barrier)))
+        c1 = len(clocks.lines)
         wall = time.perf_counter() - t0
         other_times = [slowest(list(measure(st, args.steps2, args.warmup, torch, flush, barrier)))
                        for st in others]
+        sus = []
+        if args.sustained_seconds > 0:
+            for st in [main_step] + [o for o in others if o.w.precision == "bf16"]:
+                ms_s, reps_s, clk_s = sustained(st, args.sustained_seconds, torch, clocks)
+                sus.append((st, ms_s, reps_s, clk_s))
         qkv_steps = [] if args.no_secondary else [QKVStep(synthetic.WORKLOADS[n], torch, fa) for n in args.qkv]
         qkv_times = [slowest(list(measure(st, args.steps2, args.warmup, torch, flush, barrier)))
                      for st in qkv_steps]
     main = summary(main_step, times, args.steps)
     secondary = [summary(st, t, args.steps2) for st, t in zip(others, other_times)]
+    peak_sus = float(peaks.get("bf16_tflops_sustained", 0.0)) or None
+    sustained_lines = []
+    for st, ms_s, reps_s, clk_s in sus:
+        tf = st.w.flops / (ms_s * 1e-3) / 1e12
+        sustained_lines.append({"workload": st.w.name, "kernel": "attn_kernel<bf16>", "launches": reps_s, "ms": ms_s,
+                                "achieved": tf, "peak": peak_sus, "unit": "TFLOP/s",
+                                "frac": tf / peak_sus if peak_sus else None,
+                                "peak_kind": peak_kind + " bf16 sustained", "clocks": clk_s})
     qkv = []
     for st, (s_ms, _, _) in zip(qkv_steps, qkv_times):
         # one call = the (cos, sin) table kernel + the GEMM; both are in the time
@@ -364,11 +403,12 @@ def run_ours(args):
         "attn_kernel_ms": main["attn_kernel_ms"],
         "e2e": e2e,
         "gpu_launches": main["gpu_launches"],
-        "clocks": clocks.summary(),
+        "clocks": clocks.summary(c0, c1),
         "wall_s_timed_region": wall,
         "cpu_baseline": cpu,
         "secondary": secondary,
         "qkv_projection": qkv,
+        "roofline_sustained": sustained_lines,
     }
     for st in [main_step] + others:
         st.attn.close()
@@ -508,6 +548,9 @@ def main():
     ap.add_argument("--secondary", nargs="*", default=SECONDARY, choices=sorted(synthetic.WORKLOADS),
                     help="workloads measured after the primary one and reported under \"secondary\"")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--sustained-seconds", type=float, default=2.0,
+                    help="seconds of back-to-back attention launches per BF16 workload for the power-limited "
+                         "steady state (0 skips)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--reference-rows", type=int, default=2048)
     ap.add_argument("--qkv", nargs="*", default=["flux_1024_4608", "flux_2048_16896"], choices=sorted(synthetic.WORKLOADS),
