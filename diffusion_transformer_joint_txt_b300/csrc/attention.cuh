@@ -11,7 +11,8 @@
 //
 // One CTA = two 128-row query tiles (0 and 1) of one (b, h) that share every
 // K/V tile.  Warp roles:
-//   warps 0-3  softmax + epilogue of query tile 0 (thread r owns row r, TMEM lane r)
+//   warps 0-3  softmax + epilogue of query tile 0 (thread r owns row r, TMEM lane r;
+//              the output tile leaves through shared memory and a TMA store)
 //   warps 4-7  softmax + epilogue of query tile 1
 //   warp 8     TMA producer of the K ring
 //   warp 9     TMEM allocator and tcgen05.mma issuer (one elected lane)
@@ -333,7 +334,7 @@ __device__ __forceinline__ __half2 e4m3x2_value(uint32_t c) {
 // Softmax and epilogue of query tile `t` (128 threads, thread r = row r).
 template <bool FP8>
 __device__ __forceinline__ void softmax_epilogue(Smem<FP8>& sm, uint32_t tmem, const Params& prm, int b, int h,
-                                                 int row0, int t, volatile int* ab) {
+                                                 int row0, int t, volatile int* ab, const CUtensorMap* tm_o) {
   const int r = threadIdx.x & (BM - 1);
   const uint32_t lane_base = static_cast<uint32_t>(r & ~31) << 16;  // TMEM lanes of this warp
   const uint32_t s_addr = tmem + lane_base + col_s(t);
@@ -456,8 +457,17 @@ __device__ __forceinline__ void softmax_epilogue(Smem<FP8>& sm, uint32_t tmem, c
   if (!ok) return;
   tc_fence_after_sync();
   const float inv_l = out_scale / l;
-  const int row = row0 + r;
-  __nv_bfloat16* dst = prm.out + ((static_cast<size_t>(b) * N + row) * prm.H + h) * HD;
+  // O tile (bf16, 32 KB) -> shared memory that no MMA or copy touches any
+  // more, in the SW128 layout of the out tensor map: half c / 2 holds head
+  // dims 64 (c / 2) .., row r at byte 128 r, its 16-byte chunk k at position
+  // k ^ (r % 8).  BF16: the tile's own 32 KB Q buffer (its last QK completed
+  // before the PV that signalled o_full).  FP8: a Q tile is only 16 KB, so
+  // 32 KB of the K ring, idle once both tiles' last QK has completed (it
+  // precedes PV_0(last) in issue order).  Then one thread writes the two
+  // halves with TMA stores, which also clip rows >= N: whole 128-byte rows
+  // instead of each thread's 16-byte pieces of rows H x 256 bytes apart.
+  static_assert(!FP8 || Traits<FP8>::KST * Traits<FP8>::TILE >= TILES * 2 * HALF, "FP8 staging needs 64 KB of K ring");
+  uint8_t* stage = FP8 ? &sm.k[0][0] + t * 2 * HALF : sm.q[t];
 #pragma unroll
   for (int c = 0; c < HD / 32; ++c) {
     uint32_t o[32];
@@ -467,18 +477,28 @@ __device__ __forceinline__ void softmax_epilogue(Smem<FP8>& sm, uint32_t tmem, c
 #pragma unroll
     for (int i = 0; i < 16; ++i)
       w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-    if (row < N) {
-      uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+    const int half = c >> 1;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    for (int i = 0; i < 4; ++i) {
+      const int k = (c & 1) * 4 + i;  // 16-byte chunk within the 128-byte row of this half
+      *reinterpret_cast<uint4*>(stage + half * HALF + r * 128 + ((k ^ (r & 7)) << 4)) =
+          make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
     }
+  }
+  fence_proxy_async_smem();
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + t), "n"(BM) : "memory");
+  if (r == 0) {
+    tma_store_4d(tm_o, smem_u32(stage), 0, h, row0, b);          // rows >= N are clipped
+    tma_store_4d(tm_o, smem_u32(stage) + HALF, 64, h, row0, b);
+    bulk_commit();
+    bulk_wait_all();
   }
 }
 
 template <bool FP8>
 __global__ void __launch_bounds__(THREADS, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                const __grid_constant__ CUtensorMap tm_v, const Params prm) {
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o, const Params prm) {
   constexpr int KST = Traits<FP8>::KST, VST = Traits<FP8>::VST;
   extern __shared__ uint8_t smem_raw[];
   Smem<FP8>& sm =
@@ -535,7 +555,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncwarp();
   } else {
     const int t = warp >> 2;  // query tile of this warpgroup
-    if (!*ab) softmax_epilogue<FP8>(sm, tmem, prm, b, h, q0 + t * BM, t, ab);
+    if (!*ab) softmax_epilogue<FP8>(sm, tmem, prm, b, h, q0 + t * BM, t, ab, &tm_o);
   }
   tc_fence_before_sync();
   __syncthreads();

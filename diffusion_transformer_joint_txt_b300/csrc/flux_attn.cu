@@ -226,6 +226,16 @@ int launch_attention(flux_attn* h, bool fp8, const void* qn, const void* kn, con
     int rc = encode_tiled(&tv, dt, 4, v, dims, strides, box, "V");
     if (rc) return rc;
   }
+  CUtensorMap to;
+  {
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(HD), static_cast<cuuint64_t>(H),
+                                static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(B)};
+    const cuuint64_t strides[3] = {HD * 2ull, static_cast<cuuint64_t>(H) * HD * 2ull,
+                                   static_cast<cuuint64_t>(n) * H * HD * 2ull};
+    const cuuint32_t box[4] = {64, 1, BM, 1};
+    int rc = encode_tiled(&to, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, out, dims, strides, box, "out");
+    if (rc) return rc;
+  }
   Params prm;
   prm.out = static_cast<__nv_bfloat16*>(out);
   prm.err = h->err;
@@ -237,9 +247,9 @@ int launch_attention(flux_attn* h, bool fp8, const void* qn, const void* kn, con
   prm.debug = h->cfg.debug_flags;
   const dim3 grid((n + CTA_ROWS - 1) / CTA_ROWS, B * H);
   if (fp8)
-    attn_kernel<true><<<grid, THREADS, smem_bytes<true>(), stream>>>(tq, tk, tv, prm);
+    attn_kernel<true><<<grid, THREADS, smem_bytes<true>(), stream>>>(tq, tk, tv, to, prm);
   else
-    attn_kernel<false><<<grid, THREADS, smem_bytes<false>(), stream>>>(tq, tk, tv, prm);
+    attn_kernel<false><<<grid, THREADS, smem_bytes<false>(), stream>>>(tq, tk, tv, to, prm);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   return FLUX_ATTN_OK;
