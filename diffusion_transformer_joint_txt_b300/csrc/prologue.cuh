@@ -215,21 +215,35 @@ __global__ void __launch_bounds__(kPrologueThreads, 1)
       // The whole warp works on one head pair at a time (norm_rope8 shuffles
       // across it); a half-warp past the last head computes on zeros and
       // stores nothing.
-      for (int hp = 2 * g; hp < H; hp += 2 * G) {
-        const int h = hp + half;
-        uint4 uq = make_uint4(0, 0, 0, 0), uk = uq;
-        if (h < H) {
-          uq = *reinterpret_cast<const uint4*>(sq + h * kHeadDim * 2);
-          uk = *reinterpret_cast<const uint4*>(sq + part + h * kHeadDim * 2);
+      // two head pairs per step: four independent rows, so that their
+      // shuffle reductions overlap
+      for (int hp = 2 * g; hp < H; hp += 4 * G) {
+        const int h0 = hp + half, h1 = hp + 2 * G + half;
+        uint4 uq0 = make_uint4(0, 0, 0, 0), uk0 = uq0, uq1 = uq0, uk1 = uq0;
+        if (h0 < H) {
+          uq0 = *reinterpret_cast<const uint4*>(sq + h0 * kHeadDim * 2);
+          uk0 = *reinterpret_cast<const uint4*>(sq + part + h0 * kHeadDim * 2);
         }
-        float xq[8], xk[8];
-        unpack8(uq, xq);
-        unpack8(uk, xk);
-        norm_rope8(xq, w_q, cs, sn, eps);
-        norm_rope8(xk, w_k, cs, sn, eps);
-        if (h < H) {
-          *reinterpret_cast<uint4*>(oq + h * head_stride) = pack8(xq);
-          *reinterpret_cast<uint4*>(ok_ + h * head_stride) = pack8(xk);
+        if (h1 < H) {
+          uq1 = *reinterpret_cast<const uint4*>(sq + h1 * kHeadDim * 2);
+          uk1 = *reinterpret_cast<const uint4*>(sq + part + h1 * kHeadDim * 2);
+        }
+        float xq0[8], xk0[8], xq1[8], xk1[8];
+        unpack8(uq0, xq0);
+        unpack8(uk0, xk0);
+        unpack8(uq1, xq1);
+        unpack8(uk1, xk1);
+        norm_rope8(xq0, w_q, cs, sn, eps);
+        norm_rope8(xk0, w_k, cs, sn, eps);
+        norm_rope8(xq1, w_q, cs, sn, eps);
+        norm_rope8(xk1, w_k, cs, sn, eps);
+        if (h0 < H) {
+          *reinterpret_cast<uint4*>(oq + h0 * head_stride) = pack8(xq0);
+          *reinterpret_cast<uint4*>(ok_ + h0 * head_stride) = pack8(xk0);
+        }
+        if (h1 < H) {
+          *reinterpret_cast<uint4*>(oq + h1 * head_stride) = pack8(xq1);
+          *reinterpret_cast<uint4*>(ok_ + h1 * head_stride) = pack8(xk1);
         }
       }
     }
