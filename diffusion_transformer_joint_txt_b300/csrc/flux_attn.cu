@@ -134,12 +134,13 @@ size_t row_bytes(const flux_attn* h, int n) {
 }
 
 int encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, cuuint32_t rank, const void* base,
-                 const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box, const char* what) {
+                 const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box, const char* what,
+                 CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   const Driver& d = driver();
   if (d.encode == nullptr) return fail(FLUX_ATTN_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   CUresult r = d.encode(map, dt, rank, const_cast<void*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(FLUX_ATTN_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed: %d", what, (int)r);
   return FLUX_ATTN_OK;
@@ -183,11 +184,35 @@ int launch_prologue_fp8(flux_attn* h, const void* q, const void* k, const void* 
       qb, kb, vb, wq, wk, geo, n, H, h->cfg.rms_eps, h->rope_tab, h->amax);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "amax launch");
-  flux::fp8_quant_kernel<<<grid, flux::kQuantThreads, 0, stream>>>(qb, kb, vb, wq, wk, geo, n,
-                                                                    static_cast<int>(pad16(n)), H, h->cfg.rms_eps,
-                                                                    h->rope_tab, h->amax, q8, k8, v8t, scales);
+  flux::fp8_quant_kernel<<<grid, flux::kQuantThreads, 0, stream>>>(qb, kb, wq, wk, geo, n, H, h->cfg.rms_eps,
+                                                                    h->rope_tab, h->amax, q8, k8, scales);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "quantise launch");
+  // V^T: TMA tiles of 64 tokens x 128 dims of one head, in and out
+  CUtensorMap tv, tvt;
+  {
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(flux::kHeadDim), static_cast<cuuint64_t>(H),
+                                static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(B)};
+    const cuuint64_t strides[3] = {flux::kHeadDim * 2ull, static_cast<cuuint64_t>(H) * flux::kHeadDim * 2ull,
+                                   static_cast<cuuint64_t>(n) * H * flux::kHeadDim * 2ull};
+    const cuuint32_t box[4] = {flux::kHeadDim, 1, flux::kVtTokens, 1};
+    int rc = encode_tiled(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, v, dims, strides, box, "V (tiles)",
+                          CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (rc) return rc;
+  }
+  {
+    const cuuint64_t np = pad16(n);
+    const cuuint64_t dims[3] = {np, static_cast<cuuint64_t>(flux::kHeadDim), static_cast<cuuint64_t>(B) * H};
+    const cuuint64_t strides[2] = {np, np * flux::kHeadDim};
+    const cuuint32_t box[3] = {flux::kVtTokens, flux::kHeadDim, 1};
+    int rc = encode_tiled(&tvt, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, v8t, dims, strides, box, "V^T (tiles)",
+                          CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (rc) return rc;
+  }
+  const dim3 vgrid((n + flux::kVtTokens - 1) / flux::kVtTokens, B * H);
+  flux::fp8_vt_kernel<<<vgrid, flux::kVtThreads, 0, stream>>>(tv, tvt, H, h->amax, h->err);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "V^T launch");
   return FLUX_ATTN_OK;
 }
 
@@ -458,9 +483,10 @@ size_t flux_attn_workspace_bytes(flux_attn_t h) { return h ? h->ws_bytes : 0; }
 
 int flux_attn_launches_per_forward(flux_attn_t h, int n_tokens) {
   if (h == nullptr || n_tokens <= 0) return 0;
-  // BF16: prologue + attention; FP8: amax + quantise + attention (the amax
-  // zeroing is a cudaMemsetAsync, not a kernel of this library).
-  return h->cfg.precision == FLUX_ATTN_FP8_E4M3 ? 3 : 2;
+  // BF16: prologue + attention; FP8: amax + Q'/K' codes + V^T codes +
+  // attention (the amax zeroing is a cudaMemsetAsync, not a kernel of this
+  // library).
+  return h->cfg.precision == FLUX_ATTN_FP8_E4M3 ? 4 : 2;
 }
 
 static int check_common(flux_attn* h, const void* q, const void* k, int txt, int ih, int iw, int rh, int rw,

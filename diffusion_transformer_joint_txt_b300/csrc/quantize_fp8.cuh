@@ -16,10 +16,11 @@
 //                     bits is a float max).  amax must be zero on entry.
 //   fp8_quant_kernel  recomputes Q', K', scales and writes
 //                       q8, k8   E4M3 [B, H, N, 128]
-//                       v8t      E4M3 [B, H, 128, Npad]  (V transposed, keys
-//                                contiguous; columns N..Npad-1 zero)
 //                       scales   fp32 [B, H, 3] = (s_q, s_k, s_v)
-// Both take one block of 256 threads per 64 consecutive tokens of one batch
+//   fp8_vt_kernel     v8t      E4M3 [B, H, 128, Npad]  (V transposed, keys
+//                                contiguous; columns N..Npad-1 zero), with
+//                                TMA tile loads and stores
+// The first two take one block of 256 threads per 64 consecutive tokens of one batch
 // row; inside it a warp handles one token at a time (a half-warp per head
 // row, 8 elements per lane, as in the BF16 prologue), eight heads per step
 // with all of their loads issued before the arithmetic.
@@ -132,17 +133,12 @@ __global__ void __launch_bounds__(kQuantThreads)
     if (s_amax[i] != 0u) atomicMax(&amax[static_cast<size_t>(b) * H * 3 + i], s_amax[i]);
 }
 
-// Row pitch (bytes) of the transposed V staging tile: 64 tokens + 16 bytes of
-// padding (keeps 16-byte alignment of every row for the vector read-out).
-constexpr int kVtPitch = kQuantTokens + 16;
-
 __global__ void __launch_bounds__(kQuantThreads)
     fp8_quant_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
-                     const __nv_bfloat16* __restrict__ v, const float* __restrict__ wq,
-                     const float* __restrict__ wk, TokenGeometry geo, int N, int npad, int H, float eps,
+                     const float* __restrict__ wq, const float* __restrict__ wk, TokenGeometry geo, int N, int H,
+                     float eps,
                      RopeTable tab, const uint32_t* __restrict__ amax, uint8_t* __restrict__ q8,
-                     uint8_t* __restrict__ k8, uint8_t* __restrict__ v8t, float* __restrict__ scales) {
-  __shared__ __align__(16) uint8_t s_vt[kHeadDim * kVtPitch];
+                     uint8_t* __restrict__ k8, float* __restrict__ scales) {
   const int b = blockIdx.y;
   const int n0 = blockIdx.x * kQuantTokens;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -194,49 +190,71 @@ __global__ void __launch_bounds__(kQuantThreads)
     }
   }
 
-  // V^T codes: per head, stage the [64 tokens x 128 dims] block transposed in
-  // shared memory, then write 128 rows of 64 keys.  Keys N .. npad-1 get zero.
-  const int n_here = min(kQuantTokens, npad - n0);  // columns of v8t this block owns (multiple of 16)
-  for (int h = 0; h < H; ++h) {
-    const float inv = inv_scale_of(am[3 * h + 2]);
-    // Consecutive threads take consecutive tokens, so that the byte-wide
-    // transposed stores of a warp fill consecutive bytes of one row.
-    constexpr int kChunks = kQuantTokens * (kHeadDim / 8) / kQuantThreads;  // 16-byte pieces per thread
-    uint4 raw[kChunks];
+}
+
+// V^T codes, one 64-token x 128-dim tile of one head per CTA (128 threads):
+// a TMA load brings V[b, n0 .. n0+63, h, :] into shared memory (tokens >= N
+// arrive as zeros), thread d quantises head dim d of the 64 tokens into 64
+// consecutive bytes of row d of the transposed tile, and one TMA store puts
+// the tile at v8t[b, h, :, n0 .. n0+63] (clipped at Npad; the zero tokens
+// between N and Npad become the zero padding).
+constexpr int kVtTokens = 64;
+constexpr int kVtThreads = 128;
+
+__global__ void __launch_bounds__(kVtThreads)
+    fp8_vt_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_vt, int H,
+                  const uint32_t* __restrict__ amax, uint32_t* err) {
+  __shared__ __align__(128) __nv_bfloat16 vin[kVtTokens][kHeadDim];  // 16 KB
+  __shared__ __align__(128) uint8_t vout[kHeadDim][kVtTokens];       // 8 KB
+  __shared__ uint64_t bar;
+  const int n0 = blockIdx.x * kVtTokens;
+  const int bh = blockIdx.y;
+  const int b = bh / H, h = bh - b * H;
+  const int d = threadIdx.x;
+  if (d == 0) {
+    mbar_init(&bar, 1);
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  if (d == 0) {
+    mbar_arrive_expect_tx(&bar, sizeof(vin));
+    tma_load_4d(smem_u32(vin), &tm_v, &bar, 0, h, n0, b);
+  }
+  // bounded wait on the load (every thread); a timeout leaves the tile unwritten
+  const uint32_t ba = smem_u32(&bar);
+  const uint64_t t0 = globaltimer_ns();
+  bool ok = true;
+  while (!mbar_try_wait(ba, 0))
+    if (globaltimer_ns() - t0 > kWaitLimitNs) { ok = false; break; }
+  if (__syncthreads_or(!ok)) {
+    if (d == 0) atomicOr(err, kErrTimeout);
+    // the copy may still land: keep the shared memory alive until it has (bounded)
+    const uint64_t t1 = globaltimer_ns();
+    while (!mbar_try_wait(ba, 0) && globaltimer_ns() - t1 < kWaitLimitNs) {}
+    return;
+  }
+  const float inv = inv_scale_of(amax[3 * bh + 2]);
+  uint32_t w[kVtTokens / 4];
 #pragma unroll
-    for (int r = 0; r < kChunks; ++r) {
-      const int i = threadIdx.x + r * kQuantThreads;
-      const int t = i & (kQuantTokens - 1);  // token in the block
-      const int d0 = (i / kQuantTokens) * 8; // first of 8 dims
-      const int n = n0 + t;
-      raw[r] = make_uint4(0, 0, 0, 0);
-      if (n < N)
-        raw[r] = __ldg(reinterpret_cast<const uint4*>(v + ((static_cast<size_t>(b) * N + n) * H + h) * kHeadDim + d0));
-    }
+  for (int t = 0; t < kVtTokens; t += 4) {
+    const float x0 = __bfloat162float(vin[t][d]) * inv, x1 = __bfloat162float(vin[t + 1][d]) * inv;
+    const float x2 = __bfloat162float(vin[t + 2][d]) * inv, x3 = __bfloat162float(vin[t + 3][d]) * inv;
+    w[t / 4] = __nv_cvt_float2_to_fp8x2(make_float2(x0, x1), __NV_SATFINITE, __NV_E4M3) |
+               (static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(x2, x3), __NV_SATFINITE, __NV_E4M3))
+                << 16);
+  }
 #pragma unroll
-    for (int r = 0; r < kChunks; ++r) {
-      const int i = threadIdx.x + r * kQuantThreads;
-      const int t = i & (kQuantTokens - 1);
-      const int d0 = (i / kQuantTokens) * 8;
-      uint2 code = make_uint2(0, 0);
-      if (n0 + t < N) {
-        float x[8];
-        unpack8(raw[r], x);
-        code = quant8(x, inv);
-      }
-      const uint32_t w[2] = {code.x, code.y};
-#pragma unroll
-      for (int e = 0; e < 8; ++e) s_vt[(d0 + e) * kVtPitch + t] = static_cast<uint8_t>(w[e >> 2] >> ((e & 3) * 8));
-    }
-    __syncthreads();
-    uint8_t* dst = v8t + (static_cast<size_t>(b) * H + h) * kHeadDim * static_cast<size_t>(npad) + n0;
-    const int chunks = n_here / 16;  // 16-byte pieces per row
-    for (int i = threadIdx.x; i < kHeadDim * chunks; i += blockDim.x) {
-      const int d = i / chunks, c = i - d * chunks;
-      *reinterpret_cast<uint4*>(dst + static_cast<size_t>(d) * npad + c * 16) =
-          *reinterpret_cast<const uint4*>(s_vt + d * kVtPitch + c * 16);
-    }
-    __syncthreads();
+  for (int c = 0; c < kVtTokens / 16; ++c)
+    reinterpret_cast<uint4*>(vout[d])[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __syncthreads();
+  if (d == 0) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(&tm_vt)),
+                 "r"(smem_u32(vout)), "r"(n0), "r"(0), "r"(bh)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   }
 }
 
