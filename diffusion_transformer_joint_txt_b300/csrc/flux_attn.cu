@@ -152,11 +152,11 @@ int launch_prologue(flux_attn* h, const void* q, const void* k, int txt, int ih,
   (void)rh;
   flux::TokenGeometry geo{pos, txt, ih * iw, iw, rw};
   const int B = h->cfg.batch, H = h->cfg.num_heads;
-  const int T = flux::prologue_chunk_tokens(H);
-  const long long chunks = (static_cast<long long>(B) * n + T - 1) / T;
-  const unsigned grid = static_cast<unsigned>(std::min<long long>(chunks, h->num_sms));
-  const size_t smem = static_cast<size_t>(flux::kProStages) * 2 * T * H * flux::kHeadDim * 2;
-  flux::qk_norm_rope_kernel<<<grid, flux::kPrologueThreads, smem, stream>>>(
+  const int W = flux::prologue_warps(H);
+  const long long units = (static_cast<long long>(B) * n + W - 1) / W;
+  const unsigned grid = static_cast<unsigned>(std::min<long long>(units, h->num_sms));
+  const size_t smem = static_cast<size_t>(W) * flux::kProStages * H * flux::kProRowBytes;
+  flux::qk_norm_rope_kernel<<<grid, 32 * W, smem, stream>>>(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), wq, wk, geo, B, n, H,
       h->cfg.rms_eps, h->rope_tab, qn, kn, h->err);
   cudaError_t e = cudaGetLastError();
@@ -337,7 +337,7 @@ int launch_qkv(flux_attn* h, const void* x, const void* w, const float* bias, in
 // attention kernels (per device).
 cudaError_t set_attention_smem_limits() {
   cudaError_t e = cudaFuncSetAttribute(flux::qk_norm_rope_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       flux::kProStages * flux::kProStageBytes);
+                                       flux::kProRingBytes);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(flux::qkv::qkv_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(flux::qkv::SMEM_BYTES));

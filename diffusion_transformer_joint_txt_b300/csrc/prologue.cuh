@@ -108,86 +108,123 @@ __device__ __forceinline__ uint4 pack8(const float (&x)[8]) {
   return u;
 }
 
-// Streaming layout: a persistent block per SM.  One producer warp copies
-// chunks of T consecutive tokens of q and of k -- T x H x 256 contiguous bytes
-// each, since a token's heads are adjacent in [B, N, H, 128] -- into a
-// two-stage shared-memory ring with single bulk copies.  The sixteen compute
-// warps split a chunk token by token: 16 / T warps per token, each taking
-// every (16 / T)-th head pair of it, so that a warp computes its token's
-// (cos, sin) pairs and (b, n) once per chunk and then only normalises,
-// rotates and stores rows (a half-warp per head row, read from shared memory,
-// written head-major).  The copies of the next chunk are in flight while a
-// chunk is computed.
-constexpr int kProWarps = 16;                        // compute warps
-constexpr int kProTokens = 8;                        // tokens per chunk at most
-constexpr int kPrologueThreads = 32 * (kProWarps + 1);
-constexpr int kProStages = 2;
-constexpr int kProStageBytes = 96 * 1024;            // q + k rows of one chunk
-constexpr int kProMaxHeads = kProStageBytes / (2 * kHeadDim * 2);  // 192: one token per chunk
-
-// Tokens per chunk for H heads (>= 1 for H <= kProMaxHeads).
-__host__ __device__ constexpr int prologue_chunk_tokens(int H) {
-  return kProStageBytes / (2 * kHeadDim * 2 * H) < kProTokens ? kProStageBytes / (2 * kHeadDim * 2 * H)
-                                                               : kProTokens;
+// (d0, d1) = (a0 b0, a1 b1) in one packed fp32x2 instruction.
+__device__ __forceinline__ void mul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 a, b, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
-__global__ void __launch_bounds__(kPrologueThreads, 1)
+// Per-lane coefficients of the weighted rotation.  With r the row's
+// reciprocal RMS, the weight w and the rotation (c, s) of pair (x0, x1) fold
+// into
+//   out0 = r (x0 w0 c - x1 w1 s),   out1 = r (x0 w0 s + x1 w1 c),
+// computed two pairs at a time in packed fp32x2 operations: lane pairs
+// (0, 1) and (2, 3) of its four, the even elements (x0 of each pair) in one
+// operand and the odd ones in the other.  m = 0, 1 picks the pair of pairs.
+struct RotCoef {
+  float a[4], b[4], c[4], d[4];  // [2m + e]: w0 c, -w1 s, w0 s, w1 c of pair 2m + e
+};
+
+__device__ __forceinline__ void rot_coef(const float (&w)[8], const float (&c)[4], const float (&s)[4],
+                                         RotCoef& k) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    k.a[i] = w[2 * i] * c[i];
+    k.b[i] = -w[2 * i + 1] * s[i];
+    k.c[i] = w[2 * i] * s[i];
+    k.d[i] = w[2 * i + 1] * c[i];
+  }
+}
+
+// RMSNorm, weight and rotation of the 8 elements a lane holds (a half-warp
+// holds the row), in packed fp32x2 arithmetic.
+__device__ __forceinline__ void norm_rope8_packed(float (&x)[8], const RotCoef& k, float eps) {
+  float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {
+    fma2(s0, s1, x[4 * m], x[4 * m + 2], x[4 * m], x[4 * m + 2], s0, s1);
+    fma2(s0, s1, x[4 * m + 1], x[4 * m + 3], x[4 * m + 1], x[4 * m + 3], s0, s1);
+  }
+  float ss = s0 + s1;
+#pragma unroll
+  for (int off = 8; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, off);
+  const float r = rsqrtf(ss * (1.0f / kHeadDim) + eps);
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {
+    const float e0 = x[4 * m], e1 = x[4 * m + 2];      // x0 of pairs 2m, 2m + 1
+    const float o0 = x[4 * m + 1], o1 = x[4 * m + 3];  // x1 of pairs 2m, 2m + 1
+    float u0, u1, v0, v1;
+    mul2(u0, u1, o0, o1, k.b[2 * m], k.b[2 * m + 1]);
+    fma2(u0, u1, e0, e1, k.a[2 * m], k.a[2 * m + 1], u0, u1);
+    mul2(v0, v1, o0, o1, k.d[2 * m], k.d[2 * m + 1]);
+    fma2(v0, v1, e0, e1, k.c[2 * m], k.c[2 * m + 1], v0, v1);
+    mul2(x[4 * m], x[4 * m + 2], u0, u1, r, r);
+    mul2(x[4 * m + 1], x[4 * m + 3], v0, v1, r, r);
+  }
+}
+
+// Streaming layout: a persistent block per SM of W warps (8 at the FLUX head
+// count), each streaming its own tokens through its own S-stage ring.  Warp w
+// of block x takes tokens t = W x + w, then every W * gridDim.x-th; lane 0
+// keeps the next S - 1 tokens in flight with two bulk copies per token (its
+// q and k rows, H x 256 contiguous bytes each, since a token's heads are
+// adjacent in [B, N, H, 128]) and refills a stage as soon as the warp has
+// read it.  No warp waits for another.  Per token the warp computes (b, n),
+// the (cos, sin) pairs and the rotation coefficients once, then normalises,
+// rotates and stores all of its head rows (a half-warp per row, read from
+// shared memory, written head-major).  Eight warps, one token each, beat
+// both a shared chunk ring fed by a producer warp and more, smaller warps on
+// B300 (fewer warps leave room for more independent rows per warp).
+constexpr int kProWarps = 8;                         // warps per block at most
+constexpr int kProStages = 2;                        // tokens per warp ring
+constexpr int kProRingBytes = 192 * 1024;            // all warps' rings
+constexpr int kProRowBytes = 2 * kHeadDim * 2;       // one head row of q and one of k
+constexpr int kProMaxHeads = kProRingBytes / (kProStages * kProRowBytes);  // 192: a single warp
+
+// Warps per block for H heads (1 .. kProWarps; H <= kProMaxHeads).
+__host__ __device__ constexpr int prologue_warps(int H) {
+  return kProRingBytes / (kProStages * kProRowBytes * H) < kProWarps
+             ? kProRingBytes / (kProStages * kProRowBytes * H)
+             : kProWarps;
+}
+
+__global__ void __launch_bounds__(32 * kProWarps, 1)
     qk_norm_rope_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                         const float* __restrict__ wq, const float* __restrict__ wk, TokenGeometry geo,
                         int B, int N, int H, float eps, RopeTable tab, __nv_bfloat16* __restrict__ qn,
                         __nv_bfloat16* __restrict__ kn, uint32_t* err) {
-  extern __shared__ __align__(128) uint8_t ring[];  // stage s: [T][H][128] q rows, then the same for k
-  __shared__ uint64_t full[kProStages], empty[kProStages];
+  extern __shared__ __align__(128) uint8_t ring[];  // [W][S][q rows | k rows], H x 256 bytes each
+  __shared__ uint64_t full[kProWarps][kProStages];  // per warp: stage s holds a token
   __shared__ int abort_flag;
-  const int T = prologue_chunk_tokens(H);
+  const int W = blockDim.x >> 5;
+  constexpr int S = kProStages;
+  const uint32_t row = static_cast<uint32_t>(H) * kHeadDim * 2;
   const long long tokens = static_cast<long long>(B) * N;
-  const int nchunks = static_cast<int>((tokens + T - 1) / T);
-  const uint32_t part = static_cast<uint32_t>(T) * H * kHeadDim * 2;  // bytes of q (or k) rows per stage
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* ab = &abort_flag;
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kProStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kProWarps);
-    }
-    abort_flag = 0;
+  if (threadIdx.x == 0) abort_flag = 0;
+  if (lane == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(&full[warp][s], 1);
     fence_mbarrier_init();
   }
   __syncthreads();
-
-  if (warp == kProWarps) {  // producer
-    if (lane == 0) {
-      int issued = 0;
-      for (int c = blockIdx.x, i = 0; c < nchunks; c += gridDim.x, ++i) {
-        const int s = i % kProStages;
-        const uint32_t u = i / kProStages;
-        if (u > 0 && !mbar_wait(&empty[s], (u - 1) & 1, ab, err)) break;
-        const long long t0 = static_cast<long long>(c) * T;
-        const uint32_t bytes = static_cast<uint32_t>(min(static_cast<long long>(T), tokens - t0)) * H * kHeadDim * 2;
-        const size_t off = static_cast<size_t>(t0) * H * kHeadDim;
-        mbar_arrive_expect_tx(&full[s], 2 * bytes);
-        bulk_load(smem_u32(ring + s * 2 * part), q + off, bytes, &full[s]);
-        bulk_load(smem_u32(ring + s * 2 * part + part), k + off, bytes, &full[s]);
-        ++issued;
-      }
-      for (int s = 0; s < kProStages; ++s) {  // no copy may still be writing when the block exits
-        const int cnt = issued > s ? (issued - s + kProStages - 1) / kProStages : 0;
-        if (cnt > 0) {
-          const uint32_t a = smem_u32(&full[s]);
-          const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait(a, (cnt - 1) & 1))
-            if (globaltimer_ns() - t0 > kWaitLimitNs) { atomicOr(err, kErrTimeout); break; }
-        }
-      }
+  uint8_t* wring = ring + static_cast<size_t>(warp) * S * 2 * row;
+  const long long first = static_cast<long long>(blockIdx.x) * W + warp;
+  const long long step = static_cast<long long>(gridDim.x) * W;
+  if (lane == 0)  // the warp's first S tokens
+    for (int j = 0; j < S; ++j) {
+      const long long t = first + j * step;
+      if (t >= tokens) break;
+      const size_t off = static_cast<size_t>(t) * H * kHeadDim;
+      mbar_arrive_expect_tx(&full[warp][j], 2 * row);
+      bulk_load(smem_u32(wring + j * 2 * row), q + off, row, &full[warp][j]);
+      bulk_load(smem_u32(wring + j * 2 * row + row), k + off, row, &full[warp][j]);
     }
-    return;
-  }
-
   const int sub = lane & 15;
   const int half = lane >> 4;
-  const int G = kProWarps / T;   // warps per token
-  const int tl = warp / G;       // this warp's token within each chunk (idle when >= T)
-  const int g = warp - tl * G;   // first head pair of this warp; step G
   float w_q[8], w_k[8];
   {
     const float4* a = reinterpret_cast<const float4*>(wq + sub * 8);
@@ -198,57 +235,76 @@ __global__ void __launch_bounds__(kPrologueThreads, 1)
     w_k[0] = b0.x; w_k[1] = b0.y; w_k[2] = b0.z; w_k[3] = b0.w;
     w_k[4] = b1.x; w_k[5] = b1.y; w_k[6] = b1.z; w_k[7] = b1.w;
   }
-  const size_t head_stride = static_cast<size_t>(N) * kHeadDim;  // elements between heads of Q' / K'
-  for (int c = blockIdx.x, i = 0; c < nchunks; c += gridDim.x, ++i) {
-    const int s = i % kProStages;
-    const bool ok = mbar_wait(&full[s], (i / kProStages) & 1, ab, err);
-    if (__any_sync(0xFFFFFFFFu, !ok)) break;
-    const long long token = static_cast<long long>(c) * T + tl;
-    if (tl < T && token < tokens) {
-      const int b = static_cast<int>(token / N);
-      const int n = static_cast<int>(token - static_cast<long long>(b) * N);
+  const size_t head_stride = static_cast<size_t>(N) * kHeadDim;
+  int j = 0;
+  bool aborted = false;
+  for (long long t = first; t < tokens; t += step, ++j) {
+    const int s = j % S;
+    const bool ok = mbar_wait(&full[warp][s], (j / S) & 1, ab, err);
+    if (__any_sync(0xFFFFFFFFu, !ok)) { aborted = true; break; }
+    const int b = static_cast<int>(t / N);
+    const int n = static_cast<int>(t - static_cast<long long>(b) * N);
+    RotCoef kq, kk;
+    {
       float cs[4], sn[4];
       lane_rotation(geo, tab, n, sub, cs, sn);
-      const uint8_t* sq = ring + s * 2 * part + (static_cast<size_t>(tl) * H * kHeadDim + sub * 8) * 2;
-      __nv_bfloat16* oq = qn + (static_cast<size_t>(b) * H * N + n) * kHeadDim + sub * 8;
-      __nv_bfloat16* ok_ = kn + (static_cast<size_t>(b) * H * N + n) * kHeadDim + sub * 8;
-      // The whole warp works on one head pair at a time (norm_rope8 shuffles
-      // across it); a half-warp past the last head computes on zeros and
-      // stores nothing.
-      // two head pairs per step: four independent rows, so that their
-      // shuffle reductions overlap
-      for (int hp = 2 * g; hp < H; hp += 4 * G) {
-        const int h0 = hp + half, h1 = hp + 2 * G + half;
-        uint4 uq0 = make_uint4(0, 0, 0, 0), uk0 = uq0, uq1 = uq0, uk1 = uq0;
-        if (h0 < H) {
-          uq0 = *reinterpret_cast<const uint4*>(sq + h0 * kHeadDim * 2);
-          uk0 = *reinterpret_cast<const uint4*>(sq + part + h0 * kHeadDim * 2);
-        }
-        if (h1 < H) {
-          uq1 = *reinterpret_cast<const uint4*>(sq + h1 * kHeadDim * 2);
-          uk1 = *reinterpret_cast<const uint4*>(sq + part + h1 * kHeadDim * 2);
-        }
-        float xq0[8], xk0[8], xq1[8], xk1[8];
-        unpack8(uq0, xq0);
-        unpack8(uk0, xk0);
-        unpack8(uq1, xq1);
-        unpack8(uk1, xk1);
-        norm_rope8(xq0, w_q, cs, sn, eps);
-        norm_rope8(xk0, w_k, cs, sn, eps);
-        norm_rope8(xq1, w_q, cs, sn, eps);
-        norm_rope8(xk1, w_k, cs, sn, eps);
-        if (h0 < H) {
-          *reinterpret_cast<uint4*>(oq + h0 * head_stride) = pack8(xq0);
-          *reinterpret_cast<uint4*>(ok_ + h0 * head_stride) = pack8(xk0);
-        }
-        if (h1 < H) {
-          *reinterpret_cast<uint4*>(oq + h1 * head_stride) = pack8(xq1);
-          *reinterpret_cast<uint4*>(ok_ + h1 * head_stride) = pack8(xk1);
-        }
+      rot_coef(w_q, cs, sn, kq);
+      rot_coef(w_k, cs, sn, kk);
+    }
+    const uint8_t* sq = wring + s * 2 * row + sub * 16;
+    __nv_bfloat16* oq = qn + (static_cast<size_t>(b) * H * N + n) * kHeadDim + sub * 8;
+    __nv_bfloat16* ok_ = kn + (static_cast<size_t>(b) * H * N + n) * kHeadDim + sub * 8;
+    // Two head pairs per step: four independent rows, so that their shuffle
+    // reductions overlap.  A half-warp past the last head computes on zeros
+    // and stores nothing.
+    for (int hp = 0; hp < H; hp += 4) {
+      const int h0 = hp + half, h1 = hp + 2 + half;
+      uint4 uq0 = make_uint4(0, 0, 0, 0), uk0 = uq0, uq1 = uq0, uk1 = uq0;
+      if (h0 < H) {
+        uq0 = *reinterpret_cast<const uint4*>(sq + h0 * kHeadDim * 2);
+        uk0 = *reinterpret_cast<const uint4*>(sq + row + h0 * kHeadDim * 2);
+      }
+      if (h1 < H) {
+        uq1 = *reinterpret_cast<const uint4*>(sq + h1 * kHeadDim * 2);
+        uk1 = *reinterpret_cast<const uint4*>(sq + row + h1 * kHeadDim * 2);
+      }
+      float xq0[8], xk0[8], xq1[8], xk1[8];
+      unpack8(uq0, xq0);
+      unpack8(uk0, xk0);
+      unpack8(uq1, xq1);
+      unpack8(uk1, xk1);
+      norm_rope8_packed(xq0, kq, eps);
+      norm_rope8_packed(xk0, kk, eps);
+      norm_rope8_packed(xq1, kq, eps);
+      norm_rope8_packed(xk1, kk, eps);
+      if (h0 < H) {
+        *reinterpret_cast<uint4*>(oq + h0 * head_stride) = pack8(xq0);
+        *reinterpret_cast<uint4*>(ok_ + h0 * head_stride) = pack8(xk0);
+      }
+      if (h1 < H) {
+        *reinterpret_cast<uint4*>(oq + h1 * head_stride) = pack8(xq1);
+        *reinterpret_cast<uint4*>(ok_ + h1 * head_stride) = pack8(xk1);
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
+    __syncwarp();   // every lane has read the stage: refill it with token j + S
+    if (lane == 0) {
+      const long long tn = t + S * step;
+      if (tn < tokens) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        const size_t off = static_cast<size_t>(tn) * H * kHeadDim;
+        mbar_arrive_expect_tx(&full[warp][s], 2 * row);
+        bulk_load(smem_u32(wring + s * 2 * row), q + off, row, &full[warp][s]);
+        bulk_load(smem_u32(wring + s * 2 * row + row), k + off, row, &full[warp][s]);
+      }
+    }
+  }
+  if (aborted && lane == 0) {  // loads still in flight must land before the block exits (bounded)
+    for (int jj = j; jj < j + S; ++jj) {
+      if (first + jj * step >= tokens) break;
+      const uint32_t a = smem_u32(&full[warp][jj % S]);
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(a, (jj / S) & 1) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+    }
   }
 }
 
