@@ -33,9 +33,9 @@
  *   R3 Norm first, then RoPE.
  *   R4 Softmax scale 1/sqrt(d).
  *   R5 FP8: per (batch, head) and per tensor, scale = amax / 448 (1 when
- *      amax = 0); codes are E4M3 (finite, max 448) rounded to nearest, ties
- *      to even, saturating; attention then runs exactly on the dequantised
- *      values code * scale.
+ *      amax = 0); codes are E4M3 (finite, max 448) of the real x / scale,
+ *      rounded to nearest, ties to even, saturating; attention then runs
+ *      exactly on the dequantised values code * scale.
  *   R6 QKV projection: y = x W^T (+ b) with W [3 H d, D] (output features
  *      first, as a linear layer stores it); y splits into Q (features
  *      0 .. H d - 1), K (the next H d) and V (the last H d), head h owning
@@ -169,13 +169,16 @@ static void plain_head(double* out, const src_t* x, int b, int h, int N, int H, 
 }
 
 /* Reading R5: per-tensor-per-head amax scale, quantise, dequantise in place.
- * codes (optional) receives the E4M3 codes. Returns the scale. */
+ * The code is E4M3 of the real quotient x / scale = 448 x / amax, formed as
+ * (448 x) / amax: rounding the scale first would move quotients that sit
+ * exactly halfway between two codes off the tie.  codes (optional) receives
+ * the E4M3 codes. Returns the scale. */
 static double fp8_roundtrip(double* a, int64_t count, uint8_t* codes) {
   double amax = 0.0;
   for (int64_t i = 0; i < count; ++i) if (fabs(a[i]) > amax) amax = fabs(a[i]);
   double scale = amax > 0.0 ? amax / 448.0 : 1.0;
   for (int64_t i = 0; i < count; ++i) {
-    uint8_t c = oracle_e4m3_encode(a[i] / scale);
+    uint8_t c = oracle_e4m3_encode(amax > 0.0 ? (448.0 * a[i]) / amax : a[i]);
     if (codes) codes[i] = c;
     a[i] = oracle_e4m3_decode(c) * scale;
   }

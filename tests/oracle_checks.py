@@ -354,10 +354,32 @@ def check_fp8_codes_and_scales():
             q8, k8, v8, sc = oracle.fp8_quantize_head(q, k, v, pos, wq, wk, b, h)
             for name, x, codes, s in (("q", qn, q8, sc[0]), ("k", kn, k8, sc[1]), ("v", vf, v8, sc[2])):
                 xs = x[b, :, h, :]
-                want_s = np.max(np.abs(xs)) / 448.0
+                amax = np.max(np.abs(xs))
+                want_s = amax / 448.0
                 assert abs(s - want_s) <= 1e-15 * want_s, "%s scale" % name
-                want = _torch_e4m3(xs / want_s).view(torch.uint8).numpy()
+                want = _torch_e4m3(448.0 * xs / amax).view(torch.uint8).numpy()
                 assert np.array_equal(codes, want), "%s codes differ from torch's cast" % name
+
+
+def check_fp8_codes_at_exact_ties():
+    """A quotient x / scale exactly halfway between two E4M3 codes takes the
+    even one.  With amax = 30.5, x = 183/2048 gives x / scale = 1.3125,
+    halfway between 1.25 (code 58, even mantissa) and 1.375 (code 59);
+    x = 183/512 gives 5.25, between 5.0 (code 74) and 5.5 (code 75).  Dividing
+    by a rounded scale (x / fl(amax / 448) = 1.3125000000000002) takes 59."""
+    q, k, v, pos, wq, wk = _fp8_inputs(20)
+    head = np.zeros((v.shape[1], D), np.float32)
+    head[0, 0] = 30.5
+    head[1, 5] = 183.0 / 2048
+    head[2, 7] = -183.0 / 2048
+    head[3, 9] = 183.0 / 512
+    head[4, 11] = 1.0 / 16        # 0.0625 * 448 / 30.5 = 0.918...: not a tie, rounds to 0.9375 (code 55)
+    v[0, :, 0, :] = bf16_bits_from_f32(head)
+    _, _, v8, sc = oracle.fp8_quantize_head(q, k, v, pos, wq, wk, 0, 0)
+    assert sc[2] == 30.5 / 448.0
+    assert v8[0, 0] == 0x7E and v8[1, 5] == 58 and v8[2, 7] == 0x80 | 58 and v8[3, 9] == 74
+    assert v8[4, 11] == 55
+    assert np.all(v8[5:] == 0)
 
 
 def check_fp8_attention_on_dequantised_inputs():
@@ -478,6 +500,7 @@ ALL_CHECKS = [
     check_fp8_codes_and_scales,
     check_fp8_attention_on_dequantised_inputs,
     check_fp8_zero_head,
+    check_fp8_codes_at_exact_ties,
     check_qkv_matches_numpy_matmul,
     check_qkv_identity_weights,
     check_qkv_bias_only,

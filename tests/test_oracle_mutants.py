@@ -30,6 +30,7 @@ MUTANTS = {
     "e4m3_saturate_nan": ("if (a >= 448.0) return (uint8_t)(sign | 0x7E);", "if (a >= 448.0) return (uint8_t)(sign | 0x7F);"),
     "e4m3_subnormal_shift": ("double q = nearbyint(ldexp(a, 9));", "double q = nearbyint(ldexp(a, 8));"),
     "fp8_scale_240": ("amax > 0.0 ? amax / 448.0 : 1.0", "amax > 0.0 ? amax / 240.0 : 1.0"),
+    "fp8_scale_first": ("oracle_e4m3_encode(amax > 0.0 ? (448.0 * a[i]) / amax : a[i])", "oracle_e4m3_encode(a[i] / scale)"),
     "fp8_signed_amax": ("if (fabs(a[i]) > amax) amax = fabs(a[i]);", "if (a[i] > amax) amax = a[i];"),
     "qkv_drop_bias": ("y[o] = acc + (bias ? (double)bias[o] : 0.0);", "y[o] = acc;"),
     "qkv_swap_q_k": ("rmsnorm_row(q, y + (int64_t)h * d, d, wq, eps);", "rmsnorm_row(q, y + (int64_t)(H + h) * d, d, wq, eps);"),
