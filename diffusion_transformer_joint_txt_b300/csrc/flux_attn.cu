@@ -156,9 +156,9 @@ int launch_prologue(flux_attn* h, const void* q, const void* k, int txt, int ih,
   const long long units = (static_cast<long long>(B) * n + W - 1) / W;
   const unsigned grid = static_cast<unsigned>(std::min<long long>(units, h->num_sms));
   const size_t smem = static_cast<size_t>(W) * flux::kProStages * H * flux::kProRowBytes;
-  flux::qk_norm_rope_kernel<<<grid, 32 * W, smem, stream>>>(
-      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), wq, wk, geo, B, n, H,
-      h->cfg.rms_eps, h->rope_tab, qn, kn, h->err);
+  const flux::StreamArgs a{static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), wq, wk,
+                           geo, B, n, H, h->cfg.rms_eps, h->rope_tab, h->err};
+  flux::qk_norm_rope_kernel<flux::Bf16Rows><<<grid, 32 * W, smem, stream>>>(a, flux::Bf16Rows{qn, kn});
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "prologue launch");
   return FLUX_ATTN_OK;
@@ -166,8 +166,8 @@ int launch_prologue(flux_attn* h, const void* q, const void* k, int txt, int ih,
 
 size_t pad16(int n) { return (static_cast<size_t>(n) + 15) & ~size_t(15); }
 
-// The two FP8 prologue passes: amax (after zeroing it), then the E4M3 codes
-// of Q', K' and of V transposed, and the scales.
+// The FP8 prologue: amax of V, Q', K' (after zeroing it), then the E4M3
+// codes of Q', K' and the scales, then the codes of V transposed.
 int launch_prologue_fp8(flux_attn* h, const void* q, const void* k, const void* v, int txt, int ih, int iw,
                         int rw, const int32_t* pos, const float* wq, const float* wk, int n, uint8_t* q8,
                         uint8_t* k8, uint8_t* v8t, float* scales, cudaStream_t stream) {
@@ -176,19 +176,7 @@ int launch_prologue_fp8(flux_attn* h, const void* q, const void* k, const void* 
   const size_t amax_bytes = static_cast<size_t>(B) * H * 3 * sizeof(uint32_t);
   cudaError_t e = cudaMemsetAsync(h->amax, 0, amax_bytes, stream);
   if (e != cudaSuccess) return cuda_fail(e, "clearing amax");
-  const dim3 grid((n + flux::kQuantTokens - 1) / flux::kQuantTokens, B);
-  const auto* qb = static_cast<const __nv_bfloat16*>(q);
-  const auto* kb = static_cast<const __nv_bfloat16*>(k);
-  const auto* vb = static_cast<const __nv_bfloat16*>(v);
-  flux::fp8_amax_kernel<<<grid, flux::kQuantThreads, 3 * H * sizeof(uint32_t), stream>>>(
-      qb, kb, vb, wq, wk, geo, n, H, h->cfg.rms_eps, h->rope_tab, h->amax);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e, "amax launch");
-  flux::fp8_quant_kernel<<<grid, flux::kQuantThreads, 0, stream>>>(qb, kb, wq, wk, geo, n, H, h->cfg.rms_eps,
-                                                                    h->rope_tab, h->amax, q8, k8, scales);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e, "quantise launch");
-  // V^T: TMA tiles of 64 tokens x 128 dims of one head, in and out
+  // V: TMA tiles of 64 tokens x 128 dims of one head, in (amax, V^T) and out (V^T)
   CUtensorMap tv, tvt;
   {
     const cuuint64_t dims[4] = {static_cast<cuuint64_t>(flux::kHeadDim), static_cast<cuuint64_t>(H),
@@ -210,6 +198,26 @@ int launch_prologue_fp8(flux_attn* h, const void* q, const void* k, const void* 
     if (rc) return rc;
   }
   const dim3 vgrid((n + flux::kVtTokens - 1) / flux::kVtTokens, B * H);
+  flux::fp8_vamax_kernel<<<vgrid, flux::kVtThreads, 0, stream>>>(tv, H, h->amax, h->err);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "V amax launch");
+  // Q', K': the prologue's stream kernel, once reducing to amax, once writing codes
+  const int W = flux::prologue_warps(H);
+  const long long units = (static_cast<long long>(B) * n + W - 1) / W;
+  const unsigned grid = static_cast<unsigned>(std::min<long long>(units, h->num_sms));
+  const size_t ring = static_cast<size_t>(W) * flux::kProStages * H * flux::kProRowBytes;
+  const flux::StreamArgs a{static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), wq, wk,
+                           geo, B, n, H, h->cfg.rms_eps, h->rope_tab, h->err};
+  flux::AmaxRows am{};
+  am.amax = h->amax;
+  flux::qk_norm_rope_kernel<flux::AmaxRows>
+      <<<grid, 32 * W, ring + flux::AmaxRows::scratch_bytes(W, H), stream>>>(a, am);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "amax launch");
+  const flux::E4m3Rows codes{q8, k8, h->amax, scales, H, B * H * 3};
+  flux::qk_norm_rope_kernel<flux::E4m3Rows><<<grid, 32 * W, ring, stream>>>(a, codes);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "quantise launch");
   flux::fp8_vt_kernel<<<vgrid, flux::kVtThreads, 0, stream>>>(tv, tvt, H, h->amax, h->err);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "V^T launch");
@@ -336,8 +344,15 @@ int launch_qkv(flux_attn* h, const void* x, const void* w, const float* bias, in
 // Raise the dynamic shared-memory limit of the prologue and of both
 // attention kernels (per device).
 cudaError_t set_attention_smem_limits() {
-  cudaError_t e = cudaFuncSetAttribute(flux::qk_norm_rope_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       flux::kProRingBytes);
+  cudaError_t e = cudaFuncSetAttribute(flux::qk_norm_rope_kernel<flux::Bf16Rows>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, flux::kProRingBytes);
+  if (e != cudaSuccess) return e;
+  // the amax policy's slots: W H <= 192 (the rings' bound) rows of 2 x 16 floats
+  e = cudaFuncSetAttribute(flux::qk_norm_rope_kernel<flux::AmaxRows>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           flux::kProRingBytes + static_cast<int>(flux::AmaxRows::scratch_bytes(1, flux::kProMaxHeads)));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(flux::qk_norm_rope_kernel<flux::E4m3Rows>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           flux::kProRingBytes);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(flux::qkv::qkv_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(flux::qkv::SMEM_BYTES));
@@ -483,10 +498,10 @@ size_t flux_attn_workspace_bytes(flux_attn_t h) { return h ? h->ws_bytes : 0; }
 
 int flux_attn_launches_per_forward(flux_attn_t h, int n_tokens) {
   if (h == nullptr || n_tokens <= 0) return 0;
-  // BF16: prologue + attention; FP8: amax + Q'/K' codes + V^T codes +
-  // attention (the amax zeroing is a cudaMemsetAsync, not a kernel of this
-  // library).
-  return h->cfg.precision == FLUX_ATTN_FP8_E4M3 ? 4 : 2;
+  // BF16: prologue + attention; FP8: V amax + Q'/K' amax + Q'/K' codes +
+  // V^T codes + attention (the amax zeroing is a cudaMemsetAsync, not a
+  // kernel of this library).
+  return h->cfg.precision == FLUX_ATTN_FP8_E4M3 ? 5 : 2;
 }
 
 static int check_common(flux_attn* h, const void* q, const void* k, int txt, int ih, int iw, int rh, int rw,

@@ -81,24 +81,6 @@ __device__ __forceinline__ void unpack8(const uint4& u, float (&x)[8]) {
   }
 }
 
-// RMSNorm over the 128 elements held by a half-warp, weight, then rotation.
-__device__ __forceinline__ void norm_rope8(float (&x)[8], const float (&w)[8], const float (&c)[4],
-                                           const float (&s)[4], float eps) {
-  float ss = 0.f;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) ss = fmaf(x[i], x[i], ss);
-#pragma unroll
-  for (int off = 8; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, off);
-  const float r = rsqrtf(ss * (1.0f / kHeadDim) + eps);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float y0 = x[2 * i] * r * w[2 * i];
-    const float y1 = x[2 * i + 1] * r * w[2 * i + 1];
-    x[2 * i] = y0 * c[i] - y1 * s[i];
-    x[2 * i + 1] = y0 * s[i] + y1 * c[i];
-  }
-}
-
 __device__ __forceinline__ uint4 pack8(const float (&x)[8]) {
   uint4 u;
   u.x = pack_bf16x2(x[0], x[1]);
@@ -182,6 +164,7 @@ constexpr int kProWarps = 8;                         // warps per block at most
 constexpr int kProStages = 2;                        // tokens per warp ring
 constexpr int kProRingBytes = 192 * 1024;            // all warps' rings
 constexpr int kProRowBytes = 2 * kHeadDim * 2;       // one head row of q and one of k
+constexpr int kProPairs = 2;                         // head pairs a warp works on at a time
 constexpr int kProMaxHeads = kProRingBytes / (kProStages * kProRowBytes);  // 192: a single warp
 
 // Warps per block for H heads (1 .. kProWarps; H <= kProMaxHeads).
@@ -191,18 +174,50 @@ __host__ __device__ constexpr int prologue_warps(int H) {
              : kProWarps;
 }
 
-__global__ void __launch_bounds__(32 * kProWarps, 1)
-    qk_norm_rope_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
-                        const float* __restrict__ wq, const float* __restrict__ wk, TokenGeometry geo,
-                        int B, int N, int H, float eps, RopeTable tab, __nv_bfloat16* __restrict__ qn,
-                        __nv_bfloat16* __restrict__ kn, uint32_t* err) {
-  extern __shared__ __align__(128) uint8_t ring[];  // [W][S][q rows | k rows], H x 256 bytes each
+// What the stream kernel does with the normalised, rotated rows.  Every
+// output policy has
+//   scratch_bytes(W, H)         shared memory it needs after the rings
+//   init(scratch, W, H)         once per warp (all lanes), before the first token
+//   token(b)                    warp-uniform, at every token (b its batch row)
+//   row(t, b, h, dst, x)        one lane's 8 values of row h of tensor t (0: Q',
+//                               1: K'); dst = element offset of those 8 values in
+//                               a head-major [B, H, N, 128] tensor
+//   finish()                    once per warp (all lanes), after the last token
+// The BF16 policy writes Q', K' bf16 [B, H, N, 128].
+struct Bf16Rows {
+  __nv_bfloat16* qn;
+  __nv_bfloat16* kn;
+  static __host__ __device__ size_t scratch_bytes(int, int) { return 0; }
+  __device__ __forceinline__ void init(uint8_t*, int, int) {}
+  __device__ __forceinline__ void token(int) {}
+  __device__ __forceinline__ void row(int t, int, int, size_t dst, const float (&x)[8]) {
+    *reinterpret_cast<uint4*>((t == 0 ? qn : kn) + dst) = pack8(x);
+  }
+  __device__ __forceinline__ void finish() {}
+};
+
+struct StreamArgs {
+  const __nv_bfloat16* q;  // [B, N, H, 128]
+  const __nv_bfloat16* k;
+  const float* wq;         // [128] RMSNorm weights
+  const float* wk;
+  TokenGeometry geo;
+  int B, N, H;
+  float eps;
+  RopeTable tab;
+  uint32_t* err;
+};
+
+template <class Out>
+__global__ void __launch_bounds__(32 * kProWarps, 1) qk_norm_rope_kernel(const StreamArgs a, Out out) {
+  extern __shared__ __align__(128) uint8_t ring[];  // [W][S][q rows | k rows], H x 256 bytes each; then Out's scratch
   __shared__ uint64_t full[kProWarps][kProStages];  // per warp: stage s holds a token
   __shared__ int abort_flag;
   const int W = blockDim.x >> 5;
   constexpr int S = kProStages;
+  const int H = a.H, N = a.N;
   const uint32_t row = static_cast<uint32_t>(H) * kHeadDim * 2;
-  const long long tokens = static_cast<long long>(B) * N;
+  const long long tokens = static_cast<long long>(a.B) * N;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* ab = &abort_flag;
   if (threadIdx.x == 0) abort_flag = 0;
@@ -214,76 +229,80 @@ __global__ void __launch_bounds__(32 * kProWarps, 1)
   uint8_t* wring = ring + static_cast<size_t>(warp) * S * 2 * row;
   const long long first = static_cast<long long>(blockIdx.x) * W + warp;
   const long long step = static_cast<long long>(gridDim.x) * W;
-  if (lane == 0)  // the warp's first S tokens
+  if (lane == 0) {  // the warp's first S tokens
     for (int j = 0; j < S; ++j) {
       const long long t = first + j * step;
       if (t >= tokens) break;
       const size_t off = static_cast<size_t>(t) * H * kHeadDim;
       mbar_arrive_expect_tx(&full[warp][j], 2 * row);
-      bulk_load(smem_u32(wring + j * 2 * row), q + off, row, &full[warp][j]);
-      bulk_load(smem_u32(wring + j * 2 * row + row), k + off, row, &full[warp][j]);
+      bulk_load(smem_u32(wring + j * 2 * row), a.q + off, row, &full[warp][j]);
+      bulk_load(smem_u32(wring + j * 2 * row + row), a.k + off, row, &full[warp][j]);
     }
+  }
+  out.init(ring + static_cast<size_t>(W) * S * 2 * row, W, H);
   const int sub = lane & 15;
   const int half = lane >> 4;
   float w_q[8], w_k[8];
   {
-    const float4* a = reinterpret_cast<const float4*>(wq + sub * 8);
-    const float4* bb = reinterpret_cast<const float4*>(wk + sub * 8);
-    const float4 a0 = __ldg(a), a1 = __ldg(a + 1), b0 = __ldg(bb), b1 = __ldg(bb + 1);
+    const float4* pa = reinterpret_cast<const float4*>(a.wq + sub * 8);
+    const float4* pb = reinterpret_cast<const float4*>(a.wk + sub * 8);
+    const float4 a0 = __ldg(pa), a1 = __ldg(pa + 1), b0 = __ldg(pb), b1 = __ldg(pb + 1);
     w_q[0] = a0.x; w_q[1] = a0.y; w_q[2] = a0.z; w_q[3] = a0.w;
     w_q[4] = a1.x; w_q[5] = a1.y; w_q[6] = a1.z; w_q[7] = a1.w;
     w_k[0] = b0.x; w_k[1] = b0.y; w_k[2] = b0.z; w_k[3] = b0.w;
     w_k[4] = b1.x; w_k[5] = b1.y; w_k[6] = b1.z; w_k[7] = b1.w;
   }
-  const size_t head_stride = static_cast<size_t>(N) * kHeadDim;
+  const size_t head_stride = static_cast<size_t>(N) * kHeadDim;  // elements between heads of Q' / K'
   int j = 0;
   bool aborted = false;
   for (long long t = first; t < tokens; t += step, ++j) {
     const int s = j % S;
-    const bool ok = mbar_wait(&full[warp][s], (j / S) & 1, ab, err);
+    const bool ok = mbar_wait(&full[warp][s], (j / S) & 1, ab, a.err);
     if (__any_sync(0xFFFFFFFFu, !ok)) { aborted = true; break; }
     const int b = static_cast<int>(t / N);
     const int n = static_cast<int>(t - static_cast<long long>(b) * N);
+    out.token(b);
     RotCoef kq, kk;
     {
       float cs[4], sn[4];
-      lane_rotation(geo, tab, n, sub, cs, sn);
+      lane_rotation(a.geo, a.tab, n, sub, cs, sn);
       rot_coef(w_q, cs, sn, kq);
       rot_coef(w_k, cs, sn, kk);
     }
     const uint8_t* sq = wring + s * 2 * row + sub * 16;
-    __nv_bfloat16* oq = qn + (static_cast<size_t>(b) * H * N + n) * kHeadDim + sub * 8;
-    __nv_bfloat16* ok_ = kn + (static_cast<size_t>(b) * H * N + n) * kHeadDim + sub * 8;
-    // Two head pairs per step: four independent rows, so that their shuffle
-    // reductions overlap.  A half-warp past the last head computes on zeros
-    // and stores nothing.
-    for (int hp = 0; hp < H; hp += 4) {
-      const int h0 = hp + half, h1 = hp + 2 + half;
-      uint4 uq0 = make_uint4(0, 0, 0, 0), uk0 = uq0, uq1 = uq0, uk1 = uq0;
-      if (h0 < H) {
-        uq0 = *reinterpret_cast<const uint4*>(sq + h0 * kHeadDim * 2);
-        uk0 = *reinterpret_cast<const uint4*>(sq + row + h0 * kHeadDim * 2);
+    const size_t dst = (static_cast<size_t>(b) * H * N + n) * kHeadDim + sub * 8;
+    // kProPairs head pairs per step: 2 kProPairs independent rows per
+    // half-warp, so that their shuffle reductions overlap.  A half-warp past
+    // the last head computes on zeros and stores nothing.
+    for (int hp = 0; hp < H; hp += 2 * kProPairs) {
+      uint4 uq[kProPairs], uk[kProPairs];
+#pragma unroll
+      for (int i = 0; i < kProPairs; ++i) {
+        const int h = hp + 2 * i + half;
+        uq[i] = uk[i] = make_uint4(0, 0, 0, 0);
+        if (h < H) {
+          uq[i] = *reinterpret_cast<const uint4*>(sq + h * kHeadDim * 2);
+          uk[i] = *reinterpret_cast<const uint4*>(sq + row + h * kHeadDim * 2);
+        }
       }
-      if (h1 < H) {
-        uq1 = *reinterpret_cast<const uint4*>(sq + h1 * kHeadDim * 2);
-        uk1 = *reinterpret_cast<const uint4*>(sq + row + h1 * kHeadDim * 2);
+      float xq[kProPairs][8], xk[kProPairs][8];
+#pragma unroll
+      for (int i = 0; i < kProPairs; ++i) {
+        unpack8(uq[i], xq[i]);
+        unpack8(uk[i], xk[i]);
       }
-      float xq0[8], xk0[8], xq1[8], xk1[8];
-      unpack8(uq0, xq0);
-      unpack8(uk0, xk0);
-      unpack8(uq1, xq1);
-      unpack8(uk1, xk1);
-      norm_rope8_packed(xq0, kq, eps);
-      norm_rope8_packed(xk0, kk, eps);
-      norm_rope8_packed(xq1, kq, eps);
-      norm_rope8_packed(xk1, kk, eps);
-      if (h0 < H) {
-        *reinterpret_cast<uint4*>(oq + h0 * head_stride) = pack8(xq0);
-        *reinterpret_cast<uint4*>(ok_ + h0 * head_stride) = pack8(xk0);
+#pragma unroll
+      for (int i = 0; i < kProPairs; ++i) {
+        norm_rope8_packed(xq[i], kq, a.eps);
+        norm_rope8_packed(xk[i], kk, a.eps);
       }
-      if (h1 < H) {
-        *reinterpret_cast<uint4*>(oq + h1 * head_stride) = pack8(xq1);
-        *reinterpret_cast<uint4*>(ok_ + h1 * head_stride) = pack8(xk1);
+#pragma unroll
+      for (int i = 0; i < kProPairs; ++i) {
+        const int h = hp + 2 * i + half;
+        if (h < H) {
+          out.row(0, b, h, dst + h * head_stride, xq[i]);
+          out.row(1, b, h, dst + h * head_stride, xk[i]);
+        }
       }
     }
     __syncwarp();   // every lane has read the stage: refill it with token j + S
@@ -293,19 +312,22 @@ __global__ void __launch_bounds__(32 * kProWarps, 1)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         const size_t off = static_cast<size_t>(tn) * H * kHeadDim;
         mbar_arrive_expect_tx(&full[warp][s], 2 * row);
-        bulk_load(smem_u32(wring + s * 2 * row), q + off, row, &full[warp][s]);
-        bulk_load(smem_u32(wring + s * 2 * row + row), k + off, row, &full[warp][s]);
+        bulk_load(smem_u32(wring + s * 2 * row), a.q + off, row, &full[warp][s]);
+        bulk_load(smem_u32(wring + s * 2 * row + row), a.k + off, row, &full[warp][s]);
       }
     }
   }
-  if (aborted && lane == 0) {  // loads still in flight must land before the block exits (bounded)
-    for (int jj = j; jj < j + S; ++jj) {
-      if (first + jj * step >= tokens) break;
-      const uint32_t a = smem_u32(&full[warp][jj % S]);
-      const uint64_t t0 = globaltimer_ns();
-      while (!mbar_try_wait(a, (jj / S) & 1) && globaltimer_ns() - t0 < kWaitLimitNs) {}
-    }
+  if (aborted) {
+    if (lane == 0)  // loads still in flight must land before the block exits (bounded)
+      for (int jj = j; jj < j + S; ++jj) {
+        if (first + jj * step >= tokens) break;
+        const uint32_t ba = smem_u32(&full[warp][jj % S]);
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(ba, (jj / S) & 1) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+      }
+    return;
   }
+  out.finish();
 }
 
 }  // namespace flux

@@ -60,8 +60,13 @@ def _codes_match(got: np.ndarray, want: np.ndarray, what: str):
         assert np.all(np.abs(a - b) <= step * 1.0001), what
 
 
-def test_fp8_prologue_codes_and_scales():
-    w = _fp8("fp8_prologue", 2, 3, 7, 5, 9, 2, 3)          # N = 58, Npad = 64
+@pytest.mark.parametrize("B,H,txt,ih,iw,rh,rw", [
+    (2, 3, 7, 5, 9, 2, 3),        # N = 58, Npad = 64: fewer tokens than warps of the grid
+    (2, 3, 80, 30, 40, 20, 36),   # N = 2000: every warp's tokens span both batch rows
+    (1, 40, 60, 20, 32, 0, 0),    # N = 700, H = 40: four warps per block instead of eight
+])
+def test_fp8_prologue_codes_and_scales(B, H, txt, ih, iw, rh, rw):
+    w = _fp8("fp8_prologue", B, H, txt, ih, iw, rh, rw)
     inp = synthetic.make_inputs(w, seed=3)
     d = device_inputs(inp)
     n = w.tokens
@@ -76,8 +81,41 @@ def test_fp8_prologue_codes_and_scales():
             np.testing.assert_allclose(scales[b, h].astype(np.float64), osc, rtol=1e-5)
             _codes_match(q8[b, h], oq, "q8 (%d, %d)" % (b, h))
             _codes_match(k8[b, h], ok, "k8 (%d, %d)" % (b, h))
-            _codes_match(v8t[b, h, :, :n], ov.T, "v8t (%d, %d)" % (b, h))
+            # V is bf16 and its amax a bf16 value: (448 x) / amax rounds once, so
+            # every code equals the oracle's (the case N = 700, H = 40 holds
+            # exact midpoints between codes: amax 24.5 makes x / scale = 128 x / 7)
+            np.testing.assert_array_equal(v8t[b, h, :, :n], ov.T, "v8t (%d, %d)" % (b, h))
             assert not v8t[b, h, :, n:].any(), "padding columns of V^T are not zero"
+
+
+def test_fp8_v_codes_exact_on_adversarial_heads():
+    """V^T codes equal the oracle's code for code on heads built to break a
+    quotient that is not rounded once: bf16 values with amax 30.5 (many
+    x / scale exactly halfway between two codes), amax 2^65 with tiny
+    negative values (2^-E x underflows; the code of -0 must survive), an
+    all-zero head (scale 1) and a head of subnormal bf16 values."""
+    w = _fp8("fp8_vcodes", 1, 4, 40, 10, 26, 0, 0)          # N = 300
+    inp = synthetic.make_inputs(w, seed=5)
+    rng = np.random.default_rng(11)
+    n = w.tokens
+    heads = np.zeros((4, n, 128), np.float32)
+    heads[0] = rng.uniform(-30.5, 30.5, (n, 128))
+    heads[0, 17, 3] = 30.5
+    heads[0, 5, :8] = 183.0 / 2048 * np.array([1, -1, 2, -2, 4, -4, 8, -8])   # exact ties
+    heads[1] = rng.standard_normal((n, 128)) * 2.0 ** -130
+    heads[1, 0, 0] = 2.0 ** 65
+    heads[3] = rng.standard_normal((n, 128)) * 2.0 ** -128
+    inp.v[0] = synthetic.bf16_bits_from_f32(heads.transpose(1, 0, 2))
+    d = device_inputs(inp)
+    attn = fa.FluxAttention(w.batch, w.heads, n, precision="fp8")
+    _, _, v8t, scales = attn.prologue_fp8(d["q"], d["k"], d["v"], *_geom(w), d["q_norm_w"], d["k_norm_w"])
+    assert attn.sync_status() == 0
+    v8t, scales = v8t.cpu().numpy(), scales.cpu().numpy()
+    for h in range(4):
+        _, _, ov, osc = oracle.fp8_quantize_head(inp.q, inp.k, inp.v, inp.pos, inp.w_q, inp.w_k, 0, h)
+        assert scales[0, h, 2] == np.float32(osc[2]), h
+        np.testing.assert_array_equal(v8t[0, h, :, :n], ov.T, "head %d" % h)
+    assert np.any(v8t[0, 1, :, :n] == 0x80)          # the code of -0 is there
 
 
 def test_fp8_tiny_every_row():
