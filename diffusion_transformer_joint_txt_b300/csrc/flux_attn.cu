@@ -152,10 +152,10 @@ int launch_prologue(flux_attn* h, const void* q, const void* k, int txt, int ih,
   (void)rh;
   flux::TokenGeometry geo{pos, txt, ih * iw, iw, rw};
   const int B = h->cfg.batch, H = h->cfg.num_heads;
-  const int W = flux::prologue_warps(H);
+  const int W = flux::stream_warps<flux::Bf16Rows>(H);
   const long long units = (static_cast<long long>(B) * n + W - 1) / W;
   const unsigned grid = static_cast<unsigned>(std::min<long long>(units, h->num_sms));
-  const size_t smem = static_cast<size_t>(W) * flux::kProStages * H * flux::kProRowBytes;
+  const size_t smem = flux::stream_smem<flux::Bf16Rows>(H);
   const flux::StreamArgs a{static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), wq, wk,
                            geo, B, n, H, h->cfg.rms_eps, h->rope_tab, h->err};
   flux::qk_norm_rope_kernel<flux::Bf16Rows><<<grid, 32 * W, smem, stream>>>(a, flux::Bf16Rows{qn, kn});
@@ -202,20 +202,25 @@ int launch_prologue_fp8(flux_attn* h, const void* q, const void* k, const void* 
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "V amax launch");
   // Q', K': the prologue's stream kernel, once reducing to amax, once writing codes
-  const int W = flux::prologue_warps(H);
-  const long long units = (static_cast<long long>(B) * n + W - 1) / W;
-  const unsigned grid = static_cast<unsigned>(std::min<long long>(units, h->num_sms));
-  const size_t ring = static_cast<size_t>(W) * flux::kProStages * H * flux::kProRowBytes;
   const flux::StreamArgs a{static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), wq, wk,
                            geo, B, n, H, h->cfg.rms_eps, h->rope_tab, h->err};
-  flux::AmaxRows am{};
-  am.amax = h->amax;
-  flux::qk_norm_rope_kernel<flux::AmaxRows>
-      <<<grid, 32 * W, ring + flux::AmaxRows::scratch_bytes(W, H), stream>>>(a, am);
+  const long long tokens = static_cast<long long>(B) * n;
+  {
+    const int W = flux::stream_warps<flux::AmaxRows>(H);
+    const unsigned grid = static_cast<unsigned>(std::min<long long>((tokens + W - 1) / W, h->num_sms));
+    flux::AmaxRows am{};
+    am.amax = h->amax;
+    flux::qk_norm_rope_kernel<flux::AmaxRows><<<grid, 32 * W, flux::stream_smem<flux::AmaxRows>(H), stream>>>(a, am);
+  }
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "amax launch");
-  const flux::E4m3Rows codes{q8, k8, h->amax, scales, H, B * H * 3};
-  flux::qk_norm_rope_kernel<flux::E4m3Rows><<<grid, 32 * W, ring, stream>>>(a, codes);
+  {
+    const int W = flux::stream_warps<flux::E4m3Rows>(H);
+    const unsigned grid = static_cast<unsigned>(std::min<long long>((tokens + W - 1) / W, h->num_sms));
+    const flux::E4m3Rows codes{q8, k8, h->amax, scales, H, B * H * 3};
+    flux::qk_norm_rope_kernel<flux::E4m3Rows>
+        <<<grid, 32 * W, flux::stream_smem<flux::E4m3Rows>(H), stream>>>(a, codes);
+  }
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "quantise launch");
   flux::fp8_vt_kernel<<<vgrid, flux::kVtThreads, 0, stream>>>(tv, tvt, H, h->amax, h->err);
@@ -344,15 +349,15 @@ int launch_qkv(flux_attn* h, const void* x, const void* w, const float* bias, in
 // Raise the dynamic shared-memory limit of the prologue and of both
 // attention kernels (per device).
 cudaError_t set_attention_smem_limits() {
+  // the stream kernel's rings and per-warp scratch fit kProSmemBytes (prologue_warps)
   cudaError_t e = cudaFuncSetAttribute(flux::qk_norm_rope_kernel<flux::Bf16Rows>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, flux::kProRingBytes);
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, flux::kProSmemBytes);
   if (e != cudaSuccess) return e;
-  // the amax policy's slots: W H <= 192 (the rings' bound) rows of 2 x 16 floats
   e = cudaFuncSetAttribute(flux::qk_norm_rope_kernel<flux::AmaxRows>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           flux::kProRingBytes + static_cast<int>(flux::AmaxRows::scratch_bytes(1, flux::kProMaxHeads)));
+                           flux::kProSmemBytes);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(flux::qk_norm_rope_kernel<flux::E4m3Rows>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           flux::kProRingBytes);
+                           flux::kProSmemBytes);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(flux::qkv::qkv_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(flux::qkv::SMEM_BYTES));

@@ -148,46 +148,54 @@ __device__ __forceinline__ void norm_rope8_packed(float (&x)[8], const RotCoef& 
   }
 }
 
-// Streaming layout: a persistent block per SM of W warps (8 at the FLUX head
-// count), each streaming its own tokens through its own S-stage ring.  Warp w
-// of block x takes tokens t = W x + w, then every W * gridDim.x-th; lane 0
-// keeps the next S - 1 tokens in flight with two bulk copies per token (its
-// q and k rows, H x 256 contiguous bytes each, since a token's heads are
-// adjacent in [B, N, H, 128]) and refills a stage as soon as the warp has
-// read it.  No warp waits for another.  Per token the warp computes (b, n),
-// the (cos, sin) pairs and the rotation coefficients once, then normalises,
-// rotates and stores all of its head rows (a half-warp per row, read from
-// shared memory, written head-major).  Eight warps, one token each, beat
-// both a shared chunk ring fed by a producer warp and more, smaller warps on
-// B300 (fewer warps leave room for more independent rows per warp).
-constexpr int kProWarps = 8;                         // warps per block at most
-constexpr int kProStages = 2;                        // tokens per warp ring
-constexpr int kProRingBytes = 192 * 1024;            // all warps' rings
+// Streaming layout: a persistent block per SM of W warps, each streaming its
+// own tokens through its own S-stage ring.  Warp w of block x takes tokens
+// t = W x + w, then every W * gridDim.x-th, in P parts of ceil(H / P) heads:
+// a stage holds one part (its q rows and its k rows, two bulk copies of
+// contiguous bytes, since a token's heads are adjacent in [B, N, H, 128]).
+// Lane 0 keeps the next S - 1 parts in flight and refills a stage as soon as
+// the warp has read it; no warp waits for another.  Per token the warp
+// computes (b, n), the (cos, sin) pairs and the rotation coefficients once,
+// then normalises, rotates and stores the head rows of each part (a
+// half-warp per row, read from shared memory, written head-major).
+constexpr int kProMaxWarps = 16;                     // warps per block at most (any output policy)
+constexpr int kProStages = 2;                        // parts per warp ring
+constexpr int kProSmemBytes = 220 * 1024;            // rings and the output policy's scratch
+constexpr int kProRingBytes = 192 * 1024;            // rings of one warp, for the head bound
 constexpr int kProRowBytes = 2 * kHeadDim * 2;       // one head row of q and one of k
 constexpr int kProPairs = 2;                         // head pairs a warp works on at a time
-constexpr int kProMaxHeads = kProRingBytes / (kProStages * kProRowBytes);  // 192: a single warp
+constexpr int kProMaxHeads = kProRingBytes / (kProStages * kProRowBytes);  // 192: one warp, whole tokens
 
-// Warps per block for H heads (1 .. kProWarps; H <= kProMaxHeads).
-__host__ __device__ constexpr int prologue_warps(int H) {
-  return kProRingBytes / (kProStages * kProRowBytes * H) < kProWarps
-             ? kProRingBytes / (kProStages * kProRowBytes * H)
-             : kProWarps;
+// Heads per part when a token is cut into `parts` parts.
+__host__ __device__ constexpr int prologue_part_heads(int H, int parts) { return (H + parts - 1) / parts; }
+
+// Warps per block (1 .. max_warps) for H heads in `parts` parts and
+// `scratch` bytes of policy scratch per warp (H <= kProMaxHeads).
+__host__ __device__ constexpr int prologue_warps(int H, int parts, int max_warps, int scratch) {
+  return kProSmemBytes / (kProStages * kProRowBytes * prologue_part_heads(H, parts) + scratch) < max_warps
+             ? kProSmemBytes / (kProStages * kProRowBytes * prologue_part_heads(H, parts) + scratch)
+             : max_warps;
 }
 
 // What the stream kernel does with the normalised, rotated rows.  Every
 // output policy has
-//   scratch_bytes(W, H)         shared memory it needs after the rings
+//   warp_scratch(H)             shared memory per warp it needs after the rings
 //   init(scratch, W, H)         once per warp (all lanes), before the first token
 //   token(b)                    warp-uniform, at every token (b its batch row)
 //   row(t, b, h, dst, x)        one lane's 8 values of row h of tensor t (0: Q',
 //                               1: K'); dst = element offset of those 8 values in
 //                               a head-major [B, H, N, 128] tensor
 //   finish()                    once per warp (all lanes), after the last token
-// The BF16 policy writes Q', K' bf16 [B, H, N, 128].
+// and its stream shape: kParts parts per token, kWarps warps per block at
+// most (the rings' shared memory may allow fewer).
+// The BF16 policy writes Q', K' bf16 [B, H, N, 128].  Whole tokens and eight
+// warps: with twice the bytes written per row, more and smaller parts lost.
 struct Bf16Rows {
+  static constexpr int kParts = 1;
+  static constexpr int kWarps = 8;
   __nv_bfloat16* qn;
   __nv_bfloat16* kn;
-  static __host__ __device__ size_t scratch_bytes(int, int) { return 0; }
+  static __host__ __device__ constexpr int warp_scratch(int) { return 0; }
   __device__ __forceinline__ void init(uint8_t*, int, int) {}
   __device__ __forceinline__ void token(int) {}
   __device__ __forceinline__ void row(int t, int, int, size_t dst, const float (&x)[8]) {
@@ -208,15 +216,29 @@ struct StreamArgs {
   uint32_t* err;
 };
 
+// Launch shape of the stream kernel for output policy Out and H heads.
 template <class Out>
-__global__ void __launch_bounds__(32 * kProWarps, 1) qk_norm_rope_kernel(const StreamArgs a, Out out) {
-  extern __shared__ __align__(128) uint8_t ring[];  // [W][S][q rows | k rows], H x 256 bytes each; then Out's scratch
-  __shared__ uint64_t full[kProWarps][kProStages];  // per warp: stage s holds a token
+__host__ __device__ constexpr int stream_warps(int H) {
+  return prologue_warps(H, Out::kParts, Out::kWarps, Out::warp_scratch(H));
+}
+template <class Out>
+__host__ __device__ constexpr size_t stream_smem(int H) {
+  return static_cast<size_t>(stream_warps<Out>(H)) *
+         (kProStages * kProRowBytes * prologue_part_heads(H, Out::kParts) + Out::warp_scratch(H));
+}
+
+template <class Out>
+__global__ void __launch_bounds__(32 * Out::kWarps, 1) qk_norm_rope_kernel(const StreamArgs a, Out out) {
+  static_assert(Out::kWarps <= kProMaxWarps, "barrier array");
+  extern __shared__ __align__(128) uint8_t ring[];  // [W][S][q rows | k rows] of one part; then Out's scratch
+  __shared__ uint64_t full[Out::kWarps][kProStages];  // per warp: stage s holds a part
   __shared__ int abort_flag;
   const int W = blockDim.x >> 5;
   constexpr int S = kProStages;
   const int H = a.H, N = a.N;
-  const uint32_t row = static_cast<uint32_t>(H) * kHeadDim * 2;
+  const int hs = Out::kParts == 1 ? H : prologue_part_heads(H, Out::kParts);
+  const int P = Out::kParts == 1 ? 1 : (H + hs - 1) / hs;  // parts of a token (<= kParts, none empty)
+  const uint32_t srow = static_cast<uint32_t>(hs) * kHeadDim * 2;  // q (or k) bytes of a full part
   const long long tokens = static_cast<long long>(a.B) * N;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* ab = &abort_flag;
@@ -226,20 +248,23 @@ __global__ void __launch_bounds__(32 * kProWarps, 1) qk_norm_rope_kernel(const S
     fence_mbarrier_init();
   }
   __syncthreads();
-  uint8_t* wring = ring + static_cast<size_t>(warp) * S * 2 * row;
+  uint8_t* wring = ring + static_cast<size_t>(warp) * S * 2 * srow;
   const long long first = static_cast<long long>(blockIdx.x) * W + warp;
   const long long step = static_cast<long long>(gridDim.x) * W;
-  if (lane == 0) {  // the warp's first S tokens
-    for (int j = 0; j < S; ++j) {
-      const long long t = first + j * step;
-      if (t >= tokens) break;
-      const size_t off = static_cast<size_t>(t) * H * kHeadDim;
-      mbar_arrive_expect_tx(&full[warp][j], 2 * row);
-      bulk_load(smem_u32(wring + j * 2 * row), a.q + off, row, &full[warp][j]);
-      bulk_load(smem_u32(wring + j * 2 * row + row), a.k + off, row, &full[warp][j]);
-    }
-  }
-  out.init(ring + static_cast<size_t>(W) * S * 2 * row, W, H);
+  // Part u of the warp's stream: token first + (u / P) step, heads from (u % P) hs.
+  auto issue = [&](int u, int s) {
+    const long long t = first + static_cast<long long>(u / P) * step;
+    if (t >= tokens) return;
+    const int h0 = (u % P) * hs;
+    const uint32_t bytes = static_cast<uint32_t>(min(hs, H - h0)) * kHeadDim * 2;
+    const size_t off = (static_cast<size_t>(t) * H + h0) * kHeadDim;
+    mbar_arrive_expect_tx(&full[warp][s], 2 * bytes);
+    bulk_load(smem_u32(wring + s * 2 * srow), a.q + off, bytes, &full[warp][s]);
+    bulk_load(smem_u32(wring + s * 2 * srow + srow), a.k + off, bytes, &full[warp][s]);
+  };
+  if (lane == 0)  // the warp's first S parts
+    for (int u = 0; u < S; ++u) issue(u, u);
+  out.init(ring + static_cast<size_t>(W) * S * 2 * srow, W, H);
   const int sub = lane & 15;
   const int half = lane >> 4;
   float w_q[8], w_k[8];
@@ -253,77 +278,77 @@ __global__ void __launch_bounds__(32 * kProWarps, 1) qk_norm_rope_kernel(const S
     w_k[4] = b1.x; w_k[5] = b1.y; w_k[6] = b1.z; w_k[7] = b1.w;
   }
   const size_t head_stride = static_cast<size_t>(N) * kHeadDim;  // elements between heads of Q' / K'
-  int j = 0;
+  int u = 0;
   bool aborted = false;
-  for (long long t = first; t < tokens; t += step, ++j) {
-    const int s = j % S;
-    const bool ok = mbar_wait(&full[warp][s], (j / S) & 1, ab, a.err);
-    if (__any_sync(0xFFFFFFFFu, !ok)) { aborted = true; break; }
-    const int b = static_cast<int>(t / N);
-    const int n = static_cast<int>(t - static_cast<long long>(b) * N);
-    out.token(b);
-    RotCoef kq, kk;
-    {
-      float cs[4], sn[4];
-      lane_rotation(a.geo, a.tab, n, sub, cs, sn);
-      rot_coef(w_q, cs, sn, kq);
-      rot_coef(w_k, cs, sn, kk);
-    }
-    const uint8_t* sq = wring + s * 2 * row + sub * 16;
-    const size_t dst = (static_cast<size_t>(b) * H * N + n) * kHeadDim + sub * 8;
-    // kProPairs head pairs per step: 2 kProPairs independent rows per
-    // half-warp, so that their shuffle reductions overlap.  A half-warp past
-    // the last head computes on zeros and stores nothing.
-    for (int hp = 0; hp < H; hp += 2 * kProPairs) {
-      uint4 uq[kProPairs], uk[kProPairs];
+  RotCoef kq, kk;
+  int b = 0, n = 0;
+  for (long long t = first; t < tokens; t += step) {
+    for (int p = 0; p < P; ++p, ++u) {
+      const int s = u % S;
+      const bool ok = mbar_wait(&full[warp][s], (u / S) & 1, ab, a.err);
+      if (__any_sync(0xFFFFFFFFu, !ok)) { aborted = true; break; }
+      if (p == 0) {
+        b = static_cast<int>(t / N);
+        n = static_cast<int>(t - static_cast<long long>(b) * N);
+        out.token(b);
+        float cs[4], sn[4];
+        lane_rotation(a.geo, a.tab, n, sub, cs, sn);
+        rot_coef(w_q, cs, sn, kq);
+        rot_coef(w_k, cs, sn, kk);
+      }
+      const int h0 = p * hs;
+      const int h1 = min(H, h0 + hs);
+      const uint8_t* sq = wring + s * 2 * srow + sub * 16;  // row h of the part at (h - h0) 256 bytes
+      const size_t dst = (static_cast<size_t>(b) * H * N + n) * kHeadDim + sub * 8;
+      // kProPairs head pairs per step: 2 kProPairs independent rows per
+      // half-warp, so that their shuffle reductions overlap.  A half-warp
+      // past the part's last head computes on zeros and stores nothing.
+      for (int hp = h0; hp < h1; hp += 2 * kProPairs) {
+        uint4 uq[kProPairs], uk[kProPairs];
 #pragma unroll
-      for (int i = 0; i < kProPairs; ++i) {
-        const int h = hp + 2 * i + half;
-        uq[i] = uk[i] = make_uint4(0, 0, 0, 0);
-        if (h < H) {
-          uq[i] = *reinterpret_cast<const uint4*>(sq + h * kHeadDim * 2);
-          uk[i] = *reinterpret_cast<const uint4*>(sq + row + h * kHeadDim * 2);
+        for (int i = 0; i < kProPairs; ++i) {
+          const int h = hp + 2 * i + half;
+          uq[i] = uk[i] = make_uint4(0, 0, 0, 0);
+          if (h < h1) {
+            uq[i] = *reinterpret_cast<const uint4*>(sq + (h - h0) * kHeadDim * 2);
+            uk[i] = *reinterpret_cast<const uint4*>(sq + srow + (h - h0) * kHeadDim * 2);
+          }
+        }
+        float xq[kProPairs][8], xk[kProPairs][8];
+#pragma unroll
+        for (int i = 0; i < kProPairs; ++i) {
+          unpack8(uq[i], xq[i]);
+          unpack8(uk[i], xk[i]);
+        }
+#pragma unroll
+        for (int i = 0; i < kProPairs; ++i) {
+          norm_rope8_packed(xq[i], kq, a.eps);
+          norm_rope8_packed(xk[i], kk, a.eps);
+        }
+#pragma unroll
+        for (int i = 0; i < kProPairs; ++i) {
+          const int h = hp + 2 * i + half;
+          if (h < h1) {
+            out.row(0, b, h, dst + h * head_stride, xq[i]);
+            out.row(1, b, h, dst + h * head_stride, xk[i]);
+          }
         }
       }
-      float xq[kProPairs][8], xk[kProPairs][8];
-#pragma unroll
-      for (int i = 0; i < kProPairs; ++i) {
-        unpack8(uq[i], xq[i]);
-        unpack8(uk[i], xk[i]);
-      }
-#pragma unroll
-      for (int i = 0; i < kProPairs; ++i) {
-        norm_rope8_packed(xq[i], kq, a.eps);
-        norm_rope8_packed(xk[i], kk, a.eps);
-      }
-#pragma unroll
-      for (int i = 0; i < kProPairs; ++i) {
-        const int h = hp + 2 * i + half;
-        if (h < H) {
-          out.row(0, b, h, dst + h * head_stride, xq[i]);
-          out.row(1, b, h, dst + h * head_stride, xk[i]);
-        }
-      }
-    }
-    __syncwarp();   // every lane has read the stage: refill it with token j + S
-    if (lane == 0) {
-      const long long tn = t + S * step;
-      if (tn < tokens) {
+      __syncwarp();  // every lane has read the stage: refill it with part u + S
+      if (lane == 0) {
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        const size_t off = static_cast<size_t>(tn) * H * kHeadDim;
-        mbar_arrive_expect_tx(&full[warp][s], 2 * row);
-        bulk_load(smem_u32(wring + s * 2 * row), a.q + off, row, &full[warp][s]);
-        bulk_load(smem_u32(wring + s * 2 * row + row), a.k + off, row, &full[warp][s]);
+        issue(u + S, s);
       }
     }
+    if (aborted) break;
   }
   if (aborted) {
     if (lane == 0)  // loads still in flight must land before the block exits (bounded)
-      for (int jj = j; jj < j + S; ++jj) {
-        if (first + jj * step >= tokens) break;
-        const uint32_t ba = smem_u32(&full[warp][jj % S]);
+      for (int uu = u; uu < u + S; ++uu) {
+        if (first + static_cast<long long>(uu / P) * step >= tokens) break;
+        const uint32_t ba = smem_u32(&full[warp][uu % S]);
         const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(ba, (jj / S) & 1) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+        while (!mbar_try_wait(ba, (uu / S) & 1) && globaltimer_ns() - t0 < kWaitLimitNs) {}
       }
     return;
   }

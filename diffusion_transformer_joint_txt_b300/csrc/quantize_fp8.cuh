@@ -59,12 +59,12 @@ __device__ __forceinline__ uint2 quant8(const float (&x)[8], float inv) {
 // (tensor, head) whenever the warp's batch row changes and after its last
 // token.
 struct AmaxRows {
+  static constexpr int kParts = 2;  // half tokens, twelve warps: more warps to hide latency, as
+  static constexpr int kWarps = 12; // nothing (or only codes, below) is written per row
   uint32_t* amax;  // [B*H][3]
   float* slot;
   int H, cur_b;
-  static __host__ __device__ size_t scratch_bytes(int W, int H) {
-    return static_cast<size_t>(W) * 2 * H * 16 * sizeof(float);
-  }
+  static __host__ __device__ constexpr int warp_scratch(int H) { return 2 * H * 16 * static_cast<int>(sizeof(float)); }
   __device__ __forceinline__ void init(uint8_t* scratch, int, int heads) {
     H = heads;
     cur_b = -1;
@@ -104,12 +104,14 @@ struct AmaxRows {
 // Output policy of the stream kernel: E4M3 codes of Q' / s_q and K' / s_k,
 // head-major; block 0 also writes the scales of all three tensors.
 struct E4m3Rows {
+  static constexpr int kParts = 2;
+  static constexpr int kWarps = 12;
   uint8_t* q8;
   uint8_t* k8;
   const uint32_t* amax;  // [B*H][3], complete
   float* scales;         // [B*H][3]
   int H, n_scales;
-  static __host__ __device__ size_t scratch_bytes(int, int) { return 0; }
+  static __host__ __device__ constexpr int warp_scratch(int) { return 0; }
   __device__ __forceinline__ void init(uint8_t*, int, int) {
     if (blockIdx.x == 0)
       for (int i = threadIdx.x; i < n_scales; i += blockDim.x) {
