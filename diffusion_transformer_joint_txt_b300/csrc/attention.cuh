@@ -538,6 +538,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = sm.tmem_base;
+  // The grid is launched as a programmatic dependent of the kernel before it
+  // in the stream (the prologue): the setup above overlaps that kernel's
+  // tail, and no thread reads global memory before this wait.
+  griddep_wait();
 
   if (prm.debug & 1) {  // FLUX_ATTN_DEBUG_FORCE_TIMEOUT: a wait nothing will satisfy
     if (threadIdx.x == 0) mbar_wait(&sm.never, 0, ab, prm.err);

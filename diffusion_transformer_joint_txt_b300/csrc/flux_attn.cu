@@ -166,8 +166,10 @@ int launch_prologue(flux_attn* h, const void* q, const void* k, int txt, int ih,
 
 size_t pad16(int n) { return (static_cast<size_t>(n) + 15) & ~size_t(15); }
 
-// The FP8 prologue: amax of V, Q', K' (after zeroing it), then the E4M3
-// codes of Q', K' and the scales, then the codes of V transposed.
+// The FP8 prologue: amax of V, Q', K' (after zeroing it), then the codes of
+// V transposed, then the E4M3 codes of Q', K' and the scales (last, so that
+// the kernel before the attention is the one-wave stream kernel that lets it
+// start early).
 int launch_prologue_fp8(flux_attn* h, const void* q, const void* k, const void* v, int txt, int ih, int iw,
                         int rw, const int32_t* pos, const float* wq, const float* wk, int n, uint8_t* q8,
                         uint8_t* k8, uint8_t* v8t, float* scales, cudaStream_t stream) {
@@ -214,6 +216,9 @@ int launch_prologue_fp8(flux_attn* h, const void* q, const void* k, const void* 
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "amax launch");
+  flux::fp8_vt_kernel<<<vgrid, flux::kVtThreads, 0, stream>>>(tv, tvt, H, h->amax, h->err);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "V^T launch");
   {
     const int W = flux::stream_warps<flux::E4m3Rows>(H);
     const unsigned grid = static_cast<unsigned>(std::min<long long>((tokens + W - 1) / W, h->num_sms));
@@ -223,9 +228,6 @@ int launch_prologue_fp8(flux_attn* h, const void* q, const void* k, const void* 
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "quantise launch");
-  flux::fp8_vt_kernel<<<vgrid, flux::kVtThreads, 0, stream>>>(tv, tvt, H, h->amax, h->err);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e, "V^T launch");
   return FLUX_ATTN_OK;
 }
 
@@ -283,12 +285,22 @@ int launch_attention(flux_attn* h, bool fp8, const void* qn, const void* kn, con
   prm.nkv = (n + BN - 1) / BN;
   prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(HD)));
   prm.debug = h->cfg.debug_flags;
-  const dim3 grid((n + CTA_ROWS - 1) / CTA_ROWS, B * H);
-  if (fp8)
-    attn_kernel<true><<<grid, THREADS, smem_bytes<true>(), stream>>>(tq, tk, tv, to, prm);
-  else
-    attn_kernel<false><<<grid, THREADS, smem_bytes<false>(), stream>>>(tq, tk, tv, to, prm);
-  cudaError_t e = cudaGetLastError();
+  // Programmatic stream serialisation: the grid may start before the kernel
+  // ahead of it in the stream completes; attn_kernel waits for it
+  // (griddepcontrol.wait) before its first global read.
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3((n + CTA_ROWS - 1) / CTA_ROWS, B * H);
+  lc.blockDim = dim3(THREADS);
+  lc.dynamicSmemBytes = fp8 ? smem_bytes<true>() : smem_bytes<false>();
+  lc.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  cudaError_t e = fp8 ? cudaLaunchKernelEx(&lc, attn_kernel<true>, tq, tk, tv, to, prm)
+                      : cudaLaunchKernelEx(&lc, attn_kernel<false>, tq, tk, tv, to, prm);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   return FLUX_ATTN_OK;
 }

@@ -230,6 +230,10 @@ __host__ __device__ constexpr size_t stream_smem(int H) {
 template <class Out>
 __global__ void __launch_bounds__(32 * Out::kWarps, 1) qk_norm_rope_kernel(const StreamArgs a, Out out) {
   static_assert(Out::kWarps <= kProMaxWarps, "barrier array");
+  // Every CTA of this grid is resident at once (grid <= SMs, one block per
+  // SM): the attention kernel after it may be scheduled now and set up on
+  // SMs whose block has finished.
+  griddep_launch_dependents();
   extern __shared__ __align__(128) uint8_t ring[];  // [W][S][q rows | k rows] of one part; then Out's scratch
   __shared__ uint64_t full[Out::kWarps][kProStages];  // per warp: stage s holds a part
   __shared__ int abort_flag;

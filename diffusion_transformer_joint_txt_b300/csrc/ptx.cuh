@@ -77,6 +77,21 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// ------------------------------------------------------ programmatic launch
+
+// Wait until the grids this one depends on in its stream have completed and
+// their writes are visible (immediate when it was launched without
+// programmatic stream serialisation, or they are done).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow a dependent grid launched with programmatic stream serialisation to
+// be scheduled before this grid completes (its griddep_wait still waits for
+// all of this grid).  Only for grids whose CTAs are all resident at once, so
+// that waiting dependents cannot hold SMs this grid still needs.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
