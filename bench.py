@@ -210,8 +210,7 @@ class Step:
 
     def __call__(self, ev=None):
         """One step; ev = (start, end) brackets it, ev = (start, split, end)
-        also splits it between the two calls (an event between them keeps
-        the attention from starting while the prologue finishes)."""
+        also splits it between the two calls."""
         if ev is not None:
             ev[0].record(self.stream)
         self.prologue()
@@ -285,16 +284,16 @@ def sustained(step, seconds, torch, clocks):
 
 
 def measure(step, steps, warmup, torch, flush, barrier):
-    """Mean step time (ms) over `steps` timed steps, each bracketed by two
-    events, then the mean attention-kernel and prologue times from a second
-    pass of up to `steps` steps with an event between the two calls.  L2 is
-    flushed before every step, outside its events."""
+    """Mean step, attention-kernel and prologue times (ms) over `steps` timed
+    steps, from three CUDA events per step on the launching stream (before the
+    prologue, between the two calls, after the attention); L2 is flushed
+    before every step, outside its events."""
     for _ in range(warmup):
         flush.zero_()
         step()
     if step.attn.sync_status() != 0:
         raise RuntimeError("device status error in warm-up (%s)" % step.w.name)
-    ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(2)) for _ in range(steps)]
+    ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(steps)]
     barrier()
     for e in ev:
         flush.zero_()
@@ -302,14 +301,9 @@ def measure(step, steps, warmup, torch, flush, barrier):
     barrier()
     if step.attn.sync_status() != 0:
         raise RuntimeError("device status error during the timed region (%s)" % step.w.name)
-    split = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(min(steps, 200))]
-    for e in split:
-        flush.zero_()
-        step(e)
-    torch.cuda.synchronize()
-    return (sum(a.elapsed_time(c) for a, c in ev) / steps,
-            sum(b.elapsed_time(c) for _, b, c in split) / len(split),
-            sum(a.elapsed_time(b) for a, b, _ in split) / len(split))
+    return (sum(a.elapsed_time(c) for a, _, c in ev) / steps,
+            sum(b.elapsed_time(c) for _, b, c in ev) / steps,
+            sum(a.elapsed_time(b) for a, b, _ in ev) / steps)
 
 
 def run_ours(args):
