@@ -128,7 +128,9 @@ FLUX_ATTN_API int flux_attn_attend(flux_attn_t h, const void* qn, const void* kn
 
 /* Prologue step alone (FP8 handles): per (b, h), amax of Q', K' and V, then
  * E4M3 codes (round to nearest even, saturating at 448) of x / scale with
- * scale = amax / 448 (1 when amax == 0).
+ * scale = amax / 448 (1 when amax == 0).  V's codes are those of the exact
+ * quotient, ties included; Q', K' are computed in fp32, so a value within fp32
+ * rounding of a midpoint between two codes may take the neighbouring code.
  *   q8, k8  uint8 [B, H, N, 128];  v8t  uint8 [B, H, 128, Npad] (V transposed,
  *   Npad = N rounded up to a multiple of 16, padding columns zero)
  *   scales  fp32 [B, H, 3] = (scale_q, scale_k, scale_v) */
