@@ -316,7 +316,8 @@ int launch_qkv(flux_attn* h, const void* x, const void* w, const float* bias, in
   const int F = 3 * H * flux::kHeadDim;
   flux::TokenGeometry geo{pos, txt, ih * iw, iw, rw};
   const int pairs = n * (flux::kHeadDim / 2);
-  flux::qkv::rope_table_kernel<<<(pairs + 255) / 256, 256, 0, stream>>>(geo, n, h->rope_tab, h->rope);
+  const int tblocks = std::min((pairs + kTableThreads - 1) / kTableThreads, kTableBlocksPerSm * h->num_sms);
+  flux::qkv::rope_table_kernel<<<tblocks, kTableThreads, 0, stream>>>(geo, n, h->rope_tab, h->rope);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "rope table launch");
   CUtensorMap ta, tb;
@@ -352,8 +353,20 @@ int launch_qkv(flux_attn* h, const void* x, const void* w, const float* bias, in
   p.group_m = group_rows(p.m_tiles, d_model);
   p.eps = h->cfg.rms_eps;
   const int tiles = p.m_tiles * p.n_tiles;
-  qkv_gemm_kernel<<<std::min(tiles, h->num_sms), THREADS, SMEM_BYTES, stream>>>(ta, tb, p);
-  e = cudaGetLastError();
+  // Programmatic dependent of the table kernel: producer and MMA warps start
+  // on x and W (complete before the table kernel began); the epilogue waits.
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(std::min(tiles, h->num_sms));
+  lc.blockDim = dim3(THREADS);
+  lc.dynamicSmemBytes = SMEM_BYTES;
+  lc.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  e = cudaLaunchKernelEx(&lc, qkv_gemm_kernel, ta, tb, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "QKV GEMM launch");
   return FLUX_ATTN_OK;
 }

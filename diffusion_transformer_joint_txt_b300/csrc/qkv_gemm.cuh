@@ -71,18 +71,28 @@ struct Params {
 };
 
 // (cos, sin) of pair j of token n: pos_n[axis_j] * freq_j, precise sincosf.
-__global__ void rope_table_kernel(TokenGeometry geo, int N, RopeTable tab, float2* __restrict__ out) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= N * (kHeadDim / 2)) return;
-  const int n = i / (kHeadDim / 2);
-  const int j = i - n * (kHeadDim / 2);
-  int p[3];
-  token_position(geo, n, p);
-  const int a = tab.axis[j];
-  const int pos = a == 0 ? p[0] : (a == 1 ? p[1] : p[2]);
-  float s, c;
-  sincosf(static_cast<float>(pos) * tab.freq[j], &s, &c);
-  out[i] = make_float2(c, s);
+// Launched as one wave (a grid-stride loop over the N x 64 pairs, at most
+// kTableBlocksPerSm blocks per SM), so that it may let the GEMM after it
+// start early: the GEMM's producer and MMA warps do not read the table, and
+// its epilogue waits for this grid (griddepcontrol.wait) before it does.
+constexpr int kTableThreads = 256;
+constexpr int kTableBlocksPerSm = 4;
+
+__global__ void __launch_bounds__(kTableThreads)
+    rope_table_kernel(TokenGeometry geo, int N, RopeTable tab, float2* __restrict__ out) {
+  griddep_launch_dependents();
+  const int total = N * (kHeadDim / 2);
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+    const int n = i / (kHeadDim / 2);
+    const int j = i - n * (kHeadDim / 2);
+    int p[3];
+    token_position(geo, n, p);
+    const int a = tab.axis[j];
+    const int pos = a == 0 ? p[0] : (a == 1 ? p[1] : p[2]);
+    float s, c;
+    sincosf(static_cast<float>(pos) * tab.freq[j], &s, &c);
+    out[i] = make_float2(c, s);
+  }
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1) {
@@ -306,6 +316,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     mma_issuer(sm, tmem, p, ab);
     __syncwarp();
   } else {
+    griddep_wait();  // the (cos, sin) table comes from the kernel before this one
     epilogue(sm, tmem, p, ab);
   }
   tc_fence_before_sync();

@@ -122,3 +122,36 @@ def test_forward_hidden_equals_qkv_then_attend():
                               torch.from_numpy(inp.w_k).cuda())
     assert attn.sync_status() == 0
     assert torch.equal(got, want)
+
+
+def test_qkv_alternating_geometry_no_sync():
+    """The GEMM starts before its (cos, sin) table kernel has finished and
+    only its epilogue waits for it: two geometries with the same token count
+    alternate step after step without host synchronisation, and each step's
+    Q', K' must equal those computed with a sync after the table kernel, bit
+    for bit (a stale table would rotate by the other geometry's angles)."""
+    w = synthetic.Workload("qkv_geo", 1, 4, 512, 32, 32, 0, 0)          # N = 1536
+    inp = synthetic.make_qkv_inputs(w, d_model=256, seed=31)
+    geos = [(512, 32, 32, 0, 0), (256, 16, 64, 8, 32)]                  # 512 + 1024 = 256 + 1024 + 256
+    assert len({g[0] + g[1] * g[2] + g[3] * g[4] for g in geos}) == 1
+    attn = fa.FluxAttention(w.batch, w.heads, w.tokens)
+    x, wt = dev_bf16(inp.x), dev_bf16(inp.w)
+    b = torch.from_numpy(inp.bias).cuda()
+    wq, wk = torch.from_numpy(inp.w_q).cuda(), torch.from_numpy(inp.w_k).cuda()
+    qn, kn, v = attn.qkv(x, wt, b, *geos[0], wq, wk)
+    refs = []
+    for g in geos:
+        attn.qkv(x, wt, b, *g, wq, wk, qn=qn, kn=kn, v=v)
+        torch.cuda.synchronize()
+        refs.append((qn.clone(), kn.clone()))
+    assert not torch.equal(refs[0][0], refs[1][0])
+    steps = 10
+    snaps = []
+    for i in range(steps):
+        attn.qkv(x, wt, b, *geos[i % 2], wq, wk, qn=qn, kn=kn, v=v)
+        snaps.append((qn.clone(), kn.clone()))
+    torch.cuda.synchronize()
+    assert attn.sync_status() == 0
+    bad = [i for i in range(steps) if not (torch.equal(snaps[i][0], refs[i % 2][0]) and
+                                           torch.equal(snaps[i][1], refs[i % 2][1]))]
+    assert not bad, "steps with another geometry's rotation: %s" % bad
