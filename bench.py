@@ -502,7 +502,7 @@ def cpu_baseline(w, inp, seconds):
         oracle.attention_rows(inp.q, inp.k, inp.v, inp.pos, inp.w_q, inp.w_k, rows=rows, nthreads=threads)
         return time.perf_counter() - t0
 
-    # grow the sample until it takes a meaningful share of the budget, then size
+    # grow the sample until it takes a meaningful share of `seconds`, then size
     # the measured sample from that rate (per-head set-up makes tiny probes misleading)
     count, t = 256, 0.0
     while count < 400000:
