@@ -51,6 +51,10 @@ FALLBACK_PEAKS = {"bf16_tflops": 1800.0, "hbm_gbs": 6400.0}
 L2_FLUSH_BYTES = 256 << 20
 ATTN_SOURCES = ["diffusion_transformer_joint_txt_b300/csrc/attention.cuh",
                 "diffusion_transformer_joint_txt_b300/csrc/ptx.cuh"]
+# Dense per-GPU tensor-core figures the pages print (WaveSpeedAI X DataCrunch
+# B200 page, technical-specifications table, without sparsity): context for
+# the "frac_of_nominal" keys, not the roofline denominators.
+NOMINAL_TFLOPS = {"bf16": 2250.0, "fp8": 4500.0}
 
 
 def dist_env():
@@ -333,7 +337,7 @@ def run_ours(args):
         w = step.w
         s_ms, a_ms, p_ms = times
         peak = peak_bf16 * (2.0 if step.fp8 else 1.0)
-        nominal = 4500.0 if step.fp8 else 2250.0
+        nominal = NOMINAL_TFLOPS["fp8" if step.fp8 else "bf16"]
         achieved = w.flops / (a_ms * 1e-3) / 1e12
         return {"workload": w.name, "precision": w.precision, "batch": w.batch, "heads": w.heads,
                 "tokens": w.tokens, "steps": n_steps, "value": job_throughput(w.flops, world, s_ms),
@@ -378,7 +382,7 @@ def run_ours(args):
         tf = st.flops / (s_ms * 1e-3) / 1e12
         qkv.append({"workload": st.w.name, "kernel": "qkv_gemm_kernel (+ rope_table_kernel)",
                     "gemm": [st.w.batch * st.w.tokens, 3 * st.w.heads * 128, st.w.heads * 128],
-                    "ms": s_ms, "tflops": tf, "roofline_frac": tf / peak_bf16, "frac_of_2250_nominal": tf / 2250.0,
+                    "ms": s_ms, "tflops": tf, "roofline_frac": tf / peak_bf16, "frac_of_2250_nominal": tf / NOMINAL_TFLOPS["bf16"],
                     "algorithmic_flops": st.flops, "gpu_launches": 2 * args.steps2})
         st.attn.close()
 
