@@ -161,7 +161,7 @@ __device__ __forceinline__ void norm_rope8_packed(float (&x)[8], const RotCoef& 
 constexpr int kProMaxWarps = 16;                     // warps per block at most (any output policy)
 constexpr int kProStages = 2;                        // parts per warp ring
 constexpr int kProSmemBytes = 220 * 1024;            // rings and the output policy's scratch
-constexpr int kProRingBytes = 192 * 1024;            // rings of one warp, for the head bound
+constexpr int kProRingBytes = 192 * 1024;            // bounds H: one warp's two whole-token stages fit
 constexpr int kProRowBytes = 2 * kHeadDim * 2;       // one head row of q and one of k
 constexpr int kProPairs = 2;                         // head pairs a warp works on at a time
 constexpr int kProMaxHeads = kProRingBytes / (kProStages * kProRowBytes);  // 192: one warp, whole tokens
