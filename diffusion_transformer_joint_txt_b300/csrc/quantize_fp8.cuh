@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(kVtThreads)
   // a / d comes from q0 = a rcp(d) with Markstein's correction
   // q = q0 + (a - q0 d) rcp(d) (residual exact by FMA).  A product with a
   // rounded 1 / scale alone misses the code decision when x / scale is a
-  // midpoint between two codes, which bf16 V with amax like 30.5 hits often.
+  // midpoint between two codes, which bf16 V with amax like 24.5 hits often.
   // The sign of x is copied onto the quotient, so that a negative x whose
   // 2^-E x underflows still gives the code of -0.
   const float am = __uint_as_float(amax[3 * bh + 2]);

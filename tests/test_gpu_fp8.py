@@ -90,28 +90,33 @@ def test_fp8_prologue_codes_and_scales(B, H, txt, ih, iw, rh, rw):
 
 def test_fp8_v_codes_exact_on_adversarial_heads():
     """V^T codes equal the oracle's code for code on heads built to break a
-    quotient that is not rounded once: bf16 values with amax 30.5 (many
-    x / scale exactly halfway between two codes), amax 2^65 with tiny
-    negative values (2^-E x underflows; the code of -0 must survive), an
-    all-zero head (scale 1) and a head of subnormal bf16 values."""
-    w = _fp8("fp8_vcodes", 1, 4, 40, 10, 26, 0, 0)          # N = 300
+    quotient that is not rounded once: bf16 values with amax 24.5 (many
+    x / scale = 128 x / 7 exactly halfway between two codes, where a product
+    with a rounded 448 / amax takes the odd code) and with amax 30.5 (ties
+    that a scale rounded first misses), amax 2^65 with tiny negative values
+    (2^-E x underflows; the code of -0 must survive), an all-zero head
+    (scale 1) and a head of subnormal bf16 values."""
+    w = _fp8("fp8_vcodes", 1, 5, 40, 10, 26, 0, 0)          # N = 300
     inp = synthetic.make_inputs(w, seed=5)
     rng = np.random.default_rng(11)
     n = w.tokens
-    heads = np.zeros((4, n, 128), np.float32)
-    heads[0] = rng.uniform(-30.5, 30.5, (n, 128))
-    heads[0, 17, 3] = 30.5
-    heads[0, 5, :8] = 183.0 / 2048 * np.array([1, -1, 2, -2, 4, -4, 8, -8])   # exact ties
+    heads = np.zeros((5, n, 128), np.float32)
+    heads[0] = rng.uniform(-24.5, 24.5, (n, 128))
+    heads[0, 17, 3] = 24.5
+    heads[0, 5, :8] = 203.0 / 4096 * np.array([1, -1, 2, -2, 4, -4, 8, -8])   # exact ties
     heads[1] = rng.standard_normal((n, 128)) * 2.0 ** -130
     heads[1, 0, 0] = 2.0 ** 65
     heads[3] = rng.standard_normal((n, 128)) * 2.0 ** -128
+    heads[4] = rng.uniform(-30.5, 30.5, (n, 128))
+    heads[4, 17, 3] = 30.5
+    heads[4, 5, :8] = 183.0 / 2048 * np.array([1, -1, 2, -2, 4, -4, 8, -8])   # exact ties
     inp.v[0] = synthetic.bf16_bits_from_f32(heads.transpose(1, 0, 2))
     d = device_inputs(inp)
     attn = fa.FluxAttention(w.batch, w.heads, n, precision="fp8")
     _, _, v8t, scales = attn.prologue_fp8(d["q"], d["k"], d["v"], *_geom(w), d["q_norm_w"], d["k_norm_w"])
     assert attn.sync_status() == 0
     v8t, scales = v8t.cpu().numpy(), scales.cpu().numpy()
-    for h in range(4):
+    for h in range(5):
         _, _, ov, osc = oracle.fp8_quantize_head(inp.q, inp.k, inp.v, inp.pos, inp.w_q, inp.w_k, 0, h)
         assert scales[0, h, 2] == np.float32(osc[2]), h
         np.testing.assert_array_equal(v8t[0, h, :, :n], ov.T, "head %d" % h)
