@@ -163,7 +163,6 @@ constexpr int kProStages = 2;                        // parts per warp ring
 constexpr int kProSmemBytes = 220 * 1024;            // rings and the output policy's scratch
 constexpr int kProRingBytes = 192 * 1024;            // bounds H: one warp's two whole-token stages fit
 constexpr int kProRowBytes = 2 * kHeadDim * 2;       // one head row of q and one of k
-constexpr int kProPairs = 2;                         // head pairs a warp works on at a time
 constexpr int kProMaxHeads = kProRingBytes / (kProStages * kProRowBytes);  // 192: one warp, whole tokens
 
 // Heads per part when a token is cut into `parts` parts.
@@ -187,12 +186,14 @@ __host__ __device__ constexpr int prologue_warps(int H, int parts, int max_warps
 //                               a head-major [B, H, N, 128] tensor
 //   finish()                    once per warp (all lanes), after the last token
 // and its stream shape: kParts parts per token, kWarps warps per block at
-// most (the rings' shared memory may allow fewer).
+// most (the rings' shared memory may allow fewer), kPairs head pairs a warp
+// works on at a time.
 // The BF16 policy writes Q', K' bf16 [B, H, N, 128].  Whole tokens and eight
 // warps: with twice the bytes written per row, more and smaller parts lost.
 struct Bf16Rows {
   static constexpr int kParts = 1;
   static constexpr int kWarps = 8;
+  static constexpr int kPairs = 2;
   __nv_bfloat16* qn;
   __nv_bfloat16* kn;
   static __host__ __device__ constexpr int warp_scratch(int) { return 0; }
@@ -304,9 +305,10 @@ __global__ void __launch_bounds__(32 * Out::kWarps, 1) qk_norm_rope_kernel(const
       const int h1 = min(H, h0 + hs);
       const uint8_t* sq = wring + s * 2 * srow + sub * 16;  // row h of the part at (h - h0) 256 bytes
       const size_t dst = (static_cast<size_t>(b) * H * N + n) * kHeadDim + sub * 8;
-      // kProPairs head pairs per step: 2 kProPairs independent rows per
-      // half-warp, so that their shuffle reductions overlap.  A half-warp
-      // past the part's last head computes on zeros and stores nothing.
+      // kPairs head pairs per step: 2 kPairs independent rows per half-warp,
+      // so that their shuffle reductions overlap.  A half-warp past the
+      // part's last head computes on zeros and stores nothing.
+      constexpr int kProPairs = Out::kPairs;
       for (int hp = h0; hp < h1; hp += 2 * kProPairs) {
         uint4 uq[kProPairs], uk[kProPairs];
 #pragma unroll

@@ -61,6 +61,7 @@ __device__ __forceinline__ uint2 quant8(const float (&x)[8], float inv) {
 struct AmaxRows {
   static constexpr int kParts = 2;  // half tokens, twelve warps: more warps to hide latency, as
   static constexpr int kWarps = 12; // nothing (or only codes, below) is written per row
+  static constexpr int kPairs = 3;  // six independent rows per half-warp
   uint32_t* amax;  // [B*H][3]
   float* slot;
   int H, cur_b;
@@ -106,6 +107,7 @@ struct AmaxRows {
 struct E4m3Rows {
   static constexpr int kParts = 2;
   static constexpr int kWarps = 12;
+  static constexpr int kPairs = 3;
   uint8_t* q8;
   uint8_t* k8;
   const uint32_t* amax;  // [B*H][3], complete
