@@ -33,8 +33,7 @@
  *   - The attention kernel (and the QKV GEMM) is launched with programmatic
  *     stream serialisation: it may be scheduled while the kernel before it
  *     in the stream is finishing, and it waits for that kernel to complete
- *     before it reads any memory, so stream order holds as usual (also in a
- *     captured CUDA graph, where the dependency becomes a programmatic edge).
+ *     before it reads any memory, so stream order holds as usual.
  *   - Every call returns a flux_attn_status.  On a nonzero status nothing was
  *     enqueued, except FLUX_ATTN_ERR_CUDA from a failed launch.  Errors found
  *     on the device (a bounded wait that ran out) are reported later by
