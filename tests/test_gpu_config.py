@@ -73,3 +73,21 @@ def test_qkv_with_other_rope_and_norm():
         g = host_f64(got)[0].transpose(1, 0, 2)            # [N, H, 128]
         err = np.abs(g - want)
         assert np.all(err <= 2.0 ** -8 * np.abs(want) + 1e-5), float(err.max())
+
+
+@pytest.mark.parametrize("precision", ["bf16", "fp8"])
+def test_max_head_count(precision):
+    """192 heads, the most a handle accepts: the prologue's stream kernel then
+    runs one warp per block (whole tokens) and the FP8 passes one or two (half
+    tokens of 96 heads); every output row against the oracle."""
+    w = synthetic.Workload("maxh", 1, 192, 40, 8, 8, 0, 0, precision=precision, outliers=False)   # N = 104
+    inp = synthetic.make_inputs(w, seed=41)
+    d = device_inputs(inp)
+    attn = fa.FluxAttention(w.batch, w.heads, w.tokens, precision=precision)
+    out = attn.forward(d["q"], d["k"], d["v"], *_geom(w), d["q_norm_w"], d["k_norm_w"])
+    assert attn.sync_status() == 0
+    want = oracle.attention_rows(inp.q, inp.k, inp.v, inp.pos, inp.w_q, inp.w_k, fp8=(precision == "fp8"))
+    if precision == "fp8":
+        compare(host_f64(out), want, FP8_MAX_ABS, rel_rms=FP8_REL_RMS, what="fp8, 192 heads")
+    else:
+        compare(host_f64(out), want, BF16_MAX_ABS, BF16_MEAN_ABS, BF16_REL_RMS, "bf16, 192 heads")
