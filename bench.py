@@ -9,7 +9,8 @@ Metric: joint-attention TFLOP/s = 4 B H N^2 d / step time, on the FLUX-dev
 seeded synthetic bf16 inputs already resident in HBM.  A step is one
 flux_attn_prologue + one flux_attn_attend call (= flux_attn_forward); L2 is
 flushed (a 256 MB write) before every timed step, outside the step's events.
-The FLUX 2048x2048 step (N=16896, BF16) and the FP8 classifier-free-guidance
+The FLUX 2048x2048 step (N=16896, BF16), the image-to-image step with a
+2048x2048 reference image (N=33280, BF16) and the FP8 classifier-free-guidance
 pair at 2048x2048 (B=2, N=16896: amax + E4M3 quantise + FP8 attention) are
 measured the same way and reported under "secondary"; the QKV projection
 with its fused QK-norm + RoPE epilogue (2 M F D flops: M = B N tokens,
@@ -45,7 +46,7 @@ if ROOT not in sys.path:
 import synthetic  # noqa: E402
 
 PRIMARY = "flux_1024_4608"
-SECONDARY = ["flux_2048_16896", "fp8_cfg_2048_16896"]
+SECONDARY = ["flux_2048_16896", "i2i_2048_33280", "fp8_cfg_2048_16896"]
 METRIC = "joint-attn TFLOP/s & % of B300 BF16/FP8 TC peak at 4608/16896 tokens"
 FALLBACK_PEAKS = {"bf16_tflops": 1800.0, "hbm_gbs": 6400.0}
 L2_FLUSH_BYTES = 256 << 20
@@ -76,6 +77,15 @@ def max_over_ranks(values, world, dist, torch, device):
 def job_throughput(flops_per_rank, world, ms):
     """Whole-job TFLOP/s: every rank runs its own replica of the workload."""
     return flops_per_rank * world / (ms * 1e-3) / 1e12
+
+
+def workload_config(w, world):
+    """The "config" object of a JSON line; both arms print the same one."""
+    return {"workload": w.name, "batch": w.batch, "heads": w.heads, "head_dim": 128,
+            "tokens": w.tokens, "txt_len": w.txt_len, "img": [w.img_h, w.img_w],
+            "ref": [w.ref_h, w.ref_w], "global_batch": w.batch * world, "seq_len": w.tokens,
+            "parallelism": "replicas" if world > 1 else "single",
+            "l2": "GPU arm: L2 flushed before every timed step (256 MB write, outside the step events)"}
 
 
 def load_peaks():
@@ -227,9 +237,17 @@ class Step:
     @property
     def prologue_bytes(self):
         """Algorithmic HBM bytes of the prologue per step.  BF16: read q, k and
-        write Q', K' (2 + 2 bytes per element each).  FP8: the amax pass reads
-        q, k, v; the quantise pass reads them again and writes one E4M3 byte
-        per element of Q', K', V (the scales need the whole head first)."""
+        write Q', K' (2 + 2 bytes per element each).  FP8: one E4M3 byte written
+        per element of each of Q', K', V (3 bytes per (b, n, h, d)), the
+        figure the hot-path scope fixes for this step."""
+        elems = self.w.batch * self.w.tokens * self.w.heads * 128
+        return elems * (3 if self.fp8 else 8)
+
+    @property
+    def prologue_traffic_min(self):
+        """Bytes the prologue cannot avoid moving.  FP8: the scales need the
+        amax of a whole head first, so q, k, v are read twice (2 x 6 bytes)
+        around the three code bytes: 15 bytes per (b, n, h, d)."""
         elems = self.w.batch * self.w.tokens * self.w.heads * 128
         return elems * (15 if self.fp8 else 8)
 
@@ -345,6 +363,9 @@ def run_ours(args):
                 "roofline_frac": achieved / peak, "peak_tflops": peak,
                 "frac_of_nominal": achieved / nominal, "nominal_tflops": nominal,
                 "prologue_ms": p_ms, "prologue_gbs": step.prologue_bytes / (p_ms * 1e-3) / 1e9,
+                "prologue_frac": step.prologue_bytes / (p_ms * 1e-3) / 1e9 / hbm,
+                "prologue_algorithmic_bytes": step.prologue_bytes,
+                "prologue_traffic_min_gbs": step.prologue_traffic_min / (p_ms * 1e-3) / 1e9,
                 "gpu_launches": n_steps * step.attn.launches_per_forward(w.tokens)}
 
     w = synthetic.WORKLOADS[args.workload]
@@ -397,11 +418,7 @@ def run_ours(args):
         "metric": METRIC, "value": main["value"], "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": main["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, norm weights 1+0.1N(0,1))",
-        "config": {"workload": w.name, "batch": w.batch, "heads": w.heads, "head_dim": 128,
-                   "tokens": w.tokens, "txt_len": w.txt_len, "img": [w.img_h, w.img_w],
-                   "global_batch": w.batch * world, "seq_len": w.tokens,
-                   "parallelism": "replicas" if world > 1 else "single",
-                   "l2": "flushed before every timed step (256 MB write, outside the step events)"},
+        "config": workload_config(w, world),
         "roofline": {"bound": "tensor", "kernel": "attn_kernel<bf16>", "achieved": main["attn_tflops"],
                      "peak": peak_bf16, "unit": "TFLOP/s", "frac": main["roofline_frac"],
                      "peak_kind": peak_kind + " bf16 burst", "frac_of_2250_nominal": main["frac_of_nominal"],
@@ -556,8 +573,7 @@ def run_reference(args):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1) bf16)", "impl": "reference",
-        "config": {"workload": w.name, "batch": w.batch, "heads": w.heads, "head_dim": 128,
-                   "tokens": w.tokens, "global_batch": w.batch, "seq_len": w.tokens},
+        "config": workload_config(w, world),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

@@ -5,6 +5,7 @@
 // The arithmetic of the path runs in the kernels of prologue.cuh,
 // quantize_fp8.cuh and attention.cuh.
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <cmath>
@@ -42,6 +43,16 @@ struct flux_attn {
 namespace {
 
 thread_local std::string g_last_error;
+
+// An NVTX range over the host-side enqueue of one call or one kernel launch:
+// profilers (Nsight Systems, ncu --nvtx) show the library's steps by name.
+// Header-only NVTX v3; without an attached tool each push / pop is a branch.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 int fail(int status, const char* fmt, ...) {
   char buf[512];
@@ -150,6 +161,7 @@ int launch_prologue(flux_attn* h, const void* q, const void* k, int txt, int ih,
                     const int32_t* pos, const float* wq, const float* wk, __nv_bfloat16* qn, __nv_bfloat16* kn,
                     int n, cudaStream_t stream) {
   (void)rh;
+  NvtxRange range("flux_attn/qk_norm_rope");
   flux::TokenGeometry geo{pos, txt, ih * iw, iw, rw};
   const int B = h->cfg.batch, H = h->cfg.num_heads;
   const int W = flux::stream_warps<flux::Bf16Rows>(H);
@@ -173,6 +185,7 @@ size_t pad16(int n) { return (static_cast<size_t>(n) + 15) & ~size_t(15); }
 int launch_prologue_fp8(flux_attn* h, const void* q, const void* k, const void* v, int txt, int ih, int iw,
                         int rw, const int32_t* pos, const float* wq, const float* wk, int n, uint8_t* q8,
                         uint8_t* k8, uint8_t* v8t, float* scales, cudaStream_t stream) {
+  NvtxRange range("flux_attn/fp8_prologue");
   flux::TokenGeometry geo{pos, txt, ih * iw, iw, rw};
   const int B = h->cfg.batch, H = h->cfg.num_heads;
   const size_t amax_bytes = static_cast<size_t>(B) * H * 3 * sizeof(uint32_t);
@@ -235,6 +248,7 @@ int launch_prologue_fp8(flux_attn* h, const void* q, const void* k, const void* 
 // FP8: qn, kn E4M3 [B*H, n, 128], v E4M3 V^T [B*H, 128, pad16(n)], scales [B*H, 3].
 int launch_attention(flux_attn* h, bool fp8, const void* qn, const void* kn, const void* v, const float* scales,
                      int n, void* out, cudaStream_t stream) {
+  NvtxRange range(fp8 ? "flux_attn/attention_fp8" : "flux_attn/attention");
   using namespace flux::attn;
   const int B = h->cfg.batch, H = h->cfg.num_heads;
   const size_t esz = fp8 ? 1 : 2;
@@ -310,6 +324,7 @@ int launch_attention(flux_attn* h, bool fp8, const void* qn, const void* kn, con
 int launch_qkv(flux_attn* h, const void* x, const void* w, const float* bias, int d_model, int txt, int ih, int iw,
                int rw, const int32_t* pos, const float* wq, const float* wk, void* qn, void* kn, void* v, int n,
                cudaStream_t stream) {
+  NvtxRange range("flux_attn/qkv_gemm");
   using namespace flux::qkv;
   const int B = h->cfg.batch, H = h->cfg.num_heads;
   const int M = B * n;
@@ -555,6 +570,7 @@ int flux_attn_prologue(flux_attn_t h, const void* q, const void* k, int txt_len,
                        int ref_w, const int32_t* pos_ids, const float* q_norm_w, const float* k_norm_w, void* qn,
                        void* kn, cudaStream_t stream) {
   g_last_error.clear();
+  NvtxRange range("flux_attn_prologue");
   int n = 0;
   int rc = check_common(h, q, k, txt_len, img_h, img_w, ref_h, ref_w, pos_ids, q_norm_w, k_norm_w, &n);
   if (rc || n == 0) return rc;
@@ -570,6 +586,7 @@ int flux_attn_prologue(flux_attn_t h, const void* q, const void* k, int txt_len,
 int flux_attn_attend(flux_attn_t h, const void* qn, const void* kn, const void* v, int n_tokens, void* out,
                      cudaStream_t stream) {
   g_last_error.clear();
+  NvtxRange range("flux_attn_attend");
   int rc = check_handle(h);
   if (rc) return rc;
   if (h->cfg.precision != FLUX_ATTN_BF16)
@@ -590,6 +607,7 @@ int flux_attn_forward(flux_attn_t h, const void* q, const void* k, const void* v
                       int img_w, int ref_h, int ref_w, const int32_t* pos_ids, const float* q_norm_w,
                       const float* k_norm_w, void* out, cudaStream_t stream) {
   g_last_error.clear();
+  NvtxRange range("flux_attn_forward");
   int n = 0;
   int rc = check_common(h, q, k, txt_len, img_h, img_w, ref_h, ref_w, pos_ids, q_norm_w, k_norm_w, &n);
   if (rc || n == 0) return rc;
@@ -614,6 +632,7 @@ int flux_attn_prologue_fp8(flux_attn_t h, const void* q, const void* k, const vo
                            const float* k_norm_w, void* q8, void* k8, void* v8t, float* scales,
                            cudaStream_t stream) {
   g_last_error.clear();
+  NvtxRange range("flux_attn_prologue_fp8");
   int n = 0;
   int rc = check_common(h, q, k, txt_len, img_h, img_w, ref_h, ref_w, pos_ids, q_norm_w, k_norm_w, &n);
   if (rc || n == 0) return rc;
@@ -633,6 +652,7 @@ int flux_attn_prologue_fp8(flux_attn_t h, const void* q, const void* k, const vo
 int flux_attn_attend_fp8(flux_attn_t h, const void* q8, const void* k8, const void* v8t, const float* scales,
                          int n_tokens, void* out, cudaStream_t stream) {
   g_last_error.clear();
+  NvtxRange range("flux_attn_attend_fp8");
   int rc = check_handle(h);
   if (rc) return rc;
   if (h->cfg.precision != FLUX_ATTN_FP8_E4M3)
@@ -654,6 +674,7 @@ int flux_attn_qkv(flux_attn_t h, const void* x, const void* w_qkv, const float* 
                   int img_h, int img_w, int ref_h, int ref_w, const int32_t* pos_ids, const float* q_norm_w,
                   const float* k_norm_w, void* qn, void* kn, void* v, cudaStream_t stream) {
   g_last_error.clear();
+  NvtxRange range("flux_attn_qkv");
   int rc = check_handle(h);
   if (rc) return rc;
   if (h->cfg.precision != FLUX_ATTN_BF16) return fail(FLUX_ATTN_ERR_UNSUPPORTED, "flux_attn_qkv needs a BF16 handle");
@@ -686,6 +707,7 @@ int flux_attn_forward_hidden(flux_attn_t h, const void* x, const void* w_qkv, co
                              int txt_len, int img_h, int img_w, int ref_h, int ref_w, const int32_t* pos_ids,
                              const float* q_norm_w, const float* k_norm_w, void* out, cudaStream_t stream) {
   g_last_error.clear();
+  NvtxRange range("flux_attn_forward_hidden");
   int rc = check_handle(h);
   if (rc) return rc;
   if (h->cfg.precision != FLUX_ATTN_BF16)
@@ -786,9 +808,12 @@ extern "C" int flux_attn_forward_noalloc(const flux_attn_config* cfg, const void
                                          const int32_t* pos_ids, const float* q_norm_w, const float* k_norm_w,
                                          void* out, uint32_t* device_error, cudaStream_t stream) {
   g_last_error.clear();
+  NvtxRange range("flux_attn_forward_noalloc");
   if (cfg == nullptr) return fail(FLUX_ATTN_ERR_INVALID_ARG, "cfg is NULL");
   if (cfg->head_dim != flux::kHeadDim)
     return fail(FLUX_ATTN_ERR_UNSUPPORTED, "head_dim = %d, only 128 is built", cfg->head_dim);
+  if (cfg->precision != FLUX_ATTN_BF16 && cfg->precision != FLUX_ATTN_FP8_E4M3)
+    return fail(FLUX_ATTN_ERR_INVALID_ARG, "unknown precision %d", cfg->precision);
   if (cfg->precision != FLUX_ATTN_BF16)
     return fail(FLUX_ATTN_ERR_UNSUPPORTED, "the allocation-free forward is BF16 only");
   if (cfg->batch < 1 || cfg->num_heads < 1 || cfg->max_tokens < 1)

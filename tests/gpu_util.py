@@ -6,17 +6,20 @@ import numpy as np
 import torch
 
 # Tolerances: BF16 max-abs 1e-2 and mean-abs 1e-3, FP8 max-abs 6e-2 (against
-# the oracle on its own dequantised inputs); plus an internal gate on the
-# relative RMS error so that a small systematic error cannot hide under a
-# loose absolute bound.  For FP8 that gate sits above the noise the E4M3
-# rounding of P alone brings: a relative half-step of 2^-4 per probability,
-# i.e. about 2^-4 / sqrt(3) = 3.6 % RMS relative to the output (the error
-# and the output are both sums over the same keys), so 8 %.
+# the oracle on its own dequantised inputs) on the configurations those
+# figures are stated for; plus an internal gate on the relative RMS error so
+# that a small systematic error cannot hide under a loose absolute bound.
+# FP8 output rows are also held, element by element, to the bound the E4M3
+# rounding of P allows (tests/fp8_bound.py).  The FP8 gate sits above the noise
+# of that rounding: an fp64 simulation of the method gives 1.1 - 1.8 % RMS
+# relative to the output on the tiny, edge and full-size FP8 shapes with
+# outliers, and 2.5 - 3.5 % with P rounded to two mantissa bits instead of
+# three (tests/test_fp8_bound.py), so 2.5 %.
 BF16_MAX_ABS = 1e-2
 BF16_MEAN_ABS = 1e-3
 BF16_REL_RMS = 1e-2
 FP8_MAX_ABS = 6e-2
-FP8_REL_RMS = 8e-2
+FP8_REL_RMS = 2.5e-2
 
 
 def dev_bf16(bits: np.ndarray) -> torch.Tensor:
