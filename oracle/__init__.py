@@ -82,6 +82,12 @@ def _load():
             f.argtypes = [P, P, P, I, I, I, I, P, P, P, D, D, P, I, P, L, P, I]
         lib.oracle_qkv_rows.restype = I
         lib.oracle_qkv_rows.argtypes = [P, P, P, I, I, I, I, I, P, P, P, D, D, P, P, L, P, P, P, I]
+        lib.oracle_vc_attention_rows_bf16.restype = I
+        lib.oracle_vc_attention_rows_bf16.argtypes = [P, P, P, I, I, I, I, P, P, P, D, D, P, D, P, L, P, I]
+        lib.oracle_vc_select_head_bf16.restype = L
+        lib.oracle_vc_select_head_bf16.argtypes = [P, P, P, I, I, I, I, P, P, P, D, D, P, D, I, I, P, P, I]
+        lib.oracle_vc_repair_count.restype = L
+        lib.oracle_vc_repair_count.argtypes = [D, L]
         lib.oracle_fp8_quantize_head_bf16.restype = I
         lib.oracle_fp8_quantize_head_bf16.argtypes = [P, P, P, I, I, I, I, P, P, P, D, D, P, I, I,
                                                       P, P, P, P, I]
@@ -203,6 +209,60 @@ def fp8_quantize_head(q, k, v, pos, w_q, w_k, b: int, h: int, eps: float = 1e-6,
     if rc != 0:
         raise ValueError("oracle_fp8_quantize_head failed: %d" % rc)
     return q8, k8, v8, sc
+
+
+def vc_repair_count(rho: float, n_tokens: int) -> int:
+    """R = ceil(rho N), clamped to [0, N]: how many key tokens a head repairs."""
+    return int(_load().oracle_vc_repair_count(float(rho), int(n_tokens)))
+
+
+def vc_attention_rows(q, k, v, pos, w_q, w_k, rho: float, rows: Optional[np.ndarray] = None,
+                      eps: float = 1e-6, theta: float = 10000.0, axes: Sequence[int] = AXES_DEFAULT,
+                      nthreads: int = 0) -> np.ndarray:
+    """VC-Attention FP8 rows (reading R7 of the C source): FP8 attention over the
+    dequantised Q', K', V with the ceil(rho N) worst-quantised key tokens of
+    every head taking part with their exact K', V.  Arguments and result as
+    attention_rows with bf16 inputs."""
+    lib = _load()
+    B, N, H, d = q.shape
+    full = rows is None
+    if full:
+        bb, hh, nn = np.meshgrid(np.arange(B), np.arange(H), np.arange(N), indexing="ij")
+        rows = np.stack([bb.ravel(), hh.ravel(), nn.ravel()], 1)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    R = rows.shape[0]
+    out = np.empty((R, d), np.float64)
+    q, k, v = (np.ascontiguousarray(t, dtype=np.uint16) for t in (q, k, v))
+    pos = np.ascontiguousarray(pos, dtype=np.int32)
+    wq = np.ascontiguousarray(w_q, dtype=np.float32)
+    wk = np.ascontiguousarray(w_k, dtype=np.float32)
+    rc = lib.oracle_vc_attention_rows_bf16(_ptr(q), _ptr(k), _ptr(v), B, N, H, d, _ptr(pos), _ptr(wq), _ptr(wk),
+                                           eps, theta, _ptr(_axes(axes)), float(rho), _ptr(rows), R, _ptr(out),
+                                           nthreads)
+    if rc != 0:
+        raise ValueError("oracle_vc_attention_rows failed: %d" % rc)
+    if full:
+        return out.reshape(B, H, N, d).transpose(0, 2, 1, 3).copy()
+    return out
+
+
+def vc_select_head(q, k, v, pos, w_q, w_k, rho: float, b: int, h: int, eps: float = 1e-6,
+                   theta: float = 10000.0, axes: Sequence[int] = AXES_DEFAULT, nthreads: int = 0):
+    """Reading R7 for head (b, h): (selected token indices ascending, int64 [R];
+    the quantisation error e_m of every key token, float64 [N])."""
+    lib = _load()
+    B, N, H, d = q.shape
+    q, k, v = (np.ascontiguousarray(t, dtype=np.uint16) for t in (q, k, v))
+    pos = np.ascontiguousarray(pos, dtype=np.int32)
+    wq = np.ascontiguousarray(w_q, dtype=np.float32)
+    wk = np.ascontiguousarray(w_k, dtype=np.float32)
+    sel = np.empty(N, np.int64)
+    err = np.empty(N, np.float64)
+    R = lib.oracle_vc_select_head_bf16(_ptr(q), _ptr(k), _ptr(v), B, N, H, d, _ptr(pos), _ptr(wq), _ptr(wk), eps,
+                                       theta, _ptr(_axes(axes)), float(rho), b, h, _ptr(sel), _ptr(err), nthreads)
+    if R < 0:
+        raise ValueError("oracle_vc_select_head failed: %d" % R)
+    return sel[:R].copy(), err
 
 
 def qkv_rows(x: np.ndarray, w: np.ndarray, bias: Optional[np.ndarray], n_tokens: int, pos: np.ndarray,

@@ -23,6 +23,10 @@
  *   - same page, section "GEMM kernel optimisation": the QKV projection is
  *     one GEMM of the hidden states with the stacked Q, K, V weights, and its
  *     epilogue applies the query/key normalisation and RoPE (oracle_qkv_rows).
+ *   - same page, section "Quantized and sparse attention": VC-Attention FP8
+ *     uses a repair budget (vc_repair_budget 0.005 in its configuration) that
+ *     picks the fraction of tokens with the highest quantisation error for a
+ *     residual correction (oracle_vc_attention_rows, reading R7).
  *
  * Readings taken where the pages are silent:
  *   R1 RMSNorm over the head dimension d: y_i = x_i / sqrt(mean_j x_j^2 + eps) * w_i,
@@ -41,6 +45,15 @@
  *      0 .. H d - 1), K (the next H d) and V (the last H d), head h owning
  *      features h d .. h d + d - 1 of its part; Q and K then get R1-R3, V
  *      nothing.
+ *   R7 VC-Attention repair, per (batch, head), after the quantisation of R5:
+ *      key token m has the quantisation error
+ *        e_m = |k'_m - deq(k'_m)|^2 + |v_m - deq(v_m)|^2
+ *      (squared Euclidean norms of its K' and V rows, in their own units);
+ *      the R = ceil(rho N) tokens with the largest e_m (equal errors: the
+ *      lower token index first) are repaired: their residual x - deq(x) is
+ *      added back, i.e. they take part in the attention with their exact K'
+ *      and V, every other key keeps its dequantised values, and every query
+ *      keeps its dequantised Q'.  rho = 0 is plain FP8 attention.
  *
  * Every loop below follows the definition directly: no tiling, no online
  * softmax, no reordering beyond summation order inside a dot product.
@@ -209,6 +222,62 @@ static void attention_row(double* o, const double* qh, const double* kh, const d
   }
 }
 
+/* ---------------------------------------------- VC-Attention repair (R7) */
+
+typedef struct {
+  double e;
+  int64_t m;
+} vc_key_t;
+
+/* Larger error first; equal errors: lower token index first. */
+static int vc_key_cmp(const void* a, const void* b) {
+  const vc_key_t* x = (const vc_key_t*)a;
+  const vc_key_t* y = (const vc_key_t*)b;
+  if (x->e > y->e) return -1;
+  if (x->e < y->e) return 1;
+  return (x->m > y->m) - (x->m < y->m);
+}
+
+static int i64_cmp(const void* a, const void* b) {
+  int64_t x = *(const int64_t*)a, y = *(const int64_t*)b;
+  return (x > y) - (x < y);
+}
+
+/* R = ceil(rho N), clamped to [0, N]. */
+int64_t oracle_vc_repair_count(double rho, int64_t N) {
+  double r = ceil(rho * (double)N);
+  if (!(r > 0.0)) return 0;
+  if (r > (double)N) return N;
+  return (int64_t)r;
+}
+
+/* Errors e_m of every key token of one head and its repair set: kx, vx the
+ * exact K' and V rows, kq, vq their dequantised values ([N*d] each).  err
+ * receives e_m [N], sel the R selected token indices in ascending order.
+ * Returns R, or -1 when memory runs out. */
+static int64_t vc_select(const double* kx, const double* kq, const double* vx, const double* vq, int64_t N,
+                         int d, double rho, int64_t* sel, double* err) {
+  int64_t R = oracle_vc_repair_count(rho, N);
+  vc_key_t* keys = (vc_key_t*)malloc(sizeof(vc_key_t) * (N > 0 ? N : 1));
+  if (!keys) return -1;
+  for (int64_t m = 0; m < N; ++m) {
+    double e = 0.0;
+    for (int i = 0; i < d; ++i) {
+      double dk = kx[m * d + i] - kq[m * d + i];
+      double dv = vx[m * d + i] - vq[m * d + i];
+      e += dk * dk + dv * dv;
+    }
+    err[m] = e;
+    keys[m].e = e;
+    keys[m].m = m;
+  }
+  qsort(keys, (size_t)N, sizeof(vc_key_t), vc_key_cmp);
+  for (int64_t r = 0; r < R; ++r) sel[r] = keys[r].m;
+  qsort(sel, (size_t)R, sizeof(int64_t), i64_cmp);
+  free(keys);
+  return R;
+}
+
 /* ------------------------------------------------------------ public API */
 
 int oracle_max_threads(void) {
@@ -263,7 +332,7 @@ int oracle_prologue_f64(const double* x, int B, int N, int H, int d, const int32
  * once per distinct head in order of first appearance. */
 static int attention_rows(const src_t* q, const src_t* k, const src_t* v, int B, int N, int H,
                           int d, const int32_t* pos, const double* wq, const double* wk,
-                          double eps, double theta, const int* axes, int fp8,
+                          double eps, double theta, const int* axes, int fp8, double rho,
                           const int64_t* rows, int64_t nrows, double* out, int nt) {
   if (check_axes(d, axes) || d > 1024 || B <= 0 || N <= 0 || H <= 0) return -1;
   for (int64_t r = 0; r < nrows; ++r) {
@@ -277,8 +346,14 @@ static int attention_rows(const src_t* q, const src_t* k, const src_t* v, int B,
   double* qh = (double*)malloc(sizeof(double) * nd);
   unsigned char* done = (unsigned char*)calloc((size_t)B * H, 1);
   int64_t* idx = (int64_t*)malloc(sizeof(int64_t) * (nrows > 0 ? nrows : 1));
-  if (!kh || !vh || !qh || !done || !idx) {
+  int vc = fp8 && rho > 0.0;
+  double* kx = vc ? (double*)malloc(sizeof(double) * nd) : NULL;  /* exact K', V (R7) */
+  double* vx = vc ? (double*)malloc(sizeof(double) * nd) : NULL;
+  double* err = vc ? (double*)malloc(sizeof(double) * N) : NULL;
+  int64_t* sel = vc ? (int64_t*)malloc(sizeof(int64_t) * N) : NULL;
+  if (!kh || !vh || !qh || !done || !idx || (vc && (!kx || !vx || !err || !sel))) {
     free(kh); free(vh); free(qh); free(done); free(idx);
+    free(kx); free(vx); free(err); free(sel);
     return -3;
   }
   for (int64_t r0 = 0; r0 < nrows; ++r0) {
@@ -293,9 +368,26 @@ static int attention_rows(const src_t* q, const src_t* k, const src_t* v, int B,
     plain_head(vh, v, b, h, N, H, d, nt);
     if (fp8) {
       prologue_head(qh, q, b, h, N, H, d, pos, wq, eps, theta, axes, nt);
+      if (vc) {
+        memcpy(kx, kh, sizeof(double) * nd);
+        memcpy(vx, vh, sizeof(double) * nd);
+      }
       fp8_roundtrip(qh, nd, NULL);
       fp8_roundtrip(kh, nd, NULL);
       fp8_roundtrip(vh, nd, NULL);
+      if (vc) {
+        /* R7: the selected tokens take part with their exact K' and V */
+        int64_t R = vc_select(kx, kh, vx, vh, N, d, rho, sel, err);
+        if (R < 0) {
+          free(kh); free(vh); free(qh); free(done); free(idx);
+          free(kx); free(vx); free(err); free(sel);
+          return -3;
+        }
+        for (int64_t r = 0; r < R; ++r) {
+          memcpy(kh + sel[r] * d, kx + sel[r] * d, sizeof(double) * d);
+          memcpy(vh + sel[r] * d, vx + sel[r] * d, sizeof(double) * d);
+        }
+      }
     }
     int64_t t;
 #pragma omp parallel for num_threads(nt) schedule(dynamic, 4)
@@ -320,6 +412,7 @@ static int attention_rows(const src_t* q, const src_t* k, const src_t* v, int B,
     }
   }
   free(kh); free(vh); free(qh); free(done); free(idx);
+  free(kx); free(vx); free(err); free(sel);
   return 0;
 }
 
@@ -332,7 +425,7 @@ int oracle_attention_rows_bf16(const uint16_t* q, const uint16_t* k, const uint1
   if (d > 1024 || d <= 0) return -1;
   for (int i = 0; i < d; ++i) { wq[i] = wqf[i]; wk[i] = wkf[i]; }
   src_t sq = {q, 1}, sk = {k, 1}, sv = {v, 1};
-  return attention_rows(&sq, &sk, &sv, B, N, H, d, pos, wq, wk, eps, theta, axes, fp8,
+  return attention_rows(&sq, &sk, &sv, B, N, H, d, pos, wq, wk, eps, theta, axes, fp8, 0.0,
                         rows, nrows, out, nt);
 }
 
@@ -342,7 +435,23 @@ int oracle_attention_rows_f64(const double* q, const double* k, const double* v,
                               const int* axes, int fp8, const int64_t* rows, int64_t nrows,
                               double* out, int nt) {
   src_t sq = {q, 0}, sk = {k, 0}, sv = {v, 0};
-  return attention_rows(&sq, &sk, &sv, B, N, H, d, pos, wq, wk, eps, theta, axes, fp8,
+  return attention_rows(&sq, &sk, &sv, B, N, H, d, pos, wq, wk, eps, theta, axes, fp8, 0.0,
+                        rows, nrows, out, nt);
+}
+
+/* VC-Attention FP8 (readings R5, R7): like oracle_attention_rows_bf16 with
+ * fp8 = 1, the R = ceil(rho N) worst-quantised key tokens of every head
+ * repaired. */
+int oracle_vc_attention_rows_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                  int B, int N, int H, int d, const int32_t* pos,
+                                  const float* wqf, const float* wkf, double eps, double theta,
+                                  const int* axes, double rho, const int64_t* rows, int64_t nrows,
+                                  double* out, int nt) {
+  double wq[1024], wk[1024];
+  if (d > 1024 || d <= 0 || !(rho >= 0.0 && rho <= 1.0)) return -1;
+  for (int i = 0; i < d; ++i) { wq[i] = wqf[i]; wk[i] = wkf[i]; }
+  src_t sq = {q, 1}, sk = {k, 1}, sv = {v, 1};
+  return attention_rows(&sq, &sk, &sv, B, N, H, d, pos, wq, wk, eps, theta, axes, 1, rho,
                         rows, nrows, out, nt);
 }
 
@@ -370,6 +479,43 @@ int oracle_fp8_quantize_head_bf16(const uint16_t* q, const uint16_t* k, const ui
   scales[2] = fp8_roundtrip(t, nd, v8);
   free(t);
   return 0;
+}
+
+/* Reading R7 for one head (b, h): the quantisation error e_m of every key
+ * token (err, [N]) and the repaired tokens in ascending order (sel, room for
+ * N).  Returns R, or a negative value on bad arguments. */
+int64_t oracle_vc_select_head_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                   int B, int N, int H, int d, const int32_t* pos,
+                                   const float* wqf, const float* wkf, double eps, double theta,
+                                   const int* axes, double rho, int b, int h, int64_t* sel,
+                                   double* err, int nt) {
+  double wk[1024];
+  (void)q;
+  (void)wqf;
+  if (check_axes(d, axes) || d > 1024 || b < 0 || b >= B || h < 0 || h >= H || N <= 0 ||
+      !(rho >= 0.0 && rho <= 1.0))
+    return -1;
+  for (int i = 0; i < d; ++i) wk[i] = wkf[i];
+  nt = nthreads_or_max(nt);
+  int64_t nd = (int64_t)N * d;
+  double* kx = (double*)malloc(sizeof(double) * nd);
+  double* kq = (double*)malloc(sizeof(double) * nd);
+  double* vx = (double*)malloc(sizeof(double) * nd);
+  double* vq = (double*)malloc(sizeof(double) * nd);
+  int64_t R = -3;
+  if (kx && kq && vx && vq) {
+    src_t sk = {k, 1}, sv = {v, 1};
+    prologue_head(kx, &sk, b, h, N, H, d, pos, wk, eps, theta, axes, nt);
+    plain_head(vx, &sv, b, h, N, H, d, nt);
+    memcpy(kq, kx, sizeof(double) * nd);
+    memcpy(vq, vx, sizeof(double) * nd);
+    fp8_roundtrip(kq, nd, NULL);
+    fp8_roundtrip(vq, nd, NULL);
+    R = vc_select(kx, kq, vx, vq, N, d, rho, sel, err);
+    if (R < 0) R = -3;
+  }
+  free(kx); free(kq); free(vx); free(vq);
+  return R;
 }
 
 /* Reading R6: the QKV projection of the requested token rows, then the

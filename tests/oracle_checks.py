@@ -19,7 +19,13 @@ What the checks compare the oracle with:
     midpoints round to the even code, out-of-range values saturate;
   * the QKV projection: numpy's fp64 matmul (with torch rms_norm and the
     complex-rotation RoPE on its Q and K parts), identity weights (the
-    prologue of x itself), a zero weight matrix (the bias alone).
+    prologue of x itself), a zero weight matrix (the bias alone);
+  * the VC-Attention repair (reading R7): a brute-force restatement from the
+    library routines (torch rms_norm, complex RoPE, torch's E4M3 cast, a
+    Python sort of (error, index) pairs, torch SDPA); rho = 0 is plain FP8
+    attention bit for bit, rho = 1 is SDPA over the dequantised Q' and the
+    exact K', V; equal errors go to the lower token index; a planted
+    badly-quantised token is always selected.
 """
 from __future__ import annotations
 
@@ -413,6 +419,104 @@ def check_fp8_zero_head():
     assert np.all(sc == 1.0)
 
 
+# ------------------------------------------------- VC-Attention repair (R7)
+
+def _lib_deq(x):
+    """Dequantised copy of one head's [N, d] values by torch's E4M3 cast (R5)."""
+    amax = float(np.max(np.abs(x)))
+    if amax == 0.0:
+        return x.copy()
+    return _torch_e4m3(448.0 * x / amax).to(torch.float64).numpy() * (amax / 448.0)
+
+
+def _lib_vc(q, k, v, pos, wq, wk, rho):
+    """Brute-force VC-Attention from library routines: (output [B, N, H, d],
+    per-head errors {(b, h): [N]}, per-head selections {(b, h): sorted list})."""
+    qn = lib_rope(lib_rms(bf16_bits_to_f32(q).astype(np.float64), wq), pos)
+    kn = lib_rope(lib_rms(bf16_bits_to_f32(k).astype(np.float64), wk), pos)
+    vf = bf16_bits_to_f32(v).astype(np.float64)
+    B, N, H, _ = q.shape
+    R = min(N, max(0, math.ceil(rho * N)))
+    qd, kh, vh = np.empty_like(qn), np.empty_like(kn), np.empty_like(vf)
+    errs, sels = {}, {}
+    for b in range(B):
+        for h in range(H):
+            qd[b, :, h] = _lib_deq(qn[b, :, h])
+            kd, vd = _lib_deq(kn[b, :, h]), _lib_deq(vf[b, :, h])
+            err = ((kn[b, :, h] - kd) ** 2).sum(axis=1) + ((vf[b, :, h] - vd) ** 2).sum(axis=1)
+            chosen = sorted(sorted(range(N), key=lambda m: (-err[m], m))[:R])
+            kd[chosen] = kn[b, chosen, h]
+            vd[chosen] = vf[b, chosen, h]
+            kh[b, :, h], vh[b, :, h] = kd, vd
+            errs[(b, h)], sels[(b, h)] = err, chosen
+    return lib_attention(qd, kh, vh), errs, sels
+
+
+def check_vc_matches_library_reference():
+    q, k, v, pos, wq, wk = _fp8_inputs(21)
+    for rho in (0.05, 0.3):
+        want, errs, sels = _lib_vc(q, k, v, pos, wq, wk, rho)
+        got = oracle.vc_attention_rows(q, k, v, pos, wq, wk, rho)
+        _close(got, want, 1e-12, "VC rho=%g vs the library reference" % rho)
+        assert oracle.vc_repair_count(rho, q.shape[1]) == len(sels[(0, 0)])
+        for (b, h), chosen in sels.items():
+            sel, err = oracle.vc_select_head(q, k, v, pos, wq, wk, rho, b, h)
+            assert list(sel) == chosen, "VC selection of head (%d, %d)" % (b, h)
+            np.testing.assert_allclose(err, errs[(b, h)], rtol=1e-10, atol=1e-300)
+
+
+def check_vc_rho_zero_is_fp8_and_rho_one_exact_kv():
+    q, k, v, pos, wq, wk = _fp8_inputs(22)
+    plain = oracle.attention_rows(q, k, v, pos, wq, wk, fp8=True)
+    assert np.array_equal(oracle.vc_attention_rows(q, k, v, pos, wq, wk, 0.0), plain)
+    qn = lib_rope(lib_rms(bf16_bits_to_f32(q).astype(np.float64), wq), pos)
+    kn = lib_rope(lib_rms(bf16_bits_to_f32(k).astype(np.float64), wk), pos)
+    vf = bf16_bits_to_f32(v).astype(np.float64)
+    qd = np.empty_like(qn)
+    for b in range(q.shape[0]):
+        for h in range(q.shape[2]):
+            qd[b, :, h] = _lib_deq(qn[b, :, h])
+    _close(oracle.vc_attention_rows(q, k, v, pos, wq, wk, 1.0), lib_attention(qd, kn, vf), 1e-12,
+           "VC rho=1 vs SDPA over dequantised Q' and exact K', V")
+
+
+def _plant(v, b, h, n, rng):
+    """V row n of head (b, h) at +-7 (7 * 448 / 7.75 = 404.6: between the codes
+    384 and 416, an error of 11.4 code steps per element) with the head's
+    amax 7.75 set elsewhere: by far the head's worst-quantised token."""
+    row = np.where(rng.random(D) < 0.5, -7.0, 7.0).astype(np.float32)
+    v[b, n, h] = bf16_bits_from_f32(row)
+    other = bf16_bits_to_f32(v[b, n - 1, h]).copy()
+    other[0] = 7.75
+    v[b, n - 1, h] = bf16_bits_from_f32(other)
+
+
+def check_vc_equal_errors_take_the_lower_index():
+    q, k, v, pos, wq, wk = _fp8_inputs(23)
+    rng = _rng(23)
+    _plant(v, 1, 0, 2, rng)
+    k[1, 5, 0], v[1, 5, 0] = k[1, 2, 0], v[1, 2, 0]   # text tokens 2 and 5 share position (0, 0, 0)
+    N = q.shape[1]
+    sel1, err = oracle.vc_select_head(q, k, v, pos, wq, wk, 0.5 / N, 1, 0)
+    assert err[2] == err[5] and err[2] == err.max()
+    assert list(sel1) == [2]
+    sel2, _ = oracle.vc_select_head(q, k, v, pos, wq, wk, 1.5 / N, 1, 0)
+    assert list(sel2) == [2, 5]
+
+
+def check_vc_planted_token_is_always_repaired():
+    q, k, v, pos, wq, wk = _fp8_inputs(24)
+    _plant(v, 0, 1, 17, _rng(24))
+    N = q.shape[1]
+    plain = oracle.attention_rows(q, k, v, pos, wq, wk, fp8=True)
+    for rho in (0.5 / N, 0.1, 0.6):
+        sel, err = oracle.vc_select_head(q, k, v, pos, wq, wk, rho, 0, 1)
+        assert 17 in sel and np.argmax(err) == 17
+        assert np.all(np.diff(sel) > 0)
+        got = oracle.vc_attention_rows(q, k, v, pos, wq, wk, rho)
+        assert np.max(np.abs(got[0, :, 1] - plain[0, :, 1])) > 1e-4   # the repair matters
+
+
 # --------------------------------------------------------- QKV projection
 
 def _bf16(a):
@@ -504,4 +608,8 @@ ALL_CHECKS = [
     check_qkv_matches_numpy_matmul,
     check_qkv_identity_weights,
     check_qkv_bias_only,
+    check_vc_matches_library_reference,
+    check_vc_rho_zero_is_fp8_and_rho_one_exact_kv,
+    check_vc_equal_errors_take_the_lower_index,
+    check_vc_planted_token_is_always_repaired,
 ]

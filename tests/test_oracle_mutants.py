@@ -36,6 +36,13 @@ MUTANTS = {
     "qkv_swap_q_k": ("rmsnorm_row(q, y + (int64_t)h * d, d, wq, eps);", "rmsnorm_row(q, y + (int64_t)(H + h) * d, d, wq, eps);"),
     "qkv_x_row_of_token": ("xr[c] = bf16_to_f64(x[m * D + c]);", "xr[c] = bf16_to_f64(x[n * D + c]);"),
     "qkv_q_weights_everywhere": ("bf16_to_f64(w[(int64_t)o * D + c])", "bf16_to_f64(w[(int64_t)(o % (H * d)) * D + c])"),
+    "vc_error_k_only": ("e += dk * dk + dv * dv;", "e += dk * dk;"),
+    "vc_error_of_value_not_residual": ("double dv = vx[m * d + i] - vq[m * d + i];", "double dv = vx[m * d + i];"),
+    "vc_smallest_errors": ("if (x->e > y->e) return -1;\n  if (x->e < y->e) return 1;",
+                           "if (x->e < y->e) return -1;\n  if (x->e > y->e) return 1;"),
+    "vc_ties_higher_index": ("return (x->m > y->m) - (x->m < y->m);", "return (x->m < y->m) - (x->m > y->m);"),
+    "vc_count_floor": ("double r = ceil(rho * (double)N);", "double r = floor(rho * (double)N);"),
+    "vc_repair_v_only": ("memcpy(kh + sel[r] * d, kx + sel[r] * d, sizeof(double) * d);", "(void)0;"),
     "qkv_v_normalised": ("for (int i = 0; i < d; ++i) v[i] = y[(int64_t)(2 * H + h) * d + i];", "rmsnorm_row(v, y + (int64_t)(2 * H + h) * d, d, wk, eps);"),
 }
 
