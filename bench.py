@@ -237,11 +237,12 @@ class Step:
     @property
     def prologue_bytes(self):
         """Algorithmic HBM bytes of the prologue per step.  BF16: read q, k and
-        write Q', K' (2 + 2 bytes per element each).  FP8: one E4M3 byte written
-        per element of each of Q', K', V (3 bytes per (b, n, h, d)), the
-        figure the hot-path scope fixes for this step."""
+        write Q', K' (2 + 2 bytes per element each).  FP8: per element of each
+        of Q', K', V, one bf16 read and one E4M3 byte written (3 bytes, so 9 per
+        (b, n, h, d): 934 MB on the CFG pair), the figure the hot-path scope
+        fixes for this step."""
         elems = self.w.batch * self.w.tokens * self.w.heads * 128
-        return elems * (3 if self.fp8 else 8)
+        return elems * (9 if self.fp8 else 8)
 
     @property
     def prologue_traffic_min(self):
