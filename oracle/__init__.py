@@ -86,6 +86,10 @@ def _load():
         lib.oracle_vc_attention_rows_bf16.argtypes = [P, P, P, I, I, I, I, P, P, P, D, D, P, D, P, L, P, I]
         lib.oracle_vc_select_head_bf16.restype = L
         lib.oracle_vc_select_head_bf16.argtypes = [P, P, P, I, I, I, I, P, P, P, D, D, P, D, I, I, P, P, I]
+        lib.oracle_sol_mask_bf16.restype = L
+        lib.oracle_sol_mask_bf16.argtypes = [P, P, I, I, I, I, P, P, P, D, D, P, D, I, I, P, P, I]
+        lib.oracle_sol_attention_rows_bf16.restype = I
+        lib.oracle_sol_attention_rows_bf16.argtypes = [P, P, P, I, I, I, I, P, P, P, D, D, P, D, P, L, P, I]
         lib.oracle_vc_repair_count.restype = L
         lib.oracle_vc_repair_count.argtypes = [D, L]
         lib.oracle_fp8_quantize_head_bf16.restype = I
@@ -263,6 +267,54 @@ def vc_select_head(q, k, v, pos, w_q, w_k, rho: float, b: int, h: int, eps: floa
     if R < 0:
         raise ValueError("oracle_vc_select_head failed: %d" % R)
     return sel[:R].copy(), err
+
+
+def sol_mask(q, k, pos, w_q, w_k, tau: float, b: int, h: int, eps: float = 1e-6, theta: float = 10000.0,
+             axes: Sequence[int] = AXES_DEFAULT, nthreads: int = 0):
+    """Reading R8 for head (b, h): (keep bool [nb, nb], mass float64 [nb, nb]) --
+    query block i keeps key block j, and the pooled mass mu_ij."""
+    lib = _load()
+    B, N, H, d = q.shape
+    nb = (N + 127) // 128
+    q, k = (np.ascontiguousarray(t, dtype=np.uint16) for t in (q, k))
+    pos = np.ascontiguousarray(pos, dtype=np.int32)
+    wq = np.ascontiguousarray(w_q, dtype=np.float32)
+    wk = np.ascontiguousarray(w_k, dtype=np.float32)
+    keep = np.empty((nb, nb), np.uint8)
+    mass = np.empty((nb, nb), np.float64)
+    r = lib.oracle_sol_mask_bf16(_ptr(q), _ptr(k), B, N, H, d, _ptr(pos), _ptr(wq), _ptr(wk), eps, theta,
+                                 _ptr(_axes(axes)), float(tau), b, h, _ptr(keep), _ptr(mass), nthreads)
+    if r != nb:
+        raise ValueError("oracle_sol_mask failed: %d" % r)
+    return keep.astype(bool), mass
+
+
+def sol_attention_rows(q, k, v, pos, w_q, w_k, tau: float, rows: Optional[np.ndarray] = None, eps: float = 1e-6,
+                       theta: float = 10000.0, axes: Sequence[int] = AXES_DEFAULT, nthreads: int = 0) -> np.ndarray:
+    """Sol-Attention rows (reading R8 of the C source): each query attends to
+    the keys of the 128-token key blocks its query block keeps.  Arguments
+    and result as attention_rows with bf16 inputs."""
+    lib = _load()
+    B, N, H, d = q.shape
+    full = rows is None
+    if full:
+        bb, hh, nn = np.meshgrid(np.arange(B), np.arange(H), np.arange(N), indexing="ij")
+        rows = np.stack([bb.ravel(), hh.ravel(), nn.ravel()], 1)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    R = rows.shape[0]
+    out = np.empty((R, d), np.float64)
+    q, k, v = (np.ascontiguousarray(t, dtype=np.uint16) for t in (q, k, v))
+    pos = np.ascontiguousarray(pos, dtype=np.int32)
+    wq = np.ascontiguousarray(w_q, dtype=np.float32)
+    wk = np.ascontiguousarray(w_k, dtype=np.float32)
+    rc = lib.oracle_sol_attention_rows_bf16(_ptr(q), _ptr(k), _ptr(v), B, N, H, d, _ptr(pos), _ptr(wq), _ptr(wk),
+                                            eps, theta, _ptr(_axes(axes)), float(tau), _ptr(rows), R, _ptr(out),
+                                            nthreads)
+    if rc != 0:
+        raise ValueError("oracle_sol_attention_rows failed: %d" % rc)
+    if full:
+        return out.reshape(B, H, N, d).transpose(0, 2, 1, 3).copy()
+    return out
 
 
 def qkv_rows(x: np.ndarray, w: np.ndarray, bias: Optional[np.ndarray], n_tokens: int, pos: np.ndarray,

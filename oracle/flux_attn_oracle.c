@@ -27,6 +27,9 @@
  *     uses a repair budget (vc_repair_budget 0.005 in its configuration) that
  *     picks the fraction of tokens with the highest quantisation error for a
  *     residual correction (oracle_vc_attention_rows, reading R7).
+ *   - same page, section "Quantized and sparse attention": Sol-Attention
+ *     (algorithm sol_attn, tau 1.0, disabled_until_timestep 0.96) runs
+ *     block-sparse attention (oracle_sol_attention_rows, reading R8).
  *
  * Readings taken where the pages are silent:
  *   R1 RMSNorm over the head dimension d: y_i = x_i / sqrt(mean_j x_j^2 + eps) * w_i,
@@ -54,6 +57,19 @@
  *      added back, i.e. they take part in the attention with their exact K'
  *      and V, every other key keeps its dequantised values, and every query
  *      keeps its dequantised Q'.  rho = 0 is plain FP8 attention.
+ *   R8 Sol-Attention, per (batch, head): queries and keys are cut into blocks
+ *      of 128 tokens (the last one ragged), nb blocks each.  A block's pooled
+ *      vector is the mean of its normalised, rotated rows (q_bar_i, k_bar_j);
+ *      query block i gives key block j the mass
+ *        mu_ij = c_j exp(q_bar_i . k_bar_j / sqrt(d)) / sum_j' c_j' exp(q_bar_i . k_bar_j' / sqrt(d))
+ *      (c_j = keys in block j: the pooled estimate of the softmax mass of the
+ *      block), and keeps it when mu_ij >= tau / nb, i.e. at least tau times
+ *      the mass of a uniform split; the block of largest mass (lowest index
+ *      on ties) is always kept.  A query then attends, with the usual
+ *      softmax, to the keys of its kept blocks only.  tau = 0 keeps every
+ *      block (dense attention); the timestep gate of the configuration
+ *      (dense while the timestep is above disabled_until_timestep) is the
+ *      caller's choice of tau.
  *
  * Every loop below follows the definition directly: no tiling, no online
  * softmax, no reordering beyond summation order inside a dot product.
@@ -276,6 +292,84 @@ static int64_t vc_select(const double* kx, const double* kq, const double* vx, c
   qsort(sel, (size_t)R, sizeof(int64_t), i64_cmp);
   free(keys);
   return R;
+}
+
+/* ---------------------------------------------------- Sol-Attention (R8) */
+
+/* Block mask of one head: keep[i * nb + j] = 1 when query block i keeps key
+ * block j; mass[i * nb + j] = mu_ij.  qh, kh: the head's Q', K' [N * d]. */
+static void sol_mask(const double* qh, const double* kh, int64_t N, int d, double tau, unsigned char* keep,
+                     double* mass) {
+  const int64_t bs = 128;
+  const int64_t nb = (N + bs - 1) / bs;
+  double* qb = (double*)calloc((size_t)(nb * d), sizeof(double));
+  double* kb = (double*)calloc((size_t)(nb * d), sizeof(double));
+  double* cnt = (double*)calloc((size_t)nb, sizeof(double));
+  double* sc = (double*)malloc(sizeof(double) * (nb > 0 ? nb : 1));
+  if (!qb || !kb || !cnt || !sc) {
+    free(qb); free(kb); free(cnt); free(sc);
+    for (int64_t i = 0; i < nb * nb; ++i) { keep[i] = 1; mass[i] = NAN; }
+    return;
+  }
+  for (int64_t n = 0; n < N; ++n) {
+    int64_t blk = n / bs;
+    cnt[blk] += 1.0;
+    for (int i = 0; i < d; ++i) {
+      qb[blk * d + i] += qh[n * d + i];
+      kb[blk * d + i] += kh[n * d + i];
+    }
+  }
+  for (int64_t blk = 0; blk < nb; ++blk)
+    for (int i = 0; i < d; ++i) {
+      qb[blk * d + i] /= cnt[blk];
+      kb[blk * d + i] /= cnt[blk];
+    }
+  const double scale = 1.0 / sqrt((double)d);
+  for (int64_t i = 0; i < nb; ++i) {
+    double mx = -INFINITY;
+    for (int64_t j = 0; j < nb; ++j) {
+      double s = 0.0;
+      for (int t = 0; t < d; ++t) s += qb[i * d + t] * kb[j * d + t];
+      sc[j] = s * scale + log(cnt[j]);
+      if (sc[j] > mx) mx = sc[j];
+    }
+    double z = 0.0;
+    for (int64_t j = 0; j < nb; ++j) z += exp(sc[j] - mx);
+    int64_t best = 0;
+    for (int64_t j = 0; j < nb; ++j) {
+      mass[i * nb + j] = exp(sc[j] - mx) / z;
+      if (mass[i * nb + j] > mass[i * nb + best]) best = j;
+    }
+    for (int64_t j = 0; j < nb; ++j)
+      keep[i * nb + j] = (unsigned char)(mass[i * nb + j] >= tau / (double)nb || j == best);
+  }
+  free(qb); free(kb); free(cnt); free(sc);
+}
+
+/* One output row over the keys of the kept blocks of its query block. */
+static void sol_attention_row(double* o, const double* qh, const double* kh, const double* vh, int64_t N, int d,
+                              const unsigned char* keep_row, double* srow) {
+  const double scale = 1.0 / sqrt((double)d);
+  double mx = -INFINITY;
+  for (int64_t m = 0; m < N; ++m) {
+    if (!keep_row[m / 128]) continue;
+    double s = 0.0;
+    for (int i = 0; i < d; ++i) s += qh[i] * kh[m * d + i];
+    srow[m] = s * scale;
+    if (srow[m] > mx) mx = srow[m];
+  }
+  double l = 0.0;
+  for (int64_t m = 0; m < N; ++m) {
+    if (!keep_row[m / 128]) continue;
+    srow[m] = exp(srow[m] - mx);
+    l += srow[m];
+  }
+  for (int i = 0; i < d; ++i) o[i] = 0.0;
+  for (int64_t m = 0; m < N; ++m) {
+    if (!keep_row[m / 128]) continue;
+    const double w = srow[m] / l;
+    for (int i = 0; i < d; ++i) o[i] += w * vh[m * d + i];
+  }
 }
 
 /* ------------------------------------------------------------ public API */
@@ -566,5 +660,79 @@ int oracle_qkv_rows(const uint16_t* x, const uint16_t* w, const float* bias, int
     free(y);
     free(xr);
   }
+  return 0;
+}
+
+/* Reading R8 for head (b, h): keep [nb * nb] (1 = query block i keeps key
+ * block j) and mass [nb * nb] (mu_ij).  Returns nb, or a negative value on
+ * bad arguments. */
+int64_t oracle_sol_mask_bf16(const uint16_t* q, const uint16_t* k, int B, int N, int H, int d,
+                             const int32_t* pos, const float* wqf, const float* wkf, double eps, double theta,
+                             const int* axes, double tau, int b, int h, unsigned char* keep, double* mass,
+                             int nt) {
+  double wq[1024], wk[1024];
+  if (check_axes(d, axes) || d > 1024 || b < 0 || b >= B || h < 0 || h >= H || N <= 0 || !(tau >= 0.0))
+    return -1;
+  for (int i = 0; i < d; ++i) { wq[i] = wqf[i]; wk[i] = wkf[i]; }
+  nt = nthreads_or_max(nt);
+  int64_t nd = (int64_t)N * d;
+  double* qh = (double*)malloc(sizeof(double) * nd);
+  double* kh = (double*)malloc(sizeof(double) * nd);
+  if (!qh || !kh) { free(qh); free(kh); return -3; }
+  src_t sq = {q, 1}, sk = {k, 1};
+  prologue_head(qh, &sq, b, h, N, H, d, pos, wq, eps, theta, axes, nt);
+  prologue_head(kh, &sk, b, h, N, H, d, pos, wk, eps, theta, axes, nt);
+  sol_mask(qh, kh, N, d, tau, keep, mass);
+  free(qh); free(kh);
+  return ((int64_t)N + 127) / 128;
+}
+
+/* Sol-Attention rows (readings R1-R4, R8): rows (b, h, n) as for
+ * oracle_attention_rows_bf16, each over the keys of the blocks its query
+ * block keeps. */
+int oracle_sol_attention_rows_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v, int B, int N, int H,
+                                   int d, const int32_t* pos, const float* wqf, const float* wkf, double eps,
+                                   double theta, const int* axes, double tau, const int64_t* rows, int64_t nrows,
+                                   double* out, int nt) {
+  double wq[1024], wk[1024];
+  if (check_axes(d, axes) || d > 1024 || B <= 0 || N <= 0 || H <= 0 || !(tau >= 0.0)) return -1;
+  for (int64_t r = 0; r < nrows; ++r) {
+    int64_t b = rows[3 * r], h = rows[3 * r + 1], n = rows[3 * r + 2];
+    if (b < 0 || b >= B || h < 0 || h >= H || n < 0 || n >= N) return -2;
+  }
+  for (int i = 0; i < d; ++i) { wq[i] = wqf[i]; wk[i] = wkf[i]; }
+  nt = nthreads_or_max(nt);
+  const int64_t nd = (int64_t)N * d, nb = ((int64_t)N + 127) / 128;
+  double* qh = (double*)malloc(sizeof(double) * nd);
+  double* kh = (double*)malloc(sizeof(double) * nd);
+  double* vh = (double*)malloc(sizeof(double) * nd);
+  unsigned char* keep = (unsigned char*)malloc((size_t)(nb * nb));
+  double* mass = (double*)malloc(sizeof(double) * nb * nb);
+  unsigned char* done = (unsigned char*)calloc((size_t)B * H, 1);
+  if (!qh || !kh || !vh || !keep || !mass || !done) {
+    free(qh); free(kh); free(vh); free(keep); free(mass); free(done);
+    return -3;
+  }
+  src_t sq = {q, 1}, sk = {k, 1}, sv = {v, 1};
+  for (int64_t r0 = 0; r0 < nrows; ++r0) {
+    int b = (int)rows[3 * r0], h = (int)rows[3 * r0 + 1];
+    if (done[(size_t)b * H + h]) continue;
+    done[(size_t)b * H + h] = 1;
+    prologue_head(qh, &sq, b, h, N, H, d, pos, wq, eps, theta, axes, nt);
+    prologue_head(kh, &sk, b, h, N, H, d, pos, wk, eps, theta, axes, nt);
+    plain_head(vh, &sv, b, h, N, H, d, nt);
+    sol_mask(qh, kh, N, d, tau, keep, mass);
+    int64_t t;
+#pragma omp parallel for num_threads(nt) schedule(dynamic, 4)
+    for (t = r0; t < nrows; ++t) {
+      if (rows[3 * t] != b || rows[3 * t + 1] != h) continue;
+      int64_t n = rows[3 * t + 2];
+      double* srow = (double*)malloc(sizeof(double) * N);
+      if (srow) sol_attention_row(out + t * d, qh + n * d, kh, vh, N, d, keep + (n / 128) * nb, srow);
+      else for (int i = 0; i < d; ++i) out[t * d + i] = NAN;
+      free(srow);
+    }
+  }
+  free(qh); free(kh); free(vh); free(keep); free(mass); free(done);
   return 0;
 }

@@ -25,7 +25,11 @@ What the checks compare the oracle with:
     Python sort of (error, index) pairs, torch SDPA); rho = 0 is plain FP8
     attention bit for bit, rho = 1 is SDPA over the dequantised Q' and the
     exact K', V; equal errors go to the lower token index; a planted
-    badly-quantised token is always selected.
+    badly-quantised token is always selected;
+  * the Sol-Attention block mask (reading R8): pooled means, block masses
+    and the keep rule restated with torch's softmax; tau = 0 is dense
+    attention; a tau that keeps one block per query block is torch SDPA over
+    that block's keys alone.
 """
 from __future__ import annotations
 
@@ -517,6 +521,79 @@ def check_vc_planted_token_is_always_repaired():
         assert np.max(np.abs(got[0, :, 1] - plain[0, :, 1])) > 1e-4   # the repair matters
 
 
+# ---------------------------------------------------- Sol-Attention (R8)
+
+def _lib_sol_mask(qn, kn, tau):
+    """Mask and masses of one head's [N, d] Q', K' from torch routines."""
+    N, d = qn.shape
+    nb = (N + 127) // 128
+    blocks = [slice(128 * j, min(N, 128 * j + 128)) for j in range(nb)]
+    qb = torch.stack([torch.from_numpy(qn[b]).mean(0) for b in blocks])
+    kb = torch.stack([torch.from_numpy(kn[b]).mean(0) for b in blocks])
+    cnt = torch.tensor([b.stop - b.start for b in blocks], dtype=torch.float64)
+    mass = torch.softmax(qb @ kb.T / math.sqrt(d) + torch.log(cnt)[None, :], dim=1).numpy()
+    keep = mass >= tau / nb
+    keep[np.arange(nb), np.argmax(mass, axis=1)] = True
+    return keep, mass
+
+
+def _sol_inputs(seed):
+    rng = _rng(seed)
+    pos = _geometry(40, 12, 20, 4, 9)        # N = 40 + 240 + 36 = 316: three blocks, the last ragged
+    N = pos.shape[0]
+    draw = lambda: bf16_bits_from_f32(rng.standard_normal((1, N, 2, D)).astype(np.float32))
+    q, k, v = draw(), draw(), draw()
+    # give query block 1 a preference: its queries lean toward key block 2
+    qf = bf16_bits_to_f32(q).copy()
+    kf = bf16_bits_to_f32(k).copy()
+    dirn = rng.standard_normal(D).astype(np.float32)
+    qf[0, 128:256, 0] += 3.0 * dirn
+    kf[0, 256:, 0] += 3.0 * dirn
+    q, k = bf16_bits_from_f32(qf), bf16_bits_from_f32(kf)
+    wq = (1.0 + 0.1 * rng.standard_normal(D)).astype(np.float32)
+    wk = (1.0 + 0.1 * rng.standard_normal(D)).astype(np.float32)
+    return q, k, v, pos, wq, wk
+
+
+def check_sol_mask_matches_library():
+    q, k, v, pos, wq, wk = _sol_inputs(31)
+    qn = lib_rope(lib_rms(bf16_bits_to_f32(q).astype(np.float64), wq), pos)
+    kn = lib_rope(lib_rms(bf16_bits_to_f32(k).astype(np.float64), wk), pos)
+    for tau in (0.5, 1.0, 1.6):
+        for h in range(2):
+            keep, mass = oracle.sol_mask(q, k, pos, wq, wk, tau, 0, h)
+            want_keep, want_mass = _lib_sol_mask(qn[0, :, h], kn[0, :, h], tau)
+            _close(mass, want_mass, 1e-12, "Sol block masses, head %d" % h)
+            assert np.array_equal(keep, want_keep), ("Sol mask", tau, h, keep, want_keep)
+    keep, mass = oracle.sol_mask(q, k, pos, wq, wk, 1.0, 0, 0)
+    assert keep[1, 2] and mass[1, 2] > 0.5          # the planted preference
+    _close(mass.sum(axis=1), np.ones(3), 1e-12, "Sol masses sum to one")
+
+
+def check_sol_tau_zero_is_dense():
+    q, k, v, pos, wq, wk = _sol_inputs(32)
+    dense = oracle.attention_rows(q, k, v, pos, wq, wk)
+    _close(oracle.sol_attention_rows(q, k, v, pos, wq, wk, 0.0), dense, 1e-14, "Sol tau=0 vs dense")
+
+
+def check_sol_one_block_is_subset_attention():
+    """A tau above nb leaves only each query block's block of largest mass:
+    the rows are SDPA over that block's keys alone."""
+    q, k, v, pos, wq, wk = _sol_inputs(33)
+    qn = lib_rope(lib_rms(bf16_bits_to_f32(q).astype(np.float64), wq), pos)
+    kn = lib_rope(lib_rms(bf16_bits_to_f32(k).astype(np.float64), wk), pos)
+    vf = bf16_bits_to_f32(v).astype(np.float64)
+    got = oracle.sol_attention_rows(q, k, v, pos, wq, wk, 10.0)
+    N = pos.shape[0]
+    for h in range(2):
+        keep, _ = _lib_sol_mask(qn[0, :, h], kn[0, :, h], 10.0)
+        for i in range(keep.shape[0]):
+            (j,) = np.nonzero(keep[i])[0]
+            qs, ks = slice(128 * i, min(N, 128 * i + 128)), slice(128 * j, min(N, 128 * j + 128))
+            want = lib_attention(qn[:, qs, h:h + 1], kn[:, ks, h:h + 1], vf[:, ks, h:h + 1])
+            _close(got[:, qs, h:h + 1], want, 1e-12, "Sol one block, head %d, query block %d" % (h, i))
+
+
 # --------------------------------------------------------- QKV projection
 
 def _bf16(a):
@@ -612,4 +689,7 @@ ALL_CHECKS = [
     check_vc_rho_zero_is_fp8_and_rho_one_exact_kv,
     check_vc_equal_errors_take_the_lower_index,
     check_vc_planted_token_is_always_repaired,
+    check_sol_mask_matches_library,
+    check_sol_tau_zero_is_dense,
+    check_sol_one_block_is_subset_attention,
 ]

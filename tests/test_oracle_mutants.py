@@ -43,6 +43,11 @@ MUTANTS = {
     "vc_ties_higher_index": ("return (x->m > y->m) - (x->m < y->m);", "return (x->m < y->m) - (x->m > y->m);"),
     "vc_count_floor": ("double r = ceil(rho * (double)N);", "double r = floor(rho * (double)N);"),
     "vc_repair_v_only": ("memcpy(kh + sel[r] * d, kx + sel[r] * d, sizeof(double) * d);", "(void)0;"),
+    "sol_pool_sum_not_mean": ("      qb[blk * d + i] /= cnt[blk];\n", "      (void)0;\n"),
+    "sol_no_block_size_weight": ("sc[j] = s * scale + log(cnt[j]);", "sc[j] = s * scale;"),
+    "sol_threshold_not_per_block": ("mass[i * nb + j] >= tau / (double)nb", "mass[i * nb + j] >= tau"),
+    "sol_no_best_block": ("mass[i * nb + j] >= tau / (double)nb || j == best", "mass[i * nb + j] >= tau / (double)nb"),
+    "sol_row_mask_of_key_block": ("keep_row[m / 128]) continue;\n    double s = 0.0;", "keep_row[0]) continue;\n    double s = 0.0;"),
     "qkv_v_normalised": ("for (int i = 0; i < d; ++i) v[i] = y[(int64_t)(2 * H + h) * d + i];", "rmsnorm_row(v, y + (int64_t)(2 * H + h) * d, d, wk, eps);"),
 }
 
