@@ -44,9 +44,10 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 import synthetic  # noqa: E402
+import diffusion_transformer_joint_txt_b300 as fa  # noqa: E402
 
 PRIMARY = "flux_1024_4608"
-SECONDARY = ["flux_2048_16896", "i2i_2048_33280", "fp8_cfg_2048_16896"]
+SECONDARY = ["flux_2048_16896", "i2i_2048_33280", "fp8_cfg_2048_16896", "vc_fp8_cfg_2048_16896"]
 METRIC = "joint-attn TFLOP/s & % of B300 BF16/FP8 TC peak at 4608/16896 tokens"
 FALLBACK_PEAKS = {"bf16_tflops": 1800.0, "hbm_gbs": 6400.0}
 L2_FLUSH_BYTES = 256 << 20
@@ -195,9 +196,16 @@ class Step:
         self.fp8 = w.precision == "fp8"
         self.inp, self.q, self.k, self.v, self.wq, self.wk = device_inputs(w, torch)
         n = w.tokens
-        self.attn = fa.FluxAttention(w.batch, w.heads, n, precision=w.precision)
+        self.attn = fa.FluxAttention(w.batch, w.heads, n, precision=w.precision,
+                                     vc_repair_budget=w.vc_repair_budget)
+        self.vc = w.vc_repair_budget > 0
         self.geo = (w.txt_len, w.img_h, w.img_w, w.ref_h, w.ref_w)
         B, H = w.batch, w.heads
+        if self.vc:
+            R = self.attn.vc_repair_count(n)
+            self.repair_idx = torch.empty((B, H, R), dtype=torch.int32, device="cuda")
+            self.k_rep = torch.empty((B, H, R, 128), dtype=torch.bfloat16, device="cuda")
+            self.v_rep = torch.empty_like(self.k_rep)
         if self.fp8:
             self.q8 = torch.empty((B, H, n, 128), dtype=torch.uint8, device="cuda")
             self.k8 = torch.empty_like(self.q8)
@@ -210,14 +218,21 @@ class Step:
         self.stream = torch.cuda.current_stream()
 
     def prologue(self):
-        if self.fp8:
+        if self.vc:
+            fa.flux_attn_prologue_fp8_vc(self.attn.handle, self.q, self.k, self.v, *self.geo, None, self.wq, self.wk,
+                                         self.q8, self.k8, self.v8t, self.scales, self.repair_idx, self.k_rep,
+                                         self.v_rep)
+        elif self.fp8:
             self.attn.prologue_fp8(self.q, self.k, self.v, *self.geo, self.wq, self.wk, q8=self.q8, k8=self.k8,
                                    v8t=self.v8t, scales=self.scales)
         else:
             self.attn.prologue(self.q, self.k, *self.geo, self.wq, self.wk, qn=self.qn, kn=self.kn)
 
     def attend(self):
-        if self.fp8:
+        if self.vc:
+            fa.flux_attn_attend_fp8_vc(self.attn.handle, self.q8, self.k8, self.v8t, self.scales, self.k_rep,
+                                       self.v_rep, self.w.tokens, self.out)
+        elif self.fp8:
             self.attn.attend_fp8(self.q8, self.k8, self.v8t, self.scales, out=self.out)
         else:
             self.attn.attend(self.qn, self.kn, self.v, out=self.out)

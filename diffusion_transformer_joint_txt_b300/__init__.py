@@ -45,6 +45,9 @@ class flux_attn_config(ctypes.Structure):
         ("rms_eps", ctypes.c_float),
         ("precision", ctypes.c_int),
         ("debug_flags", ctypes.c_int),
+        ("vc_repair_budget", ctypes.c_float),
+        ("sol_tau", ctypes.c_float),
+        ("sol_disabled_until_timestep", ctypes.c_float),
     ]
 
 
@@ -68,6 +71,12 @@ def _load() -> ctypes.CDLL:
         "flux_attn_attend": (I, [P, P, P, P, I, P, P]),
         "flux_attn_prologue_fp8": (I, [P, P, P, P, I, I, I, I, I, P, P, P, P, P, P, P, P]),
         "flux_attn_attend_fp8": (I, [P, P, P, P, P, I, P, P]),
+        "flux_attn_prologue_fp8_vc": (I, [P, P, P, P, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P]),
+        "flux_attn_attend_fp8_vc": (I, [P, P, P, P, P, P, P, I, P, P]),
+        "flux_attn_vc_repair_count": (I, [P, I]),
+        "flux_attn_forward_sol": (I, [P, P, P, P, I, I, I, I, I, P, P, P, ctypes.c_float, P, P]),
+        "flux_attn_sol_mask": (I, [P, P, P, I, P, P]),
+        "flux_attn_attend_sol": (I, [P, P, P, P, P, I, P, P]),
         "flux_attn_qkv": (I, [P, P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, P]),
         "flux_attn_forward_hidden": (I, [P, P, P, P, I, I, I, I, I, I, P, P, P, P, P]),
         "flux_attn_forward_noalloc": (I, [ctypes.POINTER(flux_attn_config), P, P, P, I, I, I, I, I, P, P, P, P,
@@ -131,9 +140,12 @@ def library_path() -> str:
 
 def flux_attn_create(batch: int, num_heads: int, max_tokens: int, head_dim: int = HEAD_DIM,
                      axes_dim: Sequence[int] = (16, 56, 56), rope_theta: float = 10000.0,
-                     rms_eps: float = 1e-6, precision: int = FLUX_ATTN_BF16, debug_flags: int = 0) -> int:
+                     rms_eps: float = 1e-6, precision: int = FLUX_ATTN_BF16, debug_flags: int = 0,
+                     vc_repair_budget: float = 0.0, sol_tau: float = 0.0,
+                     sol_disabled_until_timestep: float = 0.96) -> int:
     cfg = flux_attn_config(batch, num_heads, head_dim, max_tokens, (ctypes.c_int * 3)(*axes_dim),
-                           rope_theta, rms_eps, precision, debug_flags)
+                           rope_theta, rms_eps, precision, debug_flags, vc_repair_budget, sol_tau,
+                           sol_disabled_until_timestep)
     h = ctypes.c_void_p()
     _check(_L().flux_attn_create(ctypes.byref(cfg), ctypes.byref(h)))
     return h.value
@@ -171,6 +183,39 @@ def flux_attn_attend_fp8(h, q8, k8, v8t, scales, n_tokens, out, stream=None) -> 
                                      _stream(stream)))
 
 
+def flux_attn_prologue_fp8_vc(h, q, k, v, txt_len, img_h, img_w, ref_h, ref_w, pos_ids, q_norm_w, k_norm_w,
+                              q8, k8, v8t, scales, repair_idx, k_rep, v_rep, stream=None) -> None:
+    _check(_L().flux_attn_prologue_fp8_vc(h, _ptr(q), _ptr(k), _ptr(v), txt_len, img_h, img_w, ref_h, ref_w,
+                                          _ptr(pos_ids), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(q8), _ptr(k8),
+                                          _ptr(v8t), _ptr(scales), _ptr(repair_idx), _ptr(k_rep), _ptr(v_rep),
+                                          _stream(stream)))
+
+
+def flux_attn_attend_fp8_vc(h, q8, k8, v8t, scales, k_rep, v_rep, n_tokens, out, stream=None) -> None:
+    _check(_L().flux_attn_attend_fp8_vc(h, _ptr(q8), _ptr(k8), _ptr(v8t), _ptr(scales), _ptr(k_rep), _ptr(v_rep),
+                                        n_tokens, _ptr(out), _stream(stream)))
+
+
+def flux_attn_vc_repair_count(h, n_tokens: int) -> int:
+    return int(_L().flux_attn_vc_repair_count(h, n_tokens))
+
+
+def flux_attn_forward_sol(h, q, k, v, txt_len, img_h, img_w, ref_h, ref_w, pos_ids, q_norm_w, k_norm_w, timestep,
+                          out, stream=None) -> None:
+    _check(_L().flux_attn_forward_sol(h, _ptr(q), _ptr(k), _ptr(v), txt_len, img_h, img_w, ref_h, ref_w,
+                                      _ptr(pos_ids), _ptr(q_norm_w), _ptr(k_norm_w), float(timestep), _ptr(out),
+                                      _stream(stream)))
+
+
+def flux_attn_sol_mask(h, qn, kn, n_tokens, keep, stream=None) -> None:
+    _check(_L().flux_attn_sol_mask(h, _ptr(qn), _ptr(kn), n_tokens, _ptr(keep), _stream(stream)))
+
+
+def flux_attn_attend_sol(h, qn, kn, v, keep, n_tokens, out, stream=None) -> None:
+    _check(_L().flux_attn_attend_sol(h, _ptr(qn), _ptr(kn), _ptr(v), _ptr(keep), n_tokens, _ptr(out),
+                                     _stream(stream)))
+
+
 def flux_attn_qkv(h, x, w_qkv, b_qkv, d_model, txt_len, img_h, img_w, ref_h, ref_w, pos_ids, q_norm_w, k_norm_w,
                   qn, kn, v, stream=None) -> None:
     _check(_L().flux_attn_qkv(h, _ptr(x), _ptr(w_qkv), _ptr(b_qkv), d_model, txt_len, img_h, img_w, ref_h, ref_w,
@@ -187,9 +232,12 @@ def flux_attn_forward_hidden(h, x, w_qkv, b_qkv, d_model, txt_len, img_h, img_w,
 
 def make_config(batch: int, num_heads: int, max_tokens: int, head_dim: int = HEAD_DIM,
                 axes_dim: Sequence[int] = (16, 56, 56), rope_theta: float = 10000.0, rms_eps: float = 1e-6,
-                precision: int = FLUX_ATTN_BF16, debug_flags: int = 0) -> flux_attn_config:
+                precision: int = FLUX_ATTN_BF16, debug_flags: int = 0,
+                vc_repair_budget: float = 0.0, sol_tau: float = 0.0,
+                sol_disabled_until_timestep: float = 0.96) -> flux_attn_config:
     return flux_attn_config(batch, num_heads, head_dim, max_tokens, (ctypes.c_int * 3)(*axes_dim),
-                            rope_theta, rms_eps, precision, debug_flags)
+                            rope_theta, rms_eps, precision, debug_flags, vc_repair_budget, sol_tau,
+                            sol_disabled_until_timestep)
 
 
 def flux_attn_forward_noalloc(cfg: flux_attn_config, q, k, v, txt_len, img_h, img_w, ref_h, ref_w, pos_ids,
@@ -251,12 +299,16 @@ class FluxAttention:
 
     def __init__(self, batch: int, num_heads: int, max_tokens: int, precision: str = "bf16",
                  axes_dim: Sequence[int] = (16, 56, 56), rope_theta: float = 10000.0,
-                 rms_eps: float = 1e-6, debug_flags: int = 0):
+                 rms_eps: float = 1e-6, debug_flags: int = 0, vc_repair_budget: float = 0.0,
+                 sol_tau: float = 0.0, sol_disabled_until_timestep: float = 0.96):
+        """precision "bf16" or "fp8"; vc_repair_budget > 0 (FP8 only) turns on
+        the VC-Attention repair of the ceil(rho N) worst-quantised key tokens;
+        sol_tau > 0 (BF16 only) enables the block-sparse Sol-Attention calls."""
         self.batch, self.num_heads, self.max_tokens = batch, num_heads, max_tokens
         self.precision = precision
         prec = {"bf16": FLUX_ATTN_BF16, "fp8": FLUX_ATTN_FP8_E4M3}[precision]
         self.handle = flux_attn_create(batch, num_heads, max_tokens, HEAD_DIM, axes_dim, rope_theta, rms_eps,
-                                       prec, debug_flags)
+                                       prec, debug_flags, vc_repair_budget, sol_tau, sol_disabled_until_timestep)
 
     def close(self) -> None:
         if getattr(self, "handle", None):
@@ -415,6 +467,72 @@ class FluxAttention:
         out = torch.empty((B, n, H, HEAD_DIM), dtype=torch.bfloat16, device=q8.device) if out is None else out
         _require(out, torch.bfloat16, self._shape(n), "out")
         flux_attn_attend_fp8(self.handle, q8, k8, v8t, scales, n, out, stream)
+        return out
+
+    def vc_repair_count(self, n_tokens: int) -> int:
+        return flux_attn_vc_repair_count(self.handle, n_tokens)
+
+    def prologue_fp8_vc(self, q, k, v, txt_len: int, img_h: int, img_w: int, ref_h: int = 0, ref_w: int = 0,
+                        q_norm_w=None, k_norm_w=None, pos_ids=None, stream=None):
+        """VC-Attention handles: (q8, k8, v8t, scales, repair_idx, k_rep, v_rep) -- the
+        E4M3 codes with the repaired tokens moved out of the first N - R key
+        positions, the repaired tokens int32 [B, H, R] ascending, and their rows
+        k' / s_k, v / s_v bf16 [B, H, R, 128]."""
+        import torch
+        n = txt_len + img_h * img_w + ref_h * ref_w
+        for t, name in ((q, "q"), (k, "k"), (v, "v")):
+            _require(t, torch.bfloat16, self._shape(n), name)
+        _require(q_norm_w, torch.float32, (HEAD_DIM,), "q_norm_w")
+        _require(k_norm_w, torch.float32, (HEAD_DIM,), "k_norm_w")
+        if pos_ids is not None:
+            _require(pos_ids, torch.int32, (n, 3), "pos_ids")
+        B, H, R = self.batch, self.num_heads, self.vc_repair_count(n)
+        new = lambda shape, dt: torch.empty(shape, dtype=dt, device=q.device)
+        q8, k8 = new((B, H, n, HEAD_DIM), torch.uint8), new((B, H, n, HEAD_DIM), torch.uint8)
+        v8t, scales = new((B, H, HEAD_DIM, pad16(n)), torch.uint8), new((B, H, 3), torch.float32)
+        idx = new((B, H, max(R, 1)), torch.int32)
+        k_rep, v_rep = new((B, H, max(R, 1), HEAD_DIM), torch.bfloat16), new((B, H, max(R, 1), HEAD_DIM),
+                                                                             torch.bfloat16)
+        flux_attn_prologue_fp8_vc(self.handle, q, k, v, txt_len, img_h, img_w, ref_h, ref_w, pos_ids, q_norm_w,
+                                  k_norm_w, q8, k8, v8t, scales, idx, k_rep, v_rep, stream)
+        return q8, k8, v8t, scales, idx, k_rep, v_rep
+
+    def attend_fp8_vc(self, q8, k8, v8t, scales, k_rep, v_rep, out=None, stream=None):
+        import torch
+        B, H, n = self.batch, self.num_heads, q8.shape[2]
+        out = torch.empty((B, n, H, HEAD_DIM), dtype=torch.bfloat16, device=q8.device) if out is None else out
+        _require(out, torch.bfloat16, self._shape(n), "out")
+        flux_attn_attend_fp8_vc(self.handle, q8, k8, v8t, scales, k_rep, v_rep, n, out, stream)
+        return out
+
+    def forward_sol(self, q, k, v, txt_len: int, img_h: int, img_w: int, ref_h: int = 0, ref_w: int = 0,
+                    q_norm_w=None, k_norm_w=None, pos_ids=None, timestep: float = 0.0, out=None, stream=None):
+        """Sol-Attention forward (dense while timestep > sol_disabled_until_timestep)."""
+        import torch
+        n = txt_len + img_h * img_w + ref_h * ref_w
+        for t, name in ((q, "q"), (k, "k"), (v, "v")):
+            _require(t, torch.bfloat16, self._shape(n), name)
+        out = torch.empty_like(q) if out is None else out
+        _require(out, torch.bfloat16, self._shape(n), "out")
+        flux_attn_forward_sol(self.handle, q, k, v, txt_len, img_h, img_w, ref_h, ref_w, pos_ids, q_norm_w, k_norm_w,
+                              timestep, out, stream)
+        return out
+
+    def sol_mask(self, qn, kn, stream=None):
+        """Block mask uint8 [B, H, nb, nb] of Q', K' bf16 [B, H, N, 128]."""
+        import torch
+        n = qn.shape[2]
+        nb = (n + 127) // 128
+        keep = torch.empty((self.batch, self.num_heads, nb, nb), dtype=torch.uint8, device=qn.device)
+        flux_attn_sol_mask(self.handle, qn, kn, n, keep, stream)
+        return keep
+
+    def attend_sol(self, qn, kn, v, keep, out=None, stream=None):
+        import torch
+        n = qn.shape[2]
+        out = torch.empty_like(v) if out is None else out
+        _require(out, torch.bfloat16, self._shape(n), "out")
+        flux_attn_attend_sol(self.handle, qn, kn, v, keep, n, out, stream)
         return out
 
     def sync_status(self, stream=None) -> int:

@@ -54,6 +54,24 @@
 // decoding every code back to fp32 for the sum cost it a sixth of its
 // throughput.
 //
+// VC-Attention repair (REP, FP8 only; vc_repair.cuh selects the tokens):
+// the CTA first runs ceil(R / 128) repair blocks in BF16 -- K_rep = k' / s_k
+// and V_rep = v / s_v of the R repaired key tokens, so that scores and P.V
+// come out in the units of the E4M3 blocks -- and then the FP8 blocks over
+// the N - R other keys (positions 0 .. N-R-1 of the codes).  The repair QK
+// needs Q in bf16: the softmax warps convert their rows of the E4M3 Q tile
+// (exact: every E4M3 value is a bf16 value) into the K ring's memory, and the
+// repair K and V tiles go to the V ring's memory; both rings are idle until
+// the repair blocks are done, which the MMA thread signals (qbf_free,
+// vrep_free) before the producers start on the FP8 tiles.  A repair block's P
+// is bf16 (as in the BF16 kernel); its row sum adds the fp32 p.
+//
+// Sol-Attention (SOL, BF16; sol_sparse.cuh builds the lists): the CTA walks
+// only the key blocks in its list -- the union of the blocks its two query
+// tiles keep -- and a tile that does not keep a block of the list writes
+// P = 0 for it (its running max, sum and O stay as they are), so the MMA
+// schedule stays the same for both tiles.
+//
 // Every wait is bounded (ptx.cuh); a wait that runs out sets the CTA abort
 // flag and the error word, all roles stop issuing, drain what they issued,
 // free TMEM and return.
@@ -104,6 +122,10 @@ struct __align__(1024) Smem {
   uint64_t k_full[KST], k_empty[KST];
   uint64_t v_full[VST], v_empty[VST];
   uint64_t s_full[TILES], p_full[TILES], o_full[TILES];
+  uint64_t qbf_full[TILES];            // REP: tile t's rows converted to bf16 (128 arrivals)
+  uint64_t krep_full, krep_empty;      // REP: the repair K tile slot
+  uint64_t vrep_full, vrep_empty;      // REP: the repair V tile slot
+  uint64_t qbf_free, vrep_free;        // REP: last repair QK / PV of both tiles done
   uint64_t mma_drain;
   uint64_t never;  // nothing arrives here (forced-timeout debug path)
   uint32_t tmem_base;
@@ -118,7 +140,12 @@ struct Params {
   __nv_bfloat16* out;    // [B, N, H, 128]
   uint32_t* err;
   const float* scales;   // FP8: [B*H, 3] (s_q, s_k, s_v); BF16: unused
-  int N, H, nkv;
+  int N, H, nkv;         // nkv: key blocks in all (repair blocks first)
+  int nrep, rep_keys;    // REP: repair blocks and repaired keys R (0 otherwise)
+  int main_keys;         // keys of the E4M3 / BF16 blocks: N - R
+  const uint16_t* sol_list;  // SOL: [B*H][ncta][sol_nb] key block | tile keep bits << 14
+  const int* sol_count;      // SOL: [B*H][ncta] entries of each list
+  int sol_nb;
   float scale_log2;      // log2(e) / sqrt(128)
   int debug;
 };
@@ -154,30 +181,59 @@ __device__ __forceinline__ void drain_ring(uint64_t (&full)[ST], int issued, uin
   }
 }
 
-// K ring producer: K_j into stage j % KST once both tiles' QK of its
-// previous occupant have completed.
+// REP shared memory: the two bf16 Q tiles in the K ring (32 KB each), the
+// repair K tile in the first and the repair V tile in the second 32 KB of the
+// V ring.
 template <bool FP8>
-__device__ __forceinline__ void load_k(Smem<FP8>& sm, const CUtensorMap* tk, int bh, int nkv, volatile int* ab,
-                                       uint32_t* err) {
+__device__ __forceinline__ uint8_t* qbf_tile(Smem<FP8>& sm, int t) { return &sm.k[0][0] + t * 2 * HALF; }
+template <bool FP8>
+__device__ __forceinline__ uint8_t* krep_tile(Smem<FP8>& sm) { return &sm.v[0][0]; }
+template <bool FP8>
+__device__ __forceinline__ uint8_t* vrep_tile(Smem<FP8>& sm) { return &sm.v[0][0] + 2 * HALF; }
+
+// K ring producer: K_j into stage j % KST once both tiles' QK of its
+// previous occupant have completed.  REP: first the repair K tiles, each once
+// both tiles' QK of the one before it has completed; the ring's memory holds
+// the bf16 Q tiles until qbf_free.
+template <bool FP8, bool REP, bool SOL>
+__device__ __forceinline__ void load_k(Smem<FP8>& sm, const CUtensorMap* tk, const CUtensorMap* tkr, int bh,
+                                       int nkv, int nrep, const uint16_t* lst, volatile int* ab, uint32_t* err) {
   constexpr uint32_t TILE = Traits<FP8>::TILE;
   constexpr int KST = Traits<FP8>::KST;
   int issued = 0;
+  if (REP) {
+    int rep_issued = 0;
+    bool ok = true;
+    for (int i = 0; i < nrep && ok; ++i) {
+      if (i > 0 && !mbar_wait(&sm.krep_empty, (i - 1) & 1, ab, err)) { ok = false; break; }
+      mbar_arrive_expect_tx(&sm.krep_full, 2 * HALF);
+      load_rows<false>(smem_u32(krep_tile(sm)), tkr, &sm.krep_full, i * BN, bh);
+      ++rep_issued;
+    }
+    if (rep_issued > 0) mbar_drain(&sm.krep_full, (rep_issued - 1) & 1, err);
+    if (!ok || !mbar_wait(&sm.qbf_free, 0, ab, err)) return;
+    nkv -= nrep;
+  }
   for (int j = 0; j < nkv; ++j) {
+    const int kb = SOL ? (__ldg(lst + j) & 0x3FFF) : j;  // read before the wait
     const int ks = j % KST;
     const uint32_t ku = j / KST;
     if (ku > 0 && !mbar_wait(&sm.k_empty[ks], (ku - 1) & 1, ab, err)) break;
     mbar_arrive_expect_tx(&sm.k_full[ks], TILE);
-    load_rows<FP8>(smem_u32(sm.k[ks]), tk, &sm.k_full[ks], j * BN, bh);
+    load_rows<FP8>(smem_u32(sm.k[ks]), tk, &sm.k_full[ks], kb * BN, bh);
     ++issued;
   }
   drain_ring(sm.k_full, issued, err);
 }
 
 // Q and V ring producer: both Q tiles once, then V_j into stage j % VST once
-// both tiles' PV of its previous occupant have completed.
-template <bool FP8>
-__device__ __forceinline__ void load_qv(Smem<FP8>& sm, const CUtensorMap* tq, const CUtensorMap* tv, int q0, int bh,
-                                        int b, int h, int nkv, volatile int* ab, uint32_t* err) {
+// both tiles' PV of its previous occupant have completed.  REP: the repair V
+// tiles first (each once both tiles' PV of the one before it has completed),
+// and the ring only after vrep_free.
+template <bool FP8, bool REP, bool SOL>
+__device__ __forceinline__ void load_qv(Smem<FP8>& sm, const CUtensorMap* tq, const CUtensorMap* tv,
+                                        const CUtensorMap* tvr, int q0, int bh, int b, int h, int nkv, int nrep,
+                                        const uint16_t* lst, volatile int* ab, uint32_t* err) {
   constexpr uint32_t TILE = Traits<FP8>::TILE;
   constexpr int VST = Traits<FP8>::VST;
 #pragma unroll
@@ -186,18 +242,32 @@ __device__ __forceinline__ void load_qv(Smem<FP8>& sm, const CUtensorMap* tq, co
     load_rows<FP8>(smem_u32(sm.q[t]), tq, &sm.q_full[t], q0 + t * BM, bh);
   }
   int issued = 0;
+  bool rep_ok = true;
+  if (REP) {
+    int rep_issued = 0;
+    for (int i = 0; i < nrep && rep_ok; ++i) {
+      if (i > 0 && !mbar_wait(&sm.vrep_empty, (i - 1) & 1, ab, err)) { rep_ok = false; break; }
+      mbar_arrive_expect_tx(&sm.vrep_full, 2 * HALF);
+      load_rows<false>(smem_u32(vrep_tile(sm)), tvr, &sm.vrep_full, i * BN, bh);
+      ++rep_issued;
+    }
+    if (rep_issued > 0) mbar_drain(&sm.vrep_full, (rep_issued - 1) & 1, err);
+    rep_ok = rep_ok && mbar_wait(&sm.vrep_free, 0, ab, err);
+    nkv = rep_ok ? nkv - nrep : 0;
+  }
   for (int j = 0; j < nkv; ++j) {
+    const int kb = SOL ? (__ldg(lst + j) & 0x3FFF) : j;  // read before the wait
     const int vs = j % VST;
     const uint32_t vu = j / VST;
     if (vu > 0 && !mbar_wait(&sm.v_empty[vs], (vu - 1) & 1, ab, err)) break;
     mbar_arrive_expect_tx(&sm.v_full[vs], TILE);
     if (FP8) {
-      // V^T [B*H, 128, Npad]: keys j*128.. are the inner (x) coordinate.
-      tma_load_3d(smem_u32(sm.v[vs]), tv, &sm.v_full[vs], j * BN, 0, bh);
+      // V^T [B*H, 128, Npad]: keys kb*128.. are the inner (x) coordinate.
+      tma_load_3d(smem_u32(sm.v[vs]), tv, &sm.v_full[vs], kb * BN, 0, bh);
     } else {
       // V [B, N, H, 128] in place: box (64 dims, 1 head, 128 keys, 1 batch).
-      tma_load_4d(smem_u32(sm.v[vs]), tv, &sm.v_full[vs], 0, h, j * BN, b);
-      tma_load_4d(smem_u32(sm.v[vs]) + HALF, tv, &sm.v_full[vs], 64, h, j * BN, b);
+      tma_load_4d(smem_u32(sm.v[vs]), tv, &sm.v_full[vs], 0, h, kb * BN, b);
+      tma_load_4d(smem_u32(sm.v[vs]) + HALF, tv, &sm.v_full[vs], 64, h, kb * BN, b);
     }
     ++issued;
   }
@@ -256,13 +326,50 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint6
   }
 }
 
+// REP: the repair blocks, issued before the main loop -- per block QK_0 QK_1
+// (bf16, Q from the converted tiles, K from the repair slot), then PV_0 PV_1
+// once each tile's P is in.  Commits qbf_free after the last repair QK and
+// vrep_free after the last repair PV.  Returns false when a wait gave up.
+template <bool FP8>
+__device__ __forceinline__ bool mma_repair(Smem<FP8>& sm, uint32_t tmem, int nrep, volatile int* ab, uint32_t* err) {
+  uint64_t qbd[TILES];
+#pragma unroll
+  for (int t = 0; t < TILES; ++t) qbd[t] = sdesc_sw128(smem_u32(qbf_tile(sm, t)), 16, 1024);
+  const uint64_t krd = sdesc_sw128(smem_u32(krep_tile(sm)), 16, 1024);
+  const uint64_t vrd = sdesc_sw128(smem_u32(vrep_tile(sm)), HALF, 1024);
+  for (int i = 0; i < nrep; ++i) {
+    if (!mbar_wait(&sm.krep_full, i & 1, ab, err)) return false;
+#pragma unroll
+    for (int t = 0; t < TILES; ++t) {
+      if (i == 0 && !mbar_wait(&sm.qbf_full[t], 0, ab, err)) return false;
+      tc_fence_after_sync();
+      issue_qk<false>(tmem + col_s(t), qbd[t], krd);
+      mma_commit(&sm.s_full[t]);
+    }
+    mma_commit(&sm.krep_empty);
+    if (i == nrep - 1) mma_commit(&sm.qbf_free);
+    if (!mbar_wait(&sm.vrep_full, i & 1, ab, err)) return false;
+#pragma unroll
+    for (int t = 0; t < TILES; ++t) {
+      if (!mbar_wait(&sm.p_full[t], i & 1, ab, err)) return false;
+      tc_fence_after_sync();
+      issue_pv<false>(tmem + col_o(t), tmem + col_s(t), vrd, i > 0);
+    }
+    mma_commit(&sm.vrep_empty);
+    if (i == nrep - 1) mma_commit(&sm.vrep_free);
+  }
+  return true;
+}
+
 // The MMA issuer: QK_0(0) QK_1(0), then PV_0(j) QK_0(j+1) PV_1(j) QK_1(j+1)
 // for every j.  The whole warp runs this loop and one elected lane issues
 // (ptx.cuh).  One thread issues for both tiles: the fixed order is what
 // keeps the two tiles in turns (two independent issuers drift into step, and
 // then both softmaxes run at once and compete for the same schedulers).
-template <bool FP8>
-__device__ __forceinline__ void mma_issuer(Smem<FP8>& sm, uint32_t tmem, int nkv, volatile int* ab,
+// REP: the repair blocks first (mma_repair); the main loop then continues
+// the s_full / p_full phases after them and accumulates onto their O.
+template <bool FP8, bool REP>
+__device__ __forceinline__ void mma_issuer(Smem<FP8>& sm, uint32_t tmem, int nkv, int nrep, volatile int* ab,
                                            uint32_t* err) {
   constexpr uint32_t TILE = Traits<FP8>::TILE;
   constexpr int KST = Traits<FP8>::KST, VST = Traits<FP8>::VST;
@@ -273,7 +380,15 @@ __device__ __forceinline__ void mma_issuer(Smem<FP8>& sm, uint32_t tmem, int nkv
   for (int t = 0; t < TILES; ++t) qd[t] = sdesc_sw128(smem_u32(sm.q[t]), 16, 1024);
   const uint64_t kd0 = sdesc_sw128(smem_u32(sm.k[0]), 16, 1024);
   const uint64_t vd0 = sdesc_sw128(smem_u32(sm.v[0]), FP8 ? 16 : HALF, 1024);
+  const int ph = REP ? nrep : 0;  // s_full / p_full phases the repair blocks used
+  if (REP) nkv -= nrep;           // main-loop blocks
   do {
+    if (REP && !mma_repair(sm, tmem, nrep, ab, err)) break;
+    if (nkv <= 0) {
+#pragma unroll
+      for (int t = 0; t < TILES; ++t) mma_commit(&sm.o_full[t]);
+      break;
+    }
     if (!mbar_wait(&sm.k_full[0], 0, ab, err)) break;
     bool ok = true;
 #pragma unroll
@@ -295,10 +410,10 @@ __device__ __forceinline__ void mma_issuer(Smem<FP8>& sm, uint32_t tmem, int nkv
       const uint64_t kd = desc_at(kd0, ks * TILE);
 #pragma unroll
       for (int t = 0; t < TILES; ++t) {
-        ok = mbar_wait(&sm.p_full[t], j & 1, ab, err);
+        ok = mbar_wait(&sm.p_full[t], (j + ph) & 1, ab, err);
         if (!ok) break;
         tc_fence_after_sync();
-        issue_pv<FP8>(tmem + col_o(t), tmem + col_s(t), vd, j > 0);
+        issue_pv<FP8>(tmem + col_o(t), tmem + col_s(t), vd, j + ph > 0);
         if (t == TILES - 1) mma_commit(&sm.v_empty[vs]);
         if (jn < nkv) {
           if (t == 0) {
@@ -331,16 +446,164 @@ __device__ __forceinline__ __half2 e4m3x2_value(uint32_t c) {
   return __half2(__nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(c), __NV_E4M3));
 }
 
-// Softmax and epilogue of query tile `t` (128 threads, thread r = row r).
+// REP: thread r converts row r of the E4M3 Q tile t into the bf16 tile the
+// repair QK reads (both in the 128-byte-swizzled layout: a row's 16-byte
+// chunk c sits at chunk position c ^ (r % 8); the bf16 tile is two halves of
+// 64 head dims).  E4M3 values are exact in f16 and in bf16.
 template <bool FP8>
+__device__ __forceinline__ void convert_q_row(Smem<FP8>& sm, int t, int r) {
+  const uint8_t* src = sm.q[t] + r * 128;
+  uint8_t* dst = qbf_tile(sm, t);
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {  // 16 codes: head dims 16c .. 16c + 15
+    const uint4 u = *reinterpret_cast<const uint4*>(src + ((c ^ (r & 7)) << 4));
+    const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 lo = __half22float2(e4m3x2_value(wd[i] & 0xFFFFu));
+      const float2 hi = __half22float2(e4m3x2_value(wd[i] >> 16));
+      o[2 * i] = pack_bf16x2(lo.x, lo.y);
+      o[2 * i + 1] = pack_bf16x2(hi.x, hi.y);
+    }
+    // dims 16c .. 16c+7 and 16c+8 .. 16c+15: half (16c) / 64, chunks 2 (c % 4) and 2 (c % 4) + 1
+    uint8_t* row = dst + (c >> 2) * HALF + r * 128;
+    const int k0 = 2 * (c & 3);
+    *reinterpret_cast<uint4*>(row + ((k0 ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4*>(row + (((k0 + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
+// One key block of the online softmax of query tile t (128 threads, thread
+// r = row r): wait for S, mask the keys >= valid, update the running max m
+// (log2 units) and sum l, write P over S (P8: E4M3 of 256 p, four per TMEM
+// column; else bf16, two per column), rescale O when the max moved (has_o:
+// O already holds earlier blocks), and hand P to the MMA thread.  Returns
+// false when the CTA gave up.
+template <bool FP8, bool P8>
+__device__ __forceinline__ bool softmax_block(Smem<FP8>& sm, int t, uint32_t s_addr, uint32_t o_addr,
+                                              uint32_t phase, int valid, bool has_o, float sl2, float& m, float& l,
+                                              volatile int* ab, uint32_t* err, bool keep = true) {
+  // FP8 stores P as E4M3 of 256 p: the 2^8 factor is folded into the exponent
+  // and cancels against l, which sums the same scaled values.
+  constexpr float kPBias = FP8 ? 8.f : 0.f;
+  constexpr float kRescale = Traits<FP8>::RESCALE;
+  const bool ok = mbar_wait(&sm.s_full[t], phase, ab, err);
+  if (__any_sync(0xFFFFFFFFu, !ok)) return false;
+  tc_fence_after_sync();
+  if (!keep) {  // SOL: the tile does not attend to this block: P = 0 (warp-uniform)
+    uint32_t z[BN / 2];
+#pragma unroll
+    for (int i = 0; i < BN / 2; ++i) z[i] = 0u;
+    tmem_st64(s_addr, z);
+    tmem_st_wait();
+    tc_fence_before_sync();
+    mbar_arrive(&sm.p_full[t]);
+    return true;
+  }
+  uint32_t s[BN];
+  tmem_ld128(s_addr, s);
+  tmem_ld_wait(s);
+  if (valid < BN) {
+#pragma unroll
+    for (int i = 0; i < BN; ++i)
+      if (i >= valid) s[i] = __float_as_uint(-INFINITY);
+  }
+  // Row max: four independent chains of three-input max (depth 16, not 127).
+  float acc[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) acc[c] = fmaxf(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1]));
+#pragma unroll
+  for (int i = 8; i < BN; i += 8) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      acc[c] = fmax3(acc[c], __uint_as_float(s[i + 2 * c]), __uint_as_float(s[i + 2 * c + 1]));
+  }
+  const float mx = fmax3(acc[0], acc[1], fmaxf(acc[2], acc[3]));
+  const float m_tile = fmaxf(m, mx * sl2);
+  // One decision per warp (TMEM moves are warp-wide); each row keeps its own alpha.
+  const bool rescale = __any_sync(0xFFFFFFFFu, m_tile > m + kRescale);
+  const float m_new = rescale ? m_tile : m;
+  const float alpha = rescale ? ex2_approx(m - m_new) : 1.f;  // 0 on the first tile
+  const float nm = kPBias - m_new;
+  // p = 2^(s sl2 - m): the argument of two scores per packed FMA; the row
+  // sum in four packed accumulators.
+  float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  if (P8) {
+    // P codes four per word (key 4i in the lowest byte); the row sum adds
+    // the values of the codes, in eight packed f16 accumulators (each sums
+    // at most 8 values <= 256: partial sums <= 2048, rounding <= 2^-11
+    // relative per add) that are widened to fp32 once per block.
+    uint32_t pk[32];
+    __half2 hs[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) hs[i] = __float2half2_rn(0.f);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      float x0, x1, x2, x3;
+      fma2(x0, x1, __uint_as_float(s[4 * i]), __uint_as_float(s[4 * i + 1]), sl2, sl2, nm, nm);
+      fma2(x2, x3, __uint_as_float(s[4 * i + 2]), __uint_as_float(s[4 * i + 3]), sl2, sl2, nm, nm);
+      const uint32_t lo = e4m3x2(ex2_approx(x0), ex2_approx(x1));
+      const uint32_t hi = e4m3x2(ex2_approx(x2), ex2_approx(x3));
+      pk[i] = lo | (hi << 16);
+      hs[i & 7] = __hadd2(hs[i & 7], __hadd2(e4m3x2_value(lo), e4m3x2_value(hi)));
+    }
+    tmem_st32(s_addr, pk);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float2 f = __half22float2(hs[i]);
+      sum[i] = f.x + f.y;
+    }
+  } else {
+    uint32_t pk[BN / 2];
+#pragma unroll
+    for (int i = 0; i < BN / 2; ++i) {
+      float x0, x1;
+      fma2(x0, x1, __uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]), sl2, sl2, nm, nm);
+      const float p0 = ex2_approx(x0);
+      const float p1 = ex2_approx(x1);
+      add2(sum[2 * (i & 3)], sum[2 * (i & 3) + 1], p0, p1);
+      pk[i] = pack_bf16x2(p0, p1);
+    }
+    tmem_st64(s_addr, pk);
+  }
+  add2(sum[0], sum[1], sum[2], sum[3]);
+  add2(sum[4], sum[5], sum[6], sum[7]);
+  add2(sum[0], sum[1], sum[4], sum[5]);
+  l = l * alpha + (sum[0] + sum[1]);
+  // O_t holds the earlier blocks' P V already (see the issue order), and
+  // nothing else writes it until this thread arrives on p_full below.
+  if (rescale && has_o) {
+#pragma unroll
+    for (int c = 0; c < HD / 32; ++c) {
+      uint32_t o[32];
+      tmem_ld32(o_addr + c * 32, o);
+      tmem_ld_wait(o);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+      tmem_st32(o_addr + c * 32, o);
+    }
+  }
+  tmem_st_wait();
+  m = m_new;
+  tc_fence_before_sync();
+  mbar_arrive(&sm.p_full[t]);
+  return true;
+}
+
+// Softmax and epilogue of query tile `t` (128 threads, thread r = row r).
+// REP: the Q conversion and the repair blocks (bf16 P) come first, then the
+// E4M3 blocks, whose loop is the plain FP8 one with its phases shifted.
+template <bool FP8, bool REP, bool SOL>
 __device__ __forceinline__ void softmax_epilogue(Smem<FP8>& sm, uint32_t tmem, const Params& prm, int b, int h,
-                                                 int row0, int t, volatile int* ab, const CUtensorMap* tm_o) {
+                                                 int row0, int t, int nkv, const uint16_t* lst, volatile int* ab,
+                                                 const CUtensorMap* tm_o) {
   const int r = threadIdx.x & (BM - 1);
   const uint32_t lane_base = static_cast<uint32_t>(r & ~31) << 16;  // TMEM lanes of this warp
   const uint32_t s_addr = tmem + lane_base + col_s(t);
   const uint32_t o_addr = tmem + lane_base + col_o(t);
-  const int N = prm.N;
-  const int nkv = prm.nkv;
+  const int nrep = REP ? prm.nrep : 0;
+  const int nmain = nkv - nrep;
   float sl2 = prm.scale_log2;
   float out_scale = 1.f;
   if (FP8) {
@@ -348,107 +611,31 @@ __device__ __forceinline__ void softmax_epilogue(Smem<FP8>& sm, uint32_t tmem, c
     sl2 *= __ldg(sc) * __ldg(sc + 1);
     out_scale = __ldg(sc + 2);
   }
-  // FP8 stores P as E4M3 of 256 p: the 2^8 factor is folded into the exponent
-  // and cancels against l, which sums the same scaled values.
-  constexpr float kPBias = FP8 ? 8.f : 0.f;
-  constexpr float kRescale = Traits<FP8>::RESCALE;
   float m = -INFINITY;  // running max, in log2 units
   float l = 0.f;        // running row sum
   bool ok = true;
-  for (int j = 0; j < nkv; ++j) {
-    ok = mbar_wait(&sm.s_full[t], j & 1, ab, prm.err);
-    if (__any_sync(0xFFFFFFFFu, !ok)) { ok = false; break; }
-    tc_fence_after_sync();
-    uint32_t s[BN];
-    tmem_ld128(s_addr, s);
-    tmem_ld_wait(s);
-    const int valid = N - j * BN;  // keys of this tile that exist (> 0)
-    if (valid < BN) {
-#pragma unroll
-      for (int i = 0; i < BN; ++i)
-        if (i >= valid) s[i] = __float_as_uint(-INFINITY);
+  if (REP && nrep > 0) {
+    ok = mbar_wait(&sm.q_full[t], 0, ab, prm.err);
+    if (__any_sync(0xFFFFFFFFu, !ok)) return;
+    convert_q_row(sm, t, r);
+    fence_proxy_async_smem();  // generic-proxy writes, read by the MMA (async proxy)
+    mbar_arrive(&sm.qbf_full[t]);
+    for (int i = 0; i < nrep && ok; ++i)
+      ok = softmax_block<FP8, false>(sm, t, s_addr, o_addr, i & 1, prm.rep_keys - i * BN, i > 0, sl2, m, l, ab,
+                                     prm.err);
+  }
+  if (SOL) {
+    // list entry j: key block (14 bits) and the keep bits of the two tiles; a
+    // block the tile skips still gets its (zero) P, so O is written from j = 0
+    for (int j = 0; j < nmain && ok; ++j) {
+      const uint32_t e = __ldg(lst + j);
+      ok = softmax_block<FP8, false>(sm, t, s_addr, o_addr, j & 1, prm.N - static_cast<int>(e & 0x3FFFu) * BN,
+                                     j > 0, sl2, m, l, ab, prm.err, (e >> (14 + t)) & 1u);
     }
-    // Row max: four independent chains of three-input max (depth 16, not 127).
-    float acc[4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) acc[c] = fmaxf(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1]));
-#pragma unroll
-    for (int i = 8; i < BN; i += 8) {
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        acc[c] = fmax3(acc[c], __uint_as_float(s[i + 2 * c]), __uint_as_float(s[i + 2 * c + 1]));
-    }
-    const float mx = fmax3(acc[0], acc[1], fmaxf(acc[2], acc[3]));
-    const float m_tile = fmaxf(m, mx * sl2);
-    // One decision per warp (TMEM moves are warp-wide); each row keeps its own alpha.
-    const bool rescale = __any_sync(0xFFFFFFFFu, m_tile > m + kRescale);
-    const float m_new = rescale ? m_tile : m;
-    const float alpha = rescale ? ex2_approx(m - m_new) : 1.f;  // 0 on the first tile
-    const float nm = kPBias - m_new;
-    // p = 2^(s sl2 - m): the argument of two scores per packed FMA; the row
-    // sum in four packed accumulators.
-    float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    float rs;
-    if (FP8) {
-      // P codes four per word (key 4i in the lowest byte); the row sum adds
-      // the values of the codes, in eight packed f16 accumulators (each sums
-      // at most 8 values <= 256: partial sums <= 2048, rounding <= 2^-11
-      // relative per add) that are widened to fp32 once per block.
-      uint32_t pk[32];
-      __half2 hs[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) hs[i] = __float2half2_rn(0.f);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        float x0, x1, x2, x3;
-        fma2(x0, x1, __uint_as_float(s[4 * i]), __uint_as_float(s[4 * i + 1]), sl2, sl2, nm, nm);
-        fma2(x2, x3, __uint_as_float(s[4 * i + 2]), __uint_as_float(s[4 * i + 3]), sl2, sl2, nm, nm);
-        const uint32_t lo = e4m3x2(ex2_approx(x0), ex2_approx(x1));
-        const uint32_t hi = e4m3x2(ex2_approx(x2), ex2_approx(x3));
-        pk[i] = lo | (hi << 16);
-        hs[i & 7] = __hadd2(hs[i & 7], __hadd2(e4m3x2_value(lo), e4m3x2_value(hi)));
-      }
-      tmem_st32(s_addr, pk);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float2 f = __half22float2(hs[i]);
-        sum[i] = f.x + f.y;
-      }
-    } else {
-      uint32_t pk[BN / 2];
-#pragma unroll
-      for (int i = 0; i < BN / 2; ++i) {
-        float x0, x1;
-        fma2(x0, x1, __uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]), sl2, sl2, nm, nm);
-        const float p0 = ex2_approx(x0);
-        const float p1 = ex2_approx(x1);
-        add2(sum[2 * (i & 3)], sum[2 * (i & 3) + 1], p0, p1);
-        pk[i] = pack_bf16x2(p0, p1);
-      }
-      tmem_st64(s_addr, pk);
-    }
-    add2(sum[0], sum[1], sum[2], sum[3]);
-    add2(sum[4], sum[5], sum[6], sum[7]);
-    add2(sum[0], sum[1], sum[4], sum[5]);
-    rs = sum[0] + sum[1];
-    l = l * alpha + rs;
-    // O_t holds P_t(j-1) V(j-1) already (see the issue order), and nothing
-    // else writes it until this thread arrives on p_full below.
-    if (rescale && j > 0) {
-#pragma unroll
-      for (int c = 0; c < HD / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32(o_addr + c * 32, o);
-        tmem_ld_wait(o);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-        tmem_st32(o_addr + c * 32, o);
-      }
-    }
-    tmem_st_wait();
-    m = m_new;
-    tc_fence_before_sync();
-    mbar_arrive(&sm.p_full[t]);
+  } else {
+    for (int j = 0; j < nmain && ok; ++j)
+      ok = softmax_block<FP8, FP8>(sm, t, s_addr, o_addr, (j + nrep) & 1, prm.main_keys - j * BN, j + nrep > 0,
+                                   sl2, m, l, ab, prm.err);
   }
   if (ok) {
     ok = mbar_wait(&sm.o_full[t], 0, ab, prm.err);
@@ -495,10 +682,16 @@ __device__ __forceinline__ void softmax_epilogue(Smem<FP8>& sm, uint32_t tmem, c
   }
 }
 
-template <bool FP8>
+// tm_kr, tm_vr: the repair K and V tiles (REP; bf16 [B*H, R, 128], boxes of
+// 64 dims x 128 rows); other instances never read them.
+template <bool FP8, bool REP = false, bool SOL = false>
 __global__ void __launch_bounds__(THREADS, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o, const Params prm) {
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                const __grid_constant__ CUtensorMap tm_kr, const __grid_constant__ CUtensorMap tm_vr,
+                const Params prm) {
+  static_assert(FP8 || !REP, "the repair blocks belong to the FP8 kernel");
+  static_assert(!FP8 || !SOL, "the block-sparse kernel is BF16");
   constexpr int KST = Traits<FP8>::KST, VST = Traits<FP8>::VST;
   extern __shared__ uint8_t smem_raw[];
   Smem<FP8>& sm =
@@ -520,6 +713,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int s = 0; s < KST; ++s) { mbar_init(&sm.k_full[s], 1); mbar_init(&sm.k_empty[s], 1); }
     for (int s = 0; s < VST; ++s) { mbar_init(&sm.v_full[s], 1); mbar_init(&sm.v_empty[s], 1); }
+    for (int t = 0; t < TILES; ++t) mbar_init(&sm.qbf_full[t], BM);
+    mbar_init(&sm.krep_full, 1);
+    mbar_init(&sm.krep_empty, 1);
+    mbar_init(&sm.vrep_full, 1);
+    mbar_init(&sm.vrep_empty, 1);
+    mbar_init(&sm.qbf_free, 1);
+    mbar_init(&sm.vrep_free, 1);
     mbar_init(&sm.mma_drain, 1);
     mbar_init(&sm.never, 1);
     sm.abort = 0;
@@ -528,8 +728,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == WARP_LOAD_V && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_v);
+    if (REP) tma_prefetch_desc(&tm_vr);
   }
-  if (warp == WARP_LOAD_K && lane == 0) tma_prefetch_desc(&tm_k);
+  if (warp == WARP_LOAD_K && lane == 0) {
+    tma_prefetch_desc(&tm_k);
+    if (REP) tma_prefetch_desc(&tm_kr);
+  }
   if (warp == WARP_MMA) {
     tmem_alloc(&sm.tmem_base, TMEM_COLS);
     tmem_relinquish();
@@ -542,6 +746,14 @@ __global__ void __launch_bounds__(THREADS, 1)
   // in the stream (the prologue): the setup above overlaps that kernel's
   // tail, and no thread reads global memory before this wait.
   griddep_wait();
+  // SOL: this CTA's list of key blocks; otherwise every block in order
+  const uint16_t* lst = nullptr;
+  int nkv = prm.nkv;
+  if (SOL) {
+    const size_t c = static_cast<size_t>(bh) * gridDim.x + blockIdx.x;
+    lst = prm.sol_list + c * prm.sol_nb;
+    nkv = __ldg(prm.sol_count + c);
+  }
 
   if (prm.debug & 1) {  // FLUX_ATTN_DEBUG_FORCE_TIMEOUT: a wait nothing will satisfy
     if (threadIdx.x == 0) mbar_wait(&sm.never, 0, ab, prm.err);
@@ -549,17 +761,18 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 
   if (warp == WARP_LOAD_K) {
-    if (lane == 0 && !*ab) load_k<FP8>(sm, &tm_k, bh, prm.nkv, ab, prm.err);
+    if (lane == 0 && !*ab) load_k<FP8, REP, SOL>(sm, &tm_k, &tm_kr, bh, nkv, prm.nrep, lst, ab, prm.err);
     __syncwarp();
   } else if (warp == WARP_LOAD_V) {
-    if (lane == 0 && !*ab) load_qv<FP8>(sm, &tm_q, &tm_v, q0, bh, b, h, prm.nkv, ab, prm.err);
+    if (lane == 0 && !*ab)
+      load_qv<FP8, REP, SOL>(sm, &tm_q, &tm_v, &tm_vr, q0, bh, b, h, nkv, prm.nrep, lst, ab, prm.err);
     __syncwarp();
   } else if (warp == WARP_MMA) {
-    if (!*ab) mma_issuer<FP8>(sm, tmem, prm.nkv, ab, prm.err);  // the whole warp: see mma_commit
+    if (!*ab) mma_issuer<FP8, REP>(sm, tmem, nkv, prm.nrep, ab, prm.err);  // the whole warp: see mma_commit
     __syncwarp();
   } else {
     const int t = warp >> 2;  // query tile of this warpgroup
-    if (!*ab) softmax_epilogue<FP8>(sm, tmem, prm, b, h, q0 + t * BM, t, ab, &tm_o);
+    if (!*ab) softmax_epilogue<FP8, REP, SOL>(sm, tmem, prm, b, h, q0 + t * BM, t, nkv, lst, ab, &tm_o);
   }
   tc_fence_before_sync();
   __syncthreads();

@@ -20,6 +20,8 @@
 #include "prologue.cuh"
 #include "qkv_gemm.cuh"
 #include "quantize_fp8.cuh"
+#include "sol_sparse.cuh"
+#include "vc_repair.cuh"
 
 struct flux_attn {
   flux_attn_config cfg;
@@ -36,6 +38,17 @@ struct flux_attn {
   uint32_t* amax;         // FP8: [B, H, 3] fp32 bits
   float* scales;          // FP8: [B, H, 3]
   float2* rope;           // BF16: (cos, sin) table [max_tokens][64] of the QKV projection
+  float* errk;            // VC: K' quantisation error per token [B*H][max_tokens]
+  float* errv;            // VC: V quantisation error per token [B*H][max_tokens]
+  int32_t* sel;           // VC: repaired tokens [B*H][r_max]
+  __nv_bfloat16* krep;    // VC: k' / s_k of the repaired tokens [B*H][r_max][128]
+  __nv_bfloat16* vrep;    // VC: v / s_v of the repaired tokens [B*H][r_max][128]
+  int r_max;              // VC: ceil(rho max_tokens)
+  float* qbar;            // SOL: block means of Q' [B*H][nb_max][128]
+  float* kbar;            // SOL: block means of K' [B*H][nb_max][128]
+  uint8_t* keep;          // SOL: block mask [B*H][nb][nb] of the last forward
+  uint16_t* sol_list;     // SOL: key-block lists [B*H][ncta][nb]
+  int* sol_count;         // SOL: list lengths [B*H][ncta]
   uint32_t* err;          // device error word
   flux::RopeTable rope_tab;
 };
@@ -43,6 +56,9 @@ struct flux_attn {
 namespace {
 
 thread_local std::string g_last_error;
+
+// Sol-Attention's block mask holds nb^2 bytes per head (nb = max_tokens / 128).
+constexpr int kSolMaxTokens = 1 << 18;
 
 // An NVTX range over the host-side enqueue of one call or one kernel launch:
 // profilers (Nsight Systems, ncu --nvtx) show the library's steps by name.
@@ -178,13 +194,25 @@ int launch_prologue(flux_attn* h, const void* q, const void* k, int txt, int ih,
 
 size_t pad16(int n) { return (static_cast<size_t>(n) + 15) & ~size_t(15); }
 
+// Key tokens a head repairs for n tokens (VC-Attention): ceil(rho n) in
+// [0, n], rho the handle's repair budget.
+int repair_count(const flux_attn* h, int n) {
+  const double r = std::ceil(static_cast<double>(h->cfg.vc_repair_budget) * static_cast<double>(n));
+  if (!(r > 0.0)) return 0;
+  return r > n ? n : static_cast<int>(r);
+}
+
 // The FP8 prologue: amax of V, Q', K' (after zeroing it), then the codes of
 // V transposed, then the E4M3 codes of Q', K' and the scales (last, so that
 // the kernel before the attention is the one-wave stream kernel that lets it
 // start early).
+// With VC-Attention (repair count R > 0) the quantisers also write the
+// per-token K' and V errors, and two more kernels select the repaired tokens
+// (sel) and move them out of the codes, writing their exact rows (krep, vrep).
 int launch_prologue_fp8(flux_attn* h, const void* q, const void* k, const void* v, int txt, int ih, int iw,
                         int rw, const int32_t* pos, const float* wq, const float* wk, int n, uint8_t* q8,
-                        uint8_t* k8, uint8_t* v8t, float* scales, cudaStream_t stream) {
+                        uint8_t* k8, uint8_t* v8t, float* scales, int32_t* sel, __nv_bfloat16* krep,
+                        __nv_bfloat16* vrep, cudaStream_t stream) {
   NvtxRange range("flux_attn/fp8_prologue");
   flux::TokenGeometry geo{pos, txt, ih * iw, iw, rw};
   const int B = h->cfg.batch, H = h->cfg.num_heads;
@@ -229,25 +257,45 @@ int launch_prologue_fp8(flux_attn* h, const void* q, const void* k, const void* 
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "amax launch");
-  flux::fp8_vt_kernel<<<vgrid, flux::kVtThreads, 0, stream>>>(tv, tvt, H, h->amax, h->err);
+  const int R = repair_count(h, n);
+  flux::fp8_vt_kernel<<<vgrid, flux::kVtThreads, 0, stream>>>(tv, tvt, H, h->amax, h->err, R > 0 ? h->errv : nullptr,
+                                                             n);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "V^T launch");
   {
     const int W = flux::stream_warps<flux::E4m3Rows>(H);
     const unsigned grid = static_cast<unsigned>(std::min<long long>((tokens + W - 1) / W, h->num_sms));
-    const flux::E4m3Rows codes{q8, k8, h->amax, scales, H, B * H * 3};
+    const flux::E4m3Rows codes{q8, k8, h->amax, scales, H, B * H * 3, R > 0 ? h->errk : nullptr};
     flux::qk_norm_rope_kernel<flux::E4m3Rows>
         <<<grid, 32 * W, flux::stream_smem<flux::E4m3Rows>(H), stream>>>(a, codes);
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "quantise launch");
+  if (R == 0) return FLUX_ATTN_OK;
+  {
+    NvtxRange vc_range("flux_attn/vc_repair");
+    flux::vc::vc_select_kernel<<<B * H, flux::vc::kSelectThreads, 0, stream>>>(h->errk, h->errv, n, R, sel);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "repair selection launch");
+    const flux::vc::RepairArgs ra{static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), wk,
+                                  geo, h->rope_tab, n, H, R, h->cfg.rms_eps, scales, sel, k8, v8t, pad16(n), krep,
+                                  vrep};
+    flux::vc::vc_repair_kernel<<<B * H, flux::vc::kRepairThreads, 0, stream>>>(ra);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "repair launch");
+  }
   return FLUX_ATTN_OK;
 }
 
 // The attention kernel.  BF16: qn, kn bf16 [B*H, n, 128], v bf16 [B, n, H, 128].
 // FP8: qn, kn E4M3 [B*H, n, 128], v E4M3 V^T [B*H, 128, pad16(n)], scales [B*H, 3].
+// VC (FP8, R = repair_count > 0): krep, vrep bf16 [B*H, R, 128], and kn, v
+// hold the other N - R keys in their first N - R positions.
+// SOL (BF16, sol_list set): the block-sparse instance over the lists of
+// sol_list_kernel (nb = ceil(n / 128) entries per list).
 int launch_attention(flux_attn* h, bool fp8, const void* qn, const void* kn, const void* v, const float* scales,
-                     int n, void* out, cudaStream_t stream) {
+                     int n, void* out, cudaStream_t stream, const void* krep = nullptr, const void* vrep = nullptr,
+                     const uint16_t* sol_list = nullptr, const int* sol_count = nullptr) {
   NvtxRange range(fp8 ? "flux_attn/attention_fp8" : "flux_attn/attention");
   using namespace flux::attn;
   const int B = h->cfg.batch, H = h->cfg.num_heads;
@@ -290,13 +338,31 @@ int launch_attention(flux_attn* h, bool fp8, const void* qn, const void* kn, con
     int rc = encode_tiled(&to, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, out, dims, strides, box, "out");
     if (rc) return rc;
   }
+  const int R = fp8 ? repair_count(h, n) : 0;
+  CUtensorMap tkr = tq, tvr = tq;  // read only by the repair instance
+  if (R > 0) {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(HD), static_cast<cuuint64_t>(R),
+                                static_cast<cuuint64_t>(B) * H};
+    const cuuint64_t strides[2] = {HD * 2ull, static_cast<cuuint64_t>(R) * HD * 2ull};
+    const cuuint32_t box[3] = {64, BN, 1};  // rows >= R arrive as zeros
+    int rc = encode_tiled(&tkr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, krep, dims, strides, box, "K_rep");
+    if (rc) return rc;
+    rc = encode_tiled(&tvr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, vrep, dims, strides, box, "V_rep");
+    if (rc) return rc;
+  }
   Params prm;
   prm.out = static_cast<__nv_bfloat16*>(out);
   prm.err = h->err;
   prm.scales = scales;
   prm.N = n;
   prm.H = H;
-  prm.nkv = (n + BN - 1) / BN;
+  prm.nrep = (R + BN - 1) / BN;
+  prm.rep_keys = R;
+  prm.main_keys = n - R;
+  prm.nkv = prm.nrep + (n - R + BN - 1) / BN;
+  prm.sol_list = sol_list;
+  prm.sol_count = sol_count;
+  prm.sol_nb = (n + BN - 1) / BN;
   prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(HD)));
   prm.debug = h->cfg.debug_flags;
   // Programmatic stream serialisation: the grid may start before the kernel
@@ -312,11 +378,44 @@ int launch_attention(flux_attn* h, bool fp8, const void* qn, const void* kn, con
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = 1;
-  cudaError_t e = fp8 ? cudaLaunchKernelEx(&lc, attn_kernel<true>, tq, tk, tv, to, prm)
-                      : cudaLaunchKernelEx(&lc, attn_kernel<false>, tq, tk, tv, to, prm);
+  cudaError_t e = R > 0 ? cudaLaunchKernelEx(&lc, attn_kernel<true, true>, tq, tk, tv, to, tkr, tvr, prm)
+                  : fp8   ? cudaLaunchKernelEx(&lc, attn_kernel<true, false>, tq, tk, tv, to, tkr, tvr, prm)
+                  : sol_list != nullptr
+                      ? cudaLaunchKernelEx(&lc, attn_kernel<false, false, true>, tq, tk, tv, to, tkr, tvr, prm)
+                      : cudaLaunchKernelEx(&lc, attn_kernel<false, false>, tq, tk, tv, to, tkr, tvr, prm);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   return FLUX_ATTN_OK;
+}
+
+// Sol-Attention, BF16 Q', K' bf16 [B*H, n, 128]: block means and the keep
+// mask (keep: [B*H][nb][nb] uint8).
+int launch_sol_mask(flux_attn* h, const void* qn, const void* kn, int n, uint8_t* keep, cudaStream_t stream) {
+  NvtxRange range("flux_attn/sol_mask");
+  const int BH = h->cfg.batch * h->cfg.num_heads;
+  const int nb = (n + flux::sol::kBlock - 1) / flux::sol::kBlock;
+  flux::sol::sol_pool_kernel<<<dim3(nb, BH), flux::sol::kThreads, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(qn), static_cast<const __nv_bfloat16*>(kn), n, h->qbar, h->kbar);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "block pooling launch");
+  flux::sol::sol_keep_kernel<<<dim3(nb, BH), flux::sol::kThreads, 0, stream>>>(h->qbar, h->kbar, n, h->cfg.sol_tau,
+                                                                               keep);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "block mask launch");
+  return FLUX_ATTN_OK;
+}
+
+// Sol-Attention: the per-CTA key-block lists of a mask, then the sparse attention.
+int launch_sol_attention(flux_attn* h, const void* qn, const void* kn, const void* v, const uint8_t* keep, int n,
+                         void* out, cudaStream_t stream) {
+  const int BH = h->cfg.batch * h->cfg.num_heads;
+  const int nb = (n + flux::sol::kBlock - 1) / flux::sol::kBlock;
+  const int ncta = (n + flux::attn::CTA_ROWS - 1) / flux::attn::CTA_ROWS;
+  flux::sol::sol_list_kernel<<<dim3(ncta, BH), flux::sol::kThreads, 0, stream>>>(keep, nb, h->sol_list,
+                                                                                h->sol_count);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "block list launch");
+  return launch_attention(h, false, qn, kn, v, nullptr, n, out, stream, nullptr, nullptr, h->sol_list, h->sol_count);
 }
 
 // The QKV projection with its fused epilogue: the (cos, sin) table of the
@@ -402,10 +501,16 @@ cudaError_t set_attention_smem_limits() {
   e = cudaFuncSetAttribute(flux::qkv::qkv_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(flux::qkv::SMEM_BYTES));
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(flux::attn::attn_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(flux::attn::attn_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(flux::attn::smem_bytes<false>()));
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(flux::attn::attn_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(flux::attn::attn_kernel<false, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(flux::attn::smem_bytes<false>()));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(flux::attn::attn_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(flux::attn::smem_bytes<true>()));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(flux::attn::attn_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(flux::attn::smem_bytes<true>()));
 }
 
@@ -453,6 +558,16 @@ int flux_attn_create(const flux_attn_config* cfg, flux_attn_t* out) {
     return fail(FLUX_ATTN_ERR_INVALID_ARG, "rope_theta must be > 0 and rms_eps >= 0");
   if (cfg->precision != FLUX_ATTN_BF16 && cfg->precision != FLUX_ATTN_FP8_E4M3)
     return fail(FLUX_ATTN_ERR_INVALID_ARG, "unknown precision %d", cfg->precision);
+  if (!(cfg->vc_repair_budget >= 0.f && cfg->vc_repair_budget <= 1.f))
+    return fail(FLUX_ATTN_ERR_INVALID_ARG, "vc_repair_budget must be in [0, 1]");
+  if (cfg->vc_repair_budget > 0.f && cfg->precision != FLUX_ATTN_FP8_E4M3)
+    return fail(FLUX_ATTN_ERR_INVALID_ARG, "vc_repair_budget > 0 needs precision FLUX_ATTN_FP8_E4M3");
+  if (!(cfg->sol_tau >= 0.f) || cfg->sol_tau > 3.0e38f)
+    return fail(FLUX_ATTN_ERR_INVALID_ARG, "sol_tau must be finite and >= 0");
+  if (cfg->sol_tau > 0.f && cfg->precision != FLUX_ATTN_BF16)
+    return fail(FLUX_ATTN_ERR_INVALID_ARG, "sol_tau > 0 needs precision FLUX_ATTN_BF16");
+  if (cfg->sol_tau > 0.f && cfg->max_tokens > kSolMaxTokens)
+    return fail(FLUX_ATTN_ERR_UNSUPPORTED, "Sol-Attention is built for max_tokens <= %d", kSolMaxTokens);
 
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -494,7 +609,20 @@ int flux_attn_create(const flux_attn_config* cfg, flux_attn_t* out) {
   const size_t sc_bytes = fp8 ? al(bh * 3 * sizeof(float)) : 0;
   const size_t rope_bytes = fp8 ? 0 : al(static_cast<size_t>(cfg->max_tokens) * (flux::kHeadDim / 2) * sizeof(float2));
   const size_t v_bytes = fp8 ? 0 : qk_bytes;
-  const size_t err_off = 2 * qk_bytes + vt_bytes + 2 * sc_bytes + rope_bytes + v_bytes;
+  h->r_max = repair_count(h, cfg->max_tokens);
+  const size_t vc_err_bytes = h->r_max > 0 ? al(bh * cfg->max_tokens * sizeof(float)) : 0;
+  const size_t vc_sel_bytes = h->r_max > 0 ? al(bh * h->r_max * sizeof(int32_t)) : 0;
+  const size_t vc_row_bytes = h->r_max > 0 ? al(bh * h->r_max * flux::kHeadDim * 2) : 0;
+  const size_t vc_off = 2 * qk_bytes + vt_bytes + 2 * sc_bytes + rope_bytes + v_bytes;
+  const bool sol = cfg->sol_tau > 0.f;
+  const size_t nb_max = (static_cast<size_t>(cfg->max_tokens) + 127) / 128;
+  const size_t ncta_max = (static_cast<size_t>(cfg->max_tokens) + 255) / 256;
+  const size_t sol_bar_bytes = sol ? al(bh * nb_max * flux::kHeadDim * sizeof(float)) : 0;
+  const size_t sol_keep_bytes = sol ? al(bh * nb_max * nb_max) : 0;
+  const size_t sol_list_bytes = sol ? al(bh * ncta_max * nb_max * sizeof(uint16_t)) : 0;
+  const size_t sol_count_bytes = sol ? al(bh * ncta_max * sizeof(int)) : 0;
+  const size_t sol_off = vc_off + 2 * vc_err_bytes + vc_sel_bytes + 2 * vc_row_bytes;
+  const size_t err_off = sol_off + 2 * sol_bar_bytes + sol_keep_bytes + sol_list_bytes + sol_count_bytes;
   h->ws_bytes = err_off + 256;
   e = cudaMalloc(&h->ws, h->ws_bytes);
   if (e != cudaSuccess) {
@@ -515,6 +643,20 @@ int flux_attn_create(const flux_attn_config* cfg, flux_attn_t* out) {
     h->kn = reinterpret_cast<__nv_bfloat16*>(base + qk_bytes);
     h->rope = reinterpret_cast<float2*>(base + 2 * qk_bytes);
     h->vw = reinterpret_cast<__nv_bfloat16*>(base + 2 * qk_bytes + rope_bytes);
+  }
+  if (h->r_max > 0) {
+    h->errk = reinterpret_cast<float*>(base + vc_off);
+    h->errv = reinterpret_cast<float*>(base + vc_off + vc_err_bytes);
+    h->sel = reinterpret_cast<int32_t*>(base + vc_off + 2 * vc_err_bytes);
+    h->krep = reinterpret_cast<__nv_bfloat16*>(base + vc_off + 2 * vc_err_bytes + vc_sel_bytes);
+    h->vrep = reinterpret_cast<__nv_bfloat16*>(base + vc_off + 2 * vc_err_bytes + vc_sel_bytes + vc_row_bytes);
+  }
+  if (sol) {
+    h->qbar = reinterpret_cast<float*>(base + sol_off);
+    h->kbar = reinterpret_cast<float*>(base + sol_off + sol_bar_bytes);
+    h->keep = base + sol_off + 2 * sol_bar_bytes;
+    h->sol_list = reinterpret_cast<uint16_t*>(base + sol_off + 2 * sol_bar_bytes + sol_keep_bytes);
+    h->sol_count = reinterpret_cast<int*>(base + sol_off + 2 * sol_bar_bytes + sol_keep_bytes + sol_list_bytes);
   }
   h->err = reinterpret_cast<uint32_t*>(base + err_off);
   e = cudaMemset(h->err, 0, 256);
@@ -546,7 +688,9 @@ int flux_attn_launches_per_forward(flux_attn_t h, int n_tokens) {
   // BF16: prologue + attention; FP8: V amax + Q'/K' amax + Q'/K' codes +
   // V^T codes + attention (the amax zeroing is a cudaMemsetAsync, not a
   // kernel of this library).
-  return h->cfg.precision == FLUX_ATTN_FP8_E4M3 ? 5 : 2;
+  // VC-Attention adds the repair selection and the repair kernel.
+  if (h->cfg.precision != FLUX_ATTN_FP8_E4M3) return 2;
+  return repair_count(h, n_tokens) > 0 ? 7 : 5;
 }
 
 static int check_common(flux_attn* h, const void* q, const void* k, int txt, int ih, int iw, int rh, int rw,
@@ -622,9 +766,9 @@ int flux_attn_forward(flux_attn_t h, const void* q, const void* k, const void* v
     return launch_attention(h, false, h->qn, h->kn, v, nullptr, n, out, stream);
   }
   rc = launch_prologue_fp8(h, q, k, v, txt_len, img_h, img_w, ref_w, pos_ids, q_norm_w, k_norm_w, n, h->q8, h->k8,
-                           h->v8t, h->scales, stream);
+                           h->v8t, h->scales, h->sel, h->krep, h->vrep, stream);
   if (rc) return rc;
-  return launch_attention(h, true, h->q8, h->k8, h->v8t, h->scales, n, out, stream);
+  return launch_attention(h, true, h->q8, h->k8, h->v8t, h->scales, n, out, stream, h->krep, h->vrep);
 }
 
 int flux_attn_prologue_fp8(flux_attn_t h, const void* q, const void* k, const void* v, int txt_len, int img_h,
@@ -644,9 +788,44 @@ int flux_attn_prologue_fp8(flux_attn_t h, const void* q, const void* k, const vo
   if ((rc = check_buffer(k8, bh * n * flux::kHeadDim, "k8"))) return rc;
   if ((rc = check_buffer(v8t, bh * flux::kHeadDim * pad16(n), "v8t"))) return rc;
   if ((rc = check_buffer(scales, bh * 3 * sizeof(float), "scales"))) return rc;
+  if (repair_count(h, n) > 0)
+    return fail(FLUX_ATTN_ERR_INVALID_ARG, "a VC-Attention handle takes flux_attn_prologue_fp8_vc");
   return launch_prologue_fp8(h, q, k, v, txt_len, img_h, img_w, ref_w, pos_ids, q_norm_w, k_norm_w, n,
                              static_cast<uint8_t*>(q8), static_cast<uint8_t*>(k8), static_cast<uint8_t*>(v8t),
-                             scales, stream);
+                             scales, nullptr, nullptr, nullptr, stream);
+}
+
+int flux_attn_prologue_fp8_vc(flux_attn_t h, const void* q, const void* k, const void* v, int txt_len, int img_h,
+                              int img_w, int ref_h, int ref_w, const int32_t* pos_ids, const float* q_norm_w,
+                              const float* k_norm_w, void* q8, void* k8, void* v8t, float* scales,
+                              int32_t* repair_idx, void* k_rep, void* v_rep, cudaStream_t stream) {
+  g_last_error.clear();
+  NvtxRange range("flux_attn_prologue_fp8_vc");
+  int n = 0;
+  int rc = check_common(h, q, k, txt_len, img_h, img_w, ref_h, ref_w, pos_ids, q_norm_w, k_norm_w, &n);
+  if (rc || n == 0) return rc;
+  if (h->cfg.precision != FLUX_ATTN_FP8_E4M3)
+    return fail(FLUX_ATTN_ERR_INVALID_ARG, "flux_attn_prologue_fp8_vc needs an FP8 handle");
+  const int R = repair_count(h, n);
+  if (R == 0) return fail(FLUX_ATTN_ERR_INVALID_ARG, "the handle repairs no token for %d tokens", n);
+  const size_t bh = static_cast<size_t>(h->cfg.batch) * h->cfg.num_heads;
+  if ((rc = check_buffer(v, row_bytes(h, n), "v"))) return rc;
+  if ((rc = check_buffer(q8, bh * n * flux::kHeadDim, "q8"))) return rc;
+  if ((rc = check_buffer(k8, bh * n * flux::kHeadDim, "k8"))) return rc;
+  if ((rc = check_buffer(v8t, bh * flux::kHeadDim * pad16(n), "v8t"))) return rc;
+  if ((rc = check_buffer(scales, bh * 3 * sizeof(float), "scales"))) return rc;
+  if ((rc = check_buffer(repair_idx, bh * R * sizeof(int32_t), "repair_idx"))) return rc;
+  if ((rc = check_buffer(k_rep, bh * R * flux::kHeadDim * 2, "k_rep"))) return rc;
+  if ((rc = check_buffer(v_rep, bh * R * flux::kHeadDim * 2, "v_rep"))) return rc;
+  return launch_prologue_fp8(h, q, k, v, txt_len, img_h, img_w, ref_w, pos_ids, q_norm_w, k_norm_w, n,
+                             static_cast<uint8_t*>(q8), static_cast<uint8_t*>(k8), static_cast<uint8_t*>(v8t),
+                             scales, repair_idx, static_cast<__nv_bfloat16*>(k_rep),
+                             static_cast<__nv_bfloat16*>(v_rep), stream);
+}
+
+int flux_attn_vc_repair_count(flux_attn_t h, int n_tokens) {
+  if (h == nullptr || n_tokens <= 0 || h->cfg.precision != FLUX_ATTN_FP8_E4M3) return 0;
+  return repair_count(h, n_tokens);
 }
 
 int flux_attn_attend_fp8(flux_attn_t h, const void* q8, const void* k8, const void* v8t, const float* scales,
@@ -667,7 +846,105 @@ int flux_attn_attend_fp8(flux_attn_t h, const void* q8, const void* k8, const vo
   if ((rc = check_buffer(v8t, bh * flux::kHeadDim * pad16(n_tokens), "v8t"))) return rc;
   if ((rc = check_buffer(scales, bh * 3 * sizeof(float), "scales"))) return rc;
   if ((rc = check_buffer(out, row_bytes(h, n_tokens), "out"))) return rc;
+  if (repair_count(h, n_tokens) > 0)
+    return fail(FLUX_ATTN_ERR_INVALID_ARG, "a VC-Attention handle takes flux_attn_attend_fp8_vc");
   return launch_attention(h, true, q8, k8, v8t, scales, n_tokens, out, stream);
+}
+
+int flux_attn_attend_fp8_vc(flux_attn_t h, const void* q8, const void* k8, const void* v8t, const float* scales,
+                            const void* k_rep, const void* v_rep, int n_tokens, void* out, cudaStream_t stream) {
+  g_last_error.clear();
+  NvtxRange range("flux_attn_attend_fp8_vc");
+  int rc = check_handle(h);
+  if (rc) return rc;
+  if (h->cfg.precision != FLUX_ATTN_FP8_E4M3)
+    return fail(FLUX_ATTN_ERR_INVALID_ARG, "flux_attn_attend_fp8_vc needs an FP8 handle");
+  if (n_tokens < 0 || n_tokens > h->cfg.max_tokens)
+    return fail(FLUX_ATTN_ERR_INVALID_ARG, "n_tokens = %d outside [0, max_tokens = %d]", n_tokens,
+                h->cfg.max_tokens);
+  if (n_tokens == 0) return FLUX_ATTN_OK;
+  const int R = repair_count(h, n_tokens);
+  if (R == 0) return fail(FLUX_ATTN_ERR_INVALID_ARG, "the handle repairs no token for %d tokens", n_tokens);
+  const size_t bh = static_cast<size_t>(h->cfg.batch) * h->cfg.num_heads;
+  if ((rc = check_buffer(q8, bh * n_tokens * flux::kHeadDim, "q8"))) return rc;
+  if ((rc = check_buffer(k8, bh * n_tokens * flux::kHeadDim, "k8"))) return rc;
+  if ((rc = check_buffer(v8t, bh * flux::kHeadDim * pad16(n_tokens), "v8t"))) return rc;
+  if ((rc = check_buffer(scales, bh * 3 * sizeof(float), "scales"))) return rc;
+  if ((rc = check_buffer(k_rep, bh * R * flux::kHeadDim * 2, "k_rep"))) return rc;
+  if ((rc = check_buffer(v_rep, bh * R * flux::kHeadDim * 2, "v_rep"))) return rc;
+  if ((rc = check_buffer(out, row_bytes(h, n_tokens), "out"))) return rc;
+  return launch_attention(h, true, q8, k8, v8t, scales, n_tokens, out, stream, k_rep, v_rep);
+}
+
+static int sol_handle(flux_attn* h, const char* what) {
+  int rc = check_handle(h);
+  if (rc) return rc;
+  if (h->cfg.precision != FLUX_ATTN_BF16 || !(h->cfg.sol_tau > 0.f))
+    return fail(FLUX_ATTN_ERR_INVALID_ARG, "%s needs a BF16 handle with sol_tau > 0", what);
+  return FLUX_ATTN_OK;
+}
+
+int flux_attn_sol_mask(flux_attn_t h, const void* qn, const void* kn, int n_tokens, uint8_t* keep,
+                       cudaStream_t stream) {
+  g_last_error.clear();
+  NvtxRange range("flux_attn_sol_mask");
+  int rc = sol_handle(h, "flux_attn_sol_mask");
+  if (rc) return rc;
+  if (n_tokens < 0 || n_tokens > h->cfg.max_tokens)
+    return fail(FLUX_ATTN_ERR_INVALID_ARG, "n_tokens = %d outside [0, max_tokens = %d]", n_tokens,
+                h->cfg.max_tokens);
+  if (n_tokens == 0) return FLUX_ATTN_OK;
+  const size_t bh = static_cast<size_t>(h->cfg.batch) * h->cfg.num_heads;
+  const size_t nb = (static_cast<size_t>(n_tokens) + 127) / 128;
+  if ((rc = check_buffer(qn, row_bytes(h, n_tokens), "qn"))) return rc;
+  if ((rc = check_buffer(kn, row_bytes(h, n_tokens), "kn"))) return rc;
+  if ((rc = check_buffer(keep, bh * nb * nb, "keep"))) return rc;
+  return launch_sol_mask(h, qn, kn, n_tokens, keep, stream);
+}
+
+int flux_attn_attend_sol(flux_attn_t h, const void* qn, const void* kn, const void* v, const uint8_t* keep,
+                         int n_tokens, void* out, cudaStream_t stream) {
+  g_last_error.clear();
+  NvtxRange range("flux_attn_attend_sol");
+  int rc = sol_handle(h, "flux_attn_attend_sol");
+  if (rc) return rc;
+  if (n_tokens < 0 || n_tokens > h->cfg.max_tokens)
+    return fail(FLUX_ATTN_ERR_INVALID_ARG, "n_tokens = %d outside [0, max_tokens = %d]", n_tokens,
+                h->cfg.max_tokens);
+  if (n_tokens == 0) return FLUX_ATTN_OK;
+  const size_t bh = static_cast<size_t>(h->cfg.batch) * h->cfg.num_heads;
+  const size_t nb = (static_cast<size_t>(n_tokens) + 127) / 128;
+  const size_t bytes = row_bytes(h, n_tokens);
+  if ((rc = check_buffer(qn, bytes, "qn"))) return rc;
+  if ((rc = check_buffer(kn, bytes, "kn"))) return rc;
+  if ((rc = check_buffer(v, bytes, "v"))) return rc;
+  if ((rc = check_buffer(keep, bh * nb * nb, "keep"))) return rc;
+  if ((rc = check_buffer(out, bytes, "out"))) return rc;
+  return launch_sol_attention(h, qn, kn, v, keep, n_tokens, out, stream);
+}
+
+int flux_attn_forward_sol(flux_attn_t h, const void* q, const void* k, const void* v, int txt_len, int img_h,
+                          int img_w, int ref_h, int ref_w, const int32_t* pos_ids, const float* q_norm_w,
+                          const float* k_norm_w, float timestep, void* out, cudaStream_t stream) {
+  g_last_error.clear();
+  NvtxRange range("flux_attn_forward_sol");
+  int rc = sol_handle(h, "flux_attn_forward_sol");
+  if (rc) return rc;
+  int n = 0;
+  rc = check_common(h, q, k, txt_len, img_h, img_w, ref_h, ref_w, pos_ids, q_norm_w, k_norm_w, &n);
+  if (rc || n == 0) return rc;
+  const size_t bytes = row_bytes(h, n);
+  if ((rc = check_buffer(v, bytes, "v"))) return rc;
+  if ((rc = check_buffer(out, bytes, "out"))) return rc;
+  if (out == q || out == k || out == v) return fail(FLUX_ATTN_ERR_INVALID_ARG, "out aliases an input");
+  rc = launch_prologue(h, q, k, txt_len, img_h, img_w, ref_h, ref_w, pos_ids, q_norm_w, k_norm_w, h->qn, h->kn, n,
+                       stream);
+  if (rc) return rc;
+  if (timestep > h->cfg.sol_disabled_until_timestep)  // the early (noisy) steps stay dense
+    return launch_attention(h, false, h->qn, h->kn, v, nullptr, n, out, stream);
+  rc = launch_sol_mask(h, h->qn, h->kn, n, h->keep, stream);
+  if (rc) return rc;
+  return launch_sol_attention(h, h->qn, h->kn, v, h->keep, n, out, stream);
 }
 
 int flux_attn_qkv(flux_attn_t h, const void* x, const void* w_qkv, const float* b_qkv, int d_model, int txt_len,
@@ -816,6 +1093,10 @@ extern "C" int flux_attn_forward_noalloc(const flux_attn_config* cfg, const void
     return fail(FLUX_ATTN_ERR_INVALID_ARG, "unknown precision %d", cfg->precision);
   if (cfg->precision != FLUX_ATTN_BF16)
     return fail(FLUX_ATTN_ERR_UNSUPPORTED, "the allocation-free forward is BF16 only");
+  if (cfg->vc_repair_budget != 0.f)
+    return fail(FLUX_ATTN_ERR_INVALID_ARG, "vc_repair_budget > 0 needs precision FLUX_ATTN_FP8_E4M3");
+  if (cfg->sol_tau != 0.f)
+    return fail(FLUX_ATTN_ERR_UNSUPPORTED, "the allocation-free forward is dense only (sol_tau must be 0)");
   if (cfg->batch < 1 || cfg->num_heads < 1 || cfg->max_tokens < 1)
     return fail(FLUX_ATTN_ERR_INVALID_ARG, "batch, num_heads and max_tokens must be >= 1");
   if (cfg->num_heads > flux::kProMaxHeads)

@@ -90,15 +90,6 @@ __device__ __forceinline__ uint4 pack8(const float (&x)[8]) {
   return u;
 }
 
-// (d0, d1) = (a0 b0, a1 b1) in one packed fp32x2 instruction.
-__device__ __forceinline__ void mul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
-  asm("{\n\t.reg .b64 a, b, d;\n\t"
-      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
-      "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
-      : "=f"(d0), "=f"(d1)
-      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
-}
-
 // Per-lane coefficients of the weighted rotation.  With r the row's
 // reciprocal RMS, the weight w and the rotation (c, s) of pair (x0, x1) fold
 // into
@@ -181,9 +172,12 @@ __host__ __device__ constexpr int prologue_warps(int H, int parts, int max_warps
 //   warp_scratch(H)             shared memory per warp it needs after the rings
 //   init(scratch, W, H)         once per warp (all lanes), before the first token
 //   token(b)                    warp-uniform, at every token (b its batch row)
-//   row(t, b, h, dst, x)        one lane's 8 values of row h of tensor t (0: Q',
+//   row(t, b, h, dst, x, valid) one lane's 8 values of row h of tensor t (0: Q',
 //                               1: K'); dst = element offset of those 8 values in
-//                               a head-major [B, H, N, 128] tensor
+//                               a head-major [B, H, N, 128] tensor.  Called by
+//                               all 32 lanes together (warp-uniform); a half-warp
+//                               past the part's last head has valid == false,
+//                               zeros in x, and must store nothing
 //   finish()                    once per warp (all lanes), after the last token
 // and its stream shape: kParts parts per token, kWarps warps per block at
 // most (the rings' shared memory may allow fewer), kPairs head pairs a warp
@@ -199,8 +193,8 @@ struct Bf16Rows {
   static __host__ __device__ constexpr int warp_scratch(int) { return 0; }
   __device__ __forceinline__ void init(uint8_t*, int, int) {}
   __device__ __forceinline__ void token(int) {}
-  __device__ __forceinline__ void row(int t, int, int, size_t dst, const float (&x)[8]) {
-    *reinterpret_cast<uint4*>((t == 0 ? qn : kn) + dst) = pack8(x);
+  __device__ __forceinline__ void row(int t, int, int, size_t dst, const float (&x)[8], bool valid) {
+    if (valid) *reinterpret_cast<uint4*>((t == 0 ? qn : kn) + dst) = pack8(x);
   }
   __device__ __forceinline__ void finish() {}
 };
@@ -334,10 +328,10 @@ __global__ void __launch_bounds__(32 * Out::kWarps, 1) qk_norm_rope_kernel(const
 #pragma unroll
         for (int i = 0; i < kProPairs; ++i) {
           const int h = hp + 2 * i + half;
-          if (h < h1) {
-            out.row(0, b, h, dst + h * head_stride, xq[i]);
-            out.row(1, b, h, dst + h * head_stride, xk[i]);
-          }
+          const bool valid = h < h1;
+          const int hv = valid ? h : h0;
+          out.row(0, b, hv, dst + hv * head_stride, xq[i], valid);
+          out.row(1, b, hv, dst + hv * head_stride, xk[i], valid);
         }
       }
       __syncwarp();  // every lane has read the stage: refill it with part u + S

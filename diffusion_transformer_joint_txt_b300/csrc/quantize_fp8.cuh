@@ -93,7 +93,8 @@ struct AmaxRows {
       cur_b = b;
     }
   }
-  __device__ __forceinline__ void row(int t, int, int h, size_t, const float (&x)[8]) {
+  __device__ __forceinline__ void row(int t, int, int h, size_t, const float (&x)[8], bool valid) {
+    if (!valid) return;
     float* p = slot + (t * H + h) * 16 + (threadIdx.x & 15);
     *p = fmaxf(*p, absmax8(x));
   }
@@ -102,8 +103,30 @@ struct AmaxRows {
   }
 };
 
+// The values two E4M3 codes stand for (c16: two codes, the first in the low byte).
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t c16) {
+  return __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(c16), __NV_E4M3)));
+}
+
+// Squared quantisation error sum_i (x_i - code_i * s)^2 of eight values and their codes.
+__device__ __forceinline__ float sq_error8(const float (&x)[8], uint2 c, float s) {
+  const uint32_t w[4] = {c.x & 0xFFFFu, c.x >> 16, c.y & 0xFFFFu, c.y >> 16};
+  float e = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 d = e4m3x2_to_float2(w[i]);
+    const float r0 = x[2 * i] - d.x * s, r1 = x[2 * i + 1] - d.y * s;
+    e = fmaf(r0, r0, e);
+    e = fmaf(r1, r1, e);
+  }
+  return e;
+}
+
 // Output policy of the stream kernel: E4M3 codes of Q' / s_q and K' / s_k,
-// head-major; block 0 also writes the scales of all three tensors.
+// head-major; block 0 also writes the scales of all three tensors.  With
+// errk set (VC-Attention repair) it also writes, per (b, h, token), the
+// squared quantisation error |k' - code s_k|^2 of the K' row, summed by the
+// half-warp that holds the row in a fixed order.
 struct E4m3Rows {
   static constexpr int kParts = 2;
   static constexpr int kWarps = 12;
@@ -113,6 +136,7 @@ struct E4m3Rows {
   const uint32_t* amax;  // [B*H][3], complete
   float* scales;         // [B*H][3]
   int H, n_scales;
+  float* errk;           // [B*H][N] or nullptr
   static __host__ __device__ constexpr int warp_scratch(int) { return 0; }
   __device__ __forceinline__ void init(uint8_t*, int, int) {
     if (blockIdx.x == 0)
@@ -122,9 +146,18 @@ struct E4m3Rows {
       }
   }
   __device__ __forceinline__ void token(int) {}
-  __device__ __forceinline__ void row(int t, int b, int h, size_t dst, const float (&x)[8]) {
-    const float inv = inv_scale_of(__ldg(amax + (static_cast<size_t>(b) * H + h) * 3 + t));
-    *reinterpret_cast<uint2*>((t == 0 ? q8 : k8) + dst) = quant8(x, inv);
+  __device__ __forceinline__ void row(int t, int b, int h, size_t dst, const float (&x)[8], bool valid) {
+    const uint32_t a = __ldg(amax + (static_cast<size_t>(b) * H + h) * 3 + t);
+    const uint2 c = quant8(x, inv_scale_of(a));
+    if (valid) *reinterpret_cast<uint2*>((t == 0 ? q8 : k8) + dst) = c;
+    if (errk != nullptr && t == 1) {  // warp-uniform: every lane shuffles
+      const float af = __uint_as_float(a);
+      float e = sq_error8(x, c, af > 0.f ? af / kE4M3Max : 1.f);
+#pragma unroll
+      for (int off = 8; off >= 1; off >>= 1) e += __shfl_xor_sync(0xFFFFFFFFu, e, off);
+      // dst / 128 = (b H + h) N + n: the row's token index in [B*H][N]
+      if (valid && (threadIdx.x & 15) == 0) errk[dst >> 7] = e;
+    }
   }
   __device__ __forceinline__ void finish() {}
 };
@@ -192,9 +225,15 @@ __global__ void __launch_bounds__(kVtThreads)
 // consecutive bytes of row d of the transposed tile, and one TMA store puts
 // the tile at v8t[b, h, :, n0 .. n0+63] (clipped at Npad; the zero tokens
 // between N and Npad become the zero padding).
+//
+// With errv set (VC-Attention repair) the kernel also writes, per token of
+// the tile, the squared quantisation error |v - code s_v|^2 of its V row:
+// thread d holds dim d of the 64 tokens, a butterfly over the lanes leaves
+// lane l of warp w with the sums over its 32 dims of tokens 2l and 2l + 1,
+// and thread t < 64 adds the four warps' sums of token t, in a fixed order.
 __global__ void __launch_bounds__(kVtThreads)
     fp8_vt_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_vt, int H,
-                  const uint32_t* __restrict__ amax, uint32_t* err) {
+                  const uint32_t* __restrict__ amax, uint32_t* err, float* __restrict__ errv, int N) {
   __shared__ __align__(128) __nv_bfloat16 vin[kVtTokens][kHeadDim];  // 16 KB
   __shared__ __align__(128) uint8_t vout[kHeadDim][kVtTokens];       // 8 KB
   __shared__ uint64_t bar;
@@ -235,6 +274,38 @@ __global__ void __launch_bounds__(kVtThreads)
     w[t / 4] = __nv_cvt_float2_to_fp8x2(make_float2(x0, x1), __NV_SATFINITE, __NV_E4M3) |
                (static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(x2, x3), __NV_SATFINITE, __NV_E4M3))
                 << 16);
+  }
+  if (errv != nullptr) {  // block-uniform
+    __shared__ float wsum[kVtThreads / 32][kVtTokens];
+    const float sv = am > 0.f ? am / kE4M3Max : 1.f;
+    float e[kVtTokens];
+#pragma unroll
+    for (int t = 0; t < kVtTokens; t += 4) {
+      const float2 a = e4m3x2_to_float2(w[t / 4] & 0xFFFFu), c = e4m3x2_to_float2(w[t / 4] >> 16);
+      const float r0 = __bfloat162float(vin[t][d]) - a.x * sv, r1 = __bfloat162float(vin[t + 1][d]) - a.y * sv;
+      const float r2 = __bfloat162float(vin[t + 2][d]) - c.x * sv, r3 = __bfloat162float(vin[t + 3][d]) - c.y * sv;
+      e[t] = r0 * r0;
+      e[t + 1] = r1 * r1;
+      e[t + 2] = r2 * r2;
+      e[t + 3] = r3 * r3;
+    }
+    // butterfly: at offset o a lane keeps the half of its tokens its bit o selects
+    const int lane = d & 31;
+#pragma unroll
+    for (int o = 16, n = kVtTokens / 2; o >= 1; o >>= 1, n >>= 1) {
+      const bool up = (lane & o) != 0;
+#pragma unroll
+      for (int i = 0; i < n; ++i) {
+        const float keep = up ? e[i + n] : e[i];
+        const float give = up ? e[i] : e[i + n];
+        e[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, give, o);
+      }
+    }
+    wsum[d >> 5][2 * lane] = e[0];
+    wsum[d >> 5][2 * lane + 1] = e[1];
+    __syncthreads();
+    if (d < kVtTokens && n0 + d < N)
+      errv[static_cast<size_t>(bh) * N + n0 + d] = ((wsum[0][d] + wsum[1][d]) + wsum[2][d]) + wsum[3][d];
   }
 #pragma unroll
   for (int c = 0; c < kVtTokens / 16; ++c)

@@ -86,6 +86,22 @@ typedef struct {
   float rms_eps;      /* RMSNorm epsilon, FLUX uses 1e-6 */
   int precision;      /* flux_attn_precision */
   int debug_flags;    /* FLUX_ATTN_DEBUG_* bits, 0 in production */
+  float vc_repair_budget;  /* VC-Attention repair budget rho in [0, 1] (FP8 handles only; 0 = plain
+                              FP8).  Per (b, h) the R = ceil(rho N) key tokens with the largest
+                              quantisation error |k' - deq(k')|^2 + |v - deq(v)|^2 attend with their
+                              exact K', V ("Quantized and sparse attention": vc_attention,
+                              vc_repair_budget 0.005, the fraction of tokens with the highest
+                              quantisation error gets a residual correction).  Equal errors: the lower
+                              token index is repaired first. */
+  float sol_tau;      /* Sol-Attention threshold tau >= 0 (BF16 handles only; 0 = no block-sparse
+                         calls).  Per (b, h), 128-token query block i keeps 128-key block j when the
+                         pooled mass mu_ij = c_j exp(q_bar_i . k_bar_j / sqrt(128)) / sum_j' (...)
+                         (means of the normalised, rotated rows; c_j = keys in block j) is at least
+                         tau / nb, and always keeps its block of largest mass ("Quantized and sparse
+                         attention": algorithm sol_attn, tau 1.0). */
+  float sol_disabled_until_timestep;  /* flux_attn_forward_sol runs dense while timestep > this
+                                         value (the page's configuration: 0.96 on a schedule
+                                         that falls from 1 to 0) */
 } flux_attn_config;
 
 typedef struct flux_attn* flux_attn_t;
@@ -147,6 +163,67 @@ FLUX_ATTN_API int flux_attn_prologue_fp8(flux_attn_t h, const void* q, const voi
  * out bf16 [B, N, H, 128]. */
 FLUX_ATTN_API int flux_attn_attend_fp8(flux_attn_t h, const void* q8, const void* k8, const void* v8t,
                          const float* scales, int n_tokens, void* out, cudaStream_t stream);
+
+/* VC-Attention FP8 ("Speed up image generation with FLUX 3 Image Klein on
+ * NVIDIA Blackwell GPUs", section "Quantized and sparse attention":
+ * vc_attention with a repair budget), step by step, for handles whose
+ * vc_repair_budget gives R = ceil(rho N) > 0 repaired tokens
+ * (flux_attn_forward runs both steps on such a handle; the plain FP8 steps
+ * reject it).  R for n_tokens: flux_attn_vc_repair_count.
+ *
+ * flux_attn_prologue_fp8_vc: the FP8 prologue (codes and scales as for
+ * flux_attn_prologue_fp8), then per (b, h) the R tokens of largest
+ * |k' - deq(k')|^2 + |v - deq(v)|^2 (computed in fp32 from the kernel's own
+ * K' and codes; equal errors: lower index first):
+ *   repair_idx  int32 [B, H, R]: the repaired tokens, ascending
+ *   k8, v8t     the codes of the N - R other tokens sit in positions
+ *               0 .. N-R-1 (a repaired token's position below N - R receives,
+ *               in order, the codes of a non-repaired token from the last R
+ *               positions); positions N-R .. N-1 are not read afterwards
+ *   k_rep, v_rep  bf16 [B, H, R, 128]: k' / s_k and v / s_v of the repaired
+ *               tokens, in repair_idx order (the units of the codes)
+ * flux_attn_attend_fp8_vc: the attention over the outputs of the above:
+ * every query attends to the R repaired keys with their exact values and to
+ * the N - R others through their codes; out bf16 [B, N, H, 128]. */
+FLUX_ATTN_API int flux_attn_prologue_fp8_vc(flux_attn_t h, const void* q, const void* k, const void* v,
+                              int txt_len, int img_h, int img_w, int ref_h, int ref_w,
+                              const int32_t* pos_ids, const float* q_norm_w, const float* k_norm_w,
+                              void* q8, void* k8, void* v8t, float* scales, int32_t* repair_idx,
+                              void* k_rep, void* v_rep, cudaStream_t stream);
+
+FLUX_ATTN_API int flux_attn_attend_fp8_vc(flux_attn_t h, const void* q8, const void* k8, const void* v8t,
+                            const float* scales, const void* k_rep, const void* v_rep, int n_tokens,
+                            void* out, cudaStream_t stream);
+
+/* R = ceil(vc_repair_budget * n_tokens) of the handle (0 for BF16 handles or a zero budget). */
+FLUX_ATTN_API int flux_attn_vc_repair_count(flux_attn_t h, int n_tokens);
+
+/* Sol-Attention ("Speed up image generation with FLUX 3 Image Klein on NVIDIA
+ * Blackwell GPUs", section "Quantized and sparse attention": block-sparse
+ * attention, algorithm sol_attn with tau and disabled_until_timestep), BF16
+ * handles with sol_tau > 0 and max_tokens <= 262144.  nb = ceil(N / 128).
+ *
+ * flux_attn_forward_sol: as flux_attn_forward (same arguments, plus the
+ * denoising timestep), dense when timestep > sol_disabled_until_timestep,
+ * otherwise every query attends only to the keys of the blocks its query
+ * block keeps (the mask of sol_tau, computed on the device from this call's
+ * Q', K' in fp32).
+ * flux_attn_sol_mask: the mask alone, for Q', K' bf16 [B, H, N, 128] as
+ * written by flux_attn_prologue:  keep  uint8 [B, H, nb, nb], 1 = query block
+ * i keeps key block j.
+ * flux_attn_attend_sol: the block-sparse attention for Q', K' (as above), v
+ * bf16 [B, N, H, 128] and any mask keep [B, H, nb, nb] in which every query
+ * block keeps at least one block; out bf16 [B, N, H, 128]. */
+FLUX_ATTN_API int flux_attn_forward_sol(flux_attn_t h, const void* q, const void* k, const void* v,
+                          int txt_len, int img_h, int img_w, int ref_h, int ref_w,
+                          const int32_t* pos_ids, const float* q_norm_w, const float* k_norm_w,
+                          float timestep, void* out, cudaStream_t stream);
+
+FLUX_ATTN_API int flux_attn_sol_mask(flux_attn_t h, const void* qn, const void* kn, int n_tokens,
+                       uint8_t* keep, cudaStream_t stream);
+
+FLUX_ATTN_API int flux_attn_attend_sol(flux_attn_t h, const void* qn, const void* kn, const void* v,
+                         const uint8_t* keep, int n_tokens, void* out, cudaStream_t stream);
 
 /* QKV projection with the query/key normalisation and RoPE fused into the
  * GEMM epilogue ("Speed up image generation with FLUX 3 Image Klein on

@@ -55,6 +55,7 @@ class Workload:
     precision: str = "bf16"        # "bf16" or "fp8"
     outliers: bool = False
     head_dim: int = HEAD_DIM
+    vc_repair_budget: float = 0.0  # FP8 with VC-Attention repair when > 0
 
     @property
     def tokens(self) -> int:
@@ -81,6 +82,9 @@ WORKLOADS: Dict[str, Workload] = {
     "i2i_2048_33280": Workload("i2i_2048_33280", 1, 24, 512, 128, 128, 128, 128),
     "fp8_cfg_2048_16896": Workload("fp8_cfg_2048_16896", 2, 24, 512, 128, 128,
                                    precision="fp8", outliers=True),
+    # the same pair with the VC-Attention repair budget of the page's configuration
+    "vc_fp8_cfg_2048_16896": Workload("vc_fp8_cfg_2048_16896", 2, 24, 512, 128, 128,
+                                      precision="fp8", outliers=True, vc_repair_budget=0.005),
 }
 WORKLOAD_ORDER = ["tiny_320", "flux_1024_4608", "flux_2048_16896",
                   "i2i_2048_33280", "fp8_cfg_2048_16896"]

@@ -107,3 +107,44 @@ def check_rows(got, want, bound, what=""):
     assert ratio.max() <= 1.0, "%s: row %d elem %d off by %.3e, bound %.3e (ratio %.2f)" % (
         what, worst[0], worst[1], abs(got[worst] - want[worst]), bound[worst], ratio.max())
     return float(ratio.max())
+
+
+# ------------------------------------------------------- VC-Attention repair
+
+def vc_dequantised_head(inp, b: int, h: int, rho: float):
+    """The oracle's inputs of VC-Attention for head (b, h) (reading R7 of the
+    oracle): dequantised Q', and K', V dequantised except the repaired tokens,
+    which keep their exact values.  Returns (q, k, v, repaired token indices)."""
+    qd, kd, vd = dequantised_head(inp, b, h)
+    sel, _ = oracle.vc_select_head(inp.q, inp.k, inp.v, inp.pos, inp.w_q, inp.w_k, rho, b, h)
+    kx = oracle.prologue(np.ascontiguousarray(inp.k[b:b + 1, :, h:h + 1, :]), inp.pos, inp.w_k)[0, :, 0, :]
+    vx = (inp.v[b, :, h, :].astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    kd[sel] = kx[sel]
+    vd[sel] = vx[sel]
+    return qd, kd, vd, sel
+
+
+def vc_rows_and_bounds(inp, rows, rho: float):
+    """o and its bound for (b, h, n) rows of VC-Attention.  On top of the P
+    rounding bound, a repaired key carries the GPU's bf16 copies of k' / s_k and
+    v / s_v (relative half step 2^-9): its score moves by at most
+    2^-9 sum_d |q_d k_d| / sqrt(d) (a relative change of p of about as much)
+    and its value by 2^-9 |v|."""
+    d = inp.q.shape[-1]
+    o = np.empty((len(rows), d))
+    bnd = np.empty((len(rows), d))
+    heads = {}
+    for i, (b, h, _) in enumerate(rows):
+        heads.setdefault((int(b), int(h)), []).append(i)
+    for (b, h), idx in heads.items():
+        qd, kd, vd, sel = vc_dequantised_head(inp, b, h, rho)
+        ns = rows[idx, 2]
+        ob, p, l = head_rows(qd, kd, vd, ns)
+        bb = bound_from(ob, p, l, vd)
+        ds = 2.0 ** -9 * (np.abs(qd[ns]) @ np.abs(kd[sel]).T) / np.sqrt(d)     # [R_rows, R_sel]
+        ps = p[:, sel] * 1.01 * np.expm1(ds)                                   # p change of a repaired key
+        bb += (ps[:, :, None] * np.abs(vd[sel][None, :, :] - ob[:, None, :])).sum(axis=1) / l
+        bb += 2.0 ** -9 * (p[:, sel] @ np.abs(vd[sel])) / l
+        o[idx] = ob
+        bnd[idx] = bb
+    return o, bnd
