@@ -90,6 +90,8 @@ def _load():
         lib.oracle_sol_mask_bf16.argtypes = [P, P, I, I, I, I, P, P, P, D, D, P, D, I, I, P, P, I]
         lib.oracle_sol_attention_rows_bf16.restype = I
         lib.oracle_sol_attention_rows_bf16.argtypes = [P, P, P, I, I, I, I, P, P, P, D, D, P, D, P, L, P, I]
+        lib.oracle_fp8_quantize_values.restype = D
+        lib.oracle_fp8_quantize_values.argtypes = [P, L, P]
         lib.oracle_vc_repair_count.restype = L
         lib.oracle_vc_repair_count.argtypes = [D, L]
         lib.oracle_fp8_quantize_head_bf16.restype = I
@@ -213,6 +215,15 @@ def fp8_quantize_head(q, k, v, pos, w_q, w_k, b: int, h: int, eps: float = 1e-6,
     if rc != 0:
         raise ValueError("oracle_fp8_quantize_head failed: %d" % rc)
     return q8, k8, v8, sc
+
+
+def fp8_quantize(x: np.ndarray):
+    """Reading R5 on an array: (E4M3 codes uint8 of x's shape, scale = amax / 448
+    of the whole array, 1 when it is all zero)."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    codes = np.empty(x.shape, np.uint8)
+    scale = _load().oracle_fp8_quantize_values(_ptr(x), x.size, _ptr(codes))
+    return codes, float(scale)
 
 
 def vc_repair_count(rho: float, n_tokens: int) -> int:

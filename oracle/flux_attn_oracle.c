@@ -24,9 +24,9 @@
  *     one GEMM of the hidden states with the stacked Q, K, V weights, and its
  *     epilogue applies the query/key normalisation and RoPE (oracle_qkv_rows).
  *   - same page, section "Quantized and sparse attention": VC-Attention FP8
- *     uses a repair budget (vc_repair_budget 0.005 in its configuration) that
- *     picks the fraction of tokens with the highest quantisation error for a
- *     residual correction (oracle_vc_attention_rows, reading R7).
+ *     takes a repair budget (vc_repair_budget 0.005 in its configuration):
+ *     up to that share of the tokens, the worst quantised ones, get their
+ *     quantisation residual corrected (oracle_vc_attention_rows, reading R7).
  *   - same page, section "Quantized and sparse attention": Sol-Attention
  *     (algorithm sol_attn, tau 1.0, disabled_until_timestep 0.96) runs
  *     block-sparse attention (oracle_sol_attention_rows, reading R8).
@@ -735,4 +735,16 @@ int oracle_sol_attention_rows_bf16(const uint16_t* q, const uint16_t* k, const u
   }
   free(qh); free(kh); free(vh); free(keep); free(mass); free(done);
   return 0;
+}
+
+/* Reading R5 on given values: the E4M3 codes of x[0 .. n) with the scale
+ * amax / 448 of the whole array (1 when it is all zero), as the FP8 path
+ * quantises one (batch, head) of Q', K' or V.  Returns the scale. */
+double oracle_fp8_quantize_values(const double* x, int64_t n, uint8_t* codes) {
+  double* t = (double*)malloc(sizeof(double) * (n > 0 ? n : 1));
+  if (!t) return NAN;
+  memcpy(t, x, sizeof(double) * n);
+  double scale = fp8_roundtrip(t, n, codes);
+  free(t);
+  return scale;
 }

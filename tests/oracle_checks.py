@@ -414,6 +414,25 @@ def check_fp8_attention_on_dequantised_inputs():
     assert np.max(np.abs(plain - got)) > 1e-4
 
 
+def check_fp8_quantize_values_is_the_head_quantiser():
+    """The array entry point quantises like the per-head one (reading R5), and
+    matches torch's cast of 448 x / amax."""
+    q, k, v, pos, wq, wk = _fp8_inputs(25)
+    qn = oracle.prologue(q, pos, wq)
+    q8, _, v8, sc = oracle.fp8_quantize_head(q, k, v, pos, wq, wk, 1, 0)
+    codes, scale = oracle.fp8_quantize(qn[1, :, 0, :])
+    assert np.array_equal(codes, q8) and scale == sc[0]
+    vf = bf16_bits_to_f32(v).astype(np.float64)[1, :, 0, :]
+    codes, scale = oracle.fp8_quantize(vf)
+    assert np.array_equal(codes, v8) and scale == sc[2]
+    x = np.linspace(-3.0, 5.0, 77)
+    codes, scale = oracle.fp8_quantize(x)
+    assert scale == 5.0 / 448.0
+    assert np.array_equal(codes, _torch_e4m3(448.0 * x / 5.0).view(torch.uint8).numpy())
+    codes, scale = oracle.fp8_quantize(np.zeros(5))
+    assert scale == 1.0 and not codes.any()
+
+
 def check_fp8_zero_head():
     q, k, v, pos, wq, wk = _fp8_inputs(19)
     q[:, :, 1] = 0; k[:, :, 1] = 0; v[:, :, 1] = 0
@@ -681,6 +700,7 @@ ALL_CHECKS = [
     check_fp8_codes_and_scales,
     check_fp8_attention_on_dequantised_inputs,
     check_fp8_zero_head,
+    check_fp8_quantize_values_is_the_head_quantiser,
     check_fp8_codes_at_exact_ties,
     check_qkv_matches_numpy_matmul,
     check_qkv_identity_weights,
