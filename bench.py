@@ -47,7 +47,8 @@ import synthetic  # noqa: E402
 import diffusion_transformer_joint_txt_b300 as fa  # noqa: E402
 
 PRIMARY = "flux_1024_4608"
-SECONDARY = ["flux_2048_16896", "i2i_2048_33280", "fp8_cfg_2048_16896", "vc_fp8_cfg_2048_16896"]
+SECONDARY = ["flux_2048_16896", "i2i_2048_33280", "fp8_cfg_2048_16896", "vc_fp8_cfg_2048_16896",
+             "sol_flux_2048_16896"]
 METRIC = "joint-attn TFLOP/s & % of B300 BF16/FP8 TC peak at 4608/16896 tokens"
 FALLBACK_PEAKS = {"bf16_tflops": 1800.0, "hbm_gbs": 6400.0}
 L2_FLUSH_BYTES = 256 << 20
@@ -197,8 +198,12 @@ class Step:
         self.inp, self.q, self.k, self.v, self.wq, self.wk = device_inputs(w, torch)
         n = w.tokens
         self.attn = fa.FluxAttention(w.batch, w.heads, n, precision=w.precision,
-                                     vc_repair_budget=w.vc_repair_budget)
+                                     vc_repair_budget=w.vc_repair_budget, sol_tau=w.sol_tau)
         self.vc = w.vc_repair_budget > 0
+        self.sol = w.sol_tau > 0
+        if self.sol:
+            nb = (n + 127) // 128
+            self.keep = torch.empty((w.batch, w.heads, nb, nb), dtype=torch.uint8, device="cuda")
         self.geo = (w.txt_len, w.img_h, w.img_w, w.ref_h, w.ref_w)
         B, H = w.batch, w.heads
         if self.vc:
@@ -227,6 +232,8 @@ class Step:
                                    v8t=self.v8t, scales=self.scales)
         else:
             self.attn.prologue(self.q, self.k, *self.geo, self.wq, self.wk, qn=self.qn, kn=self.kn)
+            if self.sol:   # the block mask is part of the sparse step's front half
+                fa.flux_attn_sol_mask(self.attn.handle, self.qn, self.kn, self.w.tokens, self.keep)
 
     def attend(self):
         if self.vc:
@@ -234,8 +241,23 @@ class Step:
                                        self.v_rep, self.w.tokens, self.out)
         elif self.fp8:
             self.attn.attend_fp8(self.q8, self.k8, self.v8t, self.scales, out=self.out)
+        elif self.sol:
+            fa.flux_attn_attend_sol(self.attn.handle, self.qn, self.kn, self.v, self.keep, self.w.tokens, self.out)
         else:
             self.attn.attend(self.qn, self.kn, self.v, out=self.out)
+
+    def processed_fraction(self):
+        """Sparse steps: the share of the dense (query tile pair, key block) work
+        the attention kernel does -- each CTA walks the union of the key blocks
+        its two query tiles keep (1 for dense steps)."""
+        if not self.sol:
+            return 1.0, 1.0
+        keep = self.keep.cpu().numpy().astype(bool)
+        nb = keep.shape[-1]
+        if nb % 2:
+            keep = np.concatenate([keep, np.zeros(keep.shape[:2] + (1, nb), bool)], axis=2)
+        union = keep[:, :, 0::2] | keep[:, :, 1::2]
+        return float(union.mean()), float(keep[:, :, :nb].mean())
 
     def __call__(self, ev=None):
         """One step; ev = (start, end) brackets it, ev = (start, split, end)
@@ -279,19 +301,30 @@ class QKVStep:
         self.x, self.wt = dev(inp.x), dev(inp.w)
         self.bias = torch.from_numpy(inp.bias).cuda()
         self.wq, self.wk = torch.from_numpy(inp.w_q).cuda(), torch.from_numpy(inp.w_k).cuda()
-        self.attn = fa.FluxAttention(w.batch, w.heads, w.tokens)
+        self.fp8 = w.precision == "fp8"
+        self.attn = fa.FluxAttention(w.batch, w.heads, w.tokens, precision=w.precision)
         n, B, H = w.tokens, w.batch, w.heads
-        self.qn = torch.empty((B, H, n, 128), dtype=torch.bfloat16, device="cuda")
-        self.kn = torch.empty_like(self.qn)
-        self.v = torch.empty((B, n, H, 128), dtype=torch.bfloat16, device="cuda")
+        if self.fp8:   # the codes the FP8 attention reads
+            self.q8 = torch.empty((B, H, n, 128), dtype=torch.uint8, device="cuda")
+            self.k8 = torch.empty_like(self.q8)
+            self.v8t = torch.empty((B, H, 128, fa.pad16(n)), dtype=torch.uint8, device="cuda")
+            self.scales = torch.empty((B, H, 3), dtype=torch.float32, device="cuda")
+        else:
+            self.qn = torch.empty((B, H, n, 128), dtype=torch.bfloat16, device="cuda")
+            self.kn = torch.empty_like(self.qn)
+            self.v = torch.empty((B, n, H, 128), dtype=torch.bfloat16, device="cuda")
         self.stream = torch.cuda.current_stream()
         self.flops = 2 * B * n * (3 * H * 128) * inp.d_model
 
     def __call__(self, ev=None):
         if ev is not None:
             ev[0].record(self.stream)
-        self.attn.qkv(self.x, self.wt, self.bias, self.w.txt_len, self.w.img_h, self.w.img_w, self.w.ref_h,
-                      self.w.ref_w, self.wq, self.wk, qn=self.qn, kn=self.kn, v=self.v)
+        geo = (self.w.txt_len, self.w.img_h, self.w.img_w, self.w.ref_h, self.w.ref_w)
+        if self.fp8:
+            fa.flux_attn_qkv_fp8(self.attn.handle, self.x, self.wt, self.bias, self.x.shape[-1], *geo, None, self.wq,
+                                 self.wk, self.q8, self.k8, self.v8t, self.scales)
+        else:
+            self.attn.qkv(self.x, self.wt, self.bias, *geo, self.wq, self.wk, qn=self.qn, kn=self.kn, v=self.v)
         if ev is not None:
             for e in ev[1:]:
                 e.record(self.stream)
@@ -373,10 +406,19 @@ def run_ours(args):
         peak = peak_bf16 * (2.0 if step.fp8 else 1.0)
         nominal = NOMINAL_TFLOPS["fp8" if step.fp8 else "bf16"]
         achieved = w.flops / (a_ms * 1e-3) / 1e12
-        return {"workload": w.name, "precision": w.precision, "batch": w.batch, "heads": w.heads,
+        extra = {}
+        if step.sol:
+            processed, kept = step.processed_fraction()
+            # dense-equivalent rate as "attn_tflops"; the roofline counts the work done
+            extra = {"sol_tau": w.sol_tau, "kept_block_fraction": kept, "processed_fraction": processed,
+                     "attn_tflops_processed": achieved * processed}
+            achieved_roof = achieved * processed
+        else:
+            achieved_roof = achieved
+        return {**extra, "workload": w.name, "precision": w.precision, "batch": w.batch, "heads": w.heads,
                 "tokens": w.tokens, "steps": n_steps, "value": job_throughput(w.flops, world, s_ms),
                 "ms_per_step": s_ms, "attn_kernel_ms": a_ms, "attn_tflops": achieved,
-                "roofline_frac": achieved / peak, "peak_tflops": peak,
+                "roofline_frac": achieved_roof / peak, "peak_tflops": peak,
                 "frac_of_nominal": achieved / nominal, "nominal_tflops": nominal,
                 "prologue_ms": p_ms, "prologue_gbs": step.prologue_bytes / (p_ms * 1e-3) / 1e9,
                 "prologue_frac": step.prologue_bytes / (p_ms * 1e-3) / 1e9 / hbm,
@@ -397,7 +439,7 @@ def run_ours(args):
                        for st in others]
         sus = []
         if args.sustained_seconds > 0:
-            for st in [main_step] + [o for o in others if o.w.precision == "bf16"]:
+            for st in [main_step] + [o for o in others if o.w.precision == "bf16" and not o.sol]:
                 ms_s, reps_s, clk_s = sustained(st, args.sustained_seconds, torch, clocks)
                 sus.append((st, ms_s, reps_s, clk_s))
         qkv_steps = [] if args.no_secondary else [QKVStep(synthetic.WORKLOADS[n], torch, fa) for n in args.qkv]
@@ -417,10 +459,12 @@ def run_ours(args):
     for st, (s_ms, _, _) in zip(qkv_steps, qkv_times):
         # one call = the (cos, sin) table kernel + the GEMM; both are in the time
         tf = st.flops / (s_ms * 1e-3) / 1e12
-        qkv.append({"workload": st.w.name, "kernel": "qkv_gemm_kernel (+ rope_table_kernel)",
+        kern = "qkv_gemm_kernel (+ rope_table_kernel)" + (" + E4M3 codes (fp8_vt_kernel, fp8_codes_kernel)"
+                                                           if st.fp8 else "")
+        qkv.append({"workload": st.w.name, "precision": st.w.precision, "kernel": kern,
                     "gemm": [st.w.batch * st.w.tokens, 3 * st.w.heads * 128, st.w.heads * 128],
                     "ms": s_ms, "tflops": tf, "roofline_frac": tf / peak_bf16, "frac_of_2250_nominal": tf / NOMINAL_TFLOPS["bf16"],
-                    "algorithmic_flops": st.flops, "gpu_launches": 2 * args.steps2})
+                    "algorithmic_flops": st.flops, "gpu_launches": (4 if st.fp8 else 2) * args.steps2})
         st.attn.close()
 
     # end to end through the public API: pinned host inputs in, result back out, every step
@@ -613,7 +657,8 @@ def main():
                          "steady state (0 skips)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--reference-rows", type=int, default=2048)
-    ap.add_argument("--qkv", nargs="*", default=["flux_1024_4608", "flux_2048_16896"], choices=sorted(synthetic.WORKLOADS),
+    ap.add_argument("--qkv", nargs="*", default=["flux_1024_4608", "flux_2048_16896", "fp8_cfg_2048_16896"],
+                    choices=sorted(synthetic.WORKLOADS),
                     help="workloads whose QKV projection (fused QK-norm + RoPE epilogue) is measured")
     ap.add_argument("--no-secondary", action="store_true", help="measure the primary workload only")
     ap.add_argument("--no-cpu-baseline", action="store_true")

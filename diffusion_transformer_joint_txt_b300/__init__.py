@@ -79,6 +79,7 @@ def _load() -> ctypes.CDLL:
         "flux_attn_attend_sol": (I, [P, P, P, P, P, I, P, P]),
         "flux_attn_qkv": (I, [P, P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, P]),
         "flux_attn_forward_hidden": (I, [P, P, P, P, I, I, I, I, I, I, P, P, P, P, P]),
+        "flux_attn_qkv_fp8": (I, [P, P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, P, P]),
         "flux_attn_forward_noalloc": (I, [ctypes.POINTER(flux_attn_config), P, P, P, I, I, I, I, I, P, P, P, P,
                                           P, P]),
         "flux_attn_sync_status": (I, [P, P]),
@@ -221,6 +222,13 @@ def flux_attn_qkv(h, x, w_qkv, b_qkv, d_model, txt_len, img_h, img_w, ref_h, ref
     _check(_L().flux_attn_qkv(h, _ptr(x), _ptr(w_qkv), _ptr(b_qkv), d_model, txt_len, img_h, img_w, ref_h, ref_w,
                               _ptr(pos_ids), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(qn), _ptr(kn), _ptr(v),
                               _stream(stream)))
+
+
+def flux_attn_qkv_fp8(h, x, w_qkv, b_qkv, d_model, txt_len, img_h, img_w, ref_h, ref_w, pos_ids, q_norm_w,
+                      k_norm_w, q8, k8, v8t, scales, stream=None) -> None:
+    _check(_L().flux_attn_qkv_fp8(h, _ptr(x), _ptr(w_qkv), _ptr(b_qkv), d_model, txt_len, img_h, img_w, ref_h, ref_w,
+                                  _ptr(pos_ids), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(q8), _ptr(k8), _ptr(v8t),
+                                  _ptr(scales), _stream(stream)))
 
 
 def flux_attn_forward_hidden(h, x, w_qkv, b_qkv, d_model, txt_len, img_h, img_w, ref_h, ref_w, pos_ids,
@@ -405,6 +413,20 @@ class FluxAttention:
         flux_attn_qkv(self.handle, x, w_qkv, b_qkv, d_model, txt_len, img_h, img_w, ref_h, ref_w, pos_ids,
                       q_norm_w, k_norm_w, qn, kn, v, stream)
         return qn, kn, v
+
+    def qkv_fp8(self, x, w_qkv, b_qkv, txt_len: int, img_h: int, img_w: int, ref_h: int = 0, ref_w: int = 0,
+                q_norm_w=None, k_norm_w=None, pos_ids=None, stream=None):
+        """FP8 handles: the QKV projection (fused QK-norm + RoPE) to E4M3 codes;
+        returns (q8, k8, v8t, scales) as prologue_fp8 does."""
+        import torch
+        n = txt_len + img_h * img_w + ref_h * ref_w
+        B, H = self.batch, self.num_heads
+        new = lambda shape, dt: torch.empty(shape, dtype=dt, device=x.device)
+        q8, k8 = new((B, H, n, HEAD_DIM), torch.uint8), new((B, H, n, HEAD_DIM), torch.uint8)
+        v8t, scales = new((B, H, HEAD_DIM, pad16(n)), torch.uint8), new((B, H, 3), torch.float32)
+        flux_attn_qkv_fp8(self.handle, x, w_qkv, b_qkv, x.shape[-1], txt_len, img_h, img_w, ref_h, ref_w, pos_ids,
+                          q_norm_w, k_norm_w, q8, k8, v8t, scales, stream)
+        return q8, k8, v8t, scales
 
     def forward_hidden(self, x, w_qkv, b_qkv, txt_len: int, img_h: int, img_w: int, ref_h: int = 0, ref_w: int = 0,
                        q_norm_w=None, k_norm_w=None, pos_ids=None, out=None, stream=None):

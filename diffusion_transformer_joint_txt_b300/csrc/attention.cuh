@@ -60,11 +60,11 @@
 // come out in the units of the E4M3 blocks -- and then the FP8 blocks over
 // the N - R other keys (positions 0 .. N-R-1 of the codes).  The repair QK
 // needs Q in bf16: the softmax warps convert their rows of the E4M3 Q tile
-// (exact: every E4M3 value is a bf16 value) into the K ring's memory, and the
-// repair K and V tiles go to the V ring's memory; both rings are idle until
-// the repair blocks are done, which the MMA thread signals (qbf_free,
-// vrep_free) before the producers start on the FP8 tiles.  A repair block's P
-// is bf16 (as in the BF16 kernel); its row sum adds the fp32 p.
+// (exact: every E4M3 value is a bf16 value) into the V ring's memory, which
+// stays idle until the MMA thread signals the last repair QK (qbf_free); the
+// repair K and V tiles have their own 64 KB, which the E4M3 kernel has to
+// spare, so the K ring fills from the start.  A repair block's P is bf16 (as
+// in the BF16 kernel); its row sum adds the fp32 p.
 //
 // Sol-Attention (SOL, BF16; sol_sparse.cuh builds the lists): the CTA walks
 // only the key blocks in its list -- the union of the blocks its two query
@@ -118,6 +118,10 @@ struct __align__(1024) Smem {
   uint8_t q[TILES][TILE];
   uint8_t k[KST][TILE];
   uint8_t v[VST][TILE];
+  // FP8 only: the repair K and V tiles of VC-Attention (bf16, 32 KB each).  The
+  // E4M3 rings leave this much of the SM's shared memory unused anyway (one
+  // CTA per SM: TMEM holds one CTA's 512 columns).
+  uint8_t rep[FP8 ? 2 : 1][FP8 ? 2 * HALF : 16];
   uint64_t q_full[TILES];
   uint64_t k_full[KST], k_empty[KST];
   uint64_t v_full[VST], v_empty[VST];
@@ -125,7 +129,7 @@ struct __align__(1024) Smem {
   uint64_t qbf_full[TILES];            // REP: tile t's rows converted to bf16 (128 arrivals)
   uint64_t krep_full, krep_empty;      // REP: the repair K tile slot
   uint64_t vrep_full, vrep_empty;      // REP: the repair V tile slot
-  uint64_t qbf_free, vrep_free;        // REP: last repair QK / PV of both tiles done
+  uint64_t qbf_free;                   // REP: last repair QK of both tiles done
   uint64_t mma_drain;
   uint64_t never;  // nothing arrives here (forced-timeout debug path)
   uint32_t tmem_base;
@@ -181,20 +185,20 @@ __device__ __forceinline__ void drain_ring(uint64_t (&full)[ST], int issued, uin
   }
 }
 
-// REP shared memory: the two bf16 Q tiles in the K ring (32 KB each), the
-// repair K tile in the first and the repair V tile in the second 32 KB of the
-// V ring.
+// REP shared memory: the two bf16 Q tiles in the V ring (32 KB each, idle
+// until qbf_free), the repair K and V tiles in their own region, so that the
+// K ring fills from the start.
 template <bool FP8>
-__device__ __forceinline__ uint8_t* qbf_tile(Smem<FP8>& sm, int t) { return &sm.k[0][0] + t * 2 * HALF; }
+__device__ __forceinline__ uint8_t* qbf_tile(Smem<FP8>& sm, int t) { return &sm.v[0][0] + t * 2 * HALF; }
 template <bool FP8>
-__device__ __forceinline__ uint8_t* krep_tile(Smem<FP8>& sm) { return &sm.v[0][0]; }
+__device__ __forceinline__ uint8_t* krep_tile(Smem<FP8>& sm) { return &sm.rep[0][0]; }
 template <bool FP8>
-__device__ __forceinline__ uint8_t* vrep_tile(Smem<FP8>& sm) { return &sm.v[0][0] + 2 * HALF; }
+__device__ __forceinline__ uint8_t* vrep_tile(Smem<FP8>& sm) { return &sm.rep[FP8 ? 1 : 0][0]; }
 
 // K ring producer: K_j into stage j % KST once both tiles' QK of its
-// previous occupant have completed.  REP: first the repair K tiles, each once
-// both tiles' QK of the one before it has completed; the ring's memory holds
-// the bf16 Q tiles until qbf_free.
+// previous occupant have completed.  REP: the repair K tiles too (into their
+// own slot, each once both tiles' QK of the one before it has completed),
+// issued first.
 template <bool FP8, bool REP, bool SOL>
 __device__ __forceinline__ void load_k(Smem<FP8>& sm, const CUtensorMap* tk, const CUtensorMap* tkr, int bh,
                                        int nkv, int nrep, const uint16_t* lst, volatile int* ab, uint32_t* err) {
@@ -210,8 +214,10 @@ __device__ __forceinline__ void load_k(Smem<FP8>& sm, const CUtensorMap* tk, con
       load_rows<false>(smem_u32(krep_tile(sm)), tkr, &sm.krep_full, i * BN, bh);
       ++rep_issued;
     }
-    if (rep_issued > 0) mbar_drain(&sm.krep_full, (rep_issued - 1) & 1, err);
-    if (!ok || !mbar_wait(&sm.qbf_free, 0, ab, err)) return;
+    if (!ok) {
+      if (rep_issued > 0) mbar_drain(&sm.krep_full, (rep_issued - 1) & 1, err);
+      return;
+    }
     nkv -= nrep;
   }
   for (int j = 0; j < nkv; ++j) {
@@ -224,12 +230,14 @@ __device__ __forceinline__ void load_k(Smem<FP8>& sm, const CUtensorMap* tk, con
     ++issued;
   }
   drain_ring(sm.k_full, issued, err);
+  if (REP && nrep > 0) mbar_drain(&sm.krep_full, (nrep - 1) & 1, err);
 }
 
 // Q and V ring producer: both Q tiles once, then V_j into stage j % VST once
 // both tiles' PV of its previous occupant have completed.  REP: the repair V
-// tiles first (each once both tiles' PV of the one before it has completed),
-// and the ring only after vrep_free.
+// tiles first (into their own slot, each once both tiles' PV of the one
+// before it has completed), and the ring only after qbf_free (it holds the
+// bf16 Q tiles until the last repair QK).
 template <bool FP8, bool REP, bool SOL>
 __device__ __forceinline__ void load_qv(Smem<FP8>& sm, const CUtensorMap* tq, const CUtensorMap* tv,
                                         const CUtensorMap* tvr, int q0, int bh, int b, int h, int nkv, int nrep,
@@ -252,7 +260,7 @@ __device__ __forceinline__ void load_qv(Smem<FP8>& sm, const CUtensorMap* tq, co
       ++rep_issued;
     }
     if (rep_issued > 0) mbar_drain(&sm.vrep_full, (rep_issued - 1) & 1, err);
-    rep_ok = rep_ok && mbar_wait(&sm.vrep_free, 0, ab, err);
+    rep_ok = rep_ok && mbar_wait(&sm.qbf_free, 0, ab, err);
     nkv = rep_ok ? nkv - nrep : 0;
   }
   for (int j = 0; j < nkv; ++j) {
@@ -328,8 +336,8 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint6
 
 // REP: the repair blocks, issued before the main loop -- per block QK_0 QK_1
 // (bf16, Q from the converted tiles, K from the repair slot), then PV_0 PV_1
-// once each tile's P is in.  Commits qbf_free after the last repair QK and
-// vrep_free after the last repair PV.  Returns false when a wait gave up.
+// once each tile's P is in.  Commits qbf_free after the last repair QK.
+// Returns false when a wait gave up.
 template <bool FP8>
 __device__ __forceinline__ bool mma_repair(Smem<FP8>& sm, uint32_t tmem, int nrep, volatile int* ab, uint32_t* err) {
   uint64_t qbd[TILES];
@@ -356,7 +364,6 @@ __device__ __forceinline__ bool mma_repair(Smem<FP8>& sm, uint32_t tmem, int nre
       issue_pv<false>(tmem + col_o(t), tmem + col_s(t), vrd, i > 0);
     }
     mma_commit(&sm.vrep_empty);
-    if (i == nrep - 1) mma_commit(&sm.vrep_free);
   }
   return true;
 }
@@ -719,7 +726,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(&sm.vrep_full, 1);
     mbar_init(&sm.vrep_empty, 1);
     mbar_init(&sm.qbf_free, 1);
-    mbar_init(&sm.vrep_free, 1);
     mbar_init(&sm.mma_drain, 1);
     mbar_init(&sm.never, 1);
     sm.abort = 0;

@@ -206,6 +206,28 @@ int repair_count(const flux_attn* h, int n) {
 // V transposed, then the E4M3 codes of Q', K' and the scales (last, so that
 // the kernel before the attention is the one-wave stream kernel that lets it
 // start early).
+// V bf16 [B, n, H, 128] in TMA tiles of 64 tokens x 128 dims of one head (for
+// its amax and codes), and V^T E4M3 [B*H, 128, pad16(n)] out in tiles of 64 keys.
+int encode_v_maps(flux_attn* h, const void* v, void* v8t, int n, CUtensorMap* tv, CUtensorMap* tvt) {
+  const int B = h->cfg.batch, H = h->cfg.num_heads;
+  {
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(flux::kHeadDim), static_cast<cuuint64_t>(H),
+                                static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(B)};
+    const cuuint64_t strides[3] = {flux::kHeadDim * 2ull, static_cast<cuuint64_t>(H) * flux::kHeadDim * 2ull,
+                                   static_cast<cuuint64_t>(n) * H * flux::kHeadDim * 2ull};
+    const cuuint32_t box[4] = {flux::kHeadDim, 1, flux::kVtTokens, 1};
+    int rc = encode_tiled(tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, v, dims, strides, box, "V (tiles)",
+                          CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (rc) return rc;
+  }
+  const cuuint64_t np = pad16(n);
+  const cuuint64_t dims[3] = {np, static_cast<cuuint64_t>(flux::kHeadDim), static_cast<cuuint64_t>(B) * H};
+  const cuuint64_t strides[2] = {np, np * flux::kHeadDim};
+  const cuuint32_t box[3] = {flux::kVtTokens, flux::kHeadDim, 1};
+  return encode_tiled(tvt, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, v8t, dims, strides, box, "V^T (tiles)",
+                      CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 // With VC-Attention (repair count R > 0) the quantisers also write the
 // per-token K' and V errors, and two more kernels select the repaired tokens
 // (sel) and move them out of the codes, writing their exact rows (krep, vrep).
@@ -219,27 +241,9 @@ int launch_prologue_fp8(flux_attn* h, const void* q, const void* k, const void* 
   const size_t amax_bytes = static_cast<size_t>(B) * H * 3 * sizeof(uint32_t);
   cudaError_t e = cudaMemsetAsync(h->amax, 0, amax_bytes, stream);
   if (e != cudaSuccess) return cuda_fail(e, "clearing amax");
-  // V: TMA tiles of 64 tokens x 128 dims of one head, in (amax, V^T) and out (V^T)
   CUtensorMap tv, tvt;
-  {
-    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(flux::kHeadDim), static_cast<cuuint64_t>(H),
-                                static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(B)};
-    const cuuint64_t strides[3] = {flux::kHeadDim * 2ull, static_cast<cuuint64_t>(H) * flux::kHeadDim * 2ull,
-                                   static_cast<cuuint64_t>(n) * H * flux::kHeadDim * 2ull};
-    const cuuint32_t box[4] = {flux::kHeadDim, 1, flux::kVtTokens, 1};
-    int rc = encode_tiled(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, v, dims, strides, box, "V (tiles)",
-                          CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (rc) return rc;
-  }
-  {
-    const cuuint64_t np = pad16(n);
-    const cuuint64_t dims[3] = {np, static_cast<cuuint64_t>(flux::kHeadDim), static_cast<cuuint64_t>(B) * H};
-    const cuuint64_t strides[2] = {np, np * flux::kHeadDim};
-    const cuuint32_t box[3] = {flux::kVtTokens, flux::kHeadDim, 1};
-    int rc = encode_tiled(&tvt, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, v8t, dims, strides, box, "V^T (tiles)",
-                          CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (rc) return rc;
-  }
+  int rc0 = encode_v_maps(h, v, v8t, n, &tv, &tvt);
+  if (rc0) return rc0;
   const dim3 vgrid((n + flux::kVtTokens - 1) / flux::kVtTokens, B * H);
   flux::fp8_vamax_kernel<<<vgrid, flux::kVtThreads, 0, stream>>>(tv, H, h->amax, h->err);
   e = cudaGetLastError();
@@ -274,7 +278,8 @@ int launch_prologue_fp8(flux_attn* h, const void* q, const void* k, const void* 
   if (R == 0) return FLUX_ATTN_OK;
   {
     NvtxRange vc_range("flux_attn/vc_repair");
-    flux::vc::vc_select_kernel<<<B * H, flux::vc::kSelectThreads, 0, stream>>>(h->errk, h->errv, n, R, sel);
+    const size_t sel_smem = n <= flux::vc::kSelectSmemKeys ? static_cast<size_t>(n) * sizeof(uint32_t) : 0;
+    flux::vc::vc_select_kernel<<<B * H, flux::vc::kSelectThreads, sel_smem, stream>>>(h->errk, h->errv, n, R, sel);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "repair selection launch");
     const flux::vc::RepairArgs ra{static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), wk,
@@ -420,9 +425,10 @@ int launch_sol_attention(flux_attn* h, const void* qn, const void* kn, const voi
 
 // The QKV projection with its fused epilogue: the (cos, sin) table of the
 // call's tokens, then the persistent GEMM.
+// amax: FP8, the per-(b, h) maxima of the written Q', K', V ([B*H][3], zero on entry); nullptr for BF16.
 int launch_qkv(flux_attn* h, const void* x, const void* w, const float* bias, int d_model, int txt, int ih, int iw,
                int rw, const int32_t* pos, const float* wq, const float* wk, void* qn, void* kn, void* v, int n,
-               cudaStream_t stream) {
+               cudaStream_t stream, uint32_t* amax = nullptr) {
   NvtxRange range("flux_attn/qkv_gemm");
   using namespace flux::qkv;
   const int B = h->cfg.batch, H = h->cfg.num_heads;
@@ -458,6 +464,7 @@ int launch_qkv(flux_attn* h, const void* x, const void* w, const float* bias, in
   p.kn = static_cast<__nv_bfloat16*>(kn);
   p.v = static_cast<__nv_bfloat16*>(v);
   p.err = h->err;
+  p.amax = amax;
   p.M = M;
   p.N = n;
   p.H = H;
@@ -497,6 +504,9 @@ cudaError_t set_attention_smem_limits() {
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(flux::qk_norm_rope_kernel<flux::E4m3Rows>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            flux::kProSmemBytes);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(flux::vc::vc_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(flux::vc::kSelectSmemKeys * sizeof(uint32_t)));
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(flux::qkv::qkv_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(flux::qkv::SMEM_BYTES));
@@ -597,23 +607,26 @@ int flux_attn_create(const flux_attn_config* cfg, flux_attn_t* out) {
       }
   }
   // Workspace, each piece 256-byte aligned:
-  //   BF16  Q', K' bf16 [B, H, max_tokens, 128]
+  //   both  Q', K' bf16 [B, H, max_tokens, 128], V bf16 [B, max_tokens, H, 128] and the
+  //         (cos, sin) table of the QKV projection (FP8: its bf16 outputs before the codes)
   //   FP8   Q', K' E4M3 [B, H, max_tokens, 128], V^T E4M3 [B, H, 128, pad16(max_tokens)],
   //         amax and scales [B, H, 3]
-  //   both  the device error word
+  //   VC / SOL  their buffers (below); the device error word
   const size_t bh = static_cast<size_t>(cfg->batch) * cfg->num_heads;
   const bool fp8 = cfg->precision == FLUX_ATTN_FP8_E4M3;
   const auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
-  const size_t qk_bytes = al(bh * cfg->max_tokens * flux::kHeadDim * (fp8 ? 1 : 2));
+  const size_t qk_bytes = al(bh * cfg->max_tokens * flux::kHeadDim * 2);
+  const size_t q8_bytes = fp8 ? al(bh * cfg->max_tokens * flux::kHeadDim) : 0;
   const size_t vt_bytes = fp8 ? al(bh * flux::kHeadDim * pad16(cfg->max_tokens)) : 0;
   const size_t sc_bytes = fp8 ? al(bh * 3 * sizeof(float)) : 0;
-  const size_t rope_bytes = fp8 ? 0 : al(static_cast<size_t>(cfg->max_tokens) * (flux::kHeadDim / 2) * sizeof(float2));
-  const size_t v_bytes = fp8 ? 0 : qk_bytes;
+  const size_t rope_bytes = al(static_cast<size_t>(cfg->max_tokens) * (flux::kHeadDim / 2) * sizeof(float2));
+  const size_t v_bytes = qk_bytes;
   h->r_max = repair_count(h, cfg->max_tokens);
   const size_t vc_err_bytes = h->r_max > 0 ? al(bh * cfg->max_tokens * sizeof(float)) : 0;
   const size_t vc_sel_bytes = h->r_max > 0 ? al(bh * h->r_max * sizeof(int32_t)) : 0;
   const size_t vc_row_bytes = h->r_max > 0 ? al(bh * h->r_max * flux::kHeadDim * 2) : 0;
-  const size_t vc_off = 2 * qk_bytes + vt_bytes + 2 * sc_bytes + rope_bytes + v_bytes;
+  const size_t f8_off = 2 * qk_bytes + rope_bytes + v_bytes;
+  const size_t vc_off = f8_off + 2 * q8_bytes + vt_bytes + 2 * sc_bytes;
   const bool sol = cfg->sol_tau > 0.f;
   const size_t nb_max = (static_cast<size_t>(cfg->max_tokens) + 127) / 128;
   const size_t ncta_max = (static_cast<size_t>(cfg->max_tokens) + 255) / 256;
@@ -632,17 +645,16 @@ int flux_attn_create(const flux_attn_config* cfg, flux_attn_t* out) {
     return fail(FLUX_ATTN_ERR_OOM, "cudaMalloc(%zu) failed: %s", want, cudaGetErrorString(e));
   }
   uint8_t* base = static_cast<uint8_t*>(h->ws);
+  h->qn = reinterpret_cast<__nv_bfloat16*>(base);
+  h->kn = reinterpret_cast<__nv_bfloat16*>(base + qk_bytes);
+  h->rope = reinterpret_cast<float2*>(base + 2 * qk_bytes);
+  h->vw = reinterpret_cast<__nv_bfloat16*>(base + 2 * qk_bytes + rope_bytes);
   if (fp8) {
-    h->q8 = base;
-    h->k8 = base + qk_bytes;
-    h->v8t = base + 2 * qk_bytes;
-    h->amax = reinterpret_cast<uint32_t*>(base + 2 * qk_bytes + vt_bytes);
-    h->scales = reinterpret_cast<float*>(base + 2 * qk_bytes + vt_bytes + sc_bytes);
-  } else {
-    h->qn = reinterpret_cast<__nv_bfloat16*>(base);
-    h->kn = reinterpret_cast<__nv_bfloat16*>(base + qk_bytes);
-    h->rope = reinterpret_cast<float2*>(base + 2 * qk_bytes);
-    h->vw = reinterpret_cast<__nv_bfloat16*>(base + 2 * qk_bytes + rope_bytes);
+    h->q8 = base + f8_off;
+    h->k8 = base + f8_off + q8_bytes;
+    h->v8t = base + f8_off + 2 * q8_bytes;
+    h->amax = reinterpret_cast<uint32_t*>(base + f8_off + 2 * q8_bytes + vt_bytes);
+    h->scales = reinterpret_cast<float*>(base + f8_off + 2 * q8_bytes + vt_bytes + sc_bytes);
   }
   if (h->r_max > 0) {
     h->errk = reinterpret_cast<float*>(base + vc_off);
@@ -947,6 +959,83 @@ int flux_attn_forward_sol(flux_attn_t h, const void* q, const void* k, const voi
   return launch_sol_attention(h, h->qn, h->kn, v, h->keep, n, out, stream);
 }
 
+// Arguments of the QKV projection shared by its BF16 and FP8 entry points.
+static int qkv_common(flux_attn* h, const void* x, const void* w_qkv, const float* b_qkv, int d_model, int txt_len,
+                      int img_h, int img_w, int ref_h, int ref_w, const int32_t* pos_ids, const float* q_norm_w,
+                      const float* k_norm_w, int* n_out) {
+  int rc = 0;
+  if (d_model < flux::qkv::BK || d_model % flux::qkv::BK || d_model > (1 << 16))
+    return fail(FLUX_ATTN_ERR_UNSUPPORTED, "d_model = %d must be a multiple of %d in [%d, 65536]", d_model,
+                flux::qkv::BK, flux::qkv::BK);
+  int n = 0;
+  if ((rc = token_count(h, txt_len, img_h, img_w, ref_h, ref_w, &n))) return rc;
+  *n_out = n;
+  if (n == 0) return FLUX_ATTN_OK;
+  const size_t M = static_cast<size_t>(h->cfg.batch) * n;
+  const size_t F = 3ull * h->cfg.num_heads * flux::kHeadDim;
+  if ((rc = check_buffer(x, M * d_model * 2, "x"))) return rc;
+  if ((rc = check_buffer(w_qkv, F * d_model * 2, "w_qkv"))) return rc;
+  if (b_qkv != nullptr && (rc = check_buffer(b_qkv, F * sizeof(float), "b_qkv"))) return rc;
+  if ((rc = check_buffer(q_norm_w, flux::kHeadDim * sizeof(float), "q_norm_w"))) return rc;
+  if ((rc = check_buffer(k_norm_w, flux::kHeadDim * sizeof(float), "k_norm_w"))) return rc;
+  if (pos_ids != nullptr && (rc = check_buffer(pos_ids, static_cast<size_t>(n) * 3 * sizeof(int32_t), "pos_ids")))
+    return rc;
+  return FLUX_ATTN_OK;
+}
+
+// The FP8 QKV projection into q8, k8, v8t, scales: the GEMM writes bf16 Q', K',
+// V to the workspace and reduces their per-(b, h) amax, then the codes.
+static int launch_qkv_fp8(flux_attn* h, const void* x, const void* w_qkv, const float* b_qkv, int d_model,
+                          int txt_len, int img_h, int img_w, int ref_w, const int32_t* pos_ids, const float* q_norm_w,
+                          const float* k_norm_w, int n, uint8_t* q8, uint8_t* k8, uint8_t* v8t, float* scales,
+                          cudaStream_t stream) {
+  const int B = h->cfg.batch, H = h->cfg.num_heads;
+  cudaError_t e = cudaMemsetAsync(h->amax, 0, static_cast<size_t>(B) * H * 3 * sizeof(uint32_t), stream);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing amax");
+  int rc = launch_qkv(h, x, w_qkv, b_qkv, d_model, txt_len, img_h, img_w, ref_w, pos_ids, q_norm_w, k_norm_w, h->qn,
+                      h->kn, h->vw, n, stream, h->amax);
+  if (rc) return rc;
+  NvtxRange range("flux_attn/fp8_codes");
+  CUtensorMap tv, tvt;
+  if ((rc = encode_v_maps(h, h->vw, v8t, n, &tv, &tvt))) return rc;
+  const dim3 vgrid((n + flux::kVtTokens - 1) / flux::kVtTokens, B * H);
+  flux::fp8_vt_kernel<<<vgrid, flux::kVtThreads, 0, stream>>>(tv, tvt, H, h->amax, h->err, nullptr, n);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "V^T launch");
+  const size_t items = 2ull * B * H * n * flux::kHeadDim / 16;
+  const unsigned grid = static_cast<unsigned>(
+      std::min<size_t>((items + flux::kCodesThreads - 1) / flux::kCodesThreads, 8ull * h->num_sms));
+  flux::fp8_codes_kernel<<<grid, flux::kCodesThreads, 0, stream>>>(h->qn, h->kn, n, B * H, h->amax, q8, k8, scales);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "codes launch");
+  return FLUX_ATTN_OK;
+}
+
+int flux_attn_qkv_fp8(flux_attn_t h, const void* x, const void* w_qkv, const float* b_qkv, int d_model, int txt_len,
+                      int img_h, int img_w, int ref_h, int ref_w, const int32_t* pos_ids, const float* q_norm_w,
+                      const float* k_norm_w, void* q8, void* k8, void* v8t, float* scales, cudaStream_t stream) {
+  g_last_error.clear();
+  NvtxRange range("flux_attn_qkv_fp8");
+  int rc = check_handle(h);
+  if (rc) return rc;
+  if (h->cfg.precision != FLUX_ATTN_FP8_E4M3)
+    return fail(FLUX_ATTN_ERR_INVALID_ARG, "flux_attn_qkv_fp8 needs an FP8 handle");
+  if (h->cfg.vc_repair_budget > 0.f)
+    return fail(FLUX_ATTN_ERR_UNSUPPORTED, "the QKV projection has no VC-Attention repair");
+  int n = 0;
+  if ((rc = qkv_common(h, x, w_qkv, b_qkv, d_model, txt_len, img_h, img_w, ref_h, ref_w, pos_ids, q_norm_w,
+                       k_norm_w, &n)) || n == 0)
+    return rc;
+  const size_t bh = static_cast<size_t>(h->cfg.batch) * h->cfg.num_heads;
+  if ((rc = check_buffer(q8, bh * n * flux::kHeadDim, "q8"))) return rc;
+  if ((rc = check_buffer(k8, bh * n * flux::kHeadDim, "k8"))) return rc;
+  if ((rc = check_buffer(v8t, bh * flux::kHeadDim * pad16(n), "v8t"))) return rc;
+  if ((rc = check_buffer(scales, bh * 3 * sizeof(float), "scales"))) return rc;
+  return launch_qkv_fp8(h, x, w_qkv, b_qkv, d_model, txt_len, img_h, img_w, ref_w, pos_ids, q_norm_w, k_norm_w, n,
+                        static_cast<uint8_t*>(q8), static_cast<uint8_t*>(k8), static_cast<uint8_t*>(v8t), scales,
+                        stream);
+}
+
 int flux_attn_qkv(flux_attn_t h, const void* x, const void* w_qkv, const float* b_qkv, int d_model, int txt_len,
                   int img_h, int img_w, int ref_h, int ref_w, const int32_t* pos_ids, const float* q_norm_w,
                   const float* k_norm_w, void* qn, void* kn, void* v, cudaStream_t stream) {
@@ -954,7 +1043,8 @@ int flux_attn_qkv(flux_attn_t h, const void* x, const void* w_qkv, const float* 
   NvtxRange range("flux_attn_qkv");
   int rc = check_handle(h);
   if (rc) return rc;
-  if (h->cfg.precision != FLUX_ATTN_BF16) return fail(FLUX_ATTN_ERR_UNSUPPORTED, "flux_attn_qkv needs a BF16 handle");
+  if (h->cfg.precision != FLUX_ATTN_BF16)
+    return fail(FLUX_ATTN_ERR_UNSUPPORTED, "flux_attn_qkv needs a BF16 handle (FP8: flux_attn_qkv_fp8)");
   if (d_model < flux::qkv::BK || d_model % flux::qkv::BK || d_model > (1 << 16))
     return fail(FLUX_ATTN_ERR_UNSUPPORTED, "d_model = %d must be a multiple of %d in [%d, 65536]", d_model,
                 flux::qkv::BK, flux::qkv::BK);
@@ -987,13 +1077,22 @@ int flux_attn_forward_hidden(flux_attn_t h, const void* x, const void* w_qkv, co
   NvtxRange range("flux_attn_forward_hidden");
   int rc = check_handle(h);
   if (rc) return rc;
-  if (h->cfg.precision != FLUX_ATTN_BF16)
-    return fail(FLUX_ATTN_ERR_UNSUPPORTED, "flux_attn_forward_hidden needs a BF16 handle");
+  if (h->cfg.precision == FLUX_ATTN_FP8_E4M3 && h->cfg.vc_repair_budget > 0.f)
+    return fail(FLUX_ATTN_ERR_UNSUPPORTED, "the QKV projection has no VC-Attention repair");
   int n = 0;
   if ((rc = token_count(h, txt_len, img_h, img_w, ref_h, ref_w, &n))) return rc;
   if (n == 0) return FLUX_ATTN_OK;
   if ((rc = check_buffer(out, row_bytes(h, n), "out"))) return rc;
   if (out == x) return fail(FLUX_ATTN_ERR_INVALID_ARG, "out aliases x");
+  if (h->cfg.precision == FLUX_ATTN_FP8_E4M3) {
+    if ((rc = qkv_common(h, x, w_qkv, b_qkv, d_model, txt_len, img_h, img_w, ref_h, ref_w, pos_ids, q_norm_w,
+                         k_norm_w, &n)))
+      return rc;
+    rc = launch_qkv_fp8(h, x, w_qkv, b_qkv, d_model, txt_len, img_h, img_w, ref_w, pos_ids, q_norm_w, k_norm_w, n,
+                        h->q8, h->k8, h->v8t, h->scales, stream);
+    if (rc) return rc;
+    return launch_attention(h, true, h->q8, h->k8, h->v8t, h->scales, n, out, stream);
+  }
   // the projection's own checks, with the handle's workspace as its outputs
   rc = flux_attn_qkv(h, x, w_qkv, b_qkv, d_model, txt_len, img_h, img_w, ref_h, ref_w, pos_ids, q_norm_w, k_norm_w,
                      h->qn, h->kn, h->vw, stream);

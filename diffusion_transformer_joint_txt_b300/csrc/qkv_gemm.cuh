@@ -64,6 +64,8 @@ struct Params {
   __nv_bfloat16* kn;        // [B, H, N, 128]
   __nv_bfloat16* v;         // [B, N, H, 128]
   uint32_t* err;
+  uint32_t* amax;           // FP8: per-(b, h) |max| of the written Q', K', V, fp32 bits [B*H][3]
+                            // (must be zero on entry); nullptr for BF16
   int M, N, H, D;           // tokens B*N, tokens per batch row, heads, hidden size
   int m_tiles, n_tiles;
   int group_m;              // token tiles per group of the tile order
@@ -192,9 +194,15 @@ __device__ __forceinline__ void mma_issuer(Smem& sm, uint32_t tmem, const Params
   wait_drain(&sm.drain, 0, p.err);
 }
 
+// |max| of the bf16 pairs in w, accumulated in m (two bf16 halves; non-negative
+// bf16 values order like their bit patterns).
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t m, uint32_t w) { return __vmaxu2(m, w & 0x7FFF7FFFu); }
+
 // One head (128 columns) of row r: bias, then for Q and K the RMSNorm with
 // its weight and the rotation, then bf16 stores of the 256-byte row.
-__device__ __forceinline__ void epilogue_head(const Params& p, uint32_t taddr, int col0, int m) {
+// Returns the row's |max| of the values written (fp32 bits; 0 past the last
+// row), for the FP8 path's per-head scales.
+__device__ __forceinline__ uint32_t epilogue_head(const Params& p, uint32_t taddr, int col0, int m) {
   uint32_t y[128];
   tmem_ld128(taddr, y);
   tmem_ld_wait(y);
@@ -212,18 +220,23 @@ __device__ __forceinline__ void epilogue_head(const Params& p, uint32_t taddr, i
       y[4 * i + 3] = __float_as_uint(__uint_as_float(y[4 * i + 3]) + bb.w);
     }
   }
-  if (m >= p.M) return;
+  if (m >= p.M) return 0u;
   const int b = m / p.N;
   const int n = m - b * p.N;
+  uint32_t mx = 0u;
   if (part == 2) {
     uint4* dst = reinterpret_cast<uint4*>(p.v + ((static_cast<size_t>(b) * p.N + n) * p.H + h) * kHeadDim);
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
-      dst[i] = make_uint4(pack_bf16x2(__uint_as_float(y[8 * i]), __uint_as_float(y[8 * i + 1])),
-                          pack_bf16x2(__uint_as_float(y[8 * i + 2]), __uint_as_float(y[8 * i + 3])),
-                          pack_bf16x2(__uint_as_float(y[8 * i + 4]), __uint_as_float(y[8 * i + 5])),
-                          pack_bf16x2(__uint_as_float(y[8 * i + 6]), __uint_as_float(y[8 * i + 7])));
-    return;
+    for (int i = 0; i < 16; ++i) {
+      const uint4 u = make_uint4(pack_bf16x2(__uint_as_float(y[8 * i]), __uint_as_float(y[8 * i + 1])),
+                                 pack_bf16x2(__uint_as_float(y[8 * i + 2]), __uint_as_float(y[8 * i + 3])),
+                                 pack_bf16x2(__uint_as_float(y[8 * i + 4]), __uint_as_float(y[8 * i + 5])),
+                                 pack_bf16x2(__uint_as_float(y[8 * i + 6]), __uint_as_float(y[8 * i + 7])));
+      dst[i] = u;
+      if (p.amax != nullptr)
+        mx = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(mx, u.x), u.y), u.z), u.w);
+    }
+    return max(mx & 0xFFFFu, mx >> 16) << 16;
   }
   float ss = 0.f;
 #pragma unroll
@@ -249,7 +262,10 @@ __device__ __forceinline__ void epilogue_head(const Params& p, uint32_t taddr, i
       o[e] = pack_bf16x2(y0 * cv[e] - y1 * sv[e], y0 * sv[e] + y1 * cv[e]);
     }
     reinterpret_cast<uint4*>(out)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    if (p.amax != nullptr)
+      mx = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(mx, o[0]), o[1]), o[2]), o[3]);
   }
+  return max(mx & 0xFFFFu, mx >> 16) << 16;
 }
 
 __device__ __forceinline__ void epilogue(Smem& sm, uint32_t tmem, const Params& p, volatile int* ab) {
@@ -268,8 +284,24 @@ __device__ __forceinline__ void epilogue(Smem& sm, uint32_t tmem, const Params& 
 #pragma unroll 1
     for (int hs = 0; hs < BN / kHeadDim; ++hs) {
       const int col0 = n0 + hs * kHeadDim;
-      if (col0 < Nout)
-        epilogue_head(p, tmem + (static_cast<uint32_t>(q4 * 32) << 16) + buf * BN + hs * kHeadDim, col0, m0 + r);
+      if (col0 >= Nout) continue;  // tile-uniform
+      const uint32_t am =
+          epilogue_head(p, tmem + (static_cast<uint32_t>(q4 * 32) << 16) + buf * BN + hs * kHeadDim, col0, m0 + r);
+      if (p.amax != nullptr) {
+        // per-(b, h) amax: one atomic per warp when its 32 rows share a batch row
+        const int F = p.H * kHeadDim;
+        const int part = col0 / F, h = (col0 - part * F) / kHeadDim;
+        const int b = min(m0 + r, p.M - 1) / p.N;
+        const int b0 = __shfl_sync(0xFFFFFFFFu, b, 0);
+        if (__all_sync(0xFFFFFFFFu, b == b0)) {
+          uint32_t w = am;
+#pragma unroll
+          for (int off = 16; off >= 1; off >>= 1) w = max(w, __shfl_xor_sync(0xFFFFFFFFu, w, off));
+          if ((threadIdx.x & 31) == 0 && w != 0u) atomicMax(p.amax + (static_cast<size_t>(b0) * p.H + h) * 3 + part, w);
+        } else if (am != 0u) {
+          atomicMax(p.amax + (static_cast<size_t>(b) * p.H + h) * 3 + part, am);
+        }
+      }
     }
     tc_fence_before_sync();
     mbar_arrive(&sm.acc_empty[buf]);

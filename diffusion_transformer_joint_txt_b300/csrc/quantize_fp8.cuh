@@ -322,4 +322,36 @@ __global__ void __launch_bounds__(kVtThreads)
   }
 }
 
+// E4M3 codes of bf16 Q', K' (head-major [B*H][N][128], as the QKV projection
+// writes them) with the per-(b, h) scales of amax ([B*H][3], complete); each
+// thread step turns 16 values (two 16-byte loads) into one 16-byte store.
+// Block 0 also writes the three scales of every head.
+constexpr int kCodesThreads = 256;
+
+__global__ void __launch_bounds__(kCodesThreads)
+    fp8_codes_kernel(const __nv_bfloat16* __restrict__ qn, const __nv_bfloat16* __restrict__ kn, int N, int BH,
+                     const uint32_t* __restrict__ amax, uint8_t* __restrict__ q8, uint8_t* __restrict__ k8,
+                     float* __restrict__ scales) {
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < 3 * BH; i += blockDim.x) {
+      const float a = __uint_as_float(amax[i]);
+      scales[i] = a > 0.f ? a / kE4M3Max : 1.f;
+    }
+  const size_t per_head = static_cast<size_t>(N) * kHeadDim / 16;  // 16-value items of one head
+  const size_t items = 2 * static_cast<size_t>(BH) * per_head;
+  for (size_t it = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; it < items;
+       it += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const int t = it >= static_cast<size_t>(BH) * per_head;  // 0: Q', 1: K'
+    const size_t j = it - t * static_cast<size_t>(BH) * per_head;
+    const int bh = static_cast<int>(j / per_head);
+    const float inv = inv_scale_of(__ldg(amax + 3 * bh + t));
+    const uint4* src = reinterpret_cast<const uint4*>(t == 0 ? qn : kn) + 2 * j;
+    float x[8], y[8];
+    unpack8(__ldg(src), x);
+    unpack8(__ldg(src + 1), y);
+    const uint2 a = quant8(x, inv), c = quant8(y, inv);
+    reinterpret_cast<uint4*>(t == 0 ? q8 : k8)[j] = make_uint4(a.x, a.y, c.x, c.y);
+  }
+}
+
 }  // namespace flux

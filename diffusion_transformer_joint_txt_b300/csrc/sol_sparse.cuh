@@ -3,8 +3,8 @@
 //
 // "Speed up image generation with FLUX 3 Image Klein on NVIDIA Blackwell
 // GPUs", section "Quantized and sparse attention": Sol-Attention (algorithm
-// sol_attn, tau 1.0, disabled_until_timestep 0.96) runs the attention through
-// a general block-sparse kernel.  Reading taken here (the page gives no
+// sol_attn, tau 1.0, disabled_until_timestep 0.96) skips blocks of the
+// attention with a block-sparse kernel.  Reading taken here (the page gives no
 // formula): per (b, h), queries and keys are cut into blocks of 128 tokens
 // (the last one ragged); the pooled vector of a block is the mean of its
 // normalised, rotated rows; query block i gives key block j the mass

@@ -3,9 +3,9 @@
 //
 // "Speed up image generation with FLUX 3 Image Klein on NVIDIA Blackwell
 // GPUs", section "Quantized and sparse attention": VC-Attention FP8 takes a
-// repair budget (vc_repair_budget, 0.005 in the page's configuration) that
-// selects the fraction of tokens with the highest quantisation error for a
-// residual correction.  Reading taken here (the page gives no formula): key
+// repair budget (vc_repair_budget, 0.005 in the page's configuration): up to
+// that share of the tokens, the worst quantised ones, get their quantisation
+// residual corrected.  Reading taken here (the page gives no formula): key
 // token m of head (b, h) has the error
 //     e_m = |k'_m - deq(k'_m)|^2 + |v_m - deq(v_m)|^2
 // (written by the E4M3 quantisers as two arrays, errk and errv), the
@@ -37,6 +37,7 @@ namespace vc {
 
 constexpr int kSelectThreads = 1024;
 constexpr int kRepairThreads = 256;
+constexpr int kMoveChunk = 1024;  // fillers noted per round of the repair kernel
 
 // Exclusive prefix count of `flag` over the block's threads in thread order;
 // *total receives the block's count.  Uses `warp_tot` (32 entries) of shared
@@ -59,29 +60,72 @@ __device__ __forceinline__ uint32_t block_exclusive_count(bool flag, uint32_t* w
   return before + in_warp;
 }
 
+// Exclusive prefix sum of v over the block's threads in thread order (same
+// rules as block_exclusive_count).
+__device__ __forceinline__ uint32_t block_exclusive_sum(uint32_t v, uint32_t* warp_tot, uint32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) warp_tot[warp] = x;
+  __syncthreads();
+  uint32_t before = 0, all = 0;
+  const int warps = blockDim.x >> 5;
+  for (int w = 0; w < warps; ++w) {
+    const uint32_t c = warp_tot[w];
+    if (w < warp) before += c;
+    all += c;
+  }
+  __syncthreads();
+  *total = all;
+  return before + x - v;
+}
+
+// The selection's dynamic shared memory holds the error keys of up to this
+// many tokens; longer sequences read them from global memory.
+constexpr int kSelectSmemKeys = 48 * 1024;
+
 // Repair set of head blockIdx.x: the R tokens of largest errk + errv,
 // equal errors by lower index, written ascending to sel[blockIdx.x][0 .. R).
-// 1 <= R <= N.
+// 1 <= R <= N.  Dynamic shared memory: 4 N bytes when N <= kSelectSmemKeys
+// (the keys, staged once), else none.
 __global__ void __launch_bounds__(kSelectThreads)
     vc_select_kernel(const float* __restrict__ errk, const float* __restrict__ errv, int N, int R,
                      int32_t* __restrict__ sel) {
+  extern __shared__ uint32_t keys[];
   __shared__ uint32_t hist[256];
   __shared__ uint32_t warp_tot[32];
   __shared__ uint32_t s_prefix, s_rank;
+  const int lane = threadIdx.x & 31;
   const size_t base = static_cast<size_t>(blockIdx.x) * N;
   const float* ek = errk + base;
   const float* ev = errv + base;
-  auto key = [&](int m) { return __float_as_uint(ek[m] + ev[m]); };
+  const bool staged = N <= kSelectSmemKeys;
+  if (staged)
+    for (int m = threadIdx.x; m < N; m += blockDim.x) keys[m] = __float_as_uint(ek[m] + ev[m]);
+  __syncthreads();
+  auto key = [&](int m) { return staged ? keys[m] : __float_as_uint(ek[m] + ev[m]); };
   // Radix select, most significant byte first: the R-th largest key is
   // `prefix` once all four bytes are fixed; `rank` is its rank among the
-  // keys that share the bytes fixed so far (1 = largest).
+  // keys that share the bytes fixed so far (1 = largest).  Errors of one head
+  // share their top bytes, so the histogram adds are aggregated per warp.
   uint32_t prefix = 0, mask = 0, rank = static_cast<uint32_t>(R);
   for (int shift = 24; shift >= 0; shift -= 8) {
     for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
     __syncthreads();
-    for (int m = threadIdx.x; m < N; m += blockDim.x) {
-      const uint32_t u = key(m);
-      if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
+    for (int m0 = 0; m0 < N; m0 += blockDim.x) {  // warp-uniform trip count
+      const int m = m0 + threadIdx.x;
+      const uint32_t u = m < N ? key(m) : 0u;
+      const bool active = m < N && (u & mask) == prefix;
+      const uint32_t am = __ballot_sync(0xFFFFFFFFu, active);
+      if (active) {
+        const uint32_t bin = (u >> shift) & 255u;
+        const uint32_t peers = __match_any_sync(am, bin);
+        if (lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+      }
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -100,21 +144,28 @@ __global__ void __launch_bounds__(kSelectThreads)
     mask |= 255u << shift;
   }
   // Every key above the threshold, and the first `rank` keys equal to it in
-  // token order; chunks of blockDim tokens in order keep the output ascending.
-  uint32_t out = 0, eq_before = 0;
-  for (int c0 = 0; c0 < N; c0 += blockDim.x) {
-    const int m = c0 + threadIdx.x;
-    const uint32_t u = m < N ? key(m) : 0u;
-    const bool gt = m < N && u > prefix;
-    const bool eq = m < N && u == prefix;
-    uint32_t eq_total, take_total;
-    const uint32_t eq_rank = block_exclusive_count(eq, warp_tot, &eq_total);
-    const bool take = gt || (eq && eq_before + eq_rank < rank);
-    const uint32_t pos = block_exclusive_count(take, warp_tot, &take_total);
+  // token order.  Thread t owns the contiguous tokens [t E, (t + 1) E): two
+  // block scans give its first equal key's rank and its first output slot.
+  const int E = (N + blockDim.x - 1) / blockDim.x;
+  const int m0 = min(N, static_cast<int>(threadIdx.x) * E), m1 = min(N, m0 + E);
+  uint32_t n_eq = 0;
+  for (int m = m0; m < m1; ++m) n_eq += key(m) == prefix;
+  uint32_t total;
+  uint32_t eq_rank = block_exclusive_sum(n_eq, warp_tot, &total);
+  uint32_t n_take = 0;
+  for (int m = m0, r = eq_rank; m < m1; ++m) {
+    const uint32_t u = key(m);
+    n_take += u > prefix || (u == prefix && static_cast<uint32_t>(r) < rank);
+    r += u == prefix;
+  }
+  uint32_t out = block_exclusive_sum(n_take, warp_tot, &total);
+  for (int m = m0; m < m1; ++m) {
+    const uint32_t u = key(m);
+    const bool take = u > prefix || (u == prefix && eq_rank < rank);
+    eq_rank += u == prefix;
     // exactly R keys are taken; the bound only keeps a wrong count in the row
-    if (take && out + pos < static_cast<uint32_t>(R)) sel[static_cast<size_t>(blockIdx.x) * R + out + pos] = m;
-    out += take_total;
-    eq_before += eq_total;
+    if (take && out < static_cast<uint32_t>(R)) sel[static_cast<size_t>(blockIdx.x) * R + out] = m;
+    out += take;
   }
 }
 
@@ -154,20 +205,38 @@ __global__ void __launch_bounds__(kRepairThreads) vc_repair_kernel(const RepairA
   uint8_t* v8t = a.v8t + static_cast<size_t>(bh) * kHeadDim * a.npad;
   // (1) The non-repaired tokens p among the last R positions fill, in order,
   // the positions of the repaired tokens among the first N - R.  Sources and
-  // destinations are disjoint, so the moves do not race.
-  const int low = lower_bound(sel, R, split);  // repaired tokens below N - R
-  for (int p = split + threadIdx.x; p < N; p += blockDim.x) {
-    const int i = lower_bound(sel, R, p);       // repaired tokens below p
-    if (i < R && sel[i] == p) continue;         // p is repaired itself
-    const int r = (p - split) - (i - low);      // p's rank among the fillers: 0 <= r < low
-    if (r < 0 || r >= low) continue;            // (holds for a sorted set of distinct tokens)
-    const int dst = sel[r];
-    if (dst < 0 || dst >= split) continue;
-    const uint4* src = reinterpret_cast<const uint4*>(k8 + static_cast<size_t>(p) * kHeadDim);
-    uint4* out = reinterpret_cast<uint4*>(k8 + static_cast<size_t>(dst) * kHeadDim);
-#pragma unroll
-    for (int c = 0; c < kHeadDim / 16; ++c) out[c] = src[c];
-    for (int d = 0; d < kHeadDim; ++d) v8t[d * a.npad + dst] = v8t[d * a.npad + p];
+  // destinations are disjoint, so the moves do not race.  In chunks of
+  // kMoveChunk fillers: each thread finds the fillers among its candidate
+  // positions and notes (source, destination) at the filler's rank; then the
+  // whole block moves them, a K row as 8 16-byte pieces and a V^T column as
+  // 128 single bytes, one piece per thread and step.
+  __shared__ int2 moves[kMoveChunk];
+  const int low = lower_bound(sel, R, split);  // repaired tokens below N - R = fillers
+  for (int c0 = 0; c0 < low; c0 += kMoveChunk) {
+    const int cn = min(kMoveChunk, low - c0);
+    for (int p = split + threadIdx.x; p < N; p += blockDim.x) {
+      const int i = lower_bound(sel, R, p);       // repaired tokens below p
+      if (i < R && sel[i] == p) continue;         // p is repaired itself
+      const int r = (p - split) - (i - low);      // p's rank among the fillers: 0 <= r < low
+      if (r < c0 || r >= c0 + cn) continue;
+      const int dst = sel[r];
+      moves[r - c0] = make_int2(p, dst >= 0 && dst < split ? dst : -1);
+    }
+    __syncthreads();
+    constexpr int kPieces = kHeadDim / 16 + kHeadDim;  // K row pieces, then V^T bytes
+    for (int w = threadIdx.x; w < cn * kPieces; w += blockDim.x) {
+      const int f = w / kPieces, c = w - f * kPieces;
+      const int2 mv = moves[f];
+      if (mv.y < 0) continue;
+      if (c < kHeadDim / 16) {
+        reinterpret_cast<uint4*>(k8 + static_cast<size_t>(mv.y) * kHeadDim)[c] =
+            reinterpret_cast<const uint4*>(k8 + static_cast<size_t>(mv.x) * kHeadDim)[c];
+      } else {
+        const size_t d = static_cast<size_t>(c - kHeadDim / 16) * a.npad;
+        v8t[d + mv.y] = v8t[d + mv.x];
+      }
+    }
+    __syncthreads();
   }
   // (2) Repaired rows, a half-warp per row as in the E4M3 pass (lane l of the
   // half holds dims 8l .. 8l+7), two rows per warp step.

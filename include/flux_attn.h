@@ -90,8 +90,8 @@ typedef struct {
                               FP8).  Per (b, h) the R = ceil(rho N) key tokens with the largest
                               quantisation error |k' - deq(k')|^2 + |v - deq(v)|^2 attend with their
                               exact K', V ("Quantized and sparse attention": vc_attention,
-                              vc_repair_budget 0.005, the fraction of tokens with the highest
-                              quantisation error gets a residual correction).  Equal errors: the lower
+                              vc_repair_budget 0.005; the worst-quantised share of the tokens has
+                              its quantisation residual corrected).  Equal errors: the lower
                               token index is repaired first. */
   float sol_tau;      /* Sol-Attention threshold tau >= 0 (BF16 handles only; 0 = no block-sparse
                          calls).  Per (b, h), 128-token query block i keeps 128-key block j when the
@@ -238,14 +238,31 @@ FLUX_ATTN_API int flux_attn_attend_sol(flux_attn_t h, const void* qn, const void
  *   qn, kn  bf16 [B, H, N, 128] (the layout flux_attn_attend reads)
  *   v       bf16 [B, N, H, 128]
  * Outputs must not overlap each other or x.  FLUX_ATTN_ERR_UNSUPPORTED on FP8
- * handles and for other d_model. */
+ * handles (they take flux_attn_qkv_fp8) and for other d_model. */
 FLUX_ATTN_API int flux_attn_qkv(flux_attn_t h, const void* x, const void* w_qkv, const float* b_qkv, int d_model,
                   int txt_len, int img_h, int img_w, int ref_h, int ref_w, const int32_t* pos_ids,
                   const float* q_norm_w, const float* k_norm_w, void* qn, void* kn, void* v, cudaStream_t stream);
 
-/* The front half of a FLUX-style block in one call (BF16 handles): the QKV
- * projection with its fused QK-norm + RoPE epilogue (flux_attn_qkv), written
- * to the handle's workspace, then the joint attention over it.
+/* QKV projection for FP8 handles (same section): the GEMM and its epilogue
+ * as in flux_attn_qkv, written as bf16 to the handle's workspace while the
+ * epilogue reduces the per-(b, h) |max| of the Q', K', V values it writes;
+ * then one pass writes their E4M3 codes with scale = amax / 448, in the
+ * layouts flux_attn_attend_fp8 reads:
+ *   q8, k8  uint8 [B, H, N, 128];  v8t  uint8 [B, H, 128, pad16(N)];
+ *   scales  fp32 [B, H, 3]
+ * The codes are those of the bf16 values (rounded once more than the codes of
+ * flux_attn_prologue_fp8, which quantises its fp32 Q', K').  Other arguments
+ * as for flux_attn_qkv; UNSUPPORTED for handles with vc_repair_budget > 0. */
+FLUX_ATTN_API int flux_attn_qkv_fp8(flux_attn_t h, const void* x, const void* w_qkv, const float* b_qkv,
+                      int d_model, int txt_len, int img_h, int img_w, int ref_h, int ref_w,
+                      const int32_t* pos_ids, const float* q_norm_w, const float* k_norm_w, void* q8, void* k8,
+                      void* v8t, float* scales, cudaStream_t stream);
+
+/* The front half of a FLUX-style block in one call: the QKV projection with
+ * its fused QK-norm + RoPE epilogue (flux_attn_qkv; FP8 handles:
+ * flux_attn_qkv_fp8), written to the handle's workspace, then the joint
+ * attention over it (BF16 or FP8 as the handle's precision; not for handles
+ * with vc_repair_budget > 0).
  *   x, w_qkv, b_qkv, d_model, geometry, pos_ids, norm weights: as for flux_attn_qkv
  *   out     bf16 [B, N, H, 128]; must not alias x */
 FLUX_ATTN_API int flux_attn_forward_hidden(flux_attn_t h, const void* x, const void* w_qkv, const float* b_qkv,

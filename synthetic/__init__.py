@@ -56,6 +56,7 @@ class Workload:
     outliers: bool = False
     head_dim: int = HEAD_DIM
     vc_repair_budget: float = 0.0  # FP8 with VC-Attention repair when > 0
+    sol_tau: float = 0.0           # block-sparse Sol-Attention threshold when > 0
 
     @property
     def tokens(self) -> int:
@@ -85,6 +86,8 @@ WORKLOADS: Dict[str, Workload] = {
     # the same pair with the VC-Attention repair budget of the page's configuration
     "vc_fp8_cfg_2048_16896": Workload("vc_fp8_cfg_2048_16896", 2, 24, 512, 128, 128,
                                       precision="fp8", outliers=True, vc_repair_budget=0.005),
+    # FLUX 2048^2 with the block-sparse attention at the page's tau
+    "sol_flux_2048_16896": Workload("sol_flux_2048_16896", 1, 24, 512, 128, 128, sol_tau=1.0),
 }
 WORKLOAD_ORDER = ["tiny_320", "flux_1024_4608", "flux_2048_16896",
                   "i2i_2048_33280", "fp8_cfg_2048_16896"]

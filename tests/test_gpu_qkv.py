@@ -155,3 +155,65 @@ def test_qkv_alternating_geometry_no_sync():
     bad = [i for i in range(steps) if not (torch.equal(snaps[i][0], refs[i % 2][0]) and
                                            torch.equal(snaps[i][1], refs[i % 2][1]))]
     assert not bad, "steps with another geometry's rotation: %s" % bad
+
+
+# ------------------------------------------------------------------ FP8 codes
+
+_DECODE = None
+
+
+def _decode():
+    global _DECODE
+    if _DECODE is None:
+        _DECODE = oracle.e4m3_decode(np.arange(256, dtype=np.uint8))
+    return _DECODE
+
+
+def _codes_close(got, want, x, scale, what):
+    """E4M3 codes of the GPU (from its bf16 Q', K', V and a scale from their bf16
+    amax) against the oracle's (fp64 values x, fp64 amax).  A code may differ
+    only by one step, only where x / scale lies within 2^-7 (relative) of the
+    midpoint between the two codes -- the bf16 rounding before the codes can
+    move a value across it -- and for at most 5 % of the codes."""
+    diff = got != want
+    assert diff.mean() <= 0.05, "%s: %.3f of the codes differ" % (what, diff.mean())
+    if not diff.any():
+        return
+    t = _decode()
+    a, b = t[got[diff]], t[want[diff]]
+    assert np.all(np.sign(a) * np.sign(b) >= 0), what
+    mid = 0.5 * (a + b)
+    q = x[diff] / scale
+    step = np.abs(a - b)
+    assert np.all(step <= np.maximum(np.abs(b), 2.0 ** -6) * 2.0 ** -2), what   # neighbours (or the two next to 0)
+    assert np.all(np.abs(q - mid) <= 2.0 ** -7 * np.maximum(np.abs(mid), 2.0 ** -9) + 2.0 ** -10), what
+
+
+@pytest.mark.parametrize("B,H,txt,ih,iw,rh,rw,D", [
+    (2, 3, 7, 5, 9, 0, 0, 256),      # N = 52, B = 2: a token tile spans both batch rows
+    (1, 2, 100, 10, 12, 2, 3, 192),  # N = 226 with a reference stream
+])
+def test_qkv_fp8_codes_and_scales(B, H, txt, ih, iw, rh, rw, D):
+    """The FP8 QKV projection's codes and scales against the oracle's
+    projection quantised per (b, h) by the oracle (reading R5)."""
+    w = synthetic.Workload("qkv8", B, H, txt, ih, iw, rh, rw)
+    inp = synthetic.make_qkv_inputs(w, D, seed=B * 13 + H)
+    attn = fa.FluxAttention(B, H, w.tokens, precision="fp8")
+    x, wt = dev_bf16(inp.x), dev_bf16(inp.w)
+    b = torch.from_numpy(inp.bias).cuda()
+    wq, wk = torch.from_numpy(inp.w_q).cuda(), torch.from_numpy(inp.w_k).cuda()
+    q8, k8, v8t, scales = attn.qkv_fp8(x, wt, b, w.txt_len, w.img_h, w.img_w, w.ref_h, w.ref_w, wq, wk)
+    out = attn.attend_fp8(q8, k8, v8t, scales)
+    full = attn.forward_hidden(x, wt, b, w.txt_len, w.img_h, w.img_w, w.ref_h, w.ref_w, wq, wk)
+    assert attn.sync_status() == 0
+    assert torch.equal(out, full)
+    N = w.tokens
+    oq, ok, ov = oracle.qkv_rows(inp.x, inp.w, inp.bias, N, inp.pos, inp.w_q, inp.w_k, H)   # [B N, H, 128]
+    q8h, k8h, v8h, sch = (t.cpu().numpy() for t in (q8, k8, v8t, scales))
+    for bb in range(B):
+        for hh in range(H):
+            for t, (vals, codes) in enumerate(((oq, q8h[bb, hh]), (ok, k8h[bb, hh]), (ov, v8h[bb, hh, :, :N].T))):
+                xv = vals[bb * N:(bb + 1) * N, hh, :]
+                want, scale = oracle.fp8_quantize(xv)
+                np.testing.assert_allclose(sch[bb, hh, t], scale, rtol=2.0 ** -8)
+                _codes_close(codes, want, xv, scale, "(%d, %d) tensor %d" % (bb, hh, t))

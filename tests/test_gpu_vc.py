@@ -2,8 +2,8 @@
 
 "Speed up image generation with FLUX 3 Image Klein on NVIDIA Blackwell GPUs",
 section "Quantized and sparse attention": VC-Attention FP8 with a repair
-budget that selects the tokens with the highest quantisation error for a
-residual correction (reading R7 of the oracle: per (b, h) the ceil(rho N) key
+budget -- the worst-quantised share of the tokens gets its quantisation
+residual corrected (reading R7 of the oracle: per (b, h) the ceil(rho N) key
 tokens of largest |k' - deq(k')|^2 + |v - deq(v)|^2 attend with their exact
 K', V).
 
