@@ -57,8 +57,9 @@ namespace {
 
 thread_local std::string g_last_error;
 
-// Sol-Attention's block mask holds nb^2 bytes per head (nb = max_tokens / 128).
-constexpr int kSolMaxTokens = 1 << 18;
+// Sol-Attention's block mask holds nb^2 bytes per head (nb = max_tokens / 128),
+// and its keep kernel scores at most flux::sol::kMaxNb blocks.
+constexpr int kSolMaxTokens = flux::sol::kMaxNb * flux::sol::kBlock;
 
 // An NVTX range over the host-side enqueue of one call or one kernel launch:
 // profilers (Nsight Systems, ncu --nvtx) show the library's steps by name.
@@ -399,7 +400,7 @@ int launch_sol_mask(flux_attn* h, const void* qn, const void* kn, int n, uint8_t
   NvtxRange range("flux_attn/sol_mask");
   const int BH = h->cfg.batch * h->cfg.num_heads;
   const int nb = (n + flux::sol::kBlock - 1) / flux::sol::kBlock;
-  flux::sol::sol_pool_kernel<<<dim3(nb, BH), flux::sol::kThreads, 0, stream>>>(
+  flux::sol::sol_pool_kernel<<<dim3(nb, BH), flux::sol::kPoolThreads, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(qn), static_cast<const __nv_bfloat16*>(kn), n, h->qbar, h->kbar);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "block pooling launch");

@@ -29,55 +29,83 @@ namespace sol {
 constexpr int kBlock = 128;   // tokens per query / key block
 constexpr int kThreads = 128;
 constexpr int kMaxBlocks = 1 << 14;  // the list entry's 14-bit key block field
+constexpr int kMaxNb = 2048;         // key blocks per head the keep kernel scores (262144 tokens)
+constexpr int kPoolThreads = 256;
 
-// Block means of Q' and K' of block blockIdx.x of head blockIdx.y: thread d
-// sums dim d over the block's rows (one 256-byte row per step, coalesced).
-__global__ void __launch_bounds__(kThreads)
+// Block means of Q' and K' of block blockIdx.x of head blockIdx.y: thread t
+// sums the dim pair t % 64 (one bf16x2 word) over the rows t / 64, t / 64 + 4,
+// ... (eight independent loads in flight), then the four row groups are
+// added in a fixed order.
+__global__ void __launch_bounds__(kPoolThreads)
     sol_pool_kernel(const __nv_bfloat16* __restrict__ qn, const __nv_bfloat16* __restrict__ kn, int N,
                     float* __restrict__ qbar, float* __restrict__ kbar) {
-  const int blk = blockIdx.x, bh = blockIdx.y, d = threadIdx.x;
-  const int nb = gridDim.x;
+  __shared__ float2 part[2][kPoolThreads];
+  const int blk = blockIdx.x, bh = blockIdx.y, nb = gridDim.x;
+  const int dp = threadIdx.x & 63, rg = threadIdx.x >> 6;
+  constexpr int kGroups = kPoolThreads / 64;
   const int r0 = blk * kBlock, r1 = min(N, r0 + kBlock);
-  const size_t base = static_cast<size_t>(bh) * N * kHeadDim;
-  float sq = 0.f, sk = 0.f;
-  for (int r = r0; r < r1; ++r) {
-    sq += __bfloat162float(qn[base + static_cast<size_t>(r) * kHeadDim + d]);
-    sk += __bfloat162float(kn[base + static_cast<size_t>(r) * kHeadDim + d]);
+  const size_t base = static_cast<size_t>(bh) * N * (kHeadDim / 2);  // in bf16x2 words
+  const uint32_t* q = reinterpret_cast<const uint32_t*>(qn) + base;
+  const uint32_t* k = reinterpret_cast<const uint32_t*>(kn) + base;
+  float2 sq = make_float2(0.f, 0.f), sk = make_float2(0.f, 0.f);
+#pragma unroll 8
+  for (int r = r0 + rg; r < r1; r += kGroups) {
+    const uint32_t a = __ldg(q + static_cast<size_t>(r) * (kHeadDim / 2) + dp);
+    const uint32_t c = __ldg(k + static_cast<size_t>(r) * (kHeadDim / 2) + dp);
+    sq.x += __uint_as_float(a << 16);
+    sq.y += __uint_as_float(a & 0xFFFF0000u);
+    sk.x += __uint_as_float(c << 16);
+    sk.y += __uint_as_float(c & 0xFFFF0000u);
   }
-  const float inv = 1.f / static_cast<float>(r1 - r0);
-  const size_t o = (static_cast<size_t>(bh) * nb + blk) * kHeadDim + d;
-  qbar[o] = sq * inv;
-  kbar[o] = sk * inv;
+  part[0][threadIdx.x] = sq;
+  part[1][threadIdx.x] = sk;
+  __syncthreads();
+  if (rg == 0) {
+    const float inv = 1.f / static_cast<float>(r1 - r0);
+    for (int g = 1; g < kGroups; ++g) {
+      const float2 a = part[0][g * 64 + dp], c = part[1][g * 64 + dp];
+      sq.x += a.x; sq.y += a.y; sk.x += c.x; sk.y += c.y;
+    }
+    const size_t o = (static_cast<size_t>(bh) * nb + blk) * kHeadDim + 2 * dp;
+    *reinterpret_cast<float2*>(qbar + o) = make_float2(sq.x * inv, sq.y * inv);
+    *reinterpret_cast<float2*>(kbar + o) = make_float2(sk.x * inv, sk.y * inv);
+  }
 }
 
-// Keep row of query block blockIdx.x of head blockIdx.y: thread t takes key
-// blocks t, t + 128, ...; block-wide max, sum and argmax.
+// Keep row of query block blockIdx.x of head blockIdx.y: each thread scores
+// key blocks t, t + 128, ... once (into shared memory: at most kMaxNb), then
+// block-wide max with its lowest index, the normaliser and the keep bytes.
 __global__ void __launch_bounds__(kThreads)
     sol_keep_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int N, float tau,
                     uint8_t* __restrict__ keep) {
-  __shared__ float q[kHeadDim];
+  __shared__ float4 q4[kHeadDim / 4];
+  __shared__ float sc[kMaxNb];
   __shared__ float red_v[kThreads / 32];
   __shared__ int red_i[kThreads / 32];
   const int i = blockIdx.x, bh = blockIdx.y, nb = gridDim.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const float* kb = kbar + static_cast<size_t>(bh) * nb * kHeadDim;
-  q[tid] = qbar[(static_cast<size_t>(bh) * nb + i) * kHeadDim + tid];
+  const float4* kb = reinterpret_cast<const float4*>(kbar + static_cast<size_t>(bh) * nb * kHeadDim);
+  if (tid < kHeadDim / 4)
+    q4[tid] = reinterpret_cast<const float4*>(qbar + (static_cast<size_t>(bh) * nb + i) * kHeadDim)[tid];
   __syncthreads();
   const float scale = rsqrtf(static_cast<float>(kHeadDim));
-  // the scores of this thread's key blocks, in log units, with log c_j
-  auto score = [&](int j) {
-    const float* k = kb + static_cast<size_t>(j) * kHeadDim;
-    float s = 0.f;
-#pragma unroll 8
-    for (int e = 0; e < kHeadDim; ++e) s = fmaf(q[e], __ldg(k + e), s);
-    const int c = min(N, (j + 1) * kBlock) - j * kBlock;
-    return s * scale + logf(static_cast<float>(c));
-  };
-  // pass 1: max and its lowest index
+  // scores in log units, with the log of the block's key count
   float mx = -INFINITY;
   int arg = 0x7FFFFFFF;
   for (int j = tid; j < nb; j += kThreads) {
-    const float s = score(j);
+    const float4* k = kb + static_cast<size_t>(j) * (kHeadDim / 4);
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll 8
+    for (int e = 0; e < kHeadDim / 4; ++e) {
+      const float4 a = q4[e], b = __ldg(k + e);
+      s0 = fmaf(a.x, b.x, s0);
+      s1 = fmaf(a.y, b.y, s1);
+      s0 = fmaf(a.z, b.z, s0);
+      s1 = fmaf(a.w, b.w, s1);
+    }
+    const int c = min(N, (j + 1) * kBlock) - j * kBlock;
+    const float s = (s0 + s1) * scale + logf(static_cast<float>(c));
+    sc[j] = s;
     if (s > mx) { mx = s; arg = j; }
   }
 #pragma unroll
@@ -93,19 +121,17 @@ __global__ void __launch_bounds__(kThreads)
   for (int w = 1; w < kThreads / 32; ++w)
     if (red_v[w] > mx || (red_v[w] == mx && red_i[w] < arg)) { mx = red_v[w]; arg = red_i[w]; }
   __syncthreads();
-  // pass 2: the normaliser
   float z = 0.f;
-  for (int j = tid; j < nb; j += kThreads) z += expf(score(j) - mx);
+  for (int j = tid; j < nb; j += kThreads) z += expf(sc[j] - mx);
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, off);
   if (lane == 0) red_v[warp] = z;
   __syncthreads();
   z = 0.f;
   for (int w = 0; w < kThreads / 32; ++w) z += red_v[w];
-  // pass 3: keep
   const float thr = tau / static_cast<float>(nb);
   uint8_t* row = keep + (static_cast<size_t>(bh) * nb + i) * nb;
-  for (int j = tid; j < nb; j += kThreads) row[j] = (expf(score(j) - mx) / z >= thr || j == arg) ? 1 : 0;
+  for (int j = tid; j < nb; j += kThreads) row[j] = (expf(sc[j] - mx) / z >= thr || j == arg) ? 1 : 0;
 }
 
 // Union list of the key blocks kept by query blocks 2c and 2c + 1 (c =
