@@ -126,6 +126,8 @@ struct __align__(1024) Smem {
   uint64_t k_full[KST], k_empty[KST];
   uint64_t v_full[VST], v_empty[VST];
   uint64_t s_full[TILES], p_full[TILES], o_full[TILES];
+  uint64_t s_free[TILES];              // FP8: tile t's S is in registers (128 arrivals)
+  uint64_t o_done[TILES];              // FP8: PV_t of the last block has completed
   uint64_t qbf_full[TILES];            // REP: tile t's rows converted to bf16 (128 arrivals)
   uint64_t krep_full, krep_empty;      // REP: the repair K tile slot
   uint64_t vrep_full, vrep_empty;      // REP: the repair V tile slot
@@ -194,6 +196,11 @@ template <bool FP8>
 __device__ __forceinline__ uint8_t* krep_tile(Smem<FP8>& sm) { return &sm.rep[0][0]; }
 template <bool FP8>
 __device__ __forceinline__ uint8_t* vrep_tile(Smem<FP8>& sm) { return &sm.rep[FP8 ? 1 : 0][0]; }
+// FP8: tile t's P (E4M3, 128 rows x 128 keys, 16 KB in the K-major SW128
+// layout) -- the first half of the repair region, whose repair K tile is
+// consumed before the E4M3 blocks begin.
+template <bool FP8>
+__device__ __forceinline__ uint8_t* p_tile(Smem<FP8>& sm, int t) { return &sm.rep[0][0] + t * HALF; }
 
 // K ring producer: K_j into stage j % KST once both tiles' QK of its
 // previous occupant have completed.  REP: the repair K tiles too (into their
@@ -368,6 +375,72 @@ __device__ __forceinline__ bool mma_repair(Smem<FP8>& sm, uint32_t tmem, int nre
   return true;
 }
 
+// FP8: O (+)= P V with P from shared memory (pd: the P tile's K-major SW128
+// descriptor), V^T K-major: 4 MMAs of 128 x 128 x 32, step kk at byte 32kk.
+__device__ __forceinline__ void issue_pv_smem_e4m3(uint32_t o_tmem, uint64_t pd, uint64_t vd, bool accumulate) {
+  constexpr uint32_t ID = idesc_e4m3(BM, HD, false);
+#pragma unroll
+  for (int kk = 0; kk < BN / 32; ++kk)
+    mma_e4m3_ss(o_tmem, desc_at(pd, kk * 32), desc_at(vd, kk * 32), ID, (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// FP8 main loop of the MMA thread.  P goes through shared memory, so S_t's
+// TMEM columns are free as soon as the softmax has loaded them (s_free): QK_t
+// of the next block is issued then, and runs while the softmax of this block
+// works; PV_t follows when P_t is in (p_full) and signals o_done.  Per block:
+//   QK_0(j+1) QK_1(j+1)  [after s_free_0(j), s_free_1(j)]   PV_0(j) PV_1(j)  [after p_full]
+// ph: s_full / p_full phases the repair blocks used before.
+template <bool REP>
+__device__ __forceinline__ void mma_main_fp8(Smem<true>& sm, uint32_t tmem, int nkv, int ph, volatile int* ab,
+                                             uint32_t* err) {
+  constexpr uint32_t TILE = Traits<true>::TILE;
+  constexpr int KST = Traits<true>::KST, VST = Traits<true>::VST;
+  uint64_t qd[TILES], pd[TILES];
+#pragma unroll
+  for (int t = 0; t < TILES; ++t) {
+    qd[t] = sdesc_sw128(smem_u32(sm.q[t]), 16, 1024);
+    pd[t] = sdesc_sw128(smem_u32(p_tile(sm, t)), 16, 1024);
+  }
+  const uint64_t kd0 = sdesc_sw128(smem_u32(sm.k[0]), 16, 1024);
+  const uint64_t vd0 = sdesc_sw128(smem_u32(sm.v[0]), 16, 1024);
+  if (!mbar_wait(&sm.k_full[0], 0, ab, err)) return;
+#pragma unroll
+  for (int t = 0; t < TILES; ++t) {
+    if (!mbar_wait(&sm.q_full[t], 0, ab, err)) return;
+    tc_fence_after_sync();
+    issue_qk<true>(tmem + col_s(t), qd[t], kd0);
+    mma_commit(&sm.s_full[t]);
+  }
+  mma_commit(&sm.k_empty[0]);
+  for (int j = 0; j < nkv; ++j) {
+    const int jn = j + 1;
+    if (jn < nkv) {
+      const int ks = jn % KST;
+      if (!mbar_wait(&sm.k_full[ks], (jn / KST) & 1, ab, err)) return;
+#pragma unroll
+      for (int t = 0; t < TILES; ++t) {
+        if (!mbar_wait(&sm.s_free[t], j & 1, ab, err)) return;
+        tc_fence_after_sync();
+        issue_qk<true>(tmem + col_s(t), qd[t], desc_at(kd0, ks * TILE));
+        mma_commit(&sm.s_full[t]);
+      }
+      mma_commit(&sm.k_empty[ks]);
+    }
+    const int vs = j % VST;
+    if (!mbar_wait(&sm.v_full[vs], (j / VST) & 1, ab, err)) return;
+#pragma unroll
+    for (int t = 0; t < TILES; ++t) {
+      if (!mbar_wait(&sm.p_full[t], (j + ph) & 1, ab, err)) return;
+      tc_fence_after_sync();
+      issue_pv_smem_e4m3(tmem + col_o(t), pd[t], desc_at(vd0, vs * TILE), j + ph > 0);
+      mma_commit(&sm.o_done[t]);
+    }
+    mma_commit(&sm.v_empty[vs]);
+  }
+#pragma unroll
+  for (int t = 0; t < TILES; ++t) mma_commit(&sm.o_full[t]);
+}
+
 // The MMA issuer: QK_0(0) QK_1(0), then PV_0(j) QK_0(j+1) PV_1(j) QK_1(j+1)
 // for every j.  The whole warp runs this loop and one elected lane issues
 // (ptx.cuh).  One thread issues for both tiles: the fixed order is what
@@ -391,6 +464,12 @@ __device__ __forceinline__ void mma_issuer(Smem<FP8>& sm, uint32_t tmem, int nkv
   if (REP) nkv -= nrep;           // main-loop blocks
   do {
     if (REP && !mma_repair(sm, tmem, nrep, ab, err)) break;
+    if constexpr (FP8) {
+      if (nkv > 0) {
+        mma_main_fp8<REP>(sm, tmem, nkv, ph, ab, err);
+        break;
+      }
+    }
     if (nkv <= 0) {
 #pragma unroll
       for (int t = 0; t < TILES; ++t) mma_commit(&sm.o_full[t]);
@@ -598,6 +677,106 @@ __device__ __forceinline__ bool softmax_block(Smem<FP8>& sm, int t, uint32_t s_a
   return true;
 }
 
+// One E4M3 block of the FP8 main loop (128 threads, thread r = row r): as
+// softmax_block with P8, except that P goes to shared memory.  The thread
+// signals s_free as soon as S is in its registers (the MMA thread then
+// computes the next block's S into the same columns while this one works),
+// and before it writes P, or rescales O, it waits until the PV of the
+// previous block (jm - 1), which read the same P buffer and wrote O, has
+// completed (o_done).  jm: the block's index in the main loop; phase: its
+// s_full / p_full phase.
+__device__ __forceinline__ bool softmax_block_fp8(Smem<true>& sm, int t, int r, uint32_t s_addr, uint32_t o_addr,
+                                                  uint32_t phase, int jm, int valid, bool has_o, float sl2, float& m,
+                                                  float& l, volatile int* ab, uint32_t* err) {
+  constexpr float kPBias = 8.f;  // P = E4M3 of 256 p: folded into the exponent, cancels against l
+  constexpr float kRescale = Traits<true>::RESCALE;
+  bool ok = mbar_wait(&sm.s_full[t], phase, ab, err);
+  if (__any_sync(0xFFFFFFFFu, !ok)) return false;
+  tc_fence_after_sync();
+  uint32_t s[BN];
+  tmem_ld128(s_addr, s);
+  tmem_ld_wait(s);
+  tc_fence_before_sync();
+  mbar_arrive(&sm.s_free[t]);  // S_t's columns may take the next block's QK now
+  if (valid < BN) {
+#pragma unroll
+    for (int i = 0; i < BN; ++i)
+      if (i >= valid) s[i] = __float_as_uint(-INFINITY);
+  }
+  float acc[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) acc[c] = fmaxf(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1]));
+#pragma unroll
+  for (int i = 8; i < BN; i += 8) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      acc[c] = fmax3(acc[c], __uint_as_float(s[i + 2 * c]), __uint_as_float(s[i + 2 * c + 1]));
+  }
+  const float mx = fmax3(acc[0], acc[1], fmaxf(acc[2], acc[3]));
+  const float m_tile = fmaxf(m, mx * sl2);
+  const bool rescale = __any_sync(0xFFFFFFFFu, m_tile > m + kRescale);
+  const float m_new = rescale ? m_tile : m;
+  const float alpha = rescale ? ex2_approx(m - m_new) : 1.f;  // 0 on the first tile
+  const float nm = kPBias - m_new;
+  // P codes four per word (key 4i in the lowest byte); the row sum adds the
+  // values of the codes in eight packed f16 accumulators (each at most 8
+  // values <= 256), widened to fp32 once per block.
+  uint32_t pk[32];
+  __half2 hs[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) hs[i] = __float2half2_rn(0.f);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    float x0, x1, x2, x3;
+    fma2(x0, x1, __uint_as_float(s[4 * i]), __uint_as_float(s[4 * i + 1]), sl2, sl2, nm, nm);
+    fma2(x2, x3, __uint_as_float(s[4 * i + 2]), __uint_as_float(s[4 * i + 3]), sl2, sl2, nm, nm);
+    const uint32_t lo = e4m3x2(ex2_approx(x0), ex2_approx(x1));
+    const uint32_t hi = e4m3x2(ex2_approx(x2), ex2_approx(x3));
+    pk[i] = lo | (hi << 16);
+    hs[i & 7] = __hadd2(hs[i & 7], __hadd2(e4m3x2_value(lo), e4m3x2_value(hi)));
+  }
+  float sum[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float2 f = __half22float2(hs[i]);
+    sum[i] = f.x + f.y;
+  }
+  add2(sum[0], sum[1], sum[2], sum[3]);
+  add2(sum[4], sum[5], sum[6], sum[7]);
+  add2(sum[0], sum[1], sum[4], sum[5]);
+  l = l * alpha + (sum[0] + sum[1]);
+  // the previous block's PV has read the P buffer and written O
+  if (jm > 0) {
+    ok = mbar_wait(&sm.o_done[t], (jm - 1) & 1, ab, err);
+    if (__any_sync(0xFFFFFFFFu, !ok)) return false;
+    tc_fence_after_sync();
+  }
+  // P -> row r of the tile's K-major SW128 buffer: 16-byte chunk c (keys
+  // 16c .. 16c+15) at chunk position c ^ (r % 8)
+  uint8_t* prow = p_tile(sm, t) + r * 128;
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
+                                                                          pk[4 * c + 3]);
+  fence_proxy_async_smem();  // generic-proxy writes, read by the MMA (async proxy)
+  if (rescale && has_o) {
+#pragma unroll
+    for (int c = 0; c < HD / 32; ++c) {
+      uint32_t o[32];
+      tmem_ld32(o_addr + c * 32, o);
+      tmem_ld_wait(o);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+      tmem_st32(o_addr + c * 32, o);
+    }
+    tmem_st_wait();
+  }
+  m = m_new;
+  tc_fence_before_sync();
+  mbar_arrive(&sm.p_full[t]);
+  return true;
+}
+
 // Softmax and epilogue of query tile `t` (128 threads, thread r = row r).
 // REP: the Q conversion and the repair blocks (bf16 P) come first, then the
 // E4M3 blocks, whose loop is the plain FP8 one with its phases shifted.
@@ -639,6 +818,10 @@ __device__ __forceinline__ void softmax_epilogue(Smem<FP8>& sm, uint32_t tmem, c
       ok = softmax_block<FP8, false>(sm, t, s_addr, o_addr, j & 1, prm.N - static_cast<int>(e & 0x3FFFu) * BN,
                                      j > 0, sl2, m, l, ab, prm.err, (e >> (14 + t)) & 1u);
     }
+  } else if constexpr (FP8) {
+    for (int j = 0; j < nmain && ok; ++j)
+      ok = softmax_block_fp8(sm, t, r, s_addr, o_addr, (j + nrep) & 1, j, prm.main_keys - j * BN, j + nrep > 0, sl2,
+                             m, l, ab, prm.err);
   } else {
     for (int j = 0; j < nmain && ok; ++j)
       ok = softmax_block<FP8, FP8>(sm, t, s_addr, o_addr, (j + nrep) & 1, prm.main_keys - j * BN, j + nrep > 0,
@@ -720,7 +903,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int s = 0; s < KST; ++s) { mbar_init(&sm.k_full[s], 1); mbar_init(&sm.k_empty[s], 1); }
     for (int s = 0; s < VST; ++s) { mbar_init(&sm.v_full[s], 1); mbar_init(&sm.v_empty[s], 1); }
-    for (int t = 0; t < TILES; ++t) mbar_init(&sm.qbf_full[t], BM);
+    for (int t = 0; t < TILES; ++t) {
+      mbar_init(&sm.qbf_full[t], BM);
+      mbar_init(&sm.s_free[t], BM);
+      mbar_init(&sm.o_done[t], 1);
+    }
     mbar_init(&sm.krep_full, 1);
     mbar_init(&sm.krep_empty, 1);
     mbar_init(&sm.vrep_full, 1);
