@@ -17,9 +17,13 @@
 //   warp 8     TMA producer of the K ring
 //   warp 9     TMEM allocator and tcgen05.mma issuer (one elected lane)
 //   warp 10    TMA producer of both Q tiles and of the V ring
-// TMEM (512 columns): S_0 at 0, S_1 at 128, O_0 at 256, O_1 at 384.  The
-// softmax of a tile overwrites its S with P, and the P.V MMA reads P straight
-// from TMEM as its A operand.
+//   warp 11    FP8 without repair blocks: the tcgen05.mma issuer of query
+//              tile 1 (warp 9 then issues for tile 0 only); idle otherwise
+// TMEM (512 columns): S_0 at 0, S_1 at 128, O_0 at 256, O_1 at 384.  BF16
+// (and the repair blocks): the softmax of a tile overwrites its S with P, and
+// the P.V MMA reads P straight from TMEM as its A operand.  FP8: P goes to a
+// shared-memory tile instead (mma_main_fp8), so that S_t takes the next
+// block's scores while the softmax still works on this one.
 //
 // The MMA issue order is  QK_0(0) QK_1(0) | PV_0(j) QK_0(j+1) PV_1(j) QK_1(j+1) | ...
 // so while the softmax of tile 0 works on S_0(j+1) the tensor core runs
@@ -46,9 +50,10 @@
 // FP8: Q', K' are E4M3 codes [B, H, N, 128] and V is E4M3 transposed
 // [B, H, 128, Npad] (kind::f8f6f4, K = 32 per MMA).  A 128 x 128 tile is one
 // 16 KB SW128 block, K-major for all three (for V^T the keys are the K
-// dimension of P.V).  P is E4M3 of 256 p, four per TMEM column; the row sum
-// l adds the values the codes stand for, so that O = sum p~ v / sum p~ is a
-// convex combination of the V rows whatever the rounding of P.  Scores are
+// dimension of P.V).  P is E4M3 of 256 p (a K-major SW128 tile in shared
+// memory); the row sum l adds the values the codes stand for, so that
+// O = sum p~ v / sum p~ is a convex combination of the V rows whatever the
+// rounding of P.  Scores are
 // scaled by s_q s_k and the output by s_v (per-(b, h) scales).  The FP8
 // softmax sums the P values in packed f16 (E4M3 values are exact in f16):
 // decoding every code back to fp32 for the sum cost it a sixth of its
@@ -93,7 +98,8 @@ constexpr int CTA_ROWS = TILES * BM;
 constexpr int WARP_LOAD_K = 4 * TILES;          // 8: TMA producer of the K ring
 constexpr int WARP_MMA = WARP_LOAD_K + 1;       // 9: MMA issuer, TMEM owner
 constexpr int WARP_LOAD_V = WARP_MMA + 1;       // 10: TMA producer of Q and the V ring
-constexpr int THREADS = 32 * (WARP_LOAD_V + 1); // 352
+constexpr int WARP_MMA1 = WARP_LOAD_V + 1;      // 11: FP8 (no repair): MMA issuer of query tile 1
+constexpr int THREADS = 32 * (WARP_MMA1 + 1);   // 384
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t HALF = BM * 128;  // one SW128 block: 128 rows x 128 bytes = 16 KB
 
@@ -133,6 +139,7 @@ struct __align__(1024) Smem {
   uint64_t vrep_full, vrep_empty;      // REP: the repair V tile slot
   uint64_t qbf_free;                   // REP: last repair QK of both tiles done
   uint64_t mma_drain;
+  uint64_t mma_drain1;
   uint64_t never;  // nothing arrives here (forced-timeout debug path)
   uint32_t tmem_base;
   int abort;
@@ -389,15 +396,19 @@ __device__ __forceinline__ void issue_pv_smem_e4m3(uint32_t o_tmem, uint64_t pd,
 // of the next block is issued then, and runs while the softmax of this block
 // works; PV_t follows when P_t is in (p_full) and signals o_done.  Per block:
 //   QK_0(j+1) QK_1(j+1)  [after s_free_0(j), s_free_1(j)]   PV_0(j) PV_1(j)  [after p_full]
-// ph: s_full / p_full phases the repair blocks used before.
-template <bool REP>
+// ph: s_full / p_full phases the repair blocks used before.  The issuing
+// thread serves query tiles T0 .. T1-1: both (with repair blocks), or one
+// each from two warps (split_issue: tile 0 from WARP_MMA, tile 1 from
+// WARP_MMA1), which halves the issue work that lands on the scheduler of
+// each of the two warps; every K and V stage then waits for both commits.
+template <bool REP, int T0, int T1>
 __device__ __forceinline__ void mma_main_fp8(Smem<true>& sm, uint32_t tmem, int nkv, int ph, volatile int* ab,
                                              uint32_t* err) {
   constexpr uint32_t TILE = Traits<true>::TILE;
   constexpr int KST = Traits<true>::KST, VST = Traits<true>::VST;
   uint64_t qd[TILES], pd[TILES];
 #pragma unroll
-  for (int t = 0; t < TILES; ++t) {
+  for (int t = T0; t < T1; ++t) {
     qd[t] = sdesc_sw128(smem_u32(sm.q[t]), 16, 1024);
     pd[t] = sdesc_sw128(smem_u32(p_tile(sm, t)), 16, 1024);
   }
@@ -405,7 +416,7 @@ __device__ __forceinline__ void mma_main_fp8(Smem<true>& sm, uint32_t tmem, int 
   const uint64_t vd0 = sdesc_sw128(smem_u32(sm.v[0]), 16, 1024);
   if (!mbar_wait(&sm.k_full[0], 0, ab, err)) return;
 #pragma unroll
-  for (int t = 0; t < TILES; ++t) {
+  for (int t = T0; t < T1; ++t) {
     if (!mbar_wait(&sm.q_full[t], 0, ab, err)) return;
     tc_fence_after_sync();
     issue_qk<true>(tmem + col_s(t), qd[t], kd0);
@@ -418,7 +429,7 @@ __device__ __forceinline__ void mma_main_fp8(Smem<true>& sm, uint32_t tmem, int 
       const int ks = jn % KST;
       if (!mbar_wait(&sm.k_full[ks], (jn / KST) & 1, ab, err)) return;
 #pragma unroll
-      for (int t = 0; t < TILES; ++t) {
+      for (int t = T0; t < T1; ++t) {
         if (!mbar_wait(&sm.s_free[t], j & 1, ab, err)) return;
         tc_fence_after_sync();
         issue_qk<true>(tmem + col_s(t), qd[t], desc_at(kd0, ks * TILE));
@@ -429,7 +440,7 @@ __device__ __forceinline__ void mma_main_fp8(Smem<true>& sm, uint32_t tmem, int 
     const int vs = j % VST;
     if (!mbar_wait(&sm.v_full[vs], (j / VST) & 1, ab, err)) return;
 #pragma unroll
-    for (int t = 0; t < TILES; ++t) {
+    for (int t = T0; t < T1; ++t) {
       if (!mbar_wait(&sm.p_full[t], (j + ph) & 1, ab, err)) return;
       tc_fence_after_sync();
       issue_pv_smem_e4m3(tmem + col_o(t), pd[t], desc_at(vd0, vs * TILE), j + ph > 0);
@@ -438,7 +449,7 @@ __device__ __forceinline__ void mma_main_fp8(Smem<true>& sm, uint32_t tmem, int 
     mma_commit(&sm.v_empty[vs]);
   }
 #pragma unroll
-  for (int t = 0; t < TILES; ++t) mma_commit(&sm.o_full[t]);
+  for (int t = T0; t < T1; ++t) mma_commit(&sm.o_full[t]);
 }
 
 // The MMA issuer: QK_0(0) QK_1(0), then PV_0(j) QK_0(j+1) PV_1(j) QK_1(j+1)
@@ -466,7 +477,7 @@ __device__ __forceinline__ void mma_issuer(Smem<FP8>& sm, uint32_t tmem, int nkv
     if (REP && !mma_repair(sm, tmem, nrep, ab, err)) break;
     if constexpr (FP8) {
       if (nkv > 0) {
-        mma_main_fp8<REP>(sm, tmem, nkv, ph, ab, err);
+        mma_main_fp8<REP, 0, REP ? TILES : 1>(sm, tmem, nkv, ph, ab, err);
         break;
       }
     }
@@ -520,6 +531,18 @@ __device__ __forceinline__ void mma_issuer(Smem<FP8>& sm, uint32_t tmem, int nkv
   // Drain every MMA this thread issued before TMEM is released.
   mma_commit(&sm.mma_drain);
   mbar_drain(&sm.mma_drain, 0, err);
+}
+
+// FP8 without repair blocks: the MMAs of query tile 1 come from their own
+// warp (see mma_main_fp8); it drains them before TMEM is released.
+template <bool FP8, bool REP>
+__device__ __forceinline__ constexpr bool split_issue() { return FP8 && !REP; }
+
+__device__ __forceinline__ void mma_issuer_tile1(Smem<true>& sm, uint32_t tmem, int nkv, volatile int* ab,
+                                                 uint32_t* err) {
+  if (nkv > 0) mma_main_fp8<false, 1, TILES>(sm, tmem, nkv, 0, ab, err);
+  mma_commit(&sm.mma_drain1);
+  mbar_drain(&sm.mma_drain1, 0, err);
 }
 
 // Two E4M3 codes (round to nearest even, saturating) of a float pair, a in the low byte.
@@ -838,13 +861,20 @@ __device__ __forceinline__ void softmax_epilogue(Smem<FP8>& sm, uint32_t tmem, c
   // more, in the SW128 layout of the out tensor map: half c / 2 holds head
   // dims 64 (c / 2) .., row r at byte 128 r, its 16-byte chunk k at position
   // k ^ (r % 8).  BF16: the tile's own 32 KB Q buffer (its last QK completed
-  // before the PV that signalled o_full).  FP8: a Q tile is only 16 KB, so
-  // 32 KB of the K ring, idle once both tiles' last QK has completed (it
-  // precedes PV_0(last) in issue order).  Then one thread writes the two
-  // halves with TMA stores, which also clip rows >= N: whole 128-byte rows
-  // instead of each thread's 16-byte pieces of rows H x 256 bytes apart.
-  static_assert(!FP8 || Traits<FP8>::KST * Traits<FP8>::TILE >= TILES * 2 * HALF, "FP8 staging needs 64 KB of K ring");
-  uint8_t* stage = FP8 ? &sm.k[0][0] + t * 2 * HALF : sm.q[t];
+  // before the PV that signalled o_full).  FP8: the tile's own 16 KB Q buffer
+  // and its 16 KB P buffer, which only this tile's MMAs read (the K ring may
+  // still feed the other tile, whose MMAs can come from another thread).
+  // Then one thread writes the two halves with TMA stores, which also clip
+  // rows >= N: whole 128-byte rows instead of each thread's 16-byte pieces of
+  // rows H x 256 bytes apart.
+  uint8_t* stage[2];
+  if constexpr (FP8) {
+    stage[0] = sm.q[t];
+    stage[1] = p_tile(sm, t);
+  } else {
+    stage[0] = sm.q[t];
+    stage[1] = sm.q[t] + HALF;
+  }
 #pragma unroll
   for (int c = 0; c < HD / 32; ++c) {
     uint32_t o[32];
@@ -858,15 +888,15 @@ __device__ __forceinline__ void softmax_epilogue(Smem<FP8>& sm, uint32_t tmem, c
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int k = (c & 1) * 4 + i;  // 16-byte chunk within the 128-byte row of this half
-      *reinterpret_cast<uint4*>(stage + half * HALF + r * 128 + ((k ^ (r & 7)) << 4)) =
+      *reinterpret_cast<uint4*>(stage[half] + r * 128 + ((k ^ (r & 7)) << 4)) =
           make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
     }
   }
   fence_proxy_async_smem();
   asm volatile("bar.sync %0, %1;" ::"r"(1 + t), "n"(BM) : "memory");
   if (r == 0) {
-    tma_store_4d(tm_o, smem_u32(stage), 0, h, row0, b);          // rows >= N are clipped
-    tma_store_4d(tm_o, smem_u32(stage) + HALF, 64, h, row0, b);
+    tma_store_4d(tm_o, smem_u32(stage[0]), 0, h, row0, b);  // rows >= N are clipped
+    tma_store_4d(tm_o, smem_u32(stage[1]), 64, h, row0, b);
     bulk_commit();
     bulk_wait_all();
   }
@@ -901,8 +931,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&sm.p_full[t], BM);
       mbar_init(&sm.o_full[t], 1);
     }
-    for (int s = 0; s < KST; ++s) { mbar_init(&sm.k_full[s], 1); mbar_init(&sm.k_empty[s], 1); }
-    for (int s = 0; s < VST; ++s) { mbar_init(&sm.v_full[s], 1); mbar_init(&sm.v_empty[s], 1); }
+    // a K / V stage is free once every issuing thread has committed it
+    constexpr int issuers = split_issue<FP8, REP>() ? 2 : 1;
+    for (int s = 0; s < KST; ++s) { mbar_init(&sm.k_full[s], 1); mbar_init(&sm.k_empty[s], issuers); }
+    for (int s = 0; s < VST; ++s) { mbar_init(&sm.v_full[s], 1); mbar_init(&sm.v_empty[s], issuers); }
     for (int t = 0; t < TILES; ++t) {
       mbar_init(&sm.qbf_full[t], BM);
       mbar_init(&sm.s_free[t], BM);
@@ -914,6 +946,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(&sm.vrep_empty, 1);
     mbar_init(&sm.qbf_free, 1);
     mbar_init(&sm.mma_drain, 1);
+    mbar_init(&sm.mma_drain1, 1);
     mbar_init(&sm.never, 1);
     sm.abort = 0;
     fence_mbarrier_init();
@@ -962,6 +995,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncwarp();
   } else if (warp == WARP_MMA) {
     if (!*ab) mma_issuer<FP8, REP>(sm, tmem, nkv, prm.nrep, ab, prm.err);  // the whole warp: see mma_commit
+    __syncwarp();
+  } else if (warp == WARP_MMA1) {
+    if constexpr (split_issue<FP8, REP>()) {
+      if (!*ab) mma_issuer_tile1(sm, tmem, nkv, ab, prm.err);
+    }
     __syncwarp();
   } else {
     const int t = warp >> 2;  // query tile of this warpgroup

@@ -38,6 +38,7 @@ struct flux_attn {
   uint32_t* amax;         // FP8: [B, H, 3] fp32 bits
   float* scales;          // FP8: [B, H, 3]
   float2* rope;           // BF16: (cos, sin) table [max_tokens][64] of the QKV projection
+  float2* rot;            // (cos, sin) per position [kRotPositions][64], built at creation
   float* errk;            // VC: K' quantisation error per token [B*H][max_tokens]
   float* errv;            // VC: V quantisation error per token [B*H][max_tokens]
   int32_t* sel;           // VC: repaired tokens [B*H][r_max]
@@ -185,8 +186,9 @@ int launch_prologue(flux_attn* h, const void* q, const void* k, int txt, int ih,
   const long long units = (static_cast<long long>(B) * n + W - 1) / W;
   const unsigned grid = static_cast<unsigned>(std::min<long long>(units, h->num_sms));
   const size_t smem = flux::stream_smem<flux::Bf16Rows>(H);
-  const flux::StreamArgs a{static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), wq, wk,
-                           geo, B, n, H, h->cfg.rms_eps, h->rope_tab, h->err};
+  flux::StreamArgs a{static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), wq, wk,
+                     geo, B, n, H, h->cfg.rms_eps, h->rope_tab, h->err};
+  a.rot = h->rot;
   flux::qk_norm_rope_kernel<flux::Bf16Rows><<<grid, 32 * W, smem, stream>>>(a, flux::Bf16Rows{qn, kn});
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "prologue launch");
@@ -250,8 +252,9 @@ int launch_prologue_fp8(flux_attn* h, const void* q, const void* k, const void* 
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "V amax launch");
   // Q', K': the prologue's stream kernel, once reducing to amax, once writing codes
-  const flux::StreamArgs a{static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), wq, wk,
-                           geo, B, n, H, h->cfg.rms_eps, h->rope_tab, h->err};
+  flux::StreamArgs a{static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), wq, wk,
+                     geo, B, n, H, h->cfg.rms_eps, h->rope_tab, h->err};
+  a.rot = h->rot;
   const long long tokens = static_cast<long long>(B) * n;
   {
     const int W = flux::stream_warps<flux::AmaxRows>(H);
@@ -284,8 +287,8 @@ int launch_prologue_fp8(flux_attn* h, const void* q, const void* k, const void* 
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "repair selection launch");
     const flux::vc::RepairArgs ra{static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), wk,
-                                  geo, h->rope_tab, n, H, R, h->cfg.rms_eps, scales, sel, k8, v8t, pad16(n), krep,
-                                  vrep};
+                                  geo, h->rope_tab, h->rot, n, H, R, h->cfg.rms_eps, scales, sel, k8, v8t,
+                                  pad16(n), krep, vrep};
     flux::vc::vc_repair_kernel<<<B * H, flux::vc::kRepairThreads, 0, stream>>>(ra);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "repair launch");
@@ -438,7 +441,7 @@ int launch_qkv(flux_attn* h, const void* x, const void* w, const float* bias, in
   flux::TokenGeometry geo{pos, txt, ih * iw, iw, rw};
   const int pairs = n * (flux::kHeadDim / 2);
   const int tblocks = std::min((pairs + kTableThreads - 1) / kTableThreads, kTableBlocksPerSm * h->num_sms);
-  flux::qkv::rope_table_kernel<<<tblocks, kTableThreads, 0, stream>>>(geo, n, h->rope_tab, h->rope);
+  flux::qkv::rope_table_kernel<<<tblocks, kTableThreads, 0, stream>>>(geo, n, h->rope_tab, h->rot, h->rope);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "rope table launch");
   CUtensorMap ta, tb;
@@ -612,7 +615,7 @@ int flux_attn_create(const flux_attn_config* cfg, flux_attn_t* out) {
   //         (cos, sin) table of the QKV projection (FP8: its bf16 outputs before the codes)
   //   FP8   Q', K' E4M3 [B, H, max_tokens, 128], V^T E4M3 [B, H, 128, pad16(max_tokens)],
   //         amax and scales [B, H, 3]
-  //   VC / SOL  their buffers (below); the device error word
+  //   VC / SOL  their buffers (below); the per-position rotation table; the device error word
   const size_t bh = static_cast<size_t>(cfg->batch) * cfg->num_heads;
   const bool fp8 = cfg->precision == FLUX_ATTN_FP8_E4M3;
   const auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
@@ -621,6 +624,7 @@ int flux_attn_create(const flux_attn_config* cfg, flux_attn_t* out) {
   const size_t vt_bytes = fp8 ? al(bh * flux::kHeadDim * pad16(cfg->max_tokens)) : 0;
   const size_t sc_bytes = fp8 ? al(bh * 3 * sizeof(float)) : 0;
   const size_t rope_bytes = al(static_cast<size_t>(cfg->max_tokens) * (flux::kHeadDim / 2) * sizeof(float2));
+  const size_t rot_bytes = al(static_cast<size_t>(flux::kRotPositions) * (flux::kHeadDim / 2) * sizeof(float2));
   const size_t v_bytes = qk_bytes;
   h->r_max = repair_count(h, cfg->max_tokens);
   const size_t vc_err_bytes = h->r_max > 0 ? al(bh * cfg->max_tokens * sizeof(float)) : 0;
@@ -636,7 +640,8 @@ int flux_attn_create(const flux_attn_config* cfg, flux_attn_t* out) {
   const size_t sol_list_bytes = sol ? al(bh * ncta_max * nb_max * sizeof(uint16_t)) : 0;
   const size_t sol_count_bytes = sol ? al(bh * ncta_max * sizeof(int)) : 0;
   const size_t sol_off = vc_off + 2 * vc_err_bytes + vc_sel_bytes + 2 * vc_row_bytes;
-  const size_t err_off = sol_off + 2 * sol_bar_bytes + sol_keep_bytes + sol_list_bytes + sol_count_bytes;
+  const size_t rot_off = sol_off + 2 * sol_bar_bytes + sol_keep_bytes + sol_list_bytes + sol_count_bytes;
+  const size_t err_off = rot_off + rot_bytes;
   h->ws_bytes = err_off + 256;
   e = cudaMalloc(&h->ws, h->ws_bytes);
   if (e != cudaSuccess) {
@@ -672,11 +677,19 @@ int flux_attn_create(const flux_attn_config* cfg, flux_attn_t* out) {
     h->sol_count = reinterpret_cast<int*>(base + sol_off + 2 * sol_bar_bytes + sol_keep_bytes + sol_list_bytes);
   }
   h->err = reinterpret_cast<uint32_t*>(base + err_off);
+  h->rot = reinterpret_cast<float2*>(base + rot_off);
   e = cudaMemset(h->err, 0, 256);
+  if (e == cudaSuccess) {
+    // the rotation table, once (the handle's calls may come on any stream)
+    constexpr int kRotElems = flux::kRotPositions * (flux::kHeadDim / 2);
+    flux::rot_table_kernel<<<(kRotElems + 255) / 256, 256>>>(h->rope_tab, h->rot);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  }
   if (e != cudaSuccess) {
     cudaFree(h->ws);
     delete h;
-    return cuda_fail(e, "cudaMemset");
+    return cuda_fail(e, "initialising the workspace");
   }
   *out = h;
   return FLUX_ATTN_OK;

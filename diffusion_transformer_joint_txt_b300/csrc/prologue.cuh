@@ -56,11 +56,28 @@ __device__ __forceinline__ void token_position(const TokenGeometry& g, int n, in
   }
 }
 
-// Rotation angles of the four pairs a lane owns (pairs 4 sub .. 4 sub + 3);
-// the axis of a pair picks its position id with selects, not an indexed
+// (cos, sin) of pos * freq_j for the positions 0 .. kRotPositions-1 and all
+// 64 pairs, [pos][j], computed once per handle (rot_table_kernel) with the
+// same sincosf as the direct path below, so the two give the same bits.  The
+// [text | image | reference] geometries of FLUX stay inside it up to 4096
+// pixels a side (256 patches); other positions take the direct path.
+constexpr int kRotPositions = 256;
+
+__global__ void rot_table_kernel(RopeTable tab, float2* __restrict__ rot) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= kRotPositions * (kHeadDim / 2)) return;
+  const int pos = i / (kHeadDim / 2), j = i - pos * (kHeadDim / 2);
+  float s, c;
+  sincosf(static_cast<float>(pos) * tab.freq[j], &s, &c);
+  rot[i] = make_float2(c, s);
+}
+
+// Rotation angles of the four pairs a lane owns (pairs 4 sub .. 4 sub + 3):
+// from the table when rot is set and the position is in it, else sincosf.
+// The axis of a pair picks its position id with selects, not an indexed
 // local array.
-__device__ __forceinline__ void lane_rotation(const TokenGeometry& geo, const RopeTable& tab, int n, int sub,
-                                              float (&c)[4], float (&s)[4]) {
+__device__ __forceinline__ void lane_rotation(const TokenGeometry& geo, const RopeTable& tab, const float2* rot,
+                                              int n, int sub, float (&c)[4], float (&s)[4]) {
   int p[3];
   token_position(geo, n, p);
 #pragma unroll
@@ -68,7 +85,13 @@ __device__ __forceinline__ void lane_rotation(const TokenGeometry& geo, const Ro
     const int j = sub * 4 + i;
     const int a = tab.axis[j];
     const int pos = a == 0 ? p[0] : (a == 1 ? p[1] : p[2]);
-    sincosf(static_cast<float>(pos) * tab.freq[j], &s[i], &c[i]);
+    if (rot != nullptr && static_cast<unsigned>(pos) < static_cast<unsigned>(kRotPositions)) {
+      const float2 cs = __ldg(rot + pos * (kHeadDim / 2) + j);
+      c[i] = cs.x;
+      s[i] = cs.y;
+    } else {
+      sincosf(static_cast<float>(pos) * tab.freq[j], &s[i], &c[i]);
+    }
   }
 }
 
@@ -209,6 +232,7 @@ struct StreamArgs {
   float eps;
   RopeTable tab;
   uint32_t* err;
+  const float2* rot = nullptr;  // rotation table (kRotPositions x 64), or none
 };
 
 // Launch shape of the stream kernel for output policy Out and H heads.
@@ -291,7 +315,7 @@ __global__ void __launch_bounds__(32 * Out::kWarps, 1) qk_norm_rope_kernel(const
         n = static_cast<int>(t - static_cast<long long>(b) * N);
         out.token(b);
         float cs[4], sn[4];
-        lane_rotation(a.geo, a.tab, n, sub, cs, sn);
+        lane_rotation(a.geo, a.tab, a.rot, n, sub, cs, sn);
         rot_coef(w_q, cs, sn, kq);
         rot_coef(w_k, cs, sn, kk);
       }

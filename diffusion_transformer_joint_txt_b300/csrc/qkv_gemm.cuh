@@ -72,7 +72,8 @@ struct Params {
   float eps;
 };
 
-// (cos, sin) of pair j of token n: pos_n[axis_j] * freq_j, precise sincosf.
+// (cos, sin) of pair j of token n: pos_n[axis_j] * freq_j, precise sincosf
+// (looked up in the handle's per-position table when the position is in it).
 // Launched as one wave (a grid-stride loop over the N x 64 pairs, at most
 // kTableBlocksPerSm blocks per SM), so that it may let the GEMM after it
 // start early: the GEMM's producer and MMA warps do not read the table, and
@@ -81,7 +82,8 @@ constexpr int kTableThreads = 256;
 constexpr int kTableBlocksPerSm = 4;
 
 __global__ void __launch_bounds__(kTableThreads)
-    rope_table_kernel(TokenGeometry geo, int N, RopeTable tab, float2* __restrict__ out) {
+    rope_table_kernel(TokenGeometry geo, int N, RopeTable tab, const float2* __restrict__ rot,
+                      float2* __restrict__ out) {
   griddep_launch_dependents();
   const int total = N * (kHeadDim / 2);
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
@@ -91,9 +93,13 @@ __global__ void __launch_bounds__(kTableThreads)
     token_position(geo, n, p);
     const int a = tab.axis[j];
     const int pos = a == 0 ? p[0] : (a == 1 ? p[1] : p[2]);
-    float s, c;
-    sincosf(static_cast<float>(pos) * tab.freq[j], &s, &c);
-    out[i] = make_float2(c, s);
+    if (rot != nullptr && static_cast<unsigned>(pos) < static_cast<unsigned>(kRotPositions)) {
+      out[i] = __ldg(rot + pos * (kHeadDim / 2) + j);  // the same sincosf, tabulated per position
+    } else {
+      float s, c;
+      sincosf(static_cast<float>(pos) * tab.freq[j], &s, &c);
+      out[i] = make_float2(c, s);
+    }
   }
 }
 

@@ -175,6 +175,7 @@ struct RepairArgs {
   const float* wk;         // [128]
   TokenGeometry geo;
   RopeTable tab;
+  const float2* rot;       // rotation table (kRotPositions x 64), or nullptr
   int N, H, R;
   float eps;
   const float* scales;     // [B*H][3]
@@ -261,7 +262,7 @@ __global__ void __launch_bounds__(kRepairThreads) vc_repair_kernel(const RepairA
     unpack8(*reinterpret_cast<const uint4*>(a.k + src), x);
     unpack8(*reinterpret_cast<const uint4*>(a.v + src), y);
     float cs[4], sn[4];
-    lane_rotation(a.geo, a.tab, n, sub, cs, sn);
+    lane_rotation(a.geo, a.tab, a.rot, n, sub, cs, sn);
     RotCoef kc;
     rot_coef(w, cs, sn, kc);
     norm_rope8_packed(x, kc, a.eps);  // all 32 lanes: the norm's shuffles
