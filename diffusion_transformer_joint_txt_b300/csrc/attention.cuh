@@ -17,22 +17,20 @@
 //   warp 8     TMA producer of the K ring
 //   warp 9     TMEM allocator and tcgen05.mma issuer (one elected lane)
 //   warp 10    TMA producer of both Q tiles and of the V ring
-//   warp 11    FP8 without repair blocks: the tcgen05.mma issuer of query
-//              tile 1 (warp 9 then issues for tile 0 only); idle otherwise
 // TMEM (512 columns): S_0 at 0, S_1 at 128, O_0 at 256, O_1 at 384.  BF16
 // (and the repair blocks): the softmax of a tile overwrites its S with P, and
 // the P.V MMA reads P straight from TMEM as its A operand.  FP8: P goes to a
 // shared-memory tile instead (mma_main_fp8), so that S_t takes the next
 // block's scores while the softmax still works on this one.
 //
-// The MMA issue order is  QK_0(0) QK_1(0) | PV_0(j) QK_0(j+1) PV_1(j) QK_1(j+1) | ...
-// so while the softmax of tile 0 works on S_0(j+1) the tensor core runs
-// PV_1(j) and QK_1(j+1), and the other way round: each tile's softmax hides
-// behind the other tile's two MMAs.  The MMAs of one
-// thread complete in issue order, which is what makes two things safe:
-// QK_t(j+1) overwrites the S_t columns that PV_t(j) reads P from, and the
-// commit that signals S_t(j+1) also means that PV_t(j) has landed in O_t, so
-// the softmax may rescale O_t as soon as it sees S_t(j+1).
+// BF16: the MMA issue order is  QK_0(0) QK_1(0) | PV_0(j) QK_0(j+1) PV_1(j)
+// QK_1(j+1) | ...  so while the softmax of tile 0 works on S_0(j+1) the
+// tensor core runs PV_1(j) and QK_1(j+1), and the other way round: each
+// tile's softmax hides behind the other tile's two MMAs.  The
+// MMAs of one thread complete in issue order, which is what makes two things
+// safe: QK_t(j+1) overwrites the S_t columns that PV_t(j) reads P from, and
+// the commit that signals S_t(j+1) also means that PV_t(j) has landed in O_t,
+// so the softmax may rescale O_t as soon as it sees S_t(j+1).
 //
 // Online softmax in log2 units with a deferred rescale (BF16): the running
 // max m only moves when a tile's max exceeds it by more than 2^8; until then
@@ -98,8 +96,7 @@ constexpr int CTA_ROWS = TILES * BM;
 constexpr int WARP_LOAD_K = 4 * TILES;          // 8: TMA producer of the K ring
 constexpr int WARP_MMA = WARP_LOAD_K + 1;       // 9: MMA issuer, TMEM owner
 constexpr int WARP_LOAD_V = WARP_MMA + 1;       // 10: TMA producer of Q and the V ring
-constexpr int WARP_MMA1 = WARP_LOAD_V + 1;      // 11: FP8 (no repair): MMA issuer of query tile 1
-constexpr int THREADS = 32 * (WARP_MMA1 + 1);   // 384
+constexpr int THREADS = 32 * (WARP_LOAD_V + 1); // 352
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t HALF = BM * 128;  // one SW128 block: 128 rows x 128 bytes = 16 KB
 
@@ -139,7 +136,6 @@ struct __align__(1024) Smem {
   uint64_t vrep_full, vrep_empty;      // REP: the repair V tile slot
   uint64_t qbf_free;                   // REP: last repair QK of both tiles done
   uint64_t mma_drain;
-  uint64_t mma_drain1;
   uint64_t never;  // nothing arrives here (forced-timeout debug path)
   uint32_t tmem_base;
   int abort;
@@ -396,19 +392,17 @@ __device__ __forceinline__ void issue_pv_smem_e4m3(uint32_t o_tmem, uint64_t pd,
 // of the next block is issued then, and runs while the softmax of this block
 // works; PV_t follows when P_t is in (p_full) and signals o_done.  Per block:
 //   QK_0(j+1) QK_1(j+1)  [after s_free_0(j), s_free_1(j)]   PV_0(j) PV_1(j)  [after p_full]
-// ph: s_full / p_full phases the repair blocks used before.  The issuing
-// thread serves query tiles T0 .. T1-1: both (with repair blocks), or one
-// each from two warps (split_issue: tile 0 from WARP_MMA, tile 1 from
-// WARP_MMA1), which halves the issue work that lands on the scheduler of
-// each of the two warps; every K and V stage then waits for both commits.
-template <bool REP, int T0, int T1>
+// ph: s_full / p_full phases the repair blocks used before.  One thread
+// issues for both tiles (two issuers, one per tile, each on its own warp,
+// measured the same: 4.047 against 4.052 ms on the CFG pair, interleaved).
+template <bool REP>
 __device__ __forceinline__ void mma_main_fp8(Smem<true>& sm, uint32_t tmem, int nkv, int ph, volatile int* ab,
                                              uint32_t* err) {
   constexpr uint32_t TILE = Traits<true>::TILE;
   constexpr int KST = Traits<true>::KST, VST = Traits<true>::VST;
   uint64_t qd[TILES], pd[TILES];
 #pragma unroll
-  for (int t = T0; t < T1; ++t) {
+  for (int t = 0; t < TILES; ++t) {
     qd[t] = sdesc_sw128(smem_u32(sm.q[t]), 16, 1024);
     pd[t] = sdesc_sw128(smem_u32(p_tile(sm, t)), 16, 1024);
   }
@@ -416,7 +410,7 @@ __device__ __forceinline__ void mma_main_fp8(Smem<true>& sm, uint32_t tmem, int 
   const uint64_t vd0 = sdesc_sw128(smem_u32(sm.v[0]), 16, 1024);
   if (!mbar_wait(&sm.k_full[0], 0, ab, err)) return;
 #pragma unroll
-  for (int t = T0; t < T1; ++t) {
+  for (int t = 0; t < TILES; ++t) {
     if (!mbar_wait(&sm.q_full[t], 0, ab, err)) return;
     tc_fence_after_sync();
     issue_qk<true>(tmem + col_s(t), qd[t], kd0);
@@ -429,7 +423,7 @@ __device__ __forceinline__ void mma_main_fp8(Smem<true>& sm, uint32_t tmem, int 
       const int ks = jn % KST;
       if (!mbar_wait(&sm.k_full[ks], (jn / KST) & 1, ab, err)) return;
 #pragma unroll
-      for (int t = T0; t < T1; ++t) {
+      for (int t = 0; t < TILES; ++t) {
         if (!mbar_wait(&sm.s_free[t], j & 1, ab, err)) return;
         tc_fence_after_sync();
         issue_qk<true>(tmem + col_s(t), qd[t], desc_at(kd0, ks * TILE));
@@ -440,7 +434,7 @@ __device__ __forceinline__ void mma_main_fp8(Smem<true>& sm, uint32_t tmem, int 
     const int vs = j % VST;
     if (!mbar_wait(&sm.v_full[vs], (j / VST) & 1, ab, err)) return;
 #pragma unroll
-    for (int t = T0; t < T1; ++t) {
+    for (int t = 0; t < TILES; ++t) {
       if (!mbar_wait(&sm.p_full[t], (j + ph) & 1, ab, err)) return;
       tc_fence_after_sync();
       issue_pv_smem_e4m3(tmem + col_o(t), pd[t], desc_at(vd0, vs * TILE), j + ph > 0);
@@ -449,100 +443,85 @@ __device__ __forceinline__ void mma_main_fp8(Smem<true>& sm, uint32_t tmem, int 
     mma_commit(&sm.v_empty[vs]);
   }
 #pragma unroll
-  for (int t = T0; t < T1; ++t) mma_commit(&sm.o_full[t]);
+  for (int t = 0; t < TILES; ++t) mma_commit(&sm.o_full[t]);
 }
 
-// The MMA issuer: QK_0(0) QK_1(0), then PV_0(j) QK_0(j+1) PV_1(j) QK_1(j+1)
-// for every j.  The whole warp runs this loop and one elected lane issues
-// (ptx.cuh).  One thread issues for both tiles: the fixed order is what
-// keeps the two tiles in turns (two independent issuers drift into step, and
-// then both softmaxes run at once and compete for the same schedulers).
-// REP: the repair blocks first (mma_repair); the main loop then continues
-// the s_full / p_full phases after them and accumulates onto their O.
-template <bool FP8, bool REP>
-__device__ __forceinline__ void mma_issuer(Smem<FP8>& sm, uint32_t tmem, int nkv, int nrep, volatile int* ab,
-                                           uint32_t* err) {
-  constexpr uint32_t TILE = Traits<FP8>::TILE;
-  constexpr int KST = Traits<FP8>::KST, VST = Traits<FP8>::VST;
-  // Tile descriptors: K-major SW128 (SBO = 8 rows x 128 B) for Q, K and the
-  // FP8 V^T; MN-major SW128 for the BF16 V (LBO = the other 64 head dims).
+// BF16 main loop of the issuing thread, for both query tiles in one fixed
+// order: QK_0(0) QK_1(0), then per block j
+//   PV_0(j) QK_0(j+1) PV_1(j) QK_1(j+1)  [each pair after p_full_t(j)]
+// Tile descriptors: K-major SW128 (SBO = 8 rows x 128 B) for Q and K,
+// MN-major SW128 for V (LBO = the other 64 head dims).
+// S_t and P_t share TMEM columns, so QK_t(j+1) follows PV_t(j) in this
+// thread's issue order, and the commit that signals S_t(j+1) also means that
+// PV_t(j) has landed in O_t.
+__device__ __forceinline__ void mma_main_bf16(Smem<false>& sm, uint32_t tmem, int nkv, volatile int* ab,
+                                              uint32_t* err) {
+  constexpr uint32_t TILE = Traits<false>::TILE;
+  constexpr int KST = Traits<false>::KST, VST = Traits<false>::VST;
   uint64_t qd[TILES];
 #pragma unroll
   for (int t = 0; t < TILES; ++t) qd[t] = sdesc_sw128(smem_u32(sm.q[t]), 16, 1024);
   const uint64_t kd0 = sdesc_sw128(smem_u32(sm.k[0]), 16, 1024);
-  const uint64_t vd0 = sdesc_sw128(smem_u32(sm.v[0]), FP8 ? 16 : HALF, 1024);
+  const uint64_t vd0 = sdesc_sw128(smem_u32(sm.v[0]), HALF, 1024);
+  if (!mbar_wait(&sm.k_full[0], 0, ab, err)) return;
+#pragma unroll
+  for (int t = 0; t < TILES; ++t) {
+    if (!mbar_wait(&sm.q_full[t], 0, ab, err)) return;
+    tc_fence_after_sync();
+    issue_qk<false>(tmem + col_s(t), qd[t], kd0);
+    mma_commit(&sm.s_full[t]);
+  }
+  mma_commit(&sm.k_empty[0]);
+  for (int j = 0; j < nkv; ++j) {
+    const int vs = j % VST;
+    if (!mbar_wait(&sm.v_full[vs], (j / VST) & 1, ab, err)) return;
+    const uint64_t vd = desc_at(vd0, vs * TILE);
+    const int jn = j + 1;
+    const int ks = jn % KST;
+    const uint64_t kd = desc_at(kd0, ks * TILE);
+#pragma unroll
+    for (int t = 0; t < TILES; ++t) {
+      if (!mbar_wait(&sm.p_full[t], j & 1, ab, err)) return;
+      tc_fence_after_sync();
+      issue_pv<false>(tmem + col_o(t), tmem + col_s(t), vd, j > 0);
+      if (t == TILES - 1) mma_commit(&sm.v_empty[vs]);
+      if (jn < nkv) {
+        if (t == 0) {
+          if (!mbar_wait(&sm.k_full[ks], (jn / KST) & 1, ab, err)) return;
+          tc_fence_after_sync();
+        }
+        // In issue order after PV_t(j), which read P_t from these columns.
+        issue_qk<false>(tmem + col_s(t), qd[t], kd);
+        mma_commit(&sm.s_full[t]);
+        if (t == TILES - 1) mma_commit(&sm.k_empty[ks]);
+      } else {
+        mma_commit(&sm.o_full[t]);
+      }
+    }
+  }
+}
+
+// The MMA issuer (the whole warp runs the loop, one elected lane issues:
+// ptx.cuh), for both tiles.  REP: the repair blocks first (mma_repair); the main loop then continues
+// the s_full / p_full phases after them and accumulates onto their O.
+template <bool FP8, bool REP>
+__device__ __forceinline__ void mma_issuer(Smem<FP8>& sm, uint32_t tmem, int nkv, int nrep, volatile int* ab,
+                                           uint32_t* err) {
   const int ph = REP ? nrep : 0;  // s_full / p_full phases the repair blocks used
   if (REP) nkv -= nrep;           // main-loop blocks
   do {
     if (REP && !mma_repair(sm, tmem, nrep, ab, err)) break;
-    if constexpr (FP8) {
-      if (nkv > 0) {
-        mma_main_fp8<REP, 0, REP ? TILES : 1>(sm, tmem, nkv, ph, ab, err);
-        break;
-      }
-    }
     if (nkv <= 0) {
 #pragma unroll
       for (int t = 0; t < TILES; ++t) mma_commit(&sm.o_full[t]);
       break;
     }
-    if (!mbar_wait(&sm.k_full[0], 0, ab, err)) break;
-    bool ok = true;
-#pragma unroll
-    for (int t = 0; t < TILES && ok; ++t) {
-      ok = mbar_wait(&sm.q_full[t], 0, ab, err);
-      if (!ok) break;
-      tc_fence_after_sync();
-      issue_qk<FP8>(tmem + col_s(t), qd[t], kd0);
-      mma_commit(&sm.s_full[t]);
-    }
-    if (!ok) break;
-    mma_commit(&sm.k_empty[0]);
-    for (int j = 0; j < nkv && ok; ++j) {
-      const int vs = j % VST;
-      if (!mbar_wait(&sm.v_full[vs], (j / VST) & 1, ab, err)) break;
-      const uint64_t vd = desc_at(vd0, vs * TILE);
-      const int jn = j + 1;
-      const int ks = jn % KST;
-      const uint64_t kd = desc_at(kd0, ks * TILE);
-#pragma unroll
-      for (int t = 0; t < TILES; ++t) {
-        ok = mbar_wait(&sm.p_full[t], (j + ph) & 1, ab, err);
-        if (!ok) break;
-        tc_fence_after_sync();
-        issue_pv<FP8>(tmem + col_o(t), tmem + col_s(t), vd, j + ph > 0);
-        if (t == TILES - 1) mma_commit(&sm.v_empty[vs]);
-        if (jn < nkv) {
-          if (t == 0) {
-            ok = mbar_wait(&sm.k_full[ks], (jn / KST) & 1, ab, err);
-            if (!ok) break;
-            tc_fence_after_sync();
-          }
-          // In issue order after PV_t(j), which read P_t from these columns.
-          issue_qk<FP8>(tmem + col_s(t), qd[t], kd);
-          mma_commit(&sm.s_full[t]);
-          if (t == TILES - 1) mma_commit(&sm.k_empty[ks]);
-        } else {
-          mma_commit(&sm.o_full[t]);
-        }
-      }
-    }
+    if constexpr (FP8) mma_main_fp8<REP>(sm, tmem, nkv, ph, ab, err);
+    else mma_main_bf16(sm, tmem, nkv, ab, err);
   } while (0);
   // Drain every MMA this thread issued before TMEM is released.
   mma_commit(&sm.mma_drain);
   mbar_drain(&sm.mma_drain, 0, err);
-}
-
-// FP8 without repair blocks: the MMAs of query tile 1 come from their own
-// warp (see mma_main_fp8); it drains them before TMEM is released.
-template <bool FP8, bool REP>
-__device__ __forceinline__ constexpr bool split_issue() { return FP8 && !REP; }
-
-__device__ __forceinline__ void mma_issuer_tile1(Smem<true>& sm, uint32_t tmem, int nkv, volatile int* ab,
-                                                 uint32_t* err) {
-  if (nkv > 0) mma_main_fp8<false, 1, TILES>(sm, tmem, nkv, 0, ab, err);
-  mma_commit(&sm.mma_drain1);
-  mbar_drain(&sm.mma_drain1, 0, err);
 }
 
 // Two E4M3 codes (round to nearest even, saturating) of a float pair, a in the low byte.
@@ -862,8 +841,7 @@ __device__ __forceinline__ void softmax_epilogue(Smem<FP8>& sm, uint32_t tmem, c
   // dims 64 (c / 2) .., row r at byte 128 r, its 16-byte chunk k at position
   // k ^ (r % 8).  BF16: the tile's own 32 KB Q buffer (its last QK completed
   // before the PV that signalled o_full).  FP8: the tile's own 16 KB Q buffer
-  // and its 16 KB P buffer, which only this tile's MMAs read (the K ring may
-  // still feed the other tile, whose MMAs can come from another thread).
+  // and its 16 KB P buffer, which only this tile's MMAs read.
   // Then one thread writes the two halves with TMA stores, which also clip
   // rows >= N: whole 128-byte rows instead of each thread's 16-byte pieces of
   // rows H x 256 bytes apart.
@@ -931,10 +909,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&sm.p_full[t], BM);
       mbar_init(&sm.o_full[t], 1);
     }
-    // a K / V stage is free once every issuing thread has committed it
-    constexpr int issuers = split_issue<FP8, REP>() ? 2 : 1;
-    for (int s = 0; s < KST; ++s) { mbar_init(&sm.k_full[s], 1); mbar_init(&sm.k_empty[s], issuers); }
-    for (int s = 0; s < VST; ++s) { mbar_init(&sm.v_full[s], 1); mbar_init(&sm.v_empty[s], issuers); }
+    for (int s = 0; s < KST; ++s) { mbar_init(&sm.k_full[s], 1); mbar_init(&sm.k_empty[s], 1); }
+    for (int s = 0; s < VST; ++s) { mbar_init(&sm.v_full[s], 1); mbar_init(&sm.v_empty[s], 1); }
     for (int t = 0; t < TILES; ++t) {
       mbar_init(&sm.qbf_full[t], BM);
       mbar_init(&sm.s_free[t], BM);
@@ -946,7 +922,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(&sm.vrep_empty, 1);
     mbar_init(&sm.qbf_free, 1);
     mbar_init(&sm.mma_drain, 1);
-    mbar_init(&sm.mma_drain1, 1);
     mbar_init(&sm.never, 1);
     sm.abort = 0;
     fence_mbarrier_init();
@@ -995,11 +970,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncwarp();
   } else if (warp == WARP_MMA) {
     if (!*ab) mma_issuer<FP8, REP>(sm, tmem, nkv, prm.nrep, ab, prm.err);  // the whole warp: see mma_commit
-    __syncwarp();
-  } else if (warp == WARP_MMA1) {
-    if constexpr (split_issue<FP8, REP>()) {
-      if (!*ab) mma_issuer_tile1(sm, tmem, nkv, ab, prm.err);
-    }
     __syncwarp();
   } else {
     const int t = warp >> 2;  // query tile of this warpgroup
