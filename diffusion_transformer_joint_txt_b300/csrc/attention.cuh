@@ -876,7 +876,7 @@ __device__ __forceinline__ void softmax_epilogue(Smem<FP8>& sm, uint32_t tmem, c
     tma_store_4d(tm_o, smem_u32(stage[0]), 0, h, row0, b);  // rows >= N are clipped
     tma_store_4d(tm_o, smem_u32(stage[1]), 64, h, row0, b);
     bulk_commit();
-    bulk_wait_all();
+    bulk_wait_read_all();  // the staging buffer may go; the writes complete with the grid
   }
 }
 

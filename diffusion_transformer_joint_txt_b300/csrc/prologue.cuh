@@ -173,7 +173,7 @@ __device__ __forceinline__ void norm_rope8_packed(float (&x)[8], const RotCoef& 
 // then normalises, rotates and stores the head rows of each part (a
 // half-warp per row, read from shared memory, written head-major).
 constexpr int kProMaxWarps = 16;                     // warps per block at most (any output policy)
-constexpr int kProStages = 2;                        // parts per warp ring
+constexpr int kProStages = 2;                        // parts per warp ring of whole tokens (Bf16Rows)
 constexpr int kProSmemBytes = 220 * 1024;            // rings and the output policy's scratch
 constexpr int kProRingBytes = 192 * 1024;            // bounds H: one warp's two whole-token stages fit
 constexpr int kProRowBytes = 2 * kHeadDim * 2;       // one head row of q and one of k
@@ -182,11 +182,17 @@ constexpr int kProMaxHeads = kProRingBytes / (kProStages * kProRowBytes);  // 19
 // Heads per part when a token is cut into `parts` parts.
 __host__ __device__ constexpr int prologue_part_heads(int H, int parts) { return (H + parts - 1) / parts; }
 
-// Warps per block (1 .. max_warps) for H heads in `parts` parts and
-// `scratch` bytes of policy scratch per warp (H <= kProMaxHeads).
-__host__ __device__ constexpr int prologue_warps(int H, int parts, int max_warps, int scratch) {
-  return kProSmemBytes / (kProStages * kProRowBytes * prologue_part_heads(H, parts) + scratch) < max_warps
-             ? kProSmemBytes / (kProStages * kProRowBytes * prologue_part_heads(H, parts) + scratch)
+// Shared memory of one warp: its ring of `stages` parts and its scratch.
+__host__ __device__ constexpr int prologue_warp_bytes(int H, int parts, int stages, int scratch) {
+  return stages * kProRowBytes * prologue_part_heads(H, parts) + scratch;
+}
+
+// Warps per block (1 .. max_warps) for H heads in `parts` parts, rings of
+// `stages` parts and `scratch` bytes of policy scratch per warp (H <=
+// kProMaxHeads: every policy fits one warp then, checked in the kernel).
+__host__ __device__ constexpr int prologue_warps(int H, int parts, int stages, int max_warps, int scratch) {
+  return kProSmemBytes / prologue_warp_bytes(H, parts, stages, scratch) < max_warps
+             ? kProSmemBytes / prologue_warp_bytes(H, parts, stages, scratch)
              : max_warps;
 }
 
@@ -202,13 +208,15 @@ __host__ __device__ constexpr int prologue_warps(int H, int parts, int max_warps
 //                               past the part's last head has valid == false,
 //                               zeros in x, and must store nothing
 //   finish()                    once per warp (all lanes), after the last token
-// and its stream shape: kParts parts per token, kWarps warps per block at
-// most (the rings' shared memory may allow fewer), kPairs head pairs a warp
+// and its stream shape: kParts parts per token, kStages parts per warp
+// ring, kWarps warps per block at most (the rings' shared memory may allow
+// fewer), kPairs head pairs a warp
 // works on at a time.
 // The BF16 policy writes Q', K' bf16 [B, H, N, 128].  Whole tokens and eight
 // warps: with twice the bytes written per row, more and smaller parts lost.
 struct Bf16Rows {
   static constexpr int kParts = 1;
+  static constexpr int kStages = kProStages;
   static constexpr int kWarps = 8;
   static constexpr int kPairs = 2;
   __nv_bfloat16* qn;
@@ -238,26 +246,29 @@ struct StreamArgs {
 // Launch shape of the stream kernel for output policy Out and H heads.
 template <class Out>
 __host__ __device__ constexpr int stream_warps(int H) {
-  return prologue_warps(H, Out::kParts, Out::kWarps, Out::warp_scratch(H));
+  return prologue_warps(H, Out::kParts, Out::kStages, Out::kWarps, Out::warp_scratch(H));
 }
 template <class Out>
 __host__ __device__ constexpr size_t stream_smem(int H) {
   return static_cast<size_t>(stream_warps<Out>(H)) *
-         (kProStages * kProRowBytes * prologue_part_heads(H, Out::kParts) + Out::warp_scratch(H));
+         prologue_warp_bytes(H, Out::kParts, Out::kStages, Out::warp_scratch(H));
 }
 
 template <class Out>
 __global__ void __launch_bounds__(32 * Out::kWarps, 1) qk_norm_rope_kernel(const StreamArgs a, Out out) {
   static_assert(Out::kWarps <= kProMaxWarps, "barrier array");
+  static_assert(prologue_warp_bytes(kProMaxHeads, Out::kParts, Out::kStages, Out::warp_scratch(kProMaxHeads)) <=
+                    kProSmemBytes,
+                "one warp's ring and scratch fit at the largest head count");
   // Every CTA of this grid is resident at once (grid <= SMs, one block per
   // SM): the attention kernel after it may be scheduled now and set up on
   // SMs whose block has finished.
   griddep_launch_dependents();
   extern __shared__ __align__(128) uint8_t ring[];  // [W][S][q rows | k rows] of one part; then Out's scratch
-  __shared__ uint64_t full[Out::kWarps][kProStages];  // per warp: stage s holds a part
+  __shared__ uint64_t full[Out::kWarps][Out::kStages];  // per warp: stage s holds a part
   __shared__ int abort_flag;
   const int W = blockDim.x >> 5;
-  constexpr int S = kProStages;
+  constexpr int S = Out::kStages;
   const int H = a.H, N = a.N;
   const int hs = Out::kParts == 1 ? H : prologue_part_heads(H, Out::kParts);
   const int P = Out::kParts == 1 ? 1 : (H + hs - 1) / hs;  // parts of a token (<= kParts, none empty)

@@ -60,6 +60,7 @@ __device__ __forceinline__ uint2 quant8(const float (&x)[8], float inv) {
 // token.
 struct AmaxRows {
   static constexpr int kParts = 2;  // half tokens, twelve warps: more warps to hide latency, as
+  static constexpr int kStages = 2;
   static constexpr int kWarps = 12; // nothing (or only codes, below) is written per row
   static constexpr int kPairs = 3;  // six independent rows per half-warp
   uint32_t* amax;  // [B*H][3]
@@ -129,6 +130,7 @@ __device__ __forceinline__ float sq_error8(const float (&x)[8], uint2 c, float s
 // half-warp that holds the row in a fixed order.
 struct E4m3Rows {
   static constexpr int kParts = 2;
+  static constexpr int kStages = 2;
   static constexpr int kWarps = 12;
   static constexpr int kPairs = 3;
   uint8_t* q8;
