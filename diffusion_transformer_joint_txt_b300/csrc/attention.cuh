@@ -102,6 +102,15 @@ constexpr uint32_t HALF = BM * 128;  // one SW128 block: 128 rows x 128 bytes = 
 
 __host__ __device__ constexpr uint32_t col_s(int t) { return 128u * t; }        // S_t / P_t
 __host__ __device__ constexpr uint32_t col_o(int t) { return 256u + 128u * t; } // O_t
+__host__ __device__ constexpr uint32_t col_l(int t) { return 128u + 32u * t; }  // l_t (rowsum_mma): 16 used
+
+// FP8 without repair blocks: the row sums l come from the tensor core (P
+// times a tile of ones, into 16 TMEM columns per tile that O's rescale also
+// scales), and the two tiles take turns in one S region (col_s(0)) to make
+// room for them.  The repair instance keeps its register sums.
+constexpr bool kMmaRowSum = true;
+template <bool FP8, bool REP>
+__host__ __device__ constexpr bool rowsum_mma() { return FP8 && !REP && kMmaRowSum; }
 
 template <bool FP8>
 struct Traits {
@@ -204,6 +213,10 @@ __device__ __forceinline__ uint8_t* vrep_tile(Smem<FP8>& sm) { return &sm.rep[FP
 // consumed before the E4M3 blocks begin.
 template <bool FP8>
 __device__ __forceinline__ uint8_t* p_tile(Smem<FP8>& sm, int t) { return &sm.rep[0][0] + t * HALF; }
+// rowsum_mma: 16 rows x 128 keys of E4M3 1.0 (0x38; 2 KB, every byte the same,
+// so its swizzle does not matter) -- the repair V region, unused there.
+template <bool FP8>
+__device__ __forceinline__ uint8_t* ones_tile(Smem<FP8>& sm) { return &sm.rep[FP8 ? 1 : 0][0]; }
 
 // K ring producer: K_j into stage j % KST once both tiles' QK of its
 // previous occupant have completed.  REP: the repair K tiles too (into their
@@ -387,6 +400,86 @@ __device__ __forceinline__ void issue_pv_smem_e4m3(uint32_t o_tmem, uint64_t pd,
     mma_e4m3_ss(o_tmem, desc_at(pd, kk * 32), desc_at(vd, kk * 32), ID, (accumulate || kk > 0) ? 1u : 0u);
 }
 
+// l_t (+)= P_t 1: the row sums of P by the tensor core, N = 16 (16 equal
+// columns; the softmax reads the first), 4 MMAs of 128 x 16 x 32.
+__device__ __forceinline__ void issue_l_e4m3(uint32_t l_tmem, uint64_t pd, uint64_t od, bool accumulate) {
+  constexpr uint32_t ID = idesc_e4m3(BM, 16, false);
+#pragma unroll
+  for (int kk = 0; kk < BN / 32; ++kk)
+    mma_e4m3_ss(l_tmem, desc_at(pd, kk * 32), desc_at(od, kk * 32), ID, (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// FP8 main loop with the row sums on the tensor core (rowsum_mma): both
+// tiles' scores go through the one S region in turns, so per block j
+//   PV_0(j-1) l_0   [after p_full_0(j-1)]
+//   QK_1(j)         [after s_free_0(j): tile 0 has read S_0(j)]
+//   PV_1(j-1) l_1   [after p_full_1(j-1)]
+//   QK_0(j+1)       [after s_free_1(j): tile 1 has read S_1(j)]
+// -- the order in which those events come when tile 1 runs a little behind
+// tile 0, which this chain itself makes it do.  o_done_t follows each PV_t
+// with its row sum.
+__device__ __forceinline__ void mma_main_fp8_rs(Smem<true>& sm, uint32_t tmem, int nkv, volatile int* ab,
+                                                uint32_t* err) {
+  constexpr uint32_t TILE = Traits<true>::TILE;
+  constexpr int KST = Traits<true>::KST, VST = Traits<true>::VST;
+  uint64_t qd[TILES], pd[TILES];
+#pragma unroll
+  for (int t = 0; t < TILES; ++t) {
+    qd[t] = sdesc_sw128(smem_u32(sm.q[t]), 16, 1024);
+    pd[t] = sdesc_sw128(smem_u32(p_tile(sm, t)), 16, 1024);
+  }
+  const uint64_t kd0 = sdesc_sw128(smem_u32(sm.k[0]), 16, 1024);
+  const uint64_t vd0 = sdesc_sw128(smem_u32(sm.v[0]), 16, 1024);
+  const uint64_t od = sdesc_sw128(smem_u32(ones_tile(sm)), 16, 1024);
+  const uint32_t s_tmem = tmem + col_s(0);
+  // PV_t(j) and l_t after P_t(j) is in (V_j must be in)
+  auto pv = [&](int t, int j) -> bool {
+    if (!mbar_wait(&sm.p_full[t], j & 1, ab, err)) return false;
+    tc_fence_after_sync();
+    issue_pv_smem_e4m3(tmem + col_o(t), pd[t], desc_at(vd0, (j % VST) * TILE), j > 0);
+    issue_l_e4m3(tmem + col_l(t), pd[t], od, j > 0);
+    mma_commit(&sm.o_done[t]);
+    return true;
+  };
+  if (!mbar_wait(&sm.k_full[0], 0, ab, err)) return;
+  if (!mbar_wait(&sm.q_full[0], 0, ab, err)) return;
+  tc_fence_after_sync();
+  issue_qk<true>(s_tmem, qd[0], kd0);
+  mma_commit(&sm.s_full[0]);
+  for (int j = 0; j < nkv; ++j) {
+    const int ks = j % KST;
+    if (j > 0) {
+      if (!mbar_wait(&sm.v_full[(j - 1) % VST], ((j - 1) / VST) & 1, ab, err)) return;
+      if (!pv(0, j - 1)) return;
+    }
+    if (j == 0 && !mbar_wait(&sm.q_full[1], 0, ab, err)) return;
+    if (!mbar_wait(&sm.s_free[0], j & 1, ab, err)) return;
+    tc_fence_after_sync();
+    issue_qk<true>(s_tmem, qd[1], desc_at(kd0, ks * TILE));
+    mma_commit(&sm.s_full[1]);
+    mma_commit(&sm.k_empty[ks]);
+    if (j > 0) {
+      if (!pv(1, j - 1)) return;
+      mma_commit(&sm.v_empty[(j - 1) % VST]);
+    }
+    if (j + 1 < nkv) {
+      const int kn = (j + 1) % KST;
+      if (!mbar_wait(&sm.k_full[kn], ((j + 1) / KST) & 1, ab, err)) return;
+      if (!mbar_wait(&sm.s_free[1], j & 1, ab, err)) return;
+      tc_fence_after_sync();
+      issue_qk<true>(s_tmem, qd[0], desc_at(kd0, kn * TILE));
+      mma_commit(&sm.s_full[0]);
+    }
+  }
+  const int jl = nkv - 1;
+  if (!mbar_wait(&sm.v_full[jl % VST], (jl / VST) & 1, ab, err)) return;
+  if (!pv(0, jl)) return;
+  mma_commit(&sm.o_full[0]);
+  if (!pv(1, jl)) return;
+  mma_commit(&sm.v_empty[jl % VST]);
+  mma_commit(&sm.o_full[1]);
+}
+
 // FP8 main loop of the MMA thread.  P goes through shared memory, so S_t's
 // TMEM columns are free as soon as the softmax has loaded them (s_free): QK_t
 // of the next block is issued then, and runs while the softmax of this block
@@ -516,7 +609,8 @@ __device__ __forceinline__ void mma_issuer(Smem<FP8>& sm, uint32_t tmem, int nkv
       for (int t = 0; t < TILES; ++t) mma_commit(&sm.o_full[t]);
       break;
     }
-    if constexpr (FP8) mma_main_fp8<REP>(sm, tmem, nkv, ph, ab, err);
+    if constexpr (rowsum_mma<FP8, REP>()) mma_main_fp8_rs(sm, tmem, nkv, ab, err);
+    else if constexpr (FP8) mma_main_fp8<REP>(sm, tmem, nkv, ph, ab, err);
     else mma_main_bf16(sm, tmem, nkv, ab, err);
   } while (0);
   // Drain every MMA this thread issued before TMEM is released.
@@ -686,10 +780,12 @@ __device__ __forceinline__ bool softmax_block(Smem<FP8>& sm, int t, uint32_t s_a
 // and before it writes P, or rescales O, it waits until the PV of the
 // previous block (jm - 1), which read the same P buffer and wrote O, has
 // completed (o_done).  jm: the block's index in the main loop; phase: its
-// s_full / p_full phase.
+// s_full / p_full phase.  RS (rowsum_mma): no row sum here -- the tensor core
+// adds P into l_addr's column, which the rescale scales with O; l is unused.
+template <bool RS>
 __device__ __forceinline__ bool softmax_block_fp8(Smem<true>& sm, int t, int r, uint32_t s_addr, uint32_t o_addr,
-                                                  uint32_t phase, int jm, int valid, bool has_o, float sl2, float& m,
-                                                  float& l, volatile int* ab, uint32_t* err) {
+                                                  uint32_t l_addr, uint32_t phase, int jm, int valid, bool has_o,
+                                                  float sl2, float& m, float& l, volatile int* ab, uint32_t* err) {
   constexpr float kPBias = 8.f;  // P = E4M3 of 256 p: folded into the exponent, cancels against l
   constexpr float kRescale = Traits<true>::RESCALE;
   bool ok = mbar_wait(&sm.s_full[t], phase, ab, err);
@@ -724,29 +820,39 @@ __device__ __forceinline__ bool softmax_block_fp8(Smem<true>& sm, int t, int r, 
   // values of the codes in eight packed f16 accumulators (each at most 8
   // values <= 256), widened to fp32 once per block.
   uint32_t pk[32];
-  __half2 hs[8];
+  if constexpr (RS) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) hs[i] = __float2half2_rn(0.f);
+    for (int i = 0; i < 32; ++i) {
+      float x0, x1, x2, x3;
+      fma2(x0, x1, __uint_as_float(s[4 * i]), __uint_as_float(s[4 * i + 1]), sl2, sl2, nm, nm);
+      fma2(x2, x3, __uint_as_float(s[4 * i + 2]), __uint_as_float(s[4 * i + 3]), sl2, sl2, nm, nm);
+      pk[i] = e4m3x2(ex2_approx(x0), ex2_approx(x1)) | (e4m3x2(ex2_approx(x2), ex2_approx(x3)) << 16);
+    }
+  } else {
+    __half2 hs[8];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    float x0, x1, x2, x3;
-    fma2(x0, x1, __uint_as_float(s[4 * i]), __uint_as_float(s[4 * i + 1]), sl2, sl2, nm, nm);
-    fma2(x2, x3, __uint_as_float(s[4 * i + 2]), __uint_as_float(s[4 * i + 3]), sl2, sl2, nm, nm);
-    const uint32_t lo = e4m3x2(ex2_approx(x0), ex2_approx(x1));
-    const uint32_t hi = e4m3x2(ex2_approx(x2), ex2_approx(x3));
-    pk[i] = lo | (hi << 16);
-    hs[i & 7] = __hadd2(hs[i & 7], __hadd2(e4m3x2_value(lo), e4m3x2_value(hi)));
+    for (int i = 0; i < 8; ++i) hs[i] = __float2half2_rn(0.f);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      float x0, x1, x2, x3;
+      fma2(x0, x1, __uint_as_float(s[4 * i]), __uint_as_float(s[4 * i + 1]), sl2, sl2, nm, nm);
+      fma2(x2, x3, __uint_as_float(s[4 * i + 2]), __uint_as_float(s[4 * i + 3]), sl2, sl2, nm, nm);
+      const uint32_t lo = e4m3x2(ex2_approx(x0), ex2_approx(x1));
+      const uint32_t hi = e4m3x2(ex2_approx(x2), ex2_approx(x3));
+      pk[i] = lo | (hi << 16);
+      hs[i & 7] = __hadd2(hs[i & 7], __hadd2(e4m3x2_value(lo), e4m3x2_value(hi)));
+    }
+    float sum[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float2 f = __half22float2(hs[i]);
+      sum[i] = f.x + f.y;
+    }
+    add2(sum[0], sum[1], sum[2], sum[3]);
+    add2(sum[4], sum[5], sum[6], sum[7]);
+    add2(sum[0], sum[1], sum[4], sum[5]);
+    l = l * alpha + (sum[0] + sum[1]);
   }
-  float sum[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float2 f = __half22float2(hs[i]);
-    sum[i] = f.x + f.y;
-  }
-  add2(sum[0], sum[1], sum[2], sum[3]);
-  add2(sum[4], sum[5], sum[6], sum[7]);
-  add2(sum[0], sum[1], sum[4], sum[5]);
-  l = l * alpha + (sum[0] + sum[1]);
   // the previous block's PV has read the P buffer and written O
   if (jm > 0) {
     ok = mbar_wait(&sm.o_done[t], (jm - 1) & 1, ab, err);
@@ -771,6 +877,11 @@ __device__ __forceinline__ bool softmax_block_fp8(Smem<true>& sm, int t, int r, 
       for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
       tmem_st32(o_addr + c * 32, o);
     }
+    if (RS) {
+      uint32_t lv = tmem_ld1(l_addr);
+      tmem_ld_wait(lv);
+      tmem_st1(l_addr, __float_as_uint(__uint_as_float(lv) * alpha));
+    }
     tmem_st_wait();
   }
   m = m_new;
@@ -788,8 +899,10 @@ __device__ __forceinline__ void softmax_epilogue(Smem<FP8>& sm, uint32_t tmem, c
                                                  const CUtensorMap* tm_o) {
   const int r = threadIdx.x & (BM - 1);
   const uint32_t lane_base = static_cast<uint32_t>(r & ~31) << 16;  // TMEM lanes of this warp
-  const uint32_t s_addr = tmem + lane_base + col_s(t);
+  constexpr bool RS = rowsum_mma<FP8, REP>();
+  const uint32_t s_addr = tmem + lane_base + col_s(RS ? 0 : t);  // RS: one S region, in turns
   const uint32_t o_addr = tmem + lane_base + col_o(t);
+  const uint32_t l_addr = tmem + lane_base + col_l(t);
   const int nrep = REP ? prm.nrep : 0;
   const int nmain = nkv - nrep;
   float sl2 = prm.scale_log2;
@@ -821,9 +934,16 @@ __device__ __forceinline__ void softmax_epilogue(Smem<FP8>& sm, uint32_t tmem, c
                                      j > 0, sl2, m, l, ab, prm.err, (e >> (14 + t)) & 1u);
     }
   } else if constexpr (FP8) {
+    if (RS && t == 0) {
+      // the ones tile of the row-sum MMAs: row r's 16 bytes; the issuer first
+      // reads it after this tile's p_full of block 0, which follows the fence
+      *reinterpret_cast<uint4*>(ones_tile(sm) + r * 16) = make_uint4(0x38383838u, 0x38383838u, 0x38383838u,
+                                                                     0x38383838u);
+      fence_proxy_async_smem();
+    }
     for (int j = 0; j < nmain && ok; ++j)
-      ok = softmax_block_fp8(sm, t, r, s_addr, o_addr, (j + nrep) & 1, j, prm.main_keys - j * BN, j + nrep > 0, sl2,
-                             m, l, ab, prm.err);
+      ok = softmax_block_fp8<RS>(sm, t, r, s_addr, o_addr, l_addr, (j + nrep) & 1, j, prm.main_keys - j * BN,
+                                 j + nrep > 0, sl2, m, l, ab, prm.err);
   } else {
     for (int j = 0; j < nmain && ok; ++j)
       ok = softmax_block<FP8, FP8>(sm, t, s_addr, o_addr, (j + nrep) & 1, prm.main_keys - j * BN, j + nrep > 0,
@@ -835,6 +955,11 @@ __device__ __forceinline__ void softmax_epilogue(Smem<FP8>& sm, uint32_t tmem, c
   }
   if (!ok) return;
   tc_fence_after_sync();
+  if constexpr (RS) {  // the tensor core's row sum
+    uint32_t lv = tmem_ld1(l_addr);
+    tmem_ld_wait(lv);
+    l = __uint_as_float(lv);
+  }
   const float inv_l = out_scale / l;
   // O tile (bf16, 32 KB) -> shared memory that no MMA or copy touches any
   // more, in the SW128 layout of the out tensor map: half c / 2 holds head
