@@ -103,12 +103,16 @@ constexpr uint32_t HALF = BM * 128;  // one SW128 block: 128 rows x 128 bytes = 
 __host__ __device__ constexpr uint32_t col_s(int t) { return 128u * t; }        // S_t / P_t
 __host__ __device__ constexpr uint32_t col_o(int t) { return 256u + 128u * t; } // O_t
 __host__ __device__ constexpr uint32_t col_l(int t) { return 128u + 32u * t; }  // l_t (rowsum_mma): 16 used
+__host__ __device__ constexpr uint32_t col_p(int t) { return 192u + 32u * t; }  // P_t (rowsum_mma, kPInTmem)
 
 // FP8 without repair blocks: the row sums l come from the tensor core (P
 // times a tile of ones, into 16 TMEM columns per tile that O's rescale also
 // scales), and the two tiles take turns in one S region (col_s(0)) to make
 // room for them.  The repair instance keeps its register sums.
 constexpr bool kMmaRowSum = true;
+// ... and P_t then lives in TMEM too (32 columns, four E4M3 codes per column),
+// written by one tcgen05.st, the A operand of P.V and of the row sum.
+constexpr bool kPInTmem = true;
 template <bool FP8, bool REP>
 __host__ __device__ constexpr bool rowsum_mma() { return FP8 && !REP && kMmaRowSum; }
 
@@ -401,12 +405,18 @@ __device__ __forceinline__ void issue_pv_smem_e4m3(uint32_t o_tmem, uint64_t pd,
 }
 
 // l_t (+)= P_t 1: the row sums of P by the tensor core, N = 16 (16 equal
-// columns; the softmax reads the first), 4 MMAs of 128 x 16 x 32.
-__device__ __forceinline__ void issue_l_e4m3(uint32_t l_tmem, uint64_t pd, uint64_t od, bool accumulate) {
+// columns; the softmax reads the first), 4 MMAs of 128 x 16 x 32, P from
+// shared memory (pd) or from TMEM (p_tmem, kPInTmem).
+__device__ __forceinline__ void issue_l_e4m3(uint32_t l_tmem, uint64_t pd, uint32_t p_tmem, uint64_t od,
+                                             bool accumulate) {
   constexpr uint32_t ID = idesc_e4m3(BM, 16, false);
 #pragma unroll
-  for (int kk = 0; kk < BN / 32; ++kk)
-    mma_e4m3_ss(l_tmem, desc_at(pd, kk * 32), desc_at(od, kk * 32), ID, (accumulate || kk > 0) ? 1u : 0u);
+  for (int kk = 0; kk < BN / 32; ++kk) {
+    if (kPInTmem)
+      mma_e4m3_ts(l_tmem, p_tmem + kk * 8, desc_at(od, kk * 32), ID, (accumulate || kk > 0) ? 1u : 0u);
+    else
+      mma_e4m3_ss(l_tmem, desc_at(pd, kk * 32), desc_at(od, kk * 32), ID, (accumulate || kk > 0) ? 1u : 0u);
+  }
 }
 
 // FP8 main loop with the row sums on the tensor core (rowsum_mma): both
@@ -436,8 +446,11 @@ __device__ __forceinline__ void mma_main_fp8_rs(Smem<true>& sm, uint32_t tmem, i
   auto pv = [&](int t, int j) -> bool {
     if (!mbar_wait(&sm.p_full[t], j & 1, ab, err)) return false;
     tc_fence_after_sync();
-    issue_pv_smem_e4m3(tmem + col_o(t), pd[t], desc_at(vd0, (j % VST) * TILE), j > 0);
-    issue_l_e4m3(tmem + col_l(t), pd[t], od, j > 0);
+    if (kPInTmem)
+      issue_pv<true>(tmem + col_o(t), tmem + col_p(t), desc_at(vd0, (j % VST) * TILE), j > 0);
+    else
+      issue_pv_smem_e4m3(tmem + col_o(t), pd[t], desc_at(vd0, (j % VST) * TILE), j > 0);
+    issue_l_e4m3(tmem + col_l(t), pd[t], tmem + col_p(t), od, j > 0);
     mma_commit(&sm.o_done[t]);
     return true;
   };
@@ -784,7 +797,8 @@ __device__ __forceinline__ bool softmax_block(Smem<FP8>& sm, int t, uint32_t s_a
 // adds P into l_addr's column, which the rescale scales with O; l is unused.
 template <bool RS>
 __device__ __forceinline__ bool softmax_block_fp8(Smem<true>& sm, int t, int r, uint32_t s_addr, uint32_t o_addr,
-                                                  uint32_t l_addr, uint32_t phase, int jm, int valid, bool has_o,
+                                                  uint32_t l_addr, uint32_t p_addr, uint32_t phase, int jm,
+                                                  int valid, bool has_o,
                                                   float sl2, float& m, float& l, volatile int* ab, uint32_t* err) {
   constexpr float kPBias = 8.f;  // P = E4M3 of 256 p: folded into the exponent, cancels against l
   constexpr float kRescale = Traits<true>::RESCALE;
@@ -859,14 +873,18 @@ __device__ __forceinline__ bool softmax_block_fp8(Smem<true>& sm, int t, int r, 
     if (__any_sync(0xFFFFFFFFu, !ok)) return false;
     tc_fence_after_sync();
   }
-  // P -> row r of the tile's K-major SW128 buffer: 16-byte chunk c (keys
-  // 16c .. 16c+15) at chunk position c ^ (r % 8)
-  uint8_t* prow = p_tile(sm, t) + r * 128;
+  if (RS && kPInTmem) {
+    tmem_st32(p_addr, pk);  // waited for (tcgen05.wait::st) before p_full below
+  } else {
+    // P -> row r of the tile's K-major SW128 buffer: 16-byte chunk c (keys
+    // 16c .. 16c+15) at chunk position c ^ (r % 8)
+    uint8_t* prow = p_tile(sm, t) + r * 128;
 #pragma unroll
-  for (int c = 0; c < 8; ++c)
-    *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
-                                                                          pk[4 * c + 3]);
-  fence_proxy_async_smem();  // generic-proxy writes, read by the MMA (async proxy)
+    for (int c = 0; c < 8; ++c)
+      *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
+                                                                            pk[4 * c + 3]);
+    fence_proxy_async_smem();  // generic-proxy writes, read by the MMA (async proxy)
+  }
   if (rescale && has_o) {
 #pragma unroll
     for (int c = 0; c < HD / 32; ++c) {
@@ -882,8 +900,8 @@ __device__ __forceinline__ bool softmax_block_fp8(Smem<true>& sm, int t, int r, 
       tmem_ld_wait(lv);
       tmem_st1(l_addr, __float_as_uint(__uint_as_float(lv) * alpha));
     }
-    tmem_st_wait();
   }
+  if ((rescale && has_o) || (RS && kPInTmem)) tmem_st_wait();
   m = m_new;
   tc_fence_before_sync();
   mbar_arrive(&sm.p_full[t]);
@@ -903,6 +921,7 @@ __device__ __forceinline__ void softmax_epilogue(Smem<FP8>& sm, uint32_t tmem, c
   const uint32_t s_addr = tmem + lane_base + col_s(RS ? 0 : t);  // RS: one S region, in turns
   const uint32_t o_addr = tmem + lane_base + col_o(t);
   const uint32_t l_addr = tmem + lane_base + col_l(t);
+  const uint32_t p_addr = tmem + lane_base + col_p(t);
   const int nrep = REP ? prm.nrep : 0;
   const int nmain = nkv - nrep;
   float sl2 = prm.scale_log2;
@@ -942,8 +961,8 @@ __device__ __forceinline__ void softmax_epilogue(Smem<FP8>& sm, uint32_t tmem, c
       fence_proxy_async_smem();
     }
     for (int j = 0; j < nmain && ok; ++j)
-      ok = softmax_block_fp8<RS>(sm, t, r, s_addr, o_addr, l_addr, (j + nrep) & 1, j, prm.main_keys - j * BN,
-                                 j + nrep > 0, sl2, m, l, ab, prm.err);
+      ok = softmax_block_fp8<RS>(sm, t, r, s_addr, o_addr, l_addr, p_addr, (j + nrep) & 1, j,
+                                 prm.main_keys - j * BN, j + nrep > 0, sl2, m, l, ab, prm.err);
   } else {
     for (int j = 0; j < nmain && ok; ++j)
       ok = softmax_block<FP8, FP8>(sm, t, s_addr, o_addr, (j + nrep) & 1, prm.main_keys - j * BN, j + nrep > 0,
