@@ -48,14 +48,13 @@
 // FP8: Q', K' are E4M3 codes [B, H, N, 128] and V is E4M3 transposed
 // [B, H, 128, Npad] (kind::f8f6f4, K = 32 per MMA).  A 128 x 128 tile is one
 // 16 KB SW128 block, K-major for all three (for V^T the keys are the K
-// dimension of P.V).  P is E4M3 of 256 p (a K-major SW128 tile in shared
-// memory); the row sum l adds the values the codes stand for, so that
-// O = sum p~ v / sum p~ is a convex combination of the V rows whatever the
-// rounding of P.  Scores are
-// scaled by s_q s_k and the output by s_v (per-(b, h) scales).  The FP8
-// softmax sums the P values in packed f16 (E4M3 values are exact in f16):
-// decoding every code back to fp32 for the sum cost it a sixth of its
-// throughput.
+// dimension of P.V).  P is E4M3 of 256 p; the row sum l adds the values the
+// codes stand for, so that O = sum p~ v / sum p~ is a convex combination of
+// the V rows whatever the rounding of P.  Scores are scaled by s_q s_k and
+// the output by s_v (per-(b, h) scales).  The plain FP8 kernel keeps P in
+// TMEM and has the tensor core sum it (rowsum_mma: P times a tile of ones);
+// the VC instance keeps P in a shared-memory tile and sums the codes in
+// packed f16 (E4M3 values are exact in f16).
 //
 // VC-Attention repair (REP, FP8 only; vc_repair.cuh selects the tokens):
 // the CTA first runs ceil(R / 128) repair blocks in BF16 -- K_rep = k' / s_k
