@@ -104,16 +104,17 @@ __host__ __device__ constexpr uint32_t col_o(int t) { return 256u + 128u * t; } 
 __host__ __device__ constexpr uint32_t col_l(int t) { return 128u + 32u * t; }  // l_t (rowsum_mma): 16 used
 __host__ __device__ constexpr uint32_t col_p(int t) { return 192u + 32u * t; }  // P_t (rowsum_mma, kPInTmem)
 
-// FP8 without repair blocks: the row sums l come from the tensor core (P
-// times a tile of ones, into 16 TMEM columns per tile that O's rescale also
+// FP8: the row sums l of the E4M3 blocks come from the tensor core (P times
+// a tile of ones, into 16 TMEM columns per tile that O's rescale also
 // scales), and the two tiles take turns in one S region (col_s(0)) to make
-// room for them.  The repair instance keeps its register sums.
+// room for them.  The repair blocks (BF16, per-tile S columns, before the
+// E4M3 blocks) keep their register sums, carried in l beside the column.
 constexpr bool kMmaRowSum = true;
 // ... and P_t then lives in TMEM too (32 columns, four E4M3 codes per column),
 // written by one tcgen05.st, the A operand of P.V and of the row sum.
 constexpr bool kPInTmem = true;
 template <bool FP8, bool REP>
-__host__ __device__ constexpr bool rowsum_mma() { return FP8 && !REP && kMmaRowSum; }
+__host__ __device__ constexpr bool rowsum_mma() { return FP8 && kMmaRowSum; }
 
 template <bool FP8>
 struct Traits {
@@ -217,7 +218,9 @@ __device__ __forceinline__ uint8_t* vrep_tile(Smem<FP8>& sm) { return &sm.rep[FP
 template <bool FP8>
 __device__ __forceinline__ uint8_t* p_tile(Smem<FP8>& sm, int t) { return &sm.rep[0][0] + t * HALF; }
 // rowsum_mma: 16 rows x 128 keys of E4M3 1.0 (0x38; 2 KB, every byte the same,
-// so its swizzle does not matter) -- the repair V region, unused there.
+// so its swizzle does not matter) -- the repair V region, which the MMA
+// thread fills once the last repair P.V has read it (or at once without
+// repair blocks).
 template <bool FP8>
 __device__ __forceinline__ uint8_t* ones_tile(Smem<FP8>& sm) { return &sm.rep[FP8 ? 1 : 0][0]; }
 
@@ -426,9 +429,22 @@ __device__ __forceinline__ void issue_l_e4m3(uint32_t l_tmem, uint64_t pd, uint3
 //   QK_0(j+1)       [after s_free_1(j): tile 1 has read S_1(j)]
 // -- the order in which those events come when tile 1 runs a little behind
 // tile 0, which this chain itself makes it do.  o_done_t follows each PV_t
-// with its row sum.
-__device__ __forceinline__ void mma_main_fp8_rs(Smem<true>& sm, uint32_t tmem, int nkv, volatile int* ab,
+// with its row sum.  REP: after nrep repair blocks; ph = nrep continues the
+// s_full / p_full phases, and PV_t accumulates onto their O from the start.
+template <bool REP>
+__device__ __forceinline__ void mma_main_fp8_rs(Smem<true>& sm, uint32_t tmem, int nkv, int nrep, volatile int* ab,
                                                 uint32_t* err) {
+  const int ph = REP ? nrep : 0;
+  // the ones tile, 64 bytes per lane (REP: once the last repair P.V, which
+  // read V_rep from the same bytes, has completed)
+  if (REP && nrep > 0 && !mbar_wait(&sm.vrep_empty, (nrep - 1) & 1, ab, err)) return;
+  {
+    uint4* o = reinterpret_cast<uint4*>(ones_tile(sm)) + (threadIdx.x & 31) * 4;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[i] = make_uint4(0x38383838u, 0x38383838u, 0x38383838u, 0x38383838u);
+    fence_proxy_async_smem();
+    __syncwarp();
+  }
   constexpr uint32_t TILE = Traits<true>::TILE;
   constexpr int KST = Traits<true>::KST, VST = Traits<true>::VST;
   uint64_t qd[TILES], pd[TILES];
@@ -443,12 +459,12 @@ __device__ __forceinline__ void mma_main_fp8_rs(Smem<true>& sm, uint32_t tmem, i
   const uint32_t s_tmem = tmem + col_s(0);
   // PV_t(j) and l_t after P_t(j) is in (V_j must be in)
   auto pv = [&](int t, int j) -> bool {
-    if (!mbar_wait(&sm.p_full[t], j & 1, ab, err)) return false;
+    if (!mbar_wait(&sm.p_full[t], (j + ph) & 1, ab, err)) return false;
     tc_fence_after_sync();
     if (kPInTmem)
-      issue_pv<true>(tmem + col_o(t), tmem + col_p(t), desc_at(vd0, (j % VST) * TILE), j > 0);
+      issue_pv<true>(tmem + col_o(t), tmem + col_p(t), desc_at(vd0, (j % VST) * TILE), j + ph > 0);
     else
-      issue_pv_smem_e4m3(tmem + col_o(t), pd[t], desc_at(vd0, (j % VST) * TILE), j > 0);
+      issue_pv_smem_e4m3(tmem + col_o(t), pd[t], desc_at(vd0, (j % VST) * TILE), j + ph > 0);
     issue_l_e4m3(tmem + col_l(t), pd[t], tmem + col_p(t), od, j > 0);
     mma_commit(&sm.o_done[t]);
     return true;
@@ -621,7 +637,7 @@ __device__ __forceinline__ void mma_issuer(Smem<FP8>& sm, uint32_t tmem, int nkv
       for (int t = 0; t < TILES; ++t) mma_commit(&sm.o_full[t]);
       break;
     }
-    if constexpr (rowsum_mma<FP8, REP>()) mma_main_fp8_rs(sm, tmem, nkv, ab, err);
+    if constexpr (rowsum_mma<FP8, REP>()) mma_main_fp8_rs<REP>(sm, tmem, nkv, nrep, ab, err);
     else if constexpr (FP8) mma_main_fp8<REP>(sm, tmem, nkv, ph, ab, err);
     else mma_main_bf16(sm, tmem, nkv, ab, err);
   } while (0);
@@ -668,6 +684,27 @@ __device__ __forceinline__ void convert_q_row(Smem<FP8>& sm, int t, int r) {
   }
 }
 
+// Max of a row's 128 scores: four chains of three-input max, sixteen deep
+// (eight chains measured 1 % slower in BF16 at N = 4608, the same in FP8).
+constexpr int kMaxChains = 4;
+__device__ __forceinline__ float row_max128(const uint32_t (&s)[BN]) {
+  float acc[kMaxChains];
+#pragma unroll
+  for (int c = 0; c < kMaxChains; ++c) acc[c] = fmaxf(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1]));
+#pragma unroll
+  for (int i = 2 * kMaxChains; i < BN; i += 2 * kMaxChains) {
+#pragma unroll
+    for (int c = 0; c < kMaxChains; ++c)
+      acc[c] = fmax3(acc[c], __uint_as_float(s[i + 2 * c]), __uint_as_float(s[i + 2 * c + 1]));
+  }
+#pragma unroll
+  for (int w = kMaxChains; w > 1; w /= 2) {
+#pragma unroll
+    for (int c = 0; c < w / 2; ++c) acc[c] = fmaxf(acc[c], acc[c + w / 2]);
+  }
+  return acc[0];
+}
+
 // One key block of the online softmax of query tile t (128 threads, thread
 // r = row r): wait for S, mask the keys >= valid, update the running max m
 // (log2 units) and sum l, write P over S (P8: E4M3 of 256 p, four per TMEM
@@ -704,16 +741,7 @@ __device__ __forceinline__ bool softmax_block(Smem<FP8>& sm, int t, uint32_t s_a
       if (i >= valid) s[i] = __float_as_uint(-INFINITY);
   }
   // Row max: four independent chains of three-input max (depth 16, not 127).
-  float acc[4];
-#pragma unroll
-  for (int c = 0; c < 4; ++c) acc[c] = fmaxf(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1]));
-#pragma unroll
-  for (int i = 8; i < BN; i += 8) {
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-      acc[c] = fmax3(acc[c], __uint_as_float(s[i + 2 * c]), __uint_as_float(s[i + 2 * c + 1]));
-  }
-  const float mx = fmax3(acc[0], acc[1], fmaxf(acc[2], acc[3]));
+  const float mx = row_max128(s);
   const float m_tile = fmaxf(m, mx * sl2);
   // One decision per warp (TMEM moves are warp-wide); each row keeps its own alpha.
   const bool rescale = __any_sync(0xFFFFFFFFu, m_tile > m + kRescale);
@@ -793,7 +821,8 @@ __device__ __forceinline__ bool softmax_block(Smem<FP8>& sm, int t, uint32_t s_a
 // previous block (jm - 1), which read the same P buffer and wrote O, has
 // completed (o_done).  jm: the block's index in the main loop; phase: its
 // s_full / p_full phase.  RS (rowsum_mma): no row sum here -- the tensor core
-// adds P into l_addr's column, which the rescale scales with O; l is unused.
+// adds P into l_addr's column, which the rescale scales with O; l keeps the
+// repair blocks' part and follows alpha.
 template <bool RS>
 __device__ __forceinline__ bool softmax_block_fp8(Smem<true>& sm, int t, int r, uint32_t s_addr, uint32_t o_addr,
                                                   uint32_t l_addr, uint32_t p_addr, uint32_t phase, int jm,
@@ -814,16 +843,7 @@ __device__ __forceinline__ bool softmax_block_fp8(Smem<true>& sm, int t, int r, 
     for (int i = 0; i < BN; ++i)
       if (i >= valid) s[i] = __float_as_uint(-INFINITY);
   }
-  float acc[4];
-#pragma unroll
-  for (int c = 0; c < 4; ++c) acc[c] = fmaxf(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1]));
-#pragma unroll
-  for (int i = 8; i < BN; i += 8) {
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-      acc[c] = fmax3(acc[c], __uint_as_float(s[i + 2 * c]), __uint_as_float(s[i + 2 * c + 1]));
-  }
-  const float mx = fmax3(acc[0], acc[1], fmaxf(acc[2], acc[3]));
+  const float mx = row_max128(s);
   const float m_tile = fmaxf(m, mx * sl2);
   const bool rescale = __any_sync(0xFFFFFFFFu, m_tile > m + kRescale);
   const float m_new = rescale ? m_tile : m;
@@ -841,6 +861,7 @@ __device__ __forceinline__ bool softmax_block_fp8(Smem<true>& sm, int t, int r, 
       fma2(x2, x3, __uint_as_float(s[4 * i + 2]), __uint_as_float(s[4 * i + 3]), sl2, sl2, nm, nm);
       pk[i] = e4m3x2(ex2_approx(x0), ex2_approx(x1)) | (e4m3x2(ex2_approx(x2), ex2_approx(x3)) << 16);
     }
+    l *= alpha;  // the repair blocks' register sum (0 without them)
   } else {
     __half2 hs[8];
 #pragma unroll
@@ -917,6 +938,7 @@ __device__ __forceinline__ void softmax_epilogue(Smem<FP8>& sm, uint32_t tmem, c
   const int r = threadIdx.x & (BM - 1);
   const uint32_t lane_base = static_cast<uint32_t>(r & ~31) << 16;  // TMEM lanes of this warp
   constexpr bool RS = rowsum_mma<FP8, REP>();
+  const uint32_t s_rep = tmem + lane_base + col_s(t);            // the repair blocks' S / P
   const uint32_t s_addr = tmem + lane_base + col_s(RS ? 0 : t);  // RS: one S region, in turns
   const uint32_t o_addr = tmem + lane_base + col_o(t);
   const uint32_t l_addr = tmem + lane_base + col_l(t);
@@ -940,7 +962,7 @@ __device__ __forceinline__ void softmax_epilogue(Smem<FP8>& sm, uint32_t tmem, c
     fence_proxy_async_smem();  // generic-proxy writes, read by the MMA (async proxy)
     mbar_arrive(&sm.qbf_full[t]);
     for (int i = 0; i < nrep && ok; ++i)
-      ok = softmax_block<FP8, false>(sm, t, s_addr, o_addr, i & 1, prm.rep_keys - i * BN, i > 0, sl2, m, l, ab,
+      ok = softmax_block<FP8, false>(sm, t, s_rep, o_addr, i & 1, prm.rep_keys - i * BN, i > 0, sl2, m, l, ab,
                                      prm.err);
   }
   if (SOL) {
@@ -952,13 +974,6 @@ __device__ __forceinline__ void softmax_epilogue(Smem<FP8>& sm, uint32_t tmem, c
                                      j > 0, sl2, m, l, ab, prm.err, (e >> (14 + t)) & 1u);
     }
   } else if constexpr (FP8) {
-    if (RS && t == 0) {
-      // the ones tile of the row-sum MMAs: row r's 16 bytes; the issuer first
-      // reads it after this tile's p_full of block 0, which follows the fence
-      *reinterpret_cast<uint4*>(ones_tile(sm) + r * 16) = make_uint4(0x38383838u, 0x38383838u, 0x38383838u,
-                                                                     0x38383838u);
-      fence_proxy_async_smem();
-    }
     for (int j = 0; j < nmain && ok; ++j)
       ok = softmax_block_fp8<RS>(sm, t, r, s_addr, o_addr, l_addr, p_addr, (j + nrep) & 1, j,
                                  prm.main_keys - j * BN, j + nrep > 0, sl2, m, l, ab, prm.err);
@@ -973,10 +988,10 @@ __device__ __forceinline__ void softmax_epilogue(Smem<FP8>& sm, uint32_t tmem, c
   }
   if (!ok) return;
   tc_fence_after_sync();
-  if constexpr (RS) {  // the tensor core's row sum
+  if (RS && nmain > 0) {  // the tensor core's row sum of the E4M3 blocks
     uint32_t lv = tmem_ld1(l_addr);
     tmem_ld_wait(lv);
-    l = __uint_as_float(lv);
+    l += __uint_as_float(lv);
   }
   const float inv_l = out_scale / l;
   // O tile (bf16, 32 KB) -> shared memory that no MMA or copy touches any
