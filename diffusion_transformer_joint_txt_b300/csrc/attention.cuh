@@ -17,11 +17,12 @@
 //   warp 8     TMA producer of the K ring
 //   warp 9     TMEM allocator and tcgen05.mma issuer (one elected lane)
 //   warp 10    TMA producer of both Q tiles and of the V ring
-// TMEM (512 columns): S_0 at 0, S_1 at 128, O_0 at 256, O_1 at 384.  BF16
-// (and the repair blocks): the softmax of a tile overwrites its S with P, and
-// the P.V MMA reads P straight from TMEM as its A operand.  FP8: P goes to a
-// shared-memory tile instead (mma_main_fp8), so that S_t takes the next
-// block's scores while the softmax still works on this one.
+// TMEM (512 columns).  BF16 (and the repair blocks): S_0 at 0, S_1 at 128,
+// O_0 at 256, O_1 at 384; the softmax of a tile overwrites its S with P, and
+// the P.V MMA reads P straight from TMEM as its A operand.  FP8: one S region
+// at 0 that the tiles take in turns, l_0 / l_1 at 128 / 160, P_0 / P_1 at
+// 192 / 224, O as in BF16 (mma_main_fp8_rs): P has its own columns, so the S
+// region takes the next scores while the softmax still works on these.
 //
 // BF16: the MMA issue order is  QK_0(0) QK_1(0) | PV_0(j) QK_0(j+1) PV_1(j)
 // QK_1(j+1) | ...  so while the softmax of tile 0 works on S_0(j+1) the
@@ -51,10 +52,9 @@
 // dimension of P.V).  P is E4M3 of 256 p; the row sum l adds the values the
 // codes stand for, so that O = sum p~ v / sum p~ is a convex combination of
 // the V rows whatever the rounding of P.  Scores are scaled by s_q s_k and
-// the output by s_v (per-(b, h) scales).  The plain FP8 kernel keeps P in
-// TMEM and has the tensor core sum it (rowsum_mma: P times a tile of ones);
-// the VC instance keeps P in a shared-memory tile and sums the codes in
-// packed f16 (E4M3 values are exact in f16).
+// the output by s_v (per-(b, h) scales).  P stays in TMEM and the tensor
+// core sums it (P times a tile of ones); the repair blocks of the VC instance
+// sum their bf16 P in registers.
 //
 // VC-Attention repair (REP, FP8 only; vc_repair.cuh selects the tokens):
 // the CTA first runs ceil(R / 128) repair blocks in BF16 -- K_rep = k' / s_k
@@ -101,20 +101,15 @@ constexpr uint32_t HALF = BM * 128;  // one SW128 block: 128 rows x 128 bytes = 
 
 __host__ __device__ constexpr uint32_t col_s(int t) { return 128u * t; }        // S_t / P_t
 __host__ __device__ constexpr uint32_t col_o(int t) { return 256u + 128u * t; } // O_t
-__host__ __device__ constexpr uint32_t col_l(int t) { return 128u + 32u * t; }  // l_t (rowsum_mma): 16 used
-__host__ __device__ constexpr uint32_t col_p(int t) { return 192u + 32u * t; }  // P_t (rowsum_mma, kPInTmem)
+__host__ __device__ constexpr uint32_t col_l(int t) { return 128u + 32u * t; }  // FP8: l_t (16 columns used)
+__host__ __device__ constexpr uint32_t col_p(int t) { return 192u + 32u * t; }  // FP8: P_t (E4M3)
 
-// FP8: the row sums l of the E4M3 blocks come from the tensor core (P times
-// a tile of ones, into 16 TMEM columns per tile that O's rescale also
-// scales), and the two tiles take turns in one S region (col_s(0)) to make
-// room for them.  The repair blocks (BF16, per-tile S columns, before the
-// E4M3 blocks) keep their register sums, carried in l beside the column.
-constexpr bool kMmaRowSum = true;
-// ... and P_t then lives in TMEM too (32 columns, four E4M3 codes per column),
-// written by one tcgen05.st, the A operand of P.V and of the row sum.
-constexpr bool kPInTmem = true;
-template <bool FP8, bool REP>
-__host__ __device__ constexpr bool rowsum_mma() { return FP8 && kMmaRowSum; }
+// FP8 TMEM: the row sums l of the E4M3 blocks come from the tensor core (P
+// times a tile of ones, into 16 columns per tile that O's rescale also
+// scales), P_t lives in 32 columns (four E4M3 codes per column), and the two
+// tiles take turns in one S region (col_s(0)) to make room for both.  The
+// repair blocks (BF16, per-tile S columns, before the E4M3 blocks) keep their
+// register sums, carried in l beside the column.
 
 template <bool FP8>
 struct Traits {
@@ -212,12 +207,12 @@ template <bool FP8>
 __device__ __forceinline__ uint8_t* krep_tile(Smem<FP8>& sm) { return &sm.rep[0][0]; }
 template <bool FP8>
 __device__ __forceinline__ uint8_t* vrep_tile(Smem<FP8>& sm) { return &sm.rep[FP8 ? 1 : 0][0]; }
-// FP8: tile t's P (E4M3, 128 rows x 128 keys, 16 KB in the K-major SW128
-// layout) -- the first half of the repair region, whose repair K tile is
-// consumed before the E4M3 blocks begin.
+// FP8: tile t's 16 KB staging half for its output (the second half is its Q
+// tile) -- the repair K region, whose tile is consumed before the E4M3 blocks
+// begin, and unused without repair blocks.
 template <bool FP8>
-__device__ __forceinline__ uint8_t* p_tile(Smem<FP8>& sm, int t) { return &sm.rep[0][0] + t * HALF; }
-// rowsum_mma: 16 rows x 128 keys of E4M3 1.0 (0x38; 2 KB, every byte the same,
+__device__ __forceinline__ uint8_t* out_stage(Smem<FP8>& sm, int t) { return &sm.rep[0][0] + t * HALF; }
+// FP8: 16 rows x 128 keys of E4M3 1.0 (0x38; 2 KB, every byte the same,
 // so its swizzle does not matter) -- the repair V region, which the MMA
 // thread fills once the last repair P.V has read it (or at once without
 // repair blocks).
@@ -397,32 +392,18 @@ __device__ __forceinline__ bool mma_repair(Smem<FP8>& sm, uint32_t tmem, int nre
   return true;
 }
 
-// FP8: O (+)= P V with P from shared memory (pd: the P tile's K-major SW128
-// descriptor), V^T K-major: 4 MMAs of 128 x 128 x 32, step kk at byte 32kk.
-__device__ __forceinline__ void issue_pv_smem_e4m3(uint32_t o_tmem, uint64_t pd, uint64_t vd, bool accumulate) {
-  constexpr uint32_t ID = idesc_e4m3(BM, HD, false);
-#pragma unroll
-  for (int kk = 0; kk < BN / 32; ++kk)
-    mma_e4m3_ss(o_tmem, desc_at(pd, kk * 32), desc_at(vd, kk * 32), ID, (accumulate || kk > 0) ? 1u : 0u);
-}
-
 // l_t (+)= P_t 1: the row sums of P by the tensor core, N = 16 (16 equal
-// columns; the softmax reads the first), 4 MMAs of 128 x 16 x 32, P from
-// shared memory (pd) or from TMEM (p_tmem, kPInTmem).
-__device__ __forceinline__ void issue_l_e4m3(uint32_t l_tmem, uint64_t pd, uint32_t p_tmem, uint64_t od,
-                                             bool accumulate) {
+// columns; the softmax reads the first), 4 MMAs of 128 x 16 x 32 with P from
+// TMEM (p_tmem) and the ones tile from shared memory (od).
+__device__ __forceinline__ void issue_l_e4m3(uint32_t l_tmem, uint32_t p_tmem, uint64_t od, bool accumulate) {
   constexpr uint32_t ID = idesc_e4m3(BM, 16, false);
 #pragma unroll
-  for (int kk = 0; kk < BN / 32; ++kk) {
-    if (kPInTmem)
-      mma_e4m3_ts(l_tmem, p_tmem + kk * 8, desc_at(od, kk * 32), ID, (accumulate || kk > 0) ? 1u : 0u);
-    else
-      mma_e4m3_ss(l_tmem, desc_at(pd, kk * 32), desc_at(od, kk * 32), ID, (accumulate || kk > 0) ? 1u : 0u);
-  }
+  for (int kk = 0; kk < BN / 32; ++kk)
+    mma_e4m3_ts(l_tmem, p_tmem + kk * 8, desc_at(od, kk * 32), ID, (accumulate || kk > 0) ? 1u : 0u);
 }
 
-// FP8 main loop with the row sums on the tensor core (rowsum_mma): both
-// tiles' scores go through the one S region in turns, so per block j
+// FP8 main loop (the MMA thread): P_t in TMEM, the row sums on the tensor
+// core, both tiles' scores through the one S region in turns, so per block j
 //   PV_0(j-1) l_0   [after p_full_0(j-1)]
 //   QK_1(j)         [after s_free_0(j): tile 0 has read S_0(j)]
 //   PV_1(j-1) l_1   [after p_full_1(j-1)]
@@ -447,12 +428,9 @@ __device__ __forceinline__ void mma_main_fp8_rs(Smem<true>& sm, uint32_t tmem, i
   }
   constexpr uint32_t TILE = Traits<true>::TILE;
   constexpr int KST = Traits<true>::KST, VST = Traits<true>::VST;
-  uint64_t qd[TILES], pd[TILES];
+  uint64_t qd[TILES];
 #pragma unroll
-  for (int t = 0; t < TILES; ++t) {
-    qd[t] = sdesc_sw128(smem_u32(sm.q[t]), 16, 1024);
-    pd[t] = sdesc_sw128(smem_u32(p_tile(sm, t)), 16, 1024);
-  }
+  for (int t = 0; t < TILES; ++t) qd[t] = sdesc_sw128(smem_u32(sm.q[t]), 16, 1024);
   const uint64_t kd0 = sdesc_sw128(smem_u32(sm.k[0]), 16, 1024);
   const uint64_t vd0 = sdesc_sw128(smem_u32(sm.v[0]), 16, 1024);
   const uint64_t od = sdesc_sw128(smem_u32(ones_tile(sm)), 16, 1024);
@@ -461,11 +439,8 @@ __device__ __forceinline__ void mma_main_fp8_rs(Smem<true>& sm, uint32_t tmem, i
   auto pv = [&](int t, int j) -> bool {
     if (!mbar_wait(&sm.p_full[t], (j + ph) & 1, ab, err)) return false;
     tc_fence_after_sync();
-    if (kPInTmem)
-      issue_pv<true>(tmem + col_o(t), tmem + col_p(t), desc_at(vd0, (j % VST) * TILE), j + ph > 0);
-    else
-      issue_pv_smem_e4m3(tmem + col_o(t), pd[t], desc_at(vd0, (j % VST) * TILE), j + ph > 0);
-    issue_l_e4m3(tmem + col_l(t), pd[t], tmem + col_p(t), od, j > 0);
+    issue_pv<true>(tmem + col_o(t), tmem + col_p(t), desc_at(vd0, (j % VST) * TILE), j + ph > 0);
+    issue_l_e4m3(tmem + col_l(t), tmem + col_p(t), od, j > 0);
     mma_commit(&sm.o_done[t]);
     return true;
   };
@@ -506,65 +481,6 @@ __device__ __forceinline__ void mma_main_fp8_rs(Smem<true>& sm, uint32_t tmem, i
   if (!pv(1, jl)) return;
   mma_commit(&sm.v_empty[jl % VST]);
   mma_commit(&sm.o_full[1]);
-}
-
-// FP8 main loop of the MMA thread.  P goes through shared memory, so S_t's
-// TMEM columns are free as soon as the softmax has loaded them (s_free): QK_t
-// of the next block is issued then, and runs while the softmax of this block
-// works; PV_t follows when P_t is in (p_full) and signals o_done.  Per block:
-//   QK_0(j+1) QK_1(j+1)  [after s_free_0(j), s_free_1(j)]   PV_0(j) PV_1(j)  [after p_full]
-// ph: s_full / p_full phases the repair blocks used before.  One thread
-// issues for both tiles (two issuers, one per tile, each on its own warp,
-// measured the same: 4.047 against 4.052 ms on the CFG pair, interleaved).
-template <bool REP>
-__device__ __forceinline__ void mma_main_fp8(Smem<true>& sm, uint32_t tmem, int nkv, int ph, volatile int* ab,
-                                             uint32_t* err) {
-  constexpr uint32_t TILE = Traits<true>::TILE;
-  constexpr int KST = Traits<true>::KST, VST = Traits<true>::VST;
-  uint64_t qd[TILES], pd[TILES];
-#pragma unroll
-  for (int t = 0; t < TILES; ++t) {
-    qd[t] = sdesc_sw128(smem_u32(sm.q[t]), 16, 1024);
-    pd[t] = sdesc_sw128(smem_u32(p_tile(sm, t)), 16, 1024);
-  }
-  const uint64_t kd0 = sdesc_sw128(smem_u32(sm.k[0]), 16, 1024);
-  const uint64_t vd0 = sdesc_sw128(smem_u32(sm.v[0]), 16, 1024);
-  if (!mbar_wait(&sm.k_full[0], 0, ab, err)) return;
-#pragma unroll
-  for (int t = 0; t < TILES; ++t) {
-    if (!mbar_wait(&sm.q_full[t], 0, ab, err)) return;
-    tc_fence_after_sync();
-    issue_qk<true>(tmem + col_s(t), qd[t], kd0);
-    mma_commit(&sm.s_full[t]);
-  }
-  mma_commit(&sm.k_empty[0]);
-  for (int j = 0; j < nkv; ++j) {
-    const int jn = j + 1;
-    if (jn < nkv) {
-      const int ks = jn % KST;
-      if (!mbar_wait(&sm.k_full[ks], (jn / KST) & 1, ab, err)) return;
-#pragma unroll
-      for (int t = 0; t < TILES; ++t) {
-        if (!mbar_wait(&sm.s_free[t], j & 1, ab, err)) return;
-        tc_fence_after_sync();
-        issue_qk<true>(tmem + col_s(t), qd[t], desc_at(kd0, ks * TILE));
-        mma_commit(&sm.s_full[t]);
-      }
-      mma_commit(&sm.k_empty[ks]);
-    }
-    const int vs = j % VST;
-    if (!mbar_wait(&sm.v_full[vs], (j / VST) & 1, ab, err)) return;
-#pragma unroll
-    for (int t = 0; t < TILES; ++t) {
-      if (!mbar_wait(&sm.p_full[t], (j + ph) & 1, ab, err)) return;
-      tc_fence_after_sync();
-      issue_pv_smem_e4m3(tmem + col_o(t), pd[t], desc_at(vd0, vs * TILE), j + ph > 0);
-      mma_commit(&sm.o_done[t]);
-    }
-    mma_commit(&sm.v_empty[vs]);
-  }
-#pragma unroll
-  for (int t = 0; t < TILES; ++t) mma_commit(&sm.o_full[t]);
 }
 
 // BF16 main loop of the issuing thread, for both query tiles in one fixed
@@ -623,13 +539,13 @@ __device__ __forceinline__ void mma_main_bf16(Smem<false>& sm, uint32_t tmem, in
 }
 
 // The MMA issuer (the whole warp runs the loop, one elected lane issues:
-// ptx.cuh), for both tiles.  REP: the repair blocks first (mma_repair); the main loop then continues
-// the s_full / p_full phases after them and accumulates onto their O.
+// ptx.cuh), for both tiles.  REP: the repair blocks first (mma_repair); the
+// main loop then continues the s_full / p_full phases after them and
+// accumulates onto their O.
 template <bool FP8, bool REP>
 __device__ __forceinline__ void mma_issuer(Smem<FP8>& sm, uint32_t tmem, int nkv, int nrep, volatile int* ab,
                                            uint32_t* err) {
-  const int ph = REP ? nrep : 0;  // s_full / p_full phases the repair blocks used
-  if (REP) nkv -= nrep;           // main-loop blocks
+  if (REP) nkv -= nrep;  // main-loop blocks
   do {
     if (REP && !mma_repair(sm, tmem, nrep, ab, err)) break;
     if (nkv <= 0) {
@@ -637,8 +553,7 @@ __device__ __forceinline__ void mma_issuer(Smem<FP8>& sm, uint32_t tmem, int nkv
       for (int t = 0; t < TILES; ++t) mma_commit(&sm.o_full[t]);
       break;
     }
-    if constexpr (rowsum_mma<FP8, REP>()) mma_main_fp8_rs<REP>(sm, tmem, nkv, nrep, ab, err);
-    else if constexpr (FP8) mma_main_fp8<REP>(sm, tmem, nkv, ph, ab, err);
+    if constexpr (FP8) mma_main_fp8_rs<REP>(sm, tmem, nkv, nrep, ab, err);
     else mma_main_bf16(sm, tmem, nkv, ab, err);
   } while (0);
   // Drain every MMA this thread issued before TMEM is released.
@@ -706,17 +621,18 @@ __device__ __forceinline__ float row_max128(const uint32_t (&s)[BN]) {
 }
 
 // One key block of the online softmax of query tile t (128 threads, thread
-// r = row r): wait for S, mask the keys >= valid, update the running max m
-// (log2 units) and sum l, write P over S (P8: E4M3 of 256 p, four per TMEM
-// column; else bf16, two per column), rescale O when the max moved (has_o:
-// O already holds earlier blocks), and hand P to the MMA thread.  Returns
-// false when the CTA gave up.
-template <bool FP8, bool P8>
+// r = row r) with bf16 P -- the BF16 kernel's blocks and the FP8 kernel's
+// repair blocks: wait for S, mask the keys >= valid, update the running max
+// m (log2 units) and sum l, write P over S (bf16, two per TMEM column),
+// rescale O when the max moved (has_o: O already holds earlier blocks), and
+// hand P to the MMA thread.  Returns false when the CTA gave up.
+template <bool FP8>
 __device__ __forceinline__ bool softmax_block(Smem<FP8>& sm, int t, uint32_t s_addr, uint32_t o_addr,
                                               uint32_t phase, int valid, bool has_o, float sl2, float& m, float& l,
                                               volatile int* ab, uint32_t* err, bool keep = true) {
-  // FP8 stores P as E4M3 of 256 p: the 2^8 factor is folded into the exponent
-  // and cancels against l, which sums the same scaled values.
+  // The FP8 kernel's repair blocks use the scale of its E4M3 blocks, whose P
+  // is E4M3 of 256 p: the 2^8 factor is folded into the exponent and cancels
+  // against l, which sums the same scaled values.
   constexpr float kPBias = FP8 ? 8.f : 0.f;
   constexpr float kRescale = Traits<FP8>::RESCALE;
   const bool ok = mbar_wait(&sm.s_full[t], phase, ab, err);
@@ -751,32 +667,7 @@ __device__ __forceinline__ bool softmax_block(Smem<FP8>& sm, int t, uint32_t s_a
   // p = 2^(s sl2 - m): the argument of two scores per packed FMA; the row
   // sum in four packed accumulators.
   float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  if (P8) {
-    // P codes four per word (key 4i in the lowest byte); the row sum adds
-    // the values of the codes, in eight packed f16 accumulators (each sums
-    // at most 8 values <= 256: partial sums <= 2048, rounding <= 2^-11
-    // relative per add) that are widened to fp32 once per block.
-    uint32_t pk[32];
-    __half2 hs[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) hs[i] = __float2half2_rn(0.f);
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      float x0, x1, x2, x3;
-      fma2(x0, x1, __uint_as_float(s[4 * i]), __uint_as_float(s[4 * i + 1]), sl2, sl2, nm, nm);
-      fma2(x2, x3, __uint_as_float(s[4 * i + 2]), __uint_as_float(s[4 * i + 3]), sl2, sl2, nm, nm);
-      const uint32_t lo = e4m3x2(ex2_approx(x0), ex2_approx(x1));
-      const uint32_t hi = e4m3x2(ex2_approx(x2), ex2_approx(x3));
-      pk[i] = lo | (hi << 16);
-      hs[i & 7] = __hadd2(hs[i & 7], __hadd2(e4m3x2_value(lo), e4m3x2_value(hi)));
-    }
-    tmem_st32(s_addr, pk);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float2 f = __half22float2(hs[i]);
-      sum[i] = f.x + f.y;
-    }
-  } else {
+  {
     uint32_t pk[BN / 2];
 #pragma unroll
     for (int i = 0; i < BN / 2; ++i) {
@@ -813,17 +704,16 @@ __device__ __forceinline__ bool softmax_block(Smem<FP8>& sm, int t, uint32_t s_a
   return true;
 }
 
-// One E4M3 block of the FP8 main loop (128 threads, thread r = row r): as
-// softmax_block with P8, except that P goes to shared memory.  The thread
-// signals s_free as soon as S is in its registers (the MMA thread then
-// computes the next block's S into the same columns while this one works),
-// and before it writes P, or rescales O, it waits until the PV of the
-// previous block (jm - 1), which read the same P buffer and wrote O, has
-// completed (o_done).  jm: the block's index in the main loop; phase: its
-// s_full / p_full phase.  RS (rowsum_mma): no row sum here -- the tensor core
-// adds P into l_addr's column, which the rescale scales with O; l keeps the
-// repair blocks' part and follows alpha.
-template <bool RS>
+// One E4M3 block of the FP8 main loop (128 threads, thread r = row r).  The
+// thread signals s_free as soon as S is in its registers (the MMA thread
+// then puts the other tile's scores into the same S columns while this one
+// works); before it writes P (p_addr: E4M3 of 256 p, four codes per TMEM
+// column) or rescales O, it waits until the P.V and the row sum of the
+// previous block (jm - 1), which read the same P columns and wrote O and
+// l_addr, have completed (o_done).  No row sum here: the tensor core adds P
+// into l_addr's column, which the rescale scales with O; l keeps the repair
+// blocks' register sum and follows alpha.  jm: the block's index in the main
+// loop; phase: its s_full / p_full phase.
 __device__ __forceinline__ bool softmax_block_fp8(Smem<true>& sm, int t, int r, uint32_t s_addr, uint32_t o_addr,
                                                   uint32_t l_addr, uint32_t p_addr, uint32_t phase, int jm,
                                                   int valid, bool has_o,
@@ -852,59 +742,23 @@ __device__ __forceinline__ bool softmax_block_fp8(Smem<true>& sm, int t, int r, 
   // P codes four per word (key 4i in the lowest byte); the row sum adds the
   // values of the codes in eight packed f16 accumulators (each at most 8
   // values <= 256), widened to fp32 once per block.
+  // P codes four per word (key 4i in the lowest byte)
   uint32_t pk[32];
-  if constexpr (RS) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      float x0, x1, x2, x3;
-      fma2(x0, x1, __uint_as_float(s[4 * i]), __uint_as_float(s[4 * i + 1]), sl2, sl2, nm, nm);
-      fma2(x2, x3, __uint_as_float(s[4 * i + 2]), __uint_as_float(s[4 * i + 3]), sl2, sl2, nm, nm);
-      pk[i] = e4m3x2(ex2_approx(x0), ex2_approx(x1)) | (e4m3x2(ex2_approx(x2), ex2_approx(x3)) << 16);
-    }
-    l *= alpha;  // the repair blocks' register sum (0 without them)
-  } else {
-    __half2 hs[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) hs[i] = __float2half2_rn(0.f);
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      float x0, x1, x2, x3;
-      fma2(x0, x1, __uint_as_float(s[4 * i]), __uint_as_float(s[4 * i + 1]), sl2, sl2, nm, nm);
-      fma2(x2, x3, __uint_as_float(s[4 * i + 2]), __uint_as_float(s[4 * i + 3]), sl2, sl2, nm, nm);
-      const uint32_t lo = e4m3x2(ex2_approx(x0), ex2_approx(x1));
-      const uint32_t hi = e4m3x2(ex2_approx(x2), ex2_approx(x3));
-      pk[i] = lo | (hi << 16);
-      hs[i & 7] = __hadd2(hs[i & 7], __hadd2(e4m3x2_value(lo), e4m3x2_value(hi)));
-    }
-    float sum[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float2 f = __half22float2(hs[i]);
-      sum[i] = f.x + f.y;
-    }
-    add2(sum[0], sum[1], sum[2], sum[3]);
-    add2(sum[4], sum[5], sum[6], sum[7]);
-    add2(sum[0], sum[1], sum[4], sum[5]);
-    l = l * alpha + (sum[0] + sum[1]);
+  for (int i = 0; i < 32; ++i) {
+    float x0, x1, x2, x3;
+    fma2(x0, x1, __uint_as_float(s[4 * i]), __uint_as_float(s[4 * i + 1]), sl2, sl2, nm, nm);
+    fma2(x2, x3, __uint_as_float(s[4 * i + 2]), __uint_as_float(s[4 * i + 3]), sl2, sl2, nm, nm);
+    pk[i] = e4m3x2(ex2_approx(x0), ex2_approx(x1)) | (e4m3x2(ex2_approx(x2), ex2_approx(x3)) << 16);
   }
-  // the previous block's PV has read the P buffer and written O
+  l *= alpha;  // the repair blocks' register sum (0 without them)
+  // the previous block's P.V and row sum have read P and written O, l
   if (jm > 0) {
     ok = mbar_wait(&sm.o_done[t], (jm - 1) & 1, ab, err);
     if (__any_sync(0xFFFFFFFFu, !ok)) return false;
     tc_fence_after_sync();
   }
-  if (RS && kPInTmem) {
-    tmem_st32(p_addr, pk);  // waited for (tcgen05.wait::st) before p_full below
-  } else {
-    // P -> row r of the tile's K-major SW128 buffer: 16-byte chunk c (keys
-    // 16c .. 16c+15) at chunk position c ^ (r % 8)
-    uint8_t* prow = p_tile(sm, t) + r * 128;
-#pragma unroll
-    for (int c = 0; c < 8; ++c)
-      *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
-                                                                            pk[4 * c + 3]);
-    fence_proxy_async_smem();  // generic-proxy writes, read by the MMA (async proxy)
-  }
+  tmem_st32(p_addr, pk);  // waited for (tcgen05.wait::st) before p_full below
   if (rescale && has_o) {
 #pragma unroll
     for (int c = 0; c < HD / 32; ++c) {
@@ -915,13 +769,11 @@ __device__ __forceinline__ bool softmax_block_fp8(Smem<true>& sm, int t, int r, 
       for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
       tmem_st32(o_addr + c * 32, o);
     }
-    if (RS) {
-      uint32_t lv = tmem_ld1(l_addr);
-      tmem_ld_wait(lv);
-      tmem_st1(l_addr, __float_as_uint(__uint_as_float(lv) * alpha));
-    }
+    uint32_t lv = tmem_ld1(l_addr);
+    tmem_ld_wait(lv);
+    tmem_st1(l_addr, __float_as_uint(__uint_as_float(lv) * alpha));
   }
-  if ((rescale && has_o) || (RS && kPInTmem)) tmem_st_wait();
+  tmem_st_wait();
   m = m_new;
   tc_fence_before_sync();
   mbar_arrive(&sm.p_full[t]);
@@ -937,9 +789,8 @@ __device__ __forceinline__ void softmax_epilogue(Smem<FP8>& sm, uint32_t tmem, c
                                                  const CUtensorMap* tm_o) {
   const int r = threadIdx.x & (BM - 1);
   const uint32_t lane_base = static_cast<uint32_t>(r & ~31) << 16;  // TMEM lanes of this warp
-  constexpr bool RS = rowsum_mma<FP8, REP>();
   const uint32_t s_rep = tmem + lane_base + col_s(t);            // the repair blocks' S / P
-  const uint32_t s_addr = tmem + lane_base + col_s(RS ? 0 : t);  // RS: one S region, in turns
+  const uint32_t s_addr = tmem + lane_base + col_s(FP8 ? 0 : t);  // FP8: one S region, in turns
   const uint32_t o_addr = tmem + lane_base + col_o(t);
   const uint32_t l_addr = tmem + lane_base + col_l(t);
   const uint32_t p_addr = tmem + lane_base + col_p(t);
@@ -962,7 +813,7 @@ __device__ __forceinline__ void softmax_epilogue(Smem<FP8>& sm, uint32_t tmem, c
     fence_proxy_async_smem();  // generic-proxy writes, read by the MMA (async proxy)
     mbar_arrive(&sm.qbf_full[t]);
     for (int i = 0; i < nrep && ok; ++i)
-      ok = softmax_block<FP8, false>(sm, t, s_rep, o_addr, i & 1, prm.rep_keys - i * BN, i > 0, sl2, m, l, ab,
+      ok = softmax_block<FP8>(sm, t, s_rep, o_addr, i & 1, prm.rep_keys - i * BN, i > 0, sl2, m, l, ab,
                                      prm.err);
   }
   if (SOL) {
@@ -970,16 +821,16 @@ __device__ __forceinline__ void softmax_epilogue(Smem<FP8>& sm, uint32_t tmem, c
     // block the tile skips still gets its (zero) P, so O is written from j = 0
     for (int j = 0; j < nmain && ok; ++j) {
       const uint32_t e = __ldg(lst + j);
-      ok = softmax_block<FP8, false>(sm, t, s_addr, o_addr, j & 1, prm.N - static_cast<int>(e & 0x3FFFu) * BN,
+      ok = softmax_block<FP8>(sm, t, s_addr, o_addr, j & 1, prm.N - static_cast<int>(e & 0x3FFFu) * BN,
                                      j > 0, sl2, m, l, ab, prm.err, (e >> (14 + t)) & 1u);
     }
   } else if constexpr (FP8) {
     for (int j = 0; j < nmain && ok; ++j)
-      ok = softmax_block_fp8<RS>(sm, t, r, s_addr, o_addr, l_addr, p_addr, (j + nrep) & 1, j,
+      ok = softmax_block_fp8(sm, t, r, s_addr, o_addr, l_addr, p_addr, (j + nrep) & 1, j,
                                  prm.main_keys - j * BN, j + nrep > 0, sl2, m, l, ab, prm.err);
   } else {
     for (int j = 0; j < nmain && ok; ++j)
-      ok = softmax_block<FP8, FP8>(sm, t, s_addr, o_addr, (j + nrep) & 1, prm.main_keys - j * BN, j + nrep > 0,
+      ok = softmax_block<FP8>(sm, t, s_addr, o_addr, (j + nrep) & 1, prm.main_keys - j * BN, j + nrep > 0,
                                    sl2, m, l, ab, prm.err);
   }
   if (ok) {
@@ -988,7 +839,7 @@ __device__ __forceinline__ void softmax_epilogue(Smem<FP8>& sm, uint32_t tmem, c
   }
   if (!ok) return;
   tc_fence_after_sync();
-  if (RS && nmain > 0) {  // the tensor core's row sum of the E4M3 blocks
+  if (FP8 && nmain > 0) {  // the tensor core's row sum of the E4M3 blocks
     uint32_t lv = tmem_ld1(l_addr);
     tmem_ld_wait(lv);
     l += __uint_as_float(lv);
@@ -999,14 +850,15 @@ __device__ __forceinline__ void softmax_epilogue(Smem<FP8>& sm, uint32_t tmem, c
   // dims 64 (c / 2) .., row r at byte 128 r, its 16-byte chunk k at position
   // k ^ (r % 8).  BF16: the tile's own 32 KB Q buffer (its last QK completed
   // before the PV that signalled o_full).  FP8: the tile's own 16 KB Q buffer
-  // and its 16 KB P buffer, which only this tile's MMAs read.
+  // and its 16 KB half of the repair K region (out_stage), which nothing
+  // touches any more.
   // Then one thread writes the two halves with TMA stores, which also clip
   // rows >= N: whole 128-byte rows instead of each thread's 16-byte pieces of
   // rows H x 256 bytes apart.
   uint8_t* stage[2];
   if constexpr (FP8) {
     stage[0] = sm.q[t];
-    stage[1] = p_tile(sm, t);
+    stage[1] = out_stage(sm, t);
   } else {
     stage[0] = sm.q[t];
     stage[1] = sm.q[t] + HALF;
