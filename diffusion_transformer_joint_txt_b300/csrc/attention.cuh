@@ -776,16 +776,19 @@ __device__ __forceinline__ bool softmax_block_fp8(Smem<true>& sm, int t, int r, 
   }
   tmem_st32(p_addr, pk);  // waited for (tcgen05.wait::st) before p_full below
   if (rescale && has_o) {
-#pragma unroll
-    for (int c = 0; c < HD / 32; ++c) {
-      uint32_t o[32];
-      tmem_ld32(o_addr + c * 32, o);
-      tmem_ld_wait(o);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-      tmem_st32(o_addr + c * 32, o);
-    }
+    // O and l: one 128-column TMEM load, packed products, one store
+    uint32_t o[HD];
+    tmem_ld128(o_addr, o);
     uint32_t lv = tmem_ld1(l_addr);
+    tmem_ld_wait(o);
+#pragma unroll
+    for (int i = 0; i < HD; i += 2) {
+      float a0, a1;
+      mul2(a0, a1, __uint_as_float(o[i]), __uint_as_float(o[i + 1]), alpha, alpha);
+      o[i] = __float_as_uint(a0);
+      o[i + 1] = __float_as_uint(a1);
+    }
+    tmem_st128(o_addr, o);
     tmem_ld_wait(lv);
     tmem_st1(l_addr, __float_as_uint(__uint_as_float(lv) * alpha));
   }
