@@ -19,8 +19,11 @@ with p in units where the row max is 1 (p_m = exp(s_m - s_max), l = sum p),
                               by 2^-6 for the fp32 score and exp2 arithmetic
         + 2^-18               the subnormal E4M3 step (2^-10 of a code of 256)
                               when 256 p < 2^-6, in the same units,
-  2^-8 |o_i|                  the packed-f16 row sum of the code values
-                              (four adds per partial sum, 2^-11 each),
+  2^-8 |o_i|                  the row sum: exact in fp32 for the E4M3 blocks
+                              (P times ones on the tensor core); the BF16
+                              repair blocks of the VC instance weight V by
+                              bf16(p) but add the unrounded p, a mismatch of
+                              at most 2^-9 |o_i|,
   2^-9 |o_i|                  the bf16 rounding of the output.
 
 Everything here is computed in fp64 from the oracle's dequantised inputs
