@@ -92,10 +92,25 @@ constexpr int BN = 128;             // keys per tile
 constexpr int HD = 128;             // head dim
 constexpr int TILES = 2;            // query tiles per CTA
 constexpr int CTA_ROWS = TILES * BM;
-constexpr int WARP_LOAD_K = 4 * TILES;          // 8: TMA producer of the K ring
-constexpr int WARP_MMA = WARP_LOAD_K + 1;       // 9: MMA issuer, TMEM owner
-constexpr int WARP_LOAD_V = WARP_MMA + 1;       // 10: TMA producer of Q and the V ring
-constexpr int THREADS = 32 * (WARP_LOAD_V + 1); // 352
+// Warp roles of an instance.  The BF16, Sol and repair instances run one
+// softmax thread per row (4 warps per tile, 32x32b TMEM accesses).  The plain
+// FP8 instance (SPLIT) runs 8 warps per tile: warp w of a tile takes 16 of
+// the 32 TMEM lanes of quadrant w % 4 (16x64b accesses), and two threads
+// share each row, one with the even and one with the odd key columns.  Twice
+// the softmax warps per scheduler hide the latency of the per-row chains
+// (max, exp2, pack) that bound the FP8 kernel, whose MMAs take half the time
+// of the BF16 ones.
+template <bool FP8, bool REP, bool SOL>
+struct Roles {
+  static constexpr bool SPLIT = FP8 && !REP && !SOL;
+  static constexpr int SOFTMAX_WARPS = (SPLIT ? 8 : 4) * TILES;
+  static constexpr int LOAD_K = SOFTMAX_WARPS;  // TMA producer of the K ring
+  static constexpr int MMA = LOAD_K + 1;        // MMA issuer, TMEM owner
+  static constexpr int LOAD_V = MMA + 1;        // TMA producer of Q and the V ring
+  static constexpr int MMA_PV = LOAD_V + 1;     // SPLIT: issuer of the P.V and row-sum MMAs
+  static constexpr int THREADS = 32 * (SPLIT ? MMA_PV + 1 : LOAD_V + 1);  // 352, SPLIT 640
+  static constexpr int TILE_THREADS = 32 * SOFTMAX_WARPS / TILES;  // p_full / s_free arrivals per tile
+};
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t HALF = BM * 128;  // one SW128 block: 128 rows x 128 bytes = 16 KB
 
@@ -144,6 +159,7 @@ struct __align__(1024) Smem {
   uint64_t vrep_full, vrep_empty;      // REP: the repair V tile slot
   uint64_t qbf_free;                   // REP: last repair QK of both tiles done
   uint64_t mma_drain;
+  uint64_t mma_drain2;                 // SPLIT: the P.V issuer's own drain
   uint64_t never;  // nothing arrives here (forced-timeout debug path)
   uint32_t tmem_base;
   int abort;
@@ -580,6 +596,92 @@ __device__ __forceinline__ void mma_issuer(Smem<FP8>& sm, uint32_t tmem, int nkv
   mbar_drain(&sm.mma_drain, 0, err);
 }
 
+// SPLIT: the MMAs come from two warps.  A single issuing thread spent each
+// block on six barrier checks in a row between its MMA groups, and the
+// tensor pipe drained meanwhile (a per-block trace: ~1200 of ~2480 cycles).
+// The QK and the P.V streams touch disjoint TMEM (the S region; O, l and P),
+// and each has its own barriers, so one warp issues the QKs and another the
+// P.V and row-sum MMAs: one's waits overlap the other's issue.  A commit
+// tracks the MMAs of its own thread, which is all each barrier needs.
+//
+// QK warp, per block j: QK_1(j) after s_free_0(j), QK_0(j+1) after
+// s_free_1(j) (both tiles' scores go through the one S region in turns).
+__device__ __forceinline__ void mma_qk_split(Smem<true>& sm, uint32_t tmem, int nkv, volatile int* ab,
+                                             uint32_t* err) {
+  constexpr uint32_t TILE = Traits<true>::TILE;
+  constexpr int KST = Traits<true>::KST;
+  uint64_t qd[TILES];
+#pragma unroll
+  for (int t = 0; t < TILES; ++t) qd[t] = sdesc_sw128(smem_u32(sm.q[t]), 16, 1024);
+  const uint64_t kd0 = sdesc_sw128(smem_u32(sm.k[0]), 16, 1024);
+  const uint32_t s_tmem = tmem + col_s(0);
+  if (!mbar_wait(&sm.k_full[0], 0, ab, err)) return;
+  if (!mbar_wait(&sm.q_full[0], 0, ab, err)) return;
+  tc_fence_after_sync();
+  issue_qk<true>(s_tmem, qd[0], kd0);
+  mma_commit(&sm.s_full[0]);
+  for (int j = 0; j < nkv; ++j) {
+    const int ks = j % KST;
+    if (j == 0 && !mbar_wait(&sm.q_full[1], 0, ab, err)) return;
+    if (!mbar_wait(&sm.s_free[0], j & 1, ab, err)) return;
+    tc_fence_after_sync();
+    issue_qk<true>(s_tmem, qd[1], desc_at(kd0, ks * TILE));
+    mma_commit(&sm.s_full[1]);
+    mma_commit(&sm.k_empty[ks]);
+    if (j + 1 < nkv) {
+      const int kn = (j + 1) % KST;
+      if (!mbar_wait(&sm.k_full[kn], ((j + 1) / KST) & 1, ab, err)) return;
+      if (!mbar_wait(&sm.s_free[1], j & 1, ab, err)) return;
+      tc_fence_after_sync();
+      issue_qk<true>(s_tmem, qd[0], desc_at(kd0, kn * TILE));
+      mma_commit(&sm.s_full[0]);
+    }
+  }
+}
+
+// P.V warp, per block j: PV_t(j) and l_t += P_t 1 after p_full_t(j), for
+// t = 0, 1 (V_j must be in); o_done_t, then v_empty and, after the last
+// block, o_full_t.
+__device__ __forceinline__ void mma_pv_split(Smem<true>& sm, uint32_t tmem, int nkv, volatile int* ab,
+                                             uint32_t* err) {
+  {  // the ones tile of the row sums, 64 bytes per lane
+    uint4* o = reinterpret_cast<uint4*>(ones_tile(sm)) + (threadIdx.x & 31) * 4;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[i] = make_uint4(0x38383838u, 0x38383838u, 0x38383838u, 0x38383838u);
+    fence_proxy_async_smem();
+    __syncwarp();
+  }
+  constexpr uint32_t TILE = Traits<true>::TILE;
+  constexpr int VST = Traits<true>::VST;
+  const uint64_t vd0 = sdesc_sw128(smem_u32(sm.v[0]), 16, 1024);
+  const uint64_t od = sdesc_sw128(smem_u32(ones_tile(sm)), 16, 1024);
+  for (int j = 0; j < nkv; ++j) {
+    const int vs = j % VST;
+    if (!mbar_wait(&sm.v_full[vs], (j / VST) & 1, ab, err)) return;
+#pragma unroll
+    for (int t = 0; t < TILES; ++t) {
+      if (!mbar_wait(&sm.p_full[t], j & 1, ab, err)) return;
+      tc_fence_after_sync();
+      issue_pv<true>(tmem + col_o(t), tmem + col_p(t), desc_at(vd0, vs * TILE), j > 0);
+      issue_l_e4m3(tmem + col_l(t), tmem + col_p(t), od, j > 0);
+      mma_commit(&sm.o_done[t]);
+      if (j == nkv - 1) mma_commit(&sm.o_full[t]);
+    }
+    mma_commit(&sm.v_empty[vs]);
+  }
+}
+
+// Either SPLIT issuer, then the drain of its own MMAs (before TMEM goes).
+template <bool QK>
+__device__ __forceinline__ void mma_split(Smem<true>& sm, uint32_t tmem, int nkv, volatile int* ab,
+                                          uint32_t* err) {
+  if (QK) mma_qk_split(sm, tmem, nkv, ab, err);
+  else mma_pv_split(sm, tmem, nkv, ab, err);
+  uint64_t* drain = QK ? &sm.mma_drain : &sm.mma_drain2;
+  mma_commit(drain);
+  mbar_drain(drain, 0, err);
+}
+
 // Two E4M3 codes (round to nearest even, saturating) of a float pair, a in the low byte.
 __device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
   return __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
@@ -618,15 +720,16 @@ __device__ __forceinline__ void convert_q_row(Smem<FP8>& sm, int t, int r) {
   }
 }
 
-// Max of a row's 128 scores: four chains of three-input max, sixteen deep
-// (eight chains measured 1 % slower in BF16 at N = 4608, the same in FP8).
+// Max of a thread's NS scores: four chains of three-input max (eight chains
+// measured 1 % slower in BF16 at N = 4608, the same in FP8).
 constexpr int kMaxChains = 4;
-__device__ __forceinline__ float row_max128(const uint32_t (&s)[BN]) {
+template <int NS>
+__device__ __forceinline__ float row_max(const uint32_t (&s)[NS]) {
   float acc[kMaxChains];
 #pragma unroll
   for (int c = 0; c < kMaxChains; ++c) acc[c] = fmaxf(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1]));
 #pragma unroll
-  for (int i = 2 * kMaxChains; i < BN; i += 2 * kMaxChains) {
+  for (int i = 2 * kMaxChains; i < NS; i += 2 * kMaxChains) {
 #pragma unroll
     for (int c = 0; c < kMaxChains; ++c)
       acc[c] = fmax3(acc[c], __uint_as_float(s[i + 2 * c]), __uint_as_float(s[i + 2 * c + 1]));
@@ -676,7 +779,7 @@ __device__ __forceinline__ bool softmax_block(Smem<FP8>& sm, int t, uint32_t s_a
       if (i >= valid) s[i] = __float_as_uint(-INFINITY);
   }
   // Row max: four independent chains of three-input max (depth 16, not 127).
-  const float mx = row_max128(s);
+  const float mx = row_max(s);
   const float m_tile = fmaxf(m, mx * sl2);
   // One decision per warp (TMEM moves are warp-wide); each row keeps its own alpha.
   const bool rescale = __any_sync(0xFFFFFFFFu, m_tile > m + kRescale);
@@ -752,7 +855,7 @@ __device__ __forceinline__ bool softmax_block_fp8(Smem<true>& sm, int t, int r, 
     for (int i = 0; i < BN; ++i)
       if (i >= valid) s[i] = __float_as_uint(-INFINITY);
   }
-  const float mx = row_max128(s);
+  const float mx = row_max(s);
   const float m_tile = fmaxf(m, mx * sl2);
   const bool rescale = __any_sync(0xFFFFFFFFu, m_tile > m + kRescale);
   const float m_new = rescale ? m_tile : m;
@@ -909,10 +1012,161 @@ __device__ __forceinline__ void softmax_epilogue(Smem<FP8>& sm, uint32_t tmem, c
   }
 }
 
+// ---------------------------------------------------------------- SPLIT FP8
+// The plain FP8 instance with two threads per row (Roles::SPLIT).  Thread i
+// of a warp owns lane (i / 4 + 8 (i % 2)) of the warp's 16 TMEM lanes and the
+// key columns of parity (i / 2) % 2: its 64 scores of a block are keys
+// 2k + par, k = 0..63 (16x64b loads).  The row max takes one shuffle with the
+// partner thread (i ^ 2).  Its P codes go out with the same shape: register
+// k' is P column 2k' + par, whose four bytes the P.V MMA takes as keys
+// 4 (2k' + par) + b -- the thread puts there the codes of its scores 4k' + b,
+// keys 8k' + 2b + par.  So within every 8 keys the MMA's K order is the key
+// order 0, 2, 4, 6, 1, 3, 5, 7, and V^T is stored in that order
+// (fp8_vt_kernel<true>); S, the masking and the row sums see keys in order.
+
+struct SplitLanes {
+  uint32_t s, o, l, p;  // TMEM addresses of this warp's 16 lanes (S, O_t, l_t, P_t)
+  int par;              // key / column parity of this thread
+};
+
+// One key block of the online softmax of tile t for one SPLIT warp: wait for
+// S, mask keys >= valid, max (with the partner thread), exp2 into E4M3 codes,
+// wait for the previous P.V (it read P and wrote O, l), store P, rescale O
+// and l when the max moved, hand P to the MMA thread.
+__device__ __forceinline__ bool softmax_block_split(Smem<true>& sm, int t, const SplitLanes& a, uint32_t phase,
+                                                    int jm, int valid, float sl2, float& m, volatile int* ab,
+                                                    uint32_t* err) {
+  constexpr float kPBias = 8.f;  // P = E4M3 of 256 p: folded into the exponent, cancels against l
+  bool ok = mbar_wait(&sm.s_full[t], phase, ab, err);
+  if (__any_sync(0xFFFFFFFFu, !ok)) return false;
+  tc_fence_after_sync();
+  uint32_t s[BN / 2];
+  tmem_ld16x64(a.s, s);
+  tmem_ld_wait(s);
+  tc_fence_before_sync();
+  mbar_arrive(&sm.s_free[t]);  // the S region may take the next QK now
+  if (valid < BN) {
+#pragma unroll
+    for (int k = 0; k < BN / 2; ++k)
+      if (2 * k + a.par >= valid) s[k] = __float_as_uint(-INFINITY);
+  }
+  float mx = row_max(s);
+  mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));  // the row's other half
+  const float m_tile = fmaxf(m, mx * sl2);
+  // one decision per warp (TMEM moves are warp-wide); P = E4M3 of 256 p needs
+  // the exact running max, so any rise rescales
+  const bool rescale = __any_sync(0xFFFFFFFFu, m_tile > m);
+  const float m_new = rescale ? m_tile : m;
+  const float alpha = rescale ? ex2_approx(m - m_new) : 1.f;  // 0 on the first block
+  const float nm = kPBias - m_new;
+  uint32_t pk[BN / 8];
+#pragma unroll
+  for (int i = 0; i < BN / 8; ++i) {
+    float x0, x1, x2, x3;
+    fma2(x0, x1, __uint_as_float(s[4 * i]), __uint_as_float(s[4 * i + 1]), sl2, sl2, nm, nm);
+    fma2(x2, x3, __uint_as_float(s[4 * i + 2]), __uint_as_float(s[4 * i + 3]), sl2, sl2, nm, nm);
+    pk[i] = e4m3x2(ex2_approx(x0), ex2_approx(x1)) | (e4m3x2(ex2_approx(x2), ex2_approx(x3)) << 16);
+  }
+  if (jm > 0) {
+    ok = mbar_wait(&sm.o_done[t], (jm - 1) & 1, ab, err);
+    if (__any_sync(0xFFFFFFFFu, !ok)) return false;
+    tc_fence_after_sync();
+  }
+  tmem_st16x16(a.p, pk);  // waited for (tcgen05.wait::st) before p_full below
+  if (rescale && jm > 0) {
+    // this thread's 64 of the row's O columns, and its l column (the row sum
+    // MMA writes 16 equal columns; the pair keeps columns 0 and 1 scaled)
+    uint32_t o[HD / 2];
+    tmem_ld16x64(a.o, o);
+    uint32_t lv = tmem_ld16x1(a.l);
+    tmem_ld_wait(o);
+#pragma unroll
+    for (int i = 0; i < HD / 2; i += 2) {
+      float a0, a1;
+      mul2(a0, a1, __uint_as_float(o[i]), __uint_as_float(o[i + 1]), alpha, alpha);
+      o[i] = __float_as_uint(a0);
+      o[i + 1] = __float_as_uint(a1);
+    }
+    tmem_st16x64(a.o, o);
+    tmem_ld_wait(lv);
+    tmem_st16x1(a.l, __float_as_uint(__uint_as_float(lv) * alpha));
+  }
+  tmem_st_wait();
+  m = m_new;
+  tc_fence_before_sync();
+  mbar_arrive(&sm.p_full[t]);
+  return true;
+}
+
+// Softmax and epilogue of query tile t for one SPLIT warp (8 per tile).  The
+// epilogue switches to whole rows: the two warps of a TMEM quadrant read its
+// 32 lanes with 32x32b loads, warp half hh taking O columns 64 hh .. +63,
+// which is output half hh of the tile (head dims 64 hh ..).
+__device__ __forceinline__ void softmax_epilogue_split(Smem<true>& sm, uint32_t tmem, const Params& prm, int b,
+                                                       int h, int row0, int t, int nkv, volatile int* ab,
+                                                       const CUtensorMap* tm_o) {
+  const int wt = (threadIdx.x >> 5) & 7;  // warp within the tile
+  const int qd = wt & 3;                  // TMEM lane quadrant (= warp % 4)
+  const int hh = wt >> 2;                 // which 16 lanes of the quadrant; later, which output half
+  const int i = threadIdx.x & 31;
+  SplitLanes a;
+  const uint32_t lanes16 = static_cast<uint32_t>(32 * qd + 16 * hh) << 16;
+  a.s = tmem + lanes16 + col_s(0);
+  a.o = tmem + lanes16 + col_o(t);
+  a.l = tmem + lanes16 + col_l(t);
+  a.p = tmem + lanes16 + col_p(t);
+  a.par = (i >> 1) & 1;
+  const float* sc = prm.scales + 3 * (static_cast<size_t>(b) * prm.H + h);
+  const float sl2 = prm.scale_log2 * __ldg(sc) * __ldg(sc + 1);
+  const float out_scale = __ldg(sc + 2);
+  float m = -INFINITY;  // running max of this thread's row, log2 units
+  bool ok = true;
+  for (int j = 0; j < nkv && ok; ++j)
+    ok = softmax_block_split(sm, t, a, j & 1, j, prm.main_keys - j * BN, sl2, m, ab, prm.err);
+  if (ok) {
+    ok = mbar_wait(&sm.o_full[t], 0, ab, prm.err);
+    if (__any_sync(0xFFFFFFFFu, !ok)) ok = false;
+  }
+  if (!ok) return;
+  tc_fence_after_sync();
+  const int r = 32 * qd + i;  // row of the tile for the epilogue
+  const uint32_t lanes32 = static_cast<uint32_t>(32 * qd) << 16;
+  uint32_t lv = tmem_ld1(tmem + lanes32 + col_l(t));  // the tensor core's row sum (column 0)
+  tmem_ld_wait(lv);
+  const float inv_l = out_scale / __uint_as_float(lv);
+  // output half hh of the tile -> its 16 KB staging block, SW128 layout of the
+  // out tensor map: row r at byte 128 r, 16-byte chunk k at k ^ (r % 8)
+  uint8_t* stage = hh == 0 ? sm.q[t] : out_stage(sm, t);
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    uint32_t o[32];
+    tmem_ld32(tmem + lanes32 + col_o(t) + 64 * hh + 32 * c, o);
+    tmem_ld_wait(o);
+    uint32_t w[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+      w[k] = pack_bf16x2(__uint_as_float(o[2 * k]) * inv_l, __uint_as_float(o[2 * k + 1]) * inv_l);
+#pragma unroll
+    for (int k4 = 0; k4 < 4; ++k4) {
+      const int k = c * 4 + k4;
+      *reinterpret_cast<uint4*>(stage + r * 128 + ((k ^ (r & 7)) << 4)) =
+          make_uint4(w[4 * k4], w[4 * k4 + 1], w[4 * k4 + 2], w[4 * k4 + 3]);
+    }
+  }
+  fence_proxy_async_smem();
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + t), "n"(2 * BM) : "memory");
+  if (wt == 0 && i == 0) {
+    tma_store_4d(tm_o, smem_u32(sm.q[t]), 0, h, row0, b);  // rows >= N are clipped
+    tma_store_4d(tm_o, smem_u32(out_stage(sm, t)), 64, h, row0, b);
+    bulk_commit();
+    bulk_wait_read_all();
+  }
+}
+
 // tm_kr, tm_vr: the repair K and V tiles (REP; bf16 [B*H, R, 128], boxes of
 // 64 dims x 128 rows); other instances never read them.
 template <bool FP8, bool REP = false, bool SOL = false>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__((Roles<FP8, REP, SOL>::THREADS), 1)
     attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                 const __grid_constant__ CUtensorMap tm_kr, const __grid_constant__ CUtensorMap tm_vr,
@@ -920,6 +1174,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   static_assert(FP8 || !REP, "the repair blocks belong to the FP8 kernel");
   static_assert(!FP8 || !SOL, "the block-sparse kernel is BF16");
   constexpr int KST = Traits<FP8>::KST, VST = Traits<FP8>::VST;
+  using R = Roles<FP8, REP, SOL>;
   extern __shared__ uint8_t smem_raw[];
   Smem<FP8>& sm =
       *reinterpret_cast<Smem<FP8>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -935,14 +1190,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int t = 0; t < TILES; ++t) {
       mbar_init(&sm.q_full[t], 1);
       mbar_init(&sm.s_full[t], 1);
-      mbar_init(&sm.p_full[t], BM);
+      mbar_init(&sm.p_full[t], R::TILE_THREADS);
       mbar_init(&sm.o_full[t], 1);
     }
     for (int s = 0; s < KST; ++s) { mbar_init(&sm.k_full[s], 1); mbar_init(&sm.k_empty[s], 1); }
     for (int s = 0; s < VST; ++s) { mbar_init(&sm.v_full[s], 1); mbar_init(&sm.v_empty[s], 1); }
     for (int t = 0; t < TILES; ++t) {
       mbar_init(&sm.qbf_full[t], BM);
-      mbar_init(&sm.s_free[t], BM);
+      mbar_init(&sm.s_free[t], R::TILE_THREADS);
       mbar_init(&sm.o_done[t], 1);
     }
     mbar_init(&sm.krep_full, 1);
@@ -951,20 +1206,21 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(&sm.vrep_empty, 1);
     mbar_init(&sm.qbf_free, 1);
     mbar_init(&sm.mma_drain, 1);
+    mbar_init(&sm.mma_drain2, 1);
     mbar_init(&sm.never, 1);
     sm.abort = 0;
     fence_mbarrier_init();
   }
-  if (warp == WARP_LOAD_V && lane == 0) {
+  if (warp == R::LOAD_V && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_v);
     if (REP) tma_prefetch_desc(&tm_vr);
   }
-  if (warp == WARP_LOAD_K && lane == 0) {
+  if (warp == R::LOAD_K && lane == 0) {
     tma_prefetch_desc(&tm_k);
     if (REP) tma_prefetch_desc(&tm_kr);
   }
-  if (warp == WARP_MMA) {
+  if (warp == R::MMA) {
     tmem_alloc(&sm.tmem_base, TMEM_COLS);
     tmem_relinquish();
   }
@@ -990,16 +1246,28 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncthreads();
   }
 
-  if (warp == WARP_LOAD_K) {
+  if (warp == R::LOAD_K) {
     if (lane == 0 && !*ab) load_k<FP8, REP, SOL>(sm, &tm_k, &tm_kr, bh, nkv, prm.nrep, lst, ab, prm.err);
     __syncwarp();
-  } else if (warp == WARP_LOAD_V) {
+  } else if (warp == R::LOAD_V) {
     if (lane == 0 && !*ab)
       load_qv<FP8, REP, SOL>(sm, &tm_q, &tm_v, &tm_vr, q0, bh, b, h, nkv, prm.nrep, lst, ab, prm.err);
     __syncwarp();
-  } else if (warp == WARP_MMA) {
-    if (!*ab) mma_issuer<FP8, REP>(sm, tmem, nkv, prm.nrep, ab, prm.err);  // the whole warp: see mma_commit
+  } else if (warp == R::MMA) {
+    if constexpr (R::SPLIT) {
+      if (!*ab) mma_split<true>(sm, tmem, nkv, ab, prm.err);  // the QKs (the whole warp: see mma_commit)
+    } else {
+      if (!*ab) mma_issuer<FP8, REP>(sm, tmem, nkv, prm.nrep, ab, prm.err);  // the whole warp: see mma_commit
+    }
     __syncwarp();
+  } else if (R::SPLIT && warp == R::MMA_PV) {
+    if constexpr (R::SPLIT) {
+      if (!*ab) mma_split<false>(sm, tmem, nkv, ab, prm.err);  // the P.Vs and row sums
+    }
+    __syncwarp();
+  } else if constexpr (R::SPLIT) {
+    const int t = warp / (R::SOFTMAX_WARPS / TILES);  // query tile of this warp
+    if (!*ab) softmax_epilogue_split(sm, tmem, prm, b, h, q0 + t * BM, t, nkv, ab, &tm_o);
   } else {
     const int t = warp >> 2;  // query tile of this warpgroup
     if (!*ab) softmax_epilogue<FP8, REP, SOL>(sm, tmem, prm, b, h, q0 + t * BM, t, nkv, lst, ab, &tm_o);
@@ -1007,7 +1275,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-  if (warp == WARP_MMA) tmem_dealloc(tmem, TMEM_COLS);
+  if (warp == R::MMA) tmem_dealloc(tmem, TMEM_COLS);
 }
 
 }  // namespace attn

@@ -266,8 +266,11 @@ int launch_prologue_fp8(flux_attn* h, const void* q, const void* k, const void* 
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "amax launch");
   const int R = repair_count(h, n);
-  flux::fp8_vt_kernel<<<vgrid, flux::kVtThreads, 0, stream>>>(tv, tvt, H, h->amax, h->err, R > 0 ? h->errv : nullptr,
-                                                             n);
+  // V^T in the plain attention's key order, natural for the repair instance
+  if (R > 0)
+    flux::fp8_vt_kernel<false><<<vgrid, flux::kVtThreads, 0, stream>>>(tv, tvt, H, h->amax, h->err, h->errv, n);
+  else
+    flux::fp8_vt_kernel<true><<<vgrid, flux::kVtThreads, 0, stream>>>(tv, tvt, H, h->amax, h->err, nullptr, n);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "V^T launch");
   {
@@ -379,7 +382,10 @@ int launch_attention(flux_attn* h, bool fp8, const void* qn, const void* kn, con
   // (griddepcontrol.wait) before its first global read.
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3((n + CTA_ROWS - 1) / CTA_ROWS, B * H);
-  lc.blockDim = dim3(THREADS);
+  lc.blockDim = dim3(R > 0   ? Roles<true, true, false>::THREADS
+                     : fp8   ? Roles<true, false, false>::THREADS
+                     : sol_list != nullptr ? Roles<false, false, true>::THREADS
+                                           : Roles<false, false, false>::THREADS);
   lc.dynamicSmemBytes = fp8 ? smem_bytes<true>() : smem_bytes<false>();
   lc.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -1013,7 +1019,8 @@ static int launch_qkv_fp8(flux_attn* h, const void* x, const void* w_qkv, const 
   CUtensorMap tv, tvt;
   if ((rc = encode_v_maps(h, h->vw, v8t, n, &tv, &tvt))) return rc;
   const dim3 vgrid((n + flux::kVtTokens - 1) / flux::kVtTokens, B * H);
-  flux::fp8_vt_kernel<<<vgrid, flux::kVtThreads, 0, stream>>>(tv, tvt, H, h->amax, h->err, nullptr, n);
+  // the plain FP8 attention's key order (VC handles do not take this path)
+  flux::fp8_vt_kernel<true><<<vgrid, flux::kVtThreads, 0, stream>>>(tv, tvt, H, h->amax, h->err, nullptr, n);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "V^T launch");
   const size_t items = 2ull * B * H * n * flux::kHeadDim / 16;

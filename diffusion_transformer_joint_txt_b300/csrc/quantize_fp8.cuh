@@ -19,7 +19,9 @@
 //                                       q8, k8   [B, H, N, 128]
 //                                       scales   fp32 [B, H, 3] = (s_q, s_k, s_v)
 //   fp8_vt_kernel                     v8t E4M3 [B, H, 128, Npad] (V transposed,
-//                                     keys contiguous; columns N..Npad-1 zero)
+//                                     keys contiguous; columns N..Npad-1 zero;
+//                                     for the plain FP8 attention the keys of
+//                                     every 8 in the order 0 2 4 6 1 3 5 7)
 // Recomputing Q', K' in the second pass costs less than a round trip of an
 // fp32 or bf16 copy through HBM, and keeps a single rounding, fp32 -> E4M3.
 #pragma once
@@ -228,11 +230,18 @@ __global__ void __launch_bounds__(kVtThreads)
 // the tile at v8t[b, h, :, n0 .. n0+63] (clipped at Npad; the zero tokens
 // between N and Npad become the zero padding).
 //
-// With errv set (VC-Attention repair) the kernel also writes, per token of
+// MMA_ORDER: within every 8 tokens the columns hold tokens 0, 2, 4, 6, 1, 3,
+// 5, 7 -- the key order of the P.V MMA in the plain FP8 attention, whose
+// softmax threads hold the even or the odd keys of a row (attention.cuh).
+// Tiles start at multiples of 64 tokens, so the groups of 8 are those of
+// the key blocks, and Npad (a multiple of 16) never splits one.
+//
+// With errv set (VC-Attention repair, natural order only) the kernel also writes, per token of
 // the tile, the squared quantisation error |v - code s_v|^2 of its V row:
 // thread d holds dim d of the 64 tokens, a butterfly over the lanes leaves
 // lane l of warp w with the sums over its 32 dims of tokens 2l and 2l + 1,
 // and thread t < 64 adds the four warps' sums of token t, in a fixed order.
+template <bool MMA_ORDER>
 __global__ void __launch_bounds__(kVtThreads)
     fp8_vt_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_vt, int H,
                   const uint32_t* __restrict__ amax, uint32_t* err, float* __restrict__ errv, int N) {
@@ -268,16 +277,19 @@ __global__ void __launch_bounds__(kVtThreads)
   };
   uint32_t w[kVtTokens / 4];
 #pragma unroll
-  for (int t = 0; t < kVtTokens; t += 4) {
+  for (int i = 0; i < kVtTokens / 4; ++i) {
+    // byte b of word i: token 4i + b, or (MMA_ORDER) 8 (i / 2) + i % 2 + 2b
+    const int t = MMA_ORDER ? 8 * (i >> 1) + (i & 1) : 4 * i;
+    const int st = MMA_ORDER ? 2 : 1;
     const float x0 = code_value(__bfloat162float(vin[t][d]));
-    const float x1 = code_value(__bfloat162float(vin[t + 1][d]));
-    const float x2 = code_value(__bfloat162float(vin[t + 2][d]));
-    const float x3 = code_value(__bfloat162float(vin[t + 3][d]));
-    w[t / 4] = __nv_cvt_float2_to_fp8x2(make_float2(x0, x1), __NV_SATFINITE, __NV_E4M3) |
-               (static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(x2, x3), __NV_SATFINITE, __NV_E4M3))
-                << 16);
+    const float x1 = code_value(__bfloat162float(vin[t + st][d]));
+    const float x2 = code_value(__bfloat162float(vin[t + 2 * st][d]));
+    const float x3 = code_value(__bfloat162float(vin[t + 3 * st][d]));
+    w[i] = __nv_cvt_float2_to_fp8x2(make_float2(x0, x1), __NV_SATFINITE, __NV_E4M3) |
+           (static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(x2, x3), __NV_SATFINITE, __NV_E4M3))
+            << 16);
   }
-  if (errv != nullptr) {  // block-uniform
+  if (!MMA_ORDER && errv != nullptr) {  // block-uniform
     __shared__ float wsum[kVtThreads / 32][kVtTokens];
     const float sv = am > 0.f ? am / kE4M3Max : 1.f;
     float e[kVtTokens];

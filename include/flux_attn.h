@@ -152,7 +152,9 @@ FLUX_ATTN_API int flux_attn_attend(flux_attn_t h, const void* qn, const void* kn
  * quotient, ties included; Q', K' are computed in fp32, so a value within fp32
  * rounding of a midpoint between two codes may take the neighbouring code.
  *   q8, k8  uint8 [B, H, N, 128];  v8t  uint8 [B, H, 128, Npad] (V transposed,
- *   Npad = N rounded up to a multiple of 16, padding columns zero)
+ *   Npad = N rounded up to a multiple of 16, padding columns zero; within
+ *   every 8 columns, 8g .. 8g+7, the tokens 8g + 0, 2, 4, 6, 1, 3, 5, 7: the
+ *   key order of flux_attn_attend_fp8's P.V MMA)
  *   scales  fp32 [B, H, 3] = (scale_q, scale_k, scale_v) */
 FLUX_ATTN_API int flux_attn_prologue_fp8(flux_attn_t h, const void* q, const void* k, const void* v,
                            int txt_len, int img_h, int img_w, int ref_h, int ref_w,
@@ -177,7 +179,8 @@ FLUX_ATTN_API int flux_attn_attend_fp8(flux_attn_t h, const void* q8, const void
  * K' and codes; equal errors: lower index first):
  *   repair_idx  int32 [B, H, R]: the repaired tokens, ascending
  *   k8, v8t     the codes of the N - R other tokens sit in positions
- *               0 .. N-R-1 (a repaired token's position below N - R receives,
+ *               0 .. N-R-1, in token order (no 8-column interleave in v8t)
+ *               (a repaired token's position below N - R receives,
  *               in order, the codes of a non-repaired token from the last R
  *               positions); positions N-R .. N-1 are not read afterwards
  *   k_rep, v_rep  bf16 [B, H, R, 128]: k' / s_k and v / s_v of the repaired
@@ -248,8 +251,8 @@ FLUX_ATTN_API int flux_attn_qkv(flux_attn_t h, const void* x, const void* w_qkv,
  * epilogue reduces the per-(b, h) |max| of the Q', K', V values it writes;
  * then one pass writes their E4M3 codes with scale = amax / 448, in the
  * layouts flux_attn_attend_fp8 reads:
- *   q8, k8  uint8 [B, H, N, 128];  v8t  uint8 [B, H, 128, pad16(N)];
- *   scales  fp32 [B, H, 3]
+ *   q8, k8  uint8 [B, H, N, 128];  v8t  uint8 [B, H, 128, pad16(N)] (columns in
+ *   the order flux_attn_prologue_fp8 gives them);  scales  fp32 [B, H, 3]
  * The codes are those of the bf16 values (rounded once more than the codes of
  * flux_attn_prologue_fp8, which quantises its fp32 Q', K').  Other arguments
  * as for flux_attn_qkv; UNSUPPORTED for handles with vc_repair_budget > 0. */

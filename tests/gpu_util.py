@@ -54,3 +54,15 @@ def compare(got: np.ndarray, want: np.ndarray, max_abs: float, mean_abs: float =
     if rel_rms is not None:
         assert stats["rel_rms"] <= rel_rms, msg
     return stats
+
+
+def v8t_token_order(v8t: np.ndarray) -> np.ndarray:
+    """V^T codes of the plain FP8 prologue with the columns back in token order.
+    Within every 8 columns the prologue stores tokens 0, 2, 4, 6, 1, 3, 5, 7: the
+    key order of the FP8 attention's P.V MMA, whose softmax threads each hold the
+    even or the odd keys of a row.  Column 8g + 4p + b holds token 8g + 2b + p."""
+    col = np.arange(v8t.shape[-1])
+    token = 8 * (col // 8) + 2 * (col % 4) + (col % 8) // 4
+    out = np.empty_like(v8t)
+    out[..., token] = v8t
+    return out

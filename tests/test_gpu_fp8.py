@@ -23,7 +23,7 @@ import torch
 
 import oracle
 import synthetic
-from gpu_util import FP8_MAX_ABS, FP8_REL_RMS, compare, device_inputs, gather_rows, host_f64
+from gpu_util import FP8_MAX_ABS, FP8_REL_RMS, compare, device_inputs, gather_rows, host_f64, v8t_token_order
 import fp8_bound as fb
 
 pytestmark = pytest.mark.gpu
@@ -89,6 +89,7 @@ def test_fp8_prologue_codes_and_scales(B, H, txt, ih, iw, rh, rw):
     assert attn.sync_status() == 0
     q8, k8, v8t, scales = (t.cpu().numpy() for t in (q8, k8, v8t, scales))
     assert v8t.shape[-1] == fa.pad16(n)
+    v8t = v8t_token_order(v8t)
     for b in range(w.batch):
         for h in range(w.heads):
             oq, ok, ov, osc = oracle.fp8_quantize_head(inp.q, inp.k, inp.v, inp.pos, inp.w_q, inp.w_k, b, h)
@@ -129,7 +130,7 @@ def test_fp8_v_codes_exact_on_adversarial_heads():
     attn = fa.FluxAttention(w.batch, w.heads, n, precision="fp8")
     _, _, v8t, scales = attn.prologue_fp8(d["q"], d["k"], d["v"], *_geom(w), d["q_norm_w"], d["k_norm_w"])
     assert attn.sync_status() == 0
-    v8t, scales = v8t.cpu().numpy(), scales.cpu().numpy()
+    v8t, scales = v8t_token_order(v8t.cpu().numpy()), scales.cpu().numpy()
     for h in range(5):
         _, _, ov, osc = oracle.fp8_quantize_head(inp.q, inp.k, inp.v, inp.pos, inp.w_q, inp.w_k, 0, h)
         assert scales[0, h, 2] == np.float32(osc[2]), h

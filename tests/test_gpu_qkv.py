@@ -12,7 +12,7 @@ import torch
 
 import oracle
 import synthetic
-from gpu_util import dev_bf16, host_f64
+from gpu_util import dev_bf16, host_f64, v8t_token_order
 
 pytestmark = pytest.mark.gpu
 
@@ -210,6 +210,7 @@ def test_qkv_fp8_codes_and_scales(B, H, txt, ih, iw, rh, rw, D):
     N = w.tokens
     oq, ok, ov = oracle.qkv_rows(inp.x, inp.w, inp.bias, N, inp.pos, inp.w_q, inp.w_k, H)   # [B N, H, 128]
     q8h, k8h, v8h, sch = (t.cpu().numpy() for t in (q8, k8, v8t, scales))
+    v8h = v8t_token_order(v8h)
     for bb in range(B):
         for hh in range(H):
             for t, (vals, codes) in enumerate(((oq, q8h[bb, hh]), (ok, k8h[bb, hh]), (ov, v8h[bb, hh, :, :N].T))):
