@@ -10,19 +10,28 @@
 // attention"; this kernel is that step in both precisions.
 //
 // One CTA = two 128-row query tiles (0 and 1) of one (b, h) that share every
-// K/V tile.  Warp roles:
-//   warps 0-3  softmax + epilogue of query tile 0 (thread r owns row r, TMEM lane r;
-//              the output tile leaves through shared memory and a TMA store)
-//   warps 4-7  softmax + epilogue of query tile 1
-//   warp 8     TMA producer of the K ring
-//   warp 9     TMEM allocator and tcgen05.mma issuer (one elected lane)
-//   warp 10    TMA producer of both Q tiles and of the V ring
+// K/V tile.  Warp roles (Roles<>):
+//   BF16, Sol and the repair instance (352 threads):
+//     warps 0-3  softmax + epilogue of query tile 0 (thread r owns row r, TMEM
+//                lane r; the output tile leaves through shared memory and a
+//                TMA store)
+//     warps 4-7  softmax + epilogue of query tile 1
+//     warp 8     TMA producer of the K ring
+//     warp 9     TMEM allocator and tcgen05.mma issuer (one elected lane)
+//     warp 10    TMA producer of both Q tiles and of the V ring
+//   plain FP8 (SPLIT, 640 threads):
+//     warps 0-7 / 8-15  softmax + epilogue of tile 0 / 1: warp w takes 16 of
+//                the 32 TMEM lanes of quadrant w % 4, two threads per row
+//                (the even and the odd keys)
+//     warp 16    K ring; warp 17 TMEM and the QK MMAs; warp 18 Q and the V
+//                ring; warp 19 the P.V and row-sum MMAs
 // TMEM (512 columns).  BF16 (and the repair blocks): S_0 at 0, S_1 at 128,
 // O_0 at 256, O_1 at 384; the softmax of a tile overwrites its S with P, and
 // the P.V MMA reads P straight from TMEM as its A operand.  FP8: one S region
 // at 0 that the tiles take in turns, l_0 / l_1 at 128 / 160, P_0 / P_1 at
-// 192 / 224, O as in BF16 (mma_main_fp8_rs): P has its own columns, so the S
-// region takes the next scores while the softmax still works on these.
+// 192 / 224, O as in BF16: P has its own columns, so the S region takes the
+// next scores while the softmax still works on these, and the QK and P.V
+// streams share no TMEM (which is what lets two warps issue them).
 //
 // BF16: the MMA issue order is  QK_0(0) QK_1(0) | PV_0(j) QK_0(j+1) PV_1(j)
 // QK_1(j+1) | ...  so while the softmax of tile 0 works on S_0(j+1) the
@@ -47,7 +56,8 @@
 // from [B, N, H, 128]).  P is bf16, two per TMEM column.
 //
 // FP8: Q', K' are E4M3 codes [B, H, N, 128] and V is E4M3 transposed
-// [B, H, 128, Npad] (kind::f8f6f4, K = 32 per MMA).  A 128 x 128 tile is one
+// [B, H, 128, Npad] (kind::f8f6f4, K = 32 per MMA; for the plain instance the
+// keys of every 8 in the order 0 2 4 6 1 3 5 7, see SPLIT below).  A 128 x 128 tile is one
 // 16 KB SW128 block, K-major for all three (for V^T the keys are the K
 // dimension of P.V).  P is E4M3 of 256 p; the row sum l adds the values the
 // codes stand for, so that O = sum p~ v / sum p~ is a convex combination of
@@ -418,30 +428,21 @@ __device__ __forceinline__ void issue_l_e4m3(uint32_t l_tmem, uint32_t p_tmem, u
     mma_e4m3_ts(l_tmem, p_tmem + kk * 8, desc_at(od, kk * 32), ID, (accumulate || kk > 0) ? 1u : 0u);
 }
 
-// Whether, in each block of the FP8 main loop, the MMA thread puts the next
-// QK ahead of the P.V it could issue as well (the scores are what a softmax
-// waits for, P.V's result is read later in the block).  Interleaved timing on
-// the CFG pair: plain FP8 3.73 ms with the QK first against 3.81 ms with the
-// P.V first; the repair instance the other way round, 3.90 against 3.83 ms.
-// Either way the wait only moves between s_full and o_done (a per-warp trace
-// of the softmax: 450 against 110-320 cycles on s_full, 150 against 180-480
-// on o_done, of a ~2450-cycle block).
-template <bool REP>
-__host__ __device__ constexpr bool qk_first() { return !REP; }
-
-// FP8 main loop (the MMA thread): P_t in TMEM, the row sums on the tensor
-// core, both tiles' scores through the one S region in turns, so per block j
+// FP8 main loop of the repair instance's single MMA thread (after its repair
+// blocks): P_t in TMEM, the row sums on the tensor core, both tiles' scores
+// through the one S region in turns, so per block j
 //   PV_0(j-1) l_0   [after p_full_0(j-1)]
 //   QK_1(j)         [after s_free_0(j): tile 0 has read S_0(j)]
 //   PV_1(j-1) l_1   [after p_full_1(j-1)]
 //   QK_0(j+1)       [after s_free_1(j): tile 1 has read S_1(j)]
-// -- the order in which those events come when tile 1 runs a little behind
-// tile 0, which this chain itself makes it do.  o_done_t follows each PV_t
-// with its row sum.  REP: after nrep repair blocks; ph = nrep continues the
-// s_full / p_full phases, and PV_t accumulates onto their O from the start.
+// o_done_t follows each PV_t with its row sum.  ph = nrep continues the
+// s_full / p_full phases, and PV_t accumulates onto the repair blocks' O.
+// (Putting QK_1(j) ahead of PV_0(j-1) measured 3.90 against 3.83 ms on the
+// CFG pair here; the plain FP8 instance issues QKs and P.Vs from two warps.)
 template <bool REP>
 __device__ __forceinline__ void mma_main_fp8_rs(Smem<true>& sm, uint32_t tmem, int nkv, int nrep, volatile int* ab,
                                                 uint32_t* err) {
+  static_assert(REP, "the plain FP8 instance has two issuers (mma_split)");
   const int ph = REP ? nrep : 0;
   // the ones tile, 64 bytes per lane (REP: once the last repair P.V, which
   // read V_rep from the same bytes, has completed)
@@ -478,7 +479,7 @@ __device__ __forceinline__ void mma_main_fp8_rs(Smem<true>& sm, uint32_t tmem, i
   mma_commit(&sm.s_full[0]);
   for (int j = 0; j < nkv; ++j) {
     const int ks = j % KST;
-    if (!qk_first<REP>() && j > 0) {
+    if (j > 0) {
       if (!mbar_wait(&sm.v_full[(j - 1) % VST], ((j - 1) / VST) & 1, ab, err)) return;
       if (!pv(0, j - 1)) return;
     }
@@ -488,11 +489,7 @@ __device__ __forceinline__ void mma_main_fp8_rs(Smem<true>& sm, uint32_t tmem, i
     issue_qk<true>(s_tmem, qd[1], desc_at(kd0, ks * TILE));
     mma_commit(&sm.s_full[1]);
     mma_commit(&sm.k_empty[ks]);
-    if (qk_first<REP>() && j > 0) {
-      if (!mbar_wait(&sm.v_full[(j - 1) % VST], ((j - 1) / VST) & 1, ab, err)) return;
-      if (!pv(0, j - 1)) return;
-    }
-    if (!qk_first<REP>() && j > 0) {
+    if (j > 0) {
       if (!pv(1, j - 1)) return;
       mma_commit(&sm.v_empty[(j - 1) % VST]);
     }
@@ -503,10 +500,6 @@ __device__ __forceinline__ void mma_main_fp8_rs(Smem<true>& sm, uint32_t tmem, i
       tc_fence_after_sync();
       issue_qk<true>(s_tmem, qd[0], desc_at(kd0, kn * TILE));
       mma_commit(&sm.s_full[0]);
-    }
-    if (qk_first<REP>() && j > 0) {
-      if (!pv(1, j - 1)) return;
-      mma_commit(&sm.v_empty[(j - 1) % VST]);
     }
   }
   const int jl = nkv - 1;
