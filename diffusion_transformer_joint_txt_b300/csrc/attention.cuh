@@ -11,7 +11,7 @@
 //
 // One CTA = two 128-row query tiles (0 and 1) of one (b, h) that share every
 // K/V tile.  Warp roles (Roles<>):
-//   BF16, Sol and the repair instance (352 threads):
+//   BF16 and Sol (352 threads):
 //     warps 0-3  softmax + epilogue of query tile 0 (thread r owns row r, TMEM
 //                lane r; the output tile leaves through shared memory and a
 //                TMA store)
@@ -19,7 +19,7 @@
 //     warp 8     TMA producer of the K ring
 //     warp 9     TMEM allocator and tcgen05.mma issuer (one elected lane)
 //     warp 10    TMA producer of both Q tiles and of the V ring
-//   plain FP8 (SPLIT, 640 threads):
+//   FP8, plain and with repair blocks (SPLIT, 640 threads):
 //     warps 0-7 / 8-15  softmax + epilogue of tile 0 / 1: warp w takes 16 of
 //                the 32 TMEM lanes of quadrant w % 4, two threads per row
 //                (the even and the odd keys)
@@ -56,15 +56,15 @@
 // from [B, N, H, 128]).  P is bf16, two per TMEM column.
 //
 // FP8: Q', K' are E4M3 codes [B, H, N, 128] and V is E4M3 transposed
-// [B, H, 128, Npad] (kind::f8f6f4, K = 32 per MMA; for the plain instance the
-// keys of every 8 in the order 0 2 4 6 1 3 5 7, see SPLIT below).  A 128 x 128 tile is one
+// [B, H, 128, Npad] (kind::f8f6f4, K = 32 per MMA; the keys of every 8 in
+// the order 0 2 4 6 1 3 5 7, see SPLIT below).  A 128 x 128 tile is one
 // 16 KB SW128 block, K-major for all three (for V^T the keys are the K
 // dimension of P.V).  P is E4M3 of 256 p; the row sum l adds the values the
 // codes stand for, so that O = sum p~ v / sum p~ is a convex combination of
 // the V rows whatever the rounding of P.  Scores are scaled by s_q s_k and
 // the output by s_v (per-(b, h) scales).  P stays in TMEM and the tensor
 // core sums it (P times a tile of ones); the repair blocks of the VC instance
-// sum their bf16 P in registers.
+// sum their bf16 P in registers and hand the sum to the l column.
 //
 // VC-Attention repair (REP, FP8 only; vc_repair.cuh selects the tokens):
 // the CTA first runs ceil(R / 128) repair blocks in BF16 -- K_rep = k' / s_k
@@ -73,10 +73,11 @@
 // the N - R other keys (positions 0 .. N-R-1 of the codes).  The repair QK
 // needs Q in bf16: the softmax warps convert their rows of the E4M3 Q tile
 // (exact: every E4M3 value is a bf16 value) into the V ring's memory, which
-// stays idle until the MMA thread signals the last repair QK (qbf_free); the
+// stays idle until the QK warp signals the last repair QK (qbf_free); the
 // repair K and V tiles have their own 64 KB, which the E4M3 kernel has to
-// spare, so the K ring fills from the start.  A repair block's P is bf16 (as
-// in the BF16 kernel); its row sum adds the fp32 p.
+// spare, so the K ring fills from the start.  A repair block's S and P (bf16,
+// over S) take per-tile columns as in the BF16 kernel; its row sum adds the
+// fp32 p.
 //
 // Sol-Attention (SOL, BF16; sol_sparse.cuh builds the lists): the CTA walks
 // only the key blocks in its list -- the union of the blocks its two query
@@ -102,20 +103,21 @@ constexpr int BN = 128;             // keys per tile
 constexpr int HD = 128;             // head dim
 constexpr int TILES = 2;            // query tiles per CTA
 constexpr int CTA_ROWS = TILES * BM;
-// Warp roles of an instance.  The BF16, Sol and repair instances run one
-// softmax thread per row (4 warps per tile, 32x32b TMEM accesses).  The plain
-// FP8 instance (SPLIT) runs 8 warps per tile: warp w of a tile takes 16 of
-// the 32 TMEM lanes of quadrant w % 4 (16x64b accesses), and two threads
-// share each row, one with the even and one with the odd key columns.  Twice
-// the softmax warps per scheduler hide the latency of the per-row chains
-// (max, exp2, pack) that bound the FP8 kernel, whose MMAs take half the time
-// of the BF16 ones.
+// Warp roles of an instance.  The BF16 and Sol instances run one softmax
+// thread per row (4 warps per tile, 32x32b TMEM accesses) and one MMA issuer.
+// The FP8 instances (SPLIT) run 8 warps per tile: warp w of a tile takes 16
+// of the 32 TMEM lanes of quadrant w % 4 (16-lane TMEM shapes), and two
+// threads share each row of the E4M3 blocks, one with the even and one with
+// the odd key columns; two warps issue the MMAs, one the QKs and one the P.Vs
+// and row sums (mma_split).  The FP8 MMAs take half the time of the BF16
+// ones, and with one thread per row and one issuer the kernel ran at the
+// pace of the softmax chains and of the issuer's barrier checks.
 template <bool FP8, bool REP, bool SOL>
 struct Roles {
-  static constexpr bool SPLIT = FP8 && !REP && !SOL;
+  static constexpr bool SPLIT = FP8 && !SOL;
   static constexpr int SOFTMAX_WARPS = (SPLIT ? 8 : 4) * TILES;
   static constexpr int LOAD_K = SOFTMAX_WARPS;  // TMA producer of the K ring
-  static constexpr int MMA = LOAD_K + 1;        // MMA issuer, TMEM owner
+  static constexpr int MMA = LOAD_K + 1;        // MMA issuer (SPLIT: of the QKs), TMEM owner
   static constexpr int LOAD_V = MMA + 1;        // TMA producer of Q and the V ring
   static constexpr int MMA_PV = LOAD_V + 1;     // SPLIT: issuer of the P.V and row-sum MMAs
   static constexpr int THREADS = 32 * (SPLIT ? MMA_PV + 1 : LOAD_V + 1);  // 352, SPLIT 640
@@ -168,6 +170,7 @@ struct __align__(1024) Smem {
   uint64_t krep_full, krep_empty;      // REP: the repair K tile slot
   uint64_t vrep_full, vrep_empty;      // REP: the repair V tile slot
   uint64_t qbf_free;                   // REP: last repair QK of both tiles done
+  uint64_t lrep_full[TILES];           // SPLIT REP without E4M3 blocks: the repair row sums are in TMEM
   uint64_t mma_drain;
   uint64_t mma_drain2;                 // SPLIT: the P.V issuer's own drain
   uint64_t never;  // nothing arrives here (forced-timeout debug path)
@@ -384,40 +387,6 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint6
   }
 }
 
-// REP: the repair blocks, issued before the main loop -- per block QK_0 QK_1
-// (bf16, Q from the converted tiles, K from the repair slot), then PV_0 PV_1
-// once each tile's P is in.  Commits qbf_free after the last repair QK.
-// Returns false when a wait gave up.
-template <bool FP8>
-__device__ __forceinline__ bool mma_repair(Smem<FP8>& sm, uint32_t tmem, int nrep, volatile int* ab, uint32_t* err) {
-  uint64_t qbd[TILES];
-#pragma unroll
-  for (int t = 0; t < TILES; ++t) qbd[t] = sdesc_sw128(smem_u32(qbf_tile(sm, t)), 16, 1024);
-  const uint64_t krd = sdesc_sw128(smem_u32(krep_tile(sm)), 16, 1024);
-  const uint64_t vrd = sdesc_sw128(smem_u32(vrep_tile(sm)), HALF, 1024);
-  for (int i = 0; i < nrep; ++i) {
-    if (!mbar_wait(&sm.krep_full, i & 1, ab, err)) return false;
-#pragma unroll
-    for (int t = 0; t < TILES; ++t) {
-      if (i == 0 && !mbar_wait(&sm.qbf_full[t], 0, ab, err)) return false;
-      tc_fence_after_sync();
-      issue_qk<false>(tmem + col_s(t), qbd[t], krd);
-      mma_commit(&sm.s_full[t]);
-    }
-    mma_commit(&sm.krep_empty);
-    if (i == nrep - 1) mma_commit(&sm.qbf_free);
-    if (!mbar_wait(&sm.vrep_full, i & 1, ab, err)) return false;
-#pragma unroll
-    for (int t = 0; t < TILES; ++t) {
-      if (!mbar_wait(&sm.p_full[t], i & 1, ab, err)) return false;
-      tc_fence_after_sync();
-      issue_pv<false>(tmem + col_o(t), tmem + col_s(t), vrd, i > 0);
-    }
-    mma_commit(&sm.vrep_empty);
-  }
-  return true;
-}
-
 // l_t (+)= P_t 1: the row sums of P by the tensor core, N = 16 (16 equal
 // columns; the softmax reads the first), 4 MMAs of 128 x 16 x 32 with P from
 // TMEM (p_tmem) and the ones tile from shared memory (od).
@@ -426,89 +395,6 @@ __device__ __forceinline__ void issue_l_e4m3(uint32_t l_tmem, uint32_t p_tmem, u
 #pragma unroll
   for (int kk = 0; kk < BN / 32; ++kk)
     mma_e4m3_ts(l_tmem, p_tmem + kk * 8, desc_at(od, kk * 32), ID, (accumulate || kk > 0) ? 1u : 0u);
-}
-
-// FP8 main loop of the repair instance's single MMA thread (after its repair
-// blocks): P_t in TMEM, the row sums on the tensor core, both tiles' scores
-// through the one S region in turns, so per block j
-//   PV_0(j-1) l_0   [after p_full_0(j-1)]
-//   QK_1(j)         [after s_free_0(j): tile 0 has read S_0(j)]
-//   PV_1(j-1) l_1   [after p_full_1(j-1)]
-//   QK_0(j+1)       [after s_free_1(j): tile 1 has read S_1(j)]
-// o_done_t follows each PV_t with its row sum.  ph = nrep continues the
-// s_full / p_full phases, and PV_t accumulates onto the repair blocks' O.
-// (Putting QK_1(j) ahead of PV_0(j-1) measured 3.90 against 3.83 ms on the
-// CFG pair here; the plain FP8 instance issues QKs and P.Vs from two warps.)
-template <bool REP>
-__device__ __forceinline__ void mma_main_fp8_rs(Smem<true>& sm, uint32_t tmem, int nkv, int nrep, volatile int* ab,
-                                                uint32_t* err) {
-  static_assert(REP, "the plain FP8 instance has two issuers (mma_split)");
-  const int ph = REP ? nrep : 0;
-  // the ones tile, 64 bytes per lane (REP: once the last repair P.V, which
-  // read V_rep from the same bytes, has completed)
-  if (REP && nrep > 0 && !mbar_wait(&sm.vrep_empty, (nrep - 1) & 1, ab, err)) return;
-  {
-    uint4* o = reinterpret_cast<uint4*>(ones_tile(sm)) + (threadIdx.x & 31) * 4;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) o[i] = make_uint4(0x38383838u, 0x38383838u, 0x38383838u, 0x38383838u);
-    fence_proxy_async_smem();
-    __syncwarp();
-  }
-  constexpr uint32_t TILE = Traits<true>::TILE;
-  constexpr int KST = Traits<true>::KST, VST = Traits<true>::VST;
-  uint64_t qd[TILES];
-#pragma unroll
-  for (int t = 0; t < TILES; ++t) qd[t] = sdesc_sw128(smem_u32(sm.q[t]), 16, 1024);
-  const uint64_t kd0 = sdesc_sw128(smem_u32(sm.k[0]), 16, 1024);
-  const uint64_t vd0 = sdesc_sw128(smem_u32(sm.v[0]), 16, 1024);
-  const uint64_t od = sdesc_sw128(smem_u32(ones_tile(sm)), 16, 1024);
-  const uint32_t s_tmem = tmem + col_s(0);
-  // PV_t(j) and l_t after P_t(j) is in (V_j must be in)
-  auto pv = [&](int t, int j) -> bool {
-    if (!mbar_wait(&sm.p_full[t], (j + ph) & 1, ab, err)) return false;
-    tc_fence_after_sync();
-    issue_pv<true>(tmem + col_o(t), tmem + col_p(t), desc_at(vd0, (j % VST) * TILE), j + ph > 0);
-    issue_l_e4m3(tmem + col_l(t), tmem + col_p(t), od, j > 0);
-    mma_commit(&sm.o_done[t]);
-    return true;
-  };
-  if (!mbar_wait(&sm.k_full[0], 0, ab, err)) return;
-  if (!mbar_wait(&sm.q_full[0], 0, ab, err)) return;
-  tc_fence_after_sync();
-  issue_qk<true>(s_tmem, qd[0], kd0);
-  mma_commit(&sm.s_full[0]);
-  for (int j = 0; j < nkv; ++j) {
-    const int ks = j % KST;
-    if (j > 0) {
-      if (!mbar_wait(&sm.v_full[(j - 1) % VST], ((j - 1) / VST) & 1, ab, err)) return;
-      if (!pv(0, j - 1)) return;
-    }
-    if (j == 0 && !mbar_wait(&sm.q_full[1], 0, ab, err)) return;
-    if (!mbar_wait(&sm.s_free[0], j & 1, ab, err)) return;
-    tc_fence_after_sync();
-    issue_qk<true>(s_tmem, qd[1], desc_at(kd0, ks * TILE));
-    mma_commit(&sm.s_full[1]);
-    mma_commit(&sm.k_empty[ks]);
-    if (j > 0) {
-      if (!pv(1, j - 1)) return;
-      mma_commit(&sm.v_empty[(j - 1) % VST]);
-    }
-    if (j + 1 < nkv) {
-      const int kn = (j + 1) % KST;
-      if (!mbar_wait(&sm.k_full[kn], ((j + 1) / KST) & 1, ab, err)) return;
-      if (!mbar_wait(&sm.s_free[1], j & 1, ab, err)) return;
-      tc_fence_after_sync();
-      issue_qk<true>(s_tmem, qd[0], desc_at(kd0, kn * TILE));
-      mma_commit(&sm.s_full[0]);
-    }
-  }
-  const int jl = nkv - 1;
-  if (!mbar_wait(&sm.v_full[jl % VST], (jl / VST) & 1, ab, err)) return;
-  if (!pv(0, jl)) return;
-  mma_commit(&sm.o_full[0]);
-  if (!pv(1, jl)) return;
-  mma_commit(&sm.v_empty[jl % VST]);
-  mma_commit(&sm.o_full[1]);
 }
 
 // BF16 main loop of the issuing thread, for both query tiles in one fixed
@@ -566,24 +452,15 @@ __device__ __forceinline__ void mma_main_bf16(Smem<false>& sm, uint32_t tmem, in
   }
 }
 
-// The MMA issuer (the whole warp runs the loop, one elected lane issues:
-// ptx.cuh), for both tiles.  REP: the repair blocks first (mma_repair); the
-// main loop then continues the s_full / p_full phases after them and
-// accumulates onto their O.
-template <bool FP8, bool REP>
-__device__ __forceinline__ void mma_issuer(Smem<FP8>& sm, uint32_t tmem, int nkv, int nrep, volatile int* ab,
-                                           uint32_t* err) {
-  if (REP) nkv -= nrep;  // main-loop blocks
-  do {
-    if (REP && !mma_repair(sm, tmem, nrep, ab, err)) break;
-    if (nkv <= 0) {
+// The MMA issuer of the BF16 and Sol instances (the whole warp runs the
+// loop, one elected lane issues: ptx.cuh), for both tiles.
+__device__ __forceinline__ void mma_issuer(Smem<false>& sm, uint32_t tmem, int nkv, volatile int* ab, uint32_t* err) {
+  if (nkv <= 0) {
 #pragma unroll
-      for (int t = 0; t < TILES; ++t) mma_commit(&sm.o_full[t]);
-      break;
-    }
-    if constexpr (FP8) mma_main_fp8_rs<REP>(sm, tmem, nkv, nrep, ab, err);
-    else mma_main_bf16(sm, tmem, nkv, ab, err);
-  } while (0);
+    for (int t = 0; t < TILES; ++t) mma_commit(&sm.o_full[t]);
+  } else {
+    mma_main_bf16(sm, tmem, nkv, ab, err);
+  }
   // Drain every MMA this thread issued before TMEM is released.
   mma_commit(&sm.mma_drain);
   mbar_drain(&sm.mma_drain, 0, err);
@@ -599,10 +476,40 @@ __device__ __forceinline__ void mma_issuer(Smem<FP8>& sm, uint32_t tmem, int nkv
 //
 // QK warp, per block j: QK_1(j) after s_free_0(j), QK_0(j+1) after
 // s_free_1(j) (both tiles' scores go through the one S region in turns).
-__device__ __forceinline__ void mma_qk_split(Smem<true>& sm, uint32_t tmem, int nkv, volatile int* ab,
+// REP: first the repair QKs (bf16 Q from the converted tiles, K from the
+// repair slot) into S_t per tile, each after the repair P.V that read the P
+// over its columns (o_done_t); the E4M3 blocks begin once the last repair
+// P.V of both tiles is done (their S, P and l columns overlap the repair S).
+// nkv: the E4M3 blocks.
+template <bool REP>
+__device__ __forceinline__ void mma_qk_split(Smem<true>& sm, uint32_t tmem, int nkv, int nrep, volatile int* ab,
                                              uint32_t* err) {
   constexpr uint32_t TILE = Traits<true>::TILE;
   constexpr int KST = Traits<true>::KST;
+  if constexpr (REP) {
+    uint64_t qbd[TILES];
+#pragma unroll
+    for (int t = 0; t < TILES; ++t) qbd[t] = sdesc_sw128(smem_u32(qbf_tile(sm, t)), 16, 1024);
+    const uint64_t krd = sdesc_sw128(smem_u32(krep_tile(sm)), 16, 1024);
+    for (int i = 0; i < nrep; ++i) {
+      if (!mbar_wait(&sm.krep_full, i & 1, ab, err)) return;
+#pragma unroll
+      for (int t = 0; t < TILES; ++t) {
+        if (!mbar_wait(i == 0 ? &sm.qbf_full[t] : &sm.o_done[t], i == 0 ? 0 : (i - 1) & 1, ab, err)) return;
+        tc_fence_after_sync();
+        issue_qk<false>(tmem + col_s(t), qbd[t], krd);
+        mma_commit(&sm.s_full[t]);
+      }
+      mma_commit(&sm.krep_empty);
+      if (i == nrep - 1) mma_commit(&sm.qbf_free);
+    }
+    if (nkv <= 0) return;
+    if (nrep > 0) {
+#pragma unroll
+      for (int t = 0; t < TILES; ++t)
+        if (!mbar_wait(&sm.o_done[t], (nrep - 1) & 1, ab, err)) return;
+    }
+  }
   uint64_t qd[TILES];
 #pragma unroll
   for (int t = 0; t < TILES; ++t) qd[t] = sdesc_sw128(smem_u32(sm.q[t]), 16, 1024);
@@ -634,9 +541,31 @@ __device__ __forceinline__ void mma_qk_split(Smem<true>& sm, uint32_t tmem, int 
 
 // P.V warp, per block j: PV_t(j) and l_t += P_t 1 after p_full_t(j), for
 // t = 0, 1 (V_j must be in); o_done_t, then v_empty and, after the last
-// block, o_full_t.
-__device__ __forceinline__ void mma_pv_split(Smem<true>& sm, uint32_t tmem, int nkv, volatile int* ab,
+// block, o_full_t.  REP: first the repair P.Vs (bf16 P over S_t, V from the
+// repair slot), each committed on o_done_t; the ones tile then takes the
+// repair V slot, and the E4M3 P.V and row sums accumulate onto the repair
+// blocks' O and the l the softmax put in its column.  nkv: the E4M3 blocks.
+template <bool REP>
+__device__ __forceinline__ void mma_pv_split(Smem<true>& sm, uint32_t tmem, int nkv, int nrep, volatile int* ab,
                                              uint32_t* err) {
+  if constexpr (REP) {
+    const uint64_t vrd = sdesc_sw128(smem_u32(vrep_tile(sm)), HALF, 1024);
+    for (int i = 0; i < nrep; ++i) {
+      if (!mbar_wait(&sm.vrep_full, i & 1, ab, err)) return;
+#pragma unroll
+      for (int t = 0; t < TILES; ++t) {
+        if (!mbar_wait(&sm.p_full[t], i & 1, ab, err)) return;
+        tc_fence_after_sync();
+        issue_pv<false>(tmem + col_o(t), tmem + col_s(t), vrd, i > 0);
+        mma_commit(&sm.o_done[t]);
+        if (nkv <= 0 && i == nrep - 1) mma_commit(&sm.o_full[t]);
+      }
+      mma_commit(&sm.vrep_empty);
+    }
+    if (nkv <= 0) return;
+    if (nrep > 0 && !mbar_wait(&sm.vrep_empty, (nrep - 1) & 1, ab, err)) return;  // V_rep read, the slot is free
+  }
+  const int ph = REP ? nrep : 0;  // p_full phases after the repair blocks
   {  // the ones tile of the row sums, 64 bytes per lane
     uint4* o = reinterpret_cast<uint4*>(ones_tile(sm)) + (threadIdx.x & 31) * 4;
 #pragma unroll
@@ -653,10 +582,10 @@ __device__ __forceinline__ void mma_pv_split(Smem<true>& sm, uint32_t tmem, int 
     if (!mbar_wait(&sm.v_full[vs], (j / VST) & 1, ab, err)) return;
 #pragma unroll
     for (int t = 0; t < TILES; ++t) {
-      if (!mbar_wait(&sm.p_full[t], j & 1, ab, err)) return;
+      if (!mbar_wait(&sm.p_full[t], (j + ph) & 1, ab, err)) return;
       tc_fence_after_sync();
-      issue_pv<true>(tmem + col_o(t), tmem + col_p(t), desc_at(vd0, vs * TILE), j > 0);
-      issue_l_e4m3(tmem + col_l(t), tmem + col_p(t), od, j > 0);
+      issue_pv<true>(tmem + col_o(t), tmem + col_p(t), desc_at(vd0, vs * TILE), REP || j > 0);
+      issue_l_e4m3(tmem + col_l(t), tmem + col_p(t), od, REP || j > 0);
       mma_commit(&sm.o_done[t]);
       if (j == nkv - 1) mma_commit(&sm.o_full[t]);
     }
@@ -665,11 +594,13 @@ __device__ __forceinline__ void mma_pv_split(Smem<true>& sm, uint32_t tmem, int 
 }
 
 // Either SPLIT issuer, then the drain of its own MMAs (before TMEM goes).
-template <bool QK>
-__device__ __forceinline__ void mma_split(Smem<true>& sm, uint32_t tmem, int nkv, volatile int* ab,
+// nkv: all key blocks (REP: nrep repair blocks first).
+template <bool REP, bool QK>
+__device__ __forceinline__ void mma_split(Smem<true>& sm, uint32_t tmem, int nkv, int nrep, volatile int* ab,
                                           uint32_t* err) {
-  if (QK) mma_qk_split(sm, tmem, nkv, ab, err);
-  else mma_pv_split(sm, tmem, nkv, ab, err);
+  if (!REP) nrep = 0;
+  if (QK) mma_qk_split<REP>(sm, tmem, nkv - nrep, nrep, ab, err);
+  else mma_pv_split<REP>(sm, tmem, nkv - nrep, nrep, ab, err);
   uint64_t* drain = QK ? &sm.mma_drain : &sm.mma_drain2;
   mma_commit(drain);
   mbar_drain(drain, 0, err);
@@ -689,12 +620,15 @@ __device__ __forceinline__ __half2 e4m3x2_value(uint32_t c) {
 // repair QK reads (both in the 128-byte-swizzled layout: a row's 16-byte
 // chunk c sits at chunk position c ^ (r % 8); the bf16 tile is two halves of
 // 64 head dims).  E4M3 values are exact in f16 and in bf16.
-template <bool FP8>
-__device__ __forceinline__ void convert_q_row(Smem<FP8>& sm, int t, int r) {
+// NC chunks from chunk c0 on (SPLIT: the two warps of a TMEM quadrant take
+// half a row each).
+template <bool FP8, int NC = 8>
+__device__ __forceinline__ void convert_q_row(Smem<FP8>& sm, int t, int r, int c0 = 0) {
   const uint8_t* src = sm.q[t] + r * 128;
   uint8_t* dst = qbf_tile(sm, t);
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {  // 16 codes: head dims 16c .. 16c + 15
+  for (int cc = 0; cc < NC; ++cc) {  // 16 codes: head dims 16c .. 16c + 15
+    const int c = c0 + cc;
     const uint4 u = *reinterpret_cast<const uint4*>(src + ((c ^ (r & 7)) << 4));
     const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
     uint32_t o[8];
@@ -735,21 +669,16 @@ __device__ __forceinline__ float row_max(const uint32_t (&s)[NS]) {
   return acc[0];
 }
 
-// One key block of the online softmax of query tile t (128 threads, thread
-// r = row r) with bf16 P -- the BF16 kernel's blocks and the FP8 kernel's
-// repair blocks: wait for S, mask the keys >= valid, update the running max
-// m (log2 units) and sum l, write P over S (bf16, two per TMEM column),
-// rescale O when the max moved (has_o: O already holds earlier blocks), and
-// hand P to the MMA thread.  Returns false when the CTA gave up.
-template <bool FP8>
-__device__ __forceinline__ bool softmax_block(Smem<FP8>& sm, int t, uint32_t s_addr, uint32_t o_addr,
+// One key block of the online softmax of query tile t of the BF16 and Sol
+// instances (128 threads, thread r = row r): wait for S, mask the keys >=
+// valid, update the running max m (log2 units) and sum l, write P over S
+// (bf16, two per TMEM column), rescale O when the max moved (has_o: O already
+// holds earlier blocks), and hand P to the MMA thread.  Returns false when
+// the CTA gave up.
+__device__ __forceinline__ bool softmax_block(Smem<false>& sm, int t, uint32_t s_addr, uint32_t o_addr,
                                               uint32_t phase, int valid, bool has_o, float sl2, float& m, float& l,
                                               volatile int* ab, uint32_t* err, bool keep = true) {
-  // The FP8 kernel's repair blocks use the scale of its E4M3 blocks, whose P
-  // is E4M3 of 256 p: the 2^8 factor is folded into the exponent and cancels
-  // against l, which sums the same scaled values.
-  constexpr float kPBias = FP8 ? 8.f : 0.f;
-  constexpr float kRescale = Traits<FP8>::RESCALE;
+  constexpr float kRescale = Traits<false>::RESCALE;
   const bool ok = mbar_wait(&sm.s_full[t], phase, ab, err);
   if (__any_sync(0xFFFFFFFFu, !ok)) return false;
   tc_fence_after_sync();
@@ -778,7 +707,7 @@ __device__ __forceinline__ bool softmax_block(Smem<FP8>& sm, int t, uint32_t s_a
   const bool rescale = __any_sync(0xFFFFFFFFu, m_tile > m + kRescale);
   const float m_new = rescale ? m_tile : m;
   const float alpha = rescale ? ex2_approx(m - m_new) : 1.f;  // 0 on the first tile
-  const float nm = kPBias - m_new;
+  const float nm = -m_new;
   // p = 2^(s sl2 - m): the argument of two scores per packed FMA; the row
   // sum in four packed accumulators.
   float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -819,134 +748,31 @@ __device__ __forceinline__ bool softmax_block(Smem<FP8>& sm, int t, uint32_t s_a
   return true;
 }
 
-// One E4M3 block of the FP8 main loop (128 threads, thread r = row r).  The
-// thread signals s_free as soon as S is in its registers (the MMA thread
-// then puts the other tile's scores into the same S columns while this one
-// works); before it writes P (p_addr: E4M3 of 256 p, four codes per TMEM
-// column) or rescales O, it waits until the P.V and the row sum of the
-// previous block (jm - 1), which read the same P columns and wrote O and
-// l_addr, have completed (o_done).  No row sum here: the tensor core adds P
-// into l_addr's column, which the rescale scales with O; l keeps the repair
-// blocks' register sum and follows alpha.  jm: the block's index in the main
-// loop; phase: its s_full / p_full phase.
-__device__ __forceinline__ bool softmax_block_fp8(Smem<true>& sm, int t, int r, uint32_t s_addr, uint32_t o_addr,
-                                                  uint32_t l_addr, uint32_t p_addr, uint32_t phase, int jm,
-                                                  int valid, bool has_o,
-                                                  float sl2, float& m, float& l, volatile int* ab, uint32_t* err) {
-  constexpr float kPBias = 8.f;  // P = E4M3 of 256 p: folded into the exponent, cancels against l
-  constexpr float kRescale = Traits<true>::RESCALE;
-  bool ok = mbar_wait(&sm.s_full[t], phase, ab, err);
-  if (__any_sync(0xFFFFFFFFu, !ok)) return false;
-  tc_fence_after_sync();
-  uint32_t s[BN];
-  tmem_ld128(s_addr, s);
-  tmem_ld_wait(s);
-  tc_fence_before_sync();
-  mbar_arrive(&sm.s_free[t]);  // S_t's columns may take the next block's QK now
-  if (valid < BN) {
-#pragma unroll
-    for (int i = 0; i < BN; ++i)
-      if (i >= valid) s[i] = __float_as_uint(-INFINITY);
-  }
-  const float mx = row_max(s);
-  const float m_tile = fmaxf(m, mx * sl2);
-  const bool rescale = __any_sync(0xFFFFFFFFu, m_tile > m + kRescale);
-  const float m_new = rescale ? m_tile : m;
-  const float alpha = rescale ? ex2_approx(m - m_new) : 1.f;  // 0 on the first tile
-  const float nm = kPBias - m_new;
-  // P codes four per word (key 4i in the lowest byte)
-  uint32_t pk[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    float x0, x1, x2, x3;
-    fma2(x0, x1, __uint_as_float(s[4 * i]), __uint_as_float(s[4 * i + 1]), sl2, sl2, nm, nm);
-    fma2(x2, x3, __uint_as_float(s[4 * i + 2]), __uint_as_float(s[4 * i + 3]), sl2, sl2, nm, nm);
-    pk[i] = e4m3x2(ex2_approx(x0), ex2_approx(x1)) | (e4m3x2(ex2_approx(x2), ex2_approx(x3)) << 16);
-  }
-  l *= alpha;  // the repair blocks' register sum (0 without them)
-  // the previous block's P.V and row sum have read P and written O, l
-  if (jm > 0) {
-    ok = mbar_wait(&sm.o_done[t], (jm - 1) & 1, ab, err);
-    if (__any_sync(0xFFFFFFFFu, !ok)) return false;
-    tc_fence_after_sync();
-  }
-  tmem_st32(p_addr, pk);  // waited for (tcgen05.wait::st) before p_full below
-  if (rescale && has_o) {
-    // O and l: one 128-column TMEM load, packed products, one store
-    uint32_t o[HD];
-    tmem_ld128(o_addr, o);
-    uint32_t lv = tmem_ld1(l_addr);
-    tmem_ld_wait(o);
-#pragma unroll
-    for (int i = 0; i < HD; i += 2) {
-      float a0, a1;
-      mul2(a0, a1, __uint_as_float(o[i]), __uint_as_float(o[i + 1]), alpha, alpha);
-      o[i] = __float_as_uint(a0);
-      o[i + 1] = __float_as_uint(a1);
-    }
-    tmem_st128(o_addr, o);
-    tmem_ld_wait(lv);
-    tmem_st1(l_addr, __float_as_uint(__uint_as_float(lv) * alpha));
-  }
-  tmem_st_wait();
-  m = m_new;
-  tc_fence_before_sync();
-  mbar_arrive(&sm.p_full[t]);
-  return true;
-}
-
-// Softmax and epilogue of query tile `t` (128 threads, thread r = row r).
-// REP: the Q conversion and the repair blocks (bf16 P) come first, then the
-// E4M3 blocks, whose loop is the plain FP8 one with its phases shifted.
-template <bool FP8, bool REP, bool SOL>
-__device__ __forceinline__ void softmax_epilogue(Smem<FP8>& sm, uint32_t tmem, const Params& prm, int b, int h,
+// Softmax and epilogue of query tile `t` of the BF16 and Sol instances (128
+// threads, thread r = row r).
+template <bool SOL>
+__device__ __forceinline__ void softmax_epilogue(Smem<false>& sm, uint32_t tmem, const Params& prm, int b, int h,
                                                  int row0, int t, int nkv, const uint16_t* lst, volatile int* ab,
                                                  const CUtensorMap* tm_o) {
   const int r = threadIdx.x & (BM - 1);
   const uint32_t lane_base = static_cast<uint32_t>(r & ~31) << 16;  // TMEM lanes of this warp
-  const uint32_t s_rep = tmem + lane_base + col_s(t);            // the repair blocks' S / P
-  const uint32_t s_addr = tmem + lane_base + col_s(FP8 ? 0 : t);  // FP8: one S region, in turns
+  const uint32_t s_addr = tmem + lane_base + col_s(t);
   const uint32_t o_addr = tmem + lane_base + col_o(t);
-  const uint32_t l_addr = tmem + lane_base + col_l(t);
-  const uint32_t p_addr = tmem + lane_base + col_p(t);
-  const int nrep = REP ? prm.nrep : 0;
-  const int nmain = nkv - nrep;
-  float sl2 = prm.scale_log2;
-  float out_scale = 1.f;
-  if (FP8) {
-    const float* sc = prm.scales + 3 * (static_cast<size_t>(b) * prm.H + h);
-    sl2 *= __ldg(sc) * __ldg(sc + 1);
-    out_scale = __ldg(sc + 2);
-  }
+  const float sl2 = prm.scale_log2;
   float m = -INFINITY;  // running max, in log2 units
   float l = 0.f;        // running row sum
   bool ok = true;
-  if (REP && nrep > 0) {
-    ok = mbar_wait(&sm.q_full[t], 0, ab, prm.err);
-    if (__any_sync(0xFFFFFFFFu, !ok)) return;
-    convert_q_row(sm, t, r);
-    fence_proxy_async_smem();  // generic-proxy writes, read by the MMA (async proxy)
-    mbar_arrive(&sm.qbf_full[t]);
-    for (int i = 0; i < nrep && ok; ++i)
-      ok = softmax_block<FP8>(sm, t, s_rep, o_addr, i & 1, prm.rep_keys - i * BN, i > 0, sl2, m, l, ab,
-                                     prm.err);
-  }
   if (SOL) {
     // list entry j: key block (14 bits) and the keep bits of the two tiles; a
     // block the tile skips still gets its (zero) P, so O is written from j = 0
-    for (int j = 0; j < nmain && ok; ++j) {
+    for (int j = 0; j < nkv && ok; ++j) {
       const uint32_t e = __ldg(lst + j);
-      ok = softmax_block<FP8>(sm, t, s_addr, o_addr, j & 1, prm.N - static_cast<int>(e & 0x3FFFu) * BN,
-                                     j > 0, sl2, m, l, ab, prm.err, (e >> (14 + t)) & 1u);
+      ok = softmax_block(sm, t, s_addr, o_addr, j & 1, prm.N - static_cast<int>(e & 0x3FFFu) * BN, j > 0, sl2, m,
+                         l, ab, prm.err, (e >> (14 + t)) & 1u);
     }
-  } else if constexpr (FP8) {
-    for (int j = 0; j < nmain && ok; ++j)
-      ok = softmax_block_fp8(sm, t, r, s_addr, o_addr, l_addr, p_addr, (j + nrep) & 1, j,
-                                 prm.main_keys - j * BN, j + nrep > 0, sl2, m, l, ab, prm.err);
   } else {
-    for (int j = 0; j < nmain && ok; ++j)
-      ok = softmax_block<FP8>(sm, t, s_addr, o_addr, (j + nrep) & 1, prm.main_keys - j * BN, j + nrep > 0,
-                                   sl2, m, l, ab, prm.err);
+    for (int j = 0; j < nkv && ok; ++j)
+      ok = softmax_block(sm, t, s_addr, o_addr, j & 1, prm.main_keys - j * BN, j > 0, sl2, m, l, ab, prm.err);
   }
   if (ok) {
     ok = mbar_wait(&sm.o_full[t], 0, ab, prm.err);
@@ -954,30 +780,15 @@ __device__ __forceinline__ void softmax_epilogue(Smem<FP8>& sm, uint32_t tmem, c
   }
   if (!ok) return;
   tc_fence_after_sync();
-  if (FP8 && nmain > 0) {  // the tensor core's row sum of the E4M3 blocks
-    uint32_t lv = tmem_ld1(l_addr);
-    tmem_ld_wait(lv);
-    l += __uint_as_float(lv);
-  }
-  const float inv_l = out_scale / l;
-  // O tile (bf16, 32 KB) -> shared memory that no MMA or copy touches any
-  // more, in the SW128 layout of the out tensor map: half c / 2 holds head
-  // dims 64 (c / 2) .., row r at byte 128 r, its 16-byte chunk k at position
-  // k ^ (r % 8).  BF16: the tile's own 32 KB Q buffer (its last QK completed
-  // before the PV that signalled o_full).  FP8: the tile's own 16 KB Q buffer
-  // and its 16 KB half of the repair K region (out_stage), which nothing
-  // touches any more.
-  // Then one thread writes the two halves with TMA stores, which also clip
-  // rows >= N: whole 128-byte rows instead of each thread's 16-byte pieces of
-  // rows H x 256 bytes apart.
-  uint8_t* stage[2];
-  if constexpr (FP8) {
-    stage[0] = sm.q[t];
-    stage[1] = out_stage(sm, t);
-  } else {
-    stage[0] = sm.q[t];
-    stage[1] = sm.q[t] + HALF;
-  }
+  const float inv_l = 1.f / l;
+  // O tile (bf16, 32 KB) -> the tile's own 32 KB Q buffer, which no MMA or
+  // copy touches any more (its last QK completed before the PV that
+  // signalled o_full), in the SW128 layout of the out tensor map: half c / 2
+  // holds head dims 64 (c / 2) .., row r at byte 128 r, its 16-byte chunk k
+  // at position k ^ (r % 8).  Then one thread writes the two halves with TMA
+  // stores, which also clip rows >= N: whole 128-byte rows instead of each
+  // thread's 16-byte pieces of rows H x 256 bytes apart.
+  uint8_t* stage[2] = {sm.q[t], sm.q[t] + HALF};
 #pragma unroll
   for (int c = 0; c < HD / 32; ++c) {
     uint32_t o[32];
@@ -1006,7 +817,7 @@ __device__ __forceinline__ void softmax_epilogue(Smem<FP8>& sm, uint32_t tmem, c
 }
 
 // ---------------------------------------------------------------- SPLIT FP8
-// The plain FP8 instance with two threads per row (Roles::SPLIT).  Thread i
+// The FP8 instances with two threads per row (Roles::SPLIT).  Thread i
 // of a warp owns lane (i / 4 + 8 (i % 2)) of the warp's 16 TMEM lanes and the
 // key columns of parity (i / 2) % 2: its 64 scores of a block are keys
 // 2k + par, k = 0..63 (16x64b loads).  The row max takes one shuffle with the
@@ -1026,9 +837,15 @@ struct SplitLanes {
 // S, mask keys >= valid, max (with the partner thread), exp2 into E4M3 codes,
 // wait for the previous P.V (it read P and wrote O, l), store P, rescale O
 // and l when the max moved, hand P to the MMA thread.
+//
+// REP: the E4M3 blocks after nrep repair blocks: O holds their P.V from the
+// start, their o_done phases come first, and at the first E4M3 block the
+// thread puts the repair blocks' row sum l_rep (scaled like O) into its l
+// column, which the row-sum MMAs then add to.
+template <bool REP>
 __device__ __forceinline__ bool softmax_block_split(Smem<true>& sm, int t, const SplitLanes& a, uint32_t phase,
                                                     int jm, int valid, float sl2, float& m, volatile int* ab,
-                                                    uint32_t* err) {
+                                                    uint32_t* err, int nrep = 0, float l_rep = 0.f) {
   constexpr float kPBias = 8.f;  // P = E4M3 of 256 p: folded into the exponent, cancels against l
   bool ok = mbar_wait(&sm.s_full[t], phase, ab, err);
   if (__any_sync(0xFFFFFFFFu, !ok)) return false;
@@ -1061,17 +878,20 @@ __device__ __forceinline__ bool softmax_block_split(Smem<true>& sm, int t, const
     pk[i] = e4m3x2(ex2_approx(x0), ex2_approx(x1)) | (e4m3x2(ex2_approx(x2), ex2_approx(x3)) << 16);
   }
   if (jm > 0) {
-    ok = mbar_wait(&sm.o_done[t], (jm - 1) & 1, ab, err);
+    ok = mbar_wait(&sm.o_done[t], (REP ? jm - 1 + nrep : jm - 1) & 1, ab, err);
     if (__any_sync(0xFFFFFFFFu, !ok)) return false;
     tc_fence_after_sync();
   }
   tmem_st16x16(a.p, pk);  // waited for (tcgen05.wait::st) before p_full below
-  if (rescale && jm > 0) {
+  const bool has_o = REP ? (jm > 0 || nrep > 0) : jm > 0;
+  if (rescale && has_o) {
     // this thread's 64 of the row's O columns, and its l column (the row sum
     // MMA writes 16 equal columns; the pair keeps columns 0 and 1 scaled)
+    const bool l_in_tmem = !REP || jm > 0;
     uint32_t o[HD / 2];
     tmem_ld16x64(a.o, o);
-    uint32_t lv = tmem_ld16x1(a.l);
+    uint32_t lv = 0;
+    if (l_in_tmem) lv = tmem_ld16x1(a.l);
     tmem_ld_wait(o);
 #pragma unroll
     for (int i = 0; i < HD / 2; i += 2) {
@@ -1081,11 +901,120 @@ __device__ __forceinline__ bool softmax_block_split(Smem<true>& sm, int t, const
       o[i + 1] = __float_as_uint(a1);
     }
     tmem_st16x64(a.o, o);
-    tmem_ld_wait(lv);
-    tmem_st16x1(a.l, __float_as_uint(__uint_as_float(lv) * alpha));
+    if (l_in_tmem) {
+      tmem_ld_wait(lv);
+      tmem_st16x1(a.l, __float_as_uint(__uint_as_float(lv) * alpha));
+    }
   }
+  if (REP && jm == 0 && nrep > 0) tmem_st16x1(a.l, __float_as_uint(l_rep * alpha));
   tmem_st_wait();
   m = m_new;
+  tc_fence_before_sync();
+  mbar_arrive(&sm.p_full[t]);
+  return true;
+}
+
+// The repair blocks (bf16 P) of the SPLIT repair instance: thread i of a warp
+// holds rows g = i / 4 and g + 8 of the warp's 16 TMEM lanes and, of each
+// row, the keys 8k + 2q and 8k + 2q + 1 (q = i % 4, k = 0..15): a 16x256b load
+// of S puts row g + 8h, key 8k + 2q + e in register 4k + 2h + e.  P is bf16
+// with keys 2c and 2c + 1 in column c, so the thread's P is exactly columns
+// 4k + q of its two rows, which a 16x128b store writes (register 2k + h) over
+// S: no exchange between threads and no change of key order.  The row max
+// takes two shuffles over the four threads of a row; each thread keeps its
+// part of the row sums.  Row g + 8 (i % 2) is the thread's row in the 16x64b
+// layout of the E4M3 blocks that follow.
+__device__ __forceinline__ float max32_of_row(const uint32_t (&s)[BN / 2], int hr) {
+  float acc[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) acc[c] = fmaxf(__uint_as_float(s[4 * c + 2 * hr]), __uint_as_float(s[4 * c + 2 * hr + 1]));
+#pragma unroll
+  for (int k = 4; k < 16; k += 4) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      acc[c] = fmax3(acc[c], __uint_as_float(s[4 * (k + c) + 2 * hr]), __uint_as_float(s[4 * (k + c) + 2 * hr + 1]));
+  }
+  return fmaxf(fmaxf(acc[0], acc[1]), fmaxf(acc[2], acc[3]));
+}
+
+template <bool FP8>
+__device__ __forceinline__ bool softmax_block_b16s(Smem<FP8>& sm, int t, const SplitLanes& a, uint32_t phase,
+                                                   int jm, int valid, float sl2, float (&m)[2], float (&l)[2],
+                                                   volatile int* ab, uint32_t* err) {
+  // FP8: the scale of the E4M3 blocks (P of 256 p, 2^8 folded into the exponent)
+  constexpr float kPBias = FP8 ? 8.f : 0.f;
+  constexpr float kRescale = Traits<FP8>::RESCALE;
+  bool ok = mbar_wait(&sm.s_full[t], phase, ab, err);
+  if (__any_sync(0xFFFFFFFFu, !ok)) return false;
+  tc_fence_after_sync();
+  uint32_t s[BN / 2];
+  tmem_ld16x256(a.s, s);
+  tmem_ld_wait(s);
+  const int k0 = 2 * a.par;    // par = q here: the thread's first key of every 8
+  if (valid < BN) {
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+          if (8 * k + k0 + e >= valid) s[4 * k + 2 * h2 + e] = __float_as_uint(-INFINITY);
+  }
+  float mt[2], mn[2], alpha[2], nm[2];
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) {
+    float mx = max32_of_row(s, hr);
+    mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+    mt[hr] = fmaxf(m[hr], mx * sl2);
+  }
+  const bool rescale = __any_sync(0xFFFFFFFFu, mt[0] > m[0] + kRescale || mt[1] > m[1] + kRescale);
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) {
+    mn[hr] = rescale ? mt[hr] : m[hr];
+    alpha[hr] = rescale ? ex2_approx(m[hr] - mn[hr]) : 1.f;  // 0 on the first block
+    nm[hr] = kPBias - mn[hr];
+  }
+  uint32_t pk[BN / 4];
+  float sum[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      float x0, x1;
+      fma2(x0, x1, __uint_as_float(s[4 * k + 2 * hr]), __uint_as_float(s[4 * k + 2 * hr + 1]), sl2, sl2, nm[hr],
+           nm[hr]);
+      const float p0 = ex2_approx(x0);
+      const float p1 = ex2_approx(x1);
+      add2(sum[hr][0], sum[hr][1], p0, p1);
+      pk[2 * k + hr] = pack_bf16x2(p0, p1);
+    }
+  }
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) l[hr] = l[hr] * alpha[hr] + (sum[hr][0] + sum[hr][1]);
+  // P over S_t (bf16, the first 64 of its 128 columns): PV_t(j-1) has read
+  // the previous P and landed in O_t -- the QK warp waits for its commit
+  // before QK_t(j), whose commit signalled S_t(j)
+  tmem_st16x128(a.p, pk);
+  if (rescale && jm > 0) {
+    uint32_t o[HD / 2];
+    tmem_ld16x256(a.o, o);
+    tmem_ld_wait(o);
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        float a0, a1;
+        mul2(a0, a1, __uint_as_float(o[4 * k + 2 * hr]), __uint_as_float(o[4 * k + 2 * hr + 1]), alpha[hr],
+             alpha[hr]);
+        o[4 * k + 2 * hr] = __float_as_uint(a0);
+        o[4 * k + 2 * hr + 1] = __float_as_uint(a1);
+      }
+    tmem_st16x256(a.o, o);
+  }
+  tmem_st_wait();
+  m[0] = mn[0];
+  m[1] = mn[1];
   tc_fence_before_sync();
   mbar_arrive(&sm.p_full[t]);
   return true;
@@ -1095,6 +1024,10 @@ __device__ __forceinline__ bool softmax_block_split(Smem<true>& sm, int t, const
 // epilogue switches to whole rows: the two warps of a TMEM quadrant read its
 // 32 lanes with 32x32b loads, warp half hh taking O columns 64 hh .. +63,
 // which is output half hh of the tile (head dims 64 hh ..).
+// REP: first the Q conversion (each warp of a quadrant half a row) and the
+// repair blocks in the 16x256b layout; their running max and row sum carry
+// over to the E4M3 blocks (the thread's row there is its row i % 2 of them).
+template <bool REP>
 __device__ __forceinline__ void softmax_epilogue_split(Smem<true>& sm, uint32_t tmem, const Params& prm, int b,
                                                        int h, int row0, int t, int nkv, volatile int* ab,
                                                        const CUtensorMap* tm_o) {
@@ -1112,13 +1045,56 @@ __device__ __forceinline__ void softmax_epilogue_split(Smem<true>& sm, uint32_t 
   const float* sc = prm.scales + 3 * (static_cast<size_t>(b) * prm.H + h);
   const float sl2 = prm.scale_log2 * __ldg(sc) * __ldg(sc + 1);
   const float out_scale = __ldg(sc + 2);
+  const int nrep = REP ? prm.nrep : 0;
+  const int nmain = nkv - nrep;
   float m = -INFINITY;  // running max of this thread's row, log2 units
+  float l_rep = 0.f;    // REP: the repair blocks' row sum of that row
   bool ok = true;
-  for (int j = 0; j < nkv && ok; ++j)
-    ok = softmax_block_split(sm, t, a, j & 1, j, prm.main_keys - j * BN, sl2, m, ab, prm.err);
+  if (REP && nrep > 0) {
+    ok = mbar_wait(&sm.q_full[t], 0, ab, prm.err);
+    if (__any_sync(0xFFFFFFFFu, !ok)) return;
+    convert_q_row<true, 4>(sm, t, 32 * qd + i, 4 * hh);
+    fence_proxy_async_smem();  // generic-proxy writes, read by the MMA (async proxy)
+    mbar_arrive(&sm.qbf_full[t]);
+    SplitLanes ar = a;
+    ar.s = tmem + lanes16 + col_s(t);  // S_t and P over it, per tile
+    ar.p = ar.s;
+    ar.par = i & 3;
+    float m2[2] = {-INFINITY, -INFINITY}, l2[2] = {0.f, 0.f};
+    for (int k = 0; k < nrep && ok; ++k)
+      ok = softmax_block_b16s<true>(sm, t, ar, k & 1, k, prm.rep_keys - k * BN, sl2, m2, l2, ab, prm.err);
+    if (!ok) return;
+    float lt[2];
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      lt[hr] = l2[hr] + __shfl_xor_sync(0xFFFFFFFFu, l2[hr], 1);
+      lt[hr] += __shfl_xor_sync(0xFFFFFFFFu, lt[hr], 2);
+    }
+    m = (i & 1) ? m2[1] : m2[0];
+    l_rep = (i & 1) ? lt[1] : lt[0];
+  }
+  for (int j = 0; j < nmain && ok; ++j)
+    ok = softmax_block_split<REP>(sm, t, a, (j + nrep) & 1, j, prm.main_keys - j * BN, sl2, m, ab, prm.err, nrep,
+                                  l_rep);
   if (ok) {
     ok = mbar_wait(&sm.o_full[t], 0, ab, prm.err);
     if (__any_sync(0xFFFFFFFFu, !ok)) ok = false;
+  }
+  if (REP && ok && nmain == 0) {
+    // no E4M3 block: the repair sums go into the l column for the epilogue,
+    // once every P.V is done (the other tile's repair P spans these columns)
+    ok = mbar_wait(&sm.o_full[1 - t], 0, ab, prm.err);
+    if (__any_sync(0xFFFFFFFFu, !ok)) ok = false;
+    if (ok) {
+      tc_fence_after_sync();
+      tmem_st16x1(a.l, __float_as_uint(l_rep));
+      tmem_st_wait();
+      tc_fence_before_sync();
+      // the two warps of a quadrant wrote one half of its lanes each
+      mbar_arrive(&sm.lrep_full[t]);
+      ok = mbar_wait(&sm.lrep_full[t], 0, ab, prm.err);
+      if (__any_sync(0xFFFFFFFFu, !ok)) ok = false;
+    }
   }
   if (!ok) return;
   tc_fence_after_sync();
@@ -1189,7 +1165,7 @@ __global__ void __launch_bounds__((Roles<FP8, REP, SOL>::THREADS), 1)
     for (int s = 0; s < KST; ++s) { mbar_init(&sm.k_full[s], 1); mbar_init(&sm.k_empty[s], 1); }
     for (int s = 0; s < VST; ++s) { mbar_init(&sm.v_full[s], 1); mbar_init(&sm.v_empty[s], 1); }
     for (int t = 0; t < TILES; ++t) {
-      mbar_init(&sm.qbf_full[t], BM);
+      mbar_init(&sm.qbf_full[t], R::TILE_THREADS);
       mbar_init(&sm.s_free[t], R::TILE_THREADS);
       mbar_init(&sm.o_done[t], 1);
     }
@@ -1198,6 +1174,7 @@ __global__ void __launch_bounds__((Roles<FP8, REP, SOL>::THREADS), 1)
     mbar_init(&sm.vrep_full, 1);
     mbar_init(&sm.vrep_empty, 1);
     mbar_init(&sm.qbf_free, 1);
+    for (int t = 0; t < TILES; ++t) mbar_init(&sm.lrep_full[t], R::TILE_THREADS);
     mbar_init(&sm.mma_drain, 1);
     mbar_init(&sm.mma_drain2, 1);
     mbar_init(&sm.never, 1);
@@ -1248,22 +1225,22 @@ __global__ void __launch_bounds__((Roles<FP8, REP, SOL>::THREADS), 1)
     __syncwarp();
   } else if (warp == R::MMA) {
     if constexpr (R::SPLIT) {
-      if (!*ab) mma_split<true>(sm, tmem, nkv, ab, prm.err);  // the QKs (the whole warp: see mma_commit)
+      if (!*ab) mma_split<REP, true>(sm, tmem, nkv, prm.nrep, ab, prm.err);  // the QKs (the whole warp: see mma_commit)
     } else {
-      if (!*ab) mma_issuer<FP8, REP>(sm, tmem, nkv, prm.nrep, ab, prm.err);  // the whole warp: see mma_commit
+      if (!*ab) mma_issuer(sm, tmem, nkv, ab, prm.err);  // the whole warp: see mma_commit
     }
     __syncwarp();
   } else if (R::SPLIT && warp == R::MMA_PV) {
     if constexpr (R::SPLIT) {
-      if (!*ab) mma_split<false>(sm, tmem, nkv, ab, prm.err);  // the P.Vs and row sums
+      if (!*ab) mma_split<REP, false>(sm, tmem, nkv, prm.nrep, ab, prm.err);  // the P.Vs and row sums
     }
     __syncwarp();
   } else if constexpr (R::SPLIT) {
     const int t = warp / (R::SOFTMAX_WARPS / TILES);  // query tile of this warp
-    if (!*ab) softmax_epilogue_split(sm, tmem, prm, b, h, q0 + t * BM, t, nkv, ab, &tm_o);
+    if (!*ab) softmax_epilogue_split<REP>(sm, tmem, prm, b, h, q0 + t * BM, t, nkv, ab, &tm_o);
   } else {
     const int t = warp >> 2;  // query tile of this warpgroup
-    if (!*ab) softmax_epilogue<FP8, REP, SOL>(sm, tmem, prm, b, h, q0 + t * BM, t, nkv, lst, ab, &tm_o);
+    if (!*ab) softmax_epilogue<SOL>(sm, tmem, prm, b, h, q0 + t * BM, t, nkv, lst, ab, &tm_o);
   }
   tc_fence_before_sync();
   __syncthreads();

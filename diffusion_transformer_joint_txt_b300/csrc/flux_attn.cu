@@ -266,11 +266,9 @@ int launch_prologue_fp8(flux_attn* h, const void* q, const void* k, const void* 
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "amax launch");
   const int R = repair_count(h, n);
-  // V^T in the plain attention's key order, natural for the repair instance
-  if (R > 0)
-    flux::fp8_vt_kernel<false><<<vgrid, flux::kVtThreads, 0, stream>>>(tv, tvt, H, h->amax, h->err, h->errv, n);
-  else
-    flux::fp8_vt_kernel<true><<<vgrid, flux::kVtThreads, 0, stream>>>(tv, tvt, H, h->amax, h->err, nullptr, n);
+  // V^T in the key order of the attention's P.V MMA
+  flux::fp8_vt_kernel<true><<<vgrid, flux::kVtThreads, 0, stream>>>(tv, tvt, H, h->amax, h->err,
+                                                                   R > 0 ? h->errv : nullptr, n);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "V^T launch");
   {
@@ -1019,7 +1017,7 @@ static int launch_qkv_fp8(flux_attn* h, const void* x, const void* w_qkv, const 
   CUtensorMap tv, tvt;
   if ((rc = encode_v_maps(h, h->vw, v8t, n, &tv, &tvt))) return rc;
   const dim3 vgrid((n + flux::kVtTokens - 1) / flux::kVtTokens, B * H);
-  // the plain FP8 attention's key order (VC handles do not take this path)
+  // the key order of the attention's P.V MMA
   flux::fp8_vt_kernel<true><<<vgrid, flux::kVtThreads, 0, stream>>>(tv, tvt, H, h->amax, h->err, nullptr, n);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "V^T launch");

@@ -20,8 +20,8 @@
 //                                       scales   fp32 [B, H, 3] = (s_q, s_k, s_v)
 //   fp8_vt_kernel                     v8t E4M3 [B, H, 128, Npad] (V transposed,
 //                                     keys contiguous; columns N..Npad-1 zero;
-//                                     for the plain FP8 attention the keys of
-//                                     every 8 in the order 0 2 4 6 1 3 5 7)
+//                                     the keys of every 8 in the order
+//                                     0 2 4 6 1 3 5 7 of the attention's P.V)
 // Recomputing Q', K' in the second pass costs less than a round trip of an
 // fp32 or bf16 copy through HBM, and keeps a single rounding, fp32 -> E4M3.
 #pragma once
@@ -231,12 +231,12 @@ __global__ void __launch_bounds__(kVtThreads)
 // between N and Npad become the zero padding).
 //
 // MMA_ORDER: within every 8 tokens the columns hold tokens 0, 2, 4, 6, 1, 3,
-// 5, 7 -- the key order of the P.V MMA in the plain FP8 attention, whose
-// softmax threads hold the even or the odd keys of a row (attention.cuh).
-// Tiles start at multiples of 64 tokens, so the groups of 8 are those of
-// the key blocks, and Npad (a multiple of 16) never splits one.
+// 5, 7 -- the key order of the P.V MMA in the FP8 attention, whose softmax
+// threads hold the even or the odd keys of a row (attention.cuh).  Tiles
+// start at multiples of 64 tokens, so the groups of 8 are those of the key
+// blocks, and Npad (a multiple of 16) never splits one.
 //
-// With errv set (VC-Attention repair, natural order only) the kernel also writes, per token of
+// With errv set (VC-Attention repair) the kernel also writes, per token of
 // the tile, the squared quantisation error |v - code s_v|^2 of its V row:
 // thread d holds dim d of the 64 tokens, a butterfly over the lanes leaves
 // lane l of warp w with the sums over its 32 dims of tokens 2l and 2l + 1,
@@ -289,19 +289,23 @@ __global__ void __launch_bounds__(kVtThreads)
            (static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(x2, x3), __NV_SATFINITE, __NV_E4M3))
             << 16);
   }
-  if (!MMA_ORDER && errv != nullptr) {  // block-uniform
+  if (errv != nullptr) {  // block-uniform
     __shared__ float wsum[kVtThreads / 32][kVtTokens];
     const float sv = am > 0.f ? am / kE4M3Max : 1.f;
-    float e[kVtTokens];
+    float e[kVtTokens];  // by token
 #pragma unroll
-    for (int t = 0; t < kVtTokens; t += 4) {
-      const float2 a = e4m3x2_to_float2(w[t / 4] & 0xFFFFu), c = e4m3x2_to_float2(w[t / 4] >> 16);
-      const float r0 = __bfloat162float(vin[t][d]) - a.x * sv, r1 = __bfloat162float(vin[t + 1][d]) - a.y * sv;
-      const float r2 = __bfloat162float(vin[t + 2][d]) - c.x * sv, r3 = __bfloat162float(vin[t + 3][d]) - c.y * sv;
+    for (int i = 0; i < kVtTokens / 4; ++i) {
+      const int t = MMA_ORDER ? 8 * (i >> 1) + (i & 1) : 4 * i;  // token of byte 0 of word i
+      const int st = MMA_ORDER ? 2 : 1;
+      const float2 a = e4m3x2_to_float2(w[i] & 0xFFFFu), c = e4m3x2_to_float2(w[i] >> 16);
+      const float r0 = __bfloat162float(vin[t][d]) - a.x * sv;
+      const float r1 = __bfloat162float(vin[t + st][d]) - a.y * sv;
+      const float r2 = __bfloat162float(vin[t + 2 * st][d]) - c.x * sv;
+      const float r3 = __bfloat162float(vin[t + 3 * st][d]) - c.y * sv;
       e[t] = r0 * r0;
-      e[t + 1] = r1 * r1;
-      e[t + 2] = r2 * r2;
-      e[t + 3] = r3 * r3;
+      e[t + st] = r1 * r1;
+      e[t + 2 * st] = r2 * r2;
+      e[t + 3 * st] = r3 * r3;
     }
     // butterfly: at offset o a lane keeps the half of its tokens its bit o selects
     const int lane = d & 31;

@@ -233,8 +233,12 @@ __global__ void __launch_bounds__(kRepairThreads) vc_repair_kernel(const RepairA
         reinterpret_cast<uint4*>(k8 + static_cast<size_t>(mv.y) * kHeadDim)[c] =
             reinterpret_cast<const uint4*>(k8 + static_cast<size_t>(mv.x) * kHeadDim)[c];
       } else {
+        // V^T keeps the attention's key order within every 8 positions
+        // (0 2 4 6 1 3 5 7; quantize_fp8.cuh): position p sits in column
+        // 8 (p / 8) + 4 (p % 2) + (p % 8) / 2
         const size_t d = static_cast<size_t>(c - kHeadDim / 16) * a.npad;
-        v8t[d + mv.y] = v8t[d + mv.x];
+        auto col = [](int p) { return 8 * (p >> 3) + 4 * (p & 1) + ((p & 7) >> 1); };
+        v8t[d + col(mv.y)] = v8t[d + col(mv.x)];
       }
     }
     __syncthreads();

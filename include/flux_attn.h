@@ -179,7 +179,8 @@ FLUX_ATTN_API int flux_attn_attend_fp8(flux_attn_t h, const void* q8, const void
  * K' and codes; equal errors: lower index first):
  *   repair_idx  int32 [B, H, R]: the repaired tokens, ascending
  *   k8, v8t     the codes of the N - R other tokens sit in positions
- *               0 .. N-R-1, in token order (no 8-column interleave in v8t)
+ *               0 .. N-R-1 (v8t in the 8-column order of
+ *               flux_attn_prologue_fp8, by position)
  *               (a repaired token's position below N - R receives,
  *               in order, the codes of a non-repaired token from the last R
  *               positions); positions N-R .. N-1 are not read afterwards

@@ -114,7 +114,8 @@ def test_vc_every_row_and_every_step(B, H, txt, ih, iw, rh, rw, rho):
     assert plain.sync_status() == 0
     assert torch.equal(q8, pq8) and torch.equal(scales, psc)
     k8h, v8h, pk8h, pv8h = (t.cpu().numpy() for t in (k8, v8t, pk8, pv8t))
-    pv8h = v8t_token_order(pv8h)  # the plain prologue's key order; the repair prologue's is natural
+    # both prologues store V^T in the attention's key order: back to positions
+    v8h, pv8h = v8t_token_order(v8h), v8t_token_order(pv8h)
     split = n - R
     for b in range(B):
         for h in range(H):
