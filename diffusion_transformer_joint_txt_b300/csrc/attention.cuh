@@ -141,8 +141,9 @@ __host__ __device__ constexpr uint32_t col_p(int t) { return 192u + 32u * t; }  
 template <bool FP8>
 struct Traits {
   static constexpr uint32_t TILE = FP8 ? HALF : 2 * HALF;  // bytes of one 128 x 128 operand tile
-  static constexpr int KST = FP8 ? 4 : 3;                  // K ring stages
-  static constexpr int VST = FP8 ? 4 : 2;                  // V ring stages
+  // BF16: 2 K and 3 V stages measured ~1 % faster than 3 and 2 (same 160 KB)
+  static constexpr int KST = FP8 ? 4 : 2;                  // K ring stages
+  static constexpr int VST = FP8 ? 4 : 3;                  // V ring stages
   // How far (log2 units) a tile's max may exceed the running max before O
   // and l are rescaled: p = 2^(s - m) stays <= 2^RESCALE.
   static constexpr float RESCALE = FP8 ? 0.f : 8.f;
@@ -231,7 +232,10 @@ __device__ __forceinline__ void drain_ring(uint64_t (&full)[ST], int issued, uin
 // until qbf_free), the repair K and V tiles in their own region, so that the
 // K ring fills from the start.
 template <bool FP8>
-__device__ __forceinline__ uint8_t* qbf_tile(Smem<FP8>& sm, int t) { return &sm.v[0][0] + t * 2 * HALF; }
+__device__ __forceinline__ uint8_t* qbf_tile(Smem<FP8>& sm, int t) {
+  static_assert(!FP8 || sizeof(Smem<FP8>::v) >= TILES * 2 * HALF, "the bf16 Q tiles of the repair blocks live in the V ring");
+  return &sm.v[0][0] + t * 2 * HALF;
+}
 template <bool FP8>
 __device__ __forceinline__ uint8_t* krep_tile(Smem<FP8>& sm) { return &sm.rep[0][0]; }
 template <bool FP8>
