@@ -455,8 +455,9 @@ class FluxAttention:
                      q_norm_w=None, k_norm_w=None, pos_ids=None, q8=None, k8=None, v8t=None, scales=None,
                      stream=None):
         """FP8 handles: E4M3 codes q8, k8 [B, H, N, 128], v8t [B, H, 128, pad16(N)]
-        (uint8 tensors) and scales [B, H, 3] (fp32), into the given tensors or
-        new ones."""
+        (uint8 tensors; v8t holds the keys of every 8 columns in the order
+        0 2 4 6 1 3 5 7 that attend_fp8 reads) and scales [B, H, 3] (fp32), into
+        the given tensors or new ones."""
         import torch
         n = txt_len + img_h * img_w + ref_h * ref_w
         for t, name in ((q, "q"), (k, "k"), (v, "v")):
